@@ -1,0 +1,299 @@
+"""Python face of the CPU oracle (ctypes over oracle/oracle.c, numpy arrays).
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, by ``__graft_entry__.smoke()``
+and by the CPU-baseline leg of ``bench.py``; never by the product package.
+It shares no code with the CUDA library.  Each wrapper names the operator
+text it follows; the arithmetic itself lives in oracle.c, except for the
+compositions below, which only chain oracle.c calls in the order the pages
+give.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+U8, S8 = 0, 1
+ACT_IDENTITY, ACT_RELU, ACT_GELU = 0, 1, 2
+
+_lib = None
+
+
+def load(path):
+    """Open a built oracle library and declare its signatures."""
+    l = ctypes.CDLL(path)
+    p = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    i32 = ctypes.c_int32
+    f32 = ctypes.c_float
+    c_int = ctypes.c_int
+    l.or_quantize_linear.argtypes = [p, i64, i64, i64, p, p, c_int, c_int, p]
+    l.or_dequantize_linear.argtypes = [p, c_int, i64, i64, i64, p, p, c_int, p]
+    l.or_quantize_rows_u8.argtypes = [p, i64, i64, p, p, p]
+    l.or_quantize_cols_s8.argtypes = [p, i64, i64, c_int, p, p]
+    l.or_qgemm_dyn_rows.argtypes = [p, p, p, p, p, p, c_int, i64, i64, i64, p, i64, p, p]
+    l.or_f32_to_bf16.argtypes = [p, i64, p]
+    l.or_f32_to_bf16.restype = None
+    l.or_qlinearconv.argtypes = [p, c_int, i64, i64, i64, i64, f32, i32, p, c_int, i64, i64,
+                                 i64, p, p, c_int, f32, i32, p, p, p, p, i64, p, c_int]
+    l.or_lstm_cell.argtypes = [p, p, p, p, p, p, p, i64, i64]
+    for fn in ("or_quantize_linear", "or_dequantize_linear", "or_quantize_rows_u8",
+               "or_quantize_cols_s8", "or_qgemm_dyn_rows", "or_qlinearconv", "or_lstm_cell"):
+        getattr(l, fn).restype = ctypes.c_int
+    return l
+
+
+def lib():
+    """The oracle library.  ORACLE_LIB_UNDER_TEST names another build of
+    oracle.c to load instead; the mutation tests use it to check that the
+    pins fail on planted mistakes."""
+    global _lib
+    if _lib is None:
+        _lib = load(os.environ.get("ORACLE_LIB_UNDER_TEST") or _build.build())
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise RuntimeError(f"oracle {what} failed with code {rc}")
+
+
+def _qtype(t):
+    return {"u8": U8, "s8": S8, U8: U8, S8: S8}[t]
+
+
+def _np_qdtype(t):
+    return np.uint8 if _qtype(t) == U8 else np.int8
+
+
+def _axis_view(shape, axis):
+    """[outer, axis_len, inner] view of a shape for the per-axis index."""
+    rank = len(shape)
+    if axis is None:
+        n = int(np.prod(shape)) if rank else 1
+        return 1, n, 1
+    a = axis + rank if axis < 0 else axis
+    outer = int(np.prod(shape[:a])) if a > 0 else 1
+    inner = int(np.prod(shape[a + 1:])) if a + 1 < rank else 1
+    return outer, int(shape[a]), inner
+
+
+def quantize_linear(x, y_scale, y_zero_point, axis=None, ytype="u8"):
+    """QuantizeLinear (ONNX Runtime contrib schema, ver 1): saturating,
+    round-half-even x / y_scale plus zero point.  axis=None is per tensor."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    s = np.ascontiguousarray(np.atleast_1d(y_scale), dtype=np.float32)
+    z = np.ascontiguousarray(np.atleast_1d(y_zero_point), dtype=np.int32)
+    outer, alen, inner = _axis_view(x.shape, axis)
+    if axis is not None and (s.size != alen or z.size != alen):
+        raise ValueError("per-axis scale/zero point length must equal dim[axis]")
+    y = np.empty(x.shape, dtype=_np_qdtype(ytype))
+    _check(lib().or_quantize_linear(_ptr(x), outer, alen, inner, _ptr(s), _ptr(z),
+                                    int(axis is not None), _qtype(ytype), _ptr(y)), "quantize_linear")
+    return y
+
+
+def dequantize_linear(x, x_scale, x_zero_point, axis=None):
+    """DequantizeLinear (ONNX Runtime contrib schema, ver 1): (x - zp) * scale."""
+    x = np.ascontiguousarray(x)
+    xtype = U8 if x.dtype == np.uint8 else S8
+    if x.dtype not in (np.uint8, np.int8):
+        raise TypeError("x must be uint8 or int8")
+    s = np.ascontiguousarray(np.atleast_1d(x_scale), dtype=np.float32)
+    z = np.ascontiguousarray(np.atleast_1d(x_zero_point), dtype=np.int32)
+    outer, alen, inner = _axis_view(x.shape, axis)
+    y = np.empty(x.shape, dtype=np.float32)
+    _check(lib().or_dequantize_linear(_ptr(x), xtype, outer, alen, inner, _ptr(s), _ptr(z),
+                                      int(axis is not None), _ptr(y)), "dequantize_linear")
+    return y
+
+
+def bf16_bits_to_f32(bits):
+    """Exact widening of bf16 (given as uint16 bit patterns) to fp32."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16_bits(x):
+    """fp32 -> bf16 bit patterns, round to nearest even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.uint16)
+    lib().or_f32_to_bf16(_ptr(x), x.size, _ptr(y))
+    return y
+
+
+def quantize_rows_u8(A):
+    """Per-row uint8 dynamic quantization of A (M x K fp32)."""
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    M, K = A.shape
+    uA = np.empty((M, K), dtype=np.uint8)
+    sA = np.empty(M, dtype=np.float32)
+    zA = np.empty(M, dtype=np.int32)
+    _check(lib().or_quantize_rows_u8(_ptr(A), M, K, _ptr(uA), _ptr(sA), _ptr(zA)), "quantize_rows_u8")
+    return uA, sA, zA
+
+
+def quantize_cols_s8(B, avoid_overflow=False):
+    """Per-column symmetric int8 quantization of B (K x N fp32)."""
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    K, N = B.shape
+    iB = np.empty((K, N), dtype=np.int8)
+    sB = np.empty(N, dtype=np.float32)
+    _check(lib().or_quantize_cols_s8(_ptr(B), K, N, int(bool(avoid_overflow)), _ptr(iB), _ptr(sB)),
+           "quantize_cols_s8")
+    return iB, sB
+
+
+def qgemm_rows(uA, zA, sA, iB, sB, bias=None, act=ACT_IDENTITY, rows=None):
+    """Integer product, dequantization, bias and activation of the Simd
+    dynamic quantized inner product, for the listed rows (all if None).
+    Returns (int32 sums, fp32 outputs), each len(rows) x N."""
+    uA = np.ascontiguousarray(uA, dtype=np.uint8)
+    iB = np.ascontiguousarray(iB, dtype=np.int8)
+    zA = np.ascontiguousarray(zA, dtype=np.int32)
+    sA = np.ascontiguousarray(sA, dtype=np.float32)
+    sB = np.ascontiguousarray(sB, dtype=np.float32)
+    M, K = uA.shape
+    K2, N = iB.shape
+    assert K == K2
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nr = M if r is None else r.size
+    acc = np.empty((nr, N), dtype=np.int32)
+    C = np.empty((nr, N), dtype=np.float32)
+    _check(lib().or_qgemm_dyn_rows(_ptr(uA), _ptr(zA), _ptr(sA), _ptr(iB), _ptr(sB), _ptr(b), act,
+                                   M, N, K, _ptr(r), nr, _ptr(acc), _ptr(C)), "qgemm_dyn_rows")
+    return acc, C
+
+
+def dynamic_quantized_inner_product(A, B=None, *, iB=None, scaleB=None, bias=None,
+                                    act=ACT_IDENTITY, avoid_overflow=False, typeC="f32",
+                                    rows=None):
+    """Whole Simd dynamic quantized inner product: quantize A per row, take B
+    as given int8 (iB, scaleB) or quantize fp32 B per column, then the
+    integer product and its epilogue.  typeC 'bf16' returns bf16 bits.
+    A may be fp32, or bf16 bits (uint16), which widen exactly."""
+    A = np.asarray(A)
+    if A.dtype == np.uint16:
+        A = bf16_bits_to_f32(A)
+    uA, sA, zA = quantize_rows_u8(A)
+    if iB is None:
+        Bf = np.asarray(B)
+        if Bf.dtype == np.uint16:
+            Bf = bf16_bits_to_f32(Bf)
+        iB, scaleB = quantize_cols_s8(Bf, avoid_overflow)
+    acc, C = qgemm_rows(uA, zA, sA, iB, scaleB, bias, act, rows)
+    out = {"uA": uA, "scaleA": sA, "zeroA": zA, "iB": iB, "scaleB": scaleB, "acc": acc, "C32": C}
+    out["C"] = f32_to_bf16_bits(C) if typeC == "bf16" else C
+    return out
+
+
+def qlinearconv(x, x_scale, x_zero_point, w, w_scale, w_zero_point, y_scale, y_zero_point,
+                B=None, pads=(0, 0, 0, 0), strides=(1, 1), dilations=(1, 1), group=1, ytype=None):
+    """2-D QLinearConv (ONNX, since version 10) on NCHW tensors.
+    pads = (top, left, bottom, right).  Output type defaults to x's type."""
+    x = np.ascontiguousarray(x)
+    w = np.ascontiguousarray(w)
+    xt = U8 if x.dtype == np.uint8 else S8
+    wt = U8 if w.dtype == np.uint8 else S8
+    yt = xt if ytype is None else _qtype(ytype)
+    N, C, H, W = x.shape
+    M, Cg, kH, kW = w.shape
+    ws = np.ascontiguousarray(np.atleast_1d(w_scale), dtype=np.float32)
+    wz = np.ascontiguousarray(np.atleast_1d(w_zero_point), dtype=np.int32)
+    per_ch = int(ws.size == M and M > 1)
+    if ws.size not in (1, M) or wz.size != ws.size:
+        raise ValueError("w_scale / w_zero_point must be scalars or have M entries")
+    if C != Cg * group:
+        raise ValueError("x.shape[1] must equal w.shape[1] * group")
+    pads = np.asarray(pads, dtype=np.int64)
+    strides = np.asarray(strides, dtype=np.int64)
+    dil = np.asarray(dilations, dtype=np.int64)
+    OH = (H + pads[0] + pads[2] - ((kH - 1) * dil[0] + 1)) // strides[0] + 1
+    OW = (W + pads[1] + pads[3] - ((kW - 1) * dil[1] + 1)) // strides[1] + 1
+    y = np.empty((N, M, OH, OW), dtype=np.uint8 if yt == U8 else np.int8)
+    b = None if B is None else np.ascontiguousarray(B, dtype=np.int32)
+    _check(lib().or_qlinearconv(_ptr(x), xt, N, C, H, W, float(x_scale), int(x_zero_point),
+                                _ptr(w), wt, M, kH, kW, _ptr(ws), _ptr(wz), per_ch,
+                                float(y_scale), int(y_zero_point), _ptr(b), _ptr(pads),
+                                _ptr(strides), _ptr(dil), group, _ptr(y), yt), "qlinearconv")
+    return y
+
+
+def lstm_cell(Gx, Gh, Wb, Rb, c_prev):
+    """One DynamicQuantizeLSTM cell update (default activations, iofc)."""
+    Gx = np.ascontiguousarray(Gx, dtype=np.float32)
+    Gh = np.ascontiguousarray(Gh, dtype=np.float32)
+    c_prev = np.ascontiguousarray(c_prev, dtype=np.float32)
+    batch, H4 = Gx.shape
+    H = H4 // 4
+    Wb = None if Wb is None else np.ascontiguousarray(Wb, dtype=np.float32)
+    Rb = None if Rb is None else np.ascontiguousarray(Rb, dtype=np.float32)
+    h = np.empty((batch, H), dtype=np.float32)
+    c = np.empty((batch, H), dtype=np.float32)
+    _check(lib().or_lstm_cell(_ptr(Gx), _ptr(Gh), _ptr(Wb), _ptr(Rb), _ptr(c_prev), _ptr(h), _ptr(c),
+                              batch, H), "lstm_cell")
+    return h, c
+
+
+def lstm_projection(X, W, W_scale):
+    """Input projection of one direction: X (T, batch, I) quantized per row,
+    times int8 W (I x 4H) with per-column scales, no bias, fp32 out."""
+    T, batch, I = X.shape
+    out = dynamic_quantized_inner_product(X.reshape(T * batch, I), iB=W, scaleB=W_scale)
+    return out["C32"].reshape(T, batch, -1)
+
+
+def lstm_step(Gx_t, h_prev, c_prev, R, R_scale, Wb, Rb):
+    """One recurrence step of one direction: quantize h_prev per row, take
+    the dequantized product with int8 R, then the cell update."""
+    Gh = dynamic_quantized_inner_product(h_prev, iB=R, scaleB=R_scale)["C32"]
+    return lstm_cell(Gx_t, Gh, Wb, Rb, c_prev)
+
+
+def dynamic_quantize_lstm(X, W, R, B, W_scale, R_scale, h0=None, c0=None, direction="forward",
+                          steps=None):
+    """DynamicQuantizeLSTM (ONNX Runtime contrib schema) with int8 W/R, zero
+    points 0, default activations, no peepholes, no sequence_lens, no clip.
+    X (T, batch, I); W (D, I, 4H); R (D, H, 4H); B (D, 8H) or None;
+    scales (D, 4H).  Returns Y (T, D, batch, H), Y_h, Y_c (D, batch, H).
+    steps (default T) limits how many steps each direction runs; rows of Y
+    for steps not run stay zero."""
+    T, batch, I = X.shape
+    D = W.shape[0]
+    H = R.shape[1]
+    dirs = {"forward": [0], "reverse": [1], "bidirectional": [0, 1]}[direction]
+    assert len(dirs) == D
+    S = T if steps is None else steps
+    Y = np.zeros((T, D, batch, H), dtype=np.float32)
+    Yh = np.zeros((D, batch, H), dtype=np.float32)
+    Yc = np.zeros((D, batch, H), dtype=np.float32)
+    for d, kind in enumerate(dirs):
+        Gx = lstm_projection(X, W[d], W_scale[d])
+        h = np.zeros((batch, H), np.float32) if h0 is None else np.array(h0[d], np.float32)
+        c = np.zeros((batch, H), np.float32) if c0 is None else np.array(c0[d], np.float32)
+        Wb = None if B is None else B[d, :4 * H]
+        Rb = None if B is None else B[d, 4 * H:]
+        order = range(T) if kind == 0 else range(T - 1, -1, -1)
+        for n, t in enumerate(order):
+            if n >= S:
+                break
+            h, c = lstm_step(Gx[t], h, c, R[d], R_scale[d], Wb, Rb)
+            Y[t, d] = h
+        Yh[d] = h
+        Yc[d] = c
+    return Y, Yh, Yc
+
+
+def num_threads():
+    """OpenMP threads the oracle uses (OMP_NUM_THREADS, else the CPUs this
+    process may run on)."""
+    env = os.environ.get("OMP_NUM_THREADS")
+    if env and env.isdigit():
+        return int(env)
+    return len(os.sched_getaffinity(0))

@@ -1,0 +1,359 @@
+/*
+ * oracle.c -- plain, slow CPU oracle for linear int8 quantization and the
+ * quantized products it feeds.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may load or call
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg do.  It shares no code, header, table or helper with the CUDA library.
+ *
+ * Every function is a direct restatement of the operator text it cites, in
+ * the order of operations the text gives.  Floating point is IEEE fp32 where
+ * the operator is defined on fp32 (the scales, the division x / scale, the
+ * dequantization products); each operation rounds once, to nearest even.
+ * The build uses -O2 -ffp-contract=off and no fast-math so the compiler
+ * neither fuses a multiply into an add nor reorders anything.  Integer sums
+ * are carried in int64 and checked to fit the int32 the operators name.
+ *
+ * Sources (page title, section):
+ *  [QL]  ONNX Runtime contrib schemas, "QuantizeLinear" (ver 1) doc string
+ *  [DQL] ONNX Runtime contrib schemas, "DequantizeLinear" (ver 1) doc string
+ *  [DQIP] Simd, "SynetDynamicQuantizedInnerProduct16b", Detailed Description
+ *         (algorithm listing, typeB/avoidOverflow paragraph) and the
+ *         Init()/SetParams()/Forward() member documentation
+ *  [QLC] onnx-light docs, "QLinearConv" (inputs, bias rule, examples)
+ *  [LSTM] ONNX Runtime contrib schemas, "DynamicQuantizeLSTM" (inputs W, R, B,
+ *         initial_h/c, outputs Y, Y_h, Y_c); graiphic.io "DynamicQuantizeLSTM"
+ *
+ * Where the pages leave a step open the readings used are listed in the
+ * repository's design notes; each is restated at the function below.
+ */
+#include <fenv.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_OK 0
+#define OR_ERR_ROUNDING -1
+#define OR_ERR_OVERFLOW -2
+#define OR_ERR_ARG -3
+
+#define OR_U8 0
+#define OR_S8 1
+
+#define OR_ACT_IDENTITY 0
+#define OR_ACT_RELU 1
+#define OR_ACT_GELU 2
+
+static int rounding_is_nearest(void) { return fegetround() == FE_TONEAREST; }
+
+/* rintf gives the nearest integer, ties to even, under FE_TONEAREST.
+ * The result is held in a double so values far outside int32 saturate
+ * correctly instead of overflowing a conversion. */
+static int64_t sat_rint_plus(float v, int64_t zp, int64_t lo, int64_t hi) {
+  double r = (double)rintf(v) + (double)zp;
+  if (r < (double)lo) return lo;
+  if (r > (double)hi) return hi;
+  return (int64_t)r;
+}
+
+static int64_t q_lo(int t) { return t == OR_U8 ? 0 : -128; }
+static int64_t q_hi(int t) { return t == OR_U8 ? 255 : 127; }
+
+static int64_t load_q(const void* p, int t, int64_t i) {
+  return t == OR_U8 ? (int64_t)((const uint8_t*)p)[i] : (int64_t)((const int8_t*)p)[i];
+}
+
+static void store_q(void* p, int t, int64_t i, int64_t v) {
+  if (t == OR_U8)
+    ((uint8_t*)p)[i] = (uint8_t)v;
+  else
+    ((int8_t*)p)[i] = (int8_t)v;
+}
+
+/* [QL]: y = saturate(round_half_even(x / y_scale) + y_zero_point), saturating
+ * to [0,255] for uint8 and [-128,127] for int8.  The tensor is viewed as
+ * [outer, axis_len, inner]; with per_axis the scale and zero point are picked
+ * by the middle index (the 'axis' attribute), otherwise element 0 is used
+ * for every element (per tensor). */
+int or_quantize_linear(const float* x, int64_t outer, int64_t axis_len, int64_t inner,
+                       const float* y_scale, const int32_t* y_zero_point, int per_axis,
+                       int ytype, void* y) {
+  if (!rounding_is_nearest()) return OR_ERR_ROUNDING;
+  if (ytype != OR_U8 && ytype != OR_S8) return OR_ERR_ARG;
+  int64_t lo = q_lo(ytype), hi = q_hi(ytype);
+#pragma omp parallel for schedule(static)
+  for (int64_t o = 0; o < outer; ++o) {
+    for (int64_t a = 0; a < axis_len; ++a) {
+      int64_t c = per_axis ? a : 0;
+      float s = y_scale[c];
+      int64_t zp = y_zero_point[c];
+      for (int64_t n = 0; n < inner; ++n) {
+        int64_t i = (o * axis_len + a) * inner + n;
+        float q = x[i] / s;
+        store_q(y, ytype, i, sat_rint_plus(q, zp, lo, hi));
+      }
+    }
+  }
+  return OR_OK;
+}
+
+/* [DQL]: y = (x - x_zero_point) * x_scale, output float.  The integer
+ * difference is exact and converts to float exactly (|x - zp| <= 510). */
+int or_dequantize_linear(const void* x, int xtype, int64_t outer, int64_t axis_len, int64_t inner,
+                         const float* x_scale, const int32_t* x_zero_point, int per_axis, float* y) {
+  if (xtype != OR_U8 && xtype != OR_S8) return OR_ERR_ARG;
+#pragma omp parallel for schedule(static)
+  for (int64_t o = 0; o < outer; ++o) {
+    for (int64_t a = 0; a < axis_len; ++a) {
+      int64_t c = per_axis ? a : 0;
+      float s = x_scale[c];
+      int64_t zp = x_zero_point[c];
+      for (int64_t n = 0; n < inner; ++n) {
+        int64_t i = (o * axis_len + a) * inner + n;
+        float d = (float)(load_q(x, xtype, i) - zp);
+        y[i] = d * s;
+      }
+    }
+  }
+  return OR_OK;
+}
+
+/* [DQIP] step "A[i,k] -> uA[i,k], scaleA[i], zeroA[i]".  The page names only
+ * the outputs; the reading used (asymmetric uint8 per row, range widened to
+ * contain 0) is:
+ *   mn = min(0, min_k A[i,k]),  mx = max(0, max_k A[i,k])
+ *   scaleA = (mx - mn) / 255                      (fp32 division)
+ *   zeroA  = saturate_u8(round_half_even(-mn / scaleA))
+ *   uA     = saturate_u8(round_half_even(A / scaleA) + zeroA)
+ * The last line is [QL] applied with the row's scale and zero point.
+ * Degenerate row (scaleA == 0, i.e. the row is all zeros): scaleA = 1,
+ * zeroA = 0, so every uA is 0. */
+int or_quantize_rows_u8(const float* A, int64_t M, int64_t K, uint8_t* uA, float* scaleA,
+                        int32_t* zeroA) {
+  if (!rounding_is_nearest()) return OR_ERR_ROUNDING;
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < M; ++i) {
+    const float* a = A + i * K;
+    float mn = 0.0f, mx = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      if (a[k] < mn) mn = a[k];
+      if (a[k] > mx) mx = a[k];
+    }
+    float s = (mx - mn) / 255.0f;
+    int64_t z;
+    if (s == 0.0f) {
+      s = 1.0f;
+      z = 0;
+    } else {
+      z = sat_rint_plus(-mn / s, 0, 0, 255);
+    }
+    scaleA[i] = s;
+    zeroA[i] = (int32_t)z;
+    for (int64_t k = 0; k < K; ++k) uA[i * K + k] = (uint8_t)sat_rint_plus(a[k] / s, z, 0, 255);
+  }
+  return OR_OK;
+}
+
+/* [DQIP] step "B[k,j] -> iB[k,j], scaleB[j]" with the typeB/avoidOverflow
+ * paragraph: int8 in [-128,127], or the narrowed [-64,63] when avoidOverflow
+ * is set.  Reading: symmetric per column, zero point 0,
+ *   scaleB = max_k |B[k,j]| / qmax       (qmax = 127, or 63 narrowed)
+ *   iB     = saturate(round_half_even(B / scaleB))
+ * Degenerate column (all zeros): scaleB = 1, iB = 0.  B is K x N row-major. */
+int or_quantize_cols_s8(const float* B, int64_t K, int64_t N, int avoid_overflow, int8_t* iB,
+                        float* scaleB) {
+  if (!rounding_is_nearest()) return OR_ERR_ROUNDING;
+  const int64_t qmax = avoid_overflow ? 63 : 127;
+  const int64_t qmin = avoid_overflow ? -64 : -128;
+#pragma omp parallel for schedule(static)
+  for (int64_t j = 0; j < N; ++j) {
+    float m = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      float v = fabsf(B[k * N + j]);
+      if (v > m) m = v;
+    }
+    float s = m / (float)qmax;
+    if (s == 0.0f) s = 1.0f;
+    scaleB[j] = s;
+    for (int64_t k = 0; k < K; ++k)
+      iB[k * N + j] = (int8_t)sat_rint_plus(B[k * N + j] / s, 0, qmin, qmax);
+  }
+  return OR_OK;
+}
+
+/* GELU with the error function, in fp32: 0.5 * x * (1 + erf(x / sqrt(2))).
+ * Evaluated as (0.5 * x) * (1 + erff(x * (1/sqrt(2)))). */
+static float gelu_f32(float x) {
+  float t = x * 0.70710678118654752440f;
+  float e = erff(t);
+  float h = 0.5f * x;
+  return h * (1.0f + e);
+}
+
+static float activate(float v, int act) {
+  switch (act) {
+    case OR_ACT_RELU: return v > 0.0f ? v : 0.0f;
+    case OR_ACT_GELU: return gelu_f32(v);
+    default: return v;
+  }
+}
+
+/* [DQIP] algorithm listing, for the rows listed in `rows` (all rows when
+ * rows == NULL):
+ *   sum = sum_k (uA[i,k] - zeroA[i]) * iB[k,j]        (integer)
+ *   val = sum * scaleA[i] * scaleB[j]                  (left to right, fp32)
+ *   C[i,j] = Activate(val + bias[j])
+ * uA is M x K row-major, iB is K x N row-major.  The sum is carried in int64
+ * and must fit int32; its conversion to fp32 rounds to nearest even.
+ * acc_out (optional) receives the int32 sums, C_out the fp32 results,
+ * both nrows x N. */
+int or_qgemm_dyn_rows(const uint8_t* uA, const int32_t* zeroA, const float* scaleA,
+                      const int8_t* iB, const float* scaleB, const float* bias, int act,
+                      int64_t M, int64_t N, int64_t K, const int64_t* rows, int64_t nrows,
+                      int32_t* acc_out, float* C_out) {
+  if (!rounding_is_nearest()) return OR_ERR_ROUNDING;
+  int err = OR_OK;
+  if (rows == NULL) nrows = M;
+#pragma omp parallel for schedule(dynamic, 1) reduction(min : err)
+  for (int64_t r = 0; r < nrows; ++r) {
+    int64_t i = rows ? rows[r] : r;
+    if (i < 0 || i >= M) {
+      err = OR_ERR_ARG;
+      continue;
+    }
+    for (int64_t j = 0; j < N; ++j) {
+      int64_t sum = 0;
+      for (int64_t k = 0; k < K; ++k)
+        sum += ((int64_t)uA[i * K + k] - (int64_t)zeroA[i]) * (int64_t)iB[k * N + j];
+      if (sum > INT32_MAX || sum < INT32_MIN) {
+        err = OR_ERR_OVERFLOW;
+        continue;
+      }
+      if (acc_out) acc_out[r * N + j] = (int32_t)sum;
+      float val = (float)(int32_t)sum;
+      val = val * scaleA[i];
+      val = val * scaleB[j];
+      if (bias) val = val + bias[j];
+      C_out[r * N + j] = activate(val, act);
+    }
+  }
+  return err;
+}
+
+/* Conversion of fp32 to bf16, round to nearest even on the upper 16 bits
+ * (the conversion the output type bf16 implies).  NaN maps to a quiet NaN. */
+void or_f32_to_bf16(const float* x, int64_t n, uint16_t* y) {
+  for (int64_t i = 0; i < n; ++i) {
+    uint32_t u;
+    memcpy(&u, &x[i], 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u) {
+      y[i] = (uint16_t)((u >> 16) | 0x40u);
+      continue;
+    }
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    y[i] = (uint16_t)(u >> 16);
+  }
+}
+
+/* [QLC] 2-D QLinearConv on NCHW tensors.
+ *   acc[n,m,oh,ow] = sum over c in m's group, kh, kw of
+ *                    (x[n,c,ih,iw] - x_zero_point) * (w[m,c',kh,kw] - w_zero_point[m])
+ *   with ih = oh*stride_h - pad_top + kh*dil_h (likewise iw).  A position
+ *   outside the input holds real 0, i.e. the quantized value x_zero_point,
+ *   so it adds nothing.
+ *   acc += B[m]            (bias quantized with scale x_scale*w_scale, zp 0)
+ *   y = saturate(round_half_even(((float)acc * (x_scale * w_scale[m])) / y_scale)
+ *                + y_zero_point)
+ * The last line dequantizes the accumulator and applies QuantizeLinear with
+ * (y_scale, y_zero_point); the page gives no formula of its own.
+ * pads = {top, left, bottom, right}; strides, dilations = {h, w}.
+ * w_scale / w_zero_point hold M entries when per_channel, else one. */
+int or_qlinearconv(const void* x, int xtype, int64_t N, int64_t C, int64_t H, int64_t W,
+                   float x_scale, int32_t x_zero_point, const void* w, int wtype, int64_t M,
+                   int64_t kH, int64_t kW, const float* w_scale, const int32_t* w_zero_point,
+                   int per_channel, float y_scale, int32_t y_zero_point, const int32_t* B,
+                   const int64_t* pads, const int64_t* strides, const int64_t* dilations,
+                   int64_t group, void* y, int ytype) {
+  if (!rounding_is_nearest()) return OR_ERR_ROUNDING;
+  if (group <= 0 || C % group != 0 || M % group != 0) return OR_ERR_ARG;
+  const int64_t Cg = C / group, Mg = M / group;
+  const int64_t OH = (H + pads[0] + pads[2] - ((kH - 1) * dilations[0] + 1)) / strides[0] + 1;
+  const int64_t OW = (W + pads[1] + pads[3] - ((kW - 1) * dilations[1] + 1)) / strides[1] + 1;
+  if (OH <= 0 || OW <= 0) return OR_ERR_ARG;
+  const int64_t lo = q_lo(ytype), hi = q_hi(ytype);
+  int err = OR_OK;
+#pragma omp parallel for collapse(2) schedule(static) reduction(min : err)
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t m = 0; m < M; ++m) {
+      const int64_t g = m / Mg;
+      const int64_t wz = w_zero_point[per_channel ? m : 0];
+      const float ws = w_scale[per_channel ? m : 0];
+      for (int64_t oh = 0; oh < OH; ++oh) {
+        for (int64_t ow = 0; ow < OW; ++ow) {
+          int64_t acc = 0;
+          for (int64_t cc = 0; cc < Cg; ++cc) {
+            const int64_t c = g * Cg + cc;
+            for (int64_t kh = 0; kh < kH; ++kh) {
+              const int64_t ih = oh * strides[0] - pads[0] + kh * dilations[0];
+              if (ih < 0 || ih >= H) continue;
+              for (int64_t kw = 0; kw < kW; ++kw) {
+                const int64_t iw = ow * strides[1] - pads[1] + kw * dilations[1];
+                if (iw < 0 || iw >= W) continue;
+                const int64_t xv = load_q(x, xtype, ((n * C + c) * H + ih) * W + iw);
+                const int64_t wv = load_q(w, wtype, ((m * Cg + cc) * kH + kh) * kW + kw);
+                acc += (xv - x_zero_point) * (wv - wz);
+              }
+            }
+          }
+          if (B) acc += B[m];
+          if (acc > INT32_MAX || acc < INT32_MIN) {
+            err = OR_ERR_OVERFLOW;
+            continue;
+          }
+          float v = (float)(int32_t)acc;
+          float mul = x_scale * ws;
+          v = v * mul;
+          v = v / y_scale;
+          store_q(y, ytype, ((n * M + m) * OH + oh) * OW + ow, sat_rint_plus(v, y_zero_point, lo, hi));
+        }
+      }
+    }
+  }
+  return err;
+}
+
+static float sigmoid_f32(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+/* [LSTM] one cell update for one direction and one time step, default
+ * activations (f = sigmoid, g = tanh, h = tanh), no peepholes, no clip.
+ * The gate pre-activations are, per batch row b and column n of 4H,
+ *   g = ((Gx[b,n] + Gh[b,n]) + Wb[n]) + Rb[n]
+ * in the iofc column order of W, R and B:
+ *   i = sigmoid(g_i), o = sigmoid(g_o), f = sigmoid(g_f), ct = tanh(g_c)
+ *   c = f * c_prev + i * ct,   h = o * tanh(c)
+ * sigmoid(x) = 1 / (1 + exp(-x)).  Wb or Rb may be NULL (zero bias). */
+int or_lstm_cell(const float* Gx, const float* Gh, const float* Wb, const float* Rb,
+                 const float* c_prev, float* h_out, float* c_out, int64_t batch, int64_t H) {
+  for (int64_t b = 0; b < batch; ++b) {
+    for (int64_t u = 0; u < H; ++u) {
+      float g[4];
+      for (int q = 0; q < 4; ++q) {
+        int64_t n = q * H + u;
+        float v = Gx[b * 4 * H + n] + Gh[b * 4 * H + n];
+        if (Wb) v = v + Wb[n];
+        if (Rb) v = v + Rb[n];
+        g[q] = v;
+      }
+      float ig = sigmoid_f32(g[0]);
+      float og = sigmoid_f32(g[1]);
+      float fg = sigmoid_f32(g[2]);
+      float ct = tanhf(g[3]);
+      float c = fg * c_prev[b * H + u] + ig * ct;
+      c_out[b * H + u] = c;
+      h_out[b * H + u] = og * tanhf(c);
+    }
+  }
+  return OR_OK;
+}

@@ -1,0 +1,459 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU needed).
+
+Each test checks the oracle against something the pages or the mathematics
+fix: the worked examples the QLinearConv page prints, hand-worked closed
+forms of QuantizeLinear/DequantizeLinear, lossless special cases whose exact
+result is a textbook fp64 product, error bounds, invariants and library
+routines.  The choice is meant to catch a dropped term, a wrong sign or
+index, or a transposed operand anywhere in the oracle.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import read_golden, read_golden_rows
+from int8_quantized_gb300 import workloads
+
+
+def _qdt(t):
+    return np.uint8 if t == "u8" else np.int8
+
+
+# ----------------------------------------------------------------------------
+# QLinearConv: the two printed examples, bit for bit
+# ----------------------------------------------------------------------------
+
+def _run_conv_golden(orc, name, xdt, wdt, xshape, wshape):
+    g = read_golden(name)
+    x = np.array([int(v) for v in g["x"]], dtype=xdt).reshape(xshape)
+    w = np.array([int(v) for v in g["w"]], dtype=wdt).reshape(wshape)
+    y = orc.qlinearconv(x, np.float32(g["x_scale"][0]), int(g["x_zero_point"][0]), w,
+                        np.array([float(g["w_scale"][0])], np.float32),
+                        np.array([int(g["w_zero_point"][0])]),
+                        np.float32(g["y_scale"][0]), int(g["y_zero_point"][0]))
+    expect = np.array([int(v) for v in g["y"]], dtype=xdt)
+    return y.reshape(-1), expect
+
+
+def test_qlinearconv_printed_uint8_example(orc):
+    y, expect = _run_conv_golden(orc, "qlinearconv_u8_7x7.txt", np.uint8, np.uint8, (1, 1, 7, 7), (1, 1, 1, 1))
+    assert np.array_equal(y, expect)
+
+
+def test_qlinearconv_printed_int8_example(orc):
+    y, expect = _run_conv_golden(orc, "qlinearconv_s8_2x2.txt", np.int8, np.int8, (1, 1, 2, 2), (1, 1, 2, 2))
+    assert y.shape == (1,) and np.array_equal(y, expect)
+
+
+# ----------------------------------------------------------------------------
+# QuantizeLinear / DequantizeLinear closed forms
+# ----------------------------------------------------------------------------
+
+def test_quantize_linear_closed_form_cases(orc):
+    for x, s, zp, t, y in read_golden_rows("quantize_linear_cases.txt"):
+        got = orc.quantize_linear(np.array([float(x)], np.float32), np.float32(s), int(zp), None, t)
+        assert got.dtype == _qdt(t)
+        assert int(got[0]) == int(y), (x, s, zp, t, y, got)
+
+
+def test_dequantize_linear_closed_form_cases(orc):
+    for x, s, zp, t, y in read_golden_rows("dequantize_linear_cases.txt"):
+        got = orc.dequantize_linear(np.array([int(x)], _qdt(t)), np.float32(s), int(zp))
+        assert got.dtype == np.float32
+        assert got[0] == np.float32(y), (x, s, zp, t, y, got)
+
+
+@pytest.mark.parametrize("t", ["u8", "s8"])
+def test_quantize_power_of_two_scales_match_exact_rational_rounding(orc, t):
+    """With a power-of-two scale x/scale is exact, so the operator reduces to
+    Python's round() (half to even) on exact rationals, then clamp."""
+    rng = np.random.default_rng(11)
+    lo, hi = (0, 255) if t == "u8" else (-128, 127)
+    for e in (-7, -3, 0, 2):
+        s = np.float32(2.0 ** e)
+        zp = int(rng.integers(lo, hi + 1))
+        k = rng.integers(-400, 400, size=500)
+        frac = rng.choice([0.0, 0.25, 0.5, 0.75], size=500)
+        x = ((k + frac) * float(s)).astype(np.float32)
+        got = orc.quantize_linear(x, s, zp, None, t)
+        for xi, gi in zip(x, got):
+            r = round(Fraction(float(xi)) / Fraction(float(s))) + zp
+            assert int(gi) == min(max(r, lo), hi)
+
+
+def test_quantize_per_axis_equals_per_tensor_slices(orc):
+    """Per-axis quantization along axis a is per-tensor quantization of each
+    slice taken along a with that slice's scale and zero point."""
+    rng = np.random.default_rng(5)
+    x = rng.normal(0, 2, size=(3, 5, 7)).astype(np.float32)
+    for axis in (0, 1, 2, -1):
+        n = x.shape[axis]
+        s = rng.uniform(0.005, 0.05, size=n).astype(np.float32)
+        z = rng.integers(0, 256, size=n)
+        y = orc.quantize_linear(x, s, z, axis, "u8")
+        for c in range(n):
+            ref = orc.quantize_linear(np.take(x, c, axis=axis), s[c], z[c], None, "u8")
+            assert np.array_equal(np.take(y, c, axis=axis), ref)
+        d = orc.dequantize_linear(y, s, z, axis)
+        for c in range(n):
+            ref = orc.dequantize_linear(np.take(y, c, axis=axis), s[c], z[c], None)
+            assert np.array_equal(np.take(d, c, axis=axis), ref)
+
+
+def test_qdq_ties_round_to_even(orc):
+    """The tie positions the workload plants sit exactly at k + 0.5 after the
+    fp32 division; QuantizeLinear must send each to the even neighbour."""
+    w = workloads.qdq(seed=1, shape=(4, 8, 64), tie_fraction=0.2)
+    x, s, zp = w["x"], w["scale"], w["zero_point"]
+    y = orc.quantize_linear(x, s, zp, axis=2, ytype="u8")
+    flat_x = x.reshape(-1)
+    flat_y = y.reshape(-1).astype(np.int64)
+    pos = w["tie_positions"]
+    assert pos.size > 50
+    ch = pos % 64
+    q = (flat_x[pos] / s[ch]).astype(np.float32).astype(np.float64)
+    assert np.all(q - np.floor(q) == 0.5)
+    v = flat_y[pos] - zp[ch].astype(np.int64)
+    assert np.all(v % 2 == 0)
+    assert np.all(np.abs(v - q) == 0.5)
+
+
+def test_qdq_roundtrip_error_within_half_scale(orc):
+    rng = np.random.default_rng(3)
+    x = rng.normal(0, 2, size=(64, 33)).astype(np.float32)
+    s = rng.uniform(0.005, 0.05, size=33).astype(np.float32)
+    z = rng.integers(0, 256, size=33)
+    y = orc.quantize_linear(x, s, z, axis=1, ytype="u8")
+    d = orc.dequantize_linear(y, s, z, axis=1)
+    lo = (0 - z) * s.astype(np.float64)
+    hi = (255 - z) * s.astype(np.float64)
+    inside = (x >= lo) & (x <= hi)
+    err = np.abs(d.astype(np.float64) - x)
+    assert np.all(err[inside] <= 0.5 * s[np.nonzero(inside)[1]] * (1 + 1e-5))
+    # outside the representable range the result saturates at the nearer end
+    assert np.all(y[x > hi + s] == 255) and np.all(y[x < lo - s] == 0)
+
+
+# ----------------------------------------------------------------------------
+# Row / column quantization invariants
+# ----------------------------------------------------------------------------
+
+def test_row_quantization_invariants(orc):
+    rng = np.random.default_rng(7)
+    A = rng.normal(0, 1, size=(40, 97)).astype(np.float32)
+    A[3] = np.abs(A[3])          # all non-negative: zero point 0
+    A[4] = -np.abs(A[4])         # all non-positive: zero point 255
+    A[5] = 0.0                   # degenerate row
+    uA, sA, zA = orc.quantize_rows_u8(A)
+    assert sA[5] == 1.0 and zA[5] == 0 and np.all(uA[5] == 0)
+    assert zA[3] == 0 and zA[4] == 255
+    for i in range(40):
+        if i == 5:
+            continue
+        mn, mx = min(0.0, float(A[i].min())), max(0.0, float(A[i].max()))
+        assert abs(float(sA[i]) - (mx - mn) / 255) <= 1e-6 * (mx - mn) / 255
+        deq = (uA[i].astype(np.float64) - zA[i]) * float(sA[i])
+        assert np.max(np.abs(deq - A[i])) <= 0.5 * float(sA[i]) * (1 + 1e-4)
+        # the zero point is the code of real 0, the extremes map to the ends
+        if mn < 0:
+            assert uA[i, np.argmin(A[i])] == 0
+        if mx > 0:
+            assert uA[i, np.argmax(A[i])] >= 254
+
+
+@pytest.mark.parametrize("avoid", [False, True])
+def test_column_quantization_invariants(orc, avoid):
+    rng = np.random.default_rng(8)
+    B = rng.normal(0, 0.05, size=(77, 19)).astype(np.float32)
+    B[:, 4] = 0.0
+    iB, sB = orc.quantize_cols_s8(B, avoid)
+    qmax = 63 if avoid else 127
+    assert iB.min() >= (-64 if avoid else -128) and iB.max() <= qmax
+    assert sB[4] == 1.0 and np.all(iB[:, 4] == 0)
+    for j in range(19):
+        if j == 4:
+            continue
+        m = np.abs(B[:, j]).max()
+        assert abs(float(sB[j]) - m / qmax) <= 1e-6 * m / qmax
+        assert abs(int(iB[np.argmax(np.abs(B[:, j])), j])) == qmax
+        deq = iB[:, j].astype(np.float64) * float(sB[j])
+        assert np.max(np.abs(deq - B[:, j])) <= 0.5 * float(sB[j]) * (1 + 1e-4)
+
+
+# ----------------------------------------------------------------------------
+# Dynamic quantized inner product
+# ----------------------------------------------------------------------------
+
+def lossless_A(rng, M, K):
+    """Rows on the grid (q - z) * 2^e with a 0 and a 255 code present: the
+    row scale (max - min) / 255 is exactly 2^e and the zero point exactly z,
+    so quantization loses nothing."""
+    A = np.empty((M, K), np.float32)
+    for i in range(M):
+        s = 2.0 ** int(rng.integers(-9, -4))
+        z = int(rng.integers(0, 256))
+        q = rng.integers(0, 256, size=K)
+        if K == 1:
+            q[0] = 255 if z == 0 else 0
+            z = 0 if q[0] == 255 else 255
+        else:
+            lo_pos, hi_pos = rng.choice(K, size=2, replace=False)
+            q[lo_pos], q[hi_pos] = 0, 255
+        A[i] = (q - z) * s
+    return A
+
+
+def lossless_B(rng, K, N, qmax=127):
+    B = np.empty((K, N), np.float32)
+    for j in range(N):
+        t = 2.0 ** int(rng.integers(-10, -5))
+        v = rng.integers(-qmax, qmax + 1, size=K)
+        v[rng.integers(0, K)] = qmax if rng.random() < 0.5 else -qmax
+        B[:, j] = v * t
+    return B
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 2), (3, 5, 7), (8, 8, 16), (7, 13, 63), (17, 9, 129), (5, 33, 500)])
+@pytest.mark.parametrize("avoid", [False, True])
+def test_inner_product_lossless_grid_equals_fp64_product(orc, M, N, K, avoid):
+    """Lossless special case: the method's result must equal the textbook
+    fp64 product A @ B + bias, rounded once to fp32."""
+    rng = np.random.default_rng(M * 1000 + N * 10 + K)
+    A = lossless_A(rng, M, K)
+    B = lossless_B(rng, K, N, 63 if avoid else 127)
+    bias = rng.uniform(-0.1, 0.1, size=N).astype(np.float32)
+    out = orc.dynamic_quantized_inner_product(A, B, bias=bias, avoid_overflow=avoid)
+    ref = (A.astype(np.float64) @ B.astype(np.float64) + bias.astype(np.float64)).astype(np.float32)
+    assert np.array_equal(out["C"], ref)
+    relu = orc.dynamic_quantized_inner_product(A, B, bias=bias, act=orc.ACT_RELU, avoid_overflow=avoid)
+    assert np.array_equal(relu["C"], np.where(ref > 0, ref, np.float32(0)))
+
+
+def test_inner_product_gelu_matches_erf_definition(orc):
+    rng = np.random.default_rng(21)
+    A = lossless_A(rng, 9, 40)
+    B = lossless_B(rng, 40, 11)
+    bias = rng.uniform(-0.5, 0.5, size=11).astype(np.float32)
+    out = orc.dynamic_quantized_inner_product(A, B, bias=bias, act=orc.ACT_GELU)
+    v = (A.astype(np.float64) @ B.astype(np.float64) + bias).astype(np.float32).astype(np.float64)
+    ref = np.vectorize(lambda t: 0.5 * t * (1.0 + math.erf(t / math.sqrt(2.0))))(v)
+    err = np.abs(out["C"].astype(np.float64) - ref)
+    # fp32 evaluation: a few ulps of the result, plus the absolute error of
+    # rounding 1 + erf(.) (|x| * 2^-24 scale), which dominates where 1 + erf
+    # cancels for negative x
+    tol = 4 * np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64) + np.abs(v) * 2.0 ** -22
+    assert np.all(err <= tol)
+
+
+def _error_bound(A, B, bias, qmax):
+    A64, B64 = A.astype(np.float64), B.astype(np.float64)
+    rng_A = np.maximum(A64.max(1), 0) - np.minimum(A64.min(1), 0)
+    eA = 0.5 * rng_A / 255 * (1 + 1e-3)
+    eB = 0.5 * np.abs(B64).max(0) / qmax * (1 + 1e-3)
+    ref = A64 @ B64 + bias
+    bound = (np.abs(A64) @ np.ones_like(B64)) * eB[None, :] + eA[:, None] * (np.ones_like(A64) @ np.abs(B64)) \
+        + A.shape[1] * eA[:, None] * eB[None, :] + 4 * 2.0 ** -24 * (np.abs(ref) + np.abs(bias)) + 1e-30
+    return ref, bound
+
+
+@pytest.mark.parametrize("avoid", [False, True])
+def test_inner_product_within_quantization_error_bound(orc, avoid):
+    w = workloads.inner_product(seed=0)
+    out = orc.dynamic_quantized_inner_product(w["A"], w["B"], bias=w["bias"], avoid_overflow=avoid)
+    ref, bound = _error_bound(w["A"], w["B"], w["bias"], 63 if avoid else 127)
+    assert np.all(np.abs(out["C"] - ref) <= bound)
+    # and the bound is not vacuous: the error is well below the result scale
+    assert np.max(np.abs(out["C"] - ref)) < 0.05 * np.max(np.abs(ref))
+
+
+@pytest.mark.parametrize("avoid", [True, False])
+def test_usage_ramp_example_within_bound(orc, avoid):
+    """The Simd usage example (M=4 N=8 K=16 ramps, bias 0.1, constant B,
+    identity, fp32, avoidOverflow as printed = true).  The page prints no
+    outputs, so the bound is the pin."""
+    w = workloads.usage_ramp()
+    out = orc.dynamic_quantized_inner_product(w["A"], w["B"], bias=w["bias"], avoid_overflow=avoid)
+    ref, bound = _error_bound(w["A"], w["B"], w["bias"], 63 if avoid else 127)
+    assert np.all(np.abs(out["C"] - ref) <= bound)
+    assert np.all(out["zeroA"] == 0)                 # all-positive rows
+    assert out["iB"].min() >= 0 and out["iB"].max() == (63 if avoid else 127)
+
+
+def test_inner_product_zero_point_identity(orc):
+    """sum_k (u - z) b == sum_k u b - z * colsum(b), checked in int64."""
+    w = workloads.inner_product(seed=0, M=16, N=24, K=96)
+    out = orc.dynamic_quantized_inner_product(w["A"], w["B"], bias=w["bias"])
+    u = out["uA"].astype(np.int64)
+    b = out["iB"].astype(np.int64)
+    z = out["zeroA"].astype(np.int64)
+    assert np.array_equal(out["acc"].astype(np.int64), u @ b - z[:, None] * b.sum(0)[None, :])
+
+
+def test_degenerate_rows_give_activated_bias(orc):
+    A = np.zeros((3, 10), np.float32)
+    rng = np.random.default_rng(2)
+    B = rng.normal(0, 0.05, (10, 6)).astype(np.float32)
+    bias = np.array([-0.3, -0.1, 0.0, 0.1, 0.2, 0.7], np.float32)
+    out = orc.dynamic_quantized_inner_product(A, B, bias=bias, act=orc.ACT_RELU)
+    assert np.array_equal(out["C"], np.tile(np.maximum(bias, 0), (3, 1)))
+    assert np.all(out["acc"] == 0)
+
+
+def test_bf16_conversion_matches_torch(orc):
+    rng = np.random.default_rng(4)
+    x = np.concatenate([rng.normal(0, 1, 5000), rng.normal(0, 1e30, 100), [0.0, -0.0, 1e-40, 3.0e38, -3.4e38]])
+    x = x.astype(np.float32)
+    # values exactly halfway between bf16 neighbours
+    halves = (np.arange(200, dtype=np.uint32) << 16 | 0x8000).view(np.float32)
+    x = np.concatenate([x, halves, -halves])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(orc.f32_to_bf16_bits(x), ref)
+
+
+def test_bf16_input_widening_is_exact(orc):
+    rng = np.random.default_rng(9)
+    a = rng.normal(0, 3, 1000).astype(np.float32)
+    bits = torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    assert np.array_equal(orc.bf16_bits_to_f32(bits), ref)
+
+
+# ----------------------------------------------------------------------------
+# QLinearConv invariants
+# ----------------------------------------------------------------------------
+
+def _small_conv(rng, N=2, C=4, H=6, W=5, M=3, k=3, group=1):
+    x = rng.integers(0, 256, size=(N, C, H, W)).astype(np.uint8)
+    w = rng.integers(0, 256, size=(M, C // group, k, k)).astype(np.uint8)
+    ws = rng.uniform(0.001, 0.01, size=M).astype(np.float32)
+    wz = rng.integers(100, 157, size=M)
+    B = rng.integers(-5000, 5001, size=M).astype(np.int32)
+    return x, w, ws, wz, B
+
+
+def test_conv_padding_is_real_zero(orc):
+    """A padded position holds real 0, i.e. the code x_zero_point: padding
+    by p equals an unpadded conv over x framed with x_zero_point."""
+    rng = np.random.default_rng(1)
+    x, w, ws, wz, B = _small_conv(rng)
+    y = orc.qlinearconv(x, np.float32(0.0037), 132, w, ws, wz, np.float32(0.05), 128, B, pads=(1, 2, 1, 0))
+    xp = np.full((2, 4, 8, 7), 132, np.uint8)
+    xp[:, :, 1:7, 2:7] = x
+    y2 = orc.qlinearconv(xp, np.float32(0.0037), 132, w, ws, wz, np.float32(0.05), 128, B)
+    assert np.array_equal(y, y2)
+
+
+def test_depthwise_equals_block_diagonal_dense(orc):
+    rng = np.random.default_rng(2)
+    C = 5
+    x, w, ws, wz, B = _small_conv(rng, C=C, M=C, group=C)
+    y = orc.qlinearconv(x, np.float32(0.0037), 132, w, ws, wz, np.float32(0.05), 128, B,
+                        pads=(1, 1, 1, 1), group=C)
+    dense = np.empty((C, C, 3, 3), np.uint8)
+    for m in range(C):
+        dense[m] = wz[m]              # off-diagonal taps contribute w - w_zp = 0
+        dense[m, m] = w[m, 0]
+    y2 = orc.qlinearconv(x, np.float32(0.0037), 132, dense, ws, wz, np.float32(0.05), 128, B,
+                         pads=(1, 1, 1, 1))
+    assert np.array_equal(y, y2)
+
+
+def test_conv_power_of_two_scales_equal_fp64_path(orc):
+    """With power-of-two scales the requantization is exact, so QLinearConv
+    equals DequantizeLinear -> float convolution (fp64) -> QuantizeLinear."""
+    rng = np.random.default_rng(3)
+    x, w, _, wz, B = _small_conv(rng, N=2, C=3, H=7, W=6, M=4)
+    xs, ws, ys = 2.0 ** -6, np.array([2.0 ** -7, 2.0 ** -8, 2.0 ** -6, 2.0 ** -9], np.float32), 2.0 ** -1
+    y = orc.qlinearconv(x, np.float32(xs), 120, w, ws, wz, np.float32(ys), 128, B, pads=(1, 1, 1, 1))
+    ref = _fp64_conv_path(x, xs, 120, w, ws, wz, ys, 128, B, pad=1)
+    assert np.array_equal(y, ref)
+
+
+def _fp64_conv_path(x, xs, xz, w, ws, wz, ys, yz, B, pad):
+    xd = (x.astype(np.float64) - xz) * xs
+    N, C, H, W = x.shape
+    M, _, k, _ = w.shape
+    wd = (w.astype(np.float64) - np.asarray(wz, np.float64)[:, None, None, None]) * \
+        np.asarray(ws, np.float64)[:, None, None, None]
+    xp = np.zeros((N, C, H + 2 * pad, W + 2 * pad))
+    xp[:, :, pad:pad + H, pad:pad + W] = xd
+    OH, OW = H + 2 * pad - k + 1, W + 2 * pad - k + 1
+    out = np.zeros((N, M, OH, OW))
+    for kh in range(k):
+        for kw in range(k):
+            out += np.einsum("nchw,mc->nmhw", xp[:, :, kh:kh + OH, kw:kw + OW], wd[:, :, kh, kw])
+    out += (B.astype(np.float64) * xs * np.asarray(ws, np.float64))[None, :, None, None]
+    q = np.rint(out / ys) + yz
+    return np.clip(q, 0, 255).astype(np.uint8)
+
+
+def test_conv_general_scales_near_fp64_path(orc):
+    rng = np.random.default_rng(4)
+    x, w, ws, wz, B = _small_conv(rng, N=2, C=8, H=9, W=7, M=6)
+    y = orc.qlinearconv(x, np.float32(0.0037), 132, w, ws, wz, np.float32(0.05), 128, B, pads=(1, 1, 1, 1))
+    ref = _fp64_conv_path(x, float(np.float32(0.0037)), 132, w, ws, wz, float(np.float32(0.05)), 128, B, 1)
+    d = np.abs(y.astype(int) - ref.astype(int))
+    assert d.max() <= 1 and np.mean(d == 0) > 0.98
+
+
+# ----------------------------------------------------------------------------
+# DynamicQuantizeLSTM
+# ----------------------------------------------------------------------------
+
+def _sig(v):
+    return 1.0 / (1.0 + np.exp(-v))
+
+
+def _textbook_lstm(X, Wf, Rf, B, direction_rev=False):
+    """fp64 unquantized LSTM, default activations, gate columns i, o, f, c."""
+    T, b, _ = X.shape
+    H = Rf.shape[0]
+    h = np.zeros((b, H))
+    c = np.zeros((b, H))
+    Y = np.zeros((T, b, H))
+    order = range(T - 1, -1, -1) if direction_rev else range(T)
+    for t in order:
+        g = X[t] @ Wf + h @ Rf + B[:4 * H] + B[4 * H:]
+        i, o, f, ct = _sig(g[:, :H]), _sig(g[:, H:2 * H]), _sig(g[:, 2 * H:3 * H]), np.tanh(g[:, 3 * H:])
+        c = f * c + i * ct
+        h = o * np.tanh(c)
+        Y[t] = h
+    return Y
+
+
+def test_lstm_first_step_lossless_equals_textbook(orc):
+    """Step 0 with h0 = 0: the recurrent product is exactly 0 and, with X on
+    the lossless grid and power-of-two W scales, the input projection is
+    exact, so the first hidden state is the textbook LSTM cell."""
+    rng = np.random.default_rng(6)
+    T, b, I, H = 1, 4, 24, 8
+    X = lossless_A(rng, T * b, I).reshape(T, b, I)
+    W = rng.integers(-128, 128, size=(1, I, 4 * H)).astype(np.int8)
+    R = rng.integers(-128, 128, size=(1, H, 4 * H)).astype(np.int8)
+    Ws = (2.0 ** rng.integers(-9, -6, size=(1, 4 * H))).astype(np.float32)
+    Rs = (2.0 ** rng.integers(-9, -6, size=(1, 4 * H))).astype(np.float32)
+    Bb = rng.normal(0, 0.1, size=(1, 8 * H)).astype(np.float32)
+    Y, Yh, Yc = orc.dynamic_quantize_lstm(X, W, R, Bb, Ws, Rs)
+    ref = _textbook_lstm(X.astype(np.float64), W[0] * Ws[0].astype(np.float64), R[0] * Rs[0].astype(np.float64),
+                         Bb[0].astype(np.float64))
+    assert np.allclose(Y[0, 0], ref[0], rtol=2e-6, atol=2e-7)
+    assert np.array_equal(Yh[0], Y[0, 0])
+
+
+@pytest.mark.parametrize("direction", ["forward", "reverse", "bidirectional"])
+def test_lstm_within_quantization_error_of_textbook(orc, direction):
+    w = workloads.lstm(seed=4, T=6, batch=3, I=32, H=16, D=2 if direction == "bidirectional" else 1)
+    Y, Yh, Yc = orc.dynamic_quantize_lstm(w["X"], w["W"], w["R"], w["B"], w["W_scale"], w["R_scale"],
+                                          direction=direction)
+    dirs = {"forward": [False], "reverse": [True], "bidirectional": [False, True]}[direction]
+    for d, rev in enumerate(dirs):
+        ref = _textbook_lstm(w["X"].astype(np.float64), w["W"][d] * w["W_scale"][d].astype(np.float64),
+                             w["R"][d] * w["R_scale"][d].astype(np.float64), w["B"][d].astype(np.float64), rev)
+        err = np.abs(Y[:, d] - ref)
+        assert err.max() < 0.02, err.max()
+        assert np.abs(ref).max() > 0.2        # non-trivial activations
+        last = 0 if rev else -1
+        assert np.array_equal(Yh[d], Y[last, d])
