@@ -1,0 +1,338 @@
+#!/usr/bin/env python
+"""Benchmark of the dynamic quantized int8 GEMM and QuantizeLinear on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl i8q|reference]
+
+One step is one Forward of the dynamic quantized inner product on the large
+workload (A bf16 8192 x 4096 quantized per row to uint8, constant int8 B
+4096 x 14336 with per-column scales, exact int32 product, dequantization,
+bias, GELU, bf16 C): the row quantization kernel and the GEMM kernel with
+its fused epilogue.  `value` is algorithmic TOPS (2*M*N*K per step) over
+all ranks.  The same run also times QuantizeLinear and DequantizeLinear on
+the [32,1024,4096] fp32 round-trip workload (HBM GB/s).
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own
+replica (weak scaling, no data-path collective); the time is the max over
+ranks.  --impl reference times the CPU oracle on a bounded sample of the
+same workload on this host's cores (rank 0 only).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+M, K, N = 8192, 4096, 14336
+QDQ_SHAPE = (32, 1024, 4096)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD = ("dynamic quantized GEMM M=8192 K=4096 N=14336: bf16 A quantized per row to uint8, constant int8 B with "
+            "per-column scales, int32 product, dequant + bias + GELU, bf16 C")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="i8q", choices=["i8q", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-rows", type=int, default=256, help="rows of the CPU-baseline sample")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def reduce_max(value, world):
+    """Max of a float over all ranks (the initialized process group)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def weak_scaling_value(ops_per_rank_step, steps, world, max_seconds):
+    """Whole-job throughput: the work of every rank over the slowest rank's time."""
+    return ops_per_rank_step * steps * world / max_seconds
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_loop(fn, steps, stream):
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3  # seconds
+
+
+def cpu_baseline(rows, seed=2):
+    """The oracle, as it stands, on `rows` rows of the large workload:
+    row quantization, integer product and epilogue.  Returns (TOPS, threads,
+    seconds, sample text)."""
+    import numpy as np
+
+    import oracle
+    from int8_quantized_gb300 import workloads
+    w = workloads.large_gemm(seed=seed, M=rows)
+    oracle.lib()
+    t0 = time.perf_counter()
+    oracle.dynamic_quantized_inner_product(w["A_bf16"], iB=w["iB"], scaleB=w["scaleB"], bias=w["bias"],
+                                           act=oracle.ACT_GELU, typeC="bf16")
+    dt = time.perf_counter() - t0
+    del np
+    return (2.0 * rows * N * K / dt / 1e12, oracle.num_threads(), dt,
+            f"{rows} of {M} rows of the large GEMM (row quantization, int32 product, dequant, bias, GELU, bf16); "
+            f"TOPS = 2*rows*N*K / time")
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    rows = max(8, min(args.cpu_rows // 4, 64))
+    for _ in range(args.warmup):
+        cpu_baseline(rows)
+    times = []
+    info = None
+    for _ in range(args.steps):
+        tops, threads, dt, sample = cpu_baseline(rows)
+        times.append(dt)
+        info = (threads, sample)
+    total = sum(times)
+    value = 2.0 * rows * N * K * args.steps / total / 1e12
+    line = {"impl": "reference", "metric": "dyn-quant int8 GEMM TOPS & % INT8 tensor peak; QuantizeLinear HBM GB/s",
+            "value": value, "unit": "TOPS", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8*s8->s32", "data": "synthetic",
+            "config": {"workload": WORKLOAD + f"; sampled {rows} rows per step on the host CPU"},
+            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": info[0], "kind": "oracle", "sample": info[1]},
+            "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_i8q(args):
+    import numpy as np
+    import torch
+
+    import int8_quantized_gb300 as q
+    from int8_quantized_gb300 import workloads
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+
+    # ---- large dynamic quantized GEMM -------------------------------------
+    w = workloads.large_gemm(seed=2 + rank)
+    ctx = q.QGemmDyn(M, N, K, q.BF16, q.S8, q.BF16, constB=True, bias=True, activation=q.ACT_GELU)
+    ctx.set_params(torch.from_numpy(w["iB"]).to(dev), torch.from_numpy(w["scaleB"]).to(dev),
+                   torch.from_numpy(w["bias"]).to(dev))
+    A = torch.from_numpy(w["A_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    buf = torch.empty(ctx.external_buffer_size(), dtype=torch.uint8, device=dev)
+    step = lambda: ctx.forward(A, C, buf=buf)  # noqa: E731
+    for _ in range(args.warmup):
+        step()
+    q.sync_status()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    q.profile_enable(True)
+    secs = time_loop(step, args.steps, stream)
+    prof = q.profile_collect()
+    q.profile_enable(False)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    q.sync_status()
+    max_secs = reduce_max(secs, world)
+    ops = 2.0 * M * N * K
+    value = weak_scaling_value(ops, args.steps, world, max_secs) / 1e12
+    launches = sum(v[0] for v in prof.values())
+    gemm_name = max((k for k in prof if k.startswith("gemm")), key=lambda k: prof[k][1])
+    gemm_ms = prof[gemm_name][1] / prof[gemm_name][0]
+    gemm_tops = ops / (gemm_ms * 1e-3) / 1e12
+    int8_peak = q.measure_int8_mma_peak()
+    if gemm_name == "gemm_imma":
+        peak, peak_note = int8_peak, "int8 mma.sync peak measured in this run"
+    else:
+        peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        peak_note = f"bf16 dense sustained ({peak_src})"
+
+    # ---- end to end through the host-buffer entry point -------------------
+    A_h = torch.from_numpy(w["A_bf16"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    C_h = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        ctx.forward_host(A_h, C_h)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ctx.forward_host(A_h, C_h)
+    e2e_secs = reduce_max(time.perf_counter() - t0, world)
+    e2e = {"value": weak_scaling_value(ops, args.steps, world, e2e_secs) / 1e12, "unit": "TOPS",
+           "h2d_bytes_per_step": A_h.numel() * 2, "d2h_bytes_per_step": C_h.numel() * 2}
+    del A_h, C_h, buf, C, A
+    ctx.clear()
+
+    # ---- QuantizeLinear / DequantizeLinear round trip ---------------------
+    d = workloads.qdq(seed=1)
+    x = torch.from_numpy(d["x"]).to(dev)
+    s = torch.from_numpy(d["scale"]).to(dev)
+    z = torch.from_numpy(d["zero_point"]).to(dev)
+    y = torch.empty(QDQ_SHAPE, dtype=torch.uint8, device=dev)
+    xr = torch.empty(QDQ_SHAPE, dtype=torch.float32, device=dev)
+    nel = x.numel()
+    qstep = lambda: q.quantize_linear(x, s, z, y, axis=2)  # noqa: E731
+    dstep = lambda: q.dequantize_linear(y, s, z, xr, axis=2)  # noqa: E731
+    for _ in range(args.warmup):
+        qstep()
+        dstep()
+    torch.cuda.synchronize()
+    barrier(world)
+    q_secs = reduce_max(time_loop(qstep, args.steps, stream), world)
+    dq_secs = reduce_max(time_loop(dstep, args.steps, stream), world)
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    q_gbs = weak_scaling_value(5.0 * nel, args.steps, world, q_secs) / 1e9
+    dq_gbs = weak_scaling_value(5.0 * nel, args.steps, world, dq_secs) / 1e9
+    del x, y, xr
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tops, threads, dt, sample = cpu_baseline(args.cpu_rows)
+        cpu = {"value": tops, "unit": "TOPS", "cores": threads, "kind": "oracle", "sample": sample,
+               "seconds": round(dt, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": "dyn-quant int8 GEMM TOPS & % INT8 tensor peak; QuantizeLinear HBM GB/s",
+            "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": max_secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8*s8->s32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (A 67 MB + B 59 MB + C 235 MB per step)",
+                       "kernel": gemm_name},
+            "roofline": {"bound": "tensor", "achieved": gemm_tops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": gemm_tops / peak, "traffic": None, "peak_source": peak_note,
+                         "kernel": gemm_name, "kernel_ms": gemm_ms},
+            "int8_tensor_peak_tops": int8_peak,
+            "pct_int8_tensor_peak": 100.0 * value / world / int8_peak,
+            "pct_bf16_dense_peak": 100.0 * value / world / peaks.get("bf16_tflops", 1900.0),
+            "quantize_linear": {"value": q_gbs, "unit": "GB/s", "ms": q_secs / args.steps * 1e3,
+                                "frac_hbm": q_gbs / world / hbm, "frac_8tbs": q_gbs / world / 8000.0,
+                                "bytes": 5 * nel, "workload": "x fp32 [32,1024,4096] per-axis(2) -> uint8"},
+            "dequantize_linear": {"value": dq_gbs, "unit": "GB/s", "ms": dq_secs / args.steps * 1e3,
+                                  "frac_hbm": dq_gbs / world / hbm, "frac_8tbs": dq_gbs / world / 8000.0,
+                                  "bytes": 5 * nel, "workload": "uint8 [32,1024,4096] per-axis(2) -> fp32"},
+            "kernels": {k: {"launches": v[0], "ms": v[1] / max(v[0], 1)} for k, v in prof.items()},
+            "gpu_launches": launches,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clk,
+            "peaks_source": peak_src,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_i8q(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

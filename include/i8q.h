@@ -1,0 +1,302 @@
+/*
+ * i8q.h -- C ABI of libi8q.so, a single-GPU (sm_103a) engine for linear int8
+ * quantization and the quantized matrix products it feeds.
+ *
+ * Conventions for every entry point below
+ *  - Status: functions returning int give I8Q_OK (0) on success or a negative
+ *    I8Q_ERR_* code.  The text of the most recent error on the calling host
+ *    thread is returned by i8q_last_error().  Arguments are validated on the
+ *    host before anything is launched; a rejected call launches nothing and
+ *    writes nothing.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Calls are asynchronous on that stream unless stated.
+ *  - Pointers: tensor arguments are DEVICE pointers unless stated.  The
+ *    caller owns every tensor, every workspace and the stream; a context owns
+ *    only the internal buffers it allocates.  Tensors are dense and
+ *    row-major (C order) with the shapes given; no aliasing between inputs
+ *    and outputs.
+ *  - Exactness: integer results (quantized tensors, int32 accumulators) are
+ *    bit-exact.  Float epilogues evaluate each operation once, in fp32,
+ *    rounding to nearest even, in the order the operator text gives (no
+ *    fused multiply-add); fp32->bf16 rounds to nearest even.
+ *
+ * Sources, by page title and section:
+ *  [DQIP] Simd, "SynetDynamicQuantizedInnerProduct16b": Detailed Description
+ *         (algorithm listing; typeA/typeB/typeC and avoidOverflow paragraph)
+ *         and the member documentation of Init, Enable, InternalBufferSize,
+ *         ExternalBufferSize, Info, SetParams, Forward, Clear.
+ *  [QL]   ONNX Runtime contrib schemas, "QuantizeLinear" ver 1.
+ *  [DQL]  ONNX Runtime contrib schemas, "DequantizeLinear" ver 1.
+ *  [QLC]  onnx-light docs, "QLinearConv" (since version 10): inputs, bias
+ *         rule, type constraints.
+ *  [LSTM] ONNX Runtime contrib schemas, "DynamicQuantizeLSTM": attributes,
+ *         inputs X, W, R, B, initial_h, initial_c, W/R scale and zero point,
+ *         outputs Y, Y_h, Y_c.
+ */
+#ifndef I8Q_H
+#define I8Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define I8Q_OK 0
+#define I8Q_ERR_INVALID_ARG (-1)    /* bad pointer, size, type or combination */
+#define I8Q_ERR_UNSUPPORTED (-2)    /* valid operator input this build does not run */
+#define I8Q_ERR_NOT_INITIALIZED (-3) /* context missing, or SetParams not yet called */
+#define I8Q_ERR_ALLOC (-4)          /* device allocation failed */
+#define I8Q_ERR_CUDA (-5)           /* a CUDA runtime/driver call failed */
+#define I8Q_ERR_DEVICE_TIMEOUT (-6) /* a bounded device-side wait gave up */
+
+/* ---- element types ----------------------------------------------------- */
+#define I8Q_F32 0
+#define I8Q_BF16 1
+#define I8Q_S8 2
+#define I8Q_U8 3
+#define I8Q_S32 4
+
+/* ---- activations applied after the bias ([DQIP] Forward) --------------- */
+#define I8Q_ACT_IDENTITY 0
+#define I8Q_ACT_RELU 1
+#define I8Q_ACT_GELU 2 /* 0.5*x*(1+erf(x/sqrt(2))), fp32 */
+
+/* ---- QuantizeLinear / DequantizeLinear axis ------------------------------ */
+#define I8Q_NO_AXIS INT32_MIN /* no 'axis' attribute: per-tensor parameters */
+
+/* ---- LSTM direction ------------------------------------------------------ */
+#define I8Q_LSTM_FORWARD 0
+#define I8Q_LSTM_REVERSE 1
+#define I8Q_LSTM_BIDIRECTIONAL 2
+
+/* Text of the last error raised on this host thread ("" if none).  The
+ * pointer stays valid until the next call on this thread. */
+const char* i8q_last_error(void);
+
+/* Library version string, e.g. "i8q 0.1 sm_103a". */
+const char* i8q_version(void);
+
+/* ========================================================================
+ * Dynamic quantized inner product [DQIP]
+ *
+ *   A[i,k] -> uA[i,k], scaleA[i], zeroA[i]   (uint8, per row)
+ *   B[k,j] -> iB[k,j], scaleB[j]             (int8, per column; or given)
+ *   sum    = sum_k (uA[i,k] - zeroA[i]) * iB[k,j]          (exact int32)
+ *   C[i,j] = ConvertToTypeC(Activate(sum * scaleA[i] * scaleB[j] + bias[j]))
+ *
+ * Row quantization of A (the page names only its outputs): per row,
+ * mn = min(0, min A), mx = max(0, max A), scaleA = (mx - mn) / 255,
+ * zeroA = saturate_u8(rint(-mn / scaleA)), uA = saturate_u8(rint(A / scaleA)
+ * + zeroA); an all-zero row takes scaleA = 1, zeroA = 0.
+ * Column quantization of fp32/bf16 B: scaleB = max|B[:,j]| / 127 (or / 63
+ * with avoidOverflow, range [-64,63]), iB = saturate(rint(B / scaleB)); an
+ * all-zero column takes scaleB = 1.  rint rounds half to even.
+ * Layouts: A is M x K, B is K x N, C is M x N, all row-major.
+ * ====================================================================== */
+typedef struct i8q_qgemm_ctx i8q_qgemm_ctx;
+
+/* Init [DQIP]: create (*ctx == NULL) or re-initialize (*ctx != NULL) a
+ * context on the current CUDA device.  An existing context is recreated only
+ * when any argument differs from its own (sizes, types, constB, bias flag,
+ * activation, avoidOverflow); otherwise it is kept with its parameters.
+ *   typeA: I8Q_F32 | I8Q_BF16.  typeC: I8Q_F32 | I8Q_BF16.
+ *   typeB: I8Q_F32 | I8Q_S8 (constB only) when constB; I8Q_F32 | I8Q_BF16
+ *          when B is given to every Forward.
+ *   activation: I8Q_ACT_*.  avoidOverflow is ignored when typeB is I8Q_S8.
+ *   M, N, K >= 1 and K <= 65536 (so every int32 sum is exact).
+ * Synchronous.  Errors: INVALID_ARG, UNSUPPORTED, ALLOC, CUDA; on error
+ * *ctx is left as it was. */
+int i8q_qgemm_dyn_init(i8q_qgemm_ctx** ctx, size_t M, size_t N, size_t K, int typeA, int typeB,
+                       int typeC, int constB, int bias, int activation, int avoidOverflow);
+
+/* Enable [DQIP]: 1 if ctx exists and Forward can be called (for constB,
+ * SetParams has been called), else 0. */
+int i8q_qgemm_dyn_enabled(const i8q_qgemm_ctx* ctx);
+
+/* InternalBufferSize [DQIP]: bytes of device memory the context owns:
+ * quantized B (int8 and the bf16 operand copy), column sums, B scales, bias,
+ * activation parameters and the fallback scratch used when Forward gets
+ * buf == NULL.  0 for a NULL ctx. */
+size_t i8q_qgemm_dyn_internal_buffer_size(const i8q_qgemm_ctx* ctx);
+
+/* ExternalBufferSize [DQIP]: bytes of the caller's scratch `buf` for
+ * Forward: the quantized copy of A (uint8 and its bf16 operand copy),
+ * scaleA, zeroA and, for non-constant B, its quantized copy, scales and
+ * column sums.  0 for a NULL ctx. */
+size_t i8q_qgemm_dyn_external_buffer_size(const i8q_qgemm_ctx* ctx);
+
+/* Info [DQIP]: short description of the selected implementation (device
+ * architecture and algorithm).  Owned by ctx, valid until the next call of
+ * this function or i8q_qgemm_dyn_clear; NULL for a NULL ctx. */
+const char* i8q_qgemm_dyn_info(i8q_qgemm_ctx* ctx);
+
+/* SetParams [DQIP]: store weights, bias and activation parameters.
+ *   weight: K x N, fp32 (typeB F32, quantized here per column) or int8
+ *           (typeB S8, stored as given).  Required when constB; ignored
+ *           (may be NULL) otherwise.
+ *   scale:  N fp32 per-column scales; required when typeB is S8, else
+ *           ignored.
+ *   bias:   N fp32, or NULL for zeros (also ignored when Init had bias = 0).
+ *   params: activation parameters, or NULL (none of I8Q_ACT_* takes any).
+ * Pointers may be host or device memory (copied with cudaMemcpyDefault).
+ * Synchronous: returns after the copy-in and weight preparation finished.
+ * Errors: NOT_INITIALIZED, INVALID_ARG, CUDA. */
+int i8q_qgemm_dyn_set_params(i8q_qgemm_ctx* ctx, const void* weight, const float* scale,
+                             const float* bias, const float* params, void* stream);
+
+/* Forward [DQIP]: C = dynamic quantized product of A and B.
+ *   A: M x K of typeA.  B: K x N of typeB, or NULL when constB.
+ *   buf: device scratch of at least i8q_qgemm_dyn_external_buffer_size
+ *        bytes, 256-byte aligned, or NULL to use the context's own.
+ *   C: M x N of typeC.
+ * A, B and C are device pointers.  Asynchronous on stream; concurrent
+ * Forward calls on one context must use distinct buf (a NULL buf is shared).
+ * Errors: NOT_INITIALIZED, INVALID_ARG, CUDA. */
+int i8q_qgemm_dyn_forward(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf, void* C,
+                          void* stream);
+
+/* Same as Forward, but A and C are HOST pointers (pinned or pageable): A is
+ * copied to context-owned device staging memory, the product runs, and C is
+ * copied back, all on `stream`; returns after C is in host memory.  Not on
+ * the pages: it is the whole host-to-host path of Forward for callers that
+ * keep their tensors in host memory.  B must be NULL (constB contexts). */
+int i8q_qgemm_dyn_forward_host(i8q_qgemm_ctx* ctx, const void* A_host, void* C_host, void* stream);
+
+/* Test hook, not on the pages: run Forward's quantization and integer
+ * product, and write the exact int32 sums sum_k (uA - zeroA) * iB (M x N)
+ * to acc instead of the float epilogue.  Same arguments as Forward. */
+int i8q_qgemm_dyn_forward_s32(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf,
+                              int32_t* acc, void* stream);
+
+/* Test hook, not on the pages: device addresses, inside `buf` (or the
+ * context's fallback scratch when buf is NULL), of the quantized A written
+ * by the last Forward: uA (M x K uint8, row stride *lda bytes), scaleA (M
+ * fp32) and zeroA (M int32).  Any output pointer may be NULL. */
+int i8q_qgemm_dyn_buf_views(i8q_qgemm_ctx* ctx, void* buf, uint8_t** uA, size_t* lda, float** scaleA,
+                            int32_t** zeroA);
+
+/* Test hook, not on the pages: device addresses of the stored quantized
+ * constant B, transposed to N x K int8 (row stride *ldb bytes), its N fp32
+ * scales and N int32 column sums. */
+int i8q_qgemm_dyn_weight_views(i8q_qgemm_ctx* ctx, int8_t** iBt, size_t* ldb, float** scaleB,
+                               int32_t** colsum);
+
+/* Clear [DQIP]: release the context and everything it owns; *ctx = NULL.
+ * Synchronizes the device first.  NULL or *ctx == NULL is a no-op. */
+void i8q_qgemm_dyn_clear(i8q_qgemm_ctx** ctx);
+
+/* ========================================================================
+ * QuantizeLinear [QL] and DequantizeLinear [DQL]
+ *
+ * x has `rank` dims given by the HOST array `shape` (rank 0..8).  Per-tensor
+ * (axis == I8Q_NO_AXIS): n_scale == 1.  Per-axis: axis in [-rank, rank-1]
+ * and n_scale == shape[axis].  Scale and zero point are device arrays of
+ * n_scale entries; the zero point has the quantized type.
+ * ====================================================================== */
+
+/* QuantizeLinear [QL]: y = saturate(rint(x / y_scale) + y_zero_point),
+ * rint = round half to even, saturating to [0,255] (ytype I8Q_U8) or
+ * [-128,127] (I8Q_S8).  x: fp32.  y: same shape, ytype.  Scales must be
+ * finite and nonzero for defined results. */
+int i8q_quantize_linear(const float* x, const int64_t* shape, int rank, int axis, const float* y_scale,
+                        const void* y_zero_point, size_t n_scale, int ytype, void* y, void* stream);
+
+/* DequantizeLinear [DQL]: y = (x - x_zero_point) * x_scale, fp32 output.
+ * x: xtype I8Q_U8 or I8Q_S8. */
+int i8q_dequantize_linear(const void* x, int xtype, const int64_t* shape, int rank, int axis,
+                          const float* x_scale, const void* x_zero_point, size_t n_scale, float* y,
+                          void* stream);
+
+/* ========================================================================
+ * QLinearConv [QLC], 2-D, NCHW
+ *
+ *   acc = sum_{c in group, kh, kw} (x - x_zero_point) * (w - w_zero_point[m])
+ *         (a position outside x holds real 0, i.e. x_zero_point)
+ *   acc += B[m]   (int32 bias, scale x_scale*w_scale[m], zero point 0)
+ *   y = saturate(rint(((float)acc * (x_scale * w_scale[m])) / y_scale) + y_zero_point)
+ * The page gives no requantization formula; this is DequantizeLinear of the
+ * accumulator followed by QuantizeLinear with (y_scale, y_zero_point).
+ *   x: xtype (U8|S8) [N, C, H, W].  w: wtype (U8|S8) [M, C/group, kH, kW].
+ *   w_scale / w_zero_point: n_w == 1 (per tensor) or n_w == M entries
+ *   (device; the zero point has type wtype).  B: int32 [M] or NULL.
+ *   pads {top, left, bottom, right} >= 0; strides, dilations {h, w} >= 1;
+ *   C == w.shape[1] * group, M % group == 0.
+ *   y: ytype (U8|S8) [N, M, OH, OW], OH = (H + pt + pb - dh*(kH-1) - 1)/sh + 1.
+ * workspace: device scratch of at least i8q_qlinearconv_workspace_size
+ * bytes (may be NULL when that size is 0), 256-byte aligned. */
+int i8q_qlinearconv(const void* x, int xtype, const int64_t* xshape, float x_scale, int x_zero_point,
+                    const void* w, int wtype, const int64_t* wshape, const float* w_scale,
+                    const void* w_zero_point, size_t n_w, float y_scale, int y_zero_point,
+                    const int32_t* B, const int64_t* pads, const int64_t* strides,
+                    const int64_t* dilations, int64_t group, void* y, int ytype, void* workspace,
+                    size_t ws_bytes, void* stream);
+
+/* Scratch bytes i8q_qlinearconv needs for these shapes (host arrays as in
+ * i8q_qlinearconv).  Returns 0 on invalid shapes. */
+size_t i8q_qlinearconv_workspace_size(const int64_t* xshape, const int64_t* wshape, const int64_t* pads,
+                                      const int64_t* strides, const int64_t* dilations, int64_t group);
+
+/* ========================================================================
+ * DynamicQuantizeLSTM [LSTM]: int8 W and R with per-channel (or
+ * per-direction) scales and zero point 0, fp32 X, default activations
+ * (sigmoid for i, o, f; tanh for the cell candidate and the output), gate
+ * column order i, o, f, c; no peepholes, no sequence_lens, no clip,
+ * input_forget = 0.  X and each step's hidden state are quantized per row
+ * to uint8 exactly as A of the dynamic quantized inner product.
+ *   Per direction d and step t (t runs T-1..0 for the reverse direction):
+ *   Gx = X_t W[d] (dequantized), Gh = h_{t-1} R[d] (dequantized),
+ *   g = ((Gx + Gh) + Wb) + Rb; i,o,f = sigmoid; ct = tanh;
+ *   c = f*c_{t-1} + i*ct; h = o*tanh(c).
+ *   X [T, batch, input]; W [D, input, 4H]; R [D, H, 4H] (int8);
+ *   W_scale, R_scale: n == D (per direction) or D*4H (per channel) fp32;
+ *   W_zero_point, R_zero_point: int8, n entries, all zero, or NULL;
+ *   Bias [D, 8H] or NULL; h0, c0 [D, batch, H] or NULL (zeros);
+ *   Y [T, D, batch, H], Y_h, Y_c [D, batch, H]; any output may be NULL.
+ *   D = 2 for I8Q_LSTM_BIDIRECTIONAL, else 1.
+ * workspace: at least i8q_dq_lstm_workspace_size bytes, 256-byte aligned.
+ * Errors: INVALID_ARG, UNSUPPORTED (nonzero zero points), CUDA. */
+int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int64_t input, int64_t hidden,
+                        int direction, const int8_t* W, const float* W_scale, const int8_t* W_zero_point,
+                        size_t n_wscale, const int8_t* R, const float* R_scale,
+                        const int8_t* R_zero_point, size_t n_rscale, const float* Bias, const float* h0,
+                        const float* c0, float* Y, float* Y_h, float* Y_c, void* workspace,
+                        size_t ws_bytes, void* stream);
+
+size_t i8q_dq_lstm_workspace_size(int64_t T, int64_t batch, int64_t input, int64_t hidden, int direction);
+
+/* ========================================================================
+ * Measurement (not on the pages)
+ * ====================================================================== */
+
+/* Kernel timing.  While enabled, every kernel launch of this library is
+ * bracketed by CUDA events on its launch stream.  Enabling (or disabling)
+ * drops all records.  Single-threaded use. */
+int i8q_profile_enable(int on);
+
+/* Synchronize the device, fold the records into per-kernel totals and
+ * return the number of distinct kernel names (or a negative error). */
+int i8q_profile_collect(void);
+
+/* Totals of kernel i (0 <= i < count): name (owned by the library, valid
+ * until the next enable), number of launches, summed event time in ms. */
+int i8q_profile_entry(int i, const char** name, long long* launches, double* total_ms);
+
+/* Throughput of back-to-back mma.sync m16n8k32 u8 x s8 -> s32 on every SM
+ * (the int8 tensor instruction sm_103a accepts), `iters` rounds of 8 MMAs
+ * per warp.  Synchronous.  *tops receives 10^12 integer ops per second,
+ * counting a multiply-add as 2 ops. */
+int i8q_measure_int8_mma_peak(int64_t iters, void* stream, double* tops);
+
+/* Synchronize `stream` and report any error recorded by a device-side
+ * bounded wait since the last call (I8Q_ERR_DEVICE_TIMEOUT), or a pending
+ * CUDA error (I8Q_ERR_CUDA).  Clears the recorded state. */
+int i8q_sync_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* I8Q_H */

@@ -1,0 +1,263 @@
+"""int8_quantized_gb300: Python binding of libi8q.so (include/i8q.h).
+
+Argument marshalling only: every function passes device pointers of torch
+CUDA tensors, sizes and the current CUDA stream to the C ABI, and raises
+I8QError on a nonzero status.  No computation happens here, and there is no
+fallback: without the built library every call raises.
+
+Names follow the C entry points without their ``i8q_`` prefix.
+"""
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (ACT_GELU, ACT_IDENTITY, ACT_RELU, BF16, F32, LSTM_BIDIRECTIONAL, LSTM_FORWARD, LSTM_REVERSE,
+                   NO_AXIS, S8, S32, U8, I8QError, check, last_error)
+
+__all__ = ["QGemmDyn", "quantize_linear", "dequantize_linear", "qlinearconv", "qlinearconv_workspace_size",
+           "dq_lstm_forward", "dq_lstm_workspace_size", "sync_status", "version", "I8QError", "last_error",
+           "F32", "BF16", "S8", "U8", "S32", "ACT_IDENTITY", "ACT_RELU", "ACT_GELU", "NO_AXIS",
+           "LSTM_FORWARD", "LSTM_REVERSE", "LSTM_BIDIRECTIONAL"]
+
+_TORCH_TYPE = {torch.float32: F32, torch.bfloat16: BF16, torch.int8: S8, torch.uint8: U8, torch.int32: S32}
+
+
+def _L():
+    return _lib.load()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, name, dtype=None):
+    """Device pointer of a contiguous CUDA tensor (None passes NULL)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _i64_array(vals):
+    vals = list(int(v) for v in vals)
+    return (ctypes.c_int64 * max(1, len(vals)))(*vals)
+
+
+def version():
+    return _L().i8q_version().decode()
+
+
+def sync_status(stream=None):
+    """Synchronize the stream and raise if a device-side bounded wait gave up."""
+    check(_L().i8q_sync_status(_stream(stream)), "sync_status")
+
+
+def profile_enable(on=True):
+    """Start (dropping earlier records) or stop kernel timing."""
+    check(_L().i8q_profile_enable(int(bool(on))), "profile_enable")
+
+
+def profile_collect():
+    """{kernel name: (launches, total ms)} of the launches timed so far."""
+    n = _L().i8q_profile_collect()
+    if n < 0:
+        raise I8QError(n, "profile_collect")
+    out = {}
+    for i in range(n):
+        name, launches, ms = ctypes.c_char_p(), ctypes.c_longlong(), ctypes.c_double()
+        check(_L().i8q_profile_entry(i, ctypes.byref(name), ctypes.byref(launches), ctypes.byref(ms)),
+              "profile_entry")
+        out[name.value.decode()] = (int(launches.value), float(ms.value))
+    return out
+
+
+def measure_int8_mma_peak(iters=20000, stream=None):
+    """Measured TOPS of back-to-back int8 mma.sync on every SM."""
+    tops = ctypes.c_double()
+    check(_L().i8q_measure_int8_mma_peak(int(iters), _stream(stream), ctypes.byref(tops)), "measure_int8_mma_peak")
+    return float(tops.value)
+
+
+# ---------------------------------------------------------------------------
+class QGemmDyn:
+    """Dynamic quantized inner product context (Simd
+    SynetDynamicQuantizedInnerProduct16b: Init / Enable / InternalBufferSize /
+    ExternalBufferSize / Info / SetParams / Forward / Clear)."""
+
+    def __init__(self, M, N, K, typeA=F32, typeB=F32, typeC=F32, constB=True, bias=True, activation=ACT_IDENTITY,
+                 avoidOverflow=False):
+        self._ctx = ctypes.c_void_p(None)
+        self.init(M, N, K, typeA, typeB, typeC, constB, bias, activation, avoidOverflow)
+
+    def init(self, M, N, K, typeA=F32, typeB=F32, typeC=F32, constB=True, bias=True, activation=ACT_IDENTITY,
+             avoidOverflow=False):
+        check(_L().i8q_qgemm_dyn_init(ctypes.byref(self._ctx), M, N, K, typeA, typeB, typeC, int(bool(constB)),
+                                      int(bool(bias)), activation, int(bool(avoidOverflow))), "qgemm_dyn_init")
+        self.M, self.N, self.K = M, N, K
+        self.typeA, self.typeB, self.typeC = typeA, typeB, typeC
+        self.constB = bool(constB)
+
+    def enabled(self):
+        return bool(_L().i8q_qgemm_dyn_enabled(self._ctx))
+
+    def internal_buffer_size(self):
+        return int(_L().i8q_qgemm_dyn_internal_buffer_size(self._ctx))
+
+    def external_buffer_size(self):
+        return int(_L().i8q_qgemm_dyn_external_buffer_size(self._ctx))
+
+    def info(self):
+        r = _L().i8q_qgemm_dyn_info(self._ctx)
+        return None if r is None else r.decode()
+
+    def set_params(self, weight=None, scale=None, bias=None, params=None, stream=None):
+        """weight K x N (fp32 or int8), scale N fp32, bias N fp32: CUDA tensors."""
+        check(_L().i8q_qgemm_dyn_set_params(self._ctx, _dev(weight, "weight"), _dev(scale, "scale", torch.float32),
+                                            _dev(bias, "bias", torch.float32), _dev(params, "params", torch.float32),
+                                            _stream(stream)), "qgemm_dyn_set_params")
+
+    def forward(self, A, C, B=None, buf=None, stream=None):
+        check(_L().i8q_qgemm_dyn_forward(self._ctx, _dev(A, "A"), _dev(B, "B"), _dev(buf, "buf"), _dev(C, "C"),
+                                         _stream(stream)), "qgemm_dyn_forward")
+        return C
+
+    def forward_s32(self, A, acc, B=None, buf=None, stream=None):
+        check(_L().i8q_qgemm_dyn_forward_s32(self._ctx, _dev(A, "A"), _dev(B, "B"), _dev(buf, "buf"),
+                                             _dev(acc, "acc", torch.int32), _stream(stream)), "qgemm_dyn_forward_s32")
+        return acc
+
+    def forward_host(self, A_host, C_host, stream=None):
+        """A_host, C_host: CPU tensors (pinned for asynchronous copies)."""
+        for t, n in ((A_host, "A_host"), (C_host, "C_host")):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{n} must be a contiguous CPU tensor")
+        check(_L().i8q_qgemm_dyn_forward_host(self._ctx, ctypes.c_void_p(A_host.data_ptr()),
+                                              ctypes.c_void_p(C_host.data_ptr()), _stream(stream)),
+              "qgemm_dyn_forward_host")
+        return C_host
+
+    def buf_views(self, buf=None):
+        """(uA M x lda uint8, scaleA M fp32, zeroA M int32) written by the last
+        forward, as torch views of the device buffer."""
+        uA, lda, sA, zA = ctypes.c_void_p(), ctypes.c_size_t(), ctypes.c_void_p(), ctypes.c_void_p()
+        check(_L().i8q_qgemm_dyn_buf_views(self._ctx, _dev(buf, "buf"), ctypes.byref(uA), ctypes.byref(lda),
+                                           ctypes.byref(sA), ctypes.byref(zA)), "qgemm_dyn_buf_views")
+        return (_wrap(uA.value, (self.M, lda.value), torch.uint8), _wrap(sA.value, (self.M,), torch.float32),
+                _wrap(zA.value, (self.M,), torch.int32), lda.value)
+
+    def weight_views(self):
+        """(iBt N x ldb int8, scaleB N fp32, colsum N int32) of the stored B."""
+        q, ldb, s, cs = ctypes.c_void_p(), ctypes.c_size_t(), ctypes.c_void_p(), ctypes.c_void_p()
+        check(_L().i8q_qgemm_dyn_weight_views(self._ctx, ctypes.byref(q), ctypes.byref(ldb), ctypes.byref(s),
+                                              ctypes.byref(cs)), "qgemm_dyn_weight_views")
+        return (_wrap(q.value, (self.N, ldb.value), torch.int8), _wrap(s.value, (self.N,), torch.float32),
+                _wrap(cs.value, (self.N,), torch.int32), ldb.value)
+
+    def clear(self):
+        if getattr(self, "_ctx", None) is not None and self._ctx.value:
+            _L().i8q_qgemm_dyn_clear(ctypes.byref(self._ctx))
+
+    def __del__(self):
+        try:
+            self.clear()
+        except Exception:
+            pass
+
+
+_TYPESTR = {torch.uint8: "|u1", torch.int8: "|i1", torch.float32: "<f4", torch.int32: "<i4"}
+
+
+class _DeviceArray:
+    """Describes library-owned device memory to torch (CUDA array interface)."""
+
+    def __init__(self, ptr, shape, dtype):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": _TYPESTR[dtype], "data": (ptr, False),
+                                         "version": 2, "strides": None}
+
+
+def _wrap(ptr, shape, dtype):
+    """Copy of device memory owned by the library, as a torch tensor (the
+    copy does not alias library storage)."""
+    torch.cuda.current_stream().synchronize()
+    return torch.as_tensor(_DeviceArray(ptr, shape, dtype), device="cuda").clone()
+
+
+# ---------------------------------------------------------------------------
+def quantize_linear(x, y_scale, y_zero_point, y, axis=None, stream=None):
+    """QuantizeLinear: y (uint8/int8 CUDA tensor, shape of x) from fp32 x;
+    y_scale / y_zero_point CUDA tensors (1 entry, or dim[axis] entries)."""
+    yt = _TORCH_TYPE[y.dtype]
+    if y_zero_point.dtype != y.dtype:
+        raise TypeError("y_zero_point must have y's dtype")
+    shape = _i64_array(x.shape)
+    check(_L().i8q_quantize_linear(_dev(x, "x", torch.float32), shape, x.dim(), NO_AXIS if axis is None else axis,
+                                   _dev(y_scale, "y_scale", torch.float32), _dev(y_zero_point, "y_zero_point"),
+                                   y_scale.numel(), yt, _dev(y, "y"), _stream(stream)), "quantize_linear")
+    return y
+
+
+def dequantize_linear(x, x_scale, x_zero_point, y, axis=None, stream=None):
+    """DequantizeLinear: fp32 y from uint8/int8 x."""
+    xt = _TORCH_TYPE[x.dtype]
+    shape = _i64_array(x.shape)
+    check(_L().i8q_dequantize_linear(_dev(x, "x"), xt, shape, x.dim(), NO_AXIS if axis is None else axis,
+                                     _dev(x_scale, "x_scale", torch.float32), _dev(x_zero_point, "x_zero_point"),
+                                     x_scale.numel(), _dev(y, "y", torch.float32), _stream(stream)),
+          "dequantize_linear")
+    return y
+
+
+def _conv_arrays(x_shape, w_shape, pads, strides, dilations):
+    return (_i64_array(x_shape), _i64_array(w_shape), _i64_array(pads), _i64_array(strides), _i64_array(dilations))
+
+
+def qlinearconv_workspace_size(x_shape, w_shape, pads=(0, 0, 0, 0), strides=(1, 1), dilations=(1, 1), group=1):
+    xs, ws, p, s, d = _conv_arrays(x_shape, w_shape, pads, strides, dilations)
+    return int(_L().i8q_qlinearconv_workspace_size(xs, ws, p, s, d, group))
+
+
+def qlinearconv(x, x_scale, x_zero_point, w, w_scale, w_zero_point, y_scale, y_zero_point, y, B=None,
+                pads=(0, 0, 0, 0), strides=(1, 1), dilations=(1, 1), group=1, workspace=None, stream=None):
+    """QLinearConv, NCHW.  x_scale, y_scale: floats; x_zero_point,
+    y_zero_point: ints; w_scale (fp32) / w_zero_point (w's dtype): CUDA
+    tensors of 1 or M entries; B: int32 CUDA tensor [M] or None."""
+    xs, ws, p, s, d = _conv_arrays(x.shape, w.shape, pads, strides, dilations)
+    if w_zero_point.dtype != w.dtype:
+        raise TypeError("w_zero_point must have w's dtype")
+    check(_L().i8q_qlinearconv(_dev(x, "x"), _TORCH_TYPE[x.dtype], xs, float(x_scale), int(x_zero_point),
+                               _dev(w, "w"), _TORCH_TYPE[w.dtype], ws, _dev(w_scale, "w_scale", torch.float32),
+                               _dev(w_zero_point, "w_zero_point"), w_scale.numel(), float(y_scale),
+                               int(y_zero_point), _dev(B, "B", torch.int32), p, s, d, int(group), _dev(y, "y"),
+                               _TORCH_TYPE[y.dtype], _dev(workspace, "workspace"),
+                               0 if workspace is None else workspace.numel() * workspace.element_size(),
+                               _stream(stream)), "qlinearconv")
+    return y
+
+
+def dq_lstm_workspace_size(T, batch, input_size, hidden, direction):
+    return int(_L().i8q_dq_lstm_workspace_size(T, batch, input_size, hidden, direction))
+
+
+def dq_lstm_forward(X, W, R, W_scale, R_scale, workspace, direction=LSTM_FORWARD, B=None, h0=None, c0=None,
+                    Y=None, Y_h=None, Y_c=None, W_zero_point=None, R_zero_point=None, stream=None):
+    """DynamicQuantizeLSTM.  X [T, batch, I] fp32; W [D, I, 4H], R [D, H, 4H]
+    int8; scales [D] or [D, 4H]; B [D, 8H]; h0, c0 [D, batch, H];
+    outputs Y [T, D, batch, H], Y_h, Y_c [D, batch, H] (each optional)."""
+    T, batch, I = X.shape
+    H = R.shape[1]
+    check(_L().i8q_dq_lstm_forward(
+        _dev(X, "X", torch.float32), T, batch, I, H, direction, _dev(W, "W", torch.int8),
+        _dev(W_scale, "W_scale", torch.float32), _dev(W_zero_point, "W_zero_point"), W_scale.numel(),
+        _dev(R, "R", torch.int8), _dev(R_scale, "R_scale", torch.float32), _dev(R_zero_point, "R_zero_point"),
+        R_scale.numel(), _dev(B, "B", torch.float32), _dev(h0, "h0", torch.float32), _dev(c0, "c0", torch.float32),
+        _dev(Y, "Y", torch.float32), _dev(Y_h, "Y_h", torch.float32), _dev(Y_c, "Y_c", torch.float32),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "dq_lstm_forward")
+    return Y, Y_h, Y_c

@@ -1,0 +1,146 @@
+// common.cuh -- shared helpers of libi8q (CUDA side only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <string>
+#include <type_traits>
+
+#include "../../include/i8q.h"
+
+namespace i8q {
+
+// ---- error reporting (thread-local text, see i8q_last_error) -------------
+void set_error(const std::string& msg);
+int fail(int code, const std::string& msg);
+int cuda_fail(cudaError_t e, const char* what);
+
+#define I8Q_CUDA_TRY(expr)                                   \
+  do {                                                       \
+    cudaError_t e_ = (expr);                                 \
+    if (e_ != cudaSuccess) return ::i8q::cuda_fail(e_, #expr); \
+  } while (0)
+
+#define I8Q_LAUNCH_CHECK(what)                               \
+  do {                                                       \
+    cudaError_t e_ = cudaGetLastError();                     \
+    if (e_ != cudaSuccess) return ::i8q::cuda_fail(e_, what); \
+  } while (0)
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// Streaming-multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// Device-side status word for bounded waits (see i8q_sync_status).
+uint32_t* device_status_word();
+
+// Kernel timing (i8q_profile_*): while enabled, a ProfScope brackets the
+// launches made in its lifetime with CUDA events on the launch stream.
+bool profiling_enabled();
+void profile_record(const char* name, cudaStream_t s, bool begin);
+struct ProfScope {
+  const char* name;
+  cudaStream_t s;
+  bool on;
+  ProfScope(const char* n, cudaStream_t st) : name(n), s(st), on(profiling_enabled()) {
+    if (on) profile_record(name, s, true);
+  }
+  ~ProfScope() {
+    if (on) profile_record(name, s, false);
+  }
+};
+#define I8Q_PROF(name, stream) ::i8q::ProfScope i8q_prof_scope_(name, stream)
+
+// ---- exact fp32 helpers (no contraction into FMA) ------------------------
+// rint(v) saturated to [lo, hi] then cast; lo/hi already include the zero
+// point shift so the comparison happens on exactly representable values.
+__device__ __forceinline__ int sat_rint(float v, float lo, float hi) {
+  float r = rintf(v);
+  r = fminf(fmaxf(r, lo), hi);
+  return __float2int_rz(r);
+}
+
+// GELU = x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt 2)), evaluated as
+// (0.5 * x) * erfc(-(x / sqrt 2)) so nothing cancels for negative x.
+__device__ __forceinline__ float gelu_erf(float x) {
+  float t = __fmul_rn(x, 0.70710678118654752440f);
+  float e = erfcf(-t);
+  float h = __fmul_rn(0.5f, x);
+  return __fmul_rn(h, e);
+}
+
+__device__ __forceinline__ float activate(float v, int act) {
+  if (act == I8Q_ACT_RELU) return v > 0.0f ? v : 0.0f;
+  if (act == I8Q_ACT_GELU) return gelu_erf(v);
+  return v;
+}
+
+// Epilogue of the dynamic quantized inner product for one element:
+//   ((float)sum * scaleA) * scaleB + bias, activation.
+__device__ __forceinline__ float dequant_epilogue(int32_t sum, float sA, float sB, float b, int act) {
+  float v = __int2float_rn(sum);
+  v = __fmul_rn(v, sA);
+  v = __fmul_rn(v, sB);
+  v = __fadd_rn(v, b);
+  return activate(v, act);
+}
+
+// ---- internal kernel launchers (implemented in the .cu files) ------------
+
+// Row quantization of A (M x K, fp32 or bf16, row stride lda elements) into
+// uA (M x Kp uint8, zero padded), optional uA_bf16 (M x Kp bf16 holding the
+// uint8 codes), scaleA[M], zeroA[M].
+int launch_quantize_rows(const void* A, int typeA, int64_t M, int64_t K, int64_t lda, uint8_t* uA,
+                         __nv_bfloat16* uA_bf16, int64_t Kp, float* scaleA, int32_t* zeroA,
+                         cudaStream_t s);
+
+// Column quantization of B (K x N fp32/bf16 row-major) into iBt (N x Kp
+// int8, transposed, zero padded), optional iBt_bf16, scaleB[N], colsum[N].
+int launch_quantize_cols(const void* B, int typeB, int64_t K, int64_t N, int avoid_overflow,
+                         int8_t* iBt, __nv_bfloat16* iBt_bf16, int64_t Kp, float* scaleB,
+                         int32_t* colsum, cudaStream_t s);
+
+// Repack a given int8 B (K x N row-major, row stride ldb) into iBt
+// (N x Kp), optional iBt_bf16, and colsum[N].
+int launch_repack_cols_s8(const int8_t* B, int64_t K, int64_t N, int64_t ldb, int8_t* iBt,
+                          __nv_bfloat16* iBt_bf16, int64_t Kp, int32_t* colsum, cudaStream_t s);
+
+// Output modes of the GEMM epilogue.
+enum OutMode : int {
+  OUT_F32 = 0,   // dequantized fp32
+  OUT_BF16 = 1,  // dequantized bf16
+  OUT_S32 = 2,   // raw corrected int32 sums
+};
+
+struct GemmEpilogue {
+  const int32_t* zeroA;   // [M]
+  const float* scaleA;    // [M]
+  const int32_t* colsum;  // [N]
+  const float* scaleB;    // [N]
+  const float* bias;      // [N] or null
+  int act;
+  int out_mode;
+  void* C;
+  int64_t ldc;            // elements
+};
+
+// Integer GEMM core: sum_k uA[i,k] * iBt[j,k] (uint8 x int8), corrected by
+// -zeroA[i]*colsum[j], then the epilogue.  uA is M x Kp (row stride Kp),
+// iBt is N x Kp, Kp a multiple of 64 with zero padding beyond K.
+int launch_gemm_imma(const uint8_t* uA, const int8_t* iBt, int64_t M, int64_t N, int64_t Kp,
+                     const GemmEpilogue& ep, cudaStream_t s);
+
+// Exact-integer GEMM on the bf16 tensor pipe (tcgen05), same contract as
+// launch_gemm_imma but reading the bf16 copies of uA and iBt.  Returns
+// I8Q_ERR_UNSUPPORTED when the shape is outside what it handles.
+int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M, int64_t N,
+                   int64_t Kp, int max_abs_product_log2, const GemmEpilogue& ep, cudaStream_t s);
+
+}  // namespace i8q

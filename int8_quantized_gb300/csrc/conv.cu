@@ -1,0 +1,164 @@
+// conv.cu -- QLinearConv (onnx-light docs, "QLinearConv", since version 10),
+// 2-D NCHW.
+//
+//   acc = sum_{c in group, kh, kw} (x - x_zero_point) * (w - w_zero_point[m])
+//   acc += B[m]                       (int32 bias: scale x_scale*w_scale, zp 0)
+//   y   = saturate(rint(((float)acc * (x_scale * w_scale[m])) / y_scale) + y_zero_point)
+// A position outside the input holds real 0 (the code x_zero_point), so it
+// adds nothing.  The requantization is DequantizeLinear of the accumulator
+// followed by QuantizeLinear with (y_scale, y_zero_point).
+//
+// This file holds the direct form used for every group count: one thread
+// per output pixel, the centered filter of the CTA's output channel staged
+// in shared memory, exact int32 accumulation.
+#include "common.cuh"
+
+namespace i8q {
+namespace {
+
+template <typename XT, typename WT, typename YT>
+__global__ void __launch_bounds__(256)
+qlinearconv_direct(const XT* __restrict__ x, const WT* __restrict__ w, const float* __restrict__ w_scale,
+                   const WT* __restrict__ w_zp, int per_channel, const int32_t* __restrict__ B, int C, int H,
+                   int W, int M, int Cg, int Mg, int kH, int kW, int OH, int OW, int pt, int pl, int sh, int sw,
+                   int dh, int dw, float x_scale, int x_zp, float y_scale, int y_zp, float qlo, float qhi,
+                   YT* __restrict__ y) {
+  extern __shared__ int wc[];  // centered filter of channel m: Cg * kH * kW
+  const int m = blockIdx.y, n = blockIdx.z;
+  const int taps = Cg * kH * kW;
+  const int wz = (int)w_zp[per_channel ? m : 0];
+  for (int i = threadIdx.x; i < taps; i += blockDim.x) wc[i] = (int)w[(int64_t)m * taps + i] - wz;
+  __syncthreads();
+  const int g = m / Mg;
+  const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= (int64_t)OH * OW) return;
+  const int oh = (int)(p / OW), ow = (int)(p % OW);
+  const XT* xb = x + ((int64_t)n * C + (int64_t)g * Cg) * H * W;
+  int32_t acc = 0;
+  for (int cc = 0; cc < Cg; ++cc) {
+    const XT* xc = xb + (int64_t)cc * H * W;
+    const int* wcc = wc + cc * kH * kW;
+    for (int kh = 0; kh < kH; ++kh) {
+      const int ih = oh * sh - pt + kh * dh;
+      if (ih < 0 || ih >= H) continue;
+      for (int kw = 0; kw < kW; ++kw) {
+        const int iw = ow * sw - pl + kw * dw;
+        if (iw < 0 || iw >= W) continue;
+        acc += ((int)xc[(int64_t)ih * W + iw] - x_zp) * wcc[kh * kW + kw];
+      }
+    }
+  }
+  if (B) acc += B[m];
+  float v = __int2float_rn(acc);
+  const float mul = __fmul_rn(x_scale, w_scale[per_channel ? m : 0]);
+  v = __fmul_rn(v, mul);
+  v = __fdiv_rn(v, y_scale);
+  y[(((int64_t)n * M + m) * OH + oh) * OW + ow] = (YT)(sat_rint(v, qlo - (float)y_zp, qhi - (float)y_zp) + y_zp);
+}
+
+struct ConvShape {
+  int64_t N, C, H, W, M, Cg, kH, kW, OH, OW;
+  int64_t pt, pl, pb, pr, sh, sw, dh, dw, group;
+};
+
+int conv_shape(const int64_t* xs, const int64_t* ws, const int64_t* pads, const int64_t* strides,
+               const int64_t* dil, int64_t group, ConvShape* s) {
+  if (!xs || !ws) return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: NULL shape");
+  s->N = xs[0]; s->C = xs[1]; s->H = xs[2]; s->W = xs[3];
+  s->M = ws[0]; s->Cg = ws[1]; s->kH = ws[2]; s->kW = ws[3];
+  s->pt = pads ? pads[0] : 0; s->pl = pads ? pads[1] : 0;
+  s->pb = pads ? pads[2] : 0; s->pr = pads ? pads[3] : 0;
+  s->sh = strides ? strides[0] : 1; s->sw = strides ? strides[1] : 1;
+  s->dh = dil ? dil[0] : 1; s->dw = dil ? dil[1] : 1;
+  s->group = group;
+  for (int i = 0; i < 4; ++i)
+    if (xs[i] <= 0 || ws[i] <= 0) return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: dimensions must be positive");
+  if (s->pt < 0 || s->pl < 0 || s->pb < 0 || s->pr < 0) return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: negative pad");
+  if (s->sh < 1 || s->sw < 1 || s->dh < 1 || s->dw < 1)
+    return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: strides and dilations must be >= 1");
+  if (group < 1 || s->C != s->Cg * group || s->M % group != 0)
+    return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: need x.shape[1] == w.shape[1] * group and M % group == 0");
+  s->OH = (s->H + s->pt + s->pb - ((s->kH - 1) * s->dh + 1)) / s->sh + 1;
+  s->OW = (s->W + s->pl + s->pr - ((s->kW - 1) * s->dw + 1)) / s->sw + 1;
+  if (s->OH <= 0 || s->OW <= 0) return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: empty output");
+  // every |(x - xz)(w - wz)| <= 255*255; keep the int32 sum exact
+  if (s->Cg * s->kH * s->kW > 33025) return fail(I8Q_ERR_UNSUPPORTED, "qlinearconv: C/group*kH*kW > 33025");
+  if (s->M > 65535 || s->N > 65535) return fail(I8Q_ERR_UNSUPPORTED, "qlinearconv: M or N > 65535");
+  if (s->OH * s->OW > (int64_t)1 << 31) return fail(I8Q_ERR_UNSUPPORTED, "qlinearconv: output plane too large");
+  return I8Q_OK;
+}
+
+template <typename XT, typename WT, typename YT>
+int run_direct(const ConvShape& s, const void* x, float x_scale, int x_zp, const void* w, const float* w_scale,
+               const void* w_zp, int per_ch, float y_scale, int y_zp, const int32_t* B, void* y, cudaStream_t st) {
+  const int64_t taps = s.Cg * s.kH * s.kW;
+  const size_t smem = (size_t)taps * sizeof(int);
+  if (smem > 200 * 1024) return fail(I8Q_ERR_UNSUPPORTED, "qlinearconv: filter too large for shared memory");
+  auto kern = qlinearconv_direct<XT, WT, YT>;
+  if (smem > 48 * 1024) I8Q_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  const float qlo = std::is_same<YT, uint8_t>::value ? 0.0f : -128.0f;
+  const float qhi = std::is_same<YT, uint8_t>::value ? 255.0f : 127.0f;
+  dim3 grid((unsigned)ceil_div(s.OH * s.OW, 256), (unsigned)s.M, (unsigned)s.N);
+  I8Q_PROF(s.group == s.C && s.Cg == 1 ? "qlinearconv_depthwise" : "qlinearconv_direct", st);
+  kern<<<grid, 256, smem, st>>>((const XT*)x, (const WT*)w, w_scale, (const WT*)w_zp, per_ch, B, (int)s.C, (int)s.H,
+                                (int)s.W, (int)s.M, (int)s.Cg, (int)(s.M / s.group), (int)s.kH, (int)s.kW, (int)s.OH,
+                                (int)s.OW, (int)s.pt, (int)s.pl, (int)s.sh, (int)s.sw, (int)s.dh, (int)s.dw, x_scale,
+                                x_zp, y_scale, y_zp, qlo, qhi, (YT*)y);
+  I8Q_LAUNCH_CHECK("qlinearconv_direct");
+  return I8Q_OK;
+}
+
+template <typename XT, typename WT>
+int dispatch_y(int ytype, const ConvShape& s, const void* x, float xs, int xz, const void* w, const float* ws,
+               const void* wz, int pc, float ys, int yz, const int32_t* B, void* y, cudaStream_t st) {
+  if (ytype == I8Q_U8) return run_direct<XT, WT, uint8_t>(s, x, xs, xz, w, ws, wz, pc, ys, yz, B, y, st);
+  return run_direct<XT, WT, int8_t>(s, x, xs, xz, w, ws, wz, pc, ys, yz, B, y, st);
+}
+
+}  // namespace
+}  // namespace i8q
+
+using namespace i8q;
+
+extern "C" size_t i8q_qlinearconv_workspace_size(const int64_t* xshape, const int64_t* wshape, const int64_t* pads,
+                                                 const int64_t* strides, const int64_t* dilations, int64_t group) {
+  ConvShape s;
+  if (conv_shape(xshape, wshape, pads, strides, dilations, group, &s) != I8Q_OK) return 0;
+  return 0;
+}
+
+extern "C" int i8q_qlinearconv(const void* x, int xtype, const int64_t* xshape, float x_scale, int x_zero_point,
+                               const void* w, int wtype, const int64_t* wshape, const float* w_scale,
+                               const void* w_zero_point, size_t n_w, float y_scale, int y_zero_point,
+                               const int32_t* B, const int64_t* pads, const int64_t* strides,
+                               const int64_t* dilations, int64_t group, void* y, int ytype, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  ConvShape s;
+  int rc = conv_shape(xshape, wshape, pads, strides, dilations, group, &s);
+  if (rc) return rc;
+  auto is8 = [](int t) { return t == I8Q_U8 || t == I8Q_S8; };
+  if (!is8(xtype) || !is8(wtype) || !is8(ytype)) return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: types must be U8 or S8");
+  if (!x || !w || !y || !w_scale || !w_zero_point) return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: NULL tensor pointer");
+  if (n_w != 1 && (int64_t)n_w != s.M)
+    return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: w_scale / w_zero_point must have 1 or M entries");
+  const int xlo = xtype == I8Q_U8 ? 0 : -128, xhi = xtype == I8Q_U8 ? 255 : 127;
+  const int ylo = ytype == I8Q_U8 ? 0 : -128, yhi = ytype == I8Q_U8 ? 255 : 127;
+  if (x_zero_point < xlo || x_zero_point > xhi || y_zero_point < ylo || y_zero_point > yhi)
+    return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: zero point outside its type's range");
+  if (!(x_scale > 0.0f) || !(y_scale > 0.0f)) return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: scales must be > 0");
+  const int pc = n_w != 1;
+  cudaStream_t st = as_stream(stream);
+  if (xtype == I8Q_U8 && wtype == I8Q_U8)
+    return dispatch_y<uint8_t, uint8_t>(ytype, s, x, x_scale, x_zero_point, w, w_scale, w_zero_point, pc, y_scale,
+                                        y_zero_point, B, y, st);
+  if (xtype == I8Q_U8)
+    return dispatch_y<uint8_t, int8_t>(ytype, s, x, x_scale, x_zero_point, w, w_scale, w_zero_point, pc, y_scale,
+                                       y_zero_point, B, y, st);
+  if (wtype == I8Q_U8)
+    return dispatch_y<int8_t, uint8_t>(ytype, s, x, x_scale, x_zero_point, w, w_scale, w_zero_point, pc, y_scale,
+                                       y_zero_point, B, y, st);
+  return dispatch_y<int8_t, int8_t>(ytype, s, x, x_scale, x_zero_point, w, w_scale, w_zero_point, pc, y_scale,
+                                    y_zero_point, B, y, st);
+}

@@ -1,0 +1,300 @@
+// quant_rows.cu -- operand preparation of the dynamic quantized inner
+// product (Simd "SynetDynamicQuantizedInnerProduct16b", Detailed
+// Description: "A[i,k] -> uA[i,k], scaleA[i], zeroA[i]" and
+// "B[k,j] -> iB[k,j], scaleB[j]").
+//
+// Row quantization of A (uint8, per row, range widened to contain 0):
+//   mn = min(0, min_k A), mx = max(0, max_k A), scale = (mx - mn) / 255,
+//   zero = sat_u8(rint(-mn / scale)), uA = sat_u8(rint(A / scale) + zero)
+//   (an all-zero row takes scale 1, zero 0).
+// Column quantization of B (int8, symmetric, per column):
+//   scale = max_k |B| / qmax (qmax 127, or 63 with avoidOverflow),
+//   iB = saturate(rint(B / scale)) to [-128,127] / [-64,63]
+//   (an all-zero column takes scale 1).
+// Both write the operand layouts the GEMM cores read: uA as M x Kp and B
+// transposed to N x Kp (K contiguous), zero padded to Kp, plus optional bf16
+// copies of the same integer codes for the tensor-core path, and the column
+// sums of iB used by the zero-point correction  -zeroA[i] * colsum[j].
+#include "common.cuh"
+
+namespace i8q {
+namespace {
+
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// Load 8 consecutive elements as fp32 (16-byte aligned vector loads).
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+  uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    v[2 * q] = __uint_as_float(w[q] << 16);
+    v[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+  }
+}
+
+// bf16 bit pattern of a small non-negative or negative integer code (exact).
+__device__ __forceinline__ uint32_t code_bf16_bits(int c) {
+  return (uint32_t)__bfloat16_as_ushort(__int2bfloat16_rn(c));
+}
+
+// One CTA per row (grid-stride over rows).  VEC: 8 elements per access.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kRowThreads)
+quantize_rows_kernel(const T* __restrict__ A, int64_t M, int64_t K, int64_t lda, uint8_t* __restrict__ uA,
+                     __nv_bfloat16* __restrict__ uA_bf16, int64_t Kp, float* __restrict__ scaleA,
+                     int32_t* __restrict__ zeroA) {
+  __shared__ float red_mn[kRowThreads / 32], red_mx[kRowThreads / 32];
+  __shared__ float sh_scale;
+  __shared__ int sh_zero;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    const T* a = A + row * lda;
+    float mn = 0.0f, mx = 0.0f;
+    if (VEC) {
+      for (int64_t k = (int64_t)tid * 8; k < K; k += kRowThreads * 8) {
+        float v[8];
+        load8(a + k, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          mn = fminf(mn, v[q]);
+          mx = fmaxf(mx, v[q]);
+        }
+      }
+    } else {
+      for (int64_t k = tid; k < K; k += kRowThreads) {
+        float v = to_f32<T>(a[k]);
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+      }
+    }
+    mn = warp_min(mn);
+    mx = warp_max(mx);
+    if (lane == 0) {
+      red_mn[warp] = mn;
+      red_mx[warp] = mx;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float m0 = red_mn[0], m1 = red_mx[0];
+      for (int w = 1; w < kRowThreads / 32; ++w) {
+        m0 = fminf(m0, red_mn[w]);
+        m1 = fmaxf(m1, red_mx[w]);
+      }
+      float s = __fdiv_rn(__fsub_rn(m1, m0), 255.0f);
+      int z = 0;
+      if (s == 0.0f) {
+        s = 1.0f;
+      } else {
+        z = sat_rint(__fdiv_rn(-m0, s), 0.0f, 255.0f);
+      }
+      sh_scale = s;
+      sh_zero = z;
+      scaleA[row] = s;
+      zeroA[row] = z;
+    }
+    __syncthreads();
+    const float s = sh_scale;
+    const int z = sh_zero;
+    const float lo = (float)(-z), hi = (float)(255 - z);
+    uint8_t* u = uA + row * Kp;
+    __nv_bfloat16* ub = uA_bf16 ? uA_bf16 + row * Kp : nullptr;
+    // Kp is a multiple of 64, so 8-wide chunks tile it exactly.
+    for (int64_t k = (int64_t)tid * 8; k < Kp; k += kRowThreads * 8) {
+      int code[8];
+      if (VEC && k + 8 <= K) {
+        float v[8];
+        load8(a + k, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) code[q] = sat_rint(__fdiv_rn(v[q], s), lo, hi) + z;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          code[q] = (k + q < K) ? sat_rint(__fdiv_rn(to_f32<T>(a[k + q]), s), lo, hi) + z : 0;
+      }
+      uint32_t lo4 = 0, hi4 = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        lo4 |= (uint32_t)code[q] << (8 * q);
+        hi4 |= (uint32_t)code[q + 4] << (8 * q);
+      }
+      *reinterpret_cast<uint2*>(u + k) = make_uint2(lo4, hi4);
+      if (ub) {
+        uint4 o;
+        o.x = code_bf16_bits(code[0]) | (code_bf16_bits(code[1]) << 16);
+        o.y = code_bf16_bits(code[2]) | (code_bf16_bits(code[3]) << 16);
+        o.z = code_bf16_bits(code[4]) | (code_bf16_bits(code[5]) << 16);
+        o.w = code_bf16_bits(code[6]) | (code_bf16_bits(code[7]) << 16);
+        *reinterpret_cast<uint4*>(ub + k) = o;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---- columns -------------------------------------------------------------
+// A CTA owns 32 columns [j0, j0+32) and walks all of K twice: once for the
+// max-abs per column, once to quantize, transposing 64 x 32 tiles through
+// shared memory so the N x Kp output is written with contiguous K.
+constexpr int kColW = 32;
+constexpr int kColKT = 64;
+
+template <typename T, int MODE>  // MODE 0: quantize fp32/bf16 B; 1: repack int8 B
+__global__ void __launch_bounds__(256)
+cols_kernel(const T* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int qmin, int qmax,
+            int8_t* __restrict__ iBt, __nv_bfloat16* __restrict__ iBt_bf16, int64_t Kp,
+            float* __restrict__ scaleB, int32_t* __restrict__ colsum) {
+  __shared__ float red[8][kColW];
+  __shared__ float sh_scale[kColW];
+  __shared__ int sh_sum[8][kColW];
+  __shared__ int8_t tile[kColW][kColKT + 16];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t j0 = (int64_t)blockIdx.x * kColW;
+  const int64_t j = j0 + lane;
+  const bool jok = j < N;
+  if constexpr (MODE == 0) {
+    float m = 0.0f;
+    if (jok)
+      for (int64_t k = warp; k < K; k += 8) m = fmaxf(m, fabsf(to_f32<T>(B[k * ldb + j])));
+    red[warp][lane] = m;
+    __syncthreads();
+    if (warp == 0) {
+      float mm = red[0][lane];
+      for (int w = 1; w < 8; ++w) mm = fmaxf(mm, red[w][lane]);
+      float s = __fdiv_rn(mm, (float)qmax);
+      if (s == 0.0f) s = 1.0f;
+      sh_scale[lane] = s;
+      if (jok) scaleB[j] = s;
+    }
+    __syncthreads();
+  }
+  const float s = MODE == 0 ? sh_scale[lane] : 1.0f;
+  int sum = 0;
+  for (int64_t k0 = 0; k0 < Kp; k0 += kColKT) {
+    // each warp quantizes rows k0 + warp + 8*r of the 32 columns
+#pragma unroll
+    for (int r = 0; r < kColKT / 8; ++r) {
+      const int kk = warp + 8 * r;
+      const int64_t k = k0 + kk;
+      int code = 0;
+      if (jok && k < K) {
+        if constexpr (MODE == 0)
+          code = sat_rint(__fdiv_rn(to_f32<T>(B[k * ldb + j]), s), (float)qmin, (float)qmax);
+        else
+          code = (int)(int8_t)B[k * ldb + j];
+      }
+      sum += code;
+      tile[lane][kk] = (int8_t)code;
+    }
+    __syncthreads();
+    // write the 32 x 64 tile: thread -> (column c, 8-byte segment)
+    const int c = tid >> 3, seg = tid & 7;
+    const int64_t jj = j0 + c;
+    if (jj < N) {
+      const int8_t* src = &tile[c][seg * 8];
+      uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        w0 |= (uint32_t)(uint8_t)src[q] << (8 * q);
+        w1 |= (uint32_t)(uint8_t)src[q + 4] << (8 * q);
+      }
+      *reinterpret_cast<uint2*>(iBt + jj * Kp + k0 + seg * 8) = make_uint2(w0, w1);
+      if (iBt_bf16) {
+        uint4 o;
+        o.x = code_bf16_bits(src[0]) | (code_bf16_bits(src[1]) << 16);
+        o.y = code_bf16_bits(src[2]) | (code_bf16_bits(src[3]) << 16);
+        o.z = code_bf16_bits(src[4]) | (code_bf16_bits(src[5]) << 16);
+        o.w = code_bf16_bits(src[6]) | (code_bf16_bits(src[7]) << 16);
+        *reinterpret_cast<uint4*>(iBt_bf16 + jj * Kp + k0 + seg * 8) = o;
+      }
+    }
+    __syncthreads();
+  }
+  sh_sum[warp][lane] = sum;
+  __syncthreads();
+  if (warp == 0 && jok) {
+    int t = 0;
+    for (int w = 0; w < 8; ++w) t += sh_sum[w][lane];
+    colsum[j] = t;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int launch_quantize_rows(const void* A, int typeA, int64_t M, int64_t K, int64_t lda, uint8_t* uA,
+                         __nv_bfloat16* uA_bf16, int64_t Kp, float* scaleA, int32_t* zeroA, cudaStream_t s) {
+  if (M <= 0) return I8Q_OK;
+  int64_t blocks = std::min<int64_t>(M, (int64_t)sm_count() * 8);
+  I8Q_PROF("quantize_rows", s);
+  if (typeA == I8Q_F32) {
+    const float* a = static_cast<const float*>(A);
+    bool vec = aligned16(a) && K % 8 == 0 && lda % 4 == 0;
+    if (vec)
+      quantize_rows_kernel<float, true><<<blocks, kRowThreads, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA);
+    else
+      quantize_rows_kernel<float, false><<<blocks, kRowThreads, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA);
+  } else {
+    const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(A);
+    bool vec = aligned16(a) && K % 8 == 0 && lda % 8 == 0;
+    if (vec)
+      quantize_rows_kernel<__nv_bfloat16, true><<<blocks, kRowThreads, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA);
+    else
+      quantize_rows_kernel<__nv_bfloat16, false><<<blocks, kRowThreads, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA);
+  }
+  I8Q_LAUNCH_CHECK("quantize_rows_kernel");
+  return I8Q_OK;
+}
+
+int launch_quantize_cols(const void* B, int typeB, int64_t K, int64_t N, int avoid_overflow, int8_t* iBt,
+                         __nv_bfloat16* iBt_bf16, int64_t Kp, float* scaleB, int32_t* colsum, cudaStream_t s) {
+  if (N <= 0) return I8Q_OK;
+  const int qmax = avoid_overflow ? 63 : 127, qmin = avoid_overflow ? -64 : -128;
+  I8Q_PROF("quantize_cols", s);
+  dim3 grid((unsigned)ceil_div(N, kColW));
+  if (typeB == I8Q_F32)
+    cols_kernel<float, 0><<<grid, 256, 0, s>>>(static_cast<const float*>(B), K, N, N, qmin, qmax, iBt, iBt_bf16, Kp,
+                                               scaleB, colsum);
+  else
+    cols_kernel<__nv_bfloat16, 0><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(B), K, N, N, qmin, qmax,
+                                                       iBt, iBt_bf16, Kp, scaleB, colsum);
+  I8Q_LAUNCH_CHECK("cols_kernel(quantize)");
+  return I8Q_OK;
+}
+
+int launch_repack_cols_s8(const int8_t* B, int64_t K, int64_t N, int64_t ldb, int8_t* iBt, __nv_bfloat16* iBt_bf16,
+                          int64_t Kp, int32_t* colsum, cudaStream_t s) {
+  if (N <= 0) return I8Q_OK;
+  dim3 grid((unsigned)ceil_div(N, kColW));
+  I8Q_PROF("repack_cols", s);
+    cols_kernel<int8_t, 1><<<grid, 256, 0, s>>>(B, K, N, ldb, -128, 127, iBt, iBt_bf16, Kp, nullptr, colsum);
+  I8Q_LAUNCH_CHECK("cols_kernel(repack)");
+  return I8Q_OK;
+}
+
+}  // namespace i8q

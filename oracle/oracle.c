@@ -182,13 +182,15 @@ int or_quantize_cols_s8(const float* B, int64_t K, int64_t N, int avoid_overflow
   return OR_OK;
 }
 
-/* GELU with the error function, in fp32: 0.5 * x * (1 + erf(x / sqrt(2))).
- * Evaluated as (0.5 * x) * (1 + erff(x * (1/sqrt(2)))). */
+/* GELU, x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt(2))), in fp32.  Evaluated
+ * as (0.5 * x) * erfc(-(x * (1/sqrt(2)))): the same function, written with
+ * the complementary error function so that no 1 + erf(.) cancels for
+ * negative x. */
 static float gelu_f32(float x) {
   float t = x * 0.70710678118654752440f;
-  float e = erff(t);
+  float e = erfcf(-t);
   float h = 0.5f * x;
-  return h * (1.0f + e);
+  return h * e;
 }
 
 static float activate(float v, int act) {

@@ -1,0 +1,123 @@
+"""The C ABI library without a GPU: it loads, exports every entry point the
+header declares, and rejects bad arguments on the host before launching
+anything (these calls reach no CUDA API)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "i8q.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int8_quantized_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(i8q_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ["i8q_qgemm_dyn_init", "i8q_qgemm_dyn_set_params", "i8q_qgemm_dyn_forward", "i8q_quantize_linear",
+                 "i8q_dequantize_linear", "i8q_qlinearconv", "i8q_dq_lstm_forward"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from int8_quantized_gb300 import _lib
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in i8q.h but not exported"
+        assert name in _lib.SIGNATURES, f"{name} has no ctypes signature in the binding"
+
+
+def test_version(lib):
+    assert b"sm_103a" in lib.i8q_version()
+
+
+def _arr(vals, t=ctypes.c_int64):
+    return (t * len(vals))(*vals)
+
+
+def test_quantize_rejects_bad_axis_and_rank(lib):
+    from int8_quantized_gb300 import _lib
+    shape = _arr([2, 3, 4])
+    rc = lib.i8q_quantize_linear(ctypes.c_void_p(16), shape, 3, 3, ctypes.c_void_p(16), ctypes.c_void_p(16), 4,
+                                 _lib.U8, ctypes.c_void_p(16), None)
+    assert rc == _lib.ERR_INVALID_ARG and b"axis" in lib.i8q_last_error()
+    rc = lib.i8q_quantize_linear(ctypes.c_void_p(16), shape, 9, 0, None, None, 1, _lib.U8, None, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"rank" in lib.i8q_last_error()
+    # per-axis length must equal dim[axis]
+    rc = lib.i8q_quantize_linear(ctypes.c_void_p(16), shape, 3, 1, ctypes.c_void_p(16), ctypes.c_void_p(16), 4,
+                                 _lib.U8, ctypes.c_void_p(16), None)
+    assert rc == _lib.ERR_INVALID_ARG and b"dim[axis]" in lib.i8q_last_error()
+    # per-tensor needs scalars
+    rc = lib.i8q_quantize_linear(ctypes.c_void_p(16), shape, 3, _lib.NO_AXIS, ctypes.c_void_p(16),
+                                 ctypes.c_void_p(16), 3, _lib.U8, ctypes.c_void_p(16), None)
+    assert rc == _lib.ERR_INVALID_ARG and b"scalars" in lib.i8q_last_error()
+    rc = lib.i8q_dequantize_linear(ctypes.c_void_p(16), _lib.F32, shape, 3, _lib.NO_AXIS, ctypes.c_void_p(16),
+                                   ctypes.c_void_p(16), 1, ctypes.c_void_p(16), None)
+    assert rc == _lib.ERR_INVALID_ARG
+
+
+def test_qgemm_init_validation(lib):
+    from int8_quantized_gb300 import _lib
+    ctx = ctypes.c_void_p(None)
+    assert lib.i8q_qgemm_dyn_init(ctypes.byref(ctx), 0, 8, 8, 0, 0, 0, 1, 1, 0, 0) == _lib.ERR_INVALID_ARG
+    assert lib.i8q_qgemm_dyn_init(ctypes.byref(ctx), 4, 8, 70000, 0, 0, 0, 1, 1, 0, 0) == _lib.ERR_UNSUPPORTED
+    # int8 B only when constant
+    assert lib.i8q_qgemm_dyn_init(ctypes.byref(ctx), 4, 8, 16, _lib.F32, _lib.S8, _lib.F32, 0, 1, 0, 0) == \
+        _lib.ERR_INVALID_ARG
+    assert lib.i8q_qgemm_dyn_init(ctypes.byref(ctx), 4, 8, 16, _lib.S8, _lib.F32, _lib.F32, 1, 1, 0, 0) == \
+        _lib.ERR_INVALID_ARG
+    assert lib.i8q_qgemm_dyn_init(ctypes.byref(ctx), 4, 8, 16, _lib.F32, _lib.F32, _lib.F32, 1, 1, 9, 0) == \
+        _lib.ERR_UNSUPPORTED
+    assert ctx.value is None
+    assert lib.i8q_qgemm_dyn_enabled(None) == 0
+    assert lib.i8q_qgemm_dyn_info(None) is None
+    assert lib.i8q_qgemm_dyn_external_buffer_size(None) == 0
+    assert lib.i8q_qgemm_dyn_forward(None, None, None, None, None, None) == _lib.ERR_NOT_INITIALIZED
+    assert lib.i8q_qgemm_dyn_set_params(None, None, None, None, None, None) == _lib.ERR_NOT_INITIALIZED
+    lib.i8q_qgemm_dyn_clear(None)
+    lib.i8q_qgemm_dyn_clear(ctypes.byref(ctx))
+
+
+def test_qlinearconv_validation(lib):
+    from int8_quantized_gb300 import _lib
+    xs, ws = _arr([1, 4, 5, 5]), _arr([2, 3, 3, 3])  # C != w.shape[1] * group
+    pads, strides, dil = _arr([1, 1, 1, 1]), _arr([1, 1]), _arr([1, 1])
+    assert lib.i8q_qlinearconv_workspace_size(xs, ws, pads, strides, dil, 1) == 0
+    rc = lib.i8q_qlinearconv(ctypes.c_void_p(16), _lib.U8, xs, 0.1, 0, ctypes.c_void_p(16), _lib.U8, ws,
+                             ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 0.1, 0, None, pads, strides, dil, 1,
+                             ctypes.c_void_p(16), _lib.U8, None, 0, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"group" in lib.i8q_last_error()
+    ws2 = _arr([2, 4, 3, 3])
+    rc = lib.i8q_qlinearconv(ctypes.c_void_p(16), _lib.U8, xs, 0.1, 300, ctypes.c_void_p(16), _lib.U8, ws2,
+                             ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 0.1, 0, None, pads, strides, dil, 1,
+                             ctypes.c_void_p(16), _lib.U8, None, 0, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"zero point" in lib.i8q_last_error()
+    rc = lib.i8q_qlinearconv(ctypes.c_void_p(16), _lib.U8, xs, 0.1, 3, ctypes.c_void_p(16), _lib.U8, ws2,
+                             ctypes.c_void_p(16), ctypes.c_void_p(16), 3, 0.1, 0, None, pads, strides, dil, 1,
+                             ctypes.c_void_p(16), _lib.U8, None, 0, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"M entries" in lib.i8q_last_error()
+
+
+def test_lstm_validation(lib):
+    from int8_quantized_gb300 import _lib
+    assert lib.i8q_dq_lstm_workspace_size(0, 1, 1, 1, 0) == 0
+    assert lib.i8q_dq_lstm_workspace_size(2, 3, 8, 4, 2) > 0
+    p = ctypes.c_void_p(256)
+    rc = lib.i8q_dq_lstm_forward(p, 2, 3, 8, 4, 2, p, p, None, 3, p, p, None, 2, None, None, None, None, None, None,
+                                 p, 1 << 20, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"W_scale" in lib.i8q_last_error()
+    rc = lib.i8q_dq_lstm_forward(p, 2, 3, 8, 4, 2, p, p, None, 2, p, p, None, 2, None, None, None, None, None, None,
+                                 p, 16, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"workspace" in lib.i8q_last_error()

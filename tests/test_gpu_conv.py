@@ -1,0 +1,108 @@
+"""QLinearConv on the GPU vs the CPU oracle: output codes bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import int8_quantized_gb300 as q
+from conftest import read_golden
+from int8_quantized_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _t(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def run_conv(orc, dev, x, xs, xz, w, ws, wz, ys, yz, B=None, pads=(0, 0, 0, 0), strides=(1, 1), dil=(1, 1), group=1,
+             ytype=None):
+    ref = orc.qlinearconv(x, xs, xz, w, ws, wz, ys, yz, B, pads=pads, strides=strides, dilations=dil, group=group,
+                          ytype=ytype)
+    y = torch.empty(ref.shape, dtype=torch.uint8 if ref.dtype == np.uint8 else torch.int8, device=dev)
+    ws_bytes = q.qlinearconv_workspace_size(x.shape, w.shape, pads, strides, dil, group)
+    wsp = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
+    q.qlinearconv(_t(x, dev), float(xs), int(xz), _t(w, dev), _t(np.atleast_1d(ws).astype(np.float32), dev),
+                  _t(np.atleast_1d(wz).astype(w.dtype), dev), float(ys), int(yz), y,
+                  B=None if B is None else _t(B, dev), pads=pads, strides=strides, dilations=dil, group=group,
+                  workspace=wsp)
+    q.sync_status()
+    got = y.cpu().numpy()
+    assert np.array_equal(got, ref), f"{np.count_nonzero(got != ref)} of {ref.size} codes differ"
+    return got
+
+
+def test_printed_examples(orc, dev):
+    g = read_golden("qlinearconv_u8_7x7.txt")
+    x = np.array([int(v) for v in g["x"]], np.uint8).reshape(1, 1, 7, 7)
+    y = run_conv(orc, dev, x, np.float32(g["x_scale"][0]), int(g["x_zero_point"][0]), np.zeros((1, 1, 1, 1), np.uint8),
+                 np.float32(g["w_scale"][0]), int(g["w_zero_point"][0]), np.float32(g["y_scale"][0]),
+                 int(g["y_zero_point"][0]))
+    assert np.array_equal(y.reshape(-1), np.array([int(v) for v in g["y"]], np.uint8))
+    g = read_golden("qlinearconv_s8_2x2.txt")
+    x = np.array([int(v) for v in g["x"]], np.int8).reshape(1, 1, 2, 2)
+    y = run_conv(orc, dev, x, np.float32(g["x_scale"][0]), int(g["x_zero_point"][0]), np.ones((1, 1, 2, 2), np.int8),
+                 np.float32(1.0), 0, np.float32(1.0), -10)
+    assert int(y.reshape(-1)[0]) == -2
+
+
+CASES = [
+    # N, C, H, W, M, k, pads, strides, dil, group
+    (1, 3, 7, 5, 4, 3, (1, 1, 1, 1), (1, 1), (1, 1), 1),
+    (2, 8, 9, 11, 6, 3, (0, 0, 0, 0), (1, 1), (1, 1), 1),
+    (2, 8, 10, 9, 6, 3, (1, 2, 0, 1), (2, 1), (1, 1), 2),
+    (1, 6, 12, 12, 6, 3, (2, 2, 2, 2), (1, 1), (2, 2), 6),
+    (3, 16, 14, 13, 16, 3, (1, 1, 1, 1), (1, 1), (1, 1), 16),
+    (1, 4, 5, 5, 8, 1, (0, 0, 0, 0), (1, 1), (1, 1), 1),
+    (1, 5, 17, 3, 7, 5, (2, 2, 2, 2), (3, 2), (1, 1), 1),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("types", [("u8", "u8", "u8"), ("s8", "s8", "s8"), ("u8", "s8", "u8"), ("s8", "u8", "s8")])
+def test_shapes_and_types(orc, dev, case, types):
+    N, C, H, W, M, k, pads, strides, dil, group = case
+    rng = np.random.default_rng(N * 100 + C * 10 + M + k)
+    dt = {"u8": (np.uint8, 0, 256), "s8": (np.int8, -128, 128)}
+    xt, wt, yt = (dt[t] for t in types)
+    x = rng.integers(xt[1], xt[2], (N, C, H, W)).astype(xt[0])
+    w = rng.integers(wt[1], wt[2], (M, C // group, k, k)).astype(wt[0])
+    ws = rng.uniform(0.001, 0.01, M).astype(np.float32)
+    wz = rng.integers(wt[1], wt[2], M)
+    B = rng.integers(-5000, 5001, M).astype(np.int32)
+    run_conv(orc, dev, x, np.float32(0.0037), int(rng.integers(xt[1], xt[2])), w, ws, wz, np.float32(0.05),
+             int(rng.integers(yt[1], yt[2])), B, pads, strides, dil, group, ytype=types[2])
+    # per-tensor weight parameters, no bias
+    run_conv(orc, dev, x, np.float32(0.02), int(rng.integers(xt[1], xt[2])), w, np.float32(0.004),
+             int(rng.integers(wt[1], wt[2])), np.float32(0.3), int(rng.integers(yt[1], yt[2])), None, pads, strides,
+             dil, group, ytype=types[2])
+
+
+def test_full_size_dense_sampled(orc, dev):
+    """x [32,256,56,56], w [256,256,3,3]: the whole output on the GPU,
+    compared for 2 images x 24 output channels (each output depends only on
+    its image and its channel's filter)."""
+    c = workloads.qlinearconv(seed=3)
+    x, w = c["x"], c["w"]
+    ref_shape = (32, 256, 56, 56)
+    y = torch.empty(ref_shape, dtype=torch.uint8, device=dev)
+    ws_bytes = q.qlinearconv_workspace_size(x.shape, w.shape, c["pads"], (1, 1), (1, 1), 1)
+    wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    q.qlinearconv(_t(x, dev), float(c["x_scale"]), c["x_zero_point"], _t(w, dev), _t(c["w_scale"], dev),
+                  _t(c["w_zero_point"], dev), float(c["y_scale"]), c["y_zero_point"], y, B=_t(c["B"], dev),
+                  pads=c["pads"], workspace=wsp)
+    q.sync_status()
+    got = y.cpu().numpy()
+    rng = np.random.default_rng(0)
+    imgs = [0, 31]
+    chans = np.sort(rng.choice(256, 24, replace=False))
+    for n in imgs:
+        ref = orc.qlinearconv(x[n:n + 1], c["x_scale"], c["x_zero_point"], w[chans], c["w_scale"][chans],
+                              c["w_zero_point"][chans], c["y_scale"], c["y_zero_point"], c["B"][chans],
+                              pads=c["pads"])
+        assert np.array_equal(got[n][chans], ref[0])
+
+
+def test_full_size_depthwise(orc, dev):
+    c = workloads.qlinearconv(seed=3, depthwise=True)
+    run_conv(orc, dev, c["x"], c["x_scale"], c["x_zero_point"], c["w"], c["w_scale"], c["w_zero_point"],
+             c["y_scale"], c["y_zero_point"], c["B"], c["pads"], group=c["group"])

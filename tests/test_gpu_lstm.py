@@ -1,0 +1,127 @@
+"""DynamicQuantizeLSTM on the GPU vs the CPU oracle.
+
+The gates use the platform's expf/tanhf on each side, which may differ by an
+fp32 ulp; over many steps such differences can move a uint8 code of the
+next hidden state.  So parity is checked (1) step-locally: one step from a
+given (h, c) state, where the quantized codes, and so the int32 products,
+are the same on both sides and the outputs agree to within a few fp32 ulps,
+and (2) over short whole sequences within a small tolerance.  At the full
+size, sampled steps are checked step-locally: a GPU run over the first t
+inputs gives the state (h, c) that step t starts from.
+"""
+import numpy as np
+import pytest
+import torch
+
+import int8_quantized_gb300 as q
+from int8_quantized_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+DIRS = {"forward": q.LSTM_FORWARD, "reverse": q.LSTM_REVERSE, "bidirectional": q.LSTM_BIDIRECTIONAL}
+
+
+def _t(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def gpu_lstm(dev, w, direction, X=None, h0=None, c0=None, per_channel=True):
+    X = w["X"] if X is None else X
+    T, batch, I = X.shape
+    D = 2 if direction == "bidirectional" else 1
+    # the workload holds two directions: a reverse-only run uses the second
+    sel = slice(1, 2) if direction == "reverse" else slice(0, D)
+    H = w["R"].shape[1]
+    ws = torch.empty(q.dq_lstm_workspace_size(T, batch, I, H, DIRS[direction]), dtype=torch.uint8, device=dev)
+    Y = torch.empty(T, D, batch, H, device=dev)
+    Yh = torch.empty(D, batch, H, device=dev)
+    Yc = torch.empty(D, batch, H, device=dev)
+    Ws = w["W_scale"][sel] if per_channel else w["W_scale"][sel, 0].copy()
+    Rs = w["R_scale"][sel] if per_channel else w["R_scale"][sel, 0].copy()
+    q.dq_lstm_forward(_t(X, dev), _t(w["W"][sel], dev), _t(w["R"][sel], dev), _t(Ws, dev), _t(Rs, dev), ws,
+                      direction=DIRS[direction], B=_t(w["B"][sel], dev),
+                      h0=None if h0 is None else _t(h0, dev), c0=None if c0 is None else _t(c0, dev),
+                      Y=Y, Y_h=Yh, Y_c=Yc, W_zero_point=_t(np.zeros(Ws.size, np.int8), dev),
+                      R_zero_point=_t(np.zeros(Rs.size, np.int8), dev))
+    q.sync_status()
+    return Y.cpu().numpy(), Yh.cpu().numpy(), Yc.cpu().numpy()
+
+
+def oracle_step(orc, w, d, X_t, h, c):
+    """One oracle step of direction d from state (h, c)."""
+    H = w["R"].shape[1]
+    Gx = orc.dynamic_quantized_inner_product(X_t, iB=w["W"][d], scaleB=w["W_scale"][d])["C32"]
+    return orc.lstm_step(Gx, h, c, w["R"][d], w["R_scale"][d], w["B"][d, :4 * H], w["B"][d, 4 * H:])
+
+
+@pytest.mark.parametrize("direction", ["forward", "reverse", "bidirectional"])
+def test_single_step_from_given_state(orc, dev, direction):
+    w = workloads.lstm(seed=4, T=1, batch=5, I=96, H=40)
+    rng = np.random.default_rng(1)
+    D = 2 if direction == "bidirectional" else 1
+    h0 = rng.uniform(-0.9, 0.9, (D, 5, 40)).astype(np.float32)
+    c0 = rng.normal(0, 1, (D, 5, 40)).astype(np.float32)
+    Y, Yh, Yc = gpu_lstm(dev, w, direction, h0=h0, c0=c0)
+    for d in range(D):
+        widx = 1 if direction == "reverse" else d
+        h, c = oracle_step(orc, w, widx, w["X"][0], h0[d], c0[d])
+        np.testing.assert_allclose(Y[0, d], h, rtol=1e-5, atol=1e-6)
+        np.testing.assert_allclose(Yc[d], c, rtol=1e-5, atol=1e-6)
+        assert np.array_equal(Yh[d], Y[0, d])
+
+
+@pytest.mark.parametrize("direction", ["forward", "reverse", "bidirectional"])
+@pytest.mark.parametrize("per_channel", [True, False])
+def test_short_sequence(orc, dev, direction, per_channel):
+    w = workloads.lstm(seed=4, T=7, batch=3, I=64, H=32)
+    if not per_channel:
+        w["W_scale"][:] = w["W_scale"][:, :1]
+        w["R_scale"][:] = w["R_scale"][:, :1]
+    D = 2 if direction == "bidirectional" else 1
+    Y, Yh, Yc = gpu_lstm(dev, w, direction, per_channel=per_channel)
+    sl = slice(0, D) if direction != "reverse" else slice(1, 2)
+    ref = orc.dynamic_quantize_lstm(w["X"], w["W"][sl], w["R"][sl], w["B"][sl], w["W_scale"][sl], w["R_scale"][sl],
+                                    direction=direction)
+    np.testing.assert_allclose(Y, ref[0], rtol=1e-4, atol=1e-5)
+    np.testing.assert_allclose(Yh, ref[1], rtol=1e-4, atol=1e-5)
+    np.testing.assert_allclose(Yc, ref[2], rtol=1e-4, atol=1e-5)
+
+
+def test_nonzero_zero_point_rejected(dev):
+    w = workloads.lstm(seed=4, T=2, batch=2, I=16, H=8, D=1)
+    ws = torch.empty(q.dq_lstm_workspace_size(2, 2, 16, 8, q.LSTM_FORWARD), dtype=torch.uint8, device=dev)
+    zp = np.zeros(32, np.int8)
+    zp[3] = 1
+    with pytest.raises(q.I8QError) as e:
+        q.dq_lstm_forward(_t(w["X"], dev), _t(w["W"], dev), _t(w["R"], dev), _t(w["W_scale"], dev),
+                          _t(w["R_scale"], dev), ws, W_zero_point=_t(zp, dev))
+    assert e.value.code == q._lib.ERR_UNSUPPORTED
+
+
+def test_full_size_sampled_steps(orc, dev):
+    """T=512 batch=64 I=H=1024 bidirectional.  For sampled steps, the state
+    the step starts from comes from a GPU run over the preceding inputs."""
+    w = workloads.lstm(seed=4)
+    Y, Yh, Yc = gpu_lstm(dev, w, "bidirectional")
+    assert np.all(np.isfinite(Y)) and np.abs(Y).max() < 1.0
+    T = w["X"].shape[0]
+    for t in (0, 1, 200, 511):
+        # forward direction: state after steps 0..t-1
+        if t == 0:
+            h = np.zeros((64, 1024), np.float32)
+            c = np.zeros((64, 1024), np.float32)
+        else:
+            _, h, c = gpu_lstm(dev, w, "forward", X=w["X"][:t])
+            h, c = h[0], c[0]
+        hf, _ = oracle_step(orc, w, 0, w["X"][t], h, c)
+        np.testing.assert_allclose(Y[t, 0], hf, rtol=1e-5, atol=2e-6)
+    for t in (511, 300):
+        # reverse direction: state after steps T-1..t+1
+        if t == T - 1:
+            h = np.zeros((64, 1024), np.float32)
+            c = np.zeros((64, 1024), np.float32)
+        else:
+            _, h, c = gpu_lstm(dev, w, "reverse", X=w["X"][t + 1:])
+            h, c = h[0], c[0]
+        hr, _ = oracle_step(orc, w, 1, w["X"][t], h, c)
+        np.testing.assert_allclose(Y[t, 1], hr, rtol=1e-5, atol=2e-6)
