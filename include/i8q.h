@@ -188,6 +188,39 @@ int i8q_qgemm_dyn_weight_views(i8q_qgemm_ctx* ctx, int8_t** iBt, size_t* ldb, fl
  * Synchronizes the device first.  NULL or *ctx == NULL is a no-op. */
 void i8q_qgemm_dyn_clear(i8q_qgemm_ctx** ctx);
 
+/* Allocation-free dynamic quantized inner product.  The pages have no
+ * counterpart: it exists for callers that may not allocate device memory --
+ * code running inside a host application that owns all device memory
+ * through its own pool (a plugin, for instance), or code that cannot take
+ * cudaMalloc/cudaFree's possible device synchronization -- and so can
+ * neither create a context nor pass a scratch buffer of their own.
+ *
+ * Same result as a context with constB, typeB = I8Q_S8 (B given already
+ * quantized, with its per-column scales) followed by Forward:
+ *   A: M x K (typeA F32|BF16); B: K x N int8 row-major; scaleB: N fp32;
+ *   bias: N fp32 or NULL; activation: I8Q_ACT_*; C: M x N (typeC F32|BF16).
+ * All device pointers.  Every intermediate (uint8 A with its row scales and
+ * zero points, B transposed with its column sums) lives in one file-scope
+ * device array of I8Q_QGEMM_STATIC_SCRATCH_BYTES (32 MiB), held by every GPU
+ * that loads the library until the process exits; sizes whose
+ * i8q_qgemm_dyn_static_scratch_bytes exceed it are rejected with
+ * I8Q_ERR_UNSUPPORTED.  The call allocates nothing.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ * All calls share the one array: calls that overlap on the GPU (other
+ * streams, other host threads) race and corrupt each other's results.
+ * Asynchronous on stream. */
+#define I8Q_QGEMM_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+int i8q_qgemm_dyn_static(size_t M, size_t N, size_t K, int typeA, const void* A, const int8_t* B,
+                         const float* scaleB, const float* bias, int activation, int typeC, void* C,
+                         void* stream);
+
+/* Bytes of the static array i8q_qgemm_dyn_static uses for these sizes. */
+size_t i8q_qgemm_dyn_static_scratch_bytes(size_t M, size_t N, size_t K);
+
+/* Size of the static array (I8Q_QGEMM_STATIC_SCRATCH_BYTES). */
+size_t i8q_qgemm_dyn_static_scratch_capacity(void);
+
 /* ========================================================================
  * QuantizeLinear [QL] and DequantizeLinear [DQL]
  *

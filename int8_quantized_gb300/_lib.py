@@ -51,6 +51,9 @@ SIGNATURES = {
     "i8q_profile_entry": (_i, [_i, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_longlong),
                                ctypes.POINTER(ctypes.c_double)]),
     "i8q_measure_int8_mma_peak": (_i, [_i64, _p, ctypes.POINTER(ctypes.c_double)]),
+    "i8q_qgemm_dyn_static": (_i, [_sz, _sz, _sz, _i, _p, _p, _p, _p, _i, _i, _p, _p]),
+    "i8q_qgemm_dyn_static_scratch_bytes": (_sz, [_sz, _sz, _sz]),
+    "i8q_qgemm_dyn_static_scratch_capacity": (_sz, []),
 }
 
 _lib = None
