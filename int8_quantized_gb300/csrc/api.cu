@@ -263,10 +263,16 @@ int dmalloc(T** p, size_t bytes, size_t* total) {
   return I8Q_OK;
 }
 
+// Core selection.  The tensor-core path (exact integers on the bf16 pipe,
+// 128 x 256 tiles) pays off once there are enough tiles to fill the SMs; a
+// small product stays on the int8 mma.sync core.  I8Q_FORCE_CORE=imma|tc
+// overrides the choice (tests cover both cores on the same shapes).
 bool want_tc(size_t M, size_t N) {
-  (void)M;
-  (void)N;
-  return false;
+  const char* f = getenv("I8Q_FORCE_CORE");
+  if (f && std::string(f) == "imma") return false;
+  if (f && std::string(f) == "tc") return true;
+  const size_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
+  return M >= 128 && N >= 256 && tiles >= 64;
 }
 
 }  // namespace

@@ -70,7 +70,7 @@ __device__ __forceinline__ void store_out(const GemmEpilogue& ep, int64_t r, int
     float b1 = ep.bias ? __ldg(ep.bias + c + 1) : 0.0f;
     o1 = dequant_epilogue(a1, sA, __ldg(ep.scaleB + c + 1), b1, ep.act);
   }
-  const bool vec = two && ((ep.ldc & 1) == 0) && ((c & 1) == 0);
+  const bool vec = two && ((ep.ldc & 1) == 0) && ((c & 1) == 0) && (reinterpret_cast<uintptr_t>(ep.C) & 7) == 0;
   if (ep.out_mode == OUT_F32) {
     float* C = static_cast<float*>(ep.C) + r * ep.ldc + c;
     if (vec) {

@@ -1,12 +1,502 @@
-// gemm_tc.cu -- exact-integer GEMM on the bf16 tensor pipe (tcgen05).
+// gemm_tc.cu -- exact integer GEMM of the dynamic quantized inner product on
+// the bf16 tensor pipe of sm_103a (tcgen05.mma kind::f16, TMEM accumulators,
+// TMA-fed 128-byte-swizzled shared memory).
+//
+// sm_103a has no 8-bit integer tcgen05 form, but every uint8 code (0..255)
+// and every int8 code (-128..127) is exact in bf16, every product of two is
+// exact in fp32 (|p| < 2^15), and an fp32 sum of such products is exact
+// while every partial sum stays an integer below 2^24 in magnitude.  So the
+// K loop is cut into chunks of CK = 2^24 / 2^max_abs_product_log2 elements
+// (512 for uint8 x int8): each chunk accumulates in fp32 in TMEM, then the
+// epilogue warps drain it (tcgen05.ld), convert it exactly to int32 and add
+// it to an int32 running sum held in registers.  Two TMEM chunk buffers let
+// the tensor core fill one while the other drains.  The result is the exact
+// int32 sum_k uA*iB; the fused epilogue then applies -zeroA*colsum, the
+// scales, bias, activation and the store, exactly as the IMMA core does.
+//
+// CTA tile 128 x 256, K step 64 (one 128-byte swizzle row of bf16), 4-stage
+// smem ring (48 KB per stage), one CTA per SM, persistent over output tiles
+// in a grouped order so the A and B panels in flight stay in L2.
+// Warp roles: warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs (one
+// thread), warps 2..9 drain and run the epilogue (warp w reads TMEM lanes
+// 32*(w%4).. and half (w-2)/4 of the 256 columns).
+// Every mbarrier wait is bounded: on expiry the kernel records an error in
+// the device status word (read by i8q_sync_status), waits (bounded) for its
+// own copies and MMAs in flight, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 
 namespace i8q {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr int TMEM_COLS = 512;
+constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+constexpr int GROUP_M = 16;
+constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s per wait
+
+// status codes written to the device status word
+constexpr uint32_t ST_TIMEOUT_PRODUCER = 1u << 0;
+constexpr uint32_t ST_TIMEOUT_MMA = 1u << 1;
+constexpr uint32_t ST_TIMEOUT_EPILOGUE = 1u << 2;
+constexpr uint32_t ST_TIMEOUT_DRAIN = 1u << 3;
+
+struct TcParams {
+  int64_t M, N;
+  int KT;        // K steps of 64
+  int CS;        // K steps per exact fp32 chunk
+  int tiles_m, tiles_n;
+  int num_tiles;
+  GemmEpilogue ep;
+  uint32_t* status;
+};
+
+// ---- PTX wrappers -----------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: true when the phase completed; false on timeout (recorded)
+// or when another role already gave up.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* status,
+                                         uint32_t code) {
+  unsigned long long t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u) {
+      if (*abort_flag) return false;
+      unsigned long long now = global_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > WAIT_LIMIT_NS) {
+        atomicOr(status, code);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];\n" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(slot_smem), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns, one lane per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows
+// of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                   // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;                   // descriptor version
+  d |= (uint64_t)2 << 61;                   // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: bf16 x bf16 -> fp32, both K-major, M = 128, N = 256.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& mt, int& nt) {
+  const int per_group = GROUP_M * tiles_n;
+  const int g = tile / per_group;
+  const int first = g * GROUP_M;
+  const int gsize = min(tiles_m - first, GROUP_M);
+  const int r = tile - g * per_group;
+  mt = first + r % gsize;
+  nt = r / gsize;
+}
+
+__device__ __forceinline__ void store_row_segment(const GemmEpilogue& ep, int64_t row, int64_t col0, int64_t N,
+                                                  const int32_t (&run)[128], int32_t zA, float sA) {
+  // col0 .. col0+127 of one row; vector path when fully in range and aligned
+  const bool full = col0 + 128 <= N && (reinterpret_cast<uintptr_t>(ep.C) & 15) == 0;
+  if (ep.out_mode == OUT_S32) {
+    int32_t* C = static_cast<int32_t*>(ep.C) + row * ep.ldc + col0;
+    const bool vec = full && (ep.ldc % 4 == 0);
+#pragma unroll
+    for (int j = 0; j < 128; j += 4) {
+      int32_t v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t c = col0 + j + u;
+        v[u] = (c < N) ? run[j + u] - zA * __ldg(ep.colsum + c) : 0;
+      }
+      if (vec) {
+        *reinterpret_cast<int4*>(C + j) = make_int4(v[0], v[1], v[2], v[3]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (col0 + j + u < N) C[j + u] = v[u];
+      }
+    }
+    return;
+  }
+  const bool bf16 = ep.out_mode == OUT_BF16;
+  const bool vec = full && (bf16 ? (ep.ldc % 8 == 0) : (ep.ldc % 4 == 0));
+#pragma unroll
+  for (int j = 0; j < 128; j += 8) {
+    float o[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t c = col0 + j + u;
+      if (c < N) {
+        const int32_t s = run[j + u] - zA * __ldg(ep.colsum + c);
+        const float b = ep.bias ? __ldg(ep.bias + c) : 0.0f;
+        o[u] = dequant_epilogue(s, sA, __ldg(ep.scaleB + c), b, ep.act);
+      } else {
+        o[u] = 0.0f;
+      }
+    }
+    if (bf16) {
+      __nv_bfloat16* C = static_cast<__nv_bfloat16*>(ep.C) + row * ep.ldc + col0 + j;
+      if (vec) {
+        __nv_bfloat162 h0 = __floats2bfloat162_rn(o[0], o[1]), h1 = __floats2bfloat162_rn(o[2], o[3]);
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(o[4], o[5]), h3 = __floats2bfloat162_rn(o[6], o[7]);
+        uint4 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&h0);
+        pk.y = *reinterpret_cast<uint32_t*>(&h1);
+        pk.z = *reinterpret_cast<uint32_t*>(&h2);
+        pk.w = *reinterpret_cast<uint32_t*>(&h3);
+        *reinterpret_cast<uint4*>(C) = pk;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (col0 + j + u < N) C[u] = __float2bfloat16_rn(o[u]);
+      }
+    } else {
+      float* C = static_cast<float*>(ep.C) + row * ep.ldc + col0 + j;
+      if (vec) {
+        *reinterpret_cast<float4*>(C) = make_float4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<float4*>(C + 4) = make_float4(o[4], o[5], o[6], o[7]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (col0 + j + u < N) C[u] = o[u];
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t smem0 = smem_u32(smem);
+  auto sA = [&](int s) { return smem0 + (uint32_t)(s * STAGE_BYTES); };
+  auto sB = [&](int s) { return smem0 + (uint32_t)(s * STAGE_BYTES + A_STAGE); };
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto accf = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
+  auto acce = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
+  const uint32_t fin = smem_u32(bars + 2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf(b), 1);
+      mbar_init(acce(b), NUM_EPI_WARPS);
+    }
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int KT = p.KT, CS = p.CS;
+  const int nchunks = (KT + CS - 1) / CS;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int mt, nt;
+        tile_coords(tile, p.tiles_m, p.tiles_n, mt, nt);
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!wait_bar(empty(s), ph ^ 1u, abort_flag, p.status, ST_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full(s), STAGE_BYTES);
+          tma_load_2d(sA(s), &tmA, full(s), kt * BK, mt * BM);
+          tma_load_2d(sB(s), &tmB, full(s), kt * BK, nt * BN);
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA exits
+        for (int j = max(0, it - STAGES); j < it; ++j) {
+          unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(full(j % STAGES), (uint32_t)(j / STAGES) & 1u))
+            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+              atomicOr(p.status, ST_TIMEOUT_DRAIN);
+              break;
+            }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int it = 0, chunk = 0;
+      bool ok = true;
+      uint32_t d = tmem_base;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int kc = kt % CS;
+          if (kc == 0) {
+            const int b = chunk & 1;
+            if (!wait_bar(acce(b), ((uint32_t)(chunk >> 1) & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d = tmem_base + (uint32_t)(b * BN);
+          }
+          const int s = it % STAGES;
+          if (!wait_bar(full(s), (uint32_t)(it / STAGES) & 1u, abort_flag, p.status, ST_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = desc_sw128(sA(s) + (uint32_t)(k * 32));
+            const uint64_t bd = desc_sw128(sB(s) + (uint32_t)(k * 32));
+            tc_mma(d, ad, bd, IDESC, (kc == 0 && k == 0) ? 0u : 1u);
+          }
+          tc_commit(empty(s));
+          if (kc == CS - 1 || kt == KT - 1) {
+            tc_commit(accf(chunk & 1));
+            ++chunk;
+          }
+        }
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      tc_commit(fin);
+      unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(fin, 0))
+        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+          atomicOr(p.status, ST_TIMEOUT_DRAIN);
+          break;
+        }
+    }
+  } else {
+    // ---------------- drain + epilogue ----------------
+    const int q = warp & 3;                // TMEM lane quadrant of this warp
+    const int half = (warp - 2) >> 2;      // which 128 of the 256 columns
+    int chunk = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      int mt, nt;
+      tile_coords(tile, p.tiles_m, p.tiles_n, mt, nt);
+      int32_t run[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) run[j] = 0;
+      for (int c = 0; c < nchunks; ++c, ++chunk) {
+        const int b = chunk & 1;
+        // every lane waits; the outcome is made warp-uniform before the
+        // warp-collective TMEM loads
+        const bool got = wait_bar(accf(b), (uint32_t)(chunk >> 1) & 1u, abort_flag, p.status, ST_TIMEOUT_EPILOGUE);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + half * 128);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+          tmem_ld32(taddr + (uint32_t)(j * 32), r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) run[j * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce(b));
+      }
+      if (!ok) break;
+      const int64_t row = (int64_t)mt * BM + q * 32 + lane;
+      if (row < p.M) {
+        const float sA = __ldg(p.ep.scaleA + row);
+        const int32_t zA = __ldg(p.ep.zeroA + row);
+        store_row_segment(p.ep, row, (int64_t)nt * BN + half * 128, p.N, run, zA, sA);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---- host side ---------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over rows x Kp (Kp contiguous), box 64 x box_rows,
+// 128-byte swizzle; rows beyond `rows` read as zero.
+int make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t Kp, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(I8Q_ERR_CUDA, "gemm_tc: cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)Kp * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(I8Q_ERR_CUDA, "gemm_tc: cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+  return I8Q_OK;
+}
+
+}  // namespace
 
 int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M, int64_t N, int64_t Kp,
                    int max_abs_product_log2, const GemmEpilogue& ep, cudaStream_t s) {
-  (void)uA; (void)iBt; (void)M; (void)N; (void)Kp; (void)max_abs_product_log2; (void)ep; (void)s;
-  return fail(I8Q_ERR_UNSUPPORTED, "gemm_tc: not built");
+  if (M <= 0 || N <= 0) return I8Q_OK;
+  if (!uA || !iBt) return fail(I8Q_ERR_UNSUPPORTED, "gemm_tc: bf16 operands missing");
+  if (Kp % BK != 0 || Kp > (int64_t)1 << 20) return fail(I8Q_ERR_UNSUPPORTED, "gemm_tc: Kp must be a multiple of 64");
+  if (M > ((int64_t)1 << 31) - BM || N > ((int64_t)1 << 31) - BN) return fail(I8Q_ERR_UNSUPPORTED, "gemm_tc: too large");
+  if ((reinterpret_cast<uintptr_t>(uA) | reinterpret_cast<uintptr_t>(iBt)) & 15)
+    return fail(I8Q_ERR_UNSUPPORTED, "gemm_tc: operands must be 16-byte aligned");
+  if (max_abs_product_log2 < 1 || max_abs_product_log2 > 17)
+    return fail(I8Q_ERR_UNSUPPORTED, "gemm_tc: product bound out of range");
+  // largest chunk of K steps whose partial sums stay below 2^24 in magnitude
+  const int64_t chunk_k = ((int64_t)1 << 24) >> max_abs_product_log2;
+  const int CS = (int)std::max<int64_t>(1, chunk_k / BK);
+  uint32_t* status = device_status_word();
+  if (!status) return fail(I8Q_ERR_CUDA, "gemm_tc: no device status word");
+  CUtensorMap mA, mB;
+  int rc = make_map(&mA, uA, M, Kp, BM);
+  if (rc) return rc;
+  rc = make_map(&mB, iBt, N, Kp, BN);
+  if (rc) return rc;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(gemm_tc_kernel)");
+  TcParams p;
+  p.M = M;
+  p.N = N;
+  p.KT = (int)(Kp / BK);
+  p.CS = CS;
+  p.tiles_m = (int)ceil_div(M, BM);
+  p.tiles_n = (int)ceil_div(N, BN);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.ep = ep;
+  p.status = status;
+  const int grid = std::min(p.num_tiles, sm_count());
+  I8Q_PROF("gemm_tc", s);
+  gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(mA, mB, p);
+  I8Q_LAUNCH_CHECK("gemm_tc_kernel");
+  return I8Q_OK;
 }
 
 }  // namespace i8q

@@ -18,6 +18,15 @@ from int8_quantized_gb300 import workloads
 pytestmark = pytest.mark.gpu
 
 ACT = {"identity": q.ACT_IDENTITY, "relu": q.ACT_RELU, "gelu": q.ACT_GELU}
+CORE_INFO = {"imma": "mma.sync", "tc": "tcgen05"}
+
+
+@pytest.fixture(params=["imma", "tc"], autouse=True)
+def core(request, monkeypatch):
+    """Every case runs on both integer cores: the int8 mma.sync core and the
+    exact-integer tcgen05 core (forced regardless of the shape)."""
+    monkeypatch.setenv("I8Q_FORCE_CORE", request.param)
+    return request.param
 
 
 def _t(a, dev):
@@ -42,7 +51,8 @@ def run_case(orc, dev, A, B=None, iB=None, scaleB=None, bias=None, act="identity
         tB = q.BF16 if B.dtype == np.uint16 else q.F32
     ctx = q.QGemmDyn(M, N, K, tA, tB, tC, constB=constB, bias=bias is not None, activation=ACT[act],
                      avoidOverflow=avoid)
-    assert ctx.info()
+    import os
+    assert CORE_INFO[os.environ["I8Q_FORCE_CORE"]] in ctx.info()
     Ad = _t(A.view(np.int16) if typeA == "bf16" else A, dev)
     if typeA == "bf16":
         Ad = Ad.view(torch.bfloat16)
@@ -175,6 +185,27 @@ def test_worst_case_accumulator_magnitude(orc, dev):
     iB = np.full((K, N), -128, np.int8)
     iB[:, 1::2] = 127
     run_case(orc, dev, A, iB=iB, scaleB=np.full(N, 1e-3, np.float32), bias=None)
+
+
+def test_worst_case_accumulator_narrow_range(orc, dev):
+    """avoidOverflow with non-constant B: codes 255 x +-63 in every product,
+    K = 3000 (the tensor-core core sums 1024 of them in fp32 per chunk,
+    reaching 1024 * 16065 < 2^24)."""
+    M, N, K = 8, 300, 3000
+    A = np.ones((M, K), np.float32)
+    A[1::2] = -np.ones(K, np.float32)
+    B = np.full((K, N), 0.7, np.float32)
+    B[:, ::3] = -0.7
+    run_case(orc, dev, A, B, bias=None, avoid=True, constB=False)
+
+
+@pytest.mark.parametrize("K", [511, 512, 513, 1025, 2048 + 64])
+def test_chunk_boundaries(orc, dev, K):
+    rng = np.random.default_rng(K)
+    M, N = 130, 260
+    A = rng.normal(0, 1, (M, K)).astype(np.float32)
+    iB = rng.integers(-128, 128, (K, N)).astype(np.int8)
+    run_case(orc, dev, A, iB=iB, scaleB=rng.uniform(1e-3, 1e-2, N).astype(np.float32), bias=None)
 
 
 def test_context_reinit_and_errors(orc, dev):
