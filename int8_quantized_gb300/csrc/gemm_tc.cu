@@ -18,8 +18,11 @@
 // smem ring (48 KB per stage), one CTA per SM, persistent over output tiles
 // in a grouped order so the A and B panels in flight stay in L2.
 // Warp roles: warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs (one
-// thread), warps 2..9 drain and run the epilogue (warp w reads TMEM lanes
-// 32*(w%4).. and half (w-2)/4 of the 256 columns).
+// thread), warps 2..17 drain and run the epilogue: warp w reads TMEM lanes
+// 32*(w%4).. (its rows) and the 64-column slice (w-2)/4 of the tile.  The
+// final epilogue of a tile must finish within the two chunks the MMA can run
+// ahead, so it is kept short: the slice's column parameters are staged once
+// per tile in shared memory and full tiles store without bounds checks.
 // Every mbarrier wait is bounded: on expiry the kernel records an error in
 // the device status word (read by i8q_sync_status), waits (bounded) for its
 // own copies and MMAs in flight, frees TMEM and returns.
@@ -38,11 +41,13 @@ constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_EPI_WARPS = 16;
+constexpr int SLICE = BN / (NUM_EPI_WARPS / 4);  // 64 columns per epilogue warp
 constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+constexpr int PARAM_BYTES = NUM_EPI_WARPS * SLICE * 3 * 4;  // colsum, scaleB, bias per warp slice
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + PARAM_BYTES + NUM_BARS * 8 + 16;
 constexpr int GROUP_M = 16;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s per wait
 
@@ -140,18 +145,15 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 
-// 32 lanes x 32 consecutive 32-bit columns, one lane per thread.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+// 32 lanes x 16 consecutive 32-bit columns, one lane per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows
 // of 128 bytes, 8-row groups 1024 bytes apart.
@@ -178,21 +180,21 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
   nt = r / gsize;
 }
 
-__device__ __forceinline__ void store_row_segment(const GemmEpilogue& ep, int64_t row, int64_t col0, int64_t N,
-                                                  const int32_t (&run)[128], int32_t zA, float sA) {
-  // col0 .. col0+127 of one row; vector path when fully in range and aligned
-  const bool full = col0 + 128 <= N && (reinterpret_cast<uintptr_t>(ep.C) & 15) == 0;
+// The epilogue of one row's 64-column slice from the exact sums in run[].
+// Column parameters come from shared memory: pc (colsum), ps (scaleB),
+// pb (bias), SLICE entries each (zero beyond N).
+__device__ __forceinline__ void store_slice(const GemmEpilogue& ep, int64_t row, int64_t col0, int64_t N,
+                                            const int32_t (&run)[SLICE], int32_t zA, float sA, const int32_t* pc,
+                                            const float* ps, const float* pb) {
+  const bool full = col0 + SLICE <= N;
   if (ep.out_mode == OUT_S32) {
     int32_t* C = static_cast<int32_t*>(ep.C) + row * ep.ldc + col0;
-    const bool vec = full && (ep.ldc % 4 == 0);
+    const bool vec = full && (ep.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(ep.C) & 15) == 0;
 #pragma unroll
-    for (int j = 0; j < 128; j += 4) {
+    for (int j = 0; j < SLICE; j += 4) {
       int32_t v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t c = col0 + j + u;
-        v[u] = (c < N) ? run[j + u] - zA * __ldg(ep.colsum + c) : 0;
-      }
+      for (int u = 0; u < 4; ++u) v[u] = run[j + u] - zA * pc[j + u];
       if (vec) {
         *reinterpret_cast<int4*>(C + j) = make_int4(v[0], v[1], v[2], v[3]);
       } else {
@@ -204,21 +206,14 @@ __device__ __forceinline__ void store_row_segment(const GemmEpilogue& ep, int64_
     return;
   }
   const bool bf16 = ep.out_mode == OUT_BF16;
-  const bool vec = full && (bf16 ? (ep.ldc % 8 == 0) : (ep.ldc % 4 == 0));
+  const bool vec = full && (bf16 ? (ep.ldc % 8 == 0) : (ep.ldc % 4 == 0)) &&
+                   (reinterpret_cast<uintptr_t>(ep.C) & 15) == 0;
+  const int act = ep.act;
 #pragma unroll
-  for (int j = 0; j < 128; j += 8) {
+  for (int j = 0; j < SLICE; j += 8) {
     float o[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int64_t c = col0 + j + u;
-      if (c < N) {
-        const int32_t s = run[j + u] - zA * __ldg(ep.colsum + c);
-        const float b = ep.bias ? __ldg(ep.bias + c) : 0.0f;
-        o[u] = dequant_epilogue(s, sA, __ldg(ep.scaleB + c), b, ep.act);
-      } else {
-        o[u] = 0.0f;
-      }
-    }
+    for (int u = 0; u < 8; ++u) o[u] = dequant_epilogue(run[j + u] - zA * pc[j + u], sA, ps[j + u], pb[j + u], act);
     if (bf16) {
       __nv_bfloat16* C = static_cast<__nv_bfloat16*>(ep.C) + row * ep.ldc + col0 + j;
       if (vec) {
@@ -253,7 +248,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* params = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(params + PARAM_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t smem0 = smem_u32(smem);
@@ -372,16 +368,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else {
     // ---------------- drain + epilogue ----------------
-    const int q = warp & 3;                // TMEM lane quadrant of this warp
-    const int half = (warp - 2) >> 2;      // which 128 of the 256 columns
+    const int q = warp & 3;               // TMEM lane quadrant of this warp (its 32 rows)
+    const int slice = (warp - 2) >> 2;    // which 64 of the 256 columns
+    int32_t* pc = reinterpret_cast<int32_t*>(params) + (warp - 2) * SLICE * 3;
+    float* ps = reinterpret_cast<float*>(pc + SLICE);
+    float* pb = ps + SLICE;
     int chunk = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       int mt, nt;
       tile_coords(tile, p.tiles_m, p.tiles_n, mt, nt);
-      int32_t run[128];
+      const int64_t col0 = (int64_t)nt * BN + slice * SLICE;
+      // stage this slice's column parameters (read back after the K loop)
+      for (int j = lane; j < SLICE; j += 32) {
+        const int64_t c = col0 + j;
+        const bool in = c < p.N;
+        pc[j] = in ? __ldg(p.ep.colsum + c) : 0;
+        ps[j] = in ? __ldg(p.ep.scaleB + c) : 0.0f;
+        pb[j] = (in && p.ep.bias) ? __ldg(p.ep.bias + c) : 0.0f;
+      }
+      int32_t run[SLICE];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) run[j] = 0;
+      for (int j = 0; j < SLICE; ++j) run[j] = 0;
       for (int c = 0; c < nchunks; ++c, ++chunk) {
         const int b = chunk & 1;
         // every lane waits; the outcome is made warp-uniform before the
@@ -392,25 +400,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + half * 128);
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + slice * SLICE);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t r[32];
-          tmem_ld32(taddr + (uint32_t)(j * 32), r);
+        for (int j = 0; j < SLICE / 16; ++j) {
+          uint32_t r[16];
+          tmem_ld16(taddr + (uint32_t)(j * 16), r);
+          tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) run[j * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+          for (int i = 0; i < 16; ++i) run[j * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce(b));
       }
       if (!ok) break;
+      __syncwarp();
       const int64_t row = (int64_t)mt * BM + q * 32 + lane;
       if (row < p.M) {
         const float sA = __ldg(p.ep.scaleA + row);
         const int32_t zA = __ldg(p.ep.zeroA + row);
-        store_row_segment(p.ep, row, (int64_t)nt * BN + half * 128, p.N, run, zA, sA);
+        store_slice(p.ep, row, col0, p.N, run, zA, sA, pc, ps, pb);
       }
+      __syncwarp();
     }
   }
 

@@ -5,12 +5,14 @@
 //   DequantizeLinear: y = (x - x_zero_point) * x_scale
 //
 // Both are pure streams over HBM (5 bytes per element), so the kernels are
-// shaped for bandwidth: each thread moves 16 elements per iteration with
-// 16-byte loads and stores (4 x float4 on the fp32 side, one uint4 on the
-// 8-bit side), streaming cache hints, and a grid-stride loop over a grid
-// sized to fill every SM.  The per-axis parameter index is the middle index
-// of the [outer, axis_len, inner] view of the tensor; the common case of the
-// last axis (inner == 1) keeps a running channel counter instead of dividing.
+// shaped for bandwidth: a warp moves 512 consecutive elements per iteration
+// in four warp-wide accesses that are each one contiguous span (lane t takes
+// elements 128*q + 4*t .. +3: a float4 on the fp32 side, one 32-bit word of
+// codes on the 8-bit side), with streaming cache hints and a grid-stride
+// loop over a grid sized to fill every SM.  The per-axis parameter index is
+// the middle index of the [outer, axis_len, inner] view of the tensor; the
+// common case of the last axis (inner == 1) keeps a running channel per warp
+// tile instead of dividing.
 #include "common.cuh"
 
 namespace i8q {
@@ -47,108 +49,117 @@ __device__ __forceinline__ int load_zp(const QT* zp, int64_t c) {
   return (int)zp[c];
 }
 
-// Parameters of 16 consecutive elements starting at element e.
+// Channel of element e (per-axis modes).  AX_LAST: e % axis_len, kept as a
+// running value per warp tile; AX_BLOCK: (e / inner) % axis_len.
+// Parameters of 4 consecutive elements starting at channel c (AX_LAST: the
+// 4 channels c..c+3; otherwise one channel for all 4).
 template <int MODE, typename QT>
-__device__ __forceinline__ void params16(const float* __restrict__ scale, const QT* __restrict__ zp,
-                                         int64_t c0, float (&s)[16], int (&z)[16]) {
+__device__ __forceinline__ void params4(const float* __restrict__ scale, const QT* __restrict__ zp, int64_t c,
+                                        float (&s)[4], int (&z)[4]) {
   if (MODE == AX_LAST) {
-    // 16 consecutive channels; c0 is a multiple of 16 (axis_len % 16 == 0)
-    const float4* s4 = reinterpret_cast<const float4*>(scale + c0);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(scale + c));
+    s[0] = v.x;
+    s[1] = v.y;
+    s[2] = v.z;
+    s[3] = v.w;
+    const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(zp + c));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) z[q] = (int)(QT)((w >> (8 * q)) & 0xffu);
+  } else {
+    const float sv = __ldg(scale + c);
+    const int zv = (int)zp[c];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      float4 v = __ldg(s4 + q);
-      s[4 * q + 0] = v.x;
-      s[4 * q + 1] = v.y;
-      s[4 * q + 2] = v.z;
-      s[4 * q + 3] = v.w;
-    }
-    uint4 zz = __ldg(reinterpret_cast<const uint4*>(zp + c0));
-    uint32_t w[4] = {zz.x, zz.y, zz.z, zz.w};
-#pragma unroll
-    for (int q = 0; q < 16; ++q) z[q] = (int)(QT)((w[q >> 2] >> (8 * (q & 3))) & 0xff);
-  } else {
-    float sv = __ldg(scale + c0);
-    int zv = (int)zp[c0];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
       s[q] = sv;
       z[q] = zv;
     }
   }
 }
 
+// A warp tile is 512 consecutive elements.  Lane t of the warp handles, for
+// q = 0..3, the 4 elements at 128*q + 4*t: so each warp-wide access moves
+// one contiguous span (512 B of fp32 or 128 B of codes).
+template <int MODE>
+__device__ __forceinline__ int64_t channel_of(int64_t e, int64_t c_tile, int off, int64_t axis_len, int64_t inner) {
+  if (MODE == AX_TENSOR) return 0;
+  if (MODE == AX_BLOCK) return (e / inner) % axis_len;
+  int64_t c = c_tile + off;               // c_tile < axis_len, off < 512
+  if (axis_len >= 512) return c >= axis_len ? c - axis_len : c;
+  return c % axis_len;
+}
+
 template <int MODE, typename QT>
-__global__ void __launch_bounds__(256) quantize_vec16(const float* __restrict__ x, QT* __restrict__ y,
-                                                      int64_t nvec, const float* __restrict__ scale,
-                                                      const QT* __restrict__ zp, int64_t axis_len,
-                                                      int64_t inner) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  // running channel of element 16*v for the last-axis mode
-  int64_t c_last = 0, c_step = 0;
+__global__ void __launch_bounds__(256) quantize_warp512(const float* __restrict__ x, QT* __restrict__ y,
+                                                        int64_t ntiles, const float* __restrict__ scale,
+                                                        const QT* __restrict__ zp, int64_t axis_len, int64_t inner) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wstride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int64_t c_tile = 0, c_step = 0;
   if (MODE == AX_LAST) {
-    c_last = (16 * v) % axis_len;
-    c_step = (16 * stride) % axis_len;
+    c_tile = (w * 512) % axis_len;
+    c_step = (wstride * 512) % axis_len;
   }
   const float4* x4 = reinterpret_cast<const float4*>(x);
-  uint4* y16 = reinterpret_cast<uint4*>(y);
-  for (; v < nvec; v += stride) {
+  uint32_t* y32 = reinterpret_cast<uint32_t*>(y);
+  for (; w < ntiles; w += wstride) {
+    const int64_t base4 = w * 128;  // tile start in units of 4 elements
     float4 a[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) a[q] = __ldcs(x4 + 4 * v + q);
-    int64_t c0 = 0;
-    if (MODE == AX_LAST) c0 = c_last;
-    if (MODE == AX_BLOCK) c0 = ((16 * v) / inner) % axis_len;
-    float s[16];
-    int z[16];
-    params16<MODE, QT>(scale, zp, c0, s, z);
-    const float* f = reinterpret_cast<const float*>(a);
-    uint32_t w[4] = {0, 0, 0, 0};
+    for (int q = 0; q < 4; ++q) a[q] = __ldcs(x4 + base4 + 32 * q + lane);
 #pragma unroll
-    for (int q = 0; q < 16; ++q) w[q >> 2] |= quant_one<QT>(f[q], s[q], z[q]) << (8 * (q & 3));
-    __stcs(y16 + v, make_uint4(w[0], w[1], w[2], w[3]));
+    for (int q = 0; q < 4; ++q) {
+      const int off = 128 * q + 4 * lane;
+      float s[4];
+      int z[4];
+      params4<MODE, QT>(scale, zp, channel_of<MODE>(w * 512 + off, c_tile, off, axis_len, inner), s, z);
+      const uint32_t code = quant_one<QT>(a[q].x, s[0], z[0]) | (quant_one<QT>(a[q].y, s[1], z[1]) << 8) |
+                            (quant_one<QT>(a[q].z, s[2], z[2]) << 16) | (quant_one<QT>(a[q].w, s[3], z[3]) << 24);
+      __stcs(y32 + base4 + 32 * q + lane, code);
+    }
     if (MODE == AX_LAST) {
-      c_last += c_step;
-      if (c_last >= axis_len) c_last -= axis_len;
+      c_tile += c_step;
+      if (c_tile >= axis_len) c_tile -= axis_len;
     }
   }
 }
 
 template <int MODE, typename QT>
-__global__ void __launch_bounds__(256) dequantize_vec16(const QT* __restrict__ x, float* __restrict__ y,
-                                                        int64_t nvec, const float* __restrict__ scale,
-                                                        const QT* __restrict__ zp, int64_t axis_len,
-                                                        int64_t inner) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  int64_t c_last = 0, c_step = 0;
+__global__ void __launch_bounds__(256) dequantize_warp512(const QT* __restrict__ x, float* __restrict__ y,
+                                                          int64_t ntiles, const float* __restrict__ scale,
+                                                          const QT* __restrict__ zp, int64_t axis_len,
+                                                          int64_t inner) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wstride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int64_t c_tile = 0, c_step = 0;
   if (MODE == AX_LAST) {
-    c_last = (16 * v) % axis_len;
-    c_step = (16 * stride) % axis_len;
+    c_tile = (w * 512) % axis_len;
+    c_step = (wstride * 512) % axis_len;
   }
-  const uint4* x16 = reinterpret_cast<const uint4*>(x);
+  const uint32_t* x32 = reinterpret_cast<const uint32_t*>(x);
   float4* y4 = reinterpret_cast<float4*>(y);
-  for (; v < nvec; v += stride) {
-    uint4 in = __ldcs(x16 + v);
-    int64_t c0 = 0;
-    if (MODE == AX_LAST) c0 = c_last;
-    if (MODE == AX_BLOCK) c0 = ((16 * v) / inner) % axis_len;
-    float s[16];
-    int z[16];
-    params16<MODE, QT>(scale, zp, c0, s, z);
-    uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  for (; w < ntiles; w += wstride) {
+    const int64_t base4 = w * 128;
+    uint32_t in[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) in[q] = __ldcs(x32 + base4 + 32 * q + lane);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
+      const int off = 128 * q + 4 * lane;
+      float s[4];
+      int z[4];
+      params4<MODE, QT>(scale, zp, channel_of<MODE>(w * 512 + off, c_tile, off, axis_len, inner), s, z);
       float4 o;
-      o.x = dequant_one<QT>(w[q], s[4 * q + 0], z[4 * q + 0]);
-      o.y = dequant_one<QT>(w[q] >> 8, s[4 * q + 1], z[4 * q + 1]);
-      o.z = dequant_one<QT>(w[q] >> 16, s[4 * q + 2], z[4 * q + 2]);
-      o.w = dequant_one<QT>(w[q] >> 24, s[4 * q + 3], z[4 * q + 3]);
-      __stcs(y4 + 4 * v + q, o);
+      o.x = dequant_one<QT>(in[q], s[0], z[0]);
+      o.y = dequant_one<QT>(in[q] >> 8, s[1], z[1]);
+      o.z = dequant_one<QT>(in[q] >> 16, s[2], z[2]);
+      o.w = dequant_one<QT>(in[q] >> 24, s[3], z[3]);
+      __stcs(y4 + base4 + 32 * q + lane, o);
     }
     if (MODE == AX_LAST) {
-      c_last += c_step;
-      if (c_last >= axis_len) c_last -= axis_len;
+      c_tile += c_step;
+      if (c_tile >= axis_len) c_tile -= axis_len;
     }
   }
 }
@@ -209,6 +220,7 @@ int make_view(const int64_t* shape, int rank, int axis, size_t n_scale, AxisView
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 template <typename QT>
 int run_quantize(const float* x, const AxisView& v, const float* scale, const QT* zp, QT* y, cudaStream_t s) {
@@ -216,21 +228,22 @@ int run_quantize(const float* x, const AxisView& v, const float* scale, const QT
   I8Q_PROF("quantize_linear", s);
   int mode = -1;
   if (!v.per_axis) mode = AX_TENSOR;
-  else if (v.inner == 1 && v.axis_len % 16 == 0 && aligned16(scale) && aligned16(zp)) mode = AX_LAST;
-  else if (v.inner % 16 == 0) mode = AX_BLOCK;
-  int64_t nvec = (mode >= 0 && aligned16(x) && aligned16(y)) ? v.n / 16 : 0;
+  else if (v.inner == 1 && v.axis_len % 4 == 0 && aligned16(scale) && aligned4(zp)) mode = AX_LAST;
+  else if (v.inner % 4 == 0) mode = AX_BLOCK;
+  const bool ok_ptr = aligned16(x) && aligned4(y);
+  const int64_t ntiles = (mode >= 0 && ok_ptr) ? v.n / 512 : 0;
   const int threads = 256;
-  if (nvec > 0) {
-    int64_t blocks = std::min<int64_t>(ceil_div(nvec, threads), (int64_t)sm_count() * 8);
+  if (ntiles > 0) {
+    int64_t blocks = std::min<int64_t>(ceil_div(ntiles, threads / 32), (int64_t)sm_count() * 8);
     if (mode == AX_TENSOR)
-      quantize_vec16<AX_TENSOR, QT><<<blocks, threads, 0, s>>>(x, y, nvec, scale, zp, v.axis_len, v.inner);
+      quantize_warp512<AX_TENSOR, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, v.axis_len, v.inner);
     else if (mode == AX_LAST)
-      quantize_vec16<AX_LAST, QT><<<blocks, threads, 0, s>>>(x, y, nvec, scale, zp, v.axis_len, v.inner);
+      quantize_warp512<AX_LAST, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, v.axis_len, v.inner);
     else
-      quantize_vec16<AX_BLOCK, QT><<<blocks, threads, 0, s>>>(x, y, nvec, scale, zp, v.axis_len, v.inner);
-    I8Q_LAUNCH_CHECK("quantize_vec16");
+      quantize_warp512<AX_BLOCK, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, v.axis_len, v.inner);
+    I8Q_LAUNCH_CHECK("quantize_warp512");
   }
-  int64_t begin = nvec * 16;
+  int64_t begin = ntiles * 512;
   if (begin < v.n) {
     int64_t blocks = std::min<int64_t>(ceil_div(v.n - begin, threads), (int64_t)sm_count() * 8);
     quantize_scalar<QT><<<blocks, threads, 0, s>>>(x, y, begin, v.n, scale, zp, v.per_axis, v.axis_len, v.inner);
@@ -245,21 +258,22 @@ int run_dequantize(const QT* x, const AxisView& v, const float* scale, const QT*
   I8Q_PROF("dequantize_linear", s);
   int mode = -1;
   if (!v.per_axis) mode = AX_TENSOR;
-  else if (v.inner == 1 && v.axis_len % 16 == 0 && aligned16(scale) && aligned16(zp)) mode = AX_LAST;
-  else if (v.inner % 16 == 0) mode = AX_BLOCK;
-  int64_t nvec = (mode >= 0 && aligned16(x) && aligned16(y)) ? v.n / 16 : 0;
+  else if (v.inner == 1 && v.axis_len % 4 == 0 && aligned16(scale) && aligned4(zp)) mode = AX_LAST;
+  else if (v.inner % 4 == 0) mode = AX_BLOCK;
+  const bool ok_ptr = aligned4(x) && aligned16(y);
+  const int64_t ntiles = (mode >= 0 && ok_ptr) ? v.n / 512 : 0;
   const int threads = 256;
-  if (nvec > 0) {
-    int64_t blocks = std::min<int64_t>(ceil_div(nvec, threads), (int64_t)sm_count() * 8);
+  if (ntiles > 0) {
+    int64_t blocks = std::min<int64_t>(ceil_div(ntiles, threads / 32), (int64_t)sm_count() * 8);
     if (mode == AX_TENSOR)
-      dequantize_vec16<AX_TENSOR, QT><<<blocks, threads, 0, s>>>(x, y, nvec, scale, zp, v.axis_len, v.inner);
+      dequantize_warp512<AX_TENSOR, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, v.axis_len, v.inner);
     else if (mode == AX_LAST)
-      dequantize_vec16<AX_LAST, QT><<<blocks, threads, 0, s>>>(x, y, nvec, scale, zp, v.axis_len, v.inner);
+      dequantize_warp512<AX_LAST, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, v.axis_len, v.inner);
     else
-      dequantize_vec16<AX_BLOCK, QT><<<blocks, threads, 0, s>>>(x, y, nvec, scale, zp, v.axis_len, v.inner);
-    I8Q_LAUNCH_CHECK("dequantize_vec16");
+      dequantize_warp512<AX_BLOCK, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, v.axis_len, v.inner);
+    I8Q_LAUNCH_CHECK("dequantize_warp512");
   }
-  int64_t begin = nvec * 16;
+  int64_t begin = ntiles * 512;
   if (begin < v.n) {
     int64_t blocks = std::min<int64_t>(ceil_div(v.n - begin, threads), (int64_t)sm_count() * 8);
     dequantize_scalar<QT><<<blocks, threads, 0, s>>>(x, y, begin, v.n, scale, zp, v.per_axis, v.axis_len, v.inner);
