@@ -434,8 +434,9 @@ int forward_impl(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf, vo
   }
   GemmEpilogue ep{zeroA, scaleA, colsum, scaleB, ctx->bias ? ctx->biasv : nullptr, ctx->act, out_mode, C, N};
   if (ctx->use_tc) {
-    const int qb = (ctx->typeB == I8Q_S8 || !ctx->avoid) ? 7 : 6;  // |iB| <= 2^7 or 2^6
-    rc = launch_gemm_tc(uA_bf16, iBt_bf16, M, N, ctx->Kp, 8 + qb, ep, s);
+    // |uA - 128| <= 2^7; |iB| <= 2^7, or 2^6 in the narrowed range
+    const int qb = (ctx->typeB == I8Q_S8 || !ctx->avoid) ? 7 : 6;
+    rc = launch_gemm_tc(uA_bf16, iBt_bf16, M, N, ctx->Kp, 7 + qb, ep, s);
     if (rc != I8Q_ERR_UNSUPPORTED) return rc;
   }
   return launch_gemm_imma(uA, iBt, M, N, ctx->Kp, ep, s);

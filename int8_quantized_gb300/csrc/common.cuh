@@ -76,6 +76,33 @@ __device__ __forceinline__ float gelu_erf(float x) {
   return __fmul_rn(h, e);
 }
 
+// erfc from the Chebyshev fit published in Numerical Recipes (Press,
+// Teukolsky, Vetterling, Flannery, section 6.2, "erfcc"): fractional error
+// below 1.2e-7 for every x in exact arithmetic; evaluated here in fp32 with
+// the fast exponential, it stays within about 1e-6 relative -- far inside
+// half a bf16 ulp (2^-9), so it serves outputs stored as bf16.
+__device__ __forceinline__ float erfc_cheb(float x) {
+  const float z = fabsf(x);
+  const float t = __fdividef(1.0f, fmaf(0.5f, z, 1.0f));
+  float r = 0.17087277f;
+  r = fmaf(r, t, -0.82215223f);
+  r = fmaf(r, t, 1.48851587f);
+  r = fmaf(r, t, -1.13520398f);
+  r = fmaf(r, t, 0.27886807f);
+  r = fmaf(r, t, -0.18628806f);
+  r = fmaf(r, t, 0.09678418f);
+  r = fmaf(r, t, 0.37409196f);
+  r = fmaf(r, t, 1.00002368f);
+  r = fmaf(r, t, -1.26551223f);
+  const float ans = t * __expf(fmaf(-z, z, r));
+  return x >= 0.0f ? ans : 2.0f - ans;
+}
+
+// GELU for bf16 outputs (see erfc_cheb).
+__device__ __forceinline__ float gelu_bf16out(float x) {
+  return (0.5f * x) * erfc_cheb(-(x * 0.70710678118654752440f));
+}
+
 __device__ __forceinline__ float activate(float v, int act) {
   if (act == I8Q_ACT_RELU) return v > 0.0f ? v : 0.0f;
   if (act == I8Q_ACT_GELU) return gelu_erf(v);
@@ -92,11 +119,21 @@ __device__ __forceinline__ float dequant_epilogue(int32_t sum, float sA, float s
   return activate(v, act);
 }
 
+// Same, for an output stored as bf16: GELU may use the cheaper erfc.
+__device__ __forceinline__ float dequant_epilogue_bf16out(int32_t sum, float sA, float sB, float b, int act) {
+  float v = __int2float_rn(sum);
+  v = __fmul_rn(v, sA);
+  v = __fmul_rn(v, sB);
+  v = __fadd_rn(v, b);
+  if (act == I8Q_ACT_GELU) return gelu_bf16out(v);
+  return activate(v, act);
+}
+
 // ---- internal kernel launchers (implemented in the .cu files) ------------
 
 // Row quantization of A (M x K, fp32 or bf16, row stride lda elements) into
-// uA (M x Kp uint8, zero padded), optional uA_bf16 (M x Kp bf16 holding the
-// uint8 codes), scaleA[M], zeroA[M].
+// uA (M x Kp uint8, zero padded), optional uA_bf16 (M x Kp bf16 holding
+// uA - 128, zero padded), scaleA[M], zeroA[M].
 int launch_quantize_rows(const void* A, int typeA, int64_t M, int64_t K, int64_t lda, uint8_t* uA,
                          __nv_bfloat16* uA_bf16, int64_t Kp, float* scaleA, int32_t* zeroA,
                          cudaStream_t s);
@@ -137,9 +174,10 @@ struct GemmEpilogue {
 int launch_gemm_imma(const uint8_t* uA, const int8_t* iBt, int64_t M, int64_t N, int64_t Kp,
                      const GemmEpilogue& ep, cudaStream_t s);
 
-// Exact-integer GEMM on the bf16 tensor pipe (tcgen05), same contract as
-// launch_gemm_imma but reading the bf16 copies of uA and iBt.  Returns
-// I8Q_ERR_UNSUPPORTED when the shape is outside what it handles.
+// Exact-integer GEMM on the bf16 tensor pipe (tcgen05), same result as
+// launch_gemm_imma but reading the bf16 operand copies: uA - 128 and iBt.
+// max_abs_product_log2 bounds |(uA - 128) * iB| <= 2^max_abs_product_log2.
+// Returns I8Q_ERR_UNSUPPORTED when the shape is outside what it handles.
 int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M, int64_t N,
                    int64_t Kp, int max_abs_product_log2, const GemmEpilogue& ep, cudaStream_t s);
 

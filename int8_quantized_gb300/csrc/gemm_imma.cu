@@ -63,12 +63,15 @@ __device__ __forceinline__ void store_out(const GemmEpilogue& ep, int64_t r, int
     if (two) C[1] = a1;
     return;
   }
+  const bool bf16 = ep.out_mode == OUT_BF16;
   float b0 = ep.bias ? __ldg(ep.bias + c) : 0.0f;
-  float o0 = dequant_epilogue(a0, sA, __ldg(ep.scaleB + c), b0, ep.act);
+  float o0 = bf16 ? dequant_epilogue_bf16out(a0, sA, __ldg(ep.scaleB + c), b0, ep.act)
+                  : dequant_epilogue(a0, sA, __ldg(ep.scaleB + c), b0, ep.act);
   float o1 = 0.0f;
   if (two) {
     float b1 = ep.bias ? __ldg(ep.bias + c + 1) : 0.0f;
-    o1 = dequant_epilogue(a1, sA, __ldg(ep.scaleB + c + 1), b1, ep.act);
+    o1 = bf16 ? dequant_epilogue_bf16out(a1, sA, __ldg(ep.scaleB + c + 1), b1, ep.act)
+              : dequant_epilogue(a1, sA, __ldg(ep.scaleB + c + 1), b1, ep.act);
   }
   const bool vec = two && ((ep.ldc & 1) == 0) && ((c & 1) == 0) && (reinterpret_cast<uintptr_t>(ep.C) & 7) == 0;
   if (ep.out_mode == OUT_F32) {

@@ -2,17 +2,19 @@
 // the bf16 tensor pipe of sm_103a (tcgen05.mma kind::f16, TMEM accumulators,
 // TMA-fed 128-byte-swizzled shared memory).
 //
-// sm_103a has no 8-bit integer tcgen05 form, but every uint8 code (0..255)
-// and every int8 code (-128..127) is exact in bf16, every product of two is
-// exact in fp32 (|p| < 2^15), and an fp32 sum of such products is exact
-// while every partial sum stays an integer below 2^24 in magnitude.  So the
-// K loop is cut into chunks of CK = 2^24 / 2^max_abs_product_log2 elements
-// (512 for uint8 x int8): each chunk accumulates in fp32 in TMEM, then the
-// epilogue warps drain it (tcgen05.ld), convert it exactly to int32 and add
-// it to an int32 running sum held in registers.  Two TMEM chunk buffers let
-// the tensor core fill one while the other drains.  The result is the exact
-// int32 sum_k uA*iB; the fused epilogue then applies -zeroA*colsum, the
-// scales, bias, activation and the store, exactly as the IMMA core does.
+// sm_103a has no 8-bit integer tcgen05 form, but A's codes shifted to
+// uA - 128 (-128..127) and B's int8 codes are exact in bf16, every product
+// of two is exact in fp32 (|p| <= 2^14), and an fp32 sum of such products is
+// exact while every partial sum is an integer of magnitude at most 2^24.  So
+// the K loop is cut into chunks of CK = 2^24 / 2^max_abs_product_log2
+// elements (1024 for int8 B, 2048 in the narrowed [-64,63] range): each
+// chunk accumulates in fp32 in TMEM, then the epilogue warps drain it
+// (tcgen05.ld), convert it exactly to int32 and add it to an int32 running
+// sum held in registers.  Two TMEM chunk buffers let the tensor core fill
+// one while the other drains.  The result is the exact int32
+// sum_k (uA - 128) * iB; the fused epilogue adds back the shift with the
+// zero point, -(zeroA - 128) * colsum, then applies the scales, bias,
+// activation and the store, exactly as the IMMA core does.
 //
 // CTA tile 128 x 256, K step 64 (one 128-byte swizzle row of bf16), 4-stage
 // smem ring (48 KB per stage), one CTA per SM, persistent over output tiles
@@ -194,7 +196,7 @@ __device__ __forceinline__ void store_slice(const GemmEpilogue& ep, int64_t row,
     for (int j = 0; j < SLICE; j += 4) {
       int32_t v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = run[j + u] - zA * pc[j + u];
+      for (int u = 0; u < 4; ++u) v[u] = run[j + u] - zA * pc[j + u];  // zA arrives shifted by 128
       if (vec) {
         *reinterpret_cast<int4*>(C + j) = make_int4(v[0], v[1], v[2], v[3]);
       } else {
@@ -212,8 +214,14 @@ __device__ __forceinline__ void store_slice(const GemmEpilogue& ep, int64_t row,
 #pragma unroll
   for (int j = 0; j < SLICE; j += 8) {
     float o[8];
+    if (bf16) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) o[u] = dequant_epilogue(run[j + u] - zA * pc[j + u], sA, ps[j + u], pb[j + u], act);
+      for (int u = 0; u < 8; ++u)
+        o[u] = dequant_epilogue_bf16out(run[j + u] - zA * pc[j + u], sA, ps[j + u], pb[j + u], act);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) o[u] = dequant_epilogue(run[j + u] - zA * pc[j + u], sA, ps[j + u], pb[j + u], act);
+    }
     if (bf16) {
       __nv_bfloat16* C = static_cast<__nv_bfloat16*>(ep.C) + row * ep.ldc + col0 + j;
       if (vec) {
@@ -402,12 +410,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + slice * SLICE);
 #pragma unroll
-        for (int j = 0; j < SLICE / 16; ++j) {
-          uint32_t r[16];
-          tmem_ld16(taddr + (uint32_t)(j * 16), r);
+        for (int j = 0; j < SLICE / 16; j += 2) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(taddr + (uint32_t)(j * 16), r0);
+          tmem_ld16(taddr + (uint32_t)(j * 16 + 16), r1);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) run[j * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+          for (int i = 0; i < 16; ++i) {
+            run[j * 16 + i] += __float2int_rn(__uint_as_float(r0[i]));
+            run[j * 16 + 16 + i] += __float2int_rn(__uint_as_float(r1[i]));
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -418,7 +430,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int64_t row = (int64_t)mt * BM + q * 32 + lane;
       if (row < p.M) {
         const float sA = __ldg(p.ep.scaleA + row);
-        const int32_t zA = __ldg(p.ep.zeroA + row);
+        // A entered as uA - 128: sum_k (uA - zA) iB = run - (zA - 128) colsum
+        const int32_t zA = __ldg(p.ep.zeroA + row) - 128;
         store_slice(p.ep, row, col0, p.N, run, zA, sA, pc, ps, pb);
       }
       __syncwarp();

@@ -13,7 +13,8 @@
 //   (an all-zero column takes scale 1).
 // Both write the operand layouts the GEMM cores read: uA as M x Kp and B
 // transposed to N x Kp (K contiguous), zero padded to Kp, plus optional bf16
-// copies of the same integer codes for the tensor-core path, and the column
+// copies for the tensor-core path (B's codes as they are, A's shifted to
+// uA - 128 so every product stays within 2^14 in magnitude), and the column
 // sums of iB used by the zero-point correction  -zeroA[i] * colsum[j].
 #include "common.cuh"
 
@@ -144,11 +145,16 @@ quantize_rows_kernel(const T* __restrict__ A, int64_t M, int64_t K, int64_t lda,
       }
       *reinterpret_cast<uint2*>(u + k) = make_uint2(lo4, hi4);
       if (ub) {
+        // the tensor-core operand holds uA - 128 (exact in bf16), 0 in the
+        // padding beyond K
+        int cc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) cc[q] = (k + q < K) ? code[q] - 128 : 0;
         uint4 o;
-        o.x = code_bf16_bits(code[0]) | (code_bf16_bits(code[1]) << 16);
-        o.y = code_bf16_bits(code[2]) | (code_bf16_bits(code[3]) << 16);
-        o.z = code_bf16_bits(code[4]) | (code_bf16_bits(code[5]) << 16);
-        o.w = code_bf16_bits(code[6]) | (code_bf16_bits(code[7]) << 16);
+        o.x = code_bf16_bits(cc[0]) | (code_bf16_bits(cc[1]) << 16);
+        o.y = code_bf16_bits(cc[2]) | (code_bf16_bits(cc[3]) << 16);
+        o.z = code_bf16_bits(cc[4]) | (code_bf16_bits(cc[5]) << 16);
+        o.w = code_bf16_bits(cc[6]) | (code_bf16_bits(cc[7]) << 16);
         *reinterpret_cast<uint4*>(ub + k) = o;
       }
     }
