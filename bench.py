@@ -44,6 +44,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", default="i8q", choices=["i8q", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-rows", type=int, default=256, help="rows of the CPU-baseline sample")
+    p.add_argument("--no-rows", action="store_true", help="skip the other hot-path workloads")
     return p.parse_args(argv)
 
 
@@ -169,6 +170,99 @@ def cpu_baseline(rows, seed=2):
             f"TOPS = 2*rows*N*K / time")
 
 
+def _timed(fn, steps, warmup, stream):
+    """Per-call seconds over `steps` calls after `warmup`, with the library's
+    per-kernel event times {name: (launches per call, ms per call)}."""
+    import torch
+
+    import int8_quantized_gb300 as q
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    q.profile_enable(True)
+    secs = time_loop(fn, steps, stream)
+    prof = q.profile_collect()
+    q.profile_enable(False)
+    q.sync_status()
+    return secs / steps, {k: (v[0] / steps, v[1] / steps) for k, v in prof.items()}
+
+
+def measure_rows(args, dev, stream, world):
+    """The other workloads of the hot path, each timed on its own (per
+    call, device-resident inputs): algorithmic rate and per-kernel times."""
+    import numpy as np
+    import torch
+
+    import int8_quantized_gb300 as q
+    from int8_quantized_gb300 import workloads
+    steps, warm = max(3, args.steps // 2), max(2, args.warmup)
+    out = {}
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+
+    # large GEMM with avoidOverflow: non-constant fp32 B quantized in every Forward
+    w = workloads.large_gemm(seed=2, avoid_overflow=True)
+    ctx = q.QGemmDyn(M, N, K, q.BF16, q.F32, q.BF16, constB=False, bias=True, activation=q.ACT_GELU,
+                     avoidOverflow=True)
+    ctx.set_params(None, None, t(w["bias"]))
+    A = t(w["A_bf16"].view(np.int16)).view(torch.bfloat16)
+    B = t(w["B"])
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    buf = torch.empty(ctx.external_buffer_size(), dtype=torch.uint8, device=dev)
+    sec, prof = _timed(lambda: ctx.forward(A, C, B=B, buf=buf), steps, warm, stream)
+    out["large_gemm_avoid_overflow"] = {"ms": sec * 1e3, "TOPS": 2.0 * M * N * K / sec / 1e12, "kernels": prof,
+                                        "workload": "as the headline step, B fp32 [4096,14336] quantized to "
+                                                    "[-64,63] inside each Forward"}
+    ctx.clear()
+    del A, B, C, buf
+
+    # small inner product (latency)
+    w = workloads.inner_product(seed=0)
+    ctx = q.QGemmDyn(64, 128, 256, q.F32, q.F32, q.F32, constB=True, bias=True)
+    ctx.set_params(t(w["B"]), None, t(w["bias"]))
+    A = t(w["A"])
+    C = torch.empty(64, 128, device=dev)
+    sec, prof = _timed(lambda: ctx.forward(A, C), steps * 10, warm, stream)
+    out["inner_product_64x128x256"] = {"us": sec * 1e6, "kernels": prof}
+    ctx.clear()
+
+    # QLinearConv dense and depthwise
+    for dw in (False, True):
+        c = workloads.qlinearconv(seed=3, depthwise=dw)
+        x, wt = t(c["x"]), t(c["w"])
+        ws, wz, bias = t(c["w_scale"]), t(c["w_zero_point"]), t(c["B"])
+        y = torch.empty(32, 256, 56, 56, dtype=torch.uint8, device=dev)
+        wsb = q.qlinearconv_workspace_size(c["x"].shape, c["w"].shape, c["pads"], (1, 1), (1, 1), c["group"])
+        wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+        fn = lambda: q.qlinearconv(x, float(c["x_scale"]), c["x_zero_point"], wt, ws, wz,  # noqa: E731
+                                   float(c["y_scale"]), c["y_zero_point"], y, B=bias, pads=c["pads"],
+                                   group=c["group"], workspace=wsp if wsb else None)
+        sec, prof = _timed(fn, steps, warm, stream)
+        ops = 2.0 * 32 * 256 * 56 * 56 * (c["w"].shape[1] * 9)
+        moved = c["x"].nbytes + c["w"].nbytes + y.numel()
+        key = "qlinearconv_depthwise" if dw else "qlinearconv_dense"
+        out[key] = {"ms": sec * 1e3, "TOPS": ops / sec / 1e12, "GB/s": moved / sec / 1e9, "kernels": prof,
+                    "workload": "x u8 [32,256,56,56], w [256,%d,3,3], pad 1, per-channel w" % c["w"].shape[1]}
+        del x, wt, y, wsp
+
+    # DynamicQuantizeLSTM, bidirectional T=512 batch=64 I=H=1024
+    w = workloads.lstm(seed=4)
+    T_, b_, I_, H_ = 512, 64, 1024, 1024
+    X, Wd, Rd = t(w["X"]), t(w["W"]), t(w["R"])
+    Ws, Rs, Bb = t(w["W_scale"]), t(w["R_scale"]), t(w["B"])
+    wsp = torch.empty(q.dq_lstm_workspace_size(T_, b_, I_, H_, q.LSTM_BIDIRECTIONAL), dtype=torch.uint8, device=dev)
+    Y = torch.empty(T_, 2, b_, H_, device=dev)
+    Yh = torch.empty(2, b_, H_, device=dev)
+    Yc = torch.empty(2, b_, H_, device=dev)
+    fn = lambda: q.dq_lstm_forward(X, Wd, Rd, Ws, Rs, wsp, direction=q.LSTM_BIDIRECTIONAL,  # noqa: E731
+                                   B=Bb, Y=Y, Y_h=Yh, Y_c=Yc)
+    sec, prof = _timed(fn, 2, 1, stream)
+    ops = 2 * (2.0 * T_ * b_ * I_ * 4 * H_) + 2 * (2.0 * T_ * b_ * H_ * 4 * H_)
+    out["dq_lstm_bidirectional"] = {"ms": sec * 1e3, "TOPS": ops / sec / 1e12, "kernels": prof,
+                                    "workload": "T=512 batch=64 I=H=1024, projection + 512 steps per direction"}
+    del X, Wd, Rd, wsp, Y
+    return out
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -286,6 +380,8 @@ def run_i8q(args):
     dq_gbs = weak_scaling_value(5.0 * nel, args.steps, world, dq_secs) / 1e9
     del x, y, xr
 
+    rows = {} if args.no_rows else measure_rows(args, dev, stream, world)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tops, threads, dt, sample = cpu_baseline(args.cpu_rows)
@@ -314,6 +410,7 @@ def run_i8q(args):
                                   "frac_hbm": dq_gbs / world / hbm, "frac_8tbs": dq_gbs / world / 8000.0,
                                   "bytes": 5 * nel, "workload": "uint8 [32,1024,4096] per-axis(2) -> fp32"},
             "kernels": {k: {"launches": v[0], "ms": v[1] / max(v[0], 1)} for k, v in prof.items()},
+            "rows": rows,
             "gpu_launches": launches,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -69,6 +69,25 @@ __device__ __forceinline__ int sat_rint(float v, float lo, float hi) {
 
 // GELU = x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt 2)), evaluated as
 // (0.5 * x) * erfc(-(x / sqrt 2)) so nothing cancels for negative x.
+// saturate(rint(q) + zp) as the low byte of the result, for lo_z = lo - zp
+// and hi_z = hi - zp (small integers, exact in fp32).  Clamping to integer
+// bounds commutes with rounding, so q is clamped first; adding 1.5 * 2^23
+// then rounds it to the nearest integer, ties to even (the constant is an
+// even integer, so the parity of the rounded part is unchanged), and the
+// integer sits in the low mantissa bits: bits(q' + 1.5*2^23) = 0x4B400000 +
+// rint(q') for |q'| < 2^22.  Adding zp to that pattern leaves the code in
+// the low byte (two's complement for int8).
+__device__ __forceinline__ uint32_t rint_code_bits(float q, float lo_z, float hi_z, int zp) {
+  const float c = fminf(fmaxf(q, lo_z), hi_z);
+  const float r = __fadd_rn(c, 12582912.0f);
+  return (uint32_t)(__float_as_int(r) + zp);
+}
+
+// Pack the low bytes of four words into one word (byte 0 from a).
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
 __device__ __forceinline__ float gelu_erf(float x) {
   float t = __fmul_rn(x, 0.70710678118654752440f);
   float e = erfcf(-t);

@@ -31,11 +31,11 @@ struct QRange<int8_t> {
   static constexpr float lo = -128.0f, hi = 127.0f;
 };
 
+// Low byte of the result: the code of x (IEEE division, then saturating
+// round-half-even with the zero point).
 template <typename QT>
 __device__ __forceinline__ uint32_t quant_one(float x, float s, int zp) {
-  float q = __fdiv_rn(x, s);
-  int v = sat_rint(q, QRange<QT>::lo - (float)zp, QRange<QT>::hi - (float)zp) + zp;
-  return (uint32_t)(v & 0xff);
+  return rint_code_bits(__fdiv_rn(x, s), QRange<QT>::lo - (float)zp, QRange<QT>::hi - (float)zp, zp);
 }
 
 template <typename QT>
@@ -113,8 +113,8 @@ __global__ void __launch_bounds__(256) quantize_warp512(const float* __restrict_
       float s[4];
       int z[4];
       params4<MODE, QT>(scale, zp, channel_of<MODE>(w * 512 + off, c_tile, off, axis_len, inner), s, z);
-      const uint32_t code = quant_one<QT>(a[q].x, s[0], z[0]) | (quant_one<QT>(a[q].y, s[1], z[1]) << 8) |
-                            (quant_one<QT>(a[q].z, s[2], z[2]) << 16) | (quant_one<QT>(a[q].w, s[3], z[3]) << 24);
+      const uint32_t code = pack_low_bytes(quant_one<QT>(a[q].x, s[0], z[0]), quant_one<QT>(a[q].y, s[1], z[1]),
+                                           quant_one<QT>(a[q].z, s[2], z[2]), quant_one<QT>(a[q].w, s[3], z[3]));
       __stcs(y32 + base4 + 32 * q + lane, code);
     }
     if (MODE == AX_LAST) {
@@ -139,27 +139,39 @@ __global__ void __launch_bounds__(256) dequantize_warp512(const QT* __restrict__
   }
   const uint32_t* x32 = reinterpret_cast<const uint32_t*>(x);
   float4* y4 = reinterpret_cast<float4*>(y);
-  for (; w < ntiles; w += wstride) {
-    const int64_t base4 = w * 128;
-    uint32_t in[4];
+  // The 8-bit side moves only 4 bytes per lane per access, so four warp
+  // tiles (16 loads per lane) are put in flight before any is used.
+  constexpr int U = 4;
+  for (; w < ntiles; w += U * wstride) {
+    uint32_t in[U][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) in[q] = __ldcs(x32 + base4 + 32 * q + lane);
+    for (int u = 0; u < U; ++u) {
+      const int64_t wu = w + u * wstride;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int off = 128 * q + 4 * lane;
-      float s[4];
-      int z[4];
-      params4<MODE, QT>(scale, zp, channel_of<MODE>(w * 512 + off, c_tile, off, axis_len, inner), s, z);
-      float4 o;
-      o.x = dequant_one<QT>(in[q], s[0], z[0]);
-      o.y = dequant_one<QT>(in[q] >> 8, s[1], z[1]);
-      o.z = dequant_one<QT>(in[q] >> 16, s[2], z[2]);
-      o.w = dequant_one<QT>(in[q] >> 24, s[3], z[3]);
-      __stcs(y4 + base4 + 32 * q + lane, o);
+      for (int q = 0; q < 4; ++q) in[u][q] = wu < ntiles ? __ldcs(x32 + wu * 128 + 32 * q + lane) : 0u;
     }
-    if (MODE == AX_LAST) {
-      c_tile += c_step;
-      if (c_tile >= axis_len) c_tile -= axis_len;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t wu = w + u * wstride;
+      if (wu < ntiles) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int off = 128 * q + 4 * lane;
+          float s[4];
+          int z[4];
+          params4<MODE, QT>(scale, zp, channel_of<MODE>(wu * 512 + off, c_tile, off, axis_len, inner), s, z);
+          float4 o;
+          o.x = dequant_one<QT>(in[u][q], s[0], z[0]);
+          o.y = dequant_one<QT>(in[u][q] >> 8, s[1], z[1]);
+          o.z = dequant_one<QT>(in[u][q] >> 16, s[2], z[2]);
+          o.w = dequant_one<QT>(in[u][q] >> 24, s[3], z[3]);
+          __stcs(y4 + wu * 128 + 32 * q + lane, o);
+        }
+      }
+      if (MODE == AX_LAST) {
+        c_tile += c_step;
+        if (c_tile >= axis_len) c_tile -= axis_len;
+      }
     }
   }
 }

@@ -162,6 +162,88 @@ quantize_rows_kernel(const T* __restrict__ A, int64_t M, int64_t K, int64_t lda,
   }
 }
 
+// One warp per row, the whole row held in registers (one pass over HBM):
+// lane l holds the 8-element vectors l, l+32, ..., NV of them, as raw 16-byte
+// words (bf16: one word per vector; fp32: two).  Needs K % 8 == 0,
+// K <= 256 * NV, a 16-byte aligned A and a row stride that keeps rows aligned.
+template <typename T, int NV>
+__global__ void __launch_bounds__(128)
+quantize_rows_warp(const T* __restrict__ A, int64_t M, int64_t K, int64_t lda, uint8_t* __restrict__ uA,
+                   __nv_bfloat16* __restrict__ uA_bf16, int64_t Kp, float* __restrict__ scaleA,
+                   int32_t* __restrict__ zeroA) {
+  constexpr int W = sizeof(T) == 4 ? 2 : 1;  // 16-byte words per 8-element vector
+  const int lane = threadIdx.x & 31;
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (row >= M) return;
+  const T* a = A + row * lda;
+  uint4 raw[NV * W];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int64_t k = 8 * (int64_t)(lane + 32 * i);
+#pragma unroll
+    for (int w = 0; w < W; ++w)
+      raw[i * W + w] = k < K ? __ldcs(reinterpret_cast<const uint4*>(a + k) + w) : make_uint4(0, 0, 0, 0);
+  }
+  auto elem = [&](int i, int e) -> float {
+    if (W == 1) {
+      const uint32_t word = (&raw[i].x)[e >> 1];
+      return __uint_as_float((e & 1) ? (word & 0xffff0000u) : (word << 16));
+    }
+    return __uint_as_float((&raw[i * 2 + (e >> 2)].x)[e & 3]);
+  };
+  float mn = 0.0f, mx = 0.0f;  // zero padding beyond K leaves min(0, .) / max(0, .) unchanged
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float v = elem(i, e);
+      mn = fminf(mn, v);
+      mx = fmaxf(mx, v);
+    }
+  mn = warp_min(mn);
+  mx = warp_max(mx);
+  float s = __fdiv_rn(__fsub_rn(mx, mn), 255.0f);
+  int z = 0;
+  if (s == 0.0f) {
+    s = 1.0f;
+  } else {
+    z = sat_rint(__fdiv_rn(-mn, s), 0.0f, 255.0f);
+  }
+  if (lane == 0) {
+    scaleA[row] = s;
+    zeroA[row] = z;
+  }
+  const float lo_z = (float)(-z), hi_z = (float)(255 - z);
+  const float shift = (float)(z - 128) - 12582912.0f;  // takes rint + 1.5*2^23 to uA - 128
+  uint8_t* u = uA + row * Kp;
+  __nv_bfloat16* ub = uA_bf16 ? uA_bf16 + row * Kp : nullptr;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int64_t k = 8 * (int64_t)(lane + 32 * i);
+    if (k >= Kp) break;
+    uint32_t code[8], cb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      // IEEE quotient, clamp, round half to even by the 1.5*2^23 add
+      const float t = fminf(fmaxf(__fdiv_rn(elem(i, e), s), lo_z), hi_z);
+      const float r = __fadd_rn(t, 12582912.0f);
+      const bool valid = k + e < K;
+      code[e] = valid ? (uint32_t)(__float_as_int(r) + z) : 0u;
+      cb[e] = valid ? (__float_as_uint(__fadd_rn(r, shift)) >> 16) : 0u;
+    }
+    *reinterpret_cast<uint2*>(u + k) =
+        make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]), pack_low_bytes(code[4], code[5], code[6], code[7]));
+    if (ub) {
+      uint4 o;
+      o.x = cb[0] | (cb[1] << 16);
+      o.y = cb[2] | (cb[3] << 16);
+      o.z = cb[4] | (cb[5] << 16);
+      o.w = cb[6] | (cb[7] << 16);
+      *reinterpret_cast<uint4*>(ub + k) = o;
+    }
+  }
+}
+
 // ---- columns -------------------------------------------------------------
 // A CTA owns 32 columns [j0, j0+32) and walks all of K twice: once for the
 // max-abs per column, once to quantize, transposing 64 x 32 tiles through
@@ -258,6 +340,38 @@ int launch_quantize_rows(const void* A, int typeA, int64_t M, int64_t K, int64_t
   if (M <= 0) return I8Q_OK;
   int64_t blocks = std::min<int64_t>(M, (int64_t)sm_count() * 8);
   I8Q_PROF("quantize_rows", s);
+  // warp per row with the row in registers, when it fits
+  {
+    const bool bf = typeA == I8Q_BF16;
+    const int64_t esz = bf ? 2 : 4;
+    const bool aligned = aligned16(A) && K % 8 == 0 && (lda * esz) % 16 == 0;
+    const int nv_max = bf ? 16 : 8;
+    int nv = 1;
+    while (nv < nv_max && 256 * nv < K) nv *= 2;
+    if (aligned && 256 * nv >= K) {
+      const int64_t wblocks = ceil_div(M, 4);  // 4 rows (warps) per 128-thread block
+      if (bf) {
+        const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(A);
+        switch (nv) {
+          case 1: quantize_rows_warp<__nv_bfloat16, 1><<<(unsigned)wblocks, 128, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA); break;
+          case 2: quantize_rows_warp<__nv_bfloat16, 2><<<(unsigned)wblocks, 128, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA); break;
+          case 4: quantize_rows_warp<__nv_bfloat16, 4><<<(unsigned)wblocks, 128, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA); break;
+          case 8: quantize_rows_warp<__nv_bfloat16, 8><<<(unsigned)wblocks, 128, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA); break;
+          default: quantize_rows_warp<__nv_bfloat16, 16><<<(unsigned)wblocks, 128, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA); break;
+        }
+      } else {
+        const float* a = static_cast<const float*>(A);
+        switch (nv) {
+          case 1: quantize_rows_warp<float, 1><<<(unsigned)wblocks, 128, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA); break;
+          case 2: quantize_rows_warp<float, 2><<<(unsigned)wblocks, 128, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA); break;
+          case 4: quantize_rows_warp<float, 4><<<(unsigned)wblocks, 128, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA); break;
+          default: quantize_rows_warp<float, 8><<<(unsigned)wblocks, 128, 0, s>>>(a, M, K, lda, uA, uA_bf16, Kp, scaleA, zeroA); break;
+        }
+      }
+      I8Q_LAUNCH_CHECK("quantize_rows_warp");
+      return I8Q_OK;
+    }
+  }
   if (typeA == I8Q_F32) {
     const float* a = static_cast<const float*>(A);
     bool vec = aligned16(a) && K % 8 == 0 && lda % 4 == 0;
