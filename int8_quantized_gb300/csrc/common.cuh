@@ -200,4 +200,14 @@ int launch_gemm_imma(const uint8_t* uA, const int8_t* iBt, int64_t M, int64_t N,
 int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M, int64_t N,
                    int64_t Kp, int max_abs_product_log2, const GemmEpilogue& ep, cudaStream_t s);
 
+// QLinearConv on the tensor pipe (group 1, stride 1, dilation 1, tile shapes
+// it instantiates).  conv_tc_workspace: scratch bytes, 0 when the shape does
+// not take this path.
+size_t conv_tc_workspace(int64_t N, int64_t C, int64_t H, int64_t W, int64_t M, int64_t Cg, int64_t kH, int64_t kW,
+                         int64_t OH, int64_t OW, int64_t group, int64_t sh, int64_t sw, int64_t dh, int64_t dw);
+int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, int64_t W, float x_scale, int x_zp,
+                   const void* w, int wtype, int64_t M, int64_t kH, int64_t kW, const float* w_scale,
+                   const void* w_zp, int per_channel, float y_scale, int y_zp, int ytype, const int32_t* B,
+                   int64_t pt, int64_t pl, int64_t OH, int64_t OW, void* y, void* workspace, cudaStream_t s);
+
 }  // namespace i8q

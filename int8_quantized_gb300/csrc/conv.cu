@@ -124,7 +124,7 @@ extern "C" size_t i8q_qlinearconv_workspace_size(const int64_t* xshape, const in
                                                  const int64_t* strides, const int64_t* dilations, int64_t group) {
   ConvShape s;
   if (conv_shape(xshape, wshape, pads, strides, dilations, group, &s) != I8Q_OK) return 0;
-  return 0;
+  return conv_tc_workspace(s.N, s.C, s.H, s.W, s.M, s.Cg, s.kH, s.kW, s.OH, s.OW, s.group, s.sh, s.sw, s.dh, s.dw);
 }
 
 extern "C" int i8q_qlinearconv(const void* x, int xtype, const int64_t* xshape, float x_scale, int x_zero_point,
@@ -133,11 +133,17 @@ extern "C" int i8q_qlinearconv(const void* x, int xtype, const int64_t* xshape, 
                                const int32_t* B, const int64_t* pads, const int64_t* strides,
                                const int64_t* dilations, int64_t group, void* y, int ytype, void* workspace,
                                size_t ws_bytes, void* stream) {
-  (void)workspace;
-  (void)ws_bytes;
   ConvShape s;
   int rc = conv_shape(xshape, wshape, pads, strides, dilations, group, &s);
   if (rc) return rc;
+  const size_t ws_need =
+      conv_tc_workspace(s.N, s.C, s.H, s.W, s.M, s.Cg, s.kH, s.kW, s.OH, s.OW, s.group, s.sh, s.sw, s.dh, s.dw);
+  if (ws_need) {
+    if (!workspace || ws_bytes < ws_need)
+      return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: workspace missing or smaller than qlinearconv_workspace_size");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255)
+      return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: workspace must be 256-byte aligned");
+  }
   auto is8 = [](int t) { return t == I8Q_U8 || t == I8Q_S8; };
   if (!is8(xtype) || !is8(wtype) || !is8(ytype)) return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: types must be U8 or S8");
   if (!x || !w || !y || !w_scale || !w_zero_point) return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: NULL tensor pointer");
@@ -150,6 +156,9 @@ extern "C" int i8q_qlinearconv(const void* x, int xtype, const int64_t* xshape, 
   if (!(x_scale > 0.0f) || !(y_scale > 0.0f)) return fail(I8Q_ERR_INVALID_ARG, "qlinearconv: scales must be > 0");
   const int pc = n_w != 1;
   cudaStream_t st = as_stream(stream);
+  if (ws_need)
+    return launch_conv_tc(x, xtype, s.N, s.C, s.H, s.W, x_scale, x_zero_point, w, wtype, s.M, s.kH, s.kW, w_scale,
+                          w_zero_point, pc, y_scale, y_zero_point, ytype, B, s.pt, s.pl, s.OH, s.OW, y, workspace, st);
   if (xtype == I8Q_U8 && wtype == I8Q_U8)
     return dispatch_y<uint8_t, uint8_t>(ytype, s, x, x_scale, x_zero_point, w, w_scale, w_zero_point, pc, y_scale,
                                         y_zero_point, B, y, st);

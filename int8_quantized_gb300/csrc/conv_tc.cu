@@ -1,0 +1,450 @@
+// conv_tc.cu -- QLinearConv (onnx-light docs, "QLinearConv") for group 1,
+// stride 1, dilation 1 as an implicit GEMM on the bf16 tensor pipe
+// (tcgen05.mma kind::f16), exact in integers.
+//
+// Two small passes centre the operands, exactly, in bf16:
+//   xc = x - x_zero_point      NHWC  [N][H][W][Cp]      (|xc| <= 255)
+//   wc = w - w_zero_point[m]   [M][kH][kW][Cp]          (|wc| <= 255)
+// with Cp = C rounded up to 64 and zeros beyond C.  Then, for an output tile
+// of 128 output channels x R output rows (R * OW pixels),
+//   acc[m, p] = sum over taps (kh, kw) and 64-channel slabs of
+//               wc[m, kh, kw, c] * xc[n, oh + kh - pad_top, ow + kw - pad_left, c]
+// The x slab of one tap is one 4-D TMA box {64 channels, OW, R, 1} at
+// (c0, kw - pad_left, oh0 + kh - pad_top, n); coordinates outside the input
+// read 0, which is exactly the padding of QLinearConv (a padded position is
+// real 0, i.e. x_zero_point, so xc = 0 there).  Products are within
+// max|xc| * 255, so fp32 chunks of CS K-steps stay exact (partial sums at
+// most 2^24) and are drained into int32 as in the GEMM core.  The epilogue
+// requantizes each output,
+//   y = saturate(rint(((float)(acc + B[m]) * (x_scale * w_scale[m])) / y_scale) + y_zero_point),
+// and stores NCHW bytes: thread = output channel, its slice = consecutive
+// pixels of one output row.
+#include "tcgen05.cuh"
+
+namespace i8q {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int NUM_EPI_WARPS = 16;
+constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr int TMEM_COLS = 512;
+constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+
+constexpr uint32_t ST_TIMEOUT_PRODUCER = 1u << 4;
+constexpr uint32_t ST_TIMEOUT_MMA = 1u << 5;
+constexpr uint32_t ST_TIMEOUT_EPILOGUE = 1u << 6;
+constexpr uint32_t ST_TIMEOUT_DRAIN = 1u << 7;
+
+template <int TN>
+struct ConvTile {
+  static constexpr int A_STAGE = BM * BK * 2;
+  static constexpr int B_STAGE = TN * BK * 2;
+  static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+  static constexpr int SL = TN / 4;  // pixels per epilogue warp
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(TN % 32 == 0 && TN <= 256, "tile width");
+};
+
+struct ConvParams {
+  int M, CC, taps, kW, pt, pl, OH, OW, R, NB;
+  int tiles_m, row_groups, num_tiles;
+  int KT, CS;
+  float x_scale, y_scale, qlo_z, qhi_z;  // qlo_z = qlo - y_zp, qhi_z = qhi - y_zp
+  int y_zp;
+  const int32_t* bias;
+  const float* w_scale;
+  int per_channel;
+  uint8_t* y;  // NCHW bytes (uint8 or int8 codes)
+  uint32_t* status;
+};
+
+__device__ __forceinline__ void conv_tile_coords(int tile, const ConvParams& p, int& mt, int& rg, int& n) {
+  mt = tile % p.tiles_m;
+  const int rest = tile / p.tiles_m;
+  rg = rest % p.row_groups;
+  n = rest / p.row_groups;
+}
+
+template <int TN>
+__global__ void __launch_bounds__(THREADS, 1)
+conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, ConvParams p) {
+  using T = ConvTile<TN>;
+  constexpr uint32_t IDESC = idesc_bf16(BM, TN);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * T::STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t smem0 = smem_u32(smem);
+  auto sA = [&](int s) { return smem0 + (uint32_t)(s * T::STAGE_BYTES); };
+  auto sB = [&](int s) { return smem0 + (uint32_t)(s * T::STAGE_BYTES + T::A_STAGE); };
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto accf = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
+  auto acce = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
+  const uint32_t fin = smem_u32(bars + 2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf(b), 1);
+      mbar_init(acce(b), NUM_EPI_WARPS);
+    }
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int KT = p.KT, CS = p.CS;
+  const int nchunks = (KT + CS - 1) / CS;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int mt, rg, n;
+        conv_tile_coords(tile, p, mt, rg, n);
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int s = it % STAGES;
+          if (!wait_bar(empty(s), ((uint32_t)(it / STAGES) & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          const int tap = kt / p.CC, cch = kt - tap * p.CC;
+          const int kh = tap / p.kW, kw = tap - kh * p.kW;
+          mbar_arrive_expect_tx(full(s), T::STAGE_BYTES);
+          tma_load_2d(sA(s), &tmW, full(s), kt * BK, mt * BM);
+          tma_load_4d(sB(s), &tmX, full(s), cch * BK, kw - p.pl, rg * p.R + kh - p.pt, n);
+        }
+      }
+      if (!ok) {
+        for (int j = max(0, it - STAGES); j < it; ++j) {
+          unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(full(j % STAGES), (uint32_t)(j / STAGES) & 1u))
+            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+              atomicOr(p.status, ST_TIMEOUT_DRAIN);
+              break;
+            }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int it = 0, chunk = 0;
+      bool ok = true;
+      uint32_t d = tmem_base;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int kc = kt % CS;
+          if (kc == 0) {
+            const int b = chunk & 1;
+            if (!wait_bar(acce(b), ((uint32_t)(chunk >> 1) & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d = tmem_base + (uint32_t)(b * TN);
+          }
+          const int s = it % STAGES;
+          if (!wait_bar(full(s), (uint32_t)(it / STAGES) & 1u, abort_flag, p.status, ST_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = desc_sw128(sA(s) + (uint32_t)(k * 32));
+            const uint64_t bd = desc_sw128(sB(s) + (uint32_t)(k * 32));
+            tc_mma(d, ad, bd, IDESC, (kc == 0 && k == 0) ? 0u : 1u);
+          }
+          tc_commit(empty(s));
+          if (kc == CS - 1 || kt == KT - 1) {
+            tc_commit(accf(chunk & 1));
+            ++chunk;
+          }
+        }
+      }
+      tc_commit(fin);
+      unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(fin, 0))
+        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+          atomicOr(p.status, ST_TIMEOUT_DRAIN);
+          break;
+        }
+    }
+  } else {
+    // ---------------- drain + requantizing epilogue ----------------
+    constexpr int SL = T::SL;
+    const int q = warp & 3;             // TMEM lanes 32q.. = output channels of this warp
+    const int slice = (warp - 2) >> 2;  // pixels [slice*SL, slice*SL + SL) of the tile
+    int chunk = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      int mt, rg, n;
+      conv_tile_coords(tile, p, mt, rg, n);
+      int32_t run[SL];
+#pragma unroll
+      for (int j = 0; j < SL; ++j) run[j] = 0;
+      for (int c = 0; c < nchunks; ++c, ++chunk) {
+        const int b = chunk & 1;
+        const bool got = wait_bar(accf(b), (uint32_t)(chunk >> 1) & 1u, abort_flag, p.status, ST_TIMEOUT_EPILOGUE);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TN + slice * SL);
+#pragma unroll
+        for (int j = 0; j < SL / 8; j += 2) {
+          uint32_t r0[8], r1[8];
+          tmem_ld8(taddr + (uint32_t)(j * 8), r0);
+          if (j + 1 < SL / 8) tmem_ld8(taddr + (uint32_t)(j * 8 + 8), r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            run[j * 8 + i] += __float2int_rn(__uint_as_float(r0[i]));
+            if (j + 1 < SL / 8) run[j * 8 + 8 + i] += __float2int_rn(__uint_as_float(r1[i]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce(b));
+      }
+      if (!ok) break;
+      const int m = mt * BM + q * 32 + lane;
+      if (m < p.M) {
+        const int32_t bm = p.bias ? __ldg(p.bias + m) : 0;
+        const float mul = __fmul_rn(p.x_scale, __ldg(p.w_scale + (p.per_channel ? m : 0)));
+        uint8_t* yrow = p.y + ((int64_t)n * p.M + m) * p.OH * p.OW;
+        const int p0 = slice * SL;
+        if (SL == p.OW && (p.OW & 7) == 0 && (reinterpret_cast<uintptr_t>(p.y) & 7) == 0) {
+          // the slice is exactly one output row: 8-byte stores
+          const int oh = rg * p.R + slice;
+          if (oh < p.OH) {
+            uint8_t* dst = yrow + (int64_t)oh * p.OW;
+#pragma unroll
+            for (int j = 0; j < SL; j += 8) {
+              uint32_t code[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                float v = __fmul_rn(__int2float_rn(run[j + u] + bm), mul);
+                v = __fdiv_rn(v, p.y_scale);
+                code[u] = rint_code_bits(v, p.qlo_z, p.qhi_z, p.y_zp);
+              }
+              *reinterpret_cast<uint2*>(dst + j) = make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]),
+                                                              pack_low_bytes(code[4], code[5], code[6], code[7]));
+            }
+          }
+        } else {
+          int oh = rg * p.R + p0 / p.OW, ow = p0 % p.OW;
+#pragma unroll
+          for (int j = 0; j < SL; ++j) {
+            if (oh < p.OH) {
+              float v = __fmul_rn(__int2float_rn(run[j] + bm), mul);
+              v = __fdiv_rn(v, p.y_scale);
+              yrow[(int64_t)oh * p.OW + ow] = (uint8_t)rint_code_bits(v, p.qlo_z, p.qhi_z, p.y_zp);
+            }
+            if (++ow == p.OW) {
+              ow = 0;
+              ++oh;
+            }
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---- operand preparation -------------------------------------------------------
+
+// xc[n][h][w][c] = x[n][c][h][w] - xz (bf16), zero for c >= C.  One block per
+// (n, h, 64-channel slab); the slab is transposed through shared memory in
+// chunks of 32 columns.
+template <typename XT>
+__global__ void __launch_bounds__(256)
+center_x_nhwc(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv_bfloat16* __restrict__ xc) {
+  __shared__ float tile[64][33];
+  const int n = blockIdx.z, h = blockIdx.y, c0 = blockIdx.x * 64;
+  const int t = threadIdx.x;
+  for (int w0 = 0; w0 < W; w0 += 32) {
+    for (int cc = t / 32; cc < 64; cc += 8) {
+      const int c = c0 + cc, w = w0 + (t & 31);
+      float v = 0.0f;
+      if (c < C && w < W) v = (float)((int)x[(((int64_t)n * C + c) * H + h) * W + w] - xz);
+      tile[cc][t & 31] = v;
+    }
+    __syncthreads();
+    // each thread writes 8 channels (16 bytes) of one column
+    for (int i = t; i < 32 * 8; i += 256) {
+      const int wl = i / 8, cg = (i % 8) * 8, w = w0 + wl;
+      if (w < W) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t lo = __float_as_uint(tile[cg + 2 * u][wl]) >> 16;
+          const uint32_t hi = __float_as_uint(tile[cg + 2 * u + 1][wl]) & 0xffff0000u;
+          pk[u] = lo | hi;
+        }
+        *reinterpret_cast<uint4*>(xc + (((int64_t)n * H + h) * W + w) * Cp + c0 + cg) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// wc[m][kh][kw][c] = w[m][c][kh][kw] - wz[m] (bf16), zero for c >= C.
+template <typename WT>
+__global__ void center_w(const WT* __restrict__ w, const WT* __restrict__ wz, int per_channel, int M, int C, int taps,
+                         int Cp, __nv_bfloat16* __restrict__ wc) {
+  const int64_t total = (int64_t)M * taps * Cp;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % Cp);
+    const int64_t r = i / Cp;
+    const int tap = (int)(r % taps);
+    const int m = (int)(r / taps);
+    float v = 0.0f;
+    if (c < C) v = (float)((int)w[((int64_t)m * C + c) * taps + tap] - (int)wz[per_channel ? m : 0]);
+    wc[i] = __float2bfloat16_rn(v);  // exact: |v| <= 255
+  }
+}
+
+size_t a256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Output rows per tile so that R * OW is a multiple of 32 and at most 256.
+int pick_rows(int64_t OW, int64_t OH) {
+  int best = 0;
+  for (int r = 1; r * OW <= 256; ++r)
+    if ((r * OW) % 32 == 0) best = r;
+  (void)OH;
+  return best;
+}
+
+}  // namespace
+
+// Scratch bytes of the tensor-core path, or 0 when the shape does not take it.
+size_t conv_tc_workspace(int64_t N, int64_t C, int64_t H, int64_t W, int64_t M, int64_t Cg, int64_t kH, int64_t kW,
+                         int64_t OH, int64_t OW, int64_t group, int64_t sh, int64_t sw, int64_t dh, int64_t dw) {
+  if (group != 1 || sh != 1 || sw != 1 || dh != 1 || dw != 1 || Cg != C) return 0;
+  const char* f = getenv("I8Q_FORCE_CONV");
+  if (f && std::string(f) == "direct") return 0;
+  const int R = pick_rows(OW, OH);
+  if (R == 0 || R * OW != 224) return 0;  // the tile width instantiated
+  if (OW > W || C > 65536 || M > 65535 || N > 65535) return 0;
+  const int64_t Cp = round_up(C, 64);
+  return a256((size_t)(N * H * W * Cp * 2)) + a256((size_t)(M * kH * kW * Cp * 2));
+}
+
+int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, int64_t W, float x_scale, int x_zp,
+                   const void* w, int wtype, int64_t M, int64_t kH, int64_t kW, const float* w_scale,
+                   const void* w_zp, int per_channel, float y_scale, int y_zp, int ytype, const int32_t* B,
+                   int64_t pt, int64_t pl, int64_t OH, int64_t OW, void* y, void* workspace, cudaStream_t s) {
+  const int R = pick_rows(OW, OH);
+  const int64_t Cp = round_up(C, 64);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* xc = reinterpret_cast<__nv_bfloat16*>(ws);
+  __nv_bfloat16* wc = reinterpret_cast<__nv_bfloat16*>(ws + a256((size_t)(N * H * W * Cp * 2)));
+  const int taps = (int)(kH * kW);
+  uint32_t* status = device_status_word();
+  if (!status) return fail(I8Q_ERR_CUDA, "qlinearconv: no device status word");
+  {
+    I8Q_PROF("conv_center_operands", s);
+    dim3 gx((unsigned)(Cp / 64), (unsigned)H, (unsigned)N);
+    if (xtype == I8Q_U8)
+      center_x_nhwc<uint8_t><<<gx, 256, 0, s>>>((const uint8_t*)x, (int)C, (int)H, (int)W, (int)Cp, x_zp, xc);
+    else
+      center_x_nhwc<int8_t><<<gx, 256, 0, s>>>((const int8_t*)x, (int)C, (int)H, (int)W, (int)Cp, x_zp, xc);
+    const int64_t tw = M * taps * Cp;
+    const int gw = (int)std::min<int64_t>(ceil_div(tw, 256), (int64_t)sm_count() * 8);
+    if (wtype == I8Q_U8)
+      center_w<uint8_t><<<gw, 256, 0, s>>>((const uint8_t*)w, (const uint8_t*)w_zp, per_channel, (int)M, (int)C, taps,
+                                           (int)Cp, wc);
+    else
+      center_w<int8_t><<<gw, 256, 0, s>>>((const int8_t*)w, (const int8_t*)w_zp, per_channel, (int)M, (int)C, taps,
+                                          (int)Cp, wc);
+    I8Q_LAUNCH_CHECK("conv operand centering");
+  }
+  CUtensorMap mW, mX;
+  int rc = make_map_2d(&mW, wc, M, (int64_t)taps * Cp, BM, "qlinearconv");
+  if (rc) return rc;
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)Cp, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
+    cuuint64_t strides[3] = {(cuuint64_t)(Cp * 2), (cuuint64_t)(W * Cp * 2), (cuuint64_t)(H * W * Cp * 2)};
+    cuuint32_t box[4] = {64u, (cuuint32_t)OW, (cuuint32_t)R, 1u};
+    rc = make_tensor_map(&mX, xc, 4, dims, strides, box, "qlinearconv");
+    if (rc) return rc;
+  }
+  // |xc| <= max distance of x_zp to its type's ends; |wc| <= 255
+  const int xmax = xtype == I8Q_U8 ? std::max(x_zp, 255 - x_zp) : std::max(x_zp + 128, 127 - x_zp);
+  int log2b = 0;
+  while ((int64_t(1) << log2b) < (int64_t)xmax * 255) ++log2b;
+  const int CS = (int)std::max<int64_t>(1, ((int64_t(1) << 24) >> log2b) / BK);
+  constexpr int TN = 224;
+  using T = ConvTile<TN>;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(conv_tc_kernel<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(conv_tc_kernel)");
+  ConvParams p;
+  p.M = (int)M;
+  p.CC = (int)(Cp / 64);
+  p.taps = taps;
+  p.kW = (int)kW;
+  p.pt = (int)pt;
+  p.pl = (int)pl;
+  p.OH = (int)OH;
+  p.OW = (int)OW;
+  p.R = R;
+  p.NB = (int)N;
+  p.tiles_m = (int)ceil_div(M, BM);
+  p.row_groups = (int)ceil_div(OH, R);
+  p.num_tiles = p.tiles_m * p.row_groups * (int)N;
+  p.KT = taps * p.CC;
+  p.CS = CS;
+  p.x_scale = x_scale;
+  p.y_scale = y_scale;
+  const float qlo = ytype == I8Q_U8 ? 0.0f : -128.0f, qhi = ytype == I8Q_U8 ? 255.0f : 127.0f;
+  p.qlo_z = qlo - (float)y_zp;
+  p.qhi_z = qhi - (float)y_zp;
+  p.y_zp = y_zp;
+  p.bias = B;
+  p.w_scale = w_scale;
+  p.per_channel = per_channel;
+  p.y = static_cast<uint8_t*>(y);
+  p.status = status;
+  const int grid = std::min(p.num_tiles, sm_count());
+  I8Q_PROF("qlinearconv_tc", s);
+  conv_tc_kernel<TN><<<grid, THREADS, T::SMEM_BYTES, s>>>(mW, mX, p);
+  I8Q_LAUNCH_CHECK("conv_tc_kernel");
+  return I8Q_OK;
+}
+
+}  // namespace i8q

@@ -77,6 +77,52 @@ def test_shapes_and_types(orc, dev, case, types):
              dil, group, ytype=types[2])
 
 
+TC_CASES = [
+    # N, C, H, W, M, k, pads: output rows that tile into 224-pixel tiles
+    (2, 64, 14, 14, 130, 3, (1, 1, 1, 1)),   # OW 14: 16 rows per tile > OH (partial), M tail
+    (1, 72, 10, 28, 40, 3, (1, 1, 1, 1)),    # C not a multiple of 64, OW 28
+    (2, 32, 7, 56, 96, 1, (0, 0, 0, 0)),     # 1x1
+    (1, 16, 9, 56, 64, 5, (2, 2, 2, 2)),     # 5x5
+    (1, 8, 6, 58, 24, 3, (0, 0, 0, 0)),      # unpadded, OW 56 from W 58
+    (3, 128, 8, 56, 256, 3, (1, 1, 1, 1)),   # two output-channel tiles, partial row group
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES)
+@pytest.mark.parametrize("types", [("u8", "u8", "u8"), ("s8", "s8", "s8"), ("u8", "s8", "s8")])
+def test_tensor_core_path(orc, dev, case, types):
+    N, C, H, W, M, k, pads = case
+    rng = np.random.default_rng(N * 1000 + C + M + k)
+    dt = {"u8": (np.uint8, 0, 256), "s8": (np.int8, -128, 128)}
+    xt, wt, yt = (dt[t] for t in types)
+    x = rng.integers(xt[1], xt[2], (N, C, H, W)).astype(xt[0])
+    w = rng.integers(wt[1], wt[2], (M, C, k, k)).astype(wt[0])
+    ws = rng.uniform(0.001, 0.01, M).astype(np.float32)
+    wz = rng.integers(wt[1], wt[2], M)
+    B = rng.integers(-5000, 5001, M).astype(np.int32)
+    assert q.qlinearconv_workspace_size(x.shape, w.shape, pads) > 0, "shape should take the tensor-core path"
+    q.profile_enable(True)
+    run_conv(orc, dev, x, np.float32(0.0037), int(rng.integers(xt[1], xt[2])), w, ws, wz, np.float32(0.05),
+             int(rng.integers(yt[1], yt[2])), B, pads, ytype=types[2])
+    # extreme zero points: the widest centered range (|x - x_zp| up to 255)
+    run_conv(orc, dev, x, np.float32(0.02), xt[1], w, np.float32(0.004), wt[2] - 1, np.float32(0.3),
+             int(rng.integers(yt[1], yt[2])), None, pads, ytype=types[2])
+    prof = q.profile_collect()
+    q.profile_enable(False)
+    assert prof.get("qlinearconv_tc", (0,))[0] == 2
+
+
+def test_direct_path_forced(orc, dev, monkeypatch):
+    monkeypatch.setenv("I8Q_FORCE_CONV", "direct")
+    N, C, H, W, M, k, pads = TC_CASES[0]
+    rng = np.random.default_rng(3)
+    x = rng.integers(0, 256, (N, C, H, W)).astype(np.uint8)
+    w = rng.integers(0, 256, (M, C, k, k)).astype(np.uint8)
+    assert q.qlinearconv_workspace_size(x.shape, w.shape, pads) == 0
+    run_conv(orc, dev, x, np.float32(0.0037), 132, w, rng.uniform(0.001, 0.01, M).astype(np.float32),
+             rng.integers(100, 157, M), np.float32(0.05), 128, None, pads)
+
+
 def test_full_size_dense_sampled(orc, dev):
     """x [32,256,56,56], w [256,256,3,3]: the whole output on the GPU,
     compared for 2 images x 24 output channels (each output depends only on
