@@ -205,7 +205,7 @@ namespace {
 size_t a256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct BufLayout {
-  size_t uA, uA_bf16, scaleA, zeroA, iBt, iBt_bf16, scaleB, colsum, total;
+  size_t uA, uA_bf16, scaleA, zeroA, iBt, iBt_bf16, scaleB, colsum, colmax, total;
 };
 
 BufLayout buf_layout(const i8q_qgemm_ctx* c) {
@@ -225,6 +225,7 @@ BufLayout buf_layout(const i8q_qgemm_ctx* c) {
     L.iBt_bf16 = c->use_tc ? take(c->N * (size_t)c->Kp * 2) : 0;
     L.scaleB = take(c->N * 4);
     L.colsum = take(c->N * 4);
+    L.colmax = take(c->N * 4);
   }
   L.total = o;
   return L;
@@ -367,7 +368,8 @@ extern "C" int i8q_qgemm_dyn_set_params(i8q_qgemm_ctx* ctx, const void* weight, 
       return fail(I8Q_ERR_INVALID_ARG, "qgemm_dyn_set_params: scale is required for int8 B");
     const size_t wbytes = K * N * (ctx->typeB == I8Q_S8 ? 1 : 4);
     void* tmp = nullptr;
-    if (cudaMalloc(&tmp, wbytes) != cudaSuccess) {
+    // staging copy of the weight, then N words of column-max scratch
+    if (cudaMalloc(&tmp, a256(wbytes) + N * 4) != cudaSuccess) {
       cudaGetLastError();
       return fail(I8Q_ERR_ALLOC, "qgemm_dyn_set_params: staging allocation failed");
     }
@@ -382,7 +384,8 @@ extern "C" int i8q_qgemm_dyn_set_params(i8q_qgemm_ctx* ctx, const void* weight, 
           rc = cuda_fail(cudaGetLastError(), "cudaMemcpyAsync(scale)");
       } else {
         rc = launch_quantize_cols(tmp, I8Q_F32, (int64_t)K, (int64_t)N, ctx->avoid, ctx->iBt, ctx->iBt_bf16, ctx->Kp,
-                                  ctx->scaleB, ctx->colsum, s);
+                                  ctx->scaleB, ctx->colsum,
+                                  reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(tmp) + a256(wbytes)), s);
       }
     }
     cudaError_t e = cudaStreamSynchronize(s);
@@ -425,7 +428,8 @@ int forward_impl(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf, vo
     __nv_bfloat16* qb = ctx->use_tc ? reinterpret_cast<__nv_bfloat16*>(base + L.iBt_bf16) : nullptr;
     float* sb = reinterpret_cast<float*>(base + L.scaleB);
     int32_t* cs = reinterpret_cast<int32_t*>(base + L.colsum);
-    rc = launch_quantize_cols(B, ctx->typeB, K, N, ctx->avoid, q, qb, ctx->Kp, sb, cs, s);
+    rc = launch_quantize_cols(B, ctx->typeB, K, N, ctx->avoid, q, qb, ctx->Kp, sb, cs,
+                              reinterpret_cast<uint32_t*>(base + L.colmax), s);
     if (rc) return rc;
     iBt = q;
     iBt_bf16 = qb;

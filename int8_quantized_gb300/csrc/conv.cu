@@ -56,6 +56,120 @@ qlinearconv_direct(const XT* __restrict__ x, const WT* __restrict__ w, const flo
   y[(((int64_t)n * M + m) * OH + oh) * OW + ow] = (YT)(sat_rint(v, qlo - (float)y_zp, qhi - (float)y_zp) + y_zp);
 }
 
+// Depthwise form (group == C == M): one CTA per (image, channel) plane.  The
+// input plane is staged in shared memory as centred int16 (x - x_zp, with the
+// padding never read: out-of-range taps are skipped, i.e. real 0), the
+// plane's filter in registers, and every output of the plane computed from
+// shared memory, requantized and stored with consecutive threads on
+// consecutive outputs.
+template <typename XT, typename WT, typename YT>
+__global__ void __launch_bounds__(256)
+qlinearconv_depthwise_plane(const XT* __restrict__ x, const WT* __restrict__ w, const float* __restrict__ w_scale,
+                            const WT* __restrict__ w_zp, int per_channel, const int32_t* __restrict__ B, int C, int H,
+                            int W, int kH, int kW, int OH, int OW, int pt, int pl, int sh, int sw, int dh, int dw,
+                            float x_scale, int x_zp, float y_scale, int y_zp, float qlo, float qhi,
+                            YT* __restrict__ y) {
+  extern __shared__ int16_t plane[];  // H * W centred inputs
+  const int c = blockIdx.x % C, n = blockIdx.x / C;
+  const XT* xp = x + ((int64_t)n * C + c) * H * W;
+  const int HW = H * W;
+  // 16-byte loads where the plane is aligned (planes of a multiple of 16 bytes)
+  if ((reinterpret_cast<uintptr_t>(xp) & 15) == 0) {
+    const int nv = HW / 16;
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(xp) + v);
+      const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) plane[16 * v + e] = (int16_t)((int)(XT)((wd[e >> 2] >> (8 * (e & 3))) & 0xff) - x_zp);
+    }
+    for (int i = nv * 16 + threadIdx.x; i < HW; i += blockDim.x) plane[i] = (int16_t)((int)xp[i] - x_zp);
+  } else {
+    for (int i = threadIdx.x; i < HW; i += blockDim.x) plane[i] = (int16_t)((int)xp[i] - x_zp);
+  }
+  const int taps = kH * kW;
+  const int wz = (int)w_zp[per_channel ? c : 0];
+  __shared__ int wc[25];
+  if (threadIdx.x < taps) wc[threadIdx.x] = (int)w[(int64_t)c * taps + threadIdx.x] - wz;
+  const int32_t bc = B ? B[c] : 0;
+  const float mul = __fmul_rn(x_scale, w_scale[per_channel ? c : 0]);
+  const float lo_z = qlo - (float)y_zp, hi_z = qhi - (float)y_zp;
+  __syncthreads();
+  YT* yp = y + ((int64_t)n * C + c) * OH * OW;
+  const int OHW = OH * OW;
+  for (int o = threadIdx.x; o < OHW; o += blockDim.x) {
+    const int oh = o / OW, ow = o - oh * OW;
+    int32_t acc = 0;
+    for (int kh = 0; kh < kH; ++kh) {
+      const int ih = oh * sh - pt + kh * dh;
+      if (ih < 0 || ih >= H) continue;
+      for (int kw = 0; kw < kW; ++kw) {
+        const int iw = ow * sw - pl + kw * dw;
+        if (iw >= 0 && iw < W) acc += (int)plane[ih * W + iw] * wc[kh * kW + kw];
+      }
+    }
+    float v = __fmul_rn(__int2float_rn(acc + bc), mul);
+    v = __fdiv_rn(v, y_scale);
+    yp[o] = (YT)rint_code_bits(v, lo_z, hi_z, y_zp);
+  }
+}
+
+// Depthwise with a KxK filter, stride 1, dilation 1: the plane is staged with
+// a halo of zeros (centred zero = the padding value) so every tap reads
+// shared memory without a bounds check.  Shared layout: (H + 2P) rows of
+// (W + 2P) int16, P = the larger pad.
+template <typename XT, typename WT, typename YT, int KS>
+__global__ void __launch_bounds__(256)
+qlinearconv_depthwise_halo(const XT* __restrict__ x, const WT* __restrict__ w, const float* __restrict__ w_scale,
+                           const WT* __restrict__ w_zp, int per_channel, const int32_t* __restrict__ B, int C, int H,
+                           int W, int OH, int OW, int pt, int pl, int P, float x_scale, int x_zp, float y_scale,
+                           int y_zp, float qlo, float qhi, YT* __restrict__ y) {
+  extern __shared__ int16_t hp[];
+  const int c = blockIdx.x % C, n = blockIdx.x / C;
+  const int HP = H + 2 * P, WP = W + 2 * P;
+  const XT* xp = x + ((int64_t)n * C + c) * H * W;
+  for (int i = threadIdx.x; i < HP * WP; i += blockDim.x) hp[i] = 0;
+  __syncthreads();
+  const int HW = H * W;
+  if ((reinterpret_cast<uintptr_t>(xp) & 15) == 0 && (W & 15) == 0) {
+    for (int v = threadIdx.x; v < HW / 16; v += blockDim.x) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(xp) + v);
+      const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+      const int e0 = 16 * v, r = e0 / W, col = e0 - r * W;
+      int16_t* dst = hp + (r + P) * WP + col + P;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) dst[e] = (int16_t)((int)(XT)((wd[e >> 2] >> (8 * (e & 3))) & 0xff) - x_zp);
+    }
+  } else {
+    for (int i = threadIdx.x; i < HW; i += blockDim.x) {
+      const int r = i / W, col = i - r * W;
+      hp[(r + P) * WP + col + P] = (int16_t)((int)xp[i] - x_zp);
+    }
+  }
+  const int wz = (int)w_zp[per_channel ? c : 0];
+  int wc[KS * KS];
+#pragma unroll
+  for (int t = 0; t < KS * KS; ++t) wc[t] = (int)w[(int64_t)c * KS * KS + t] - wz;
+  const int32_t bc = B ? B[c] : 0;
+  const float mul = __fmul_rn(x_scale, w_scale[per_channel ? c : 0]);
+  const float lo_z = qlo - (float)y_zp, hi_z = qhi - (float)y_zp;
+  __syncthreads();
+  YT* yp = y + ((int64_t)n * C + c) * OH * OW;
+  // output (oh, ow) reads hp rows oh - pt + P + kh, columns ow - pl + P + kw
+  const int ro = P - pt, co = P - pl;
+  for (int oh = threadIdx.x / 32; oh < OH; oh += blockDim.x / 32)
+    for (int ow = threadIdx.x & 31; ow < OW; ow += 32) {
+      const int16_t* base = hp + (oh + ro) * WP + ow + co;
+      int32_t acc = 0;
+#pragma unroll
+      for (int kh = 0; kh < KS; ++kh)
+#pragma unroll
+        for (int kw = 0; kw < KS; ++kw) acc += (int)base[kh * WP + kw] * wc[kh * KS + kw];
+      float v = __fmul_rn(__int2float_rn(acc + bc), mul);
+      v = __fdiv_rn(v, y_scale);
+      yp[oh * OW + ow] = (YT)rint_code_bits(v, lo_z, hi_z, y_zp);
+    }
+}
+
 struct ConvShape {
   int64_t N, C, H, W, M, Cg, kH, kW, OH, OW;
   int64_t pt, pl, pb, pr, sh, sw, dh, dw, group;
@@ -91,6 +205,36 @@ int conv_shape(const int64_t* xs, const int64_t* ws, const int64_t* pads, const 
 template <typename XT, typename WT, typename YT>
 int run_direct(const ConvShape& s, const void* x, float x_scale, int x_zp, const void* w, const float* w_scale,
                const void* w_zp, int per_ch, float y_scale, int y_zp, const int32_t* B, void* y, cudaStream_t st) {
+  const float dq_lo = std::is_same<YT, uint8_t>::value ? 0.0f : -128.0f;
+  const float dq_hi = std::is_same<YT, uint8_t>::value ? 255.0f : 127.0f;
+  const int64_t P = std::max(std::max(s.pt, s.pb), std::max(s.pl, s.pr));
+  if (s.group == s.C && s.M == s.C && s.Cg == 1 && s.sh == 1 && s.sw == 1 && s.dh == 1 && s.dw == 1 &&
+      s.kH == s.kW && (s.kH == 3 || s.kH == 5) && (s.H + 2 * P) * (s.W + 2 * P) * 2 <= 160 * 1024) {
+    const size_t hsmem = (size_t)(s.H + 2 * P) * (s.W + 2 * P) * 2;
+    auto kern = s.kH == 3 ? qlinearconv_depthwise_halo<XT, WT, YT, 3> : qlinearconv_depthwise_halo<XT, WT, YT, 5>;
+    if (hsmem > 48 * 1024)
+      I8Q_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem));
+    I8Q_PROF("qlinearconv_depthwise", st);
+    kern<<<(unsigned)(s.N * s.C), 256, hsmem, st>>>((const XT*)x, (const WT*)w, w_scale, (const WT*)w_zp, per_ch, B,
+                                                    (int)s.C, (int)s.H, (int)s.W, (int)s.OH, (int)s.OW, (int)s.pt,
+                                                    (int)s.pl, (int)P, x_scale, x_zp, y_scale, y_zp, dq_lo, dq_hi,
+                                                    (YT*)y);
+    I8Q_LAUNCH_CHECK("qlinearconv_depthwise_halo");
+    return I8Q_OK;
+  }
+  if (s.group == s.C && s.M == s.C && s.Cg == 1 && s.kH * s.kW <= 25 && s.H * s.W * 2 <= 160 * 1024) {
+    auto kern = qlinearconv_depthwise_plane<XT, WT, YT>;
+    const size_t psmem = (size_t)s.H * s.W * 2;
+    if (psmem > 48 * 1024)
+      I8Q_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem));
+    I8Q_PROF("qlinearconv_depthwise", st);
+    kern<<<(unsigned)(s.N * s.C), 256, psmem, st>>>((const XT*)x, (const WT*)w, w_scale, (const WT*)w_zp, per_ch, B,
+                                                    (int)s.C, (int)s.H, (int)s.W, (int)s.kH, (int)s.kW, (int)s.OH,
+                                                    (int)s.OW, (int)s.pt, (int)s.pl, (int)s.sh, (int)s.sw, (int)s.dh,
+                                                    (int)s.dw, x_scale, x_zp, y_scale, y_zp, dq_lo, dq_hi, (YT*)y);
+    I8Q_LAUNCH_CHECK("qlinearconv_depthwise_plane");
+    return I8Q_OK;
+  }
   const int64_t taps = s.Cg * s.kH * s.kW;
   const size_t smem = (size_t)taps * sizeof(int);
   if (smem > 200 * 1024) return fail(I8Q_ERR_UNSUPPORTED, "qlinearconv: filter too large for shared memory");
@@ -99,7 +243,7 @@ int run_direct(const ConvShape& s, const void* x, float x_scale, int x_zp, const
   const float qlo = std::is_same<YT, uint8_t>::value ? 0.0f : -128.0f;
   const float qhi = std::is_same<YT, uint8_t>::value ? 255.0f : 127.0f;
   dim3 grid((unsigned)ceil_div(s.OH * s.OW, 256), (unsigned)s.M, (unsigned)s.N);
-  I8Q_PROF(s.group == s.C && s.Cg == 1 ? "qlinearconv_depthwise" : "qlinearconv_direct", st);
+  I8Q_PROF("qlinearconv_direct", st);
   kern<<<grid, 256, smem, st>>>((const XT*)x, (const WT*)w, w_scale, (const WT*)w_zp, per_ch, B, (int)s.C, (int)s.H,
                                 (int)s.W, (int)s.M, (int)s.Cg, (int)(s.M / s.group), (int)s.kH, (int)s.kW, (int)s.OH,
                                 (int)s.OW, (int)s.pt, (int)s.pl, (int)s.sh, (int)s.sw, (int)s.dh, (int)s.dw, x_scale,

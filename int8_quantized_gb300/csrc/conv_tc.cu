@@ -319,6 +319,61 @@ center_x_nhwc(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __n
   }
 }
 
+// Same result, one CTA per (n, h): the whole NHWC row xc[n][h][:][:] is
+// W * Cp * 2 contiguous bytes.  Inputs land in shared memory as [w][c] with
+// a row stride of Cp + 2 halfwords (consecutive w fall in consecutive banks),
+// then leave in 16-byte pieces of the contiguous output row.
+template <typename XT>
+__global__ void __launch_bounds__(256)
+center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv_bfloat16* __restrict__ xc) {
+  extern __shared__ uint16_t rowt[];  // W x (Cp + 2)
+  const int n = blockIdx.y, h = blockIdx.x;
+  const int ld = Cp + 2;
+  const XT* xr = x + ((int64_t)n * C * H + h) * W;  // + c * H * W + w
+  if ((W & 7) == 0 && ((int64_t)H * W) % 8 == 0 && (reinterpret_cast<uintptr_t>(xr) & 7) == 0) {
+    // 8-byte pieces of the channel rows, eight loads in flight per thread
+    const int cw = W / 8, total = Cp * cw;
+    for (int base = 0; base < total; base += 8 * blockDim.x) {
+      uint2 v[8];
+      int cc[8], ww[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int idx = base + threadIdx.x + u * blockDim.x;
+        cc[u] = idx < total ? idx / cw : Cp;
+        ww[u] = (idx - cc[u] * cw) * 8;
+        v[u] = (idx < total && cc[u] < C) ? __ldg(reinterpret_cast<const uint2*>(xr + (int64_t)cc[u] * H * W + ww[u]))
+                                          : make_uint2(0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (cc[u] >= Cp) continue;
+        const uint32_t wd[2] = {v[u].x, v[u].y};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float f = cc[u] < C ? (float)((int)(XT)((wd[e >> 2] >> (8 * (e & 3))) & 0xff) - xz) : 0.0f;
+          rowt[(ww[u] + e) * ld + cc[u]] = (uint16_t)(__float_as_uint(f) >> 16);  // exact: |f| <= 255
+        }
+      }
+    }
+  } else {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    for (int c = warp; c < Cp; c += nwarps)
+      for (int w = lane; w < W; w += 32) {
+        float v = 0.0f;
+        if (c < C) v = (float)((int)xr[(int64_t)c * H * W + w] - xz);
+        rowt[w * ld + c] = (uint16_t)(__float_as_uint(v) >> 16);  // exact: |v| <= 255
+      }
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(xc + ((int64_t)n * H + h) * W * Cp);
+  const int per_w = Cp / 8;
+  for (int qi = threadIdx.x; qi < W * per_w; qi += blockDim.x) {
+    const int w = qi / per_w, c8 = (qi - w * per_w) * 8;
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(rowt + w * ld + c8);
+    dst[qi] = make_uint4(src[0], src[1], src[2], src[3]);
+  }
+}
+
 // wc[m][kh][kw][c] = w[m][c][kh][kw] - wz[m] (bf16), zero for c >= C.
 template <typename WT>
 __global__ void center_w(const WT* __restrict__ w, const WT* __restrict__ wz, int per_channel, int M, int C, int taps,
@@ -375,11 +430,29 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
   if (!status) return fail(I8Q_ERR_CUDA, "qlinearconv: no device status word");
   {
     I8Q_PROF("conv_center_operands", s);
-    dim3 gx((unsigned)(Cp / 64), (unsigned)H, (unsigned)N);
-    if (xtype == I8Q_U8)
-      center_x_nhwc<uint8_t><<<gx, 256, 0, s>>>((const uint8_t*)x, (int)C, (int)H, (int)W, (int)Cp, x_zp, xc);
-    else
-      center_x_nhwc<int8_t><<<gx, 256, 0, s>>>((const int8_t*)x, (int)C, (int)H, (int)W, (int)Cp, x_zp, xc);
+    const size_t row_smem = (size_t)W * (Cp + 2) * 2;
+    if (row_smem <= 200 * 1024) {
+      static std::once_flag once_u8, once_s8;
+      if (xtype == I8Q_U8) {
+        std::call_once(once_u8, [] {
+          cudaFuncSetAttribute(center_x_row<uint8_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        });
+        center_x_row<uint8_t><<<dim3((unsigned)H, (unsigned)N), 256, row_smem, s>>>((const uint8_t*)x, (int)C, (int)H,
+                                                                                   (int)W, (int)Cp, x_zp, xc);
+      } else {
+        std::call_once(once_s8, [] {
+          cudaFuncSetAttribute(center_x_row<int8_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        });
+        center_x_row<int8_t><<<dim3((unsigned)H, (unsigned)N), 256, row_smem, s>>>((const int8_t*)x, (int)C, (int)H,
+                                                                                 (int)W, (int)Cp, x_zp, xc);
+      }
+    } else {
+      dim3 gx((unsigned)(Cp / 64), (unsigned)H, (unsigned)N);
+      if (xtype == I8Q_U8)
+        center_x_nhwc<uint8_t><<<gx, 256, 0, s>>>((const uint8_t*)x, (int)C, (int)H, (int)W, (int)Cp, x_zp, xc);
+      else
+        center_x_nhwc<int8_t><<<gx, 256, 0, s>>>((const int8_t*)x, (int)C, (int)H, (int)W, (int)Cp, x_zp, xc);
+    }
     const int64_t tw = M * taps * Cp;
     const int gw = (int)std::min<int64_t>(ceil_div(tw, 256), (int64_t)sm_count() * 8);
     if (wtype == I8Q_U8)

@@ -331,6 +331,135 @@ cols_kernel(const T* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int qmin
   }
 }
 
+// ---- columns, two wide passes ---------------------------------------------
+// Each lane owns 4 consecutive columns, so a warp reads 128 columns of one
+// row per access (512 B of fp32, 256 B of bf16).  Pass 1 folds max|B| per
+// column over a K range and merges it with atomicMax on the bit pattern
+// (non-negative floats order like their bits).  Pass 2 quantizes 64-row
+// tiles, transposes them through shared memory into the K-contiguous
+// outputs and merges partial column sums with atomicAdd.
+constexpr int kWideCols = 128, kWideKT = 64, kWideKSplit = 512;
+
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 a = __ldcs(reinterpret_cast<const uint2*>(p));
+  v[0] = __uint_as_float(a.x << 16);
+  v[1] = __uint_as_float(a.x & 0xffff0000u);
+  v[2] = __uint_as_float(a.y << 16);
+  v[3] = __uint_as_float(a.y & 0xffff0000u);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+col_absmax_wide(const T* __restrict__ B, int64_t K, int64_t N, uint32_t* __restrict__ colmax) {
+  __shared__ float red[8][kWideCols];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t j = (int64_t)blockIdx.x * kWideCols + 4 * lane;
+  const int64_t k_end = std::min<int64_t>(K, (int64_t)(blockIdx.y + 1) * kWideKSplit);
+  float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (j < N)
+#pragma unroll 8
+    for (int64_t k = (int64_t)blockIdx.y * kWideKSplit + warp; k < k_end; k += 8) {
+      float v[4];
+      load4(B + k * N + j, v);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) m[u] = fmaxf(m[u], fabsf(v[u]));
+    }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) red[warp][4 * lane + u] = m[u];
+  __syncthreads();
+  if (threadIdx.x < kWideCols) {
+    float r = red[0][threadIdx.x];
+    for (int w = 1; w < 8; ++w) r = fmaxf(r, red[w][threadIdx.x]);
+    const int64_t jj = (int64_t)blockIdx.x * kWideCols + threadIdx.x;
+    if (jj < N) atomicMax(colmax + jj, __float_as_uint(r));
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+col_quant_wide(const T* __restrict__ B, int64_t K, int64_t N, int64_t Kp, const uint32_t* __restrict__ colmax,
+               int qmin, int qmax, int8_t* __restrict__ iBt, __nv_bfloat16* __restrict__ iBt_bf16,
+               float* __restrict__ scaleB, int32_t* __restrict__ colsum) {
+  __shared__ int8_t tile[kWideCols][kWideKT + 16];
+  __shared__ int sums[8][kWideCols];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t j0 = (int64_t)blockIdx.x * kWideCols;
+  const int64_t j = j0 + 4 * lane;
+  const bool jok = j < N;
+  float s[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    float sv = jok ? __fdiv_rn(__uint_as_float(colmax[j + u]), (float)qmax) : 1.0f;
+    s[u] = sv == 0.0f ? 1.0f : sv;
+  }
+  if (blockIdx.y == 0 && warp == 0 && jok) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) scaleB[j + u] = s[u];
+  }
+  int sum[4] = {0, 0, 0, 0};
+  const int64_t kbeg = (int64_t)blockIdx.y * kWideKSplit;
+  const int64_t kend = std::min<int64_t>(Kp, kbeg + kWideKSplit);
+  for (int64_t k0 = kbeg; k0 < kend; k0 += kWideKT) {
+#pragma unroll
+    for (int r = 0; r < kWideKT / 8; ++r) {
+      const int kk = warp + 8 * r;
+      const int64_t k = k0 + kk;
+      int code[4] = {0, 0, 0, 0};
+      if (jok && k < K) {
+        float v[4];
+        load4(B + k * N + j, v);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          code[u] = sat_rint(__fdiv_rn(v[u], s[u]), (float)qmin, (float)qmax);
+          sum[u] += code[u];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) tile[4 * lane + u][kk] = (int8_t)code[u];
+    }
+    __syncthreads();
+    // each thread writes half of one column's 64 codes (32 B) and their bf16 copies (64 B)
+    const int c = threadIdx.x >> 1, h = threadIdx.x & 1;
+    const int64_t jj = j0 + c;
+    if (jj < N) {
+      const int8_t* src = &tile[c][h * 32];
+      uint32_t wds[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        wds[q] = (uint32_t)(uint8_t)src[4 * q] | ((uint32_t)(uint8_t)src[4 * q + 1] << 8) |
+                 ((uint32_t)(uint8_t)src[4 * q + 2] << 16) | ((uint32_t)(uint8_t)src[4 * q + 3] << 24);
+      uint4* dst = reinterpret_cast<uint4*>(iBt + jj * Kp + k0 + h * 32);
+      dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+      dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+      if (iBt_bf16) {
+        uint4* db = reinterpret_cast<uint4*>(iBt_bf16 + jj * Kp + k0 + h * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            pk[e] = code_bf16_bits(src[8 * q + 2 * e]) | (code_bf16_bits(src[8 * q + 2 * e + 1]) << 16);
+          db[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) sums[warp][4 * lane + u] = sum[u];
+  __syncthreads();
+  if (threadIdx.x < kWideCols) {
+    int t = 0;
+    for (int w = 0; w < 8; ++w) t += sums[w][threadIdx.x];
+    const int64_t jj = j0 + threadIdx.x;
+    if (jj < N) atomicAdd(colsum + jj, t);
+  }
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -392,10 +521,29 @@ int launch_quantize_rows(const void* A, int typeA, int64_t M, int64_t K, int64_t
 }
 
 int launch_quantize_cols(const void* B, int typeB, int64_t K, int64_t N, int avoid_overflow, int8_t* iBt,
-                         __nv_bfloat16* iBt_bf16, int64_t Kp, float* scaleB, int32_t* colsum, cudaStream_t s) {
+                         __nv_bfloat16* iBt_bf16, int64_t Kp, float* scaleB, int32_t* colsum,
+                         uint32_t* colmax_scratch, cudaStream_t s) {
   if (N <= 0) return I8Q_OK;
   const int qmax = avoid_overflow ? 63 : 127, qmin = avoid_overflow ? -64 : -128;
   I8Q_PROF("quantize_cols", s);
+  if (colmax_scratch && N % 4 == 0 && aligned16(B)) {
+    I8Q_CUDA_TRY(cudaMemsetAsync(colmax_scratch, 0, (size_t)N * 4, s));
+    I8Q_CUDA_TRY(cudaMemsetAsync(colsum, 0, (size_t)N * 4, s));
+    dim3 g1((unsigned)ceil_div(N, kWideCols), (unsigned)ceil_div(K, kWideKSplit));
+    dim3 g2((unsigned)ceil_div(N, kWideCols), (unsigned)ceil_div(Kp, kWideKSplit));
+    if (typeB == I8Q_F32) {
+      const float* b = static_cast<const float*>(B);
+      col_absmax_wide<float><<<g1, 256, 0, s>>>(b, K, N, colmax_scratch);
+      col_quant_wide<float><<<g2, 256, 0, s>>>(b, K, N, Kp, colmax_scratch, qmin, qmax, iBt, iBt_bf16, scaleB, colsum);
+    } else {
+      const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(B);
+      col_absmax_wide<__nv_bfloat16><<<g1, 256, 0, s>>>(b, K, N, colmax_scratch);
+      col_quant_wide<__nv_bfloat16><<<g2, 256, 0, s>>>(b, K, N, Kp, colmax_scratch, qmin, qmax, iBt, iBt_bf16, scaleB,
+                                                       colsum);
+    }
+    I8Q_LAUNCH_CHECK("col_quant_wide");
+    return I8Q_OK;
+  }
   dim3 grid((unsigned)ceil_div(N, kColW));
   if (typeB == I8Q_F32)
     cols_kernel<float, 0><<<grid, 256, 0, s>>>(static_cast<const float*>(B), K, N, N, qmin, qmax, iBt, iBt_bf16, Kp,
