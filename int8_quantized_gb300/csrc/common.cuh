@@ -67,8 +67,6 @@ __device__ __forceinline__ int sat_rint(float v, float lo, float hi) {
   return __float2int_rz(r);
 }
 
-// GELU = x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt 2)), evaluated as
-// (0.5 * x) * erfc(-(x / sqrt 2)) so nothing cancels for negative x.
 // saturate(rint(q) + zp) as the low byte of the result, for lo_z = lo - zp
 // and hi_z = hi - zp (small integers, exact in fp32).  Clamping to integer
 // bounds commutes with rounding, so q is clamped first; adding 1.5 * 2^23
@@ -88,6 +86,8 @@ __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint3
   return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
+// GELU = x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt 2)), evaluated as
+// (0.5 * x) * erfc(-(x / sqrt 2)) so nothing cancels for negative x.
 __device__ __forceinline__ float gelu_erf(float x) {
   float t = __fmul_rn(x, 0.70710678118654752440f);
   float e = erfcf(-t);
@@ -168,6 +168,12 @@ int launch_quantize_cols(const void* B, int typeB, int64_t K, int64_t N, int avo
 // (N x Kp), optional iBt_bf16, and colsum[N].
 int launch_repack_cols_s8(const int8_t* B, int64_t K, int64_t N, int64_t ldb, int8_t* iBt,
                           __nv_bfloat16* iBt_bf16, int64_t Kp, int32_t* colsum, cudaStream_t s);
+
+// Same, with the columns of an iofc-ordered 4H-wide matrix (N == 4 * gates_H)
+// interleaved per hidden unit: column q*H + u becomes row 4u + q of iBt.
+int launch_repack_cols_s8_gates(const int8_t* B, int64_t K, int64_t N, int64_t ldb, int8_t* iBt,
+                                __nv_bfloat16* iBt_bf16, int64_t Kp, int32_t* colsum, int64_t gates_H,
+                                cudaStream_t s);
 
 // Output modes of the GEMM epilogue.
 enum OutMode : int {

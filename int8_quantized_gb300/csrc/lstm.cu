@@ -7,12 +7,21 @@
 // i, o, f gates, tanh for the cell candidate and the output); gate column
 // order i, o, f, c.  X and each step's hidden state are quantized per row to
 // uint8 exactly like A of the dynamic quantized inner product.
-//   input projection (all steps at once, both directions): Gx = X W[d]
+//   input projection (all steps at once): Gx = X W[d]
 //   per step t: Gh = h_{t-1} R[d]; g = ((Gx_t + Gh) + Wb) + Rb
 //               i, o, f = sigmoid(g); ct = tanh(g_c)
 //               c = f*c_{t-1} + i*ct;  h = o*tanh(c)
-// The reverse direction walks t = T-1 .. 0.  X is quantized once and shared
-// by both directions.
+// The reverse direction walks t = T-1 .. 0.
+//
+// Layout: the 4H gate columns of W, R, their scales and the biases are
+// interleaved per hidden unit (column q*H + u stored at 4u + q), so any
+// 64-column tile holds all four gates of 16 hidden units.  Then one kernel
+// per step does, for both directions at once, the recurrent integer product
+// of a 64-row x 64-column tile (uint8 h x int8 R on mma.sync, exact int32)
+// and the whole cell update in its epilogue.  The projection runs once over
+// all T * batch rows on the tensor-core GEMM; X is quantized once for both
+// directions.  Each step's new h is quantized per row (both directions in
+// one launch) for the next step.
 #include "common.cuh"
 
 namespace i8q {
@@ -20,8 +29,8 @@ namespace {
 
 struct LstmLayout {
   int64_t D, TB, Ip, Hp, H4;
-  size_t off_Wt, off_Wcs, off_Rt, off_Rcs, off_Wsc, off_Rsc, off_uX, off_sX, off_zX, off_Gx, off_uh, off_sh, off_zh,
-      off_Gh, off_h, off_c, total;
+  size_t off_Wt, off_Wtb, off_Wcs, off_Rt, off_Rcs, off_Wsc, off_Rsc, off_Wbi, off_Rbi, off_uX, off_uXc, off_sX,
+      off_zX, off_Gx, off_uh, off_sh, off_zh, off_h, off_c, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -40,29 +49,47 @@ LstmLayout lstm_layout(int64_t T, int64_t batch, int64_t input, int64_t hidden, 
     return at;
   };
   L.off_Wt = take((size_t)L.D * L.H4 * L.Ip);
+  L.off_Wtb = take((size_t)L.D * L.H4 * L.Ip * 2);
   L.off_Wcs = take((size_t)L.D * L.H4 * 4);
   L.off_Rt = take((size_t)L.D * L.H4 * L.Hp);
   L.off_Rcs = take((size_t)L.D * L.H4 * 4);
   L.off_Wsc = take((size_t)L.D * L.H4 * 4);
   L.off_Rsc = take((size_t)L.D * L.H4 * 4);
+  L.off_Wbi = take((size_t)L.D * L.H4 * 4);
+  L.off_Rbi = take((size_t)L.D * L.H4 * 4);
   L.off_uX = take((size_t)L.TB * L.Ip);
+  L.off_uXc = take((size_t)L.TB * L.Ip * 2);
   L.off_sX = take((size_t)L.TB * 4);
   L.off_zX = take((size_t)L.TB * 4);
   L.off_Gx = take((size_t)L.D * L.TB * L.H4 * 4);
   L.off_uh = take((size_t)L.D * batch * L.Hp);
   L.off_sh = take((size_t)L.D * batch * 4);
   L.off_zh = take((size_t)L.D * batch * 4);
-  L.off_Gh = take((size_t)L.D * batch * L.H4 * 4);
-  L.off_h = take((size_t)L.D * 2 * batch * hidden * 4);
+  L.off_h = take((size_t)2 * L.D * batch * hidden * 4);
   L.off_c = take((size_t)L.D * batch * hidden * 4);
   L.total = o;
   return L;
 }
 
-// Expand per-direction scales (n == D) or copy per-channel scales (n == D*4H).
-__global__ void expand_scales(const float* __restrict__ src, int64_t n, int64_t D, int64_t H4, float* __restrict__ dst) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < D * H4; i += (int64_t)gridDim.x * blockDim.x)
-    dst[i] = n == D ? src[i / H4] : src[i];
+// Per-direction (n == D) or per-channel (n == D*4H) scales, interleaved.
+__global__ void interleave_scales(const float* __restrict__ src, int64_t n, int64_t D, int64_t H,
+                                  float* __restrict__ dst) {
+  const int64_t H4 = 4 * H;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < D * H4; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t d = i / H4, jp = i % H4, u = jp / 4, q = jp % 4;
+    dst[i] = n == D ? src[d] : src[d * H4 + q * H + u];
+  }
+}
+
+// Wb, Rb halves of B [D, 8H], interleaved (zeros when B is absent).
+__global__ void interleave_bias(const float* __restrict__ B, int64_t D, int64_t H, float* __restrict__ Wbi,
+                                float* __restrict__ Rbi) {
+  const int64_t H4 = 4 * H;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < D * H4; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t d = i / H4, jp = i % H4, u = jp / 4, q = jp % 4;
+    Wbi[i] = B ? B[d * 2 * H4 + q * H + u] : 0.0f;
+    Rbi[i] = B ? B[d * 2 * H4 + H4 + q * H + u] : 0.0f;
+  }
 }
 
 __global__ void init_state(const float* __restrict__ h0, const float* __restrict__ c0, int64_t n, float* __restrict__ h,
@@ -70,37 +97,6 @@ __global__ void init_state(const float* __restrict__ h0, const float* __restrict
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     h[i] = h0 ? h0[i] : 0.0f;
     c[i] = c0 ? c0[i] : 0.0f;
-  }
-}
-
-__device__ __forceinline__ float sigmoid_f32(float x) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x))); }
-
-// One cell update for one direction: batch x H elements.  c_prev and c_out
-// may be the same buffer (each element is read, then written, by one thread).
-__global__ void lstm_cell_kernel(const float* __restrict__ Gx, const float* __restrict__ Gh,
-                                 const float* __restrict__ Wb, const float* __restrict__ Rb,
-                                 const float* c_prev, float* __restrict__ h_out, float* c_out,
-                                 float* __restrict__ Y, int64_t batch, int64_t H) {
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < batch * H; e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t b = e / H, u = e % H;
-    float g[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int64_t n = q * H + u;
-      float v = __fadd_rn(Gx[b * 4 * H + n], Gh[b * 4 * H + n]);
-      if (Wb) v = __fadd_rn(v, Wb[n]);
-      if (Rb) v = __fadd_rn(v, Rb[n]);
-      g[q] = v;
-    }
-    const float ig = sigmoid_f32(g[0]);
-    const float og = sigmoid_f32(g[1]);
-    const float fg = sigmoid_f32(g[2]);
-    const float ct = tanhf(g[3]);
-    const float c = __fadd_rn(__fmul_rn(fg, c_prev[e]), __fmul_rn(ig, ct));
-    const float h = __fmul_rn(og, tanhf(c));
-    c_out[e] = c;
-    h_out[e] = h;
-    if (Y) Y[e] = h;
   }
 }
 
@@ -114,8 +110,184 @@ __global__ void any_nonzero_s8(const int8_t* __restrict__ p, int64_t n, int* __r
     if (p[i] != 0) atomicOr(flag, 1);
 }
 
+__device__ __forceinline__ float sigmoid_f32(float x) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x))); }
+
+// ---- the fused step ------------------------------------------------------------
+constexpr int SB = 64, SN = 64, SK = 64, SSTAGES = 3, STHREADS = 128;
+constexpr int S_STAGE = (SB + SN) * SK;
+
+__device__ __forceinline__ uint32_t s_smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void s_cp_async16(uint32_t dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(bytes));
+}
+__device__ __forceinline__ void s_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void s_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+__device__ __forceinline__ void s_ldsm4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(a));
+}
+__device__ __forceinline__ void s_mma(int32_t (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ int s_swz(int r, int c) { return r * SK + ((c ^ ((r >> 1) & 3)) << 4); }
+
+struct StepParams {
+  const uint8_t* uh;   // [D*B, Hp] quantized h of the previous step
+  const float* sh;     // [D*B]
+  const int32_t* zh;   // [D*B]
+  const int8_t* Rt;    // [D, 4H, Hp] interleaved rows
+  const int32_t* Rcs;  // [D, 4H]
+  const float* Rsc;    // [D, 4H]
+  const float* Gx;     // [D, T*B, 4H] interleaved columns
+  const float* Wbi;    // [D, 4H]
+  const float* Rbi;    // [D, 4H]
+  float* c;            // [D, B, H] in place
+  float* h_next;       // [D, B, H]
+  float* Y;            // [T, D, B, H] or null
+  int step, T, B, H, Hp, D, direction;
+};
+
+// grid (4H/64, D, ceil(B/64)), 128 threads.
+__global__ void __launch_bounds__(STHREADS) lstm_step_kernel(StepParams p) {
+  __shared__ __align__(128) uint8_t smem[SSTAGES * S_STAGE];
+  __shared__ float gs[SB][SN + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int wm = warp >> 1, wn = warp & 1;
+  const int d = blockIdx.y, m0 = blockIdx.z * SB, n0 = blockIdx.x * SN;
+  const int H4 = 4 * p.H;
+  const int KT = p.Hp / SK;
+  const uint8_t* A = p.uh + (int64_t)d * p.B * p.Hp;
+  const int8_t* Bm = p.Rt + (int64_t)d * H4 * p.Hp;
+
+  auto load_stage = [&](int stage, int kt) {
+    uint8_t* sA = smem + stage * S_STAGE;
+    uint8_t* sB = sA + SB * SK;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int idx = tid + i * STHREADS;  // 0..255: row = idx/4, chunk = idx%4
+      const int r = idx >> 2, ch = idx & 3;
+      const int ga = m0 + r, gb = n0 + r;
+      const uint8_t* pa = A + (int64_t)(ga < p.B ? ga : p.B - 1) * p.Hp + kt * SK + ch * 16;
+      const int8_t* pb = Bm + (int64_t)(gb < H4 ? gb : H4 - 1) * p.Hp + kt * SK + ch * 16;
+      s_cp_async16(s_smem_u32(sA + s_swz(r, ch)), pa, ga < p.B ? 16 : 0);
+      s_cp_async16(s_smem_u32(sB + s_swz(r, ch)), pb, gb < H4 ? 16 : 0);
+    }
+  };
+
+  int32_t acc[2][4][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[i][j][q] = 0;
+
+#pragma unroll
+  for (int s = 0; s < SSTAGES - 1; ++s) {
+    if (s < KT) load_stage(s, s);
+    s_commit();
+  }
+  for (int kt = 0; kt < KT; ++kt) {
+    s_wait<SSTAGES - 2>();
+    __syncthreads();
+    {
+      const int nk = kt + SSTAGES - 1;
+      if (nk < KT) load_stage(nk % SSTAGES, nk);
+      s_commit();
+    }
+    const uint8_t* sA = smem + (kt % SSTAGES) * S_STAGE;
+    const uint8_t* sB = sA + SB * SK;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t af[2][4], bf[4][2];
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) {
+        const int r = wm * 32 + mi * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        s_ldsm4(s_smem_u32(sA + s_swz(r, kk * 2 + (lane >> 4))), af[mi][0], af[mi][1], af[mi][2], af[mi][3]);
+      }
+#pragma unroll
+      for (int nj = 0; nj < 2; ++nj) {
+        const int r = wn * 32 + nj * 16 + (lane & 7) + (lane >> 4) * 8;
+        s_ldsm4(s_smem_u32(sB + s_swz(r, kk * 2 + ((lane >> 3) & 1))), bf[2 * nj][0], bf[2 * nj][1], bf[2 * nj + 1][0],
+                bf[2 * nj + 1][1]);
+      }
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) s_mma(acc[mi][ni], af[mi], bf[ni][0], bf[ni][1]);
+    }
+  }
+  s_wait<0>();
+
+  // gate pre-activations of the tile: ((Gx + Gh) + Wb) + Rb
+  const bool rev = p.direction == I8Q_LSTM_REVERSE || (p.direction == I8Q_LSTM_BIDIRECTIONAL && d == 1);
+  const int t = rev ? p.T - 1 - p.step : p.step;
+  const int64_t TB = (int64_t)p.T * p.B;
+  const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+  for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = wm * 32 + mi * 16 + g + 8 * hh;
+      const int b = m0 + r;
+      if (b >= p.B) continue;
+      const float sH = __ldg(p.sh + d * p.B + b);
+      const int32_t zH = __ldg(p.zh + d * p.B + b);
+      const float* gx = p.Gx + ((int64_t)d * TB + (int64_t)t * p.B + b) * H4;
+#pragma unroll
+      for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int cc = wn * 32 + ni * 8 + 2 * t4 + e;
+          const int n = n0 + cc;
+          if (n >= H4) continue;
+          const int64_t dn = (int64_t)d * H4 + n;
+          const int32_t v = acc[mi][ni][2 * hh + e] - zH * __ldg(p.Rcs + dn);
+          float gh = __fmul_rn(__int2float_rn(v), sH);
+          gh = __fmul_rn(gh, __ldg(p.Rsc + dn));
+          float gg = __fadd_rn(__ldg(gx + n), gh);
+          gg = __fadd_rn(gg, __ldg(p.Wbi + dn));
+          gg = __fadd_rn(gg, __ldg(p.Rbi + dn));
+          gs[r][cc] = gg;
+        }
+    }
+  __syncthreads();
+
+  // cell update: 64 rows x 16 hidden units per tile
+  for (int pi = tid; pi < SB * (SN / 4); pi += STHREADS) {
+    const int r = pi >> 4, uu = pi & 15;
+    const int b = m0 + r, u = n0 / 4 + uu;
+    if (b >= p.B || u >= p.H) continue;
+    const float ig = sigmoid_f32(gs[r][4 * uu + 0]);
+    const float og = sigmoid_f32(gs[r][4 * uu + 1]);
+    const float fg = sigmoid_f32(gs[r][4 * uu + 2]);
+    const float ct = tanhf(gs[r][4 * uu + 3]);
+    const int64_t e = ((int64_t)d * p.B + b) * p.H + u;
+    const float cn = __fadd_rn(__fmul_rn(fg, p.c[e]), __fmul_rn(ig, ct));
+    const float hn = __fmul_rn(og, tanhf(cn));
+    p.c[e] = cn;
+    p.h_next[e] = hn;
+    if (p.Y) p.Y[(((int64_t)t * p.D + d) * p.B + b) * p.H + u] = hn;
+  }
+}
+
 int grid_for(int64_t n, int threads = 256) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n, threads), (int64_t)sm_count() * 8));
+}
+
+bool lstm_use_tc(int64_t rows, int64_t cols) {
+  const char* f = getenv("I8Q_FORCE_CORE");
+  if (f && std::string(f) == "imma") return false;
+  if (f && std::string(f) == "tc") return true;
+  return rows >= 128 && cols >= 256 && ((rows + 127) / 128) * ((cols + 255) / 256) >= 64;
 }
 
 }  // namespace
@@ -141,6 +313,7 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
     return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: bad direction");
   if (!X || !W || !R || !W_scale || !R_scale) return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: NULL tensor pointer");
   if (input > 65536 || hidden > 65536) return fail(I8Q_ERR_UNSUPPORTED, "dq_lstm: input/hidden > 65536");
+  if (T * batch > ((int64_t)1 << 31) - 1) return fail(I8Q_ERR_UNSUPPORTED, "dq_lstm: T * batch too large");
   const LstmLayout L = lstm_layout(T, batch, input, hidden, direction);
   if ((int64_t)n_wscale != L.D && (int64_t)n_wscale != L.D * L.H4)
     return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: W_scale must have D or D*4H entries");
@@ -151,27 +324,30 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
   cudaStream_t s = as_stream(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int8_t* Wt = (int8_t*)(ws + L.off_Wt);
+  __nv_bfloat16* Wtb = (__nv_bfloat16*)(ws + L.off_Wtb);
   int32_t* Wcs = (int32_t*)(ws + L.off_Wcs);
   int8_t* Rt = (int8_t*)(ws + L.off_Rt);
   int32_t* Rcs = (int32_t*)(ws + L.off_Rcs);
   float* Wsc = (float*)(ws + L.off_Wsc);
   float* Rsc = (float*)(ws + L.off_Rsc);
+  float* Wbi = (float*)(ws + L.off_Wbi);
+  float* Rbi = (float*)(ws + L.off_Rbi);
   uint8_t* uX = ws + L.off_uX;
+  __nv_bfloat16* uXc = (__nv_bfloat16*)(ws + L.off_uXc);
   float* sX = (float*)(ws + L.off_sX);
   int32_t* zX = (int32_t*)(ws + L.off_zX);
   float* Gx = (float*)(ws + L.off_Gx);
   uint8_t* uh = ws + L.off_uh;
   float* sh = (float*)(ws + L.off_sh);
   int32_t* zh = (int32_t*)(ws + L.off_zh);
-  float* Gh = (float*)(ws + L.off_Gh);
   float* hbuf = (float*)(ws + L.off_h);
   float* cbuf = (float*)(ws + L.off_c);
-  const int64_t H = hidden, BH = batch * hidden;
+  const int64_t H = hidden, BH = batch * hidden, DBH = L.D * BH;
 
   // Zero points must be zero (the only form this engine runs).  Checked on
   // the device, reported synchronously.
   if (W_zero_point || R_zero_point) {
-    int* flag = reinterpret_cast<int*>(Gh);  // scratch word, overwritten later
+    int* flag = reinterpret_cast<int*>(sh);  // scratch word, overwritten later
     I8Q_CUDA_TRY(cudaMemsetAsync(flag, 0, sizeof(int), s));
     if (W_zero_point) any_nonzero_s8<<<grid_for((int64_t)n_wscale), 256, 0, s>>>(W_zero_point, (int64_t)n_wscale, flag);
     if (R_zero_point) any_nonzero_s8<<<grid_for((int64_t)n_rscale), 256, 0, s>>>(R_zero_point, (int64_t)n_rscale, flag);
@@ -181,60 +357,75 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
     if (hflag) return fail(I8Q_ERR_UNSUPPORTED, "dq_lstm: nonzero W/R zero points are not supported");
   }
 
+  // weights: gate-interleaved K-major copies, column sums, scales, biases
+  const bool tc = lstm_use_tc(L.TB, L.H4);
   int rc;
   for (int64_t d = 0; d < L.D; ++d) {
-    rc = launch_repack_cols_s8(W + d * input * L.H4, input, L.H4, L.H4, Wt + d * L.H4 * L.Ip, nullptr, L.Ip,
-                               Wcs + d * L.H4, s);
+    rc = launch_repack_cols_s8_gates(W + d * input * L.H4, input, L.H4, L.H4, Wt + d * L.H4 * L.Ip,
+                                     tc ? Wtb + d * L.H4 * L.Ip : nullptr, L.Ip, Wcs + d * L.H4, H, s);
     if (rc) return rc;
-    rc = launch_repack_cols_s8(R + d * H * L.H4, H, L.H4, L.H4, Rt + d * L.H4 * L.Hp, nullptr, L.Hp, Rcs + d * L.H4, s);
+    rc = launch_repack_cols_s8_gates(R + d * H * L.H4, H, L.H4, L.H4, Rt + d * L.H4 * L.Hp, nullptr, L.Hp,
+                                     Rcs + d * L.H4, H, s);
     if (rc) return rc;
   }
-  expand_scales<<<grid_for(L.D * L.H4), 256, 0, s>>>(W_scale, (int64_t)n_wscale, L.D, L.H4, Wsc);
-  expand_scales<<<grid_for(L.D * L.H4), 256, 0, s>>>(R_scale, (int64_t)n_rscale, L.D, L.H4, Rsc);
-  I8Q_LAUNCH_CHECK("expand_scales");
+  interleave_scales<<<grid_for(L.D * L.H4), 256, 0, s>>>(W_scale, (int64_t)n_wscale, L.D, H, Wsc);
+  interleave_scales<<<grid_for(L.D * L.H4), 256, 0, s>>>(R_scale, (int64_t)n_rscale, L.D, H, Rsc);
+  interleave_bias<<<grid_for(L.D * L.H4), 256, 0, s>>>(Bias, L.D, H, Wbi, Rbi);
+  I8Q_LAUNCH_CHECK("lstm parameter layout");
 
   // input projection: X quantized once, one GEMM per direction
-  rc = launch_quantize_rows(X, I8Q_F32, L.TB, input, input, uX, nullptr, L.Ip, sX, zX, s);
+  rc = launch_quantize_rows(X, I8Q_F32, L.TB, input, input, uX, tc ? uXc : nullptr, L.Ip, sX, zX, s);
   if (rc) return rc;
   for (int64_t d = 0; d < L.D; ++d) {
     GemmEpilogue ep{zX, sX, Wcs + d * L.H4, Wsc + d * L.H4, nullptr, I8Q_ACT_IDENTITY, OUT_F32,
                     Gx + d * L.TB * L.H4, L.H4};
-    rc = launch_gemm_imma(uX, Wt + d * L.H4 * L.Ip, L.TB, L.H4, L.Ip, ep, s);
+    rc = I8Q_ERR_UNSUPPORTED;
+    if (tc) rc = launch_gemm_tc(uXc, Wtb + d * L.H4 * L.Ip, L.TB, L.H4, L.Ip, 14, ep, s);
+    if (rc == I8Q_ERR_UNSUPPORTED) rc = launch_gemm_imma(uX, Wt + d * L.H4 * L.Ip, L.TB, L.H4, L.Ip, ep, s);
     if (rc) return rc;
   }
 
-  for (int64_t d = 0; d < L.D; ++d)
-    init_state<<<grid_for(BH), 256, 0, s>>>(h0 ? h0 + d * BH : nullptr, c0 ? c0 + d * BH : nullptr, BH,
-                                             hbuf + d * 2 * BH, cbuf + d * BH);
+  // recurrence: both directions per launch
+  init_state<<<grid_for(DBH), 256, 0, s>>>(h0, c0, DBH, hbuf, cbuf);
   I8Q_LAUNCH_CHECK("init_state");
-
+  rc = launch_quantize_rows(hbuf, I8Q_F32, L.D * batch, H, H, uh, nullptr, L.Hp, sh, zh, s);
+  if (rc) return rc;
+  StepParams sp;
+  sp.uh = uh;
+  sp.sh = sh;
+  sp.zh = zh;
+  sp.Rt = Rt;
+  sp.Rcs = Rcs;
+  sp.Rsc = Rsc;
+  sp.Gx = Gx;
+  sp.Wbi = Wbi;
+  sp.Rbi = Rbi;
+  sp.c = cbuf;
+  sp.Y = Y;
+  sp.T = (int)T;
+  sp.B = (int)batch;
+  sp.H = (int)H;
+  sp.Hp = (int)L.Hp;
+  sp.D = (int)L.D;
+  sp.direction = direction;
+  const dim3 sgrid((unsigned)ceil_div(L.H4, SN), (unsigned)L.D, (unsigned)ceil_div(batch, SB));
   for (int64_t step = 0; step < T; ++step) {
-    for (int64_t d = 0; d < L.D; ++d) {
-      const bool rev = direction == I8Q_LSTM_REVERSE || (direction == I8Q_LSTM_BIDIRECTIONAL && d == 1);
-      const int64_t t = rev ? T - 1 - step : step;
-      float* h_prev = hbuf + d * 2 * BH + (step & 1) * BH;
-      float* h_next = hbuf + d * 2 * BH + ((step + 1) & 1) * BH;
-      rc = launch_quantize_rows(h_prev, I8Q_F32, batch, H, H, uh + d * batch * L.Hp, nullptr, L.Hp, sh + d * batch,
-                                zh + d * batch, s);
+    float* h_next = hbuf + ((step + 1) & 1) * DBH;
+    sp.step = (int)step;
+    sp.h_next = h_next;
+    {
+      I8Q_PROF("lstm_step", s);
+      lstm_step_kernel<<<sgrid, STHREADS, 0, s>>>(sp);
+      I8Q_LAUNCH_CHECK("lstm_step_kernel");
+    }
+    if (step + 1 < T) {
+      rc = launch_quantize_rows(h_next, I8Q_F32, L.D * batch, H, H, uh, nullptr, L.Hp, sh, zh, s);
       if (rc) return rc;
-      GemmEpilogue ep{zh + d * batch, sh + d * batch, Rcs + d * L.H4, Rsc + d * L.H4, nullptr, I8Q_ACT_IDENTITY,
-                      OUT_F32, Gh + d * batch * L.H4, L.H4};
-      rc = launch_gemm_imma(uh + d * batch * L.Hp, Rt + d * L.H4 * L.Hp, batch, L.H4, L.Hp, ep, s);
-      if (rc) return rc;
-      const float* Wb = Bias ? Bias + d * 8 * H : nullptr;
-      const float* Rb = Bias ? Bias + d * 8 * H + 4 * H : nullptr;
-      float* Yt = Y ? Y + (t * L.D + d) * BH : nullptr;
-      I8Q_PROF("lstm_cell", s);
-      lstm_cell_kernel<<<grid_for(BH), 256, 0, s>>>(Gx + d * L.TB * L.H4 + t * batch * L.H4, Gh + d * batch * L.H4, Wb,
-                                                    Rb, cbuf + d * BH, h_next, cbuf + d * BH, Yt, batch, H);
-      I8Q_LAUNCH_CHECK("lstm_cell_kernel");
     }
   }
-  for (int64_t d = 0; d < L.D; ++d) {
-    const float* h_last = hbuf + d * 2 * BH + (T & 1) * BH;
-    if (Y_h) copy_f32<<<grid_for(BH), 256, 0, s>>>(h_last, Y_h + d * BH, BH);
-    if (Y_c) copy_f32<<<grid_for(BH), 256, 0, s>>>(cbuf + d * BH, Y_c + d * BH, BH);
-  }
+  const float* h_last = hbuf + (T & 1) * DBH;
+  if (Y_h) copy_f32<<<grid_for(DBH), 256, 0, s>>>(h_last, Y_h, DBH);
+  if (Y_c) copy_f32<<<grid_for(DBH), 256, 0, s>>>(cbuf, Y_c, DBH);
   I8Q_LAUNCH_CHECK("copy_f32");
   return I8Q_OK;
 }

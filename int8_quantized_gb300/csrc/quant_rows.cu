@@ -251,11 +251,18 @@ quantize_rows_warp(const T* __restrict__ A, int64_t M, int64_t K, int64_t lda, u
 constexpr int kColW = 32;
 constexpr int kColKT = 64;
 
+// Destination row of column j: j itself, or, with gates_H > 0, the gate
+// interleaving 4 * (j % gates_H) + j / gates_H (column q*H + u of an
+// iofc-ordered 4H-wide matrix lands at 4u + q).
+__device__ __forceinline__ int64_t dest_row(int64_t j, int64_t gates_H) {
+  return gates_H > 0 ? 4 * (j % gates_H) + j / gates_H : j;
+}
+
 template <typename T, int MODE>  // MODE 0: quantize fp32/bf16 B; 1: repack int8 B
 __global__ void __launch_bounds__(256)
 cols_kernel(const T* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int qmin, int qmax,
             int8_t* __restrict__ iBt, __nv_bfloat16* __restrict__ iBt_bf16, int64_t Kp,
-            float* __restrict__ scaleB, int32_t* __restrict__ colsum) {
+            float* __restrict__ scaleB, int32_t* __restrict__ colsum, int64_t gates_H) {
   __shared__ float red[8][kColW];
   __shared__ float sh_scale[kColW];
   __shared__ int sh_sum[8][kColW];
@@ -304,20 +311,21 @@ cols_kernel(const T* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int qmin
     const int64_t jj = j0 + c;
     if (jj < N) {
       const int8_t* src = &tile[c][seg * 8];
+      const int64_t jd = dest_row(jj, gates_H);
       uint32_t w0 = 0, w1 = 0;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         w0 |= (uint32_t)(uint8_t)src[q] << (8 * q);
         w1 |= (uint32_t)(uint8_t)src[q + 4] << (8 * q);
       }
-      *reinterpret_cast<uint2*>(iBt + jj * Kp + k0 + seg * 8) = make_uint2(w0, w1);
+      *reinterpret_cast<uint2*>(iBt + jd * Kp + k0 + seg * 8) = make_uint2(w0, w1);
       if (iBt_bf16) {
         uint4 o;
         o.x = code_bf16_bits(src[0]) | (code_bf16_bits(src[1]) << 16);
         o.y = code_bf16_bits(src[2]) | (code_bf16_bits(src[3]) << 16);
         o.z = code_bf16_bits(src[4]) | (code_bf16_bits(src[5]) << 16);
         o.w = code_bf16_bits(src[6]) | (code_bf16_bits(src[7]) << 16);
-        *reinterpret_cast<uint4*>(iBt_bf16 + jj * Kp + k0 + seg * 8) = o;
+        *reinterpret_cast<uint4*>(iBt_bf16 + jd * Kp + k0 + seg * 8) = o;
       }
     }
     __syncthreads();
@@ -327,7 +335,7 @@ cols_kernel(const T* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int qmin
   if (warp == 0 && jok) {
     int t = 0;
     for (int w = 0; w < 8; ++w) t += sh_sum[w][lane];
-    colsum[j] = t;
+    colsum[dest_row(j, gates_H)] = t;
   }
 }
 
@@ -547,20 +555,26 @@ int launch_quantize_cols(const void* B, int typeB, int64_t K, int64_t N, int avo
   dim3 grid((unsigned)ceil_div(N, kColW));
   if (typeB == I8Q_F32)
     cols_kernel<float, 0><<<grid, 256, 0, s>>>(static_cast<const float*>(B), K, N, N, qmin, qmax, iBt, iBt_bf16, Kp,
-                                               scaleB, colsum);
+                                               scaleB, colsum, 0);
   else
     cols_kernel<__nv_bfloat16, 0><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(B), K, N, N, qmin, qmax,
-                                                       iBt, iBt_bf16, Kp, scaleB, colsum);
+                                                       iBt, iBt_bf16, Kp, scaleB, colsum, 0);
   I8Q_LAUNCH_CHECK("cols_kernel(quantize)");
   return I8Q_OK;
 }
 
 int launch_repack_cols_s8(const int8_t* B, int64_t K, int64_t N, int64_t ldb, int8_t* iBt, __nv_bfloat16* iBt_bf16,
                           int64_t Kp, int32_t* colsum, cudaStream_t s) {
+  return launch_repack_cols_s8_gates(B, K, N, ldb, iBt, iBt_bf16, Kp, colsum, 0, s);
+}
+
+int launch_repack_cols_s8_gates(const int8_t* B, int64_t K, int64_t N, int64_t ldb, int8_t* iBt,
+                                __nv_bfloat16* iBt_bf16, int64_t Kp, int32_t* colsum, int64_t gates_H, cudaStream_t s) {
   if (N <= 0) return I8Q_OK;
+  if (gates_H > 0 && N != 4 * gates_H) return fail(I8Q_ERR_INVALID_ARG, "repack: gate interleave needs N == 4H");
   dim3 grid((unsigned)ceil_div(N, kColW));
   I8Q_PROF("repack_cols", s);
-    cols_kernel<int8_t, 1><<<grid, 256, 0, s>>>(B, K, N, ldb, -128, 127, iBt, iBt_bf16, Kp, nullptr, colsum);
+  cols_kernel<int8_t, 1><<<grid, 256, 0, s>>>(B, K, N, ldb, -128, 127, iBt, iBt_bf16, Kp, nullptr, colsum, gates_H);
   I8Q_LAUNCH_CHECK("cols_kernel(repack)");
   return I8Q_OK;
 }
