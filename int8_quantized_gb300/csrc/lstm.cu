@@ -22,15 +22,19 @@
 // all T * batch rows on the tensor-core GEMM; X is quantized once for both
 // directions.  Each step's new h is quantized per row (both directions in
 // one launch) for the next step.
-#include "common.cuh"
+#include <cstring>
+#include <functional>
+#include <mutex>
+
+#include "tcgen05.cuh"
 
 namespace i8q {
 namespace {
 
 struct LstmLayout {
   int64_t D, TB, Ip, Hp, H4;
-  size_t off_Wt, off_Wtb, off_Wcs, off_Rt, off_Rcs, off_Wsc, off_Rsc, off_Wbi, off_Rbi, off_uX, off_uXc, off_sX,
-      off_zX, off_Gx, off_uh, off_sh, off_zh, off_h, off_c, total;
+  size_t off_Wt, off_Wtb, off_Wcs, off_Rt, off_Rtb, off_Rcs, off_Wsc, off_Rsc, off_Wbi, off_Rbi, off_uX, off_uXc,
+      off_sX, off_zX, off_Gx, off_uh, off_uhc, off_sh, off_zh, off_h, off_c, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -52,6 +56,7 @@ LstmLayout lstm_layout(int64_t T, int64_t batch, int64_t input, int64_t hidden, 
   L.off_Wtb = take((size_t)L.D * L.H4 * L.Ip * 2);
   L.off_Wcs = take((size_t)L.D * L.H4 * 4);
   L.off_Rt = take((size_t)L.D * L.H4 * L.Hp);
+  L.off_Rtb = take((size_t)L.D * L.H4 * L.Hp * 2);
   L.off_Rcs = take((size_t)L.D * L.H4 * 4);
   L.off_Wsc = take((size_t)L.D * L.H4 * 4);
   L.off_Rsc = take((size_t)L.D * L.H4 * 4);
@@ -63,6 +68,7 @@ LstmLayout lstm_layout(int64_t T, int64_t batch, int64_t input, int64_t hidden, 
   L.off_zX = take((size_t)L.TB * 4);
   L.off_Gx = take((size_t)L.D * L.TB * L.H4 * 4);
   L.off_uh = take((size_t)L.D * batch * L.Hp);
+  L.off_uhc = take((size_t)L.D * batch * L.Hp * 2);
   L.off_sh = take((size_t)L.D * batch * 4);
   L.off_zh = take((size_t)L.D * batch * 4);
   L.off_h = take((size_t)2 * L.D * batch * hidden * 4);
@@ -279,6 +285,207 @@ __global__ void __launch_bounds__(STHREADS) lstm_step_kernel(StepParams p) {
   }
 }
 
+// ---- the fused step on the tensor pipe ----------------------------------------
+// The same step with the recurrent product on tcgen05 (bf16 operands holding
+// exact integer codes, fp32 accumulation exact within chunks of 2^24 / 2^14
+// = 1024 K-elements, drained into int32 registers).  Orientation: M = 128
+// gate rows of R (rows 4u + q), N = 64 batch rows of h, so TMEM lane r holds
+// gate row r for 64 batch columns; the four gates of unit u sit in four
+// consecutive lanes of one warp and meet through warp shuffles.
+// Warps: 0 = TMA producer, 1 = TMEM owner and MMA issuer, 2..5 = drain and
+// cell update (warp w reads TMEM lanes 32 * (w % 4) ..).
+namespace tcs {
+using namespace tc;
+constexpr int BM = 128, BN = 64, BK = 64, STAGES = 4, EPI_WARPS = 8, THREADS = 64 + 32 * EPI_WARPS, TMEM_COLS = 64;
+constexpr int HALF = BN / 2;  // batch columns per epilogue warp
+constexpr int A_STAGE = BM * BK * 2, B_STAGE = BN * BK * 2, STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int NUM_BARS = 2 * STAGES + 2;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+constexpr uint32_t ST_TIMEOUT = 1u << 8;
+
+struct TcStepParams {
+  const float* sh;     // [D*B]
+  const int32_t* zh;   // [D*B]
+  const int32_t* Rcs;  // [D, 4H]
+  const float* Rsc;    // [D, 4H]
+  const float* Gx;     // [D, T*B, 4H]
+  const float* Wbi;    // [D, 4H]
+  const float* Rbi;    // [D, 4H]
+  float* c;            // [D, B, H]
+  float* h_next;       // [D, B, H]
+  float* Y;            // [T, D, B, H] or null
+  int step, T, B, H, Hp, D, direction, CS;
+  uint32_t* status;
+};
+
+// grid (ceil(4H/128), D, ceil(B/64))
+__global__ void __launch_bounds__(THREADS, 1)
+lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmH, TcStepParams p) {
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t smem0 = smem_u32(smem);
+  auto sA = [&](int s) { return smem0 + (uint32_t)(s * STAGE_BYTES); };
+  auto sB = [&](int s) { return smem0 + (uint32_t)(s * STAGE_BYTES + A_STAGE); };
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  const uint32_t accf = smem_u32(bars + 2 * STAGES), acce = smem_u32(bars + 2 * STAGES + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = blockIdx.y, mt = blockIdx.x, nb = blockIdx.z;
+  const int H4 = 4 * p.H;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, EPI_WARPS);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int KT = p.Hp / BK, CS = p.CS;
+  const int nchunks = (KT + CS - 1) / CS;
+  if (warp == 0) {
+    if (lane == 0) {
+      int kt = 0;
+      for (; kt < KT; ++kt) {
+        const int s = kt % STAGES;
+        if (!wait_bar(empty(s), ((uint32_t)(kt / STAGES) & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT)) break;
+        mbar_arrive_expect_tx(full(s), STAGE_BYTES);
+        tma_load_2d(sA(s), &tmR, full(s), kt * BK, d * H4 + mt * BM);
+        tma_load_2d(sB(s), &tmH, full(s), kt * BK, d * p.B + nb * BN);
+      }
+      if (kt < KT)
+        for (int j = max(0, kt - STAGES); j < kt; ++j) {
+          unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(full(j % STAGES), (uint32_t)(j / STAGES) & 1u))
+            if (global_ns() - t0 > WAIT_LIMIT_NS) break;
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int chunk = 0;
+      for (int kt = 0; kt < KT; ++kt) {
+        const int kc = kt % CS;
+        if (kc == 0) {
+          if (!wait_bar(acce, ((uint32_t)chunk & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT)) break;
+          tc_fence_after();
+        }
+        const int s = kt % STAGES;
+        if (!wait_bar(full(s), (uint32_t)(kt / STAGES) & 1u, abort_flag, p.status, ST_TIMEOUT)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          tc_mma(tmem, desc_sw128(sA(s) + (uint32_t)(k * 32)), desc_sw128(sB(s) + (uint32_t)(k * 32)), IDESC,
+                 (kc == 0 && k == 0) ? 0u : 1u);
+        tc_commit(empty(s));
+        if (kc == CS - 1 || kt == KT - 1) {
+          tc_commit(accf);
+          ++chunk;
+        }
+      }
+    }
+  } else {
+    const int q4 = warp & 3;                     // TMEM lane quadrant
+    const int half = (warp - 2) >> 2;            // which 32 of the 64 batch columns
+    const int r = q4 * 32 + lane;                // gate row within the tile
+    const int n = mt * BM + r;                   // interleaved gate column 4u + q
+    const bool rev = p.direction == I8Q_LSTM_REVERSE || (p.direction == I8Q_LSTM_BIDIRECTIONAL && d == 1);
+    const int t = rev ? p.T - 1 - p.step : p.step;
+    const int64_t TB = (int64_t)p.T * p.B;
+    const bool nvalid = n < H4;
+    const int q = n & 3, u = n >> 2;
+    const int b0 = nb * BN + half * HALF;
+    // operands of the epilogue that do not depend on the product: fetched
+    // while the tensor core works
+    float gx[HALF], cprev[HALF];
+#pragma unroll
+    for (int j = 0; j < HALF; ++j) {
+      const int b = b0 + j;
+      const bool ok_b = b < p.B && nvalid;
+      gx[j] = ok_b ? __ldg(p.Gx + ((int64_t)d * TB + (int64_t)t * p.B + b) * H4 + n) : 0.0f;
+      cprev[j] = (ok_b && q == 0 && u < p.H) ? p.c[((int64_t)d * p.B + b) * p.H + u] : 0.0f;
+    }
+    int32_t run[HALF];
+#pragma unroll
+    for (int j = 0; j < HALF; ++j) run[j] = 0;
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      const bool got = wait_bar(accf, (uint32_t)c & 1u, abort_flag, p.status, ST_TIMEOUT);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t v0[16], v1[16];
+      tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(half * HALF), v0);
+      tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(half * HALF + 16), v1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        run[i] += __float2int_rn(__uint_as_float(v0[i]));
+        run[16 + i] += __float2int_rn(__uint_as_float(v1[i]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce);
+    }
+    if (ok) {
+      const int64_t dn = (int64_t)d * H4 + (nvalid ? n : 0);
+      const int32_t cs = nvalid ? __ldg(p.Rcs + dn) : 0;
+      const float rsc = nvalid ? __ldg(p.Rsc + dn) : 0.0f;
+      const float wb = nvalid ? __ldg(p.Wbi + dn) : 0.0f;
+      const float rb = nvalid ? __ldg(p.Rbi + dn) : 0.0f;
+      const int base_lane = lane & ~3;
+#pragma unroll
+      for (int j = 0; j < HALF; ++j) {
+        const int b = b0 + j;
+        const bool bvalid = b < p.B;
+        float act = 0.0f;
+        if (bvalid && nvalid) {
+          const float sH = __ldg(p.sh + d * p.B + b);
+          // h entered as uh - 128: sum_k (uh - zh) R = run - (zh - 128) colsum
+          const int32_t v = run[j] - (__ldg(p.zh + d * p.B + b) - 128) * cs;
+          float gh = __fmul_rn(__int2float_rn(v), sH);
+          gh = __fmul_rn(gh, rsc);
+          float gg = __fadd_rn(gx[j], gh);
+          gg = __fadd_rn(gg, wb);
+          gg = __fadd_rn(gg, rb);
+          act = q < 3 ? sigmoid_f32(gg) : tanhf(gg);
+        }
+        const float ig = __shfl_sync(0xffffffffu, act, base_lane + 0);
+        const float og = __shfl_sync(0xffffffffu, act, base_lane + 1);
+        const float fg = __shfl_sync(0xffffffffu, act, base_lane + 2);
+        const float ct = __shfl_sync(0xffffffffu, act, base_lane + 3);
+        if (q == 0 && bvalid && nvalid && u < p.H) {
+          const int64_t e = ((int64_t)d * p.B + b) * p.H + u;
+          const float cn = __fadd_rn(__fmul_rn(fg, cprev[j]), __fmul_rn(ig, ct));
+          const float hn = __fmul_rn(og, tanhf(cn));
+          p.c[e] = cn;
+          p.h_next[e] = hn;
+          if (p.Y) p.Y[(((int64_t)t * p.D + d) * p.B + b) * p.H + u] = hn;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+}  // namespace tcs
+
 int grid_for(int64_t n, int threads = 256) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n, threads), (int64_t)sm_count() * 8));
 }
@@ -291,6 +498,18 @@ bool lstm_use_tc(int64_t rows, int64_t cols) {
 }
 
 }  // namespace
+
+// The arguments that fix a captured recurrence (every field 8 bytes wide,
+// so the struct has no padding and compares with memcmp).
+struct LstmGraphKey {
+  const void *X, *W, *R, *W_scale, *R_scale, *Bias, *h0, *c0, *Y, *Y_h, *Y_c, *workspace;
+  int64_t T, batch, input, hidden, direction, n_wscale, n_rscale;
+};
+
+// Launch the recurrence as a CUDA graph on s: the cached one when key
+// matches, else capture `issue` on s and instantiate (or update) it.
+int run_cached_graph(const LstmGraphKey& key, cudaStream_t s, const std::function<int()>& issue);
+
 }  // namespace i8q
 
 using namespace i8q;
@@ -327,6 +546,7 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
   __nv_bfloat16* Wtb = (__nv_bfloat16*)(ws + L.off_Wtb);
   int32_t* Wcs = (int32_t*)(ws + L.off_Wcs);
   int8_t* Rt = (int8_t*)(ws + L.off_Rt);
+  __nv_bfloat16* Rtb = (__nv_bfloat16*)(ws + L.off_Rtb);
   int32_t* Rcs = (int32_t*)(ws + L.off_Rcs);
   float* Wsc = (float*)(ws + L.off_Wsc);
   float* Rsc = (float*)(ws + L.off_Rsc);
@@ -338,6 +558,7 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
   int32_t* zX = (int32_t*)(ws + L.off_zX);
   float* Gx = (float*)(ws + L.off_Gx);
   uint8_t* uh = ws + L.off_uh;
+  __nv_bfloat16* uhc = (__nv_bfloat16*)(ws + L.off_uhc);
   float* sh = (float*)(ws + L.off_sh);
   int32_t* zh = (int32_t*)(ws + L.off_zh);
   float* hbuf = (float*)(ws + L.off_h);
@@ -359,13 +580,17 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
 
   // weights: gate-interleaved K-major copies, column sums, scales, biases
   const bool tc = lstm_use_tc(L.TB, L.H4);
+  // recurrent product on the tensor pipe when the step has enough gate
+  // rows to spread (or when forced); exact chunks need |uh - 128| * |R| <= 2^14
+  const char* force = getenv("I8Q_FORCE_CORE");
+  const bool step_tc = force ? std::string(force) == "tc" : (L.H4 >= 1024);
   int rc;
   for (int64_t d = 0; d < L.D; ++d) {
     rc = launch_repack_cols_s8_gates(W + d * input * L.H4, input, L.H4, L.H4, Wt + d * L.H4 * L.Ip,
                                      tc ? Wtb + d * L.H4 * L.Ip : nullptr, L.Ip, Wcs + d * L.H4, H, s);
     if (rc) return rc;
-    rc = launch_repack_cols_s8_gates(R + d * H * L.H4, H, L.H4, L.H4, Rt + d * L.H4 * L.Hp, nullptr, L.Hp,
-                                     Rcs + d * L.H4, H, s);
+    rc = launch_repack_cols_s8_gates(R + d * H * L.H4, H, L.H4, L.H4, Rt + d * L.H4 * L.Hp,
+                                     step_tc ? Rtb + d * L.H4 * L.Hp : nullptr, L.Hp, Rcs + d * L.H4, H, s);
     if (rc) return rc;
   }
   interleave_scales<<<grid_for(L.D * L.H4), 256, 0, s>>>(W_scale, (int64_t)n_wscale, L.D, H, Wsc);
@@ -385,47 +610,164 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
     if (rc) return rc;
   }
 
-  // recurrence: both directions per launch
-  init_state<<<grid_for(DBH), 256, 0, s>>>(h0, c0, DBH, hbuf, cbuf);
-  I8Q_LAUNCH_CHECK("init_state");
-  rc = launch_quantize_rows(hbuf, I8Q_F32, L.D * batch, H, H, uh, nullptr, L.Hp, sh, zh, s);
-  if (rc) return rc;
-  StepParams sp;
-  sp.uh = uh;
-  sp.sh = sh;
-  sp.zh = zh;
-  sp.Rt = Rt;
-  sp.Rcs = Rcs;
-  sp.Rsc = Rsc;
-  sp.Gx = Gx;
-  sp.Wbi = Wbi;
-  sp.Rbi = Rbi;
-  sp.c = cbuf;
-  sp.Y = Y;
-  sp.T = (int)T;
-  sp.B = (int)batch;
-  sp.H = (int)H;
-  sp.Hp = (int)L.Hp;
-  sp.D = (int)L.D;
-  sp.direction = direction;
-  const dim3 sgrid((unsigned)ceil_div(L.H4, SN), (unsigned)L.D, (unsigned)ceil_div(batch, SB));
-  for (int64_t step = 0; step < T; ++step) {
-    float* h_next = hbuf + ((step + 1) & 1) * DBH;
-    sp.step = (int)step;
-    sp.h_next = h_next;
-    {
-      I8Q_PROF("lstm_step", s);
-      lstm_step_kernel<<<sgrid, STHREADS, 0, s>>>(sp);
-      I8Q_LAUNCH_CHECK("lstm_step_kernel");
+  // tensor maps of the step on the tensor pipe
+  CUtensorMap mR, mH;
+  if (step_tc) {
+    rc = tc::make_map_2d(&mR, Rtb, L.D * L.H4, L.Hp, tcs::BM, "dq_lstm");
+    if (rc) return rc;
+    rc = tc::make_map_2d(&mH, uhc, L.D * batch, L.Hp, tcs::BN, "dq_lstm");
+    if (rc) return rc;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+      attr_err = cudaFuncSetAttribute(tcs::lstm_step_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      tcs::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(lstm_step_tc_kernel)");
+  }
+
+  // recurrence: both directions per launch, 2 launches per step
+  auto recurrence = [&]() -> int {
+    init_state<<<grid_for(DBH), 256, 0, s>>>(h0, c0, DBH, hbuf, cbuf);
+    I8Q_LAUNCH_CHECK("init_state");
+    int rc2 = launch_quantize_rows(hbuf, I8Q_F32, L.D * batch, H, H, uh, step_tc ? uhc : nullptr, L.Hp, sh, zh, s);
+    if (rc2) return rc2;
+    StepParams sp;
+    sp.uh = uh;
+    sp.sh = sh;
+    sp.zh = zh;
+    sp.Rt = Rt;
+    sp.Rcs = Rcs;
+    sp.Rsc = Rsc;
+    sp.Gx = Gx;
+    sp.Wbi = Wbi;
+    sp.Rbi = Rbi;
+    sp.c = cbuf;
+    sp.Y = Y;
+    sp.T = (int)T;
+    sp.B = (int)batch;
+    sp.H = (int)H;
+    sp.Hp = (int)L.Hp;
+    sp.D = (int)L.D;
+    sp.direction = direction;
+    const dim3 sgrid((unsigned)ceil_div(L.H4, SN), (unsigned)L.D, (unsigned)ceil_div(batch, SB));
+    const dim3 tgrid((unsigned)ceil_div(L.H4, tcs::BM), (unsigned)L.D, (unsigned)ceil_div(batch, tcs::BN));
+    tcs::TcStepParams tp;
+    tp.sh = sh;
+    tp.zh = zh;
+    tp.Rcs = Rcs;
+    tp.Rsc = Rsc;
+    tp.Gx = Gx;
+    tp.Wbi = Wbi;
+    tp.Rbi = Rbi;
+    tp.c = cbuf;
+    tp.Y = Y;
+    tp.T = (int)T;
+    tp.B = (int)batch;
+    tp.H = (int)H;
+    tp.Hp = (int)L.Hp;
+    tp.D = (int)L.D;
+    tp.direction = direction;
+    tp.CS = 16;  // 1024 K-elements per exact fp32 chunk
+    tp.status = device_status_word();
+    if (step_tc && !tp.status) return fail(I8Q_ERR_CUDA, "dq_lstm: no device status word");
+    for (int64_t step = 0; step < T; ++step) {
+      float* h_next = hbuf + ((step + 1) & 1) * DBH;
+      sp.step = (int)step;
+      sp.h_next = h_next;
+      if (step_tc) {
+        I8Q_PROF("lstm_step_tc", s);
+        tp.step = (int)step;
+        tp.h_next = h_next;
+        tcs::lstm_step_tc_kernel<<<tgrid, tcs::THREADS, tcs::SMEM_BYTES, s>>>(mR, mH, tp);
+        I8Q_LAUNCH_CHECK("lstm_step_tc_kernel");
+      } else {
+        I8Q_PROF("lstm_step", s);
+        lstm_step_kernel<<<sgrid, STHREADS, 0, s>>>(sp);
+        I8Q_LAUNCH_CHECK("lstm_step_kernel");
+      }
+      if (step + 1 < T) {
+        rc2 = launch_quantize_rows(h_next, I8Q_F32, L.D * batch, H, H, uh, step_tc ? uhc : nullptr, L.Hp, sh, zh, s);
+        if (rc2) return rc2;
+      }
     }
-    if (step + 1 < T) {
-      rc = launch_quantize_rows(h_next, I8Q_F32, L.D * batch, H, H, uh, nullptr, L.Hp, sh, zh, s);
-      if (rc) return rc;
+    const float* h_last = hbuf + (T & 1) * DBH;
+    if (Y_h) copy_f32<<<grid_for(DBH), 256, 0, s>>>(h_last, Y_h, DBH);
+    if (Y_c) copy_f32<<<grid_for(DBH), 256, 0, s>>>(cbuf, Y_c, DBH);
+    I8Q_LAUNCH_CHECK("copy_f32");
+    return I8Q_OK;
+  };
+
+  // The recurrence is thousands of short launches: issue it as one CUDA
+  // graph, captured once per distinct argument set and relaunched (or
+  // updated in place) afterwards.  Direct launches when the caller is
+  // itself capturing, on the legacy default stream, or while kernel timing
+  // is on (which brackets each launch).
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  I8Q_CUDA_TRY(cudaStreamIsCapturing(s, &cap));
+  if (s == nullptr || cap != cudaStreamCaptureStatusNone || profiling_enabled() || T < 4) return recurrence();
+  const LstmGraphKey key{X, W, R, W_scale, R_scale, Bias, h0, c0, Y, Y_h, Y_c, workspace, T, batch, input, hidden,
+                         direction, (int64_t)n_wscale, (int64_t)n_rscale};
+  return run_cached_graph(key, s, recurrence);
+}
+
+namespace i8q {
+namespace {
+
+std::mutex g_graph_mu;
+struct {
+  bool valid = false;
+  int device = -1;
+  LstmGraphKey key{};
+  cudaGraphExec_t exec = nullptr;
+} g_graph;
+
+}  // namespace
+
+int run_cached_graph(const LstmGraphKey& key, cudaStream_t s, const std::function<int()>& issue) {
+  std::lock_guard<std::mutex> lk(g_graph_mu);
+  int dev = 0;
+  I8Q_CUDA_TRY(cudaGetDevice(&dev));
+  if (g_graph.valid && g_graph.device == dev && std::memcmp(&g_graph.key, &key, sizeof(key)) == 0) {
+    I8Q_CUDA_TRY(cudaGraphLaunch(g_graph.exec, s));
+    return I8Q_OK;
+  }
+  I8Q_CUDA_TRY(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+  const int rc = issue();
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(s, &graph);
+  if (rc) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (ec != cudaSuccess) return cuda_fail(ec, "cudaStreamEndCapture(lstm recurrence)");
+  bool updated = false;
+  if (g_graph.valid && g_graph.device == dev) {
+    cudaGraphExecUpdateResultInfo info;
+    if (cudaGraphExecUpdate(g_graph.exec, graph, &info) == cudaSuccess) {
+      updated = true;
+    } else {
+      cudaGetLastError();
+      cudaGraphExecDestroy(g_graph.exec);
+      g_graph.valid = false;
+    }
+  } else if (g_graph.valid) {
+    cudaGraphExecDestroy(g_graph.exec);  // made on another device
+    g_graph.valid = false;
+  }
+  if (!updated) {
+    const cudaError_t ei = cudaGraphInstantiate(&g_graph.exec, graph, 0);
+    if (ei != cudaSuccess) {
+      cudaGraphDestroy(graph);
+      return cuda_fail(ei, "cudaGraphInstantiate(lstm recurrence)");
     }
   }
-  const float* h_last = hbuf + (T & 1) * DBH;
-  if (Y_h) copy_f32<<<grid_for(DBH), 256, 0, s>>>(h_last, Y_h, DBH);
-  if (Y_c) copy_f32<<<grid_for(DBH), 256, 0, s>>>(cbuf, Y_c, DBH);
-  I8Q_LAUNCH_CHECK("copy_f32");
+  cudaGraphDestroy(graph);
+  g_graph.valid = true;
+  g_graph.device = dev;
+  g_graph.key = key;
+  I8Q_CUDA_TRY(cudaGraphLaunch(g_graph.exec, s));
   return I8Q_OK;
 }
+
+}  // namespace i8q

@@ -21,6 +21,14 @@ pytestmark = pytest.mark.gpu
 DIRS = {"forward": q.LSTM_FORWARD, "reverse": q.LSTM_REVERSE, "bidirectional": q.LSTM_BIDIRECTIONAL}
 
 
+@pytest.fixture(params=["imma", "tc"], autouse=True)
+def core(request, monkeypatch):
+    """Every case runs with the recurrent product on the int8 mma.sync core
+    and on the exact-integer tcgen05 core."""
+    monkeypatch.setenv("I8Q_FORCE_CORE", request.param)
+    return request.param
+
+
 def _t(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
