@@ -39,12 +39,14 @@ WORKLOAD = ("dynamic quantized GEMM M=8192 K=4096 N=14336: bf16 A quantized per 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="i8q", choices=["i8q", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-rows", type=int, default=256, help="rows of the CPU-baseline sample")
     p.add_argument("--no-rows", action="store_true", help="skip the other hot-path workloads")
+    p.add_argument("--m", type=int, default=M,
+                   help="rows of A in the GEMM step (default: the full workload; smaller for profiler captures)")
     return p.parse_args(argv)
 
 
@@ -75,6 +77,16 @@ def weak_scaling_value(ops_per_rank_step, steps, world, max_seconds):
     return ops_per_rank_step * steps * world / max_seconds
 
 
+def pci_bus_id(dev):
+    """'dddddddd:bb:dd.0' of a torch CUDA device, or None."""
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    try:
+        return "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except AttributeError:
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -86,27 +98,84 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    """SM clock and clock-event reasons sampled while the timed region runs:
+    NVML (read-only queries through ctypes) every 10 ms, else nvidia-smi
+    every 200 ms."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # clock-event reason bits of the NVML API
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, index):
+    def __init__(self, index, pci_bus_id=None):
         self.index = index
+        self.pci = pci_bus_id
         self.proc = None
         self.file = None
+        self.thread = None
+        self.samples = []
+        self.smax = None
+
+    def _nvml_handle(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.pci:
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(self.pci.encode(), ctypes.byref(h)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        try:
+            reasons = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons
 
     def start(self):
+        import ctypes
+        import threading
+        try:
+            lib, h, reasons = self._nvml_handle()
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.smax = float(mx.value)
+            self.stop_flag = threading.Event()
+
+            def poll():
+                clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self.stop_flag.is_set():
+                    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                            reasons(h, ctypes.byref(rs)) == 0:
+                        self.samples.append((float(clk.value), int(rs.value)))
+                    self.stop_flag.wait(0.01)
+
+            self.thread = threading.Thread(target=poll, daemon=True)
+            self.thread.start()
+            return
+        except (OSError, AttributeError):
+            self.thread = None
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.pci or str(self.index), f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.file,
                                          stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
 
     def stop(self):
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+            if not self.samples:
+                return None
+            reasons = sorted(n for n, b in self.REASON_BITS.items() if any(r & b for _, r in self.samples))
+            return {"sm_mhz": statistics.median(s for s, _ in self.samples),
+                    "sm_max_mhz": self.smax or max(s for s, _ in self.samples), "reasons": reasons,
+                    "samples": len(self.samples), "source": "nvml, 10 ms"}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -135,7 +204,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi, 200 ms"}
 
 
 def time_loop(fn, steps, stream):
@@ -308,12 +377,13 @@ def run_i8q(args):
     peaks, peak_src = load_peaks()
 
     # ---- large dynamic quantized GEMM -------------------------------------
-    w = workloads.large_gemm(seed=2 + rank)
-    ctx = q.QGemmDyn(M, N, K, q.BF16, q.S8, q.BF16, constB=True, bias=True, activation=q.ACT_GELU)
+    Mr = args.m
+    w = workloads.large_gemm(seed=2 + rank, M=Mr)
+    ctx = q.QGemmDyn(Mr, N, K, q.BF16, q.S8, q.BF16, constB=True, bias=True, activation=q.ACT_GELU)
     ctx.set_params(torch.from_numpy(w["iB"]).to(dev), torch.from_numpy(w["scaleB"]).to(dev),
                    torch.from_numpy(w["bias"]).to(dev))
     A = torch.from_numpy(w["A_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
-    C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    C = torch.empty(Mr, N, dtype=torch.bfloat16, device=dev)
     buf = torch.empty(ctx.external_buffer_size(), dtype=torch.uint8, device=dev)
     step = lambda: ctx.forward(A, C, buf=buf)  # noqa: E731
     for _ in range(args.warmup):
@@ -321,7 +391,7 @@ def run_i8q(args):
     q.sync_status()
     barrier(world)
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, pci_bus_id(dev))
     clocks.start()
     q.profile_enable(True)
     secs = time_loop(step, args.steps, stream)
@@ -332,7 +402,7 @@ def run_i8q(args):
     clk = clocks.stop()
     q.sync_status()
     max_secs = reduce_max(secs, world)
-    ops = 2.0 * M * N * K
+    ops = 2.0 * Mr * N * K
     value = weak_scaling_value(ops, args.steps, world, max_secs) / 1e12
     launches = sum(v[0] for v in prof.values())
     gemm_name = max((k for k in prof if k.startswith("gemm")), key=lambda k: prof[k][1])
@@ -347,7 +417,7 @@ def run_i8q(args):
 
     # ---- end to end through the host-buffer entry point -------------------
     A_h = torch.from_numpy(w["A_bf16"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    C_h = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    C_h = torch.empty(Mr, N, dtype=torch.bfloat16).pin_memory()
     for _ in range(2):
         ctx.forward_host(A_h, C_h)
     barrier(world)
@@ -396,7 +466,8 @@ def run_i8q(args):
             "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": max_secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u8*s8->s32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "parallelism": f"replicas x{world}",
+            "config": {"workload": WORKLOAD if Mr == M else WORKLOAD.replace("M=8192", f"M={Mr}"),
+                       "M": Mr, "K": K, "N": N, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (A 67 MB + B 59 MB + C 235 MB per step)",
                        "kernel": gemm_name},
             "roofline": {"bound": "tensor", "achieved": gemm_tops, "peak": peak, "unit": "TFLOP/s",

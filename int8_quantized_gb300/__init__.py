@@ -227,10 +227,16 @@ def qlinearconv(x, x_scale, x_zero_point, w, w_scale, w_zero_point, y_scale, y_z
                 pads=(0, 0, 0, 0), strides=(1, 1), dilations=(1, 1), group=1, workspace=None, stream=None):
     """QLinearConv, NCHW.  x_scale, y_scale: floats; x_zero_point,
     y_zero_point: ints; w_scale (fp32) / w_zero_point (w's dtype): CUDA
-    tensors of 1 or M entries; B: int32 CUDA tensor [M] or None."""
+    tensors of 1 or M entries; B: int32 CUDA tensor [M] or None.
+    workspace: uint8 CUDA tensor of qlinearconv_workspace_size bytes; when
+    None and the shape needs one, it is allocated here for this call."""
     xs, ws, p, s, d = _conv_arrays(x.shape, w.shape, pads, strides, dilations)
     if w_zero_point.dtype != w.dtype:
         raise TypeError("w_zero_point must have w's dtype")
+    if workspace is None:
+        need = int(_L().i8q_qlinearconv_workspace_size(xs, ws, p, s, d, int(group)))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=y.device)
     check(_L().i8q_qlinearconv(_dev(x, "x"), _TORCH_TYPE[x.dtype], xs, float(x_scale), int(x_zero_point),
                                _dev(w, "w"), _TORCH_TYPE[w.dtype], ws, _dev(w_scale, "w_scale", torch.float32),
                                _dev(w_zero_point, "w_zero_point"), w_scale.numel(), float(y_scale),

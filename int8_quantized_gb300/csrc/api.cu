@@ -185,7 +185,8 @@ struct i8q_qgemm_ctx {
   int typeA = 0, typeB = 0, typeC = 0, constB = 0, bias = 0, act = 0, avoid = 0;
   int64_t Kp = 0;
   bool params_set = false;
-  bool use_tc = false;
+  int core = 0;           // CORE_* below
+  bool use_tc = false;    // core == CORE_TC: bf16 operand copies are kept
   // internal storage
   int8_t* iBt = nullptr;
   __nv_bfloat16* iBt_bf16 = nullptr;
@@ -264,16 +265,24 @@ int dmalloc(T** p, size_t bytes, size_t* total) {
   return I8Q_OK;
 }
 
-// Core selection.  The tensor-core path (exact integers on the bf16 pipe,
-// 128 x 256 tiles) pays off once there are enough tiles to fill the SMs; a
-// small product stays on the int8 mma.sync core.  I8Q_FORCE_CORE=imma|tc
-// overrides the choice (tests cover both cores on the same shapes).
-bool want_tc(size_t M, size_t N) {
+// Core selection.  Products with enough work run on the tensor-core path
+// (exact integers on the bf16 pipe, 128 x 256 tiles); small ones run in one
+// fused launch on dp4a (row quantization and sums together), whose fixed
+// cost is a few microseconds.  The int8 mma.sync core is kept for the
+// override and as the path for very long K outside both.
+// I8Q_FORCE_CORE=imma|tc|small overrides the choice (tests run every core
+// on the same shapes).
+enum Core : int { CORE_IMMA = 0, CORE_TC = 1, CORE_SMALL = 2 };
+
+int choose_core(size_t M, size_t N, int64_t Kp) {
   const char* f = getenv("I8Q_FORCE_CORE");
-  if (f && std::string(f) == "imma") return false;
-  if (f && std::string(f) == "tc") return true;
-  const size_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
-  return M >= 128 && N >= 256 && tiles >= 64;
+  const bool small_ok = Kp <= small_max_kp();
+  if (f && std::string(f) == "imma") return CORE_IMMA;
+  if (f && std::string(f) == "tc") return CORE_TC;
+  if (f && std::string(f) == "small") return small_ok ? CORE_SMALL : CORE_IMMA;
+  const double macs = (double)M * (double)N * (double)Kp;
+  if (small_ok && macs <= (double)(1 << 27)) return CORE_SMALL;
+  return CORE_TC;
 }
 
 }  // namespace
@@ -313,7 +322,8 @@ extern "C" int i8q_qgemm_dyn_init(i8q_qgemm_ctx** ctx, size_t M, size_t N, size_
   c->act = activation;
   c->avoid = avoidOverflow;
   c->Kp = round_up((int64_t)K, 64);
-  c->use_tc = want_tc(M, N);
+  c->core = choose_core(M, N, c->Kp);
+  c->use_tc = c->core == CORE_TC;
   int rc = I8Q_OK;
   size_t total = 0;
   if (constB) {
@@ -350,8 +360,9 @@ extern "C" size_t i8q_qgemm_dyn_external_buffer_size(const i8q_qgemm_ctx* ctx) {
 extern "C" const char* i8q_qgemm_dyn_info(i8q_qgemm_ctx* ctx) {
   if (!ctx) return nullptr;
   ctx->info = std::string("sm_103a ") +
-              (ctx->use_tc ? "tcgen05.kind::f16 exact-int (bf16 operands, fp32 chunks drained to int32)"
-                           : "mma.sync.m16n8k32.u8.s8 int32 128x128x64 4-stage") +
+              (ctx->core == CORE_TC      ? "tcgen05.kind::f16 exact-int (bf16 operands, fp32 chunks drained to int32)"
+               : ctx->core == CORE_SMALL ? "fused row quantization + dp4a.u32.s32 int32, 4 rows x 32 columns per CTA"
+                                         : "mma.sync.m16n8k32.u8.s8 int32 128x128x64 4-stage") +
               "; A per-row uint8, B per-column int8" + (ctx->avoid && ctx->typeB != I8Q_S8 ? " [-64,63]" : "");
   return ctx->info.c_str();
 }
@@ -417,8 +428,12 @@ int forward_impl(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf, vo
   float* scaleA = reinterpret_cast<float*>(base + L.scaleA);
   int32_t* zeroA = reinterpret_cast<int32_t*>(base + L.zeroA);
   const int64_t M = (int64_t)ctx->M, N = (int64_t)ctx->N, K = (int64_t)ctx->K;
-  int rc = launch_quantize_rows(A, ctx->typeA, M, K, K, uA, uA_bf16, ctx->Kp, scaleA, zeroA, s);
-  if (rc) return rc;
+  const bool small = ctx->core == CORE_SMALL;
+  int rc = I8Q_OK;
+  if (!small) {
+    rc = launch_quantize_rows(A, ctx->typeA, M, K, K, uA, uA_bf16, ctx->Kp, scaleA, zeroA, s);
+    if (rc) return rc;
+  }
   const int8_t* iBt = ctx->iBt;
   const __nv_bfloat16* iBt_bf16 = ctx->iBt_bf16;
   const float* scaleB = ctx->scaleB;
@@ -437,6 +452,7 @@ int forward_impl(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf, vo
     colsum = cs;
   }
   GemmEpilogue ep{zeroA, scaleA, colsum, scaleB, ctx->bias ? ctx->biasv : nullptr, ctx->act, out_mode, C, N};
+  if (small) return launch_gemm_small(A, ctx->typeA, M, K, ctx->Kp, iBt, N, uA, scaleA, zeroA, ep, s);
   if (ctx->use_tc) {
     // |uA - 128| <= 2^7; |iB| <= 2^7, or 2^6 in the narrowed range
     const int qb = (ctx->typeB == I8Q_S8 || !ctx->avoid) ? 7 : 6;

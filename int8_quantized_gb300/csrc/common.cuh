@@ -81,6 +81,26 @@ __device__ __forceinline__ uint32_t rint_code_bits(float q, float lo_z, float hi
   return (uint32_t)(__float_as_int(r) + zp);
 }
 
+// Row quantization of A (uint8, per row, range widened to contain 0) from
+// the row's mn = min(0, min A) and mx = max(0, max A):
+//   scale = (mx - mn) / 255, zero = sat_u8(rint(-mn / scale)),
+// and an all-zero row (scale 0) takes scale 1, zero 0.
+__device__ __forceinline__ void row_scale_zero(float mn, float mx, float& s, int& z) {
+  s = __fdiv_rn(__fsub_rn(mx, mn), 255.0f);
+  z = 0;
+  if (s == 0.0f) {
+    s = 1.0f;
+  } else {
+    z = sat_rint(__fdiv_rn(-mn, s), 0.0f, 255.0f);
+  }
+}
+
+// uA = sat_u8(rint(v / scale) + zero) as the low byte of the result, for
+// lo_z = -zero and hi_z = 255 - zero.
+__device__ __forceinline__ uint32_t row_code(float v, float s, float lo_z, float hi_z, int z) {
+  return rint_code_bits(__fdiv_rn(v, s), lo_z, hi_z, z) & 0xffu;
+}
+
 // Pack the low bytes of four words into one word (byte 0 from a).
 __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
@@ -206,6 +226,13 @@ int launch_gemm_imma(const uint8_t* uA, const int8_t* iBt, int64_t M, int64_t N,
 // Returns I8Q_ERR_UNSUPPORTED when the shape is outside what it handles.
 int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M, int64_t N,
                    int64_t Kp, int max_abs_product_log2, const GemmEpilogue& ep, cudaStream_t s);
+
+// Small products in one launch: row quantization of A (fp32/bf16, row
+// stride K) into uA / scaleA / zeroA, then the integer sums against iBt
+// (N x Kp int8) with dp4a and the epilogue.  Kp <= small_max_kp().
+int64_t small_max_kp();
+int launch_gemm_small(const void* A, int typeA, int64_t M, int64_t K, int64_t Kp, const int8_t* iBt, int64_t N,
+                      uint8_t* uA, float* scaleA, int32_t* zeroA, const GemmEpilogue& ep, cudaStream_t s);
 
 // QLinearConv on the tensor pipe (group 1, stride 1, dilation 1, tile shapes
 // it instantiates).  conv_tc_workspace: scratch bytes, 0 when the shape does

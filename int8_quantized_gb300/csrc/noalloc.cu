@@ -89,14 +89,17 @@ extern "C" int i8q_qgemm_dyn_static(size_t M, size_t N, size_t K, int typeA, con
   o += a256(N * (size_t)Kp);
   int32_t* colsum = reinterpret_cast<int32_t*>(base + o);
   cudaStream_t s = as_stream(stream);
-  // every byte read below is written first in this call: the row kernel
-  // writes uA over all Kp columns (zero beyond K), the repack writes iBt
-  // over all Kp columns and every column sum
-  rc = launch_quantize_rows(A, typeA, (int64_t)M, (int64_t)K, (int64_t)K, uA, nullptr, Kp, scaleA, zeroA, s);
-  if (rc) return rc;
+  // every byte read below is written first in this call: the repack writes
+  // iBt over all Kp columns and every column sum; the row quantization (on
+  // its own, or inside the fused small-product kernel) writes uA over all Kp
+  // columns (zero beyond K)
   rc = launch_repack_cols_s8(B, (int64_t)K, (int64_t)N, (int64_t)N, iBt, nullptr, Kp, colsum, s);
   if (rc) return rc;
   GemmEpilogue ep{zeroA, scaleA, colsum, scaleB, bias, activation, typeC == I8Q_BF16 ? OUT_BF16 : OUT_F32, C,
                   (int64_t)N};
+  if (Kp <= small_max_kp())
+    return launch_gemm_small(A, typeA, (int64_t)M, (int64_t)K, Kp, iBt, (int64_t)N, uA, scaleA, zeroA, ep, s);
+  rc = launch_quantize_rows(A, typeA, (int64_t)M, (int64_t)K, (int64_t)K, uA, nullptr, Kp, scaleA, zeroA, s);
+  if (rc) return rc;
   return launch_gemm_imma(uA, iBt, (int64_t)M, (int64_t)N, Kp, ep, s);
 }

@@ -18,13 +18,14 @@ from int8_quantized_gb300 import workloads
 pytestmark = pytest.mark.gpu
 
 ACT = {"identity": q.ACT_IDENTITY, "relu": q.ACT_RELU, "gelu": q.ACT_GELU}
-CORE_INFO = {"imma": "mma.sync", "tc": "tcgen05"}
+CORE_INFO = {"imma": "mma.sync", "tc": "tcgen05", "small": "dp4a"}
 
 
-@pytest.fixture(params=["imma", "tc"], autouse=True)
+@pytest.fixture(params=["imma", "tc", "small"], autouse=True)
 def core(request, monkeypatch):
-    """Every case runs on both integer cores: the int8 mma.sync core and the
-    exact-integer tcgen05 core (forced regardless of the shape)."""
+    """Every case runs on each integer core, forced regardless of the shape:
+    the int8 mma.sync core, the exact-integer tcgen05 core and the fused
+    small-product dp4a kernel."""
     monkeypatch.setenv("I8Q_FORCE_CORE", request.param)
     return request.param
 
@@ -206,6 +207,19 @@ def test_chunk_boundaries(orc, dev, K):
     A = rng.normal(0, 1, (M, K)).astype(np.float32)
     iB = rng.integers(-128, 128, (K, N)).astype(np.int8)
     run_case(orc, dev, A, iB=iB, scaleB=rng.uniform(1e-3, 1e-2, N).astype(np.float32), bias=None)
+
+
+@pytest.mark.parametrize("M,N,K,expect", [(64, 128, 256, "dp4a"), (1, 7, 3, "dp4a"), (8192, 14336, 4096, "tcgen05"),
+                                          (64, 1024, 4096, "tcgen05"), (64, 128, 10000, "tcgen05")])
+def test_default_core_choice(monkeypatch, core, M, N, K, expect):
+    """Without the override, small products take the fused dp4a kernel and
+    the rest the tensor-core path."""
+    if core != "tc":
+        pytest.skip("the default choice does not depend on the forced core")
+    monkeypatch.delenv("I8Q_FORCE_CORE")
+    ctx = q.QGemmDyn(M, N, K, constB=True, bias=False)
+    assert expect in ctx.info()
+    ctx.clear()
 
 
 def test_context_reinit_and_errors(orc, dev):
