@@ -271,14 +271,15 @@ int dmalloc(T** p, size_t bytes, size_t* total) {
 // cost is a few microseconds.  The int8 mma.sync core is kept for the
 // override and as the path for very long K outside both.
 // I8Q_FORCE_CORE=imma|tc|small overrides the choice (tests run every core
-// on the same shapes).
+// on the same shapes); tc1 / tc2 also pin the tensor-core path to its
+// single-CTA or CTA-pair kernel.
 enum Core : int { CORE_IMMA = 0, CORE_TC = 1, CORE_SMALL = 2 };
 
 int choose_core(size_t M, size_t N, int64_t Kp) {
   const char* f = getenv("I8Q_FORCE_CORE");
   const bool small_ok = Kp <= small_max_kp();
   if (f && std::string(f) == "imma") return CORE_IMMA;
-  if (f && std::string(f) == "tc") return CORE_TC;
+  if (f && (std::string(f) == "tc" || std::string(f) == "tc1" || std::string(f) == "tc2")) return CORE_TC;
   if (f && std::string(f) == "small") return small_ok ? CORE_SMALL : CORE_IMMA;
   const double macs = (double)M * (double)N * (double)Kp;
   if (small_ok && macs <= (double)(1 << 27)) return CORE_SMALL;

@@ -341,7 +341,307 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
+// ---- CTA-pair kernel -------------------------------------------------------
+// A cluster of two CTAs computes 256 x 256 output tiles with one
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16) per 16 K elements:
+// CTA r of the pair holds rows 128r..128r+127 of the A tile and rows
+// 128r..128r+127 of the B tile (output columns) in its shared memory, and
+// the accumulator rows 128r.. in its TMEM.  Per SM this halves the bytes the
+// tensor core reads from shared memory and the bytes TMA writes there per
+// multiply-add, compared with the 128 x 256 single-CTA tile, where the two
+// together exceed the shared-memory bandwidth before the tensor pipe is full.
+// Roles as in the single-CTA kernel; the even CTA of the pair (the leader)
+// issues the MMAs and owns the stage-full and accumulator-empty barriers:
+// both CTAs' TMA loads complete on the leader's stage barrier, and both
+// CTAs' epilogue warps arrive on its accumulator-empty barrier.  The MMA
+// commits arrive on the stage-empty and accumulator-full barriers of both
+// CTAs (multicast).
+constexpr int PBM = 256, PBN = 256;
+constexpr int HALF_ROWS = 128;
+constexpr int P_STAGES = 6;
+constexpr int P_A_STAGE = HALF_ROWS * BK * 2;  // 16 KB
+constexpr int P_B_STAGE = HALF_ROWS * BK * 2;  // 16 KB
+constexpr int P_STAGE_BYTES = P_A_STAGE + P_B_STAGE;
+constexpr int P_NUM_BARS = 2 * P_STAGES + 4 + 1;
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + PARAM_BYTES + P_NUM_BARS * 8 + 16;
+constexpr int P_GROUP_M = 8;
+constexpr uint32_t IDESC_PAIR = idesc_bf16(PBM, PBN);
+static_assert(P_SMEM_BYTES <= 227 * 1024, "shared memory of the pair kernel");
+
+__device__ __forceinline__ void tile_coords_g(int tile, int tiles_m, int tiles_n, int group, int& mt, int& nt) {
+  const int per_group = group * tiles_n;
+  const int g = tile / per_group;
+  const int first = g * group;
+  const int gsize = min(tiles_m - first, group);
+  const int r = tile - g * per_group;
+  mt = first + r % gsize;
+  nt = r / gsize;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;\n" : "=r"(r));
+  return r;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* params = smem + P_STAGES * P_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(params + PARAM_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + P_NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t smem0 = smem_u32(smem);
+  auto sA = [&](int s) { return smem0 + (uint32_t)(s * P_STAGE_BYTES); };
+  auto sB = [&](int s) { return smem0 + (uint32_t)(s * P_STAGE_BYTES + P_A_STAGE); };
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + P_STAGES + s); };
+  auto accf = [&](int b) { return smem_u32(bars + 2 * P_STAGES + b); };
+  auto acce = [&](int b) { return smem_u32(bars + 2 * P_STAGES + 2 + b); };
+  const uint32_t fin = smem_u32(bars + 2 * P_STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf(b), 1);
+      mbar_init(acce(b), 2 * NUM_EPI_WARPS);
+    }
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  // the peer's barriers are initialised before any remote arrival or copy
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int KT = p.KT, CS = p.CS;
+  const int nchunks = (KT + CS - 1) / CS;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      int it = 0, s = 0;
+      uint32_t ph = 0;  // phase parity of stage s
+      bool ok = true;
+      const uint32_t full0 = map_shared_rank(full(0), 0);  // the leader's stage barriers
+      for (int tile = cid; ok && tile < p.num_tiles; tile += ncl) {
+        int mt, nt;
+        tile_coords_g(tile, p.tiles_m, p.tiles_n, P_GROUP_M, mt, nt);
+        const int ya = mt * PBM + (int)rank * HALF_ROWS, yb = nt * PBN + (int)rank * HALF_ROWS;
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          if (!wait_bar<true>(empty(s), ph ^ 1u, abort_flag, p.status, ST_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + (uint32_t)(s * 8);
+          if (leader) mbar_arrive_expect_tx(full(s), 2 * P_STAGE_BYTES);
+          tma_load_2d_pair(sA(s), &tmA, fb, kt * BK, ya);
+          tma_load_2d_pair(sB(s), &tmB, fb, kt * BK, yb);
+          if (++s == P_STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // Wait until the MMAs have released every stage: the last commits
+      // arrive on this CTA's stage-empty barriers, which must not outlive it.
+      if (ok) {
+        for (int j = it; j < it + P_STAGES; ++j)
+          if (!wait_bar<true>(empty(j % P_STAGES), ((uint32_t)(j / P_STAGES) & 1u) ^ 1u, abort_flag, p.status,
+                              ST_TIMEOUT_DRAIN))
+            break;
+      } else if (leader) {
+        for (int j = max(0, it - P_STAGES); j < it; ++j) {
+          unsigned long long t0 = global_ns();
+          while (!mbar_try_wait_cluster(full(j % P_STAGES), (uint32_t)(j / P_STAGES) & 1u))
+            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+              atomicOr(p.status, ST_TIMEOUT_DRAIN);
+              break;
+            }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (leader CTA) ----------------
+    if (leader && lane == 0) {
+      // Kept lean: this one thread feeds the tensor pipe and shares its
+      // sub-partition with epilogue warps, so stage, phase and chunk are
+      // counters and the descriptors advance by addition (the start-address
+      // field holds address / 16; the sums stay inside shared memory).
+      int s = 0, kc = 0, chunk = 0;
+      uint32_t ph = 0, cph = 0;  // stage phase; accumulator-buffer phase
+      bool ok = true;
+      uint32_t d = tmem_base;
+      const uint64_t a0 = desc_sw128(sA(0)), b0 = desc_sw128(sB(0));
+      constexpr uint64_t STAGE_STEP = P_STAGE_BYTES >> 4, K_STEP = 32 >> 4;
+      for (int tile = cid; ok && tile < p.num_tiles; tile += ncl) {
+        for (int kt = 0; kt < KT; ++kt) {
+          if (kc == 0) {
+            const int b = chunk & 1;
+            if (!wait_bar<true>(acce(b), cph ^ 1u, abort_flag, p.status, ST_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d = tmem_base + (uint32_t)(b * PBN);
+          }
+          if (!wait_bar<true>(full(s), ph, abort_flag, p.status, ST_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = a0 + (uint64_t)s * STAGE_STEP, bd = b0 + (uint64_t)s * STAGE_STEP;
+          tc_mma_pair(d, ad, bd, IDESC_PAIR, kc == 0 ? 0u : 1u);
+#pragma unroll
+          for (int k = 1; k < BK / 16; ++k) tc_mma_pair(d, ad + k * K_STEP, bd + k * K_STEP, IDESC_PAIR, 1u);
+          tc_commit_pair_mc(empty(s), 0x3);
+          if (++kc == CS || kt == KT - 1) {
+            tc_commit_pair_mc(accf(chunk & 1), 0x3);
+            ++chunk;
+            kc = 0;
+            if ((chunk & 1) == 0) cph ^= 1u;
+          }
+          if (++s == P_STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // all MMAs issued by this thread complete before either CTA releases
+      // its TMEM or its shared memory
+      tc_commit_pair_mc(fin, 0x1);
+      unsigned long long t0 = global_ns();
+      while (!mbar_try_wait_cluster(fin, 0))
+        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+          atomicOr(p.status, ST_TIMEOUT_DRAIN);
+          break;
+        }
+    }
+  } else {
+    // ---------------- drain + epilogue (both CTAs) ----------------
+    const int q = warp & 3;
+    const int slice = (warp - 2) >> 2;
+    int32_t* pc = reinterpret_cast<int32_t*>(params) + (warp - 2) * SLICE * 3;
+    float* ps = reinterpret_cast<float*>(pc + SLICE);
+    float* pb = ps + SLICE;
+    const uint32_t acce_leader0 = map_shared_rank(acce(0), 0), acce_leader1 = map_shared_rank(acce(1), 0);
+    int chunk = 0;
+    bool ok = true;
+    for (int tile = cid; ok && tile < p.num_tiles; tile += ncl) {
+      int mt, nt;
+      tile_coords_g(tile, p.tiles_m, p.tiles_n, P_GROUP_M, mt, nt);
+      const int64_t col0 = (int64_t)nt * PBN + slice * SLICE;
+      for (int j = lane; j < SLICE; j += 32) {
+        const int64_t c = col0 + j;
+        const bool in = c < p.N;
+        pc[j] = in ? __ldg(p.ep.colsum + c) : 0;
+        ps[j] = in ? __ldg(p.ep.scaleB + c) : 0.0f;
+        pb[j] = (in && p.ep.bias) ? __ldg(p.ep.bias + c) : 0.0f;
+      }
+      int32_t run[SLICE];
+#pragma unroll
+      for (int j = 0; j < SLICE; ++j) run[j] = 0;
+      for (int c = 0; c < nchunks; ++c, ++chunk) {
+        const int b = chunk & 1;
+        const bool got =
+            wait_bar<true>(accf(b), (uint32_t)(chunk >> 1) & 1u, abort_flag, p.status, ST_TIMEOUT_EPILOGUE);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * PBN + slice * SLICE);
+#pragma unroll
+        for (int j = 0; j < SLICE / 16; j += 2) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(taddr + (uint32_t)(j * 16), r0);
+          tmem_ld16(taddr + (uint32_t)(j * 16 + 16), r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            run[j * 16 + i] += __float2int_rn(__uint_as_float(r0[i]));
+            run[j * 16 + 16 + i] += __float2int_rn(__uint_as_float(r1[i]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(b ? acce_leader1 : acce_leader0);
+      }
+      if (!ok) break;
+      __syncwarp();
+      const int64_t row = (int64_t)mt * PBM + (int64_t)rank * HALF_ROWS + q * 32 + lane;
+      if (row < p.M) {
+        const float sA = __ldg(p.ep.scaleA + row);
+        const int32_t zA = __ldg(p.ep.zeroA + row) - 128;
+        store_slice(p.ep, row, col0, p.N, run, zA, sA, pc, ps, pb);
+      }
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // the leader's MMAs into this CTA's TMEM and its arrivals here are done
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 }  // namespace
+
+// Clusters of two CTAs of the pair kernel that fit on the device at once
+// (0 when none do; -1 on a CUDA error), computed once.
+int pair_max_clusters() {
+  static std::once_flag once;
+  static int n = -1;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+    if (err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * sm_count()));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    err = cudaOccupancyMaxActiveClusters(&c, gemm_tc_pair_kernel, &cfg);
+    if (err == cudaSuccess) n = c;
+  });
+  if (err != cudaSuccess) {
+    cuda_fail(err, "gemm_tc: pair kernel setup");
+    return -1;
+  }
+  return n;
+}
 
 int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M, int64_t N, int64_t Kp,
                    int max_abs_product_log2, const GemmEpilogue& ep, cudaStream_t s) {
@@ -374,11 +674,48 @@ int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M,
   p.N = N;
   p.KT = (int)(Kp / BK);
   p.CS = CS;
+  p.ep = ep;
+  p.status = status;
+
+  // CTA pairs when there is at least a wave of 256 x 256 tiles;
+  // I8Q_FORCE_CORE=tc1 / tc2 picks the single-CTA / pair kernel.
+  const char* force = getenv("I8Q_FORCE_CORE");
+  const int pair_clusters = pair_max_clusters();
+  if (pair_clusters < 0) return I8Q_ERR_CUDA;
+  const int64_t pair_tiles = ceil_div(M, PBM) * ceil_div(N, PBN);
+  bool use_pair = M >= PBM && pair_clusters > 0 && pair_tiles >= pair_clusters;
+  if (force && std::string(force) == "tc1") use_pair = false;
+  if (force && std::string(force) == "tc2") use_pair = pair_clusters > 0;
+  if (use_pair) {
+    CUtensorMap pA, pB;
+    rc = make_map_2d(&pA, uA, M, Kp, HALF_ROWS, "gemm_tc");
+    if (rc) return rc;
+    rc = make_map_2d(&pB, iBt, N, Kp, HALF_ROWS, "gemm_tc");
+    if (rc) return rc;
+    p.tiles_m = (int)ceil_div(M, PBM);
+    p.tiles_n = (int)ceil_div(N, PBN);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    const int clusters = std::min(p.num_tiles, pair_clusters);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    I8Q_PROF("gemm_tc_pair", s);
+    I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel, pA, pB, p));
+    I8Q_LAUNCH_CHECK("gemm_tc_pair_kernel");
+    return I8Q_OK;
+  }
   p.tiles_m = (int)ceil_div(M, BM);
   p.tiles_n = (int)ceil_div(N, BN);
   p.num_tiles = p.tiles_m * p.tiles_n;
-  p.ep = ep;
-  p.status = status;
   const int grid = std::min(p.num_tiles, sm_count());
   I8Q_PROF("gemm_tc", s);
   gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(mA, mB, p);

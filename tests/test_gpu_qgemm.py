@@ -18,13 +18,14 @@ from int8_quantized_gb300 import workloads
 pytestmark = pytest.mark.gpu
 
 ACT = {"identity": q.ACT_IDENTITY, "relu": q.ACT_RELU, "gelu": q.ACT_GELU}
-CORE_INFO = {"imma": "mma.sync", "tc": "tcgen05", "small": "dp4a"}
+CORE_INFO = {"imma": "mma.sync", "tc1": "tcgen05", "tc2": "tcgen05", "small": "dp4a"}
 
 
-@pytest.fixture(params=["imma", "tc", "small"], autouse=True)
+@pytest.fixture(params=["imma", "tc1", "tc2", "small"], autouse=True)
 def core(request, monkeypatch):
     """Every case runs on each integer core, forced regardless of the shape:
-    the int8 mma.sync core, the exact-integer tcgen05 core and the fused
+    the int8 mma.sync core, the exact-integer tcgen05 core with single-CTA
+    128 x 256 tiles and with CTA-pair 256 x 256 tiles, and the fused
     small-product dp4a kernel."""
     monkeypatch.setenv("I8Q_FORCE_CORE", request.param)
     return request.param
@@ -214,7 +215,7 @@ def test_chunk_boundaries(orc, dev, K):
 def test_default_core_choice(monkeypatch, core, M, N, K, expect):
     """Without the override, small products take the fused dp4a kernel and
     the rest the tensor-core path."""
-    if core != "tc":
+    if core != "tc1":
         pytest.skip("the default choice does not depend on the forced core")
     monkeypatch.delenv("I8Q_FORCE_CORE")
     ctx = q.QGemmDyn(M, N, K, constB=True, bias=False)
