@@ -36,6 +36,36 @@ WORKLOAD = ("dynamic quantized GEMM M=8192 K=4096 N=14336: bf16 A quantized per 
             "per-column scales, int32 product, dequant + bias + GELU, bf16 C")
 
 
+# DRAM bytes (read + written) per launch of the GEMM kernels, from one ncu
+# capture of the headline step (dram__bytes_read.sum + dram__bytes_write.sum,
+# a single-pass capture of the full-size launch).  Keyed by the SHA-256 of the
+# kernel's sources: the figure is reported only while they are unchanged.
+NCU_TRAFFIC = {
+    "gemm_tc_pair": {"sources": ["int8_quantized_gb300/csrc/gemm_tc.cu", "int8_quantized_gb300/csrc/tcgen05.cuh",
+                                 "int8_quantized_gb300/csrc/common.cuh"],
+                     "sha256": "b72ea7efab4779035cf8bfc9c5f43571eabbf8baaf1343a977a74386804bab7e",
+                     "bytes": (592.50 + 231.21) * 1e6,
+                     "profile": "profiles/gemm_tc_pair_large_gemm.md"},
+}
+
+
+def ncu_traffic(kernel):
+    """Bytes per launch from the committed capture, or None when the kernel
+    has no capture or its sources changed since."""
+    import hashlib
+    e = NCU_TRAFFIC.get(kernel)
+    if e is None:
+        return None
+    h = hashlib.sha256()
+    try:
+        for f in e["sources"]:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    return e["bytes"] if h.hexdigest() == e["sha256"] else None
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -43,7 +73,7 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="i8q", choices=["i8q", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-rows", type=int, default=256, help="rows of the CPU-baseline sample")
+    p.add_argument("--cpu-rows", type=int, default=2048, help="rows of the CPU-baseline sample")
     p.add_argument("--no-rows", action="store_true", help="skip the other hot-path workloads")
     p.add_argument("--m", type=int, default=M,
                    help="rows of A in the GEMM step (default: the full workload; smaller for profiler captures)")
@@ -471,7 +501,7 @@ def run_i8q(args):
                        "l2": "inputs larger than L2 (A 67 MB + B 59 MB + C 235 MB per step)",
                        "kernel": gemm_name},
             "roofline": {"bound": "tensor", "achieved": gemm_tops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": gemm_tops / peak, "traffic": None, "peak_source": peak_note,
+                         "frac": gemm_tops / peak, "traffic": ncu_traffic(gemm_name), "peak_source": peak_note,
                          "kernel": gemm_name, "kernel_ms": gemm_ms},
             "int8_tensor_peak_tops": int8_peak,
             "pct_int8_tensor_peak": 100.0 * value / world / int8_peak,

@@ -17,11 +17,15 @@
 // interleaved per hidden unit (column q*H + u stored at 4u + q), so any
 // 64-column tile holds all four gates of 16 hidden units.  Then one kernel
 // per step does, for both directions at once, the recurrent integer product
-// of a 64-row x 64-column tile (uint8 h x int8 R on mma.sync, exact int32)
-// and the whole cell update in its epilogue.  The projection runs once over
-// all T * batch rows on the tensor-core GEMM; X is quantized once for both
-// directions.  Each step's new h is quantized per row (both directions in
-// one launch) for the next step.
+// and the whole cell update in its epilogue: on the tensor pipe
+// (tcgen05, 128 gate columns x 64 batch rows per CTA, h codes centred to
+// uh - 128 in bf16, fp32 chunks drained exactly to int32, the step's
+// x-projection and previous cell state loaded while the MMAs run) for wide
+// layers, or on the int8 mma.sync form (64 x 64 tiles) otherwise.  The
+// projection runs once over all T * batch rows on the tensor-core GEMM; X is
+// quantized once for both directions.  Each step's new h is quantized per
+// row (both directions in one launch) for the next step, and the whole
+// sequence of steps is replayed as one CUDA graph, cached per argument set.
 #include <cstring>
 #include <functional>
 #include <mutex>
