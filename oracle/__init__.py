@@ -38,8 +38,10 @@ def load(path):
     l.or_qlinearconv.argtypes = [p, c_int, i64, i64, i64, i64, f32, i32, p, c_int, i64, i64,
                                  i64, p, p, c_int, f32, i32, p, p, p, p, i64, p, c_int]
     l.or_lstm_cell.argtypes = [p, p, p, p, p, p, p, i64, i64]
+    l.or_qgemm.argtypes = [p, c_int, c_int, i64, i64, f32, i32, p, c_int, c_int, i64, p, p, i64, p, i64, i64,
+                           f32, c_int, f32, i32, c_int, p]
     for fn in ("or_quantize_linear", "or_dequantize_linear", "or_quantize_rows_u8",
-               "or_quantize_cols_s8", "or_qgemm_dyn_rows", "or_qlinearconv", "or_lstm_cell"):
+               "or_quantize_cols_s8", "or_qgemm_dyn_rows", "or_qlinearconv", "or_lstm_cell", "or_qgemm"):
         getattr(l, fn).restype = ctypes.c_int
     return l
 
@@ -223,6 +225,51 @@ def qlinearconv(x, x_scale, x_zero_point, w, w_scale, w_zero_point, y_scale, y_z
                                 float(y_scale), int(y_zero_point), _ptr(b), _ptr(pads),
                                 _ptr(strides), _ptr(dil), group, _ptr(y), yt), "qlinearconv")
     return y
+
+
+def qgemm(A, a_scale, a_zero_point, B, b_scale, b_zero_point=None, C=None, alpha=1.0, y_scale=None,
+          y_zero_point=None, transA=False, transB=False, ytype=None):
+    """QGemm (ONNX Runtime contrib schemas).  A: uint8/int8 (M, K), or (K, M)
+    when transA; B: uint8/int8 (K, N), or (N, K) when transB; b_scale and
+    b_zero_point: scalars or N entries; C: int32 broadcastable to (M, N)
+    ((M, N), (1, N), (N,), (M, 1), (1, 1) or a scalar).  Float output unless
+    y_scale is given; the quantized type is y_zero_point's (uint8 when it is
+    a plain int and ytype is not given)."""
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    at = U8 if A.dtype == np.uint8 else S8
+    bt = U8 if B.dtype == np.uint8 else S8
+    M, K = (A.shape[1], A.shape[0]) if transA else A.shape
+    N = B.shape[0] if transB else B.shape[1]
+    if (B.shape[1] if transB else B.shape[0]) != K:
+        raise ValueError("inner dimensions differ")
+    bs = np.ascontiguousarray(np.atleast_1d(b_scale), dtype=np.float32)
+    bz = None if b_zero_point is None else np.ascontiguousarray(np.atleast_1d(b_zero_point), dtype=np.int32)
+    if bs.size not in (1, N) or (bz is not None and bz.size != bs.size):
+        raise ValueError("b_scale / b_zero_point must be scalars or have N entries")
+    c = None
+    cr = cc = 0
+    if C is not None:
+        c = np.asarray(C, dtype=np.int32)
+        if c.ndim == 0:
+            c = c.reshape(1, 1)
+        elif c.ndim == 1:
+            c = c.reshape(1, -1)
+        cr, cc = c.shape
+        c = np.ascontiguousarray(c)
+    quant = y_scale is not None
+    if quant:
+        yt = _qtype(ytype) if ytype is not None else (
+            S8 if isinstance(y_zero_point, np.integer) and np.asarray(y_zero_point).dtype == np.int8 else U8)
+        Y = np.empty((M, N), dtype=np.uint8 if yt == U8 else np.int8)
+    else:
+        yt = U8
+        Y = np.empty((M, N), dtype=np.float32)
+    _check(lib().or_qgemm(_ptr(A), at, int(bool(transA)), M, K, float(a_scale), int(a_zero_point), _ptr(B), bt,
+                          int(bool(transB)), N, _ptr(bs), _ptr(bz), bs.size, _ptr(c), cr, cc, float(alpha),
+                          int(quant), float(y_scale) if quant else 1.0,
+                          int(y_zero_point) if quant and y_zero_point is not None else 0, yt, _ptr(Y)), "qgemm")
+    return Y
 
 
 def lstm_cell(Gx, Gh, Wb, Rb, c_prev):

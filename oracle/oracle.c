@@ -23,6 +23,8 @@
  *  [QLC] onnx-light docs, "QLinearConv" (inputs, bias rule, examples)
  *  [LSTM] ONNX Runtime contrib schemas, "DynamicQuantizeLSTM" (inputs W, R, B,
  *         initial_h/c, outputs Y, Y_h, Y_c); graiphic.io "DynamicQuantizeLSTM"
+ *  [QG]  ONNX Runtime contrib schemas, "QGemm" (inputs A .. y_zero_point,
+ *         attributes transA, transB, alpha)
  *
  * Where the pages leave a step open the readings used are listed in the
  * repository's design notes; each is restated at the function below.
@@ -320,6 +322,60 @@ int or_qlinearconv(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
           v = v / y_scale;
           store_q(y, ytype, ((n * M + m) * OH + oh) * OW + ow, sat_rint_plus(v, y_zero_point, lo, hi));
         }
+      }
+    }
+  }
+  return err;
+}
+
+/* [QG] QGemm.  A is (M, K), or (K, M) when transA; B is (K, N), or (N, K)
+ * when transB; both hold 8-bit codes of type atype / btype.
+ *   acc[i,j] = sum_k (A[i,k] - a_zero_point) * (B[k,j] - b_zero_point[j])
+ *   acc += C[i,j] when C is given; C is (c_rows, c_cols) with c_rows in
+ *          {1, M} and c_cols in {1, N}, broadcast to (M, N).  Its scale is
+ *          alpha * a_scale * b_scale and its zero point 0, so it adds to the
+ *          integer sum (the page writes alpha / beta but defines no beta:
+ *          beta = 1).
+ *   y = (float)acc * ((alpha * a_scale) * b_scale[j])
+ *   quantized output: y = saturate(round_half_even(y / y_scale) + y_zero_point)
+ * The page gives no formula for the rescale; this is DequantizeLinear of the
+ * integer sum, then QuantizeLinear with (y_scale, y_zero_point), the three
+ * scale factors multiplied in the order they are listed.  b_scale and
+ * b_zero_point hold N entries when n_b == N, else one.  Y is float (M, N)
+ * unless quantize_y, then ytype codes. */
+int or_qgemm(const void* A, int atype, int transA, int64_t M, int64_t K, float a_scale, int32_t a_zero_point,
+             const void* B, int btype, int transB, int64_t N, const float* b_scale, const int32_t* b_zero_point,
+             int64_t n_b, const int32_t* C, int64_t c_rows, int64_t c_cols, float alpha, int quantize_y,
+             float y_scale, int32_t y_zero_point, int ytype, void* Y) {
+  if (!rounding_is_nearest()) return OR_ERR_ROUNDING;
+  if (n_b != 1 && n_b != N) return OR_ERR_ARG;
+  if (C && !((c_rows == 1 || c_rows == M) && (c_cols == 1 || c_cols == N))) return OR_ERR_ARG;
+  const int64_t lo = q_lo(ytype), hi = q_hi(ytype);
+  int err = OR_OK;
+#pragma omp parallel for schedule(static) reduction(min : err)
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      const int64_t bz = b_zero_point ? b_zero_point[n_b == N ? j : 0] : 0;
+      int64_t acc = 0;
+      for (int64_t k = 0; k < K; ++k) {
+        const int64_t av = load_q(A, atype, transA ? k * M + i : i * K + k);
+        const int64_t bv = load_q(B, btype, transB ? j * K + k : k * N + j);
+        acc += (av - a_zero_point) * (bv - bz);
+      }
+      if (C) acc += C[(c_rows == 1 ? 0 : i) * c_cols + (c_cols == 1 ? 0 : j)];
+      if (acc > INT32_MAX || acc < INT32_MIN) {
+        err = OR_ERR_OVERFLOW;
+        continue;
+      }
+      float mul = alpha * a_scale;
+      mul = mul * b_scale[n_b == N ? j : 0];
+      float v = (float)(int32_t)acc;
+      v = v * mul;
+      if (quantize_y) {
+        v = v / y_scale;
+        store_q(Y, ytype, i * N + j, sat_rint_plus(v, y_zero_point, lo, hi));
+      } else {
+        ((float*)Y)[i * N + j] = v;
       }
     }
   }

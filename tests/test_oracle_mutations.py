@@ -45,6 +45,13 @@ MUTATIONS = {
                                "float og = sigmoid_f32(g[2]);\n      float fg = sigmoid_f32(g[1]);"),
     "lstm_recurrent_bias_dropped": ("if (Rb) v = v + Rb[n];", "(void)Rb;"),
     "bf16_truncates": ("u += 0x7fffu + lsb;", "(void)lsb;"),
+    "qgemm_b_zero_point_per_tensor": ("const int64_t bz = b_zero_point ? b_zero_point[n_b == N ? j : 0] : 0;",
+                                      "const int64_t bz = b_zero_point ? b_zero_point[0] : 0;"),
+    "qgemm_transB_ignored": ("const int64_t bv = load_q(B, btype, transB ? j * K + k : k * N + j);",
+                             "const int64_t bv = load_q(B, btype, k * N + j);"),
+    "qgemm_C_broadcast_rows": ("if (C) acc += C[(c_rows == 1 ? 0 : i) * c_cols + (c_cols == 1 ? 0 : j)];",
+                               "if (C) acc += C[(c_cols == 1 ? 0 : j)];"),
+    "qgemm_alpha_dropped": ("float mul = alpha * a_scale;", "float mul = a_scale;"),
 }
 
 

@@ -8,6 +8,7 @@ routines.  The choice is meant to catch a dropped term, a wrong sign or
 index, or a transposed operand anywhere in the oracle.
 """
 import math
+import zlib
 from fractions import Fraction
 
 import numpy as np
@@ -461,3 +462,95 @@ def test_lstm_within_quantization_error_of_textbook(orc, direction):
         assert np.abs(ref).max() > 0.2        # non-trivial activations
         last = 0 if rev else -1
         assert np.array_equal(Yh[d], Y[last, d])
+
+
+# ---- QGemm (ONNX Runtime contrib schema "QGemm") -----------------------------
+
+def _qgemm_golden():
+    g = read_golden("qgemm_small_example.txt")
+    M, K = map(int, g["M_K"])
+    K2, N = map(int, g["K_N"])
+    A = np.array(g["A_u8"], dtype=np.int64).astype(np.uint8).reshape(M, K)
+    B = np.array(g["B_s8"], dtype=np.int64).astype(np.int8).reshape(K2, N)
+    return g, A, B
+
+
+@pytest.mark.parametrize("transA,transB", [(False, False), (True, False), (False, True), (True, True)])
+def test_qgemm_worked_example(orc, transA, transB):
+    g, A, B = _qgemm_golden()
+    a = A.T.copy() if transA else A
+    b = B.T.copy() if transB else B
+    kw = dict(b_zero_point=np.array(g["b_zero_point"], np.int32), C=np.array([g["C_1xN"]], np.int32),
+              alpha=float(g["alpha"][0]), transA=transA, transB=transB)
+    bs = np.array(g["b_scale"], np.float32)
+    y = orc.qgemm(a, float(g["a_scale"][0]), int(g["a_zero_point"][0]), b, bs, **kw)
+    assert np.array_equal(y.ravel(), np.array(g["y_float"], np.float32))
+    yq = orc.qgemm(a, float(g["a_scale"][0]), int(g["a_zero_point"][0]), b, bs, y_scale=float(g["y_scale"][0]),
+                   y_zero_point=int(g["y_zero_point"][0]), **kw)
+    assert yq.dtype == np.uint8 and np.array_equal(yq.ravel(), np.array(g["y_u8"], np.int64))
+
+
+def _exact_qgemm(A, za, B, zb, C, alpha, a_s, b_s):
+    """fp64 textbook: alpha * a_scale * b_scale * (sum (A - za)(B - zb) + C)."""
+    acc = (A.astype(np.int64) - za) @ (B.astype(np.int64) - np.asarray(zb, np.int64).reshape(1, -1))
+    if C is not None:
+        acc = acc + np.asarray(C, np.int64)
+    return acc, alpha * a_s * np.asarray(b_s, np.float64).reshape(1, -1) * acc
+
+
+@pytest.mark.parametrize("atype,btype", [("u8", "s8"), ("s8", "s8"), ("u8", "u8"), ("s8", "u8")])
+@pytest.mark.parametrize("cshape", [None, "MN", "1N", "N", "M1", "11"])
+def test_qgemm_power_of_two_scales_exact(orc, atype, btype, cshape):
+    """With power-of-two scales and alpha and |acc| < 2^24 every fp32 step
+    is exact, so the float output equals the fp64 textbook value."""
+    rng = np.random.default_rng(zlib.crc32(f"{atype}{btype}{cshape}".encode()))
+    M, K, N = 5, 37, 6
+    lo = {"u8": (0, 256), "s8": (-128, 128)}
+    dt = {"u8": np.uint8, "s8": np.int8}
+    A = rng.integers(*lo[atype], (M, K)).astype(dt[atype])
+    B = rng.integers(*lo[btype], (K, N)).astype(dt[btype])
+    za = int(rng.integers(*lo[atype]))
+    zb = rng.integers(*lo[btype], N).astype(np.int32)
+    bs = np.float32(2.0) ** rng.integers(-8, -2, N).astype(np.float32)
+    C = {None: None, "MN": rng.integers(-999, 999, (M, N)), "1N": rng.integers(-999, 999, (1, N)),
+         "N": rng.integers(-999, 999, N), "M1": rng.integers(-999, 999, (M, 1)),
+         "11": rng.integers(-999, 999, (1, 1))}[cshape]
+    y = orc.qgemm(A, 0.25, za, B, bs, zb, C=C, alpha=0.5)
+    acc, ref = _exact_qgemm(A, za, B, zb, None if C is None else np.broadcast_to(np.asarray(C).reshape(
+        (1, -1) if np.asarray(C).ndim == 1 else np.asarray(C).shape), (M, N)), 0.5, 0.25, bs)
+    assert np.abs(acc).max() < 2**24
+    assert np.array_equal(y.astype(np.float64), ref)
+
+
+def test_qgemm_quantized_output_is_quantize_linear_of_float_output(orc):
+    """The quantized output is QuantizeLinear of the float output (same
+    fp32 value divided by y_scale), for both output types."""
+    rng = np.random.default_rng(3)
+    A = rng.integers(0, 256, (9, 70)).astype(np.uint8)
+    B = rng.integers(-128, 128, (70, 11)).astype(np.int8)
+    bs = rng.uniform(1e-3, 1e-2, 11).astype(np.float32)
+    y = orc.qgemm(A, 0.02, 131, B, bs, alpha=1.5)
+    for zp, t in ((np.uint8(120), "u8"), (np.int8(-3), "s8")):
+        yq = orc.qgemm(A, 0.02, 131, B, bs, alpha=1.5, y_scale=0.37, y_zero_point=int(zp), ytype=t)
+        ref = orc.quantize_linear(y, np.float32(0.37), np.array(zp), ytype=t)
+        assert np.array_equal(yq, ref)
+
+
+def test_qgemm_brute_force_matches_integer_definition(orc):
+    """Tiny shapes, every combination of per-tensor / per-column B
+    parameters: the integer sum before rescaling, recovered with unit scales,
+    equals the definition evaluated directly in int64."""
+    rng = np.random.default_rng(8)
+    for M, K, N in [(1, 1, 1), (2, 3, 4), (3, 1, 2), (4, 5, 1)]:
+        A = rng.integers(-128, 128, (M, K)).astype(np.int8)
+        B = rng.integers(0, 256, (K, N)).astype(np.uint8)
+        for per_col in (False, True):
+            zb = rng.integers(0, 256, N if per_col else 1).astype(np.int32)
+            bs = np.ones(N if per_col else 1, np.float32)
+            y = orc.qgemm(A, 1.0, -7, B, bs, zb)
+            ref = np.zeros((M, N), np.int64)
+            for i in range(M):
+                for j in range(N):
+                    z = int(zb[j if per_col else 0])
+                    ref[i, j] = sum((int(A[i, k]) + 7) * (int(B[k, j]) - z) for k in range(K))
+            assert np.array_equal(y.astype(np.int64), ref)
