@@ -345,6 +345,22 @@ def measure_rows(args, dev, stream, world):
                     "workload": "x u8 [32,256,56,56], w [256,%d,3,3], pad 1, per-channel w" % c["w"].shape[1]}
         del x, wt, y, wsp
 
+    # QGemm at the large GEMM's shape: u8 A x s8 B with per-column
+    # parameters, int32 C of shape (1, N), alpha, u8 output
+    w = workloads.qgemm(seed=5)
+    A, B = t(w["A"]), t(w["B"])
+    bs, bz, Cb = t(w["b_scale"]), t(w["b_zero_point"]), t(w["C"])
+    Y = torch.empty(M, N, dtype=torch.uint8, device=dev)
+    wsp = torch.empty(q.qgemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+    fn = lambda: q.qgemm(A, float(w["a_scale"]), w["a_zero_point"], B, bs, Y, b_zero_point=bz, C=Cb,  # noqa: E731
+                         alpha=float(w["alpha"]), y_scale=float(w["y_scale"]), y_zero_point=w["y_zero_point"],
+                         workspace=wsp)
+    sec, prof = _timed(fn, steps, warm, stream)
+    out["qgemm_u8s8_to_u8"] = {"ms": sec * 1e3, "TOPS": 2.0 * M * N * K / sec / 1e12, "kernels": prof,
+                               "workload": "QGemm M=8192 K=4096 N=14336, u8 A, s8 B per-column scale and zero point, "
+                                           "C (1,N), alpha 1.5, u8 Y; both operands centred every call"}
+    del A, B, Y, wsp
+
     # DynamicQuantizeLSTM, bidirectional T=512 batch=64 I=H=1024
     w = workloads.lstm(seed=4)
     T_, b_, I_, H_ = 512, 64, 1024, 1024

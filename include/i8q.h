@@ -32,6 +32,9 @@
  *  [LSTM] ONNX Runtime contrib schemas, "DynamicQuantizeLSTM": attributes,
  *         inputs X, W, R, B, initial_h, initial_c, W/R scale and zero point,
  *         outputs Y, Y_h, Y_c.
+ *  [QG]   ONNX Runtime contrib schemas, "QGemm": inputs A, a_scale,
+ *         a_zero_point, B, b_scale, b_zero_point, C, y_scale, y_zero_point;
+ *         attributes transA, transB, alpha.
  */
 #ifndef I8Q_H
 #define I8Q_H
@@ -271,6 +274,39 @@ int i8q_qlinearconv(const void* x, int xtype, const int64_t* xshape, float x_sca
  * i8q_qlinearconv).  Returns 0 on invalid shapes. */
 size_t i8q_qlinearconv_workspace_size(const int64_t* xshape, const int64_t* wshape, const int64_t* pads,
                                       const int64_t* strides, const int64_t* dilations, int64_t group);
+
+/* ========================================================================
+ * QGemm [QG] (ONNX Runtime contrib schemas, "QGemm", inputs A .. y_zero_point
+ * and attributes transA, transB, alpha):
+ *   acc[i,j] = sum_k (A[i,k] - a_zero_point) * (B[k,j] - b_zero_point[j])
+ *   acc += C[i,j]            (int32; scale alpha * a_scale * b_scale, zp 0)
+ *   y = (float)acc * ((alpha * a_scale) * b_scale[j])
+ *   quantized output: y = saturate(rint(y / y_scale) + y_zero_point)
+ * The schema gives C the scale alpha / beta * a_scale * b_scale but defines
+ * no beta; it is read as 1.  The rescale is DequantizeLinear of the integer
+ * sum, then QuantizeLinear (the schema gives no formula).
+ *   A: device, atype (U8|S8) codes, (M, K) row-major, or (K, M) if transA.
+ *   a_scale, a_zero_point: per-tensor scalars (host values); a_zero_point
+ *   within A's range.
+ *   B: device, btype (U8|S8) codes, (K, N) row-major, or (N, K) if transB.
+ *   b_scale: device fp32, n_b == 1 (per tensor) or N (per column) entries.
+ *   b_zero_point: device, btype, n_b entries, or NULL (zero).
+ *   C: device int32 (c_rows, c_cols) row-major with c_rows in {1, M} and
+ *   c_cols in {1, N}, broadcast to (M, N); or NULL.
+ *   quantize_y == 0: Y is fp32 (M, N).  Otherwise Y holds ytype (U8|S8)
+ *   codes with y_scale / y_zero_point (host values).
+ *   workspace: device scratch of at least i8q_qgemm_workspace_size bytes,
+ *   256-byte aligned (the centred bf16 operands, their sums and the column
+ *   parameters); the caller owns it and all tensors.
+ * Errors: INVALID_ARG (types, ranges, shapes, workspace), UNSUPPORTED
+ * (K > 65536), CUDA. */
+int i8q_qgemm(const void* A, int atype, int transA, int64_t M, int64_t K, float a_scale, int a_zero_point,
+              const void* B, int btype, int transB, int64_t N, const float* b_scale, const void* b_zero_point,
+              size_t n_b, const int32_t* C, int64_t c_rows, int64_t c_cols, float alpha, int quantize_y,
+              float y_scale, int y_zero_point, int ytype, void* Y, void* workspace, size_t ws_bytes, void* stream);
+
+/* Scratch bytes i8q_qgemm needs for M x N x K (0 for sizes below 1). */
+size_t i8q_qgemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /* ========================================================================
  * DynamicQuantizeLSTM [LSTM]: int8 W and R with per-channel (or

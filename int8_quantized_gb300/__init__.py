@@ -247,6 +247,48 @@ def qlinearconv(x, x_scale, x_zero_point, w, w_scale, w_zero_point, y_scale, y_z
     return y
 
 
+def qgemm_workspace_size(M, N, K):
+    return int(_L().i8q_qgemm_workspace_size(M, N, K))
+
+
+def qgemm(A, a_scale, a_zero_point, B, b_scale, Y, b_zero_point=None, C=None, alpha=1.0, y_scale=None,
+          y_zero_point=0, transA=False, transB=False, workspace=None, stream=None):
+    """QGemm.  A: uint8/int8 CUDA (M, K), or (K, M) with transA; B: uint8/int8
+    CUDA (K, N), or (N, K) with transB; a_scale, a_zero_point: Python
+    scalars; b_scale: fp32 CUDA tensor of 1 or N entries; b_zero_point: B's
+    dtype, same count, or None; C: int32 CUDA tensor broadcastable to (M, N)
+    as (1|M, 1|N) or (N,), or None.  Y: fp32 (M, N), or uint8/int8 (M, N)
+    with y_scale given.  workspace: uint8 CUDA tensor of
+    qgemm_workspace_size(M, N, K) bytes; allocated here when None."""
+    M, K = (A.shape[1], A.shape[0]) if transA else (A.shape[0], A.shape[1])
+    N = B.shape[0] if transB else B.shape[1]
+    if b_zero_point is not None and b_zero_point.dtype != B.dtype:
+        raise TypeError("b_zero_point must have B's dtype")
+    cr = cc = 0
+    if C is not None:
+        if C.dim() == 0:
+            cr, cc = 1, 1
+        elif C.dim() == 1:
+            cr, cc = 1, C.shape[0]
+        else:
+            cr, cc = C.shape
+    quant = y_scale is not None
+    if quant and Y.dtype not in (torch.uint8, torch.int8):
+        raise TypeError("quantized Y must be uint8 or int8")
+    if not quant and Y.dtype != torch.float32:
+        raise TypeError("Y must be float32 when y_scale is None")
+    if workspace is None:
+        workspace = torch.empty(qgemm_workspace_size(M, N, K), dtype=torch.uint8, device=Y.device)
+    check(_L().i8q_qgemm(_dev(A, "A"), _TORCH_TYPE[A.dtype], int(bool(transA)), M, K, float(a_scale),
+                         int(a_zero_point), _dev(B, "B"), _TORCH_TYPE[B.dtype], int(bool(transB)), N,
+                         _dev(b_scale, "b_scale", torch.float32), _dev(b_zero_point, "b_zero_point"),
+                         b_scale.numel(), _dev(C, "C", torch.int32), cr, cc, float(alpha), int(quant),
+                         float(y_scale) if quant else 1.0, int(y_zero_point), _TORCH_TYPE[Y.dtype], _dev(Y, "Y"),
+                         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream)),
+          "qgemm")
+    return Y
+
+
 def dq_lstm_workspace_size(T, batch, input_size, hidden, direction):
     return int(_L().i8q_dq_lstm_workspace_size(T, batch, input_size, hidden, direction))
 

@@ -214,6 +214,29 @@ struct GemmEpilogue {
   int64_t ldc;            // elements
 };
 
+// Epilogue of QGemm on the tensor-core path.  The operands enter centred,
+// A' = A - ca and B' = B - cb (ca, cb = 128 for uint8 codes, 0 for int8), so
+// with run = sum_k A'[i,k] B'[k,j]:
+//   acc = run + rowsum[i] * g[j] + h[j] + C[i,j]
+//   rowsum[i] = sum_k A'[i,k],  g[j] = cb - b_zero_point[j],
+//   h[j] = (ca - a_zero_point) * sum_k B'[k,j] + K (ca - a_zero_point) g[j]
+// (int32, wrapping: the true sum fits int32, so the modular result is it),
+// then y = (float)acc * mult[j] with mult[j] = (alpha * a_scale) * b_scale[j],
+// stored as fp32 or requantized: saturate(rint(y / y_scale) + y_zero_point).
+struct QgEpilogue {
+  const int32_t* rowsum;  // [M]
+  const int32_t* g;       // [N]
+  const int32_t* h;       // [N]
+  const float* mult;      // [N]
+  const int32_t* C;       // element (i, j) at C[i * c_si + j * c_sj], or null
+  int64_t c_si, c_sj;
+  int ytype;              // I8Q_F32, I8Q_U8 or I8Q_S8
+  float y_scale;
+  int y_zero_point;
+  void* Y;
+  int64_t ldy;
+};
+
 // Integer GEMM core: sum_k uA[i,k] * iBt[j,k] (uint8 x int8), corrected by
 // -zeroA[i]*colsum[j], then the epilogue.  uA is M x Kp (row stride Kp),
 // iBt is N x Kp, Kp a multiple of 64 with zero padding beyond K.
@@ -226,6 +249,11 @@ int launch_gemm_imma(const uint8_t* uA, const int8_t* iBt, int64_t M, int64_t N,
 // Returns I8Q_ERR_UNSUPPORTED when the shape is outside what it handles.
 int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M, int64_t N,
                    int64_t Kp, int max_abs_product_log2, const GemmEpilogue& ep, cudaStream_t s);
+
+// The same product of centred operands A' (M x Kp) and B' (N x Kp) with the
+// QGemm epilogue.
+int launch_qgemm_tc(const __nv_bfloat16* Ac, const __nv_bfloat16* Bc, int64_t M, int64_t N, int64_t Kp,
+                    int max_abs_product_log2, const QgEpilogue& qg, cudaStream_t s);
 
 // Small products in one launch: row quantization of A (fp32/bf16, row
 // stride K) into uA / scaleA / zeroA, then the integer sums against iBt

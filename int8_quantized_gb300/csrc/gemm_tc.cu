@@ -59,9 +59,13 @@ struct TcParams {
   int CS;        // K steps per exact fp32 chunk
   int tiles_m, tiles_n;
   int num_tiles;
-  GemmEpilogue ep;
+  GemmEpilogue ep;  // the dynamic quantized inner product (EPI_DYN)
+  QgEpilogue qg;    // QGemm (EPI_QG)
   uint32_t* status;
 };
+
+// Epilogue kinds the kernels are instantiated for.
+constexpr int EPI_DYN = 0, EPI_QG = 1;
 
 using namespace tc;
 
@@ -147,6 +151,98 @@ __device__ __forceinline__ void store_slice(const GemmEpilogue& ep, int64_t row,
   }
 }
 
+// QGemm epilogue of one row's 64-column slice (see QgEpilogue): column
+// parameters pg (g), pm (mult), ph (h) from shared memory, rs = rowsum[row].
+__device__ __forceinline__ void store_slice_qg(const QgEpilogue& qg, int64_t row, int64_t col0, int64_t N,
+                                               const int32_t (&run)[SLICE], int32_t rs, const int32_t* pg,
+                                               const float* pm, const int32_t* ph) {
+  const bool full = col0 + SLICE <= N;
+  const int32_t* crow = qg.C ? qg.C + row * qg.c_si : nullptr;
+  auto sum_at = [&](int j) -> int32_t {
+    // wrapping int32 arithmetic: the exact sum fits int32
+    uint32_t a = (uint32_t)run[j] + (uint32_t)rs * (uint32_t)pg[j] + (uint32_t)ph[j];
+    if (crow && col0 + j < N) a += (uint32_t)__ldg(crow + (col0 + j) * qg.c_sj);
+    return (int32_t)a;
+  };
+  if (qg.ytype == I8Q_F32) {
+    float* Y = static_cast<float*>(qg.Y) + row * qg.ldy + col0;
+    const bool vec = full && (qg.ldy % 4 == 0) && (reinterpret_cast<uintptr_t>(qg.Y) & 15) == 0;
+#pragma unroll
+    for (int j = 0; j < SLICE; j += 4) {
+      float o[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) o[u] = __fmul_rn(__int2float_rn(sum_at(j + u)), pm[j + u]);
+      if (vec) {
+        *reinterpret_cast<float4*>(Y + j) = make_float4(o[0], o[1], o[2], o[3]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (col0 + j + u < N) Y[j + u] = o[u];
+      }
+    }
+    return;
+  }
+  const int zp = qg.y_zero_point;
+  const float lo = (qg.ytype == I8Q_U8 ? 0.0f : -128.0f) - (float)zp;
+  const float hi = (qg.ytype == I8Q_U8 ? 255.0f : 127.0f) - (float)zp;
+  uint8_t* Y = static_cast<uint8_t*>(qg.Y) + row * qg.ldy + col0;
+  const bool vec = full && (qg.ldy % 16 == 0) && (reinterpret_cast<uintptr_t>(qg.Y) & 15) == 0;
+#pragma unroll
+  for (int j = 0; j < SLICE; j += 16) {
+    uint32_t b[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float v = __fmul_rn(__int2float_rn(sum_at(j + u)), pm[j + u]);
+      b[u] = rint_code_bits(__fdiv_rn(v, qg.y_scale), lo, hi, zp);
+    }
+    if (vec) {
+      *reinterpret_cast<uint4*>(Y + j) =
+          make_uint4(pack_low_bytes(b[0], b[1], b[2], b[3]), pack_low_bytes(b[4], b[5], b[6], b[7]),
+                     pack_low_bytes(b[8], b[9], b[10], b[11]), pack_low_bytes(b[12], b[13], b[14], b[15]));
+    } else {
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (col0 + j + u < N) Y[j + u] = (uint8_t)b[u];
+    }
+  }
+}
+
+// Stage one epilogue warp's column parameters for the tile (read back after
+// the K loop).
+template <int EPI>
+__device__ __forceinline__ void stage_params(const TcParams& p, int64_t col0, int lane, int32_t* pc, float* ps,
+                                             float* pb) {
+  for (int j = lane; j < SLICE; j += 32) {
+    const int64_t c = col0 + j;
+    const bool in = c < p.N;
+    if constexpr (EPI == EPI_DYN) {
+      pc[j] = in ? __ldg(p.ep.colsum + c) : 0;
+      ps[j] = in ? __ldg(p.ep.scaleB + c) : 0.0f;
+      pb[j] = (in && p.ep.bias) ? __ldg(p.ep.bias + c) : 0.0f;
+    } else {
+      pc[j] = in ? __ldg(p.qg.g + c) : 0;
+      ps[j] = in ? __ldg(p.qg.mult + c) : 0.0f;
+      reinterpret_cast<int32_t*>(pb)[j] = in ? __ldg(p.qg.h + c) : 0;
+    }
+  }
+}
+
+// The epilogue of one row of the tile from its exact sums.
+template <int EPI>
+__device__ __forceinline__ void finish_row(const TcParams& p, int64_t row, int64_t col0, const int32_t (&run)[SLICE],
+                                           const int32_t* pc, const float* ps, const float* pb) {
+  if constexpr (EPI == EPI_DYN) {
+    const float sA = __ldg(p.ep.scaleA + row);
+    // A entered as uA - 128: sum_k (uA - zA) iB = run - (zA - 128) colsum
+    const int32_t zA = __ldg(p.ep.zeroA + row) - 128;
+    store_slice(p.ep, row, col0, p.N, run, zA, sA, pc, ps, pb);
+  } else {
+    store_slice_qg(p.qg, row, col0, p.N, run, __ldg(p.qg.rowsum + row), pc, ps,
+                   reinterpret_cast<const int32_t*>(pb));
+  }
+}
+
+template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -283,13 +379,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tile_coords(tile, p.tiles_m, p.tiles_n, mt, nt);
       const int64_t col0 = (int64_t)nt * BN + slice * SLICE;
       // stage this slice's column parameters (read back after the K loop)
-      for (int j = lane; j < SLICE; j += 32) {
-        const int64_t c = col0 + j;
-        const bool in = c < p.N;
-        pc[j] = in ? __ldg(p.ep.colsum + c) : 0;
-        ps[j] = in ? __ldg(p.ep.scaleB + c) : 0.0f;
-        pb[j] = (in && p.ep.bias) ? __ldg(p.ep.bias + c) : 0.0f;
-      }
+      stage_params<EPI>(p, col0, lane, pc, ps, pb);
       int32_t run[SLICE];
 #pragma unroll
       for (int j = 0; j < SLICE; ++j) run[j] = 0;
@@ -323,12 +413,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (!ok) break;
       __syncwarp();
       const int64_t row = (int64_t)mt * BM + q * 32 + lane;
-      if (row < p.M) {
-        const float sA = __ldg(p.ep.scaleA + row);
-        // A entered as uA - 128: sum_k (uA - zA) iB = run - (zA - 128) colsum
-        const int32_t zA = __ldg(p.ep.zeroA + row) - 128;
-        store_slice(p.ep, row, col0, p.N, run, zA, sA, pc, ps, pb);
-      }
+      if (row < p.M) finish_row<EPI>(p, row, col0, run, pc, ps, pb);
       __syncwarp();
     }
   }
@@ -389,6 +474,7 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
   return r;
 }
 
+template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -552,13 +638,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       int mt, nt;
       tile_coords_g(tile, p.tiles_m, p.tiles_n, P_GROUP_M, mt, nt);
       const int64_t col0 = (int64_t)nt * PBN + slice * SLICE;
-      for (int j = lane; j < SLICE; j += 32) {
-        const int64_t c = col0 + j;
-        const bool in = c < p.N;
-        pc[j] = in ? __ldg(p.ep.colsum + c) : 0;
-        ps[j] = in ? __ldg(p.ep.scaleB + c) : 0.0f;
-        pb[j] = (in && p.ep.bias) ? __ldg(p.ep.bias + c) : 0.0f;
-      }
+      stage_params<EPI>(p, col0, lane, pc, ps, pb);
       int32_t run[SLICE];
 #pragma unroll
       for (int j = 0; j < SLICE; ++j) run[j] = 0;
@@ -591,11 +671,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       if (!ok) break;
       __syncwarp();
       const int64_t row = (int64_t)mt * PBM + (int64_t)rank * HALF_ROWS + q * 32 + lane;
-      if (row < p.M) {
-        const float sA = __ldg(p.ep.scaleA + row);
-        const int32_t zA = __ldg(p.ep.zeroA + row) - 128;
-        store_slice(p.ep, row, col0, p.N, run, zA, sA, pc, ps, pb);
-      }
+      if (row < p.M) finish_row<EPI>(p, row, col0, run, pc, ps, pb);
       __syncwarp();
     }
   }
@@ -610,16 +686,15 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   }
 }
 
-}  // namespace
-
 // Clusters of two CTAs of the pair kernel that fit on the device at once
-// (0 when none do; -1 on a CUDA error), computed once.
+// (0 when none do; -1 on a CUDA error), computed once per instantiation.
+template <int EPI>
 int pair_max_clusters() {
   static std::once_flag once;
   static int n = -1;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+    err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
     if (err != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -633,7 +708,7 @@ int pair_max_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int c = 0;
-    err = cudaOccupancyMaxActiveClusters(&c, gemm_tc_pair_kernel, &cfg);
+    err = cudaOccupancyMaxActiveClusters(&c, gemm_tc_pair_kernel<EPI>, &cfg);
     if (err == cudaSuccess) n = c;
   });
   if (err != cudaSuccess) {
@@ -643,8 +718,12 @@ int pair_max_clusters() {
   return n;
 }
 
-int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M, int64_t N, int64_t Kp,
-                   int max_abs_product_log2, const GemmEpilogue& ep, cudaStream_t s) {
+// Shared launch of both kernels for either epilogue kind.  prof1 / prof2
+// name the single-CTA and pair launches in the kernel timing.
+template <int EPI>
+int launch_tc_impl(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M, int64_t N, int64_t Kp,
+                   int max_abs_product_log2, const TcParams& base, cudaStream_t s, const char* prof1,
+                   const char* prof2) {
   if (M <= 0 || N <= 0) return I8Q_OK;
   if (!uA || !iBt) return fail(I8Q_ERR_UNSUPPORTED, "gemm_tc: bf16 operands missing");
   if (Kp % BK != 0 || Kp > (int64_t)1 << 20) return fail(I8Q_ERR_UNSUPPORTED, "gemm_tc: Kp must be a multiple of 64");
@@ -658,34 +737,29 @@ int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M,
   const int CS = (int)std::max<int64_t>(1, chunk_k / BK);
   uint32_t* status = device_status_word();
   if (!status) return fail(I8Q_ERR_CUDA, "gemm_tc: no device status word");
-  CUtensorMap mA, mB;
-  int rc = make_map_2d(&mA, uA, M, Kp, BM, "gemm_tc");
-  if (rc) return rc;
-  rc = make_map_2d(&mB, iBt, N, Kp, BN, "gemm_tc");
-  if (rc) return rc;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(gemm_tc_kernel)");
-  TcParams p;
+  TcParams p = base;
   p.M = M;
   p.N = N;
   p.KT = (int)(Kp / BK);
   p.CS = CS;
-  p.ep = ep;
   p.status = status;
 
   // CTA pairs when there is at least a wave of 256 x 256 tiles;
   // I8Q_FORCE_CORE=tc1 / tc2 picks the single-CTA / pair kernel.
   const char* force = getenv("I8Q_FORCE_CORE");
-  const int pair_clusters = pair_max_clusters();
+  const int pair_clusters = pair_max_clusters<EPI>();
   if (pair_clusters < 0) return I8Q_ERR_CUDA;
   const int64_t pair_tiles = ceil_div(M, PBM) * ceil_div(N, PBN);
   bool use_pair = M >= PBM && pair_clusters > 0 && pair_tiles >= pair_clusters;
   if (force && std::string(force) == "tc1") use_pair = false;
   if (force && std::string(force) == "tc2") use_pair = pair_clusters > 0;
+  int rc;
   if (use_pair) {
     CUtensorMap pA, pB;
     rc = make_map_2d(&pA, uA, M, Kp, HALF_ROWS, "gemm_tc");
@@ -708,19 +782,40 @@ int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M,
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    I8Q_PROF("gemm_tc_pair", s);
-    I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel, pA, pB, p));
+    I8Q_PROF(prof2, s);
+    I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI>, pA, pB, p));
     I8Q_LAUNCH_CHECK("gemm_tc_pair_kernel");
     return I8Q_OK;
   }
+  CUtensorMap mA, mB;
+  rc = make_map_2d(&mA, uA, M, Kp, BM, "gemm_tc");
+  if (rc) return rc;
+  rc = make_map_2d(&mB, iBt, N, Kp, BN, "gemm_tc");
+  if (rc) return rc;
   p.tiles_m = (int)ceil_div(M, BM);
   p.tiles_n = (int)ceil_div(N, BN);
   p.num_tiles = p.tiles_m * p.tiles_n;
   const int grid = std::min(p.num_tiles, sm_count());
-  I8Q_PROF("gemm_tc", s);
-  gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(mA, mB, p);
+  I8Q_PROF(prof1, s);
+  gemm_tc_kernel<EPI><<<grid, THREADS, SMEM_BYTES, s>>>(mA, mB, p);
   I8Q_LAUNCH_CHECK("gemm_tc_kernel");
   return I8Q_OK;
+}
+
+}  // namespace
+
+int launch_gemm_tc(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M, int64_t N, int64_t Kp,
+                   int max_abs_product_log2, const GemmEpilogue& ep, cudaStream_t s) {
+  TcParams p{};
+  p.ep = ep;
+  return launch_tc_impl<EPI_DYN>(uA, iBt, M, N, Kp, max_abs_product_log2, p, s, "gemm_tc", "gemm_tc_pair");
+}
+
+int launch_qgemm_tc(const __nv_bfloat16* Ac, const __nv_bfloat16* Bc, int64_t M, int64_t N, int64_t Kp,
+                    int max_abs_product_log2, const QgEpilogue& qg, cudaStream_t s) {
+  TcParams p{};
+  p.qg = qg;
+  return launch_tc_impl<EPI_QG>(Ac, Bc, M, N, Kp, max_abs_product_log2, p, s, "qgemm_tc", "qgemm_tc_pair");
 }
 
 }  // namespace i8q

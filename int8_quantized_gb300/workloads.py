@@ -12,6 +12,8 @@ Workloads (sizes are the defaults; every generator takes smaller ones):
   large_gemm      dynamic quantized GEMM M=8192 K=4096 N=14336, bf16 A
   qlinearconv     u8 NCHW [32,256,56,56] with a 3x3 (or depthwise) filter
   lstm            bidirectional DynamicQuantizeLSTM, T=512 batch=64 I=H=1024
+  qgemm           QGemm of 8-bit codes, M=8192 K=4096 N=14336 (the large GEMM's
+                  shape), per-column B parameters, int32 C of shape (1, N)
 """
 import numpy as np
 import torch
@@ -155,3 +157,31 @@ def lstm(seed=4, T=512, batch=64, I=1024, H=1024, D=2):
     Bias = _normal(g, (D, 8 * H), 0.1)
     return {"X": X, "W": Wq, "R": Rq, "W_scale": W_scale, "R_scale": R_scale, "B": Bias,
             "W_zero_point": np.zeros((D, 4 * H), np.int8), "R_zero_point": np.zeros((D, 4 * H), np.int8)}
+
+
+def qgemm(seed=5, M=8192, K=4096, N=14336, atype="u8", btype="s8", per_column=True, c_shape="1N"):
+    """8-bit A (M, K) and B (K, N) codes ~U over the type's range; a_scale
+    0.02, a_zero_point ~U over A's range; b_scale ~U(1e-3, 1e-2) and
+    b_zero_point ~U over B's range, per column (or one of each); C int32
+    ~U{-5000..5000} of shape c_shape ("MN", "1N", "N", "M1", "11" or None);
+    alpha 1.5; y_scale 0.05 and y_zero_point ~U over the output type's range
+    for a quantized output of A's type."""
+    g = _gen(seed)
+    rng = {"u8": (0, 255, np.uint8), "s8": (-128, 127, np.int8)}
+    alo, ahi, adt = rng[atype]
+    blo, bhi, bdt = rng[btype]
+    nb = N if per_column else 1
+    out = {
+        "A": _randint(g, (M, K), alo, ahi, adt),
+        "B": _randint(g, (K, N), blo, bhi, bdt),
+        "a_scale": np.float32(0.02),
+        "a_zero_point": int(_randint(g, (1,), alo, ahi, np.int64)[0]),
+        "b_scale": _uniform(g, (nb,), 1e-3, 1e-2),
+        "b_zero_point": _randint(g, (nb,), blo, bhi, bdt),
+        "alpha": np.float32(1.5),
+        "y_scale": np.float32(0.05),
+        "y_zero_point": int(_randint(g, (1,), alo, ahi, np.int64)[0]),
+    }
+    shapes = {"MN": (M, N), "1N": (1, N), "N": (N,), "M1": (M, 1), "11": (1, 1), None: None}
+    out["C"] = None if c_shape is None else _randint(g, shapes[c_shape], -5000, 5000, np.int32)
+    return out

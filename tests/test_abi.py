@@ -121,3 +121,24 @@ def test_lstm_validation(lib):
     rc = lib.i8q_dq_lstm_forward(p, 2, 3, 8, 4, 2, p, p, None, 2, p, p, None, 2, None, None, None, None, None, None,
                                  p, 16, None)
     assert rc == _lib.ERR_INVALID_ARG and b"workspace" in lib.i8q_last_error()
+
+
+def test_qgemm_validation(lib):
+    from int8_quantized_gb300 import _lib
+    p = ctypes.c_void_p(256)
+    assert lib.i8q_qgemm_workspace_size(0, 4, 4) == 0
+    assert lib.i8q_qgemm_workspace_size(3, 5, 7) > 0
+
+    def call(atype=_lib.U8, btype=_lib.S8, M=4, K=8, N=3, za=0, n_b=1, C=None, cr=0, cc=0, quant=0, yzp=0,
+             ytype=_lib.U8, ws=1 << 20):
+        return lib.i8q_qgemm(p, atype, 0, M, K, 0.1, za, p, btype, 0, N, p, None, n_b, C, cr, cc, 1.0, quant, 0.5, yzp,
+                             ytype, p, p, ws, None)
+    assert call(atype=_lib.F32) == _lib.ERR_INVALID_ARG and b"U8 or I8Q_S8" in lib.i8q_last_error()
+    assert call(n_b=2) == _lib.ERR_INVALID_ARG and b"b_scale" in lib.i8q_last_error()
+    assert call(za=256) == _lib.ERR_INVALID_ARG and b"a_zero_point" in lib.i8q_last_error()
+    assert call(atype=_lib.S8, za=200) == _lib.ERR_INVALID_ARG
+    assert call(C=p, cr=2, cc=3) == _lib.ERR_INVALID_ARG and b"broadcastable" in lib.i8q_last_error()
+    assert call(quant=1, ytype=_lib.F32) == _lib.ERR_INVALID_ARG
+    assert call(quant=1, ytype=_lib.S8, yzp=128) == _lib.ERR_INVALID_ARG
+    assert call(ws=16) == _lib.ERR_INVALID_ARG and b"workspace" in lib.i8q_last_error()
+    assert call(K=70000) == _lib.ERR_UNSUPPORTED
