@@ -40,8 +40,10 @@ def load(path):
     l.or_lstm_cell.argtypes = [p, p, p, p, p, p, p, i64, i64]
     l.or_qgemm.argtypes = [p, c_int, c_int, i64, i64, f32, i32, p, c_int, c_int, i64, p, p, i64, p, i64, i64,
                            f32, c_int, f32, i32, c_int, p]
+    l.or_matmul_integer_to_float.argtypes = [p, c_int, i64, i64, p, c_int, i64, p, p, i64, p, p, i64, p, p]
     for fn in ("or_quantize_linear", "or_dequantize_linear", "or_quantize_rows_u8",
-               "or_quantize_cols_s8", "or_qgemm_dyn_rows", "or_qlinearconv", "or_lstm_cell", "or_qgemm"):
+               "or_quantize_cols_s8", "or_qgemm_dyn_rows", "or_qlinearconv", "or_lstm_cell", "or_qgemm",
+               "or_matmul_integer_to_float"):
         getattr(l, fn).restype = ctypes.c_int
     return l
 
@@ -270,6 +272,50 @@ def qgemm(A, a_scale, a_zero_point, B, b_scale, b_zero_point=None, C=None, alpha
                           int(quant), float(y_scale) if quant else 1.0,
                           int(y_zero_point) if quant and y_zero_point is not None else 0, yt, _ptr(Y)), "qgemm")
     return Y
+
+
+def matmul_integer_to_float(A, B, a_scale, b_scale, a_zero_point=None, b_zero_point=None, bias=None):
+    """MatMulIntegerToFloat (ONNX Runtime contrib schemas).  A: uint8/int8
+    (..., K), B: uint8/int8 (K, N); a_scale / a_zero_point: 1 entry or one
+    per row of A (rows = all leading dimensions); b_scale / b_zero_point: 1
+    or N entries; bias: N floats or None.  Returns fp32 (..., N)."""
+    A = np.asarray(A)
+    lead = A.shape[:-1]
+    A2 = np.ascontiguousarray(A.reshape(-1, A.shape[-1]))
+    B = np.ascontiguousarray(B)
+    M, K = A2.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    at = U8 if A.dtype == np.uint8 else S8
+    bt = U8 if B.dtype == np.uint8 else S8
+    asc = np.ascontiguousarray(np.atleast_1d(a_scale), dtype=np.float32)
+    bsc = np.ascontiguousarray(np.atleast_1d(b_scale), dtype=np.float32)
+    az = None if a_zero_point is None else np.ascontiguousarray(np.atleast_1d(a_zero_point), dtype=np.int32)
+    bz = None if b_zero_point is None else np.ascontiguousarray(np.atleast_1d(b_zero_point), dtype=np.int32)
+    if asc.size not in (1, M) or (az is not None and az.size != asc.size):
+        raise ValueError("a_scale / a_zero_point must have 1 entry or one per row of A")
+    if bsc.size not in (1, N) or (bz is not None and bz.size != bsc.size):
+        raise ValueError("b_scale / b_zero_point must have 1 or N entries")
+    bi = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    Y = np.empty((M, N), np.float32)
+    _check(lib().or_matmul_integer_to_float(_ptr(A2), at, M, K, _ptr(B), bt, N, _ptr(asc), _ptr(az), asc.size,
+                                            _ptr(bsc), _ptr(bz), bsc.size, _ptr(bi), _ptr(Y)),
+           "matmul_integer_to_float")
+    return Y.reshape(*lead, N)
+
+
+def dynamic_quantize_matmul(A, B, b_scale, b_zero_point=None, bias=None):
+    """DynamicQuantizeMatMul (ONNX Runtime contrib schemas): fp32 A
+    (..., K) quantized to uint8 per tensor with the same formula as the rows
+    of the dynamic inner product (range widened to contain 0, scale =
+    (max - min) / 255, zero point = saturate(rint(-min / scale))), then
+    MatMulIntegerToFloat.  Returns {"Y", "uA", "a_scale", "a_zero_point"}."""
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    uA, s, z = quantize_rows_u8(A.reshape(1, -1))
+    uA = uA.reshape(A.shape)
+    Y = matmul_integer_to_float(uA, B, s[0], b_scale, np.int32(z[0]), b_zero_point, bias)
+    return {"Y": Y, "uA": uA, "a_scale": s[0], "a_zero_point": int(z[0])}
 
 
 def lstm_cell(Gx, Gh, Wb, Rb, c_prev):

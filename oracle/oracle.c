@@ -25,6 +25,8 @@
  *         initial_h/c, outputs Y, Y_h, Y_c); graiphic.io "DynamicQuantizeLSTM"
  *  [QG]  ONNX Runtime contrib schemas, "QGemm" (inputs A .. y_zero_point,
  *         attributes transA, transB, alpha)
+ *  [MITF] ONNX Runtime contrib schemas, "MatMulIntegerToFloat" and
+ *         "DynamicQuantizeMatMul" (inputs A, B, scales, zero points, bias)
  *
  * Where the pages leave a step open the readings used are listed in the
  * repository's design notes; each is restated at the function below.
@@ -377,6 +379,48 @@ int or_qgemm(const void* A, int atype, int transA, int64_t M, int64_t K, float a
       } else {
         ((float*)Y)[i * N + j] = v;
       }
+    }
+  }
+  return err;
+}
+
+/* [MITF] MatMulIntegerToFloat on 2-D operands (leading dimensions of an
+ * N-dimensional A are rows):
+ *   acc[i,j] = sum_k (A[i,k] - a_zero_point[i]) * (B[k,j] - b_zero_point[j])
+ *   Y[i,j]   = (float)acc * (a_scale[i] * b_scale[j]) + bias[j]
+ * b_scale / b_zero_point hold 1 or N entries (per tensor or per column of B).
+ * For A the schema repeats B's sentence ("per-column", "the number of
+ * columns of input 'A'"); a scale per summation index cannot be taken out
+ * of the integer sum, so the reading used is 1 entry (per tensor) or M
+ * entries (one per row of A, the dimension that remains in Y).  A missing
+ * zero point is 0, a missing bias adds nothing.  The product of the two
+ * scales is formed first, as the per-element multiplier. */
+int or_matmul_integer_to_float(const void* A, int atype, int64_t M, int64_t K, const void* B, int btype,
+                               int64_t N, const float* a_scale, const int32_t* a_zero_point, int64_t n_a,
+                               const float* b_scale, const int32_t* b_zero_point, int64_t n_b, const float* bias,
+                               float* Y) {
+  if (!rounding_is_nearest()) return OR_ERR_ROUNDING;
+  if ((n_a != 1 && n_a != M) || (n_b != 1 && n_b != N)) return OR_ERR_ARG;
+  int err = OR_OK;
+#pragma omp parallel for schedule(static) reduction(min : err)
+  for (int64_t i = 0; i < M; ++i) {
+    const int64_t pa = n_a == M ? i : 0;
+    const int64_t az = a_zero_point ? a_zero_point[pa] : 0;
+    for (int64_t j = 0; j < N; ++j) {
+      const int64_t pb = n_b == N ? j : 0;
+      const int64_t bz = b_zero_point ? b_zero_point[pb] : 0;
+      int64_t acc = 0;
+      for (int64_t k = 0; k < K; ++k)
+        acc += (load_q(A, atype, i * K + k) - az) * (load_q(B, btype, k * N + j) - bz);
+      if (acc > INT32_MAX || acc < INT32_MIN) {
+        err = OR_ERR_OVERFLOW;
+        continue;
+      }
+      float mul = a_scale[pa] * b_scale[pb];
+      float v = (float)(int32_t)acc;
+      v = v * mul;
+      if (bias) v = v + bias[j];
+      Y[i * N + j] = v;
     }
   }
   return err;

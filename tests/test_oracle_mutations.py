@@ -52,6 +52,10 @@ MUTATIONS = {
     "qgemm_C_broadcast_rows": ("if (C) acc += C[(c_rows == 1 ? 0 : i) * c_cols + (c_cols == 1 ? 0 : j)];",
                                "if (C) acc += C[(c_cols == 1 ? 0 : j)];"),
     "qgemm_alpha_dropped": ("float mul = alpha * a_scale;", "float mul = a_scale;"),
+    "mitf_a_zero_point_per_tensor": ("const int64_t az = a_zero_point ? a_zero_point[pa] : 0;",
+                                     "const int64_t az = a_zero_point ? a_zero_point[0] : 0;"),
+    "mitf_bias_dropped": ("if (bias) v = v + bias[j];", "(void)bias;"),
+    "mitf_scale_by_row_of_b": ("float mul = a_scale[pa] * b_scale[pb];", "float mul = a_scale[pa] * b_scale[0];"),
 }
 
 

@@ -554,3 +554,87 @@ def test_qgemm_brute_force_matches_integer_definition(orc):
                     z = int(zb[j if per_col else 0])
                     ref[i, j] = sum((int(A[i, k]) + 7) * (int(B[k, j]) - z) for k in range(K))
             assert np.array_equal(y.astype(np.int64), ref)
+
+
+# ---- MatMulIntegerToFloat / DynamicQuantizeMatMul (contrib schemas) -------
+
+def test_matmul_integer_to_float_worked_example(orc):
+    g = read_golden("matmul_integer_to_float_example.txt")
+    A = np.array(g["A_u8"], np.int64).astype(np.uint8).reshape(2, 2)
+    B = np.array(g["B_s8"], np.int64).astype(np.int8).reshape(2, 2)
+    Y = orc.matmul_integer_to_float(A, B, float(g["a_scale"][0]), np.array(g["b_scale"], np.float32),
+                                    np.int32(int(g["a_zero_point"][0])), np.array(g["b_zero_point"], np.int32),
+                                    np.array(g["bias"], np.float32))
+    assert np.array_equal(Y.ravel(), np.array(g["Y"], np.float32))
+
+
+@pytest.mark.parametrize("atype,btype", [("u8", "s8"), ("s8", "u8"), ("u8", "u8"), ("s8", "s8")])
+@pytest.mark.parametrize("a_rows,b_cols", [(False, False), (True, True), (True, False), (False, True)])
+def test_matmul_integer_to_float_power_of_two_exact(orc, atype, btype, a_rows, b_cols):
+    """Power-of-two scales and bias on a 2^-4 grid: every fp32 step is exact,
+    so Y equals the fp64 textbook value."""
+    rng = np.random.default_rng(zlib.crc32(f"mitf{atype}{btype}{a_rows}{b_cols}".encode()))
+    M, K, N = 6, 45, 7
+    lo = {"u8": (0, 256), "s8": (-128, 128)}
+    dt = {"u8": np.uint8, "s8": np.int8}
+    A = rng.integers(*lo[atype], (M, K)).astype(dt[atype])
+    B = rng.integers(*lo[btype], (K, N)).astype(dt[btype])
+    na, nb = (M if a_rows else 1), (N if b_cols else 1)
+    az = rng.integers(*lo[atype], na).astype(np.int32)
+    bz = rng.integers(*lo[btype], nb).astype(np.int32)
+    as_ = (2.0 ** rng.integers(-6, -1, na)).astype(np.float32)
+    bs = (2.0 ** rng.integers(-6, -1, nb)).astype(np.float32)
+    bias = (rng.integers(-64, 64, N) / 16.0).astype(np.float32)
+    Y = orc.matmul_integer_to_float(A, B, as_, bs, az, bz, bias)
+    acc = (A.astype(np.int64) - az.reshape(-1, 1)) @ (B.astype(np.int64) - bz.reshape(1, -1))
+    assert np.abs(acc).max() < 2**24
+    ref = acc * (as_.astype(np.float64).reshape(-1, 1) * bs.astype(np.float64).reshape(1, -1)) + bias
+    assert np.array_equal(Y.astype(np.float64), ref)
+
+
+def test_matmul_integer_to_float_per_row_equals_per_tensor_rows(orc):
+    """With one scale and zero point per row of A, each output row equals the
+    per-tensor product of that row alone; an N-D A equals its flattened
+    rows."""
+    rng = np.random.default_rng(21)
+    A = rng.integers(0, 256, (2, 3, 40)).astype(np.uint8)
+    B = rng.integers(-128, 128, (40, 9)).astype(np.int8)
+    as_ = rng.uniform(0.01, 0.1, 6).astype(np.float32)
+    az = rng.integers(0, 256, 6).astype(np.int32)
+    bs = rng.uniform(1e-3, 1e-2, 9).astype(np.float32)
+    Y = orc.matmul_integer_to_float(A, B, as_, bs, az, None, None)
+    assert Y.shape == (2, 3, 9)
+    flat = A.reshape(6, 40)
+    for i in range(6):
+        yi = orc.matmul_integer_to_float(flat[i:i + 1], B, as_[i], bs, np.int32(az[i]))
+        assert np.array_equal(Y.reshape(6, 9)[i], yi[0])
+
+
+def test_dynamic_quantize_matmul_lossless_grid(orc):
+    """A on the grid k * 2^-7 spanning exactly [-128, 127] * 2^-7 quantizes
+    losslessly (scale 2^-7, zero point 128), so with power-of-two b_scale Y is
+    the fp64 textbook A (B - zb) b_scale + bias."""
+    rng = np.random.default_rng(22)
+    M, K, N = 5, 64, 6
+    k = rng.integers(-128, 128, (M, K))
+    k[0, 0], k[0, 1] = -128, 127
+    A = (k * 2.0 ** -7).astype(np.float32)
+    B = rng.integers(-128, 128, (K, N)).astype(np.int8)
+    bz = rng.integers(-128, 128, N).astype(np.int32)
+    bs = (2.0 ** rng.integers(-8, -3, N)).astype(np.float32)
+    bias = (rng.integers(-64, 64, N) / 8.0).astype(np.float32)
+    out = orc.dynamic_quantize_matmul(A, B, bs, bz, bias)
+    assert out["a_scale"] == np.float32(2.0 ** -7) and out["a_zero_point"] == 128
+    ref = A.astype(np.float64) @ ((B.astype(np.int64) - bz) * bs.astype(np.float64)) + bias
+    assert np.array_equal(out["Y"].astype(np.float64), ref)
+
+
+def test_dynamic_quantize_matmul_tensor_quantization_invariants(orc):
+    rng = np.random.default_rng(23)
+    A = rng.normal(0, 2, (7, 33)).astype(np.float32)
+    A[3, 4] = 9.5
+    out = orc.dynamic_quantize_matmul(A, rng.integers(-128, 128, (33, 4)).astype(np.int8), np.float32(0.01))
+    s, z, uA = out["a_scale"], out["a_zero_point"], out["uA"].astype(np.int64)
+    assert s == np.float32((np.float32(9.5) - np.float32(A.min())) / np.float32(255))
+    assert uA.max() == 255 and uA.min() == 0
+    assert np.all(np.abs((uA - z) * np.float64(s) - A) <= np.float64(s) / 2 * (1 + 1e-6))
