@@ -359,7 +359,28 @@ def measure_rows(args, dev, stream, world):
     out["qgemm_u8s8_to_u8"] = {"ms": sec * 1e3, "TOPS": 2.0 * M * N * K / sec / 1e12, "kernels": prof,
                                "workload": "QGemm M=8192 K=4096 N=14336, u8 A, s8 B per-column scale and zero point, "
                                            "C (1,N), alpha 1.5, u8 Y; both operands centred every call"}
-    del A, B, Y, wsp
+    del Y, wsp
+
+    # MatMulIntegerToFloat and DynamicQuantizeMatMul at the same shape, fp32 Y
+    Yf = torch.empty(M, N, dtype=torch.float32, device=dev)
+    wsp = torch.empty(q.matmul_integer_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+    a_s = torch.tensor([float(w["a_scale"])], device=dev)
+    a_z = torch.tensor([w["a_zero_point"]], dtype=torch.uint8, device=dev)
+    bias = torch.from_numpy(workloads.large_gemm(seed=2, M=1, K=1, N=N)["bias"]).to(dev)
+    fn = lambda: q.matmul_integer_to_float(A, B, a_s, bs, Yf, a_zero_point=a_z, b_zero_point=bz,  # noqa: E731
+                                           bias=bias, workspace=wsp)
+    sec, prof = _timed(fn, steps, warm, stream)
+    out["matmul_integer_to_float"] = {"ms": sec * 1e3, "TOPS": 2.0 * M * N * K / sec / 1e12, "kernels": prof,
+                                      "workload": "M=8192 K=4096 N=14336, u8 A per tensor, s8 B per column, bias, "
+                                                  "fp32 Y"}
+    del A
+    Af = t((workloads.large_gemm(seed=2, M=M, K=K, N=1)["A_bf16"].astype(np.uint32) << 16).view(np.float32))
+    fn = lambda: q.dynamic_quantize_matmul(Af, B, bs, Yf, b_zero_point=bz, bias=bias, workspace=wsp)  # noqa: E731
+    sec, prof = _timed(fn, steps, warm, stream)
+    out["dynamic_quantize_matmul"] = {"ms": sec * 1e3, "TOPS": 2.0 * M * N * K / sec / 1e12, "kernels": prof,
+                                      "workload": "M=8192 K=4096 N=14336, fp32 A quantized per tensor, s8 B per "
+                                                  "column, bias, fp32 Y"}
+    del Af, B, Yf, wsp
 
     # DynamicQuantizeLSTM, bidirectional T=512 batch=64 I=H=1024
     w = workloads.lstm(seed=4)

@@ -35,6 +35,9 @@
  *  [QG]   ONNX Runtime contrib schemas, "QGemm": inputs A, a_scale,
  *         a_zero_point, B, b_scale, b_zero_point, C, y_scale, y_zero_point;
  *         attributes transA, transB, alpha.
+ *  [MITF] ONNX Runtime contrib schemas, "MatMulIntegerToFloat" and
+ *         "DynamicQuantizeMatMul": inputs A, B, a_scale, b_scale,
+ *         a_zero_point, b_zero_point, bias.
  */
 #ifndef I8Q_H
 #define I8Q_H
@@ -307,6 +310,47 @@ int i8q_qgemm(const void* A, int atype, int transA, int64_t M, int64_t K, float 
 
 /* Scratch bytes i8q_qgemm needs for M x N x K (0 for sizes below 1). */
 size_t i8q_qgemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* ========================================================================
+ * MatMulIntegerToFloat [MITF]:
+ *   acc[i,j] = sum_k (A[i,k] - a_zero_point[i]) * (B[k,j] - b_zero_point[j])
+ *   Y[i,j]   = (float)acc * (a_scale[i] * b_scale[j]) + bias[j]
+ *   A: device, atype (U8|S8) codes (M, K) row-major (the leading dimensions
+ *   of an N-dimensional A flattened into M).  B: device, btype (U8|S8)
+ *   (K, N) row-major.
+ *   a_scale: device fp32, n_a == 1 (per tensor) or M (per row of A) entries;
+ *   a_zero_point: device, atype, n_a entries, or NULL (zero).  The schema
+ *   repeats B's "per-column" sentence for A; a scale per summation index
+ *   cannot leave the integer sum, so A's parameters are read as per tensor
+ *   or per row.
+ *   b_scale: device fp32, n_b == 1 or N entries; b_zero_point: device,
+ *   btype, n_b entries, or NULL.  bias: device fp32 [N] or NULL.
+ *   Y: device fp32 (M, N).
+ *   workspace: at least i8q_matmul_integer_workspace_size bytes, 256-byte
+ *   aligned.
+ * Errors: INVALID_ARG, UNSUPPORTED (K > 65536), CUDA. */
+int i8q_matmul_integer_to_float(const void* A, int atype, int64_t M, int64_t K, const void* B, int btype, int64_t N,
+                                const float* a_scale, const void* a_zero_point, size_t n_a, const float* b_scale,
+                                const void* b_zero_point, size_t n_b, const float* bias, float* Y, void* workspace,
+                                size_t ws_bytes, void* stream);
+
+/* DynamicQuantizeMatMul [MITF]: fp32 A (M, K) is quantized to uint8 per
+ * tensor (the schema names no method; the formula is that of a row of the
+ * dynamic inner product applied to the whole tensor: range widened to
+ * contain 0, scale = (max - min) / 255, zero point = saturate(rint(-min /
+ * scale)), codes = saturate(rint(A / scale) + zero point)), then
+ * MatMulIntegerToFloat with B's parameters as above.  a_scale_out (device
+ * fp32, 1 entry) and a_zero_point_out (device uint8, 1 entry) receive the
+ * computed parameters when not NULL.  Same workspace as
+ * i8q_matmul_integer_to_float. */
+int i8q_dynamic_quantize_matmul(const float* A, int64_t M, int64_t K, const void* B, int btype, int64_t N,
+                                const float* b_scale, const void* b_zero_point, size_t n_b, const float* bias,
+                                float* Y, float* a_scale_out, uint8_t* a_zero_point_out, void* workspace,
+                                size_t ws_bytes, void* stream);
+
+/* Scratch bytes of i8q_matmul_integer_to_float / i8q_dynamic_quantize_matmul
+ * for M x N x K (0 for sizes below 1). */
+size_t i8q_matmul_integer_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /* ========================================================================
  * DynamicQuantizeLSTM [LSTM]: int8 W and R with per-channel (or

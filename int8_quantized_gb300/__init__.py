@@ -289,6 +289,56 @@ def qgemm(A, a_scale, a_zero_point, B, b_scale, Y, b_zero_point=None, C=None, al
     return Y
 
 
+def matmul_integer_workspace_size(M, N, K):
+    return int(_L().i8q_matmul_integer_workspace_size(M, N, K))
+
+
+def matmul_integer_to_float(A, B, a_scale, b_scale, Y, a_zero_point=None, b_zero_point=None, bias=None,
+                            workspace=None, stream=None):
+    """MatMulIntegerToFloat.  A: uint8/int8 CUDA (..., K) (leading dims are
+    rows); B: uint8/int8 CUDA (K, N); a_scale: fp32 CUDA, 1 entry or one per
+    row of A; a_zero_point: A's dtype, same count, or None; b_scale /
+    b_zero_point: 1 or N entries; bias: fp32 CUDA [N] or None; Y: fp32 CUDA
+    (..., N)."""
+    K = A.shape[-1]
+    M = A.numel() // K
+    N = B.shape[1]
+    for z, t, n in ((a_zero_point, A, "a_zero_point"), (b_zero_point, B, "b_zero_point")):
+        if z is not None and z.dtype != t.dtype:
+            raise TypeError(f"{n} must have the dtype of its operand")
+    if workspace is None:
+        workspace = torch.empty(matmul_integer_workspace_size(M, N, K), dtype=torch.uint8, device=Y.device)
+    check(_L().i8q_matmul_integer_to_float(
+        _dev(A, "A"), _TORCH_TYPE[A.dtype], M, K, _dev(B, "B"), _TORCH_TYPE[B.dtype], N,
+        _dev(a_scale, "a_scale", torch.float32), _dev(a_zero_point, "a_zero_point"), a_scale.numel(),
+        _dev(b_scale, "b_scale", torch.float32), _dev(b_zero_point, "b_zero_point"), b_scale.numel(),
+        _dev(bias, "bias", torch.float32), _dev(Y, "Y", torch.float32), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "matmul_integer_to_float")
+    return Y
+
+
+def dynamic_quantize_matmul(A, B, b_scale, Y, b_zero_point=None, bias=None, a_scale_out=None, a_zero_point_out=None,
+                            workspace=None, stream=None):
+    """DynamicQuantizeMatMul.  A: fp32 CUDA (..., K), quantized to uint8 per
+    tensor; B: uint8/int8 CUDA (K, N); b_scale / b_zero_point: 1 or N
+    entries; bias: fp32 [N] or None; Y: fp32 (..., N).  a_scale_out (fp32,
+    1) and a_zero_point_out (uint8, 1) receive A's parameters when given."""
+    K = A.shape[-1]
+    M = A.numel() // K
+    N = B.shape[1]
+    if b_zero_point is not None and b_zero_point.dtype != B.dtype:
+        raise TypeError("b_zero_point must have B's dtype")
+    if workspace is None:
+        workspace = torch.empty(matmul_integer_workspace_size(M, N, K), dtype=torch.uint8, device=Y.device)
+    check(_L().i8q_dynamic_quantize_matmul(
+        _dev(A, "A", torch.float32), M, K, _dev(B, "B"), _TORCH_TYPE[B.dtype], N, _dev(b_scale, "b_scale", torch.float32),
+        _dev(b_zero_point, "b_zero_point"), b_scale.numel(), _dev(bias, "bias", torch.float32),
+        _dev(Y, "Y", torch.float32), _dev(a_scale_out, "a_scale_out", torch.float32),
+        _dev(a_zero_point_out, "a_zero_point_out", torch.uint8), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "dynamic_quantize_matmul")
+    return Y
+
+
 def dq_lstm_workspace_size(T, batch, input_size, hidden, direction):
     return int(_L().i8q_dq_lstm_workspace_size(T, batch, input_size, hidden, direction))
 

@@ -214,20 +214,27 @@ struct GemmEpilogue {
   int64_t ldc;            // elements
 };
 
-// Epilogue of QGemm on the tensor-core path.  The operands enter centred,
-// A' = A - ca and B' = B - cb (ca, cb = 128 for uint8 codes, 0 for int8), so
-// with run = sum_k A'[i,k] B'[k,j]:
-//   acc = run + rowsum[i] * g[j] + h[j] + C[i,j]
-//   rowsum[i] = sum_k A'[i,k],  g[j] = cb - b_zero_point[j],
-//   h[j] = (ca - a_zero_point) * sum_k B'[k,j] + K (ca - a_zero_point) g[j]
+// Epilogue of the 8-bit-code products on the tensor-core path (QGemm,
+// MatMulIntegerToFloat, DynamicQuantizeMatMul).  The operands enter
+// centred, A' = A - ca and B' = B - cb (ca, cb = 128 for uint8 codes, 0 for
+// int8), so with run = sum_k A'[i,k] B'[k,j]:
+//   acc = run + rowsum[i] * g[j] + d[i] * e[j] + C[i,j]
+//   rowsum[i] = sum_k A'[i,k],  d[i] = ca - a_zero_point[i],
+//   g[j] = cb - b_zero_point[j],  e[j] = sum_k B'[k,j] + K g[j]
 // (int32, wrapping: the true sum fits int32, so the modular result is it),
-// then y = (float)acc * mult[j] with mult[j] = (alpha * a_scale) * b_scale[j],
-// stored as fp32 or requantized: saturate(rint(y / y_scale) + y_zero_point).
+// then y = (float)acc * (asc[i] * bsc[j]) (+ bias[j]), stored as fp32 or
+// requantized: saturate(rint(y / y_scale) + y_zero_point).  Per-row values
+// are read at i * stride (stride 0: one value for the tensor).
 struct QgEpilogue {
   const int32_t* rowsum;  // [M]
+  const int32_t* d;       // d[i * d_stride]
+  int64_t d_stride;
+  const float* asc;       // asc[i * asc_stride]
+  int64_t asc_stride;
   const int32_t* g;       // [N]
-  const int32_t* h;       // [N]
-  const float* mult;      // [N]
+  const int32_t* e;       // [N]
+  const float* bsc;       // [N]
+  const float* bias;      // [N] or null
   const int32_t* C;       // element (i, j) at C[i * c_si + j * c_sj], or null
   int64_t c_si, c_sj;
   int ytype;              // I8Q_F32, I8Q_U8 or I8Q_S8

@@ -43,7 +43,7 @@ constexpr int SLICE = BN / (NUM_EPI_WARPS / 4);  // 64 columns per epilogue warp
 constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
-constexpr int PARAM_BYTES = NUM_EPI_WARPS * SLICE * 3 * 4;  // colsum, scaleB, bias per warp slice
+constexpr int PARAM_BYTES = NUM_EPI_WARPS * SLICE * 4 * 4;  // up to four column parameters per warp slice
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + PARAM_BYTES + NUM_BARS * 8 + 16;
 constexpr int GROUP_M = 16;
 
@@ -151,18 +151,23 @@ __device__ __forceinline__ void store_slice(const GemmEpilogue& ep, int64_t row,
   }
 }
 
-// QGemm epilogue of one row's 64-column slice (see QgEpilogue): column
-// parameters pg (g), pm (mult), ph (h) from shared memory, rs = rowsum[row].
+// Epilogue of one row's 64-column slice for the 8-bit-code products (see
+// QgEpilogue): column parameters pg (g), pe (e), pb (bsc), pz (bias) from
+// shared memory; rs, dr, ar: the row's rowsum, d and asc.
 __device__ __forceinline__ void store_slice_qg(const QgEpilogue& qg, int64_t row, int64_t col0, int64_t N,
-                                               const int32_t (&run)[SLICE], int32_t rs, const int32_t* pg,
-                                               const float* pm, const int32_t* ph) {
+                                               const int32_t (&run)[SLICE], int32_t rs, int32_t dr, float ar,
+                                               const int32_t* pg, const int32_t* pe, const float* pb,
+                                               const float* pz) {
   const bool full = col0 + SLICE <= N;
   const int32_t* crow = qg.C ? qg.C + row * qg.c_si : nullptr;
-  auto sum_at = [&](int j) -> int32_t {
+  const bool has_bias = qg.bias != nullptr;
+  auto value_at = [&](int j) -> float {
     // wrapping int32 arithmetic: the exact sum fits int32
-    uint32_t a = (uint32_t)run[j] + (uint32_t)rs * (uint32_t)pg[j] + (uint32_t)ph[j];
+    uint32_t a = (uint32_t)run[j] + (uint32_t)rs * (uint32_t)pg[j] + (uint32_t)dr * (uint32_t)pe[j];
     if (crow && col0 + j < N) a += (uint32_t)__ldg(crow + (col0 + j) * qg.c_sj);
-    return (int32_t)a;
+    float v = __fmul_rn(__int2float_rn((int32_t)a), __fmul_rn(ar, pb[j]));
+    if (has_bias) v = __fadd_rn(v, pz[j]);
+    return v;
   };
   if (qg.ytype == I8Q_F32) {
     float* Y = static_cast<float*>(qg.Y) + row * qg.ldy + col0;
@@ -171,7 +176,7 @@ __device__ __forceinline__ void store_slice_qg(const QgEpilogue& qg, int64_t row
     for (int j = 0; j < SLICE; j += 4) {
       float o[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) o[u] = __fmul_rn(__int2float_rn(sum_at(j + u)), pm[j + u]);
+      for (int u = 0; u < 4; ++u) o[u] = value_at(j + u);
       if (vec) {
         *reinterpret_cast<float4*>(Y + j) = make_float4(o[0], o[1], o[2], o[3]);
       } else {
@@ -191,10 +196,7 @@ __device__ __forceinline__ void store_slice_qg(const QgEpilogue& qg, int64_t row
   for (int j = 0; j < SLICE; j += 16) {
     uint32_t b[16];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const float v = __fmul_rn(__int2float_rn(sum_at(j + u)), pm[j + u]);
-      b[u] = rint_code_bits(__fdiv_rn(v, qg.y_scale), lo, hi, zp);
-    }
+    for (int u = 0; u < 16; ++u) b[u] = rint_code_bits(__fdiv_rn(value_at(j + u), qg.y_scale), lo, hi, zp);
     if (vec) {
       *reinterpret_cast<uint4*>(Y + j) =
           make_uint4(pack_low_bytes(b[0], b[1], b[2], b[3]), pack_low_bytes(b[4], b[5], b[6], b[7]),
@@ -211,7 +213,7 @@ __device__ __forceinline__ void store_slice_qg(const QgEpilogue& qg, int64_t row
 // the K loop).
 template <int EPI>
 __device__ __forceinline__ void stage_params(const TcParams& p, int64_t col0, int lane, int32_t* pc, float* ps,
-                                             float* pb) {
+                                             float* pb, float* pd) {
   for (int j = lane; j < SLICE; j += 32) {
     const int64_t c = col0 + j;
     const bool in = c < p.N;
@@ -221,8 +223,9 @@ __device__ __forceinline__ void stage_params(const TcParams& p, int64_t col0, in
       pb[j] = (in && p.ep.bias) ? __ldg(p.ep.bias + c) : 0.0f;
     } else {
       pc[j] = in ? __ldg(p.qg.g + c) : 0;
-      ps[j] = in ? __ldg(p.qg.mult + c) : 0.0f;
-      reinterpret_cast<int32_t*>(pb)[j] = in ? __ldg(p.qg.h + c) : 0;
+      reinterpret_cast<int32_t*>(ps)[j] = in ? __ldg(p.qg.e + c) : 0;
+      pb[j] = in ? __ldg(p.qg.bsc + c) : 0.0f;
+      pd[j] = (in && p.qg.bias) ? __ldg(p.qg.bias + c) : 0.0f;
     }
   }
 }
@@ -230,15 +233,15 @@ __device__ __forceinline__ void stage_params(const TcParams& p, int64_t col0, in
 // The epilogue of one row of the tile from its exact sums.
 template <int EPI>
 __device__ __forceinline__ void finish_row(const TcParams& p, int64_t row, int64_t col0, const int32_t (&run)[SLICE],
-                                           const int32_t* pc, const float* ps, const float* pb) {
+                                           const int32_t* pc, const float* ps, const float* pb, const float* pd) {
   if constexpr (EPI == EPI_DYN) {
     const float sA = __ldg(p.ep.scaleA + row);
     // A entered as uA - 128: sum_k (uA - zA) iB = run - (zA - 128) colsum
     const int32_t zA = __ldg(p.ep.zeroA + row) - 128;
     store_slice(p.ep, row, col0, p.N, run, zA, sA, pc, ps, pb);
   } else {
-    store_slice_qg(p.qg, row, col0, p.N, run, __ldg(p.qg.rowsum + row), pc, ps,
-                   reinterpret_cast<const int32_t*>(pb));
+    store_slice_qg(p.qg, row, col0, p.N, run, __ldg(p.qg.rowsum + row), __ldg(p.qg.d + row * p.qg.d_stride),
+                   __ldg(p.qg.asc + row * p.qg.asc_stride), pc, reinterpret_cast<const int32_t*>(ps), pb, pd);
   }
 }
 
@@ -369,9 +372,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ---------------- drain + epilogue ----------------
     const int q = warp & 3;               // TMEM lane quadrant of this warp (its 32 rows)
     const int slice = (warp - 2) >> 2;    // which 64 of the 256 columns
-    int32_t* pc = reinterpret_cast<int32_t*>(params) + (warp - 2) * SLICE * 3;
+    int32_t* pc = reinterpret_cast<int32_t*>(params) + (warp - 2) * SLICE * 4;
     float* ps = reinterpret_cast<float*>(pc + SLICE);
     float* pb = ps + SLICE;
+    float* pd = pb + SLICE;
     int chunk = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
@@ -379,7 +383,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tile_coords(tile, p.tiles_m, p.tiles_n, mt, nt);
       const int64_t col0 = (int64_t)nt * BN + slice * SLICE;
       // stage this slice's column parameters (read back after the K loop)
-      stage_params<EPI>(p, col0, lane, pc, ps, pb);
+      stage_params<EPI>(p, col0, lane, pc, ps, pb, pd);
       int32_t run[SLICE];
 #pragma unroll
       for (int j = 0; j < SLICE; ++j) run[j] = 0;
@@ -413,7 +417,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (!ok) break;
       __syncwarp();
       const int64_t row = (int64_t)mt * BM + q * 32 + lane;
-      if (row < p.M) finish_row<EPI>(p, row, col0, run, pc, ps, pb);
+      if (row < p.M) finish_row<EPI>(p, row, col0, run, pc, ps, pb, pd);
       __syncwarp();
     }
   }
@@ -628,9 +632,10 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // ---------------- drain + epilogue (both CTAs) ----------------
     const int q = warp & 3;
     const int slice = (warp - 2) >> 2;
-    int32_t* pc = reinterpret_cast<int32_t*>(params) + (warp - 2) * SLICE * 3;
+    int32_t* pc = reinterpret_cast<int32_t*>(params) + (warp - 2) * SLICE * 4;
     float* ps = reinterpret_cast<float*>(pc + SLICE);
     float* pb = ps + SLICE;
+    float* pd = pb + SLICE;
     const uint32_t acce_leader0 = map_shared_rank(acce(0), 0), acce_leader1 = map_shared_rank(acce(1), 0);
     int chunk = 0;
     bool ok = true;
@@ -638,7 +643,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       int mt, nt;
       tile_coords_g(tile, p.tiles_m, p.tiles_n, P_GROUP_M, mt, nt);
       const int64_t col0 = (int64_t)nt * PBN + slice * SLICE;
-      stage_params<EPI>(p, col0, lane, pc, ps, pb);
+      stage_params<EPI>(p, col0, lane, pc, ps, pb, pd);
       int32_t run[SLICE];
 #pragma unroll
       for (int j = 0; j < SLICE; ++j) run[j] = 0;
@@ -671,7 +676,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       if (!ok) break;
       __syncwarp();
       const int64_t row = (int64_t)mt * PBM + (int64_t)rank * HALF_ROWS + q * 32 + lane;
-      if (row < p.M) finish_row<EPI>(p, row, col0, run, pc, ps, pb);
+      if (row < p.M) finish_row<EPI>(p, row, col0, run, pc, ps, pb, pd);
       __syncwarp();
     }
   }

@@ -1,6 +1,8 @@
-// qgemm.cu -- QGemm (ONNX Runtime contrib schemas, "QGemm") on the
-// exact-integer tensor-core path.
+// qgemm.cu -- the products of 8-bit codes on the exact-integer tensor-core
+// path: QGemm, MatMulIntegerToFloat and DynamicQuantizeMatMul (ONNX Runtime
+// contrib schemas).
 //
+// QGemm:
 //   acc[i,j] = sum_k (A[i,k] - a_zero_point) * (B[k,j] - b_zero_point[j])
 //   acc += C[i,j]                           (int32, broadcast from (1|M, 1|N))
 //   y = (float)acc * ((alpha * a_scale) * b_scale[j])
@@ -8,6 +10,12 @@
 // C carries the scale alpha * a_scale * b_scale and zero point 0 (the schema
 // writes alpha / beta but defines no beta), so it adds to the integer sum;
 // the rescale is DequantizeLinear of the sum followed by QuantizeLinear.
+// MatMulIntegerToFloat:
+//   Y[i,j] = (float)acc * (a_scale[i] * b_scale[j]) + bias[j]
+// with A's scale and zero point per tensor or per row of A.
+// DynamicQuantizeMatMul: fp32 A quantized to uint8 per tensor (range widened
+// to contain 0, scale (max - min) / 255, zero point rint(-min / scale)),
+// then MatMulIntegerToFloat.
 //
 // The 8-bit codes enter the tensor pipe centred, A' = A - ca and
 // B' = B - cb with ca, cb = 128 for uint8 and 0 for int8, so every operand is
@@ -79,28 +87,122 @@ center_operand(const uint8_t* __restrict__ X, int64_t R, int64_t K, int64_t Kp, 
   if ((t & 3) == 0 && r < R) sums[r] = part;
 }
 
-// g[j] = cb - bz[j]; h[j] = (ca - za) * colsum[j] + K (ca - za) g[j] (wrapping
-// int32); mult[j] = (alpha * a_scale) * b_scale[j].
-__global__ void qgemm_col_params(const int32_t* __restrict__ colsum, const float* __restrict__ b_scale,
-                                 const uint8_t* __restrict__ b_zp, int b_signed, int64_t n_b, int64_t N, int64_t K,
-                                 int ca, int za, int cb, float alpha, float a_scale, int32_t* __restrict__ g,
-                                 int32_t* __restrict__ h, float* __restrict__ mult) {
+// g[j] = cb - bz[j]; e[j] = colsum[j] + K g[j] (wrapping int32);
+// bsc[j] = b_scale[j] (expanded when per tensor).  Thread 0 also writes the
+// per-tensor row values d0 = ca - za and asc0 when asked (write_row0).
+__global__ void col_params(const int32_t* __restrict__ colsum, const float* __restrict__ b_scale,
+                           const uint8_t* __restrict__ b_zp, int b_signed, int64_t n_b, int64_t N, int64_t K, int cb,
+                           int32_t* __restrict__ g, int32_t* __restrict__ e, float* __restrict__ bsc, int write_row0,
+                           int32_t d0, float asc0, int32_t* __restrict__ d, float* __restrict__ asc) {
   const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (write_row0 && j == 0) {
+    d[0] = d0;
+    asc[0] = asc0;
+  }
   if (j >= N) return;
   const int64_t pj = n_b == N ? j : 0;
   const int bz = b_zp ? (b_signed ? (int)(int8_t)b_zp[pj] : (int)b_zp[pj]) : 0;
   const int32_t gj = cb - bz;
-  const uint32_t da = (uint32_t)(ca - za);
   g[j] = gj;
-  h[j] = (int32_t)(da * (uint32_t)colsum[j] + (uint32_t)K * da * (uint32_t)gj);
-  const float m = __fmul_rn(alpha, a_scale);
-  mult[j] = __fmul_rn(m, __ldg(b_scale + pj));
+  e[j] = (int32_t)((uint32_t)colsum[j] + (uint32_t)K * (uint32_t)gj);
+  bsc[j] = __ldg(b_scale + pj);
+}
+
+// d[i] = ca - a_zero_point[i] for per-row zero points (0 when none).
+__global__ void row_params(const uint8_t* __restrict__ a_zp, int a_signed, int64_t n, int ca,
+                           int32_t* __restrict__ d) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int za = a_zp ? (a_signed ? (int)(int8_t)a_zp[i] : (int)a_zp[i]) : 0;
+  d[i] = ca - za;
+}
+
+// Range of a whole fp32 tensor, widened to contain 0: mm[0] = -min(0, min x)
+// and mm[1] = max(0, max x), both non-negative, so their bit patterns order
+// like the values and atomicMax on them is exact.  mm starts at 0.
+__global__ void __launch_bounds__(256) tensor_range(const float* __restrict__ x, int64_t n, uint32_t* mm) {
+  float nmn = 0.0f, mx = 0.0f;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+    const int64_t n4 = n / 4;
+    for (int64_t i = t; i < n4; i += stride) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(x) + i);
+      mx = fmaxf(fmaxf(mx, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
+      nmn = fmaxf(fmaxf(nmn, fmaxf(-v.x, -v.y)), fmaxf(-v.z, -v.w));
+    }
+    for (int64_t i = n4 * 4 + t; i < n; i += stride) {
+      mx = fmaxf(mx, x[i]);
+      nmn = fmaxf(nmn, -x[i]);
+    }
+  } else {
+    for (int64_t i = t; i < n; i += stride) {
+      mx = fmaxf(mx, x[i]);
+      nmn = fmaxf(nmn, -x[i]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    nmn = fmaxf(nmn, __shfl_xor_sync(0xffffffffu, nmn, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicMax(mm, __float_as_uint(nmn));
+    atomicMax(mm + 1, __float_as_uint(mx));
+  }
+}
+
+// Per-tensor uint8 quantization of fp32 A (M x K) straight into the centred
+// bf16 operand: code = saturate(rint(A / s) + z), A' = code - 128, with s, z
+// from the tensor's range exactly as a row of the dynamic inner product;
+// rowsum[i] = sum_k A'.  One warp per row.  Block 0 publishes d = 128 - z and
+// s for the epilogue and, when given, the scale and zero point.
+__global__ void __launch_bounds__(256)
+quantize_tensor_center(const float* __restrict__ A, int64_t M, int64_t K, int64_t Kp, const uint32_t* __restrict__ mm,
+                       __nv_bfloat16* __restrict__ Ac, int32_t* __restrict__ rowsum, int32_t* __restrict__ d_out,
+                       float* __restrict__ asc_out, float* __restrict__ a_scale_out,
+                       uint8_t* __restrict__ a_zp_out) {
+  const float mn = -__uint_as_float(mm[0]), mx = __uint_as_float(mm[1]);
+  float sc;
+  int z;
+  row_scale_zero(mn, mx, sc, z);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *d_out = 128 - z;
+    *asc_out = sc;
+    if (a_scale_out) *a_scale_out = sc;
+    if (a_zp_out) *a_zp_out = (uint8_t)z;
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (row >= M) return;
+  const float lo_z = (float)(-z), hi_z = (float)(255 - z);
+  const float* a = A + row * K;
+  __nv_bfloat16* out = Ac + row * Kp;
+  int part = 0;
+  for (int64_t k0 = (int64_t)lane * 8; k0 < Kp; k0 += 256) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      int c[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t k = k0 + 2 * e2 + h;
+        c[h] = k < K ? (int)(row_code(a[k], sc, lo_z, hi_z, z)) - 128 : 0;
+        part += c[h];
+      }
+      w[e2] = (__float_as_uint((float)c[0]) >> 16) | (__float_as_uint((float)c[1]) & 0xffff0000u);
+    }
+    *reinterpret_cast<uint4*>(out + k0) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if (lane == 0) rowsum[row] = part;
 }
 
 size_t a256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct QgLayout {
-  size_t Ac, rowsum, Bc, colsum, g, h, mult, total;
+  size_t Ac, rowsum, Bc, colsum, g, e, bsc, d, asc, mm, total;
 };
 
 QgLayout qg_layout(int64_t M, int64_t N, int64_t K) {
@@ -117,8 +219,11 @@ QgLayout qg_layout(int64_t M, int64_t N, int64_t K) {
   L.Bc = take((size_t)N * Kp * 2);
   L.colsum = take((size_t)N * 4);
   L.g = take((size_t)N * 4);
-  L.h = take((size_t)N * 4);
-  L.mult = take((size_t)N * 4);
+  L.e = take((size_t)N * 4);
+  L.bsc = take((size_t)N * 4);
+  L.d = take((size_t)M * 4);
+  L.asc = take(4);
+  L.mm = take(8);
   L.total = o;
   return L;
 }
@@ -137,6 +242,85 @@ int launch_center(const void* X, int type, int64_t R, int64_t K, int64_t Kp, int
   return I8Q_OK;
 }
 
+// Where the per-row values d = ca - a_zero_point and asc (the row scale) come
+// from.
+enum RowMode : int {
+  ROWS_HOST = 0,    // one d and asc given on the host (written by col_params)
+  ROWS_DEVICE = 1,  // a_scale and a_zero_point on the device, 1 or M entries
+  ROWS_READY = 2,   // d[0] and asc[0] already written on the device
+};
+struct RowParams {
+  int mode;
+  int32_t d0;             // ROWS_HOST
+  float asc0;             // ROWS_HOST
+  const float* asc_dev;   // ROWS_DEVICE
+  const uint8_t* za_dev;  // ROWS_DEVICE, or null (zero)
+  int64_t n_a;            // ROWS_DEVICE: 1 or M
+  int a_signed;
+};
+
+// Everything after the A operand is centred: centre B, form the column and
+// row parameters, run the product with the epilogue in qg (its C, bias and
+// output fields already set).
+int finish_product(const QgLayout& L, uint8_t* base, int64_t M, int64_t N, int64_t K, int64_t Kp, const void* B,
+                   int btype, int transB, const float* b_scale, const void* b_zero_point, int64_t n_b, int ca,
+                   const RowParams& rp, QgEpilogue qg, cudaStream_t s) {
+  auto* Ac = reinterpret_cast<__nv_bfloat16*>(base + L.Ac);
+  auto* Bc = reinterpret_cast<__nv_bfloat16*>(base + L.Bc);
+  auto* colsum = reinterpret_cast<int32_t*>(base + L.colsum);
+  auto* g = reinterpret_cast<int32_t*>(base + L.g);
+  auto* e = reinterpret_cast<int32_t*>(base + L.e);
+  auto* bsc = reinterpret_cast<float*>(base + L.bsc);
+  auto* d = reinterpret_cast<int32_t*>(base + L.d);
+  auto* asc = reinterpret_cast<float*>(base + L.asc);
+  int rc = launch_center(B, btype, N, K, Kp, transB ? 1 : 0, Bc, colsum, s);
+  if (rc) return rc;
+  const int cb = btype == I8Q_U8 ? 128 : 0;
+  {
+    I8Q_PROF("qgemm_params", s);
+    col_params<<<(unsigned)ceil_div(N, 256), 256, 0, s>>>(colsum, b_scale, static_cast<const uint8_t*>(b_zero_point),
+                                                         btype == I8Q_S8, n_b, N, K, cb, g, e, bsc,
+                                                         rp.mode == ROWS_HOST ? 1 : 0, rp.d0, rp.asc0, d, asc);
+    I8Q_LAUNCH_CHECK("col_params");
+    if (rp.mode == ROWS_DEVICE) {
+      row_params<<<(unsigned)ceil_div(rp.n_a, 256), 256, 0, s>>>(rp.za_dev, rp.a_signed, rp.n_a, ca, d);
+      I8Q_LAUNCH_CHECK("row_params");
+    }
+  }
+  qg.rowsum = reinterpret_cast<int32_t*>(base + L.rowsum);
+  qg.d = d;
+  qg.g = g;
+  qg.e = e;
+  qg.bsc = bsc;
+  if (rp.mode == ROWS_DEVICE) {
+    const int64_t st = rp.n_a == M && M > 1 ? 1 : 0;
+    qg.d_stride = st;
+    qg.asc = rp.asc_dev;
+    qg.asc_stride = st;
+  } else {
+    qg.d_stride = 0;
+    qg.asc = asc;
+    qg.asc_stride = 0;
+  }
+  qg.ldy = N;
+  // |A'| <= 2^7 and |B'| <= 2^7
+  return launch_qgemm_tc(Ac, Bc, M, N, Kp, 14, qg, s);
+}
+
+int check_common(const char* who, int64_t M, int64_t N, int64_t K, int btype, const void* B, const float* b_scale,
+                 const void* Y, size_t n_b, void* workspace, size_t ws_bytes, const QgLayout& L) {
+  const std::string w(who);
+  if (M <= 0 || N <= 0 || K <= 0) return fail(I8Q_ERR_INVALID_ARG, w + ": M, N, K must be >= 1");
+  if (K > 65536) return fail(I8Q_ERR_UNSUPPORTED, w + ": K > 65536 (int32 sums could overflow)");
+  if (btype != I8Q_U8 && btype != I8Q_S8) return fail(I8Q_ERR_INVALID_ARG, w + ": B must be I8Q_U8 or I8Q_S8");
+  if (!B || !b_scale || !Y) return fail(I8Q_ERR_INVALID_ARG, w + ": B, b_scale and Y are required");
+  if (n_b != 1 && (int64_t)n_b != N) return fail(I8Q_ERR_INVALID_ARG, w + ": b_scale must have 1 or N entries");
+  if (!workspace || ws_bytes < L.total)
+    return fail(I8Q_ERR_INVALID_ARG, w + ": workspace missing or smaller than the workspace size");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(I8Q_ERR_INVALID_ARG, w + ": workspace must be 256-byte aligned");
+  return I8Q_OK;
+}
+
 }  // namespace
 }  // namespace i8q
 
@@ -147,17 +331,20 @@ extern "C" size_t i8q_qgemm_workspace_size(int64_t M, int64_t N, int64_t K) {
   return qg_layout(M, N, K).total;
 }
 
+extern "C" size_t i8q_matmul_integer_workspace_size(int64_t M, int64_t N, int64_t K) {
+  return i8q_qgemm_workspace_size(M, N, K);
+}
+
 extern "C" int i8q_qgemm(const void* A, int atype, int transA, int64_t M, int64_t K, float a_scale,
                          int a_zero_point, const void* B, int btype, int transB, int64_t N, const float* b_scale,
                          const void* b_zero_point, size_t n_b, const int32_t* C, int64_t c_rows, int64_t c_cols,
                          float alpha, int quantize_y, float y_scale, int y_zero_point, int ytype, void* Y,
                          void* workspace, size_t ws_bytes, void* stream) {
-  if (M <= 0 || N <= 0 || K <= 0) return fail(I8Q_ERR_INVALID_ARG, "qgemm: M, N, K must be >= 1");
-  if (K > 65536) return fail(I8Q_ERR_UNSUPPORTED, "qgemm: K > 65536 (int32 sums could overflow)");
-  if ((atype != I8Q_U8 && atype != I8Q_S8) || (btype != I8Q_U8 && btype != I8Q_S8))
-    return fail(I8Q_ERR_INVALID_ARG, "qgemm: A and B must be I8Q_U8 or I8Q_S8");
-  if (!A || !B || !b_scale || !Y) return fail(I8Q_ERR_INVALID_ARG, "qgemm: A, B, b_scale and Y are required");
-  if (n_b != 1 && (int64_t)n_b != N) return fail(I8Q_ERR_INVALID_ARG, "qgemm: b_scale must have 1 or N entries");
+  if (atype != I8Q_U8 && atype != I8Q_S8) return fail(I8Q_ERR_INVALID_ARG, "qgemm: A and B must be I8Q_U8 or I8Q_S8");
+  const QgLayout L = qg_layout(M, N, K);
+  int rc = check_common("qgemm", M, N, K, btype, B, b_scale, Y, n_b, workspace, ws_bytes, L);
+  if (rc) return rc;
+  if (!A) return fail(I8Q_ERR_INVALID_ARG, "qgemm: A is required");
   const int alo = atype == I8Q_U8 ? 0 : -128, ahi = atype == I8Q_U8 ? 255 : 127;
   if (a_zero_point < alo || a_zero_point > ahi) return fail(I8Q_ERR_INVALID_ARG, "qgemm: a_zero_point out of A's range");
   if (C && !((c_rows == 1 || c_rows == M) && (c_cols == 1 || c_cols == N)))
@@ -167,40 +354,20 @@ extern "C" int i8q_qgemm(const void* A, int atype, int transA, int64_t M, int64_
     const int ylo = ytype == I8Q_U8 ? 0 : -128, yhi = ytype == I8Q_U8 ? 255 : 127;
     if (y_zero_point < ylo || y_zero_point > yhi) return fail(I8Q_ERR_INVALID_ARG, "qgemm: y_zero_point out of range");
   }
-  const QgLayout L = qg_layout(M, N, K);
-  if (!workspace || ws_bytes < L.total)
-    return fail(I8Q_ERR_INVALID_ARG, "qgemm: workspace missing or smaller than qgemm_workspace_size");
-  if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(I8Q_ERR_INVALID_ARG, "qgemm: workspace must be 256-byte aligned");
   cudaStream_t s = as_stream(stream);
   const int64_t Kp = round_up(K, 64);
   uint8_t* base = static_cast<uint8_t*>(workspace);
-  auto* Ac = reinterpret_cast<__nv_bfloat16*>(base + L.Ac);
-  auto* Bc = reinterpret_cast<__nv_bfloat16*>(base + L.Bc);
-  auto* rowsum = reinterpret_cast<int32_t*>(base + L.rowsum);
-  auto* colsum = reinterpret_cast<int32_t*>(base + L.colsum);
-  auto* g = reinterpret_cast<int32_t*>(base + L.g);
-  auto* h = reinterpret_cast<int32_t*>(base + L.h);
-  auto* mult = reinterpret_cast<float*>(base + L.mult);
   // A is (M, K), K contiguous, unless transA; B is (K, N), N contiguous,
   // unless transB
-  int rc = launch_center(A, atype, M, K, Kp, transA ? 0 : 1, Ac, rowsum, s);
+  rc = launch_center(A, atype, M, K, Kp, transA ? 0 : 1, reinterpret_cast<__nv_bfloat16*>(base + L.Ac),
+                     reinterpret_cast<int32_t*>(base + L.rowsum), s);
   if (rc) return rc;
-  rc = launch_center(B, btype, N, K, Kp, transB ? 1 : 0, Bc, colsum, s);
-  if (rc) return rc;
-  const int ca = atype == I8Q_U8 ? 128 : 0, cb = btype == I8Q_U8 ? 128 : 0;
-  {
-    I8Q_PROF("qgemm_col_params", s);
-    qgemm_col_params<<<(unsigned)ceil_div(N, 256), 256, 0, s>>>(colsum, b_scale,
-                                                               static_cast<const uint8_t*>(b_zero_point),
-                                                               btype == I8Q_S8, (int64_t)n_b, N, K, ca, a_zero_point,
-                                                               cb, alpha, a_scale, g, h, mult);
-    I8Q_LAUNCH_CHECK("qgemm_col_params");
-  }
-  QgEpilogue qg;
-  qg.rowsum = rowsum;
-  qg.g = g;
-  qg.h = h;
-  qg.mult = mult;
+  const int ca = atype == I8Q_U8 ? 128 : 0;
+  RowParams rp{};
+  rp.mode = ROWS_HOST;
+  rp.d0 = ca - a_zero_point;
+  rp.asc0 = alpha * a_scale;  // the multiplier's first factor, rounded once
+  QgEpilogue qg{};
   qg.C = C;
   qg.c_si = C ? (c_rows == 1 ? 0 : c_cols) : 0;
   qg.c_sj = C ? (c_cols == 1 ? 0 : 1) : 0;
@@ -208,7 +375,74 @@ extern "C" int i8q_qgemm(const void* A, int atype, int transA, int64_t M, int64_
   qg.y_scale = y_scale;
   qg.y_zero_point = y_zero_point;
   qg.Y = Y;
-  qg.ldy = N;
-  // |A'| <= 2^7 and |B'| <= 2^7
-  return launch_qgemm_tc(Ac, Bc, M, N, Kp, 14, qg, s);
+  return finish_product(L, base, M, N, K, Kp, B, btype, transB, b_scale, b_zero_point, (int64_t)n_b, ca, rp, qg, s);
+}
+
+extern "C" int i8q_matmul_integer_to_float(const void* A, int atype, int64_t M, int64_t K, const void* B, int btype,
+                                           int64_t N, const float* a_scale, const void* a_zero_point, size_t n_a,
+                                           const float* b_scale, const void* b_zero_point, size_t n_b,
+                                           const float* bias, float* Y, void* workspace, size_t ws_bytes,
+                                           void* stream) {
+  if (atype != I8Q_U8 && atype != I8Q_S8)
+    return fail(I8Q_ERR_INVALID_ARG, "matmul_integer_to_float: A must be I8Q_U8 or I8Q_S8");
+  const QgLayout L = qg_layout(M, N, K);
+  int rc = check_common("matmul_integer_to_float", M, N, K, btype, B, b_scale, Y, n_b, workspace, ws_bytes, L);
+  if (rc) return rc;
+  if (!A || !a_scale) return fail(I8Q_ERR_INVALID_ARG, "matmul_integer_to_float: A and a_scale are required");
+  if (n_a != 1 && (int64_t)n_a != M)
+    return fail(I8Q_ERR_INVALID_ARG, "matmul_integer_to_float: a_scale must have 1 entry or one per row of A");
+  cudaStream_t s = as_stream(stream);
+  const int64_t Kp = round_up(K, 64);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  rc = launch_center(A, atype, M, K, Kp, 1, reinterpret_cast<__nv_bfloat16*>(base + L.Ac),
+                     reinterpret_cast<int32_t*>(base + L.rowsum), s);
+  if (rc) return rc;
+  RowParams rp{};
+  rp.mode = ROWS_DEVICE;
+  rp.asc_dev = a_scale;
+  rp.za_dev = static_cast<const uint8_t*>(a_zero_point);
+  rp.n_a = (int64_t)n_a;
+  rp.a_signed = atype == I8Q_S8;
+  QgEpilogue qg{};
+  qg.bias = bias;
+  qg.ytype = I8Q_F32;
+  qg.Y = Y;
+  return finish_product(L, base, M, N, K, Kp, B, btype, 0, b_scale, b_zero_point, (int64_t)n_b,
+                        atype == I8Q_U8 ? 128 : 0, rp, qg, s);
+}
+
+extern "C" int i8q_dynamic_quantize_matmul(const float* A, int64_t M, int64_t K, const void* B, int btype, int64_t N,
+                                           const float* b_scale, const void* b_zero_point, size_t n_b,
+                                           const float* bias, float* Y, float* a_scale_out,
+                                           uint8_t* a_zero_point_out, void* workspace, size_t ws_bytes,
+                                           void* stream) {
+  const QgLayout L = qg_layout(M, N, K);
+  int rc = check_common("dynamic_quantize_matmul", M, N, K, btype, B, b_scale, Y, n_b, workspace, ws_bytes, L);
+  if (rc) return rc;
+  if (!A) return fail(I8Q_ERR_INVALID_ARG, "dynamic_quantize_matmul: A is required");
+  cudaStream_t s = as_stream(stream);
+  const int64_t Kp = round_up(K, 64);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  auto* mm = reinterpret_cast<uint32_t*>(base + L.mm);
+  {
+    I8Q_PROF("dqmm_quantize_a", s);
+    I8Q_CUDA_TRY(cudaMemsetAsync(mm, 0, 8, s));
+    const int64_t n = M * K;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n, 256 * 8), (int64_t)sm_count() * 8));
+    tensor_range<<<grid, 256, 0, s>>>(A, n, mm);
+    I8Q_LAUNCH_CHECK("tensor_range");
+    const int64_t blocks = ceil_div(M, 8);
+    if (blocks > 0x7fffffff) return fail(I8Q_ERR_UNSUPPORTED, "dynamic_quantize_matmul: too many rows");
+    quantize_tensor_center<<<(unsigned)blocks, 256, 0, s>>>(
+        A, M, K, Kp, mm, reinterpret_cast<__nv_bfloat16*>(base + L.Ac), reinterpret_cast<int32_t*>(base + L.rowsum),
+        reinterpret_cast<int32_t*>(base + L.d), reinterpret_cast<float*>(base + L.asc), a_scale_out, a_zero_point_out);
+    I8Q_LAUNCH_CHECK("quantize_tensor_center");
+  }
+  RowParams rp{};
+  rp.mode = ROWS_READY;
+  QgEpilogue qg{};
+  qg.bias = bias;
+  qg.ytype = I8Q_F32;
+  qg.Y = Y;
+  return finish_product(L, base, M, N, K, Kp, B, btype, 0, b_scale, b_zero_point, (int64_t)n_b, 128, rp, qg, s);
 }

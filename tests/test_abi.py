@@ -142,3 +142,19 @@ def test_qgemm_validation(lib):
     assert call(quant=1, ytype=_lib.S8, yzp=128) == _lib.ERR_INVALID_ARG
     assert call(ws=16) == _lib.ERR_INVALID_ARG and b"workspace" in lib.i8q_last_error()
     assert call(K=70000) == _lib.ERR_UNSUPPORTED
+
+
+def test_matmul_integer_validation(lib):
+    from int8_quantized_gb300 import _lib
+    p = ctypes.c_void_p(256)
+    assert lib.i8q_matmul_integer_workspace_size(3, 5, 7) == lib.i8q_qgemm_workspace_size(3, 5, 7)
+    rc = lib.i8q_matmul_integer_to_float(p, _lib.U8, 4, 8, p, _lib.S8, 3, p, None, 2, p, None, 1, None, p, p, 1 << 20,
+                                         None)
+    assert rc == _lib.ERR_INVALID_ARG and b"one per row" in lib.i8q_last_error()
+    rc = lib.i8q_matmul_integer_to_float(p, _lib.F32, 4, 8, p, _lib.S8, 3, p, None, 1, p, None, 1, None, p, p, 1 << 20,
+                                         None)
+    assert rc == _lib.ERR_INVALID_ARG
+    rc = lib.i8q_dynamic_quantize_matmul(p, 4, 8, p, _lib.S8, 3, p, None, 3, None, p, None, None, p, 16, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"workspace" in lib.i8q_last_error()
+    rc = lib.i8q_dynamic_quantize_matmul(p, 4, 8, p, _lib.S8, 3, p, None, 2, None, p, None, None, p, 1 << 20, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"b_scale" in lib.i8q_last_error()
