@@ -41,9 +41,12 @@ def load(path):
     l.or_qgemm.argtypes = [p, c_int, c_int, i64, i64, f32, i32, p, c_int, c_int, i64, p, p, i64, p, i64, i64,
                            f32, c_int, f32, i32, c_int, p]
     l.or_matmul_integer_to_float.argtypes = [p, c_int, i64, i64, p, c_int, i64, p, p, i64, p, p, i64, p, p]
+    l.or_mul_integer.argtypes = [p, c_int, p, i32, p, c_int, p, i32, p, c_int, p]
+    l.or_qlinear_binary.argtypes = [c_int, p, p, f32, i32, p, p, f32, i32, f32, i32, p, c_int, c_int, p]
+    l.or_qlinear_unary.argtypes = [c_int, p, i64, c_int, f32, i32, f32, i32, f32, p]
     for fn in ("or_quantize_linear", "or_dequantize_linear", "or_quantize_rows_u8",
                "or_quantize_cols_s8", "or_qgemm_dyn_rows", "or_qlinearconv", "or_lstm_cell", "or_qgemm",
-               "or_matmul_integer_to_float"):
+               "or_matmul_integer_to_float", "or_mul_integer", "or_qlinear_binary", "or_qlinear_unary"):
         getattr(l, fn).restype = ctypes.c_int
     return l
 
@@ -316,6 +319,53 @@ def dynamic_quantize_matmul(A, B, b_scale, b_zero_point=None, bias=None):
     uA = uA.reshape(A.shape)
     Y = matmul_integer_to_float(uA, B, s[0], b_scale, np.int32(z[0]), b_zero_point, bias)
     return {"Y": Y, "uA": uA, "a_scale": s[0], "a_zero_point": int(z[0])}
+
+
+def _bcast_shapes(a, b):
+    """Numpy-style broadcast of two shapes: (a_padded, b_padded, out) as int64
+    arrays of one rank."""
+    out = np.broadcast_shapes(a, b)
+    r = max(len(out), 1)
+    pad = lambda s: np.array((1,) * (r - len(s)) + tuple(s), dtype=np.int64)  # noqa: E731
+    return pad(a), pad(b), pad(out), tuple(out)
+
+
+def mul_integer(A, B, a_zero_point=0, b_zero_point=0):
+    """MulInteger: int32 (A - a_zp) * (B - b_zp), Numpy-style broadcast."""
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    sa, sb, so, out = _bcast_shapes(A.shape, B.shape)
+    C = np.empty(out, np.int32)
+    _check(lib().or_mul_integer(_ptr(A), U8 if A.dtype == np.uint8 else S8, _ptr(sa), int(a_zero_point), _ptr(B),
+                                U8 if B.dtype == np.uint8 else S8, _ptr(sb), int(b_zero_point), _ptr(so), len(so),
+                                _ptr(C)), "mul_integer")
+    return C
+
+
+def qlinear_binary(op, A, a_scale, a_zero_point, B, b_scale, b_zero_point, c_scale, c_zero_point):
+    """QLinearAdd (op "add") / QLinearMul (op "mul"); A, B, C of one 8-bit
+    type, broadcast."""
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    if A.dtype != B.dtype:
+        raise ValueError("A and B must have one type")
+    sa, sb, so, out = _bcast_shapes(A.shape, B.shape)
+    C = np.empty(out, A.dtype)
+    _check(lib().or_qlinear_binary({"add": 0, "mul": 1}[op], _ptr(A), _ptr(sa), float(a_scale), int(a_zero_point),
+                                   _ptr(B), _ptr(sb), float(b_scale), int(b_zero_point), float(c_scale),
+                                   int(c_zero_point), _ptr(so), len(so), U8 if A.dtype == np.uint8 else S8, _ptr(C)),
+           "qlinear_binary")
+    return C
+
+
+def qlinear_unary(op, X, x_scale, x_zero_point, y_scale, y_zero_point, alpha=0.01):
+    """QLinearLeakyRelu (op "leaky_relu") / QLinearSigmoid (op "sigmoid")."""
+    X = np.ascontiguousarray(X)
+    Y = np.empty_like(X)
+    _check(lib().or_qlinear_unary({"leaky_relu": 0, "sigmoid": 1}[op], _ptr(X), X.size,
+                                  U8 if X.dtype == np.uint8 else S8, float(x_scale), int(x_zero_point), float(y_scale),
+                                  int(y_zero_point), float(alpha), _ptr(Y)), "qlinear_unary")
+    return Y
 
 
 def lstm_cell(Gx, Gh, Wb, Rb, c_prev):

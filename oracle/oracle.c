@@ -27,6 +27,9 @@
  *         attributes transA, transB, alpha)
  *  [MITF] ONNX Runtime contrib schemas, "MatMulIntegerToFloat" and
  *         "DynamicQuantizeMatMul" (inputs A, B, scales, zero points, bias)
+ *  [QEW] ONNX Runtime contrib schemas, "MulInteger", "QLinearAdd",
+ *         "QLinearMul" (doc formulas, Numpy-style broadcasting),
+ *         "QLinearLeakyRelu", "QLinearSigmoid" (doc strings)
  *
  * Where the pages leave a step open the readings used are listed in the
  * repository's design notes; each is restated at the function below.
@@ -424,6 +427,90 @@ int or_matmul_integer_to_float(const void* A, int atype, int64_t M, int64_t K, c
     }
   }
   return err;
+}
+
+/* Numpy-style broadcasting of two shapes already padded to one rank: the
+ * offset of output element `flat` in an operand with shape `sh` (its size-1
+ * dimensions repeat). */
+static int64_t bcast_offset(int64_t flat, const int64_t* out_shape, const int64_t* sh, int rank) {
+  int64_t off = 0, stride = 1;
+  for (int d = rank - 1; d >= 0; --d) {
+    const int64_t idx = flat % out_shape[d];
+    flat /= out_shape[d];
+    if (sh[d] != 1) off += idx * stride;
+    stride *= sh[d];
+  }
+  return off;
+}
+
+/* [QEW] MulInteger: C (int32) = (A - A_zero_point) * (B - B_zero_point),
+ * broadcast.  a_shape / b_shape / out_shape share one rank (left-padded with
+ * 1s by the caller). */
+int or_mul_integer(const void* A, int atype, const int64_t* a_shape, int32_t a_zp, const void* B, int btype,
+                   const int64_t* b_shape, int32_t b_zp, const int64_t* out_shape, int rank, int32_t* C) {
+  int64_t n = 1;
+  for (int d = 0; d < rank; ++d) n *= out_shape[d];
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t a = load_q(A, atype, bcast_offset(i, out_shape, a_shape, rank)) - a_zp;
+    const int64_t b = load_q(B, btype, bcast_offset(i, out_shape, b_shape, rank)) - b_zp;
+    C[i] = (int32_t)(a * b);
+  }
+  return OR_OK;
+}
+
+/* [QEW] QLinearAdd (op 0) and QLinearMul (op 1), broadcast; A, B and C are
+ * codes of one 8-bit type.  Read in the order the formulas are written:
+ *   add: C = (A_scale * (A - A_zp) + B_scale * (B - B_zp)) / C_scale + C_zp
+ *   mul: C = ((A - A_zp) * (B - B_zp)) * (A_scale * B_scale) / C_scale + C_zp
+ * with the integer differences (and their product) exact, every fp32
+ * operation rounding once, then round half to even and saturation. */
+int or_qlinear_binary(int op, const void* A, const int64_t* a_shape, float a_scale, int32_t a_zp, const void* B,
+                      const int64_t* b_shape, float b_scale, int32_t b_zp, float c_scale, int32_t c_zp,
+                      const int64_t* out_shape, int rank, int qtype, void* C) {
+  if (!rounding_is_nearest()) return OR_ERR_ROUNDING;
+  int64_t n = 1;
+  for (int d = 0; d < rank; ++d) n *= out_shape[d];
+  const int64_t lo = q_lo(qtype), hi = q_hi(qtype);
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t a = load_q(A, qtype, bcast_offset(i, out_shape, a_shape, rank)) - a_zp;
+    const int64_t b = load_q(B, qtype, bcast_offset(i, out_shape, b_shape, rank)) - b_zp;
+    float v;
+    if (op == 0) {
+      float fa = a_scale * (float)a;
+      float fb = b_scale * (float)b;
+      v = fa + fb;
+    } else {
+      float m = a_scale * b_scale;
+      v = (float)(a * b) * m;
+    }
+    v = v / c_scale;
+    store_q(C, qtype, i, sat_rint_plus(v, c_zp, lo, hi));
+  }
+  return OR_OK;
+}
+
+/* [QEW] QLinearLeakyRelu (op 0) and QLinearSigmoid (op 1) on n codes:
+ *   d = DequantizeLinear(x) = (x - X_zp) * X_scale
+ *   leaky relu: f = alpha * d when d < 0, else d
+ *   sigmoid:    f = 1 / (1 + exp(-d))
+ *   y = QuantizeLinear(f) = saturate(rint(f / Y_scale) + Y_zp) */
+int or_qlinear_unary(int op, const void* X, int64_t n, int qtype, float x_scale, int32_t x_zp, float y_scale,
+                     int32_t y_zp, float alpha, void* Y) {
+  if (!rounding_is_nearest()) return OR_ERR_ROUNDING;
+  const int64_t lo = q_lo(qtype), hi = q_hi(qtype);
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) {
+    const float d = (float)(load_q(X, qtype, i) - x_zp) * x_scale;
+    float f;
+    if (op == 0)
+      f = d < 0.0f ? alpha * d : d;
+    else
+      f = 1.0f / (1.0f + expf(-d));
+    store_q(Y, qtype, i, sat_rint_plus(f / y_scale, y_zp, lo, hi));
+  }
+  return OR_OK;
 }
 
 static float sigmoid_f32(float x) { return 1.0f / (1.0f + expf(-x)); }

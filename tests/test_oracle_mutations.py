@@ -56,6 +56,12 @@ MUTATIONS = {
                                      "const int64_t az = a_zero_point ? a_zero_point[0] : 0;"),
     "mitf_bias_dropped": ("if (bias) v = v + bias[j];", "(void)bias;"),
     "mitf_scale_by_row_of_b": ("float mul = a_scale[pa] * b_scale[pb];", "float mul = a_scale[pa] * b_scale[0];"),
+    "bcast_index_reversed": ("    if (sh[d] != 1) off += idx * stride;", "    if (sh[d] != 1) off += (sh[d] - 1 - idx) * stride;"),
+    "qadd_b_scale_on_a": ("float fb = b_scale * (float)b;", "float fb = a_scale * (float)b;"),
+    "qmul_divides_by_scale_product": ("v = (float)(a * b) * m;", "v = (float)(a * b) / m;"),
+    "leaky_alpha_on_positive": ("f = d < 0.0f ? alpha * d : d;", "f = d > 0.0f ? alpha * d : d;"),
+    "mul_integer_zero_point_b_dropped": ("const int64_t b = load_q(B, btype, bcast_offset(i, out_shape, b_shape, rank)) - b_zp;",
+                                         "const int64_t b = load_q(B, btype, bcast_offset(i, out_shape, b_shape, rank));"),
 }
 
 

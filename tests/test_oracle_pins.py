@@ -638,3 +638,104 @@ def test_dynamic_quantize_matmul_tensor_quantization_invariants(orc):
     assert s == np.float32((np.float32(9.5) - np.float32(A.min())) / np.float32(255))
     assert uA.max() == 255 and uA.min() == 0
     assert np.all(np.abs((uA - z) * np.float64(s) - A) <= np.float64(s) / 2 * (1 + 1e-6))
+
+
+# ---- QLinear elementwise family (contrib schemas) ---------------------------
+
+def _golden_ints(g, key, dt=np.int64):
+    return np.array(g[key], np.int64).astype(dt)
+
+
+def test_qlinear_elementwise_worked_cases(orc):
+    g = read_golden("qlinear_elementwise_cases.txt")
+    A = _golden_ints(g, "A", np.uint8).reshape(2, 2)
+    B = _golden_ints(g, "B", np.uint8)
+    assert np.array_equal(orc.mul_integer(A, B, 10, 100).ravel(), _golden_ints(g, "mul_integer"))
+    cs, cz = g["add_c_scale_zp"]
+    assert np.array_equal(orc.qlinear_binary("add", A, 0.5, 10, B, 0.25, 100, float(cs), int(cz)).ravel(),
+                          _golden_ints(g, "add"))
+    cs, cz = g["mul_c_scale_zp"]
+    assert np.array_equal(orc.qlinear_binary("mul", A, 0.5, 10, B, 0.25, 100, float(cs), int(cz)).ravel(),
+                          _golden_ints(g, "mul"))
+    y = orc.qlinear_unary("leaky_relu", _golden_ints(g, "leaky_x", np.uint8), 0.5, 128, 0.5, 128, 0.25)
+    assert np.array_equal(y, _golden_ints(g, "leaky_y"))
+
+
+def _half_even(fr):
+    """Round a Fraction to the nearest integer, ties to even."""
+    f = math.floor(fr)
+    d = fr - f
+    if d > Fraction(1, 2) or (d == Fraction(1, 2) and f % 2 == 1):
+        return f + 1
+    return f
+
+
+@pytest.mark.parametrize("qt", ["u8", "s8"])
+@pytest.mark.parametrize("op", ["add", "mul"])
+def test_qlinear_binary_power_of_two_exact(orc, qt, op):
+    """Power-of-two scales: each fp32 step is exact, so every code equals the
+    rational formula rounded half to even and saturated."""
+    rng = np.random.default_rng(zlib.crc32(f"qbin{qt}{op}".encode()))
+    lo, hi, dt = (0, 255, np.uint8) if qt == "u8" else (-128, 127, np.int8)
+    A = rng.integers(lo, hi + 1, (7, 9)).astype(dt)
+    B = rng.integers(lo, hi + 1, (7, 9)).astype(dt)
+    za, zb, zc = (int(v) for v in rng.integers(lo, hi + 1, 3))
+    sa, sb, sc = Fraction(1, 8), Fraction(1, 4), (Fraction(1, 2) if op == "add" else Fraction(16))
+    C = orc.qlinear_binary(op, A, float(sa), za, B, float(sb), zb, float(sc), zc)
+    for (i, j), c in np.ndenumerate(C):
+        a, b = int(A[i, j]) - za, int(B[i, j]) - zb
+        v = (sa * a + sb * b) / sc if op == "add" else (a * b) * (sa * sb) / sc
+        assert int(c) == min(max(_half_even(v) + zc, lo), hi)
+
+
+@pytest.mark.parametrize("shapes", [((3, 4, 5), (5,)), ((3, 1, 5), (1, 4, 1)), ((1,), (2, 3)), ((2, 3), ())])
+def test_qlinear_broadcast_equals_explicit(orc, shapes):
+    rng = np.random.default_rng(7)
+    sa, sb = shapes
+    A = rng.integers(0, 256, sa).astype(np.uint8)
+    B = rng.integers(0, 256, sb).astype(np.uint8)
+    out = np.broadcast_shapes(sa, sb)
+    Ae, Be = np.broadcast_to(A, out).copy(), np.broadcast_to(B, out).copy()
+    for op in ("add", "mul"):
+        assert np.array_equal(orc.qlinear_binary(op, A, 0.03, 7, B, 0.02, 250, 0.07, 3),
+                              orc.qlinear_binary(op, Ae, 0.03, 7, Be, 0.02, 250, 0.07, 3))
+    assert np.array_equal(orc.mul_integer(A, B, 7, 250), orc.mul_integer(Ae, Be, 7, 250))
+
+
+def test_mul_integer_exact(orc):
+    rng = np.random.default_rng(8)
+    A = rng.integers(-128, 128, (6, 1, 8)).astype(np.int8)
+    B = rng.integers(0, 256, (5, 1)).astype(np.uint8)
+    C = orc.mul_integer(A, B, -3, 200)
+    ref = (A.astype(np.int64) + 3) * (B.astype(np.int64) - 200)
+    assert C.shape == ref.shape and np.array_equal(C, ref)
+
+
+@pytest.mark.parametrize("qt", ["u8", "s8"])
+def test_qlinear_leaky_relu_power_of_two_exact(orc, qt):
+    lo, hi, dt = (0, 255, np.uint8) if qt == "u8" else (-128, 127, np.int8)
+    X = np.arange(lo, hi + 1).astype(dt)
+    zx, zy = (100, 30) if qt == "u8" else (-20, 5)
+    Y = orc.qlinear_unary("leaky_relu", X, 0.25, zx, 0.125, zy, 0.375)
+    for x, y in zip(X.astype(np.int64), Y.astype(np.int64)):
+        d = Fraction(int(x) - zx, 4)
+        f = d * Fraction(3, 8) if d < 0 else d
+        assert int(y) == min(max(_half_even(f * 8) + zy, lo), hi)
+
+
+def test_qlinear_sigmoid_against_fp64(orc):
+    """Every code equals the fp64 sigmoid quantized, except where the fp64
+    value lies within 1e-5 of a rounding boundary (the fp32 exp may move it
+    across); outputs are non-decreasing in the input."""
+    X = np.arange(256).astype(np.uint8)
+    xs, zx, ys, zy = 0.07, 131, 1.0 / 256, 0
+    Y = orc.qlinear_unary("sigmoid", X, xs, zx, ys, zy).astype(np.int64)
+    assert np.all(np.diff(Y) >= 0)
+    for x, y in zip(range(256), Y):
+        d = float(np.float32((x - zx) * np.float32(xs)))
+        t = 1.0 / (1.0 + math.exp(-d)) / ys
+        exact = min(max(int(np.rint(t)) + zy, 0), 255)
+        if abs(t - math.floor(t) - 0.5) > 1e-5:
+            assert y == exact
+        else:
+            assert abs(y - exact) <= 1
