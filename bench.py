@@ -382,6 +382,25 @@ def measure_rows(args, dev, stream, world):
                                                   "column, bias, fp32 Y"}
     del Af, B, Yf, wsp
 
+    # QLinear elementwise on the [32,1024,4096] uint8 tensors: QLinearAdd of
+    # two same-shape tensors (3 B per element), QLinearLeakyRelu (2 B)
+    g = torch.Generator(device="cpu").manual_seed(6)
+    Xa = torch.randint(0, 256, QDQ_SHAPE, generator=g, dtype=torch.uint8).to(dev)
+    Xb = torch.randint(0, 256, QDQ_SHAPE, generator=g, dtype=torch.uint8).to(dev)
+    Yq = torch.empty(QDQ_SHAPE, dtype=torch.uint8, device=dev)
+    nel = Xa.numel()
+    fn = lambda: q.qlinear_binary("add", Xa, 0.02, 128, Xb, 0.03, 120, 0.04, 125, Yq)  # noqa: E731
+    sec, prof = _timed(fn, steps, warm, stream)
+    hbm = load_peaks()[0].get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    out["qlinear_add"] = {"ms": sec * 1e3, "GB/s": 3.0 * nel / sec / 1e9, "frac_hbm": 3.0 * nel / sec / 1e9 / hbm,
+                          "kernels": prof, "workload": "QLinearAdd u8 [32,1024,4096] + same shape, 3 B per element"}
+    fn = lambda: q.qlinear_unary("leaky_relu", Xa, 0.02, 128, 0.015, 100, Yq, alpha=0.1)  # noqa: E731
+    sec, prof = _timed(fn, steps, warm, stream)
+    out["qlinear_leaky_relu"] = {"ms": sec * 1e3, "GB/s": 2.0 * nel / sec / 1e9,
+                                 "frac_hbm": 2.0 * nel / sec / 1e9 / hbm, "kernels": prof,
+                                 "workload": "QLinearLeakyRelu u8 [32,1024,4096], 2 B per element"}
+    del Xa, Xb, Yq
+
     # DynamicQuantizeLSTM, bidirectional T=512 batch=64 I=H=1024
     w = workloads.lstm(seed=4)
     T_, b_, I_, H_ = 512, 64, 1024, 1024

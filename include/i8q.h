@@ -38,6 +38,9 @@
  *  [MITF] ONNX Runtime contrib schemas, "MatMulIntegerToFloat" and
  *         "DynamicQuantizeMatMul": inputs A, B, a_scale, b_scale,
  *         a_zero_point, b_zero_point, bias.
+ *  [QEW]  ONNX Runtime contrib schemas, "MulInteger", "QLinearAdd",
+ *         "QLinearMul" (doc formulas, Numpy-style broadcasting),
+ *         "QLinearLeakyRelu", "QLinearSigmoid" (doc strings).
  */
 #ifndef I8Q_H
 #define I8Q_H
@@ -351,6 +354,38 @@ int i8q_dynamic_quantize_matmul(const float* A, int64_t M, int64_t K, const void
 /* Scratch bytes of i8q_matmul_integer_to_float / i8q_dynamic_quantize_matmul
  * for M x N x K (0 for sizes below 1). */
 size_t i8q_matmul_integer_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* ========================================================================
+ * Quantized elementwise operators [QEW].  Scales and zero points are
+ * per-tensor scalars (host values); zero points lie in their type's range.
+ * A and B broadcast Numpy-style (shapes right-aligned, size-1 dimensions
+ * repeat; ranks 0..8); the caller allocates C with the broadcast shape,
+ * row-major.  A, B, C, X, Y are device pointers.  Errors: INVALID_ARG. */
+#define I8Q_QLINEAR_ADD 0
+#define I8Q_QLINEAR_MUL 1
+#define I8Q_QLINEAR_LEAKY_RELU 0
+#define I8Q_QLINEAR_SIGMOID 1
+
+/* QLinearAdd / QLinearMul, A, B and C all of qtype (U8|S8):
+ *   add: C = (A_scale * (A - A_zp) + B_scale * (B - B_zp)) / C_scale + C_zp
+ *   mul: C = ((A - A_zp) * (B - B_zp)) * (A_scale * B_scale) / C_scale + C_zp
+ * evaluated in the order written (fp32, each operation rounded once), then
+ * round half to even and saturation. */
+int i8q_qlinear_binary(int op, const void* A, const int64_t* a_shape, int a_rank, float a_scale, int a_zero_point,
+                       const void* B, const int64_t* b_shape, int b_rank, float b_scale, int b_zero_point,
+                       float c_scale, int c_zero_point, int qtype, void* C, void* stream);
+
+/* MulInteger: C (int32) = (A - A_zp) * (B - B_zp); atype, btype U8|S8. */
+int i8q_mul_integer(const void* A, int atype, const int64_t* a_shape, int a_rank, int a_zero_point, const void* B,
+                    int btype, const int64_t* b_shape, int b_rank, int b_zero_point, int32_t* C, void* stream);
+
+/* QLinearLeakyRelu (alpha used) / QLinearSigmoid on n codes of qtype:
+ *   d = (x - x_zp) * x_scale;  f = alpha * d if d < 0 else d  |  1 / (1 + exp(-d))
+ *   y = saturate(rint(f / y_scale) + y_zp).
+ * The sigmoid uses the device expf, which may differ from another
+ * library's by an ulp and so move a code that lies at a rounding boundary. */
+int i8q_qlinear_unary(int op, const void* X, int64_t n, int qtype, float x_scale, int x_zero_point, float y_scale,
+                      int y_zero_point, float alpha, void* Y, void* stream);
 
 /* ========================================================================
  * DynamicQuantizeLSTM [LSTM]: int8 W and R with per-channel (or

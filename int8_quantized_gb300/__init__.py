@@ -339,6 +339,44 @@ def dynamic_quantize_matmul(A, B, b_scale, Y, b_zero_point=None, bias=None, a_sc
     return Y
 
 
+QLINEAR_ADD, QLINEAR_MUL = 0, 1
+QLINEAR_LEAKY_RELU, QLINEAR_SIGMOID = 0, 1
+
+
+def _shape_array(t):
+    return _i64_array(t.shape) if t.dim() > 0 else None
+
+
+def qlinear_binary(op, A, a_scale, a_zero_point, B, b_scale, b_zero_point, c_scale, c_zero_point, C, stream=None):
+    """QLinearAdd (op "add") / QLinearMul (op "mul"): A, B, C uint8 or int8
+    CUDA tensors of one dtype; C has the broadcast shape of A and B."""
+    if not (A.dtype == B.dtype == C.dtype):
+        raise TypeError("A, B and C must have one dtype")
+    check(_L().i8q_qlinear_binary({"add": QLINEAR_ADD, "mul": QLINEAR_MUL}[op], _dev(A, "A"), _shape_array(A), A.dim(),
+                                  float(a_scale), int(a_zero_point), _dev(B, "B"), _shape_array(B), B.dim(),
+                                  float(b_scale), int(b_zero_point), float(c_scale), int(c_zero_point),
+                                  _TORCH_TYPE[A.dtype], _dev(C, "C"), _stream(stream)), "qlinear_binary")
+    return C
+
+
+def mul_integer(A, a_zero_point, B, b_zero_point, C, stream=None):
+    """MulInteger: C int32 with the broadcast shape of A and B."""
+    check(_L().i8q_mul_integer(_dev(A, "A"), _TORCH_TYPE[A.dtype], _shape_array(A), A.dim(), int(a_zero_point),
+                               _dev(B, "B"), _TORCH_TYPE[B.dtype], _shape_array(B), B.dim(), int(b_zero_point),
+                               _dev(C, "C", torch.int32), _stream(stream)), "mul_integer")
+    return C
+
+
+def qlinear_unary(op, X, x_scale, x_zero_point, y_scale, y_zero_point, Y, alpha=0.01, stream=None):
+    """QLinearLeakyRelu (op "leaky_relu") / QLinearSigmoid (op "sigmoid")."""
+    if X.dtype != Y.dtype or X.numel() != Y.numel():
+        raise TypeError("X and Y must have one dtype and size")
+    check(_L().i8q_qlinear_unary({"leaky_relu": QLINEAR_LEAKY_RELU, "sigmoid": QLINEAR_SIGMOID}[op], _dev(X, "X"),
+                                 X.numel(), _TORCH_TYPE[X.dtype], float(x_scale), int(x_zero_point), float(y_scale),
+                                 int(y_zero_point), float(alpha), _dev(Y, "Y"), _stream(stream)), "qlinear_unary")
+    return Y
+
+
 def dq_lstm_workspace_size(T, batch, input_size, hidden, direction):
     return int(_L().i8q_dq_lstm_workspace_size(T, batch, input_size, hidden, direction))
 

@@ -158,3 +158,20 @@ def test_matmul_integer_validation(lib):
     assert rc == _lib.ERR_INVALID_ARG and b"workspace" in lib.i8q_last_error()
     rc = lib.i8q_dynamic_quantize_matmul(p, 4, 8, p, _lib.S8, 3, p, None, 2, None, p, None, None, p, 1 << 20, None)
     assert rc == _lib.ERR_INVALID_ARG and b"b_scale" in lib.i8q_last_error()
+
+
+def test_qlinear_elementwise_validation(lib):
+    from int8_quantized_gb300 import _lib
+    p = ctypes.c_void_p(256)
+    s34, s54 = _arr([3, 4]), _arr([5, 4])
+    rc = lib.i8q_qlinear_binary(0, p, s34, 2, 0.1, 0, p, s54, 2, 0.1, 0, 0.1, 0, _lib.U8, p, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"broadcastable" in lib.i8q_last_error()
+    rc = lib.i8q_qlinear_binary(7, p, s34, 2, 0.1, 0, p, s34, 2, 0.1, 0, 0.1, 0, _lib.U8, p, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"op" in lib.i8q_last_error()
+    rc = lib.i8q_qlinear_binary(1, p, s34, 2, 0.1, 0, p, s34, 2, 0.1, 0, 0.1, -1, _lib.U8, p, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"zero point" in lib.i8q_last_error()
+    rc = lib.i8q_mul_integer(p, _lib.F32, s34, 2, 0, p, _lib.U8, s34, 2, 0, p, None)
+    assert rc == _lib.ERR_INVALID_ARG
+    rc = lib.i8q_qlinear_unary(1, p, 10, _lib.S8, 0.1, 0, 0.1, 200, 0.01, p, None)
+    assert rc == _lib.ERR_INVALID_ARG and b"zero point" in lib.i8q_last_error()
+    assert lib.i8q_qlinear_unary(0, None, 0, _lib.U8, 0.1, 0, 0.1, 0, 0.01, None, None) == _lib.OK
