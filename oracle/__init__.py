@@ -38,6 +38,8 @@ def load(path):
     l.or_qlinearconv.argtypes = [p, c_int, i64, i64, i64, i64, f32, i32, p, c_int, i64, i64,
                                  i64, p, p, c_int, f32, i32, p, p, p, p, i64, p, c_int]
     l.or_lstm_cell.argtypes = [p, p, p, p, p, p, p, i64, i64]
+    l.or_lstm_cell_ex.argtypes = [p, p, p, p, p, f32, c_int, p, p, p, i64, i64]
+    l.or_dyn_product_zp.argtypes = [p, p, p, p, c_int, p, i64, p, i64, i64, i64, p]
     l.or_qgemm.argtypes = [p, c_int, c_int, i64, i64, f32, i32, p, c_int, c_int, i64, p, p, i64, p, i64, i64,
                            f32, c_int, f32, i32, c_int, p]
     l.or_matmul_integer_to_float.argtypes = [p, c_int, i64, i64, p, c_int, i64, p, p, i64, p, p, i64, p, p]
@@ -46,7 +48,8 @@ def load(path):
     l.or_qlinear_unary.argtypes = [c_int, p, i64, c_int, f32, i32, f32, i32, f32, p]
     for fn in ("or_quantize_linear", "or_dequantize_linear", "or_quantize_rows_u8",
                "or_quantize_cols_s8", "or_qgemm_dyn_rows", "or_qlinearconv", "or_lstm_cell", "or_qgemm",
-               "or_matmul_integer_to_float", "or_mul_integer", "or_qlinear_binary", "or_qlinear_unary"):
+               "or_matmul_integer_to_float", "or_mul_integer", "or_qlinear_binary", "or_qlinear_unary",
+               "or_lstm_cell_ex", "or_dyn_product_zp"):
         getattr(l, fn).restype = ctypes.c_int
     return l
 
@@ -368,8 +371,9 @@ def qlinear_unary(op, X, x_scale, x_zero_point, y_scale, y_zero_point, alpha=0.0
     return Y
 
 
-def lstm_cell(Gx, Gh, Wb, Rb, c_prev):
-    """One DynamicQuantizeLSTM cell update (default activations, iofc)."""
+def lstm_cell(Gx, Gh, Wb, Rb, c_prev, P=None, clip=0.0, input_forget=False):
+    """One DynamicQuantizeLSTM cell update (default activations, iofc);
+    P: peepholes (3H, iof) or None; clip <= 0: no clip."""
     Gx = np.ascontiguousarray(Gx, dtype=np.float32)
     Gh = np.ascontiguousarray(Gh, dtype=np.float32)
     c_prev = np.ascontiguousarray(c_prev, dtype=np.float32)
@@ -377,57 +381,92 @@ def lstm_cell(Gx, Gh, Wb, Rb, c_prev):
     H = H4 // 4
     Wb = None if Wb is None else np.ascontiguousarray(Wb, dtype=np.float32)
     Rb = None if Rb is None else np.ascontiguousarray(Rb, dtype=np.float32)
+    P = None if P is None else np.ascontiguousarray(P, dtype=np.float32)
     h = np.empty((batch, H), dtype=np.float32)
     c = np.empty((batch, H), dtype=np.float32)
-    _check(lib().or_lstm_cell(_ptr(Gx), _ptr(Gh), _ptr(Wb), _ptr(Rb), _ptr(c_prev), _ptr(h), _ptr(c),
-                              batch, H), "lstm_cell")
+    _check(lib().or_lstm_cell_ex(_ptr(Gx), _ptr(Gh), _ptr(Wb), _ptr(Rb), _ptr(P), float(clip), int(bool(input_forget)),
+                                 _ptr(c_prev), _ptr(h), _ptr(c), batch, H), "lstm_cell")
     return h, c
 
 
-def lstm_projection(X, W, W_scale):
+def dyn_product_zp(A, B, scaleB, zeroB=None):
+    """The dequantized product of fp32 A (rows quantized to uint8 as in the
+    inner product) with 8-bit B (K x N, uint8 or int8) whose zero point is
+    per column or per tensor: ((float)sum (uA - zA)(B - zB) * sA) * sB."""
+    uA, sA, zA = quantize_rows_u8(A)
+    B = np.ascontiguousarray(B)
+    M, K = uA.shape
+    N = B.shape[1]
+    zb = None if zeroB is None else np.ascontiguousarray(np.atleast_1d(zeroB), dtype=np.int32)
+    sB = np.ascontiguousarray(np.broadcast_to(np.asarray(scaleB, np.float32), (N,)))
+    C = np.empty((M, N), np.float32)
+    _check(lib().or_dyn_product_zp(_ptr(uA), _ptr(zA), _ptr(sA), _ptr(B), U8 if B.dtype == np.uint8 else S8, _ptr(zb),
+                                   0 if zb is None else zb.size, _ptr(sB), M, N, K, _ptr(C)), "dyn_product_zp")
+    return C
+
+
+def _lstm_product(A, Wq, scale, zero_point):
+    """Gx or Gh: the int8-B inner product when W is int8 without zero point,
+    else the zero-point product (same arithmetic when the zero point is 0)."""
+    if zero_point is None and Wq.dtype == np.int8:
+        return dynamic_quantized_inner_product(A, iB=Wq, scaleB=scale)["C32"]
+    return dyn_product_zp(A, Wq, scale, zero_point)
+
+
+def lstm_projection(X, W, W_scale, W_zero_point=None):
     """Input projection of one direction: X (T, batch, I) quantized per row,
-    times int8 W (I x 4H) with per-column scales, no bias, fp32 out."""
+    times 8-bit W (I x 4H) with per-column scales (and zero points), no
+    bias, fp32 out."""
     T, batch, I = X.shape
-    out = dynamic_quantized_inner_product(X.reshape(T * batch, I), iB=W, scaleB=W_scale)
-    return out["C32"].reshape(T, batch, -1)
+    return _lstm_product(X.reshape(T * batch, I), W, W_scale, W_zero_point).reshape(T, batch, -1)
 
 
-def lstm_step(Gx_t, h_prev, c_prev, R, R_scale, Wb, Rb):
+def lstm_step(Gx_t, h_prev, c_prev, R, R_scale, Wb, Rb, R_zero_point=None, P=None, clip=0.0, input_forget=False):
     """One recurrence step of one direction: quantize h_prev per row, take
-    the dequantized product with int8 R, then the cell update."""
-    Gh = dynamic_quantized_inner_product(h_prev, iB=R, scaleB=R_scale)["C32"]
-    return lstm_cell(Gx_t, Gh, Wb, Rb, c_prev)
+    the dequantized product with 8-bit R, then the cell update."""
+    Gh = _lstm_product(h_prev, R, R_scale, R_zero_point)
+    return lstm_cell(Gx_t, Gh, Wb, Rb, c_prev, P, clip, input_forget)
 
 
-def dynamic_quantize_lstm(X, W, R, B, W_scale, R_scale, h0=None, c0=None, direction="forward",
-                          steps=None):
-    """DynamicQuantizeLSTM (ONNX Runtime contrib schema) with int8 W/R, zero
-    points 0, default activations, no peepholes, no sequence_lens, no clip.
-    X (T, batch, I); W (D, I, 4H); R (D, H, 4H); B (D, 8H) or None;
-    scales (D, 4H).  Returns Y (T, D, batch, H), Y_h, Y_c (D, batch, H).
-    steps (default T) limits how many steps each direction runs; rows of Y
-    for steps not run stay zero."""
+def dynamic_quantize_lstm(X, W, R, B, W_scale, R_scale, h0=None, c0=None, direction="forward", steps=None,
+                          W_zero_point=None, R_zero_point=None, P=None, clip=0.0, input_forget=False,
+                          sequence_lens=None):
+    """DynamicQuantizeLSTM (ONNX Runtime contrib schema), default
+    activations.  X (T, batch, I); W (D, I, 4H) and R (D, H, 4H) uint8 or
+    int8 with zero points (D, 4H) / (D,) or None; scales (D, 4H); B (D, 8H)
+    or None; P (D, 3H) or None; sequence_lens (batch,) or None.  A batch row
+    with length L runs steps t = 0..L-1 (forward) or L-1..0 (reverse); Y is 0
+    for t >= L and Y_h, Y_c hold the state after its last step.
+    Returns Y (T, D, batch, H), Y_h, Y_c (D, batch, H).  steps (default T)
+    limits how many steps each direction runs."""
     T, batch, I = X.shape
     D = W.shape[0]
     H = R.shape[1]
     dirs = {"forward": [0], "reverse": [1], "bidirectional": [0, 1]}[direction]
     assert len(dirs) == D
     S = T if steps is None else steps
+    L = np.full(batch, T, np.int64) if sequence_lens is None else np.asarray(sequence_lens, np.int64)
     Y = np.zeros((T, D, batch, H), dtype=np.float32)
     Yh = np.zeros((D, batch, H), dtype=np.float32)
     Yc = np.zeros((D, batch, H), dtype=np.float32)
+    zp = lambda z, d: None if z is None else np.asarray(z)[d]  # noqa: E731
+    rows = np.arange(batch)
     for d, kind in enumerate(dirs):
-        Gx = lstm_projection(X, W[d], W_scale[d])
+        Gx = lstm_projection(X, W[d], W_scale[d], zp(W_zero_point, d))
         h = np.zeros((batch, H), np.float32) if h0 is None else np.array(h0[d], np.float32)
         c = np.zeros((batch, H), np.float32) if c0 is None else np.array(c0[d], np.float32)
         Wb = None if B is None else B[d, :4 * H]
         Rb = None if B is None else B[d, 4 * H:]
-        order = range(T) if kind == 0 else range(T - 1, -1, -1)
-        for n, t in enumerate(order):
-            if n >= S:
-                break
-            h, c = lstm_step(Gx[t], h, c, R[d], R_scale[d], Wb, Rb)
-            Y[t, d] = h
+        Pd = None if P is None else P[d]
+        for n in range(min(S, T)):
+            t_b = np.where(kind == 0, n, L - 1 - n)
+            active = n < L
+            Gx_t = Gx[np.clip(t_b, 0, T - 1), rows]
+            hn, cn = lstm_step(Gx_t, h, c, R[d], R_scale[d], Wb, Rb, zp(R_zero_point, d), Pd, clip, input_forget)
+            h = np.where(active[:, None], hn, h)
+            c = np.where(active[:, None], cn, c)
+            for b in np.nonzero(active)[0]:
+                Y[t_b[b], d, b] = h[b]
         Yh[d] = h
         Yc[d] = c
     return Y, Yh, Yc

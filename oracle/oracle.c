@@ -516,33 +516,88 @@ int or_qlinear_unary(int op, const void* X, int64_t n, int qtype, float x_scale,
 static float sigmoid_f32(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 /* [LSTM] one cell update for one direction and one time step, default
- * activations (f = sigmoid, g = tanh, h = tanh), no peepholes, no clip.
- * The gate pre-activations are, per batch row b and column n of 4H,
- *   g = ((Gx[b,n] + Gh[b,n]) + Wb[n]) + Rb[n]
- * in the iofc column order of W, R and B:
- *   i = sigmoid(g_i), o = sigmoid(g_o), f = sigmoid(g_f), ct = tanh(g_c)
- *   c = f * c_prev + i * ct,   h = o * tanh(c)
- * sigmoid(x) = 1 / (1 + exp(-x)).  Wb or Rb may be NULL (zero bias). */
-int or_lstm_cell(const float* Gx, const float* Gh, const float* Wb, const float* Rb,
-                 const float* c_prev, float* h_out, float* c_out, int64_t batch, int64_t H) {
+ * activations (sigmoid for i, o, f; tanh for the candidate and the output),
+ * gate columns in iofc order.  The ONNX LSTM equations the schema points to
+ * (not printed on the pages) give each gate's terms in this order, summed
+ * left to right:
+ *   i = f(X Wi + H Ri + Pi (.) C_prev + Wbi + Rbi)
+ *   f = f(X Wf + H Rf + Pf (.) C_prev + Wbf + Rbf)     (1 - i when input_forget)
+ *   c~ = g(X Wc + H Rc + Wbc + Rbc)
+ *   C = f (.) C_prev + i (.) c~
+ *   o = f(X Wo + H Ro + Po (.) C + Wbo + Rbo)
+ *   H = o (.) h(C)
+ * Gx and Gh are the two dequantized products.  P holds Pi, Po, Pf (3H,
+ * "P[iof]") or is NULL (no peephole terms).  clip > 0 bounds each gate's
+ * input to [-clip, clip] before its activation; clip <= 0 is no clip (the
+ * schema: "No clip if not specified"; the third-party page lists a default
+ * of 0, read as the same).  A missing bias adds nothing. */
+int or_lstm_cell_ex(const float* Gx, const float* Gh, const float* Wb, const float* Rb, const float* P, float clip,
+                    int input_forget, const float* c_prev, float* h_out, float* c_out, int64_t batch, int64_t H) {
   for (int64_t b = 0; b < batch; ++b) {
     for (int64_t u = 0; u < H; ++u) {
+      const float cp = c_prev[b * H + u];
       float g[4];
       for (int q = 0; q < 4; ++q) {
         int64_t n = q * H + u;
         float v = Gx[b * 4 * H + n] + Gh[b * 4 * H + n];
-        if (Wb) v = v + Wb[n];
-        if (Rb) v = v + Rb[n];
+        if (P && q == 0) v = v + P[u] * cp;
+        if (P && q == 2) v = v + P[2 * H + u] * cp;
+        if (q != 1) {
+          if (Wb) v = v + Wb[n];
+          if (Rb) v = v + Rb[n];
+          if (clip > 0.0f) v = v < -clip ? -clip : (v > clip ? clip : v);
+        }
         g[q] = v;
       }
       float ig = sigmoid_f32(g[0]);
-      float og = sigmoid_f32(g[1]);
-      float fg = sigmoid_f32(g[2]);
+      float fg = input_forget ? 1.0f - ig : sigmoid_f32(g[2]);
       float ct = tanhf(g[3]);
-      float c = fg * c_prev[b * H + u] + ig * ct;
+      float c = fg * cp + ig * ct;
+      float vo = g[1];
+      if (P) vo = vo + P[H + u] * c;
+      if (Wb) vo = vo + Wb[H + u];
+      if (Rb) vo = vo + Rb[H + u];
+      if (clip > 0.0f) vo = vo < -clip ? -clip : (vo > clip ? clip : vo);
+      float og = sigmoid_f32(vo);
       c_out[b * H + u] = c;
       h_out[b * H + u] = og * tanhf(c);
     }
   }
   return OR_OK;
+}
+
+/* The default cell: no peepholes, no clip, input_forget 0. */
+int or_lstm_cell(const float* Gx, const float* Gh, const float* Wb, const float* Rb, const float* c_prev,
+                 float* h_out, float* c_out, int64_t batch, int64_t H) {
+  return or_lstm_cell_ex(Gx, Gh, Wb, Rb, NULL, 0.0f, 0, c_prev, h_out, c_out, batch, H);
+}
+
+/* [DQIP] / [LSTM] the dequantized product of per-row uint8 codes uA (M x K,
+ * scaleA, zeroA) with 8-bit B codes (K x N, type btype) that carry a zero
+ * point per column (n_zb == N) or per tensor (n_zb == 1; NULL: 0):
+ *   C[i,j] = ((float)sum_k (uA[i,k] - zeroA[i]) * (B[k,j] - zeroB[j]) * scaleA[i]) * scaleB[j]
+ * in the order of the inner product's epilogue; the int32 sum is exact. */
+int or_dyn_product_zp(const uint8_t* uA, const int32_t* zeroA, const float* scaleA, const void* B, int btype,
+                      const int32_t* zeroB, int64_t n_zb, const float* scaleB, int64_t M, int64_t N, int64_t K,
+                      float* C) {
+  if (!rounding_is_nearest()) return OR_ERR_ROUNDING;
+  int err = OR_OK;
+#pragma omp parallel for schedule(static) reduction(min : err)
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      const int64_t zb = zeroB ? zeroB[n_zb == N ? j : 0] : 0;
+      int64_t acc = 0;
+      for (int64_t k = 0; k < K; ++k)
+        acc += ((int64_t)uA[i * K + k] - (int64_t)zeroA[i]) * (load_q(B, btype, k * N + j) - zb);
+      if (acc > INT32_MAX || acc < INT32_MIN) {
+        err = OR_ERR_OVERFLOW;
+        continue;
+      }
+      float v = (float)(int32_t)acc;
+      v = v * scaleA[i];
+      v = v * scaleB[j];
+      C[i * N + j] = v;
+    }
+  }
+  return err;
 }

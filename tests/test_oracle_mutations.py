@@ -41,8 +41,15 @@ MUTATIONS = {
     "conv_bias_dropped": ("if (B) acc += B[m];", "(void)B;"),
     "conv_weight_zero_point_per_tensor": ("const int64_t wz = w_zero_point[per_channel ? m : 0];",
                                           "const int64_t wz = w_zero_point[0];"),
-    "lstm_gates_o_f_swapped": ("float og = sigmoid_f32(g[1]);\n      float fg = sigmoid_f32(g[2]);",
-                               "float og = sigmoid_f32(g[2]);\n      float fg = sigmoid_f32(g[1]);"),
+    "lstm_gates_o_f_swapped": ("float fg = input_forget ? 1.0f - ig : sigmoid_f32(g[2]);",
+                               "float fg = input_forget ? 1.0f - ig : sigmoid_f32(g[1]);"),
+    "lstm_peephole_o_uses_old_cell": ("if (P) vo = vo + P[H + u] * c;", "if (P) vo = vo + P[H + u] * cp;"),
+    "lstm_coupled_gate_is_i": ("float fg = input_forget ? 1.0f - ig : sigmoid_f32(g[2]);",
+                               "float fg = input_forget ? ig : sigmoid_f32(g[2]);"),
+    "lstm_clip_skips_candidate": ("        if (q != 1) {\n          if (Wb) v = v + Wb[n];\n          if (Rb) v = v + Rb[n];\n          if (clip > 0.0f)",
+                                  "        if (q != 1) {\n          if (Wb) v = v + Wb[n];\n          if (Rb) v = v + Rb[n];\n          if (clip > 0.0f && q != 3)"),
+    "zp_product_zero_point_per_tensor": ("const int64_t zb = zeroB ? zeroB[n_zb == N ? j : 0] : 0;",
+                                         "const int64_t zb = zeroB ? zeroB[0] : 0;"),
     "lstm_recurrent_bias_dropped": ("if (Rb) v = v + Rb[n];", "(void)Rb;"),
     "bf16_truncates": ("u += 0x7fffu + lsb;", "(void)lsb;"),
     "qgemm_b_zero_point_per_tensor": ("const int64_t bz = b_zero_point ? b_zero_point[n_b == N ? j : 0] : 0;",

@@ -739,3 +739,110 @@ def test_qlinear_sigmoid_against_fp64(orc):
             assert y == exact
         else:
             assert abs(y - exact) <= 1
+
+
+# ---- DynamicQuantizeLSTM variants ------------------------------------------
+
+def _textbook_cell(gx, c0, Bv, H, P=None, clip=0.0, input_forget=False):
+    """fp64 ONNX LSTM cell from pre-activation products gx (b, 4H) and c0,
+    peepholes P (3H, iof), clip and coupled gates."""
+    Wb, Rb = Bv[:4 * H], Bv[4 * H:]
+    cl = (lambda v: np.clip(v, -clip, clip)) if clip > 0 else (lambda v: v)  # noqa: E731
+    pi = 0 if P is None else P[:H] * c0
+    pf = 0 if P is None else P[2 * H:] * c0
+    i = _sig(cl(gx[:, :H] + pi + Wb[:H] + Rb[:H]))
+    f = 1 - i if input_forget else _sig(cl(gx[:, 2 * H:3 * H] + pf + Wb[2 * H:3 * H] + Rb[2 * H:3 * H]))
+    ct = np.tanh(cl(gx[:, 3 * H:] + Wb[3 * H:] + Rb[3 * H:]))
+    c = f * c0 + i * ct
+    po = 0 if P is None else P[H:2 * H] * c
+    o = _sig(cl(gx[:, H:2 * H] + po + Wb[H:2 * H] + Rb[H:2 * H]))
+    return o * np.tanh(c), c
+
+
+@pytest.mark.parametrize("peep,clip,coupled", [(True, 0.0, False), (False, 0.7, False), (False, 0.0, True),
+                                               (True, 1.3, True)])
+def test_lstm_variant_first_step_equals_textbook(orc, peep, clip, coupled):
+    """Step 0 with h0 = 0 (Gh exactly 0) and X on the lossless grid with
+    power-of-two W scales (Gx exact): the cell with peepholes, clip or
+    coupled gates is the fp64 textbook cell to fp32 rounding."""
+    rng = np.random.default_rng(61)
+    T, b, I, H = 1, 4, 24, 8
+    X = lossless_A(rng, T * b, I).reshape(T, b, I)
+    W = rng.integers(-128, 128, size=(1, I, 4 * H)).astype(np.int8)
+    R = rng.integers(-128, 128, size=(1, H, 4 * H)).astype(np.int8)
+    Ws = (2.0 ** rng.integers(-9, -6, size=(1, 4 * H))).astype(np.float32)
+    Rs = (2.0 ** rng.integers(-9, -6, size=(1, 4 * H))).astype(np.float32)
+    Bb = rng.normal(0, 0.1, size=(1, 8 * H)).astype(np.float32)
+    c0 = rng.normal(0, 1, size=(1, b, H)).astype(np.float32)
+    P = rng.normal(0, 0.5, size=(1, 3 * H)).astype(np.float32) if peep else None
+    Y, Yh, Yc = orc.dynamic_quantize_lstm(X, W, R, Bb, Ws, Rs, c0=c0, P=P, clip=clip, input_forget=coupled)
+    gx = X[0].astype(np.float64) @ (W[0] * Ws[0].astype(np.float64))
+    h, c = _textbook_cell(gx, c0[0].astype(np.float64), Bb[0].astype(np.float64), H,
+                          None if P is None else P[0].astype(np.float64), clip, coupled)
+    assert np.allclose(Yc[0], c, rtol=4e-6, atol=4e-7)
+    assert np.allclose(Yh[0], h, rtol=4e-6, atol=4e-7)
+
+
+def test_lstm_variant_neutral_settings(orc):
+    """Zero peepholes equal none; a clip above every gate input equals none."""
+    w = workloads.lstm(seed=4, T=4, batch=3, I=32, H=16, D=1)
+    base = orc.dynamic_quantize_lstm(w["X"], w["W"], w["R"], w["B"], w["W_scale"], w["R_scale"])
+    zp = orc.dynamic_quantize_lstm(w["X"], w["W"], w["R"], w["B"], w["W_scale"], w["R_scale"],
+                                   P=np.zeros((1, 48), np.float32))
+    cl = orc.dynamic_quantize_lstm(w["X"], w["W"], w["R"], w["B"], w["W_scale"], w["R_scale"], clip=1e30)
+    for a, b_, c_ in zip(base, zp, cl):
+        assert np.array_equal(a, b_) and np.array_equal(a, c_)
+    lim = orc.dynamic_quantize_lstm(w["X"], w["W"], w["R"], w["B"], w["W_scale"], w["R_scale"], clip=0.05)
+    assert not np.array_equal(lim[0], base[0])
+
+
+def test_lstm_uint8_weights_with_zero_point_equal_shifted_int8(orc):
+    """uint8 W, R with zero point 128 per channel give the same sums as the
+    int8 codes W - 128 without zero point, so the same outputs."""
+    w = workloads.lstm(seed=4, T=5, batch=2, I=32, H=16, D=2)
+    Wu = (w["W"].astype(np.int16) + 128).astype(np.uint8)
+    Ru = (w["R"].astype(np.int16) + 128).astype(np.uint8)
+    z = np.full((2, 64), 128, np.int32)
+    a = orc.dynamic_quantize_lstm(w["X"], w["W"], w["R"], w["B"], w["W_scale"], w["R_scale"], direction="bidirectional")
+    b_ = orc.dynamic_quantize_lstm(w["X"], Wu, Ru, w["B"], w["W_scale"], w["R_scale"], direction="bidirectional",
+                                   W_zero_point=z, R_zero_point=z)
+    for x, y in zip(a, b_):
+        assert np.array_equal(x, y)
+
+
+def test_dyn_product_zero_point_brute_force(orc):
+    rng = np.random.default_rng(62)
+    A = rng.normal(0, 1, (5, 13)).astype(np.float32)
+    B = rng.integers(0, 256, (13, 7)).astype(np.uint8)
+    zb = rng.integers(0, 256, 7).astype(np.int32)
+    sb = np.full(7, 0.25, np.float32)
+    C = orc.dyn_product_zp(A, B, sb, zb)
+    uA, sA, zA = orc.quantize_rows_u8(A)
+    acc = (uA.astype(np.int64) - zA[:, None]) @ (B.astype(np.int64) - zb[None, :])
+    ref = ((acc.astype(np.float32) * sA[:, None]).astype(np.float32) * sb[None, :]).astype(np.float32)
+    assert np.array_equal(C, ref)
+    iB = rng.integers(-128, 128, (13, 7)).astype(np.int8)
+    assert np.array_equal(orc.dyn_product_zp(A, iB, sb), orc.dynamic_quantized_inner_product(A, iB=iB, scaleB=sb)["C32"])
+
+
+@pytest.mark.parametrize("direction", ["forward", "reverse"])
+def test_lstm_sequence_lens_equal_truncated_runs(orc, direction):
+    """A batch row of length L gives the run over its first L inputs alone;
+    Y is zero from t = L on; rows of full length are unchanged."""
+    w = workloads.lstm(seed=4, T=6, batch=4, I=32, H=16, D=1)
+    sel = slice(0, 1)
+    lens = np.array([6, 3, 1, 0])
+    Y, Yh, Yc = orc.dynamic_quantize_lstm(w["X"], w["W"][sel], w["R"][sel], w["B"][sel], w["W_scale"][sel],
+                                          w["R_scale"][sel], direction=direction, sequence_lens=lens)
+    Yf, Yhf, Ycf = orc.dynamic_quantize_lstm(w["X"], w["W"][sel], w["R"][sel], w["B"][sel], w["W_scale"][sel],
+                                             w["R_scale"][sel], direction=direction)
+    assert np.array_equal(Y[:, :, 0], Yf[:, :, 0]) and np.array_equal(Yh[:, 0], Yhf[:, 0])
+    for b, L in enumerate(lens):
+        assert np.all(Y[L:, :, b] == 0)
+        if L == 0:
+            assert np.all(Yh[:, b] == 0) and np.all(Yc[:, b] == 0)
+            continue
+        Yb, Yhb, Ycb = orc.dynamic_quantize_lstm(w["X"][:L, b:b + 1], w["W"][sel], w["R"][sel], w["B"][sel],
+                                                 w["W_scale"][sel], w["R_scale"][sel], direction=direction)
+        assert np.array_equal(Y[:L, :, b], Yb[:, :, 0])
+        assert np.array_equal(Yh[:, b], Yhb[:, 0]) and np.array_equal(Yc[:, b], Ycb[:, 0])
