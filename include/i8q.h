@@ -404,8 +404,9 @@ int i8q_qlinear_unary(int op, const void* X, int64_t n, int qtype, float x_scale
  *   Bias [D, 8H] or NULL; h0, c0 [D, batch, H] or NULL (zeros);
  *   Y [T, D, batch, H], Y_h, Y_c [D, batch, H]; any output may be NULL.
  *   D = 2 for I8Q_LSTM_BIDIRECTIONAL, else 1.
+ * Nonzero zero points are taken as in i8q_dq_lstm_forward_ex.
  * workspace: at least i8q_dq_lstm_workspace_size bytes, 256-byte aligned.
- * Errors: INVALID_ARG, UNSUPPORTED (nonzero zero points), CUDA. */
+ * Errors: INVALID_ARG, CUDA. */
 int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int64_t input, int64_t hidden,
                         int direction, const int8_t* W, const float* W_scale, const int8_t* W_zero_point,
                         size_t n_wscale, const int8_t* R, const float* R_scale,
@@ -414,6 +415,32 @@ int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int64_t input,
                         size_t ws_bytes, void* stream);
 
 size_t i8q_dq_lstm_workspace_size(int64_t T, int64_t batch, int64_t input, int64_t hidden, int direction);
+
+/* DynamicQuantizeLSTM [LSTM] with the schema's optional inputs and
+ * attributes (default activations only: the pages do not list the others).
+ *   W, R: device codes of wtype (I8Q_S8 | I8Q_U8), shapes as above.
+ *   W_zero_point, R_zero_point: device codes of wtype, n_wscale / n_rscale
+ *   entries (per direction or per channel, in iofc column order), or NULL.
+ *   sequence_lens: device int32 [batch] or NULL.  Row b runs t = 0..L-1
+ *   (forward) or L-1..0 (reverse) with L = sequence_lens[b] clamped to
+ *   [0, T]; Y is 0 from t = L on; Y_h, Y_c hold the row's last state.
+ *   P: device fp32 [D, 3H] peepholes (Pi, Po, Pf) or NULL.
+ *   clip > 0 bounds every gate input to [-clip, clip]; clip <= 0: no clip.
+ *   input_forget != 0: f = 1 - i.
+ *   Gate terms are summed in the order of the default ONNX LSTM equations:
+ *   i = sigmoid(clip(X Wi + H Ri + Pi*C_prev + Wbi + Rbi)),
+ *   f = sigmoid(clip(X Wf + H Rf + Pf*C_prev + Wbf + Rbf)),
+ *   c~ = tanh(clip(X Wc + H Rc + Wbc + Rbc)), C = f*C_prev + i*c~,
+ *   o = sigmoid(clip(X Wo + H Ro + Po*C + Wbo + Rbo)), H = o*tanh(C),
+ *   where X W and H R are the dequantized products of the per-row uint8
+ *   codes with (W - W_zero_point), (R - R_zero_point).
+ * Same workspace as i8q_dq_lstm_forward.  Errors: INVALID_ARG, CUDA. */
+int i8q_dq_lstm_forward_ex(const float* X, int64_t T, int64_t batch, int64_t input, int64_t hidden, int direction,
+                           const void* W, const void* R, int wtype, const float* W_scale, const void* W_zero_point,
+                           size_t n_wscale, const float* R_scale, const void* R_zero_point, size_t n_rscale,
+                           const float* Bias, const int32_t* sequence_lens, const float* h0, const float* c0,
+                           const float* P, float clip, int input_forget, float* Y, float* Y_h, float* Y_c,
+                           void* workspace, size_t ws_bytes, void* stream);
 
 /* ========================================================================
  * Measurement (not on the pages)

@@ -397,3 +397,29 @@ def dq_lstm_forward(X, W, R, W_scale, R_scale, workspace, direction=LSTM_FORWARD
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream)),
         "dq_lstm_forward")
     return Y, Y_h, Y_c
+
+
+def dq_lstm_forward_ex(X, W, R, W_scale, R_scale, workspace, direction=LSTM_FORWARD, B=None, sequence_lens=None,
+                       h0=None, c0=None, P=None, clip=0.0, input_forget=False, Y=None, Y_h=None, Y_c=None,
+                       W_zero_point=None, R_zero_point=None, stream=None):
+    """DynamicQuantizeLSTM with the optional inputs and attributes: W, R
+    uint8 or int8 (one dtype) with zero points of that dtype ([D] or
+    [D, 4H]); sequence_lens int32 [batch]; P [D, 3H]; clip (<= 0: none);
+    input_forget.  Shapes otherwise as dq_lstm_forward."""
+    T, batch, I = X.shape
+    H = R.shape[1]
+    if W.dtype != R.dtype or W.dtype not in (torch.uint8, torch.int8):
+        raise TypeError("W and R must both be uint8 or both int8")
+    for z, n in ((W_zero_point, "W_zero_point"), (R_zero_point, "R_zero_point")):
+        if z is not None and z.dtype != W.dtype:
+            raise TypeError(f"{n} must have W's dtype")
+    check(_L().i8q_dq_lstm_forward_ex(
+        _dev(X, "X", torch.float32), T, batch, I, H, direction, _dev(W, "W"), _dev(R, "R"), _TORCH_TYPE[W.dtype],
+        _dev(W_scale, "W_scale", torch.float32), _dev(W_zero_point, "W_zero_point"), W_scale.numel(),
+        _dev(R_scale, "R_scale", torch.float32), _dev(R_zero_point, "R_zero_point"), R_scale.numel(),
+        _dev(B, "B", torch.float32), _dev(sequence_lens, "sequence_lens", torch.int32),
+        _dev(h0, "h0", torch.float32), _dev(c0, "c0", torch.float32), _dev(P, "P", torch.float32), float(clip),
+        int(bool(input_forget)), _dev(Y, "Y", torch.float32), _dev(Y_h, "Y_h", torch.float32),
+        _dev(Y_c, "Y_c", torch.float32), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "dq_lstm_forward_ex")
+    return Y, Y_h, Y_c

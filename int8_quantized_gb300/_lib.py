@@ -49,6 +49,8 @@ SIGNATURES = {
                                          _p]),
     "i8q_dynamic_quantize_matmul": (_i, [_p, _i64, _i64, _p, _i, _i64, _p, _p, _sz, _p, _p, _p, _p, _p, _sz, _p]),
     "i8q_matmul_integer_workspace_size": (_sz, [_i64, _i64, _i64]),
+    "i8q_dq_lstm_forward_ex": (_i, [_p, _i64, _i64, _i64, _i64, _i, _p, _p, _i, _p, _p, _sz, _p, _p, _sz, _p, _p, _p,
+                                    _p, _p, _f, _i, _p, _p, _p, _p, _sz, _p]),
     "i8q_qlinear_binary": (_i, [_i, _p, _p, _i, _f, _i, _p, _p, _i, _f, _i, _f, _i, _i, _p, _p]),
     "i8q_mul_integer": (_i, [_p, _i, _p, _i, _i, _p, _i, _p, _i, _i, _p, _p]),
     "i8q_qlinear_unary": (_i, [_i, _p, _i64, _i, _f, _i, _f, _i, _f, _p, _p]),

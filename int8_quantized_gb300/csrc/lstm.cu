@@ -120,6 +120,61 @@ __global__ void any_nonzero_s8(const int8_t* __restrict__ p, int64_t n, int* __r
     if (p[i] != 0) atomicOr(flag, 1);
 }
 
+// W or R of one direction (K x 4H, 8-bit codes, columns in iofc order) with
+// its zero point subtracted, as bf16 rows of the gate-interleaved K-major
+// operand: column q*H + u lands at row 4u + q, K contiguous, zeros beyond K;
+// colsum[row] = sum_k (W - zp).  zp: typed codes, one per direction
+// (n_zp == 1) or per column (n_zp == 4H), or null (0).  |W - zp| <= 255 is
+// exact in bf16.  One CTA per 32 columns; 64 K-rows per step through shared
+// memory.
+template <bool SIGNED>
+__global__ void __launch_bounds__(256)
+repack_gates_zp(const uint8_t* __restrict__ W, int64_t K, int64_t H, const uint8_t* __restrict__ zp, int64_t n_zp,
+                int64_t Kp, __nv_bfloat16* __restrict__ out, int32_t* __restrict__ colsum) {
+  __shared__ int16_t tile[32][64 + 2];
+  __shared__ int32_t sums[8][32];
+  const int64_t H4 = 4 * H;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int64_t j0 = (int64_t)blockIdx.x * 32;
+  const int64_t j = j0 + lane;  // loading: lane -> column
+  const bool jok = j < H4;
+  auto code = [&](uint8_t v) { return SIGNED ? (int)(int8_t)v : (int)v; };
+  const int z = (jok && zp) ? code(zp[n_zp == 1 ? 0 : j]) : 0;
+  int part = 0;
+  for (int64_t k0 = 0; k0 < Kp; k0 += 64) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int kk = warp + 8 * r;
+      const int64_t k = k0 + kk;
+      const int v = (jok && k < K) ? code(W[k * H4 + j]) - z : 0;
+      part += v;
+      tile[lane][kk] = (int16_t)v;
+    }
+    __syncthreads();
+    // write: thread -> column c (of 32), 16-byte chunk ch (of 8)
+    const int c = t >> 3, ch = t & 7;
+    const int64_t jj = j0 + c;
+    if (jj < H4) {
+      const int64_t row = 4 * (jj % H) + jj / H;
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float f0 = (float)tile[c][ch * 8 + 2 * e], f1 = (float)tile[c][ch * 8 + 2 * e + 1];
+        w[e] = (__float_as_uint(f0) >> 16) | (__float_as_uint(f1) & 0xffff0000u);
+      }
+      *reinterpret_cast<uint4*>(out + row * Kp + k0 + ch * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+  }
+  sums[warp][lane] = part;
+  __syncthreads();
+  if (warp == 0 && jok) {
+    int total = 0;
+    for (int w8 = 0; w8 < 8; ++w8) total += sums[w8][lane];
+    colsum[4 * (j % H) + j / H] = total;
+  }
+}
+
 __device__ __forceinline__ float sigmoid_f32(float x) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x))); }
 
 // ---- the fused step ------------------------------------------------------------
@@ -320,9 +375,22 @@ struct TcStepParams {
   float* Y;            // [T, D, B, H] or null
   int step, T, B, H, Hp, D, direction, CS;
   uint32_t* status;
+  // variants (the VAR instantiation)
+  const float* h_prev;       // [D, B, H]: carried when a row's sequence has ended
+  const int32_t* seq_lens;   // [B] or null (every row has length T)
+  const float* P;            // [D, 3H] peepholes (i, o, f) or null
+  float clip;                // > 0: gate inputs bounded to [-clip, clip]
+  int input_forget;          // f = 1 - i
 };
 
-// grid (ceil(4H/128), D, ceil(B/64))
+__device__ __forceinline__ float clip_gate(float v, float clip) {
+  return clip > 0.0f ? fminf(fmaxf(v, -clip), clip) : v;
+}
+
+// grid (ceil(4H/128), D, ceil(B/64)).  VAR adds sequence lengths,
+// peepholes, clip and coupled gates: the output gate is then formed after
+// the new cell state (its peephole reads it).
+template <bool VAR>
 __global__ void __launch_bounds__(THREADS, 1)
 lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmH, TcStepParams p) {
   constexpr uint32_t IDESC = idesc_bf16(BM, BN);
@@ -410,14 +478,25 @@ lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
     const int q = n & 3, u = n >> 2;
     const int b0 = nb * BN + half * HALF;
     // operands of the epilogue that do not depend on the product: fetched
-    // while the tensor core works
+    // while the tensor core works.  A row whose sequence has ended (VAR,
+    // step >= its length) is inactive; the reverse direction of a row of
+    // length L walks t = L-1 .. 0.
     float gx[HALF], cprev[HALF];
+    uint32_t active = 0;
 #pragma unroll
     for (int j = 0; j < HALF; ++j) {
       const int b = b0 + j;
       const bool ok_b = b < p.B && nvalid;
-      gx[j] = ok_b ? __ldg(p.Gx + ((int64_t)d * TB + (int64_t)t * p.B + b) * H4 + n) : 0.0f;
-      cprev[j] = (ok_b && q == 0 && u < p.H) ? p.c[((int64_t)d * p.B + b) * p.H + u] : 0.0f;
+      int tb = t;
+      bool act_b = ok_b;
+      if (VAR && ok_b && p.seq_lens) {
+        const int L = min(max(__ldg(p.seq_lens + b), 0), p.T);  // lengths outside [0, T] are clamped
+        act_b = p.step < L;
+        tb = rev ? L - 1 - p.step : p.step;
+      }
+      active |= (act_b ? 1u : 0u) << j;
+      gx[j] = act_b ? __ldg(p.Gx + ((int64_t)d * TB + (int64_t)tb * p.B + b) * H4 + n) : 0.0f;
+      cprev[j] = (ok_b && (VAR || q == 0) && u < p.H) ? p.c[((int64_t)d * p.B + b) * p.H + u] : 0.0f;
     }
     int32_t run[HALF];
 #pragma unroll
@@ -443,7 +522,66 @@ lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(acce);
     }
-    if (ok) {
+    if (ok && VAR) {
+      const int64_t dn = (int64_t)d * H4 + (nvalid ? n : 0);
+      const int32_t cs = nvalid ? __ldg(p.Rcs + dn) : 0;
+      const float rsc = nvalid ? __ldg(p.Rsc + dn) : 0.0f;
+      const float wb = nvalid ? __ldg(p.Wbi + dn) : 0.0f;
+      const float rb = nvalid ? __ldg(p.Rbi + dn) : 0.0f;
+      // this lane's peephole weight: P[d] holds Pi, Po, Pf (H each)
+      const int pq = q == 0 ? 0 : (q == 1 ? 1 : 2);
+      const float pw = (p.P && nvalid && q < 3 && u < p.H) ? __ldg(p.P + (int64_t)d * 3 * p.H + pq * p.H + u) : 0.0f;
+      const int base_lane = lane & ~3;
+#pragma unroll
+      for (int j = 0; j < HALF; ++j) {
+        const int b = b0 + j;
+        const bool live = (active >> j) & 1u;
+        // phase 1: i, f, c~ (the o lane keeps its partial sum)
+        float sum = 0.0f, act = 0.0f;
+        if (live) {
+          const float sH = __ldg(p.sh + d * p.B + b);
+          const int32_t v = run[j] - (__ldg(p.zh + d * p.B + b) - 128) * cs;
+          float gh = __fmul_rn(__int2float_rn(v), sH);
+          gh = __fmul_rn(gh, rsc);
+          sum = __fadd_rn(gx[j], gh);
+          if (p.P && (q == 0 || q == 2)) sum = __fadd_rn(sum, __fmul_rn(pw, cprev[j]));
+          if (q != 1) {
+            float gg = __fadd_rn(__fadd_rn(sum, wb), rb);
+            gg = clip_gate(gg, p.clip);
+            act = q == 3 ? tanhf(gg) : sigmoid_f32(gg);
+          }
+        }
+        const float ig = __shfl_sync(0xffffffffu, act, base_lane + 0);
+        const float fg0 = __shfl_sync(0xffffffffu, act, base_lane + 2);
+        const float ct = __shfl_sync(0xffffffffu, act, base_lane + 3);
+        const float fg = p.input_forget ? __fsub_rn(1.0f, ig) : fg0;
+        const float cn = __fadd_rn(__fmul_rn(fg, cprev[j]), __fmul_rn(ig, ct));  // meaningful on live rows
+        // phase 2: o from the new cell state
+        float og = 0.0f;
+        if (live && q == 1) {
+          float so = sum;
+          if (p.P) so = __fadd_rn(so, __fmul_rn(pw, cn));
+          so = __fadd_rn(__fadd_rn(so, wb), rb);
+          og = sigmoid_f32(clip_gate(so, p.clip));
+        }
+        og = __shfl_sync(0xffffffffu, og, base_lane + 1);
+        if (q == 0 && b < p.B && nvalid && u < p.H) {
+          const int64_t e = ((int64_t)d * p.B + b) * p.H + u;
+          if (live) {
+            const float hn = __fmul_rn(og, tanhf(cn));
+            p.c[e] = cn;
+            p.h_next[e] = hn;
+            if (p.Y) {
+              const int tb = p.seq_lens ? (rev ? min(max(__ldg(p.seq_lens + b), 0), p.T) - 1 - p.step : p.step) : t;
+              p.Y[(((int64_t)tb * p.D + d) * p.B + b) * p.H + u] = hn;
+            }
+          } else {
+            p.h_next[e] = p.h_prev[e];  // the row's state is carried
+          }
+        }
+      }
+    }
+    if (ok && !VAR) {
       const int64_t dn = (int64_t)d * H4 + (nvalid ? n : 0);
       const int32_t cs = nvalid ? __ldg(p.Rcs + dn) : 0;
       const float rsc = nvalid ? __ldg(p.Rsc + dn) : 0.0f;
@@ -507,7 +645,8 @@ bool lstm_use_tc(int64_t rows, int64_t cols) {
 // so the struct has no padding and compares with memcmp).
 struct LstmGraphKey {
   const void *X, *W, *R, *W_scale, *R_scale, *Bias, *h0, *c0, *Y, *Y_h, *Y_c, *workspace;
-  int64_t T, batch, input, hidden, direction, n_wscale, n_rscale;
+  const void *W_zero_point, *R_zero_point, *seq_lens, *P;
+  int64_t T, batch, input, hidden, direction, n_wscale, n_rscale, wtype, input_forget, clip_bits;
 };
 
 // Launch the recurrence as a CUDA graph on s: the cached one when key
@@ -524,12 +663,20 @@ extern "C" size_t i8q_dq_lstm_workspace_size(int64_t T, int64_t batch, int64_t i
   return lstm_layout(T, batch, input, hidden, direction).total;
 }
 
-extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int64_t input, int64_t hidden,
-                                   int direction, const int8_t* W, const float* W_scale, const int8_t* W_zero_point,
-                                   size_t n_wscale, const int8_t* R, const float* R_scale,
-                                   const int8_t* R_zero_point, size_t n_rscale, const float* Bias, const float* h0,
-                                   const float* c0, float* Y, float* Y_h, float* Y_c, void* workspace,
-                                   size_t ws_bytes, void* stream) {
+namespace {
+
+int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, int64_t hidden, int direction,
+                      const void* W_, const void* R_, int wtype, const float* W_scale, const void* W_zero_point_,
+                      size_t n_wscale, const float* R_scale, const void* R_zero_point_, size_t n_rscale,
+                      const float* Bias, const int32_t* seq_lens, const float* h0, const float* c0, const float* P,
+                      float clip, int input_forget, float* Y, float* Y_h, float* Y_c, void* workspace,
+                      size_t ws_bytes, void* stream) {
+  const int8_t* W = static_cast<const int8_t*>(W_);
+  const int8_t* R = static_cast<const int8_t*>(R_);
+  const int8_t* W_zero_point = static_cast<const int8_t*>(W_zero_point_);
+  const int8_t* R_zero_point = static_cast<const int8_t*>(R_zero_point_);
+  if (wtype != I8Q_S8 && wtype != I8Q_U8) return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: W and R must be I8Q_S8 or I8Q_U8");
+  if (!(clip == clip)) return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: clip is NaN");
   if (T <= 0 || batch <= 0 || input <= 0 || hidden <= 0)
     return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: T, batch, input, hidden must be positive");
   if (direction < I8Q_LSTM_FORWARD || direction > I8Q_LSTM_BIDIRECTIONAL)
@@ -569,9 +716,14 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
   float* cbuf = (float*)(ws + L.off_c);
   const int64_t H = hidden, BH = batch * hidden, DBH = L.D * BH;
 
-  // Zero points must be zero (the only form this engine runs).  Checked on
-  // the device, reported synchronously.
-  if (W_zero_point || R_zero_point) {
+  // The general form (uint8 weights, zero points, sequence lengths,
+  // peepholes, clip, coupled gates) runs on the tensor-core kernels: the
+  // weights enter as bf16 W - zp (|W - zp| <= 255), so products stay within
+  // 2^15 and the exact fp32 chunks hold 512 K-elements.  int8 weights whose
+  // given zero points are all 0 (checked on the device, reported
+  // synchronously) keep the plain form.
+  bool var = wtype != I8Q_S8 || seq_lens || P || clip > 0.0f || input_forget;
+  if (!var && (W_zero_point || R_zero_point)) {
     int* flag = reinterpret_cast<int*>(sh);  // scratch word, overwritten later
     I8Q_CUDA_TRY(cudaMemsetAsync(flag, 0, sizeof(int), s));
     if (W_zero_point) any_nonzero_s8<<<grid_for((int64_t)n_wscale), 256, 0, s>>>(W_zero_point, (int64_t)n_wscale, flag);
@@ -579,17 +731,40 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
     int hflag = 0;
     I8Q_CUDA_TRY(cudaMemcpyAsync(&hflag, flag, sizeof(int), cudaMemcpyDeviceToHost, s));
     I8Q_CUDA_TRY(cudaStreamSynchronize(s));
-    if (hflag) return fail(I8Q_ERR_UNSUPPORTED, "dq_lstm: nonzero W/R zero points are not supported");
+    var = hflag != 0;
   }
 
   // weights: gate-interleaved K-major copies, column sums, scales, biases
-  const bool tc = lstm_use_tc(L.TB, L.H4);
+  const bool tc = var || lstm_use_tc(L.TB, L.H4);
   // recurrent product on the tensor pipe when the step has enough gate
   // rows to spread (or when forced); exact chunks need |uh - 128| * |R| <= 2^14
   const char* force = getenv("I8Q_FORCE_CORE");
-  const bool step_tc = force ? std::string(force) == "tc" : (L.H4 >= 1024);
+  const bool step_tc = var || (force ? std::string(force) == "tc" : (L.H4 >= 1024));
+  const int prod_log2 = var ? 15 : 14;
   int rc;
   for (int64_t d = 0; d < L.D; ++d) {
+    if (var) {
+      const auto* zw = reinterpret_cast<const uint8_t*>(W_zero_point);
+      const auto* zr = reinterpret_cast<const uint8_t*>(R_zero_point);
+      const int64_t nzw = (int64_t)n_wscale == L.D ? 1 : L.H4, nzr = (int64_t)n_rscale == L.D ? 1 : L.H4;
+      const auto* Wd = reinterpret_cast<const uint8_t*>(W) + d * input * L.H4;
+      const auto* Rd = reinterpret_cast<const uint8_t*>(R) + d * H * L.H4;
+      const unsigned blocks = (unsigned)ceil_div(L.H4, 32);
+      I8Q_PROF("repack_cols", s);
+      if (wtype == I8Q_S8) {
+        repack_gates_zp<true><<<blocks, 256, 0, s>>>(Wd, input, H, zw ? zw + d * nzw : nullptr, nzw, L.Ip,
+                                                     Wtb + d * L.H4 * L.Ip, Wcs + d * L.H4);
+        repack_gates_zp<true><<<blocks, 256, 0, s>>>(Rd, H, H, zr ? zr + d * nzr : nullptr, nzr, L.Hp,
+                                                     Rtb + d * L.H4 * L.Hp, Rcs + d * L.H4);
+      } else {
+        repack_gates_zp<false><<<blocks, 256, 0, s>>>(Wd, input, H, zw ? zw + d * nzw : nullptr, nzw, L.Ip,
+                                                      Wtb + d * L.H4 * L.Ip, Wcs + d * L.H4);
+        repack_gates_zp<false><<<blocks, 256, 0, s>>>(Rd, H, H, zr ? zr + d * nzr : nullptr, nzr, L.Hp,
+                                                      Rtb + d * L.H4 * L.Hp, Rcs + d * L.H4);
+      }
+      I8Q_LAUNCH_CHECK("repack_gates_zp");
+      continue;
+    }
     rc = launch_repack_cols_s8_gates(W + d * input * L.H4, input, L.H4, L.H4, Wt + d * L.H4 * L.Ip,
                                      tc ? Wtb + d * L.H4 * L.Ip : nullptr, L.Ip, Wcs + d * L.H4, H, s);
     if (rc) return rc;
@@ -609,8 +784,9 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
     GemmEpilogue ep{zX, sX, Wcs + d * L.H4, Wsc + d * L.H4, nullptr, I8Q_ACT_IDENTITY, OUT_F32,
                     Gx + d * L.TB * L.H4, L.H4};
     rc = I8Q_ERR_UNSUPPORTED;
-    if (tc) rc = launch_gemm_tc(uXc, Wtb + d * L.H4 * L.Ip, L.TB, L.H4, L.Ip, 14, ep, s);
-    if (rc == I8Q_ERR_UNSUPPORTED) rc = launch_gemm_imma(uX, Wt + d * L.H4 * L.Ip, L.TB, L.H4, L.Ip, ep, s);
+    if (tc) rc = launch_gemm_tc(uXc, Wtb + d * L.H4 * L.Ip, L.TB, L.H4, L.Ip, prod_log2, ep, s);
+    if (rc == I8Q_ERR_UNSUPPORTED && !var)
+      rc = launch_gemm_imma(uX, Wt + d * L.H4 * L.Ip, L.TB, L.H4, L.Ip, ep, s);
     if (rc) return rc;
   }
 
@@ -624,8 +800,11 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-      attr_err = cudaFuncSetAttribute(tcs::lstm_step_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      attr_err = cudaFuncSetAttribute(tcs::lstm_step_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       tcs::SMEM_BYTES);
+      if (attr_err == cudaSuccess)
+        attr_err = cudaFuncSetAttribute(tcs::lstm_step_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        tcs::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(lstm_step_tc_kernel)");
   }
@@ -634,6 +813,8 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
   auto recurrence = [&]() -> int {
     init_state<<<grid_for(DBH), 256, 0, s>>>(h0, c0, DBH, hbuf, cbuf);
     I8Q_LAUNCH_CHECK("init_state");
+    // rows whose sequence ends early leave the rest of Y zero
+    if (Y && seq_lens) I8Q_CUDA_TRY(cudaMemsetAsync(Y, 0, (size_t)T * DBH * sizeof(float), s));
     int rc2 = launch_quantize_rows(hbuf, I8Q_F32, L.D * batch, H, H, uh, step_tc ? uhc : nullptr, L.Hp, sh, zh, s);
     if (rc2) return rc2;
     StepParams sp;
@@ -672,7 +853,11 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
     tp.Hp = (int)L.Hp;
     tp.D = (int)L.D;
     tp.direction = direction;
-    tp.CS = 16;  // 1024 K-elements per exact fp32 chunk
+    tp.CS = (int)((((int64_t)1 << 24) >> prod_log2) / tcs::BK);  // exact fp32 chunk: 1024 (512) K-elements
+    tp.seq_lens = seq_lens;
+    tp.P = P;
+    tp.clip = clip;
+    tp.input_forget = input_forget ? 1 : 0;
     tp.status = device_status_word();
     if (step_tc && !tp.status) return fail(I8Q_ERR_CUDA, "dq_lstm: no device status word");
     for (int64_t step = 0; step < T; ++step) {
@@ -683,7 +868,11 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
         I8Q_PROF("lstm_step_tc", s);
         tp.step = (int)step;
         tp.h_next = h_next;
-        tcs::lstm_step_tc_kernel<<<tgrid, tcs::THREADS, tcs::SMEM_BYTES, s>>>(mR, mH, tp);
+        tp.h_prev = hbuf + (step & 1) * DBH;
+        if (var)
+          tcs::lstm_step_tc_kernel<true><<<tgrid, tcs::THREADS, tcs::SMEM_BYTES, s>>>(mR, mH, tp);
+        else
+          tcs::lstm_step_tc_kernel<false><<<tgrid, tcs::THREADS, tcs::SMEM_BYTES, s>>>(mR, mH, tp);
         I8Q_LAUNCH_CHECK("lstm_step_tc_kernel");
       } else {
         I8Q_PROF("lstm_step", s);
@@ -710,9 +899,37 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   I8Q_CUDA_TRY(cudaStreamIsCapturing(s, &cap));
   if (s == nullptr || cap != cudaStreamCaptureStatusNone || profiling_enabled() || T < 4) return recurrence();
-  const LstmGraphKey key{X, W, R, W_scale, R_scale, Bias, h0, c0, Y, Y_h, Y_c, workspace, T, batch, input, hidden,
-                         direction, (int64_t)n_wscale, (int64_t)n_rscale};
+  int64_t clip_bits = 0;
+  std::memcpy(&clip_bits, &clip, sizeof(float));
+  const LstmGraphKey key{X, W, R, W_scale, R_scale, Bias, h0, c0, Y, Y_h, Y_c, workspace, W_zero_point, R_zero_point,
+                         seq_lens, P, T, batch, input, hidden, direction, (int64_t)n_wscale, (int64_t)n_rscale,
+                         (int64_t)wtype, (int64_t)(input_forget ? 1 : 0), clip_bits};
   return run_cached_graph(key, s, recurrence);
+}
+
+}  // namespace
+
+extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int64_t input, int64_t hidden,
+                                   int direction, const int8_t* W, const float* W_scale, const int8_t* W_zero_point,
+                                   size_t n_wscale, const int8_t* R, const float* R_scale,
+                                   const int8_t* R_zero_point, size_t n_rscale, const float* Bias, const float* h0,
+                                   const float* c0, float* Y, float* Y_h, float* Y_c, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+  return lstm_forward_impl(X, T, batch, input, hidden, direction, W, R, I8Q_S8, W_scale, W_zero_point, n_wscale,
+                           R_scale, R_zero_point, n_rscale, Bias, nullptr, h0, c0, nullptr, 0.0f, 0, Y, Y_h, Y_c,
+                           workspace, ws_bytes, stream);
+}
+
+extern "C" int i8q_dq_lstm_forward_ex(const float* X, int64_t T, int64_t batch, int64_t input, int64_t hidden,
+                                      int direction, const void* W, const void* R, int wtype, const float* W_scale,
+                                      const void* W_zero_point, size_t n_wscale, const float* R_scale,
+                                      const void* R_zero_point, size_t n_rscale, const float* Bias,
+                                      const int32_t* sequence_lens, const float* h0, const float* c0, const float* P,
+                                      float clip, int input_forget, float* Y, float* Y_h, float* Y_c,
+                                      void* workspace, size_t ws_bytes, void* stream) {
+  return lstm_forward_impl(X, T, batch, input, hidden, direction, W, R, wtype, W_scale, W_zero_point, n_wscale,
+                           R_scale, R_zero_point, n_rscale, Bias, sequence_lens, h0, c0, P, clip, input_forget, Y,
+                           Y_h, Y_c, workspace, ws_bytes, stream);
 }
 
 namespace i8q {

@@ -95,15 +95,22 @@ def test_short_sequence(orc, dev, direction, per_channel):
     np.testing.assert_allclose(Yc, ref[2], rtol=1e-4, atol=1e-5)
 
 
-def test_nonzero_zero_point_rejected(dev):
-    w = workloads.lstm(seed=4, T=2, batch=2, I=16, H=8, D=1)
-    ws = torch.empty(q.dq_lstm_workspace_size(2, 2, 16, 8, q.LSTM_FORWARD), dtype=torch.uint8, device=dev)
-    zp = np.zeros(32, np.int8)
-    zp[3] = 1
-    with pytest.raises(q.I8QError) as e:
-        q.dq_lstm_forward(_t(w["X"], dev), _t(w["W"], dev), _t(w["R"], dev), _t(w["W_scale"], dev),
-                          _t(w["R_scale"], dev), ws, W_zero_point=_t(zp, dev))
-    assert e.value.code == q._lib.ERR_UNSUPPORTED
+def test_nonzero_zero_point(orc, dev):
+    """int8 W, R with nonzero per-channel zero points through the plain
+    entry point (they run on the general tensor-core path)."""
+    w = workloads.lstm(seed=4, T=3, batch=2, I=16, H=8, D=1)
+    ws = torch.empty(q.dq_lstm_workspace_size(3, 2, 16, 8, q.LSTM_FORWARD), dtype=torch.uint8, device=dev)
+    zp = np.zeros((1, 32), np.int8)
+    zp[0, 3] = 1
+    zp[0, 17] = -5
+    Y = torch.empty(3, 1, 2, 8, device=dev)
+    q.dq_lstm_forward(_t(w["X"], dev), _t(w["W"], dev), _t(w["R"], dev), _t(w["W_scale"], dev),
+                      _t(w["R_scale"], dev), ws, B=_t(w["B"], dev), Y=Y, W_zero_point=_t(zp, dev),
+                      R_zero_point=_t(zp, dev))
+    q.sync_status()
+    ref = orc.dynamic_quantize_lstm(w["X"], w["W"], w["R"], w["B"], w["W_scale"], w["R_scale"],
+                                    W_zero_point=zp.astype(np.int32), R_zero_point=zp.astype(np.int32))
+    np.testing.assert_allclose(Y.cpu().numpy(), ref[0], rtol=1e-4, atol=1e-5)
 
 
 def test_full_size_sampled_steps(orc, dev):
