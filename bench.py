@@ -43,8 +43,8 @@ WORKLOAD = ("dynamic quantized GEMM M=8192 K=4096 N=14336: bf16 A quantized per 
 NCU_TRAFFIC = {
     "gemm_tc_pair": {"sources": ["int8_quantized_gb300/csrc/gemm_tc.cu", "int8_quantized_gb300/csrc/tcgen05.cuh",
                                  "int8_quantized_gb300/csrc/common.cuh"],
-                     "sha256": "b72ea7efab4779035cf8bfc9c5f43571eabbf8baaf1343a977a74386804bab7e",
-                     "bytes": (592.50 + 231.21) * 1e6,
+                     "sha256": "183baa2615f014a7dd3047b4b94eec8548de3fd9ed300be21001df25e58f06c3",
+                     "bytes": (577.92 + 224.25) * 1e6,
                      "profile": "profiles/gemm_tc_pair_large_gemm.md"},
 }
 
