@@ -16,7 +16,7 @@
 // copies for the tensor-core path (B's codes as they are, A's shifted to
 // uA - 128 so every product stays within 2^14 in magnitude), and the column
 // sums of iB used by the zero-point correction  -zeroA[i] * colsum[j].
-#include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace i8q {
 namespace {
@@ -242,6 +242,162 @@ quantize_rows_warp(const T* __restrict__ A, int64_t M, int64_t K, int64_t lda, u
       *reinterpret_cast<uint4*>(ub + k) = o;
     }
   }
+}
+
+// Rows staged in shared memory: a persistent CTA of 32 warps takes groups of
+// 8 rows; one thread copies each group into shared memory with bulk copies
+// (one per row, double-buffered, the next group in flight while this one is
+// processed), then 4 warps share each row: a min/max pass (combined through
+// shared memory) and a quantization pass over shared memory, 8 elements per
+// lane and step, with coalesced stores of the codes and of their bf16 copy
+// (uA - 128).  The
+// arithmetic is that of quantize_rows_warp.  Needs K % 8 == 0, 16-byte
+// aligned rows, and 2 * 8 rows in shared memory.
+constexpr int kStageRows = 8;
+constexpr int kWarpsPerRow = 4;  // 32 warps per CTA: enough to hide the quantization's latencies
+constexpr int kStageThreads = 32 * kStageRows * kWarpsPerRow;
+constexpr uint32_t ST_TIMEOUT_ROWS = 1u << 12;
+
+template <typename T>
+__global__ void __launch_bounds__(kStageThreads, 1)
+quantize_rows_staged(const T* __restrict__ A, int64_t M, int64_t K, int64_t lda, uint8_t* __restrict__ uA,
+                     __nv_bfloat16* __restrict__ uA_bf16, int64_t Kp, float* __restrict__ scaleA,
+                     int32_t* __restrict__ zeroA, uint32_t* status) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const uint32_t row_bytes = (uint32_t)(K * sizeof(T));
+  const uint32_t group_bytes = kStageRows * row_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 2 * (size_t)group_bytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2);
+  __shared__ float red[kStageRows][kWarpsPerRow][2];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rw = warp / kWarpsPerRow, part = warp % kWarpsPerRow;  // row of the group, quarter of the work
+  const int64_t groups = (M + kStageRows - 1) / kStageRows;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(tc::smem_u32(bars), 1);
+    tc::mbar_init(tc::smem_u32(bars + 1), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  auto issue = [&](int64_t g, int b) {
+    const int64_t r0 = g * kStageRows;
+    const int rows = (int)(M - r0 < kStageRows ? M - r0 : kStageRows);
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    tc::mbar_arrive_expect_tx(tc::smem_u32(bars + b), (uint32_t)rows * row_bytes);
+    for (int r = 0; r < rows; ++r)
+      tc::bulk_load(tc::smem_u32(sm + (size_t)b * group_bytes + (size_t)r * row_bytes), A + (r0 + r) * lda, row_bytes,
+                    tc::smem_u32(bars + b));
+  };
+  int64_t g = blockIdx.x;
+  int issued = 0, waited = 0;  // groups copied / consumed (thread 0 issues)
+  if (threadIdx.x == 0 && g < groups) {
+    issue(g, 0);
+    issued = 1;
+  }
+  const int nunits = (int)(K / 8);  // 8-element units of a row
+  for (int it = 0; g < groups; g += gridDim.x, ++it) {
+    const int b = it & 1;
+    const int64_t gn = g + gridDim.x;
+    if (threadIdx.x == 0 && gn < groups) {
+      issue(gn, b ^ 1);
+      ++issued;
+    }
+    if (!tc::wait_bar(tc::smem_u32(bars + b), (uint32_t)(it >> 1) & 1u, abort_flag, status, ST_TIMEOUT_ROWS)) break;
+    ++waited;
+    const int64_t row = g * kStageRows + rw;
+    const bool live = row < M;
+    {
+      const uint8_t* base = sm + (size_t)b * group_bytes + (size_t)rw * row_bytes;
+      auto unit = [&](int c, float (&v)[8]) {
+        if (sizeof(T) == 2) {
+          const uint4 w = *reinterpret_cast<const uint4*>(base + (size_t)c * 16);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            v[2 * q] = __uint_as_float(ws[q] << 16);
+            v[2 * q + 1] = __uint_as_float(ws[q] & 0xffff0000u);
+          }
+        } else {
+          const float4 x0 = *reinterpret_cast<const float4*>(base + (size_t)c * 32);
+          const float4 x1 = *reinterpret_cast<const float4*>(base + (size_t)c * 32 + 16);
+          v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+          v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+        }
+      };
+      float mn = 0.0f, mx = 0.0f;
+      if (live) {
+#pragma unroll 4
+        for (int c = part * 32 + lane; c < nunits; c += 32 * kWarpsPerRow) {
+          float v[8];
+          unit(c, v);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            mn = fminf(mn, v[e]);
+            mx = fmaxf(mx, v[e]);
+          }
+        }
+      }
+      mn = warp_min(mn);
+      mx = warp_max(mx);
+      if (lane == 0) {
+        red[rw][part][0] = mn;
+        red[rw][part][1] = mx;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int w2 = 0; w2 < kWarpsPerRow; ++w2) {
+        mn = fminf(mn, red[rw][w2][0]);
+        mx = fmaxf(mx, red[rw][w2][1]);
+      }
+      float sc = __fdiv_rn(__fsub_rn(mx, mn), 255.0f);
+      int z = 0;
+      if (sc == 0.0f) {
+        sc = 1.0f;
+      } else {
+        z = sat_rint(__fdiv_rn(-mn, sc), 0.0f, 255.0f);
+      }
+      if (live && part == 0 && lane == 0) {
+        scaleA[row] = sc;
+        zeroA[row] = z;
+      }
+      const float lo_z = (float)(-z), hi_z = (float)(255 - z);
+      const float shift = (float)(z - 128) - 12582912.0f;  // takes rint + 1.5*2^23 to uA - 128
+      uint8_t* u = uA + (live ? row : 0) * Kp;
+      __nv_bfloat16* ub = uA_bf16 ? uA_bf16 + (live ? row : 0) * Kp : nullptr;
+#pragma unroll 2
+      for (int c = part * 32 + lane; live && c < nunits; c += 32 * kWarpsPerRow) {
+        float v[8];
+        unit(c, v);
+        uint32_t code[8], cb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float t = fminf(fmaxf(__fdiv_rn(v[e], sc), lo_z), hi_z);
+          const float r = __fadd_rn(t, 12582912.0f);
+          code[e] = (uint32_t)(__float_as_int(r) + z);
+          cb[e] = __float_as_uint(__fadd_rn(r, shift)) >> 16;
+        }
+        *reinterpret_cast<uint2*>(u + (size_t)c * 8) = make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]),
+                                                                   pack_low_bytes(code[4], code[5], code[6], code[7]));
+        if (ub)
+          *reinterpret_cast<uint4*>(ub + (size_t)c * 8) = make_uint4(cb[0] | (cb[1] << 16), cb[2] | (cb[3] << 16),
+                                                                     cb[4] | (cb[5] << 16), cb[6] | (cb[7] << 16));
+      }
+      // zero padding K .. Kp
+      for (int c = nunits + part * 32 + lane; live && c < (int)(Kp / 8); c += 32 * kWarpsPerRow) {
+        *reinterpret_cast<uint2*>(u + (size_t)c * 8) = make_uint2(0u, 0u);
+        if (ub) *reinterpret_cast<uint4*>(ub + (size_t)c * 8) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    __syncthreads();  // the buffer is free for the group after next
+  }
+  // after a timeout: let the copies this CTA still has in flight land
+  // (bounded) before it exits
+  if (threadIdx.x == 0)
+    for (int j = waited; j < issued; ++j) {
+      const unsigned long long t0 = tc::global_ns();
+      while (!tc::mbar_try_wait(tc::smem_u32(bars + (j & 1)), (uint32_t)(j >> 1) & 1u))
+        if (tc::global_ns() - t0 > tc::WAIT_LIMIT_NS) break;
+    }
 }
 
 // ---- columns -------------------------------------------------------------
@@ -477,6 +633,36 @@ int launch_quantize_rows(const void* A, int typeA, int64_t M, int64_t K, int64_t
   if (M <= 0) return I8Q_OK;
   int64_t blocks = std::min<int64_t>(M, (int64_t)sm_count() * 8);
   I8Q_PROF("quantize_rows", s);
+  // rows staged in shared memory, when they fit
+  {
+    const bool bf = typeA == I8Q_BF16;
+    const int64_t esz = bf ? 2 : 4;
+    const size_t smem = 2 * (size_t)kStageRows * (size_t)(K * esz) + 64;
+    const bool aligned = aligned16(A) && K % 8 == 0 && (lda * esz) % 16 == 0;
+    uint32_t* status = device_status_word();
+    const int64_t groups = ceil_div(M, kStageRows);
+    // worth it once the row groups fill the GPU; fewer rows keep the
+    // register form (lower latency per launch)
+    if (aligned && status && smem <= 200 * 1024 && groups >= sm_count() && !getenv("I8Q_ROWS_REGISTER")) {
+      const int per_sm = (int)std::max<size_t>(1, (200 * 1024) / smem);
+      const int grid = (int)std::min<int64_t>(groups, (int64_t)sm_count() * per_sm);
+      static bool attr_done[2] = {false, false};
+      if (!attr_done[bf]) {
+        I8Q_CUDA_TRY(cudaFuncSetAttribute(bf ? (const void*)quantize_rows_staged<__nv_bfloat16>
+                                             : (const void*)quantize_rows_staged<float>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024 + 64));
+        attr_done[bf] = true;
+      }
+      if (bf)
+        quantize_rows_staged<__nv_bfloat16><<<grid, kStageThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(A), M, K, lda,
+                                                                    uA, uA_bf16, Kp, scaleA, zeroA, status);
+      else
+        quantize_rows_staged<float><<<grid, kStageThreads, smem, s>>>(static_cast<const float*>(A), M, K, lda, uA, uA_bf16, Kp,
+                                                            scaleA, zeroA, status);
+      I8Q_LAUNCH_CHECK("quantize_rows_staged");
+      return I8Q_OK;
+    }
+  }
   // warp per row with the row in registers, when it fits
   {
     const bool bf = typeA == I8Q_BF16;
