@@ -170,6 +170,108 @@ qlinearconv_depthwise_halo(const XT* __restrict__ x, const WT* __restrict__ w, c
     }
 }
 
+// Depthwise KS x KS, stride 1, dilation 1: one CTA of 128 threads per
+// (image, channel) plane.  The plane sits in shared memory as centred
+// values (x - x_zero_point, held as fp32) with a zero halo, rows padded to a
+// multiple of 4 words; each thread computes strips of 8 consecutive outputs
+// of a row from a window loaded with 16-byte shared-memory reads, and
+// writes them as one 8-byte store.  The taps accumulate in fp32 with FMAs:
+// every product (|v w| <= 255^2) and every partial sum (<= 25 * 255^2 <
+// 2^24) is an integer exactly representable, so the sum is the exact int32
+// one; the bias is then added in int32.
+constexpr int kStrip = 8;
+template <typename XT, typename WT, typename YT, int KS>
+__global__ void __launch_bounds__(128)
+qlinearconv_depthwise_strip(const XT* __restrict__ x, const WT* __restrict__ w, const float* __restrict__ w_scale,
+                            const WT* __restrict__ w_zp, int per_channel, const int32_t* __restrict__ B, int C, int H,
+                            int W, int OH, int OW, int pt, int pl, float x_scale, int x_zp, float y_scale, int y_zp,
+                            float qlo, float qhi, YT* __restrict__ y) {
+  extern __shared__ __align__(16) float plf[];
+  const int c = blockIdx.x % C, n = blockIdx.x / C;
+  const int nstrips = (OW + kStrip - 1) / kStrip;
+  const int HP = OH + KS - 1, WPs = (nstrips * kStrip + KS - 1 + 3) & ~3;  // shared plane: HP x WPs
+  const XT* xp = x + ((int64_t)n * C + c) * H * W;
+  // shared (r, col) holds x(r - pt, col - pl) - x_zp, 0 outside the input:
+  // zero the padded plane, then scatter the plane's codes into it, read in
+  // one burst of 16-byte loads when aligned (one or two per thread)
+  for (int i = threadIdx.x; i < HP * WPs / 4; i += blockDim.x)
+    reinterpret_cast<float4*>(plf)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  __syncthreads();
+  const int HW = H * W;
+  if ((reinterpret_cast<uintptr_t>(xp) & 15) == 0 && (HW & 15) == 0) {
+    for (int v16 = threadIdx.x; v16 < HW / 16; v16 += blockDim.x) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(xp) + v16);
+      const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+      int r = (16 * v16) / W, col = 16 * v16 - r * W;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        plf[(r + pt) * WPs + col + pl] = (float)((int)(XT)((wd[e >> 2] >> (8 * (e & 3))) & 0xffu) - x_zp);
+        if (++col == W) {
+          col = 0;
+          ++r;
+        }
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < HW; i += blockDim.x) {
+      const int r = i / W, col = i - r * W;
+      plf[(r + pt) * WPs + col + pl] = (float)((int)xp[i] - x_zp);
+    }
+  }
+  const int wz = (int)w_zp[per_channel ? c : 0];
+  float wc[KS * KS];
+#pragma unroll
+  for (int t = 0; t < KS * KS; ++t) wc[t] = (float)((int)w[(int64_t)c * KS * KS + t] - wz);
+  const int32_t bc = B ? B[c] : 0;
+  const float mul = __fmul_rn(x_scale, w_scale[per_channel ? c : 0]);
+  const float lo_z = qlo - (float)y_zp, hi_z = qhi - (float)y_zp;
+  __syncthreads();
+  YT* yp = y + ((int64_t)n * C + c) * OH * OW;
+  const bool vec_rows = (OW % kStrip) == 0 && (reinterpret_cast<uintptr_t>(y) & 7) == 0;
+  constexpr int NV = (kStrip + KS - 1 + 3) & ~3;  // window words, whole 16-byte reads
+  for (int sidx = threadIdx.x; sidx < OH * nstrips; sidx += blockDim.x) {
+    const int oh = sidx / nstrips, ow0 = (sidx - oh * nstrips) * kStrip;
+    float acc[kStrip];
+#pragma unroll
+    for (int e = 0; e < kStrip; ++e) acc[e] = 0.0f;
+#pragma unroll
+    for (int kh = 0; kh < KS; ++kh) {
+      // 16-byte aligned: WPs and ow0 are multiples of 4 words
+      const float4* row = reinterpret_cast<const float4*>(plf + (oh + kh) * WPs + ow0);
+      float v[NV];
+#pragma unroll
+      for (int q4 = 0; q4 < NV / 4; ++q4) {
+        const float4 t4 = row[q4];
+        v[4 * q4] = t4.x;
+        v[4 * q4 + 1] = t4.y;
+        v[4 * q4 + 2] = t4.z;
+        v[4 * q4 + 3] = t4.w;
+      }
+#pragma unroll
+      for (int kw = 0; kw < KS; ++kw)
+#pragma unroll
+        for (int e = 0; e < kStrip; ++e) acc[e] = fmaf(v[e + kw], wc[kh * KS + kw], acc[e]);
+    }
+    uint32_t code[kStrip];
+#pragma unroll
+    for (int e = 0; e < kStrip; ++e) {
+      const int32_t a = __float2int_rn(acc[e]) + bc;
+      float vq = __fmul_rn(__int2float_rn(a), mul);
+      vq = __fdiv_rn(vq, y_scale);
+      code[e] = rint_code_bits(vq, lo_z, hi_z, y_zp);
+    }
+    YT* out = yp + oh * OW + ow0;
+    if (vec_rows && ((reinterpret_cast<uintptr_t>(out) & 7) == 0)) {
+      *reinterpret_cast<uint2*>(out) =
+          make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]), pack_low_bytes(code[4], code[5], code[6], code[7]));
+    } else {
+#pragma unroll
+      for (int e = 0; e < kStrip; ++e)
+        if (ow0 + e < OW) out[e] = (YT)code[e];
+    }
+  }
+}
+
 struct ConvShape {
   int64_t N, C, H, W, M, Cg, kH, kW, OH, OW;
   int64_t pt, pl, pb, pr, sh, sw, dh, dw, group;
@@ -208,6 +310,23 @@ int run_direct(const ConvShape& s, const void* x, float x_scale, int x_zp, const
   const float dq_lo = std::is_same<YT, uint8_t>::value ? 0.0f : -128.0f;
   const float dq_hi = std::is_same<YT, uint8_t>::value ? 255.0f : 127.0f;
   const int64_t P = std::max(std::max(s.pt, s.pb), std::max(s.pl, s.pr));
+  {
+    // strip kernel: depthwise 3x3 / 5x5, stride 1, dilation 1
+    const int64_t nstrips = (s.OW + kStrip - 1) / kStrip;
+    const size_t ssmem = (size_t)(s.OH + s.kH - 1) * ((nstrips * kStrip + s.kW - 1 + 3) & ~3) * 4;
+    if (s.group == s.C && s.M == s.C && s.Cg == 1 && s.sh == 1 && s.sw == 1 && s.dh == 1 && s.dw == 1 &&
+        s.kH == s.kW && (s.kH == 3 || s.kH == 5) && ssmem <= 160 * 1024 && !getenv("I8Q_FORCE_CONV_HALO")) {
+      auto kern = s.kH == 3 ? qlinearconv_depthwise_strip<XT, WT, YT, 3> : qlinearconv_depthwise_strip<XT, WT, YT, 5>;
+      if (ssmem > 48 * 1024)
+        I8Q_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem));
+      I8Q_PROF("qlinearconv_depthwise", st);
+      kern<<<(unsigned)(s.N * s.C), 128, ssmem, st>>>((const XT*)x, (const WT*)w, w_scale, (const WT*)w_zp, per_ch, B,
+                                                      (int)s.C, (int)s.H, (int)s.W, (int)s.OH, (int)s.OW, (int)s.pt,
+                                                      (int)s.pl, x_scale, x_zp, y_scale, y_zp, dq_lo, dq_hi, (YT*)y);
+      I8Q_LAUNCH_CHECK("qlinearconv_depthwise_strip");
+      return I8Q_OK;
+    }
+  }
   if (s.group == s.C && s.M == s.C && s.Cg == 1 && s.sh == 1 && s.sw == 1 && s.dh == 1 && s.dw == 1 &&
       s.kH == s.kW && (s.kH == 3 || s.kH == 5) && (s.H + 2 * P) * (s.W + 2 * P) * 2 <= 160 * 1024) {
     const size_t hsmem = (size_t)(s.H + 2 * P) * (s.W + 2 * P) * 2;

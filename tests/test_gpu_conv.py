@@ -152,3 +152,32 @@ def test_full_size_depthwise(orc, dev):
     c = workloads.qlinearconv(seed=3, depthwise=True)
     run_conv(orc, dev, c["x"], c["x_scale"], c["x_zero_point"], c["w"], c["w_scale"], c["w_zero_point"],
              c["y_scale"], c["y_zero_point"], c["B"], c["pads"], group=c["group"])
+
+
+DW_CASES = [
+    # N, C, H, W, k, pads
+    (2, 8, 56, 56, 3, (1, 1, 1, 1)),
+    (1, 5, 17, 23, 3, (0, 2, 1, 0)),
+    (3, 4, 9, 16, 5, (2, 2, 2, 2)),
+    (1, 6, 30, 7, 5, (0, 0, 0, 0)),
+    (2, 3, 8, 8, 3, (2, 1, 0, 2)),
+]
+
+
+@pytest.mark.parametrize("kernel", ["strip", "halo"])
+@pytest.mark.parametrize("case", DW_CASES)
+@pytest.mark.parametrize("types", [("u8", "u8", "u8"), ("s8", "s8", "s8"), ("u8", "s8", "s8")])
+def test_depthwise_kernels(orc, dev, monkeypatch, kernel, case, types):
+    if kernel == "halo":
+        monkeypatch.setenv("I8Q_FORCE_CONV_HALO", "1")
+    N, C, H, W, k, pads = case
+    rng = np.random.default_rng(N * 100 + C * 10 + k)
+    rg = {"u8": (0, 256, np.uint8), "s8": (-128, 128, np.int8)}
+    xt, wt, yt = (rg[t] for t in types)
+    x = rng.integers(xt[0], xt[1], (N, C, H, W)).astype(xt[2])
+    w = rng.integers(wt[0], wt[1], (C, 1, k, k)).astype(wt[2])
+    ws = rng.uniform(0.001, 0.01, C).astype(np.float32)
+    wz = rng.integers(wt[0], wt[1], C)
+    B = rng.integers(-5000, 5001, C).astype(np.int32)
+    run_conv(orc, dev, x, np.float32(0.0037), int(rng.integers(xt[0], xt[1])), w, ws, wz, np.float32(0.05),
+             int(rng.integers(yt[0], yt[1])), B, pads, group=C, ytype=types[2])
