@@ -81,9 +81,78 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
   nt = r / gsize;
 }
 
-// The epilogue of one row's 64-column slice from the exact sums in run[].
-// Column parameters come from shared memory: pc (colsum), ps (scaleB),
-// pb (bias), SLICE entries each (zero beyond N).
+// Dequantized values of one row's 64-column slice, eight at a time, as
+// ((float)sum * scaleA) * scaleB + bias (the roundings of dequant_epilogue),
+// then the activation ACT (GELU on pairs for bf16 outputs), then stored as
+// bf16 or fp32.  Column parameters come from shared
+// memory: pc (colsum), ps (scaleB), pb (bias), SLICE entries each (zero
+// beyond N), 16-byte aligned.
+template <int ACT, bool BF16>
+__device__ __forceinline__ void store_slice_float(const GemmEpilogue& ep, int64_t row, int64_t col0, int64_t N,
+                                                  const int32_t (&run)[SLICE], int32_t zA, float sA,
+                                                  const int32_t* pc, const float* ps, const float* pb, bool vec) {
+#pragma unroll
+  for (int j = 0; j < SLICE; j += 8) {
+    const int4 c0 = *reinterpret_cast<const int4*>(pc + j), c1 = *reinterpret_cast<const int4*>(pc + j + 4);
+    const float4 s0 = *reinterpret_cast<const float4*>(ps + j), s1 = *reinterpret_cast<const float4*>(ps + j + 4);
+    const float4 b0 = *reinterpret_cast<const float4*>(pb + j), b1 = *reinterpret_cast<const float4*>(pb + j + 4);
+    const int32_t cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float2 sb[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
+                          make_float2(s1.z, s1.w)};
+    const float2 bb[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                          make_float2(b1.z, b1.w)};
+    float2 o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      // zA arrives shifted by 128.  Scalar operations: the compiler may
+      // fuse a paired multiply and a following paired add.
+      float2 v = make_float2(__int2float_rn(run[j + 2 * u] - zA * cc[2 * u]),
+                             __int2float_rn(run[j + 2 * u + 1] - zA * cc[2 * u + 1]));
+      v.x = __fadd_rn(__fmul_rn(__fmul_rn(v.x, sA), sb[u].x), bb[u].x);
+      v.y = __fadd_rn(__fmul_rn(__fmul_rn(v.y, sA), sb[u].y), bb[u].y);
+      if constexpr (ACT == I8Q_ACT_RELU) {
+        v = make_float2(v.x > 0.0f ? v.x : 0.0f, v.y > 0.0f ? v.y : 0.0f);
+      } else if constexpr (ACT == I8Q_ACT_GELU) {
+        if constexpr (BF16)
+          v = gelu_bf16out2(v);
+        else
+          v = make_float2(gelu_erf(v.x), gelu_erf(v.y));
+      }
+      o[u] = v;
+    }
+    if constexpr (BF16) {
+      __nv_bfloat16* C = static_cast<__nv_bfloat16*>(ep.C) + row * ep.ldc + col0 + j;
+      __nv_bfloat162 h[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) h[u] = __float22bfloat162_rn(o[u]);
+      if (vec) {
+        uint4 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&h[0]);
+        pk.y = *reinterpret_cast<uint32_t*>(&h[1]);
+        pk.z = *reinterpret_cast<uint32_t*>(&h[2]);
+        pk.w = *reinterpret_cast<uint32_t*>(&h[3]);
+        *reinterpret_cast<uint4*>(C) = pk;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (col0 + j + u < N) C[u] = (u & 1) ? h[u >> 1].y : h[u >> 1].x;
+      }
+    } else {
+      float* C = static_cast<float*>(ep.C) + row * ep.ldc + col0 + j;
+      if (vec) {
+        *reinterpret_cast<float4*>(C) = make_float4(o[0].x, o[0].y, o[1].x, o[1].y);
+        *reinterpret_cast<float4*>(C + 4) = make_float4(o[2].x, o[2].y, o[3].x, o[3].y);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (col0 + j + u < N) C[u] = (u & 1) ? o[u >> 1].y : o[u >> 1].x;
+      }
+    }
+  }
+}
+
+// The epilogue of one row's 64-column slice from the exact sums in run[]
+// (column parameters as for store_slice_float).
 __device__ __forceinline__ void store_slice(const GemmEpilogue& ep, int64_t row, int64_t col0, int64_t N,
                                             const int32_t (&run)[SLICE], int32_t zA, float sA, const int32_t* pc,
                                             const float* ps, const float* pb) {
@@ -93,9 +162,8 @@ __device__ __forceinline__ void store_slice(const GemmEpilogue& ep, int64_t row,
     const bool vec = full && (ep.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(ep.C) & 15) == 0;
 #pragma unroll
     for (int j = 0; j < SLICE; j += 4) {
-      int32_t v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = run[j + u] - zA * pc[j + u];  // zA arrives shifted by 128
+      const int4 c = *reinterpret_cast<const int4*>(pc + j);
+      const int32_t v[4] = {run[j] - zA * c.x, run[j + 1] - zA * c.y, run[j + 2] - zA * c.z, run[j + 3] - zA * c.w};
       if (vec) {
         *reinterpret_cast<int4*>(C + j) = make_int4(v[0], v[1], v[2], v[3]);
       } else {
@@ -109,46 +177,17 @@ __device__ __forceinline__ void store_slice(const GemmEpilogue& ep, int64_t row,
   const bool bf16 = ep.out_mode == OUT_BF16;
   const bool vec = full && (bf16 ? (ep.ldc % 8 == 0) : (ep.ldc % 4 == 0)) &&
                    (reinterpret_cast<uintptr_t>(ep.C) & 15) == 0;
-  const int act = ep.act;
-#pragma unroll
-  for (int j = 0; j < SLICE; j += 8) {
-    float o[8];
-    if (bf16) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        o[u] = dequant_epilogue_bf16out(run[j + u] - zA * pc[j + u], sA, ps[j + u], pb[j + u], act);
-    } else {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) o[u] = dequant_epilogue(run[j + u] - zA * pc[j + u], sA, ps[j + u], pb[j + u], act);
-    }
-    if (bf16) {
-      __nv_bfloat16* C = static_cast<__nv_bfloat16*>(ep.C) + row * ep.ldc + col0 + j;
-      if (vec) {
-        __nv_bfloat162 h0 = __floats2bfloat162_rn(o[0], o[1]), h1 = __floats2bfloat162_rn(o[2], o[3]);
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(o[4], o[5]), h3 = __floats2bfloat162_rn(o[6], o[7]);
-        uint4 pk;
-        pk.x = *reinterpret_cast<uint32_t*>(&h0);
-        pk.y = *reinterpret_cast<uint32_t*>(&h1);
-        pk.z = *reinterpret_cast<uint32_t*>(&h2);
-        pk.w = *reinterpret_cast<uint32_t*>(&h3);
-        *reinterpret_cast<uint4*>(C) = pk;
-      } else {
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (col0 + j + u < N) C[u] = __float2bfloat16_rn(o[u]);
-      }
-    } else {
-      float* C = static_cast<float*>(ep.C) + row * ep.ldc + col0 + j;
-      if (vec) {
-        *reinterpret_cast<float4*>(C) = make_float4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<float4*>(C + 4) = make_float4(o[4], o[5], o[6], o[7]);
-      } else {
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (col0 + j + u < N) C[u] = o[u];
-      }
-    }
+#define I8Q_SLICE(A, B) store_slice_float<A, B>(ep, row, col0, N, run, zA, sA, pc, ps, pb, vec)
+  if (bf16) {
+    if (ep.act == I8Q_ACT_GELU) I8Q_SLICE(I8Q_ACT_GELU, true);
+    else if (ep.act == I8Q_ACT_RELU) I8Q_SLICE(I8Q_ACT_RELU, true);
+    else I8Q_SLICE(I8Q_ACT_IDENTITY, true);
+  } else {
+    if (ep.act == I8Q_ACT_GELU) I8Q_SLICE(I8Q_ACT_GELU, false);
+    else if (ep.act == I8Q_ACT_RELU) I8Q_SLICE(I8Q_ACT_RELU, false);
+    else I8Q_SLICE(I8Q_ACT_IDENTITY, false);
   }
+#undef I8Q_SLICE
 }
 
 // Epilogue of one row's 64-column slice for the 8-bit-code products (see

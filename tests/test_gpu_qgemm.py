@@ -148,6 +148,23 @@ def test_types_and_activations_int8_B(orc, dev, act, typeA, typeC):
     run_case(orc, dev, A, iB=iB, scaleB=sB, bias=bias, act=act, typeA=typeA, typeC=typeC)
 
 
+@pytest.mark.parametrize("typeC", ["bf16", "f32"])
+def test_gelu_over_its_whole_range(orc, dev, typeC):
+    """With every B code zero the sum is 0 and each output is GELU(bias[j])
+    exactly, so the bias sweeps the activation's input: [-20, 20] densely,
+    the negative tail where GELU falls through the bf16 subnormals to zero,
+    tiny and subnormal magnitudes of both signs, and huge ones."""
+    rng = np.random.default_rng(21)
+    xs = np.concatenate([np.linspace(-20, 20, 8001), -np.geomspace(12.5, 14.5, 2001),
+                         np.geomspace(1e-44, 1e-3, 401), -np.geomspace(1e-44, 1e-3, 401),
+                         [0.0, -0.0, 1e30, -1e30, 3e38, -3e38]]).astype(np.float32)
+    M, K, N = 256, 64, xs.size
+    A = rng.normal(0, 1, (M, K)).astype(np.float32)
+    iB = np.zeros((K, N), np.int8)
+    sB = np.ones(N, np.float32)
+    run_case(orc, dev, A, iB=iB, scaleB=sB, bias=xs, act="gelu", typeC=typeC, check_codes=False)
+
+
 @pytest.mark.parametrize("Btype", ["f32", "bf16"])
 @pytest.mark.parametrize("avoid", [False, True])
 def test_non_constant_B(orc, dev, Btype, avoid):
