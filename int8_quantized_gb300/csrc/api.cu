@@ -444,7 +444,8 @@ int forward_impl(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf, vo
     __nv_bfloat16* qb = ctx->use_tc ? reinterpret_cast<__nv_bfloat16*>(base + L.iBt_bf16) : nullptr;
     float* sb = reinterpret_cast<float*>(base + L.scaleB);
     int32_t* cs = reinterpret_cast<int32_t*>(base + L.colsum);
-    rc = launch_quantize_cols(B, ctx->typeB, K, N, ctx->avoid, q, qb, ctx->Kp, sb, cs,
+    // the tensor-core product reads only the bf16 codes
+    rc = launch_quantize_cols(B, ctx->typeB, K, N, ctx->avoid, ctx->use_tc ? nullptr : q, qb, ctx->Kp, sb, cs,
                               reinterpret_cast<uint32_t*>(base + L.colmax), s);
     if (rc) return rc;
     iBt = q;
@@ -459,6 +460,13 @@ int forward_impl(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf, vo
     const int qb = (ctx->typeB == I8Q_S8 || !ctx->avoid) ? 7 : 6;
     rc = launch_gemm_tc(uA_bf16, iBt_bf16, M, N, ctx->Kp, 7 + qb, ep, s);
     if (rc != I8Q_ERR_UNSUPPORTED) return rc;
+    if (!ctx->constB) {
+      // the int8 codes were not written for the tensor-core product
+      rc = launch_quantize_cols(B, ctx->typeB, K, N, ctx->avoid, const_cast<int8_t*>(iBt), nullptr, ctx->Kp,
+                                const_cast<float*>(scaleB), const_cast<int32_t*>(colsum),
+                                reinterpret_cast<uint32_t*>(base + L.colmax), s);
+      if (rc) return rc;
+    }
   }
   return launch_gemm_imma(uA, iBt, M, N, ctx->Kp, ep, s);
 }

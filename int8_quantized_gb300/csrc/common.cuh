@@ -239,7 +239,8 @@ int launch_quantize_rows(const void* A, int typeA, int64_t M, int64_t K, int64_t
                          cudaStream_t s);
 
 // Column quantization of B (K x N fp32/bf16 row-major) into iBt (N x Kp
-// int8, transposed, zero padded), optional iBt_bf16, scaleB[N], colsum[N].
+// int8, transposed, zero padded) and iBt_bf16 (the same codes as bf16),
+// either of which may be null, scaleB[N], colsum[N].
 // colmax_scratch: N words of device scratch for the two-pass form, or null.
 int launch_quantize_cols(const void* B, int typeB, int64_t K, int64_t N, int avoid_overflow,
                          int8_t* iBt, __nv_bfloat16* iBt_bf16, int64_t Kp, float* scaleB,

@@ -474,7 +474,7 @@ cols_kernel(const T* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int qmin
         w0 |= (uint32_t)(uint8_t)src[q] << (8 * q);
         w1 |= (uint32_t)(uint8_t)src[q + 4] << (8 * q);
       }
-      *reinterpret_cast<uint2*>(iBt + jd * Kp + k0 + seg * 8) = make_uint2(w0, w1);
+      if (iBt) *reinterpret_cast<uint2*>(iBt + jd * Kp + k0 + seg * 8) = make_uint2(w0, w1);
       if (iBt_bf16) {
         uint4 o;
         o.x = code_bf16_bits(src[0]) | (code_bf16_bits(src[1]) << 16);
@@ -596,9 +596,11 @@ col_quant_wide(const T* __restrict__ B, int64_t K, int64_t N, int64_t Kp, const 
       for (int q = 0; q < 8; ++q)
         wds[q] = (uint32_t)(uint8_t)src[4 * q] | ((uint32_t)(uint8_t)src[4 * q + 1] << 8) |
                  ((uint32_t)(uint8_t)src[4 * q + 2] << 16) | ((uint32_t)(uint8_t)src[4 * q + 3] << 24);
-      uint4* dst = reinterpret_cast<uint4*>(iBt + jj * Kp + k0 + h * 32);
-      dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
-      dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+      if (iBt) {
+        uint4* dst = reinterpret_cast<uint4*>(iBt + jj * Kp + k0 + h * 32);
+        dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+        dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+      }
       if (iBt_bf16) {
         uint4* db = reinterpret_cast<uint4*>(iBt_bf16 + jj * Kp + k0 + h * 32);
 #pragma unroll
@@ -622,6 +624,209 @@ col_quant_wide(const T* __restrict__ B, int64_t K, int64_t N, int64_t Kp, const 
     const int64_t jj = j0 + threadIdx.x;
     if (jj < N) atomicAdd(colsum + jj, t);
   }
+}
+
+// ---- columns, one strip per CTA -------------------------------------------
+// A persistent CTA owns a strip of 128 bytes of every row of B (32 fp32 or
+// 64 bf16 columns).  One thread streams the strip through a 4-stage ring of
+// 256-row TMA boxes twice: first for max|B| per column, then -- from L2: a
+// strip per SM is 0.5 MB at K = 4096 -- for the codes.  Each consumer
+// thread owns one column and a run of R adjacent rows of every box (16 for
+// fp32, 32 for bf16), reads it down the column in shared memory and writes
+// its R codes, contiguous along K, straight to the transposed outputs.  Rows
+// past K read as zero from the tensor map, which gives the zero padding up
+// to Kp.  The rounding avoids the conversion units: q is clamped to
+// [qmin, qmax] (integer bounds, so clamping commutes with rounding) and
+// 1.5 * 2^23 is added, which rounds to nearest even; taking it off again
+// gives the code as an exact float, whose bf16 bits are its top 16 bits and
+// whose column sum is exact in fp32 (|sum| <= 2^23).
+constexpr int kCqConsumers = 512, kCqThreads = kCqConsumers + 32;
+constexpr int kCqBoxRows = 256, kCqStages = 4, kCqStageBytes = kCqBoxRows * 128;
+constexpr size_t kCqSmem = 1024 + (size_t)kCqStages * kCqStageBytes + 2 * kCqStages * 8 + 16;
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr uint32_t ST_TIMEOUT_COLS = 1u << 13;
+
+// int8 code of a bf16 code held in the high half of a word (an exact small
+// integer): the low byte of code + 1.5 * 2^23.
+__device__ __forceinline__ uint32_t code_byte(uint32_t bf16_bits_high) {
+  return (uint32_t)__float_as_int(__fadd_rn(__uint_as_float(bf16_bits_high), kRoundMagic)) & 0xffu;
+}
+
+__device__ __forceinline__ float elem_f32(const uint8_t* p, float) { return *reinterpret_cast<const float*>(p); }
+__device__ __forceinline__ float elem_f32(const uint8_t* p, __nv_bfloat16) {
+  return __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(p) << 16);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kCqThreads, 1)
+col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int64_t Kp, int qmin, int qmax,
+              int8_t* __restrict__ iBt, __nv_bfloat16* __restrict__ iBt_bf16, float* __restrict__ scaleB,
+              int32_t* __restrict__ colsum, uint32_t* status) {
+  constexpr int W = 128 / (int)sizeof(T);   // strip width in columns
+  constexpr int RG = kCqConsumers / W;      // row groups of a box
+  constexpr int R = kCqBoxRows / RG;        // rows per consumer thread per box
+  extern __shared__ uint8_t cq_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(cq_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)kCqStages * kCqStageBytes);
+  uint64_t* empty = full + kCqStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCqStages);
+  __shared__ float red[RG][W];
+  __shared__ float sscale[W];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int b = 0; b < kCqStages; ++b) {
+      tc::mbar_init(tc::smem_u32(full + b), 1);
+      tc::mbar_init(tc::smem_u32(empty + b), kCqConsumers / 32);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  const int64_t nstrips = (N + W - 1) / W;
+  const int nb1 = (int)((K + kCqBoxRows - 1) / kCqBoxRows);   // boxes of the max pass
+  const int nb2 = (int)((Kp + kCqBoxRows - 1) / kCqBoxRows);  // boxes of the code pass
+  if (warp == kCqConsumers / 32) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int64_t strip = blockIdx.x; ok && strip < nstrips; strip += gridDim.x)
+        for (int b = 0; ok && b < nb1 + nb2; ++b, ++it) {
+          const uint32_t st = it % kCqStages;
+          if (it >= (uint32_t)kCqStages &&
+              !tc::wait_bar(tc::smem_u32(empty + st), ((it / kCqStages) - 1) & 1u, abort_flag, status, ST_TIMEOUT_COLS)) {
+            ok = false;
+            break;
+          }
+          const int y = (b < nb1 ? b : b - nb1) * kCqBoxRows;
+          tc::mbar_arrive_expect_tx(tc::smem_u32(full + st), (uint32_t)kCqStageBytes);
+          tc::tma_load_2d(tc::smem_u32(ring + (size_t)st * kCqStageBytes), &tmB, tc::smem_u32(full + st),
+                          (int)(strip * W), y);
+        }
+      // the copies in flight land before the CTA leaves (bounded)
+      const uint32_t first = it > (uint32_t)kCqStages ? it - kCqStages : 0u;
+      for (uint32_t i = first; i < it; ++i) {
+        const uint64_t t0 = tc::global_ns();
+        while (!tc::mbar_try_wait(tc::smem_u32(full + i % kCqStages), (i / kCqStages) & 1u))
+          if (tc::global_ns() - t0 > tc::WAIT_LIMIT_NS) {
+            atomicOr(status, ST_TIMEOUT_COLS);
+            break;
+          }
+      }
+    }
+    return;
+  }
+  // ---------------- consumers ----------------
+  const int c = tid % W, rg = tid / W;
+  const float lo = (float)qmin, hi = (float)qmax;
+  uint32_t it = 0;
+  bool ok = true;
+  auto consumers_sync = [] { asm volatile("bar.sync 1, %0;\n" ::"n"(kCqConsumers) : "memory"); };
+  for (int64_t strip = blockIdx.x; strip < nstrips; strip += gridDim.x) {
+    const int64_t j = strip * W + c;
+    // pass 1: max |B| of this column over the thread's rows
+    float m = 0.0f;
+    for (int b = 0; b < nb1; ++b, ++it) {
+      const uint32_t st = it % kCqStages;
+      if (ok) ok = tc::wait_bar(tc::smem_u32(full + st), (it / kCqStages) & 1u, abort_flag, status, ST_TIMEOUT_COLS);
+      if (ok) {
+        const uint8_t* src = ring + (size_t)st * kCqStageBytes + (size_t)(rg * R) * 128 + (size_t)c * sizeof(T);
+#pragma unroll
+        for (int r = 0; r < R; ++r) m = fmaxf(m, fabsf(elem_f32(src + r * 128, T())));
+      }
+      __syncwarp();
+      if (ok && lane == 0) tc::mbar_arrive(tc::smem_u32(empty + st));
+    }
+    red[rg][c] = m;
+    consumers_sync();
+    if (tid < W) {
+      float r = red[0][tid];
+#pragma unroll
+      for (int g = 1; g < RG; ++g) r = fmaxf(r, red[g][tid]);
+      float sv = __fdiv_rn(r, hi);
+      sv = sv == 0.0f ? 1.0f : sv;
+      sscale[tid] = sv;
+      if (ok && strip * W + tid < N) scaleB[strip * W + tid] = sv;
+    }
+    consumers_sync();
+    const float s = sscale[c];
+    float fsum = 0.0f;
+    // pass 2: codes of the thread's R rows of each box
+    for (int b = 0; b < nb2; ++b, ++it) {
+      const uint32_t st = it % kCqStages;
+      if (ok) ok = tc::wait_bar(tc::smem_u32(full + st), (it / kCqStages) & 1u, abort_flag, status, ST_TIMEOUT_COLS);
+      uint32_t w[R / 2];
+      if (ok) {
+        const uint8_t* src = ring + (size_t)st * kCqStageBytes + (size_t)(rg * R) * 128 + (size_t)c * sizeof(T);
+#pragma unroll
+        for (int r = 0; r < R; r += 2) {
+          float f[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float q = fminf(fmaxf(__fdiv_rn(elem_f32(src + (r + h) * 128, T()), s), lo), hi);
+            f[h] = __fsub_rn(__fadd_rn(q, kRoundMagic), kRoundMagic);
+            fsum = __fadd_rn(fsum, f[h]);
+          }
+          w[r / 2] = (__float_as_uint(f[0]) >> 16) | (__float_as_uint(f[1]) & 0xffff0000u);
+        }
+      }
+      __syncwarp();
+      if (ok && lane == 0) tc::mbar_arrive(tc::smem_u32(empty + st));
+      const int64_t k = (int64_t)b * kCqBoxRows + rg * R;
+      if (ok && j < N && k < Kp) {
+        if (iBt_bf16) {
+          uint4* d = reinterpret_cast<uint4*>(iBt_bf16 + j * Kp + k);
+#pragma unroll
+          for (int q = 0; q < R / 8; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+        if (iBt) {
+          uint4* d = reinterpret_cast<uint4*>(iBt + j * Kp + k);
+#pragma unroll
+          for (int q = 0; q < R / 16; ++q) {
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t w0 = w[8 * q + 2 * e], w1 = w[8 * q + 2 * e + 1];
+              o[e] = code_byte(w0 << 16) | (code_byte(w0 & 0xffff0000u) << 8) | (code_byte(w1 << 16) << 16) |
+                     (code_byte(w1 & 0xffff0000u) << 24);
+            }
+            d[q] = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+    }
+    // column sums (exact integers in fp32)
+    red[rg][c] = fsum;
+    consumers_sync();
+    if (tid < W && ok && strip * W + tid < N) {
+      float t = red[0][tid];
+#pragma unroll
+      for (int g = 1; g < RG; ++g) t = __fadd_rn(t, red[g][tid]);
+      colsum[strip * W + tid] = __float2int_rn(t);
+    }
+    consumers_sync();
+  }
+}
+
+template <typename T>
+int launch_col_quant_tma(const T* B, int64_t K, int64_t N, int64_t Kp, int qmin, int qmax, int8_t* iBt,
+                         __nv_bfloat16* iBt_bf16, float* scaleB, int32_t* colsum, uint32_t* status, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(col_quant_tma<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCqSmem);
+  });
+  I8Q_CUDA_TRY(attr);
+  constexpr int W = 128 / (int)sizeof(T);
+  CUtensorMap map;
+  const int rc = tc::make_map_plain_2d(&map, B,
+                                       sizeof(T) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                       N, K, N * (int64_t)sizeof(T), W, kCqBoxRows, "quantize_cols");
+  if (rc) return rc;
+  const int grid = (int)std::min<int64_t>(ceil_div(N, (int64_t)W), (int64_t)sm_count());
+  col_quant_tma<T><<<grid, kCqThreads, kCqSmem, s>>>(map, K, N, Kp, qmin, qmax, iBt, iBt_bf16, scaleB, colsum, status);
+  I8Q_LAUNCH_CHECK("col_quant_tma");
+  return I8Q_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -720,6 +925,16 @@ int launch_quantize_cols(const void* B, int typeB, int64_t K, int64_t N, int avo
   if (N <= 0) return I8Q_OK;
   const int qmax = avoid_overflow ? 63 : 127, qmin = avoid_overflow ? -64 : -128;
   I8Q_PROF("quantize_cols", s);
+  const bool bf = typeB == I8Q_BF16;
+  uint32_t* status = device_status_word();
+  if (status && N % (bf ? 8 : 4) == 0 && Kp % 64 == 0 && K < ((int64_t)1 << 31) && N < ((int64_t)1 << 31) &&
+      aligned16(B) && aligned16(iBt) && aligned16(iBt_bf16) && !getenv("I8Q_COLS_TWO_PASS")) {
+    if (bf)
+      return launch_col_quant_tma(static_cast<const __nv_bfloat16*>(B), K, N, Kp, qmin, qmax, iBt, iBt_bf16, scaleB,
+                                  colsum, status, s);
+    return launch_col_quant_tma(static_cast<const float*>(B), K, N, Kp, qmin, qmax, iBt, iBt_bf16, scaleB, colsum,
+                                status, s);
+  }
   if (colmax_scratch && N % 4 == 0 && aligned16(B)) {
     I8Q_CUDA_TRY(cudaMemsetAsync(colmax_scratch, 0, (size_t)N * 4, s));
     I8Q_CUDA_TRY(cudaMemsetAsync(colsum, 0, (size_t)N * 4, s));

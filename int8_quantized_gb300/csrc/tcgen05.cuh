@@ -246,6 +246,25 @@ inline int make_tensor_map(CUtensorMap* map, const void* base, int rank, const c
   return I8Q_OK;
 }
 
+// 2-D tensor map without swizzle (fp32 or bf16 elements, dtype a
+// CU_TENSOR_MAP_DATA_TYPE_*): `inner` contiguous elements per row, `rows`
+// rows `row_bytes` apart; a box lands in shared memory as box_rows dense
+// rows of box_inner elements.  Elements outside the tensor read as zero.
+inline int make_map_plain_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int64_t inner, int64_t rows,
+                             int64_t row_bytes, int box_inner, int box_rows, const char* who) {
+  auto fn = encode_fn();
+  if (!fn) return fail(I8Q_ERR_CUDA, std::string(who) + ": cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype, 2u, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(I8Q_ERR_CUDA, std::string(who) + ": cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+  return I8Q_OK;
+}
+
 // 2-D bf16 tensor map over rows x Kp (Kp contiguous), box 64 x box_rows.
 inline int make_map_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t Kp, int box_rows, const char* who) {
   cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)rows};

@@ -165,6 +165,25 @@ def test_gelu_over_its_whole_range(orc, dev, typeC):
     run_case(orc, dev, A, iB=iB, scaleB=sB, bias=xs, act="gelu", typeC=typeC, check_codes=False)
 
 
+@pytest.mark.parametrize("path", ["strip", "two_pass"])
+@pytest.mark.parametrize("Btype", ["f32", "bf16"])
+@pytest.mark.parametrize("K,N", [(300, 104), (1000, 200), (520, 64)])
+def test_column_quantization_paths(orc, dev, monkeypatch, path, Btype, K, N):
+    """B quantized per column inside Forward by the one-read strip kernel
+    (TMA boxes past K and strips past N read as zero) and by the two-pass
+    kernels, with K not a multiple of the 256-row box and N not a multiple
+    of the strip width."""
+    if path == "two_pass":
+        monkeypatch.setenv("I8Q_COLS_TWO_PASS", "1")
+    rng = np.random.default_rng(K + N)
+    A = rng.normal(0, 1, (40, K)).astype(np.float32)
+    B = rng.normal(0, 0.05, (K, N)).astype(np.float32)
+    B[:, 3] = 0.0  # a zero column: scale 1
+    if Btype == "bf16":
+        B = workloads.bf16_bits(B)
+    run_case(orc, dev, A, B, bias=None, avoid=True, constB=False)
+
+
 @pytest.mark.parametrize("Btype", ["f32", "bf16"])
 @pytest.mark.parametrize("avoid", [False, True])
 def test_non_constant_B(orc, dev, Btype, avoid):
