@@ -38,7 +38,7 @@ namespace {
 struct LstmLayout {
   int64_t D, TB, Ip, Hp, H4;
   size_t off_Wt, off_Wtb, off_Wcs, off_Rt, off_Rtb, off_Rcs, off_Wsc, off_Rsc, off_Wbi, off_Rbi, off_uX, off_uXc,
-      off_sX, off_zX, off_Gx, off_uh, off_uhc, off_sh, off_zh, off_h, off_c, total;
+      off_sX, off_zX, off_Gx, off_uh, off_uhc, off_sh, off_zh, off_mm, off_gbar, off_h, off_c, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -72,9 +72,14 @@ LstmLayout lstm_layout(int64_t T, int64_t batch, int64_t input, int64_t hidden, 
   L.off_zX = take((size_t)L.TB * 4);
   L.off_Gx = take((size_t)L.D * L.TB * L.H4 * 4);
   L.off_uh = take((size_t)L.D * batch * L.Hp);
-  L.off_uhc = take((size_t)L.D * batch * L.Hp * 2);
-  L.off_sh = take((size_t)L.D * batch * 4);
-  L.off_zh = take((size_t)L.D * batch * 4);
+  // h codes, scales and zero points: two step parities (the per-step
+  // kernels use the first), per-row min/max pairs and a barrier counter
+  // for the persistent recurrence
+  L.off_uhc = take((size_t)2 * L.D * batch * L.Hp * 2);
+  L.off_sh = take((size_t)2 * L.D * batch * 4);
+  L.off_zh = take((size_t)2 * L.D * batch * 4);
+  L.off_mm = take((size_t)2 * L.D * batch * 2 * 4);
+  L.off_gbar = take(2 * 4);
   L.off_h = take((size_t)2 * L.D * batch * hidden * 4);
   L.off_c = take((size_t)L.D * batch * hidden * 4);
   L.total = o;
@@ -628,6 +633,463 @@ lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
 }
 }  // namespace tcs
 
+// ---- the persistent recurrence ------------------------------------------------
+// One cooperative launch runs every step.  CTA (d, g) owns the 16 hidden
+// units 16g .. 16g + 15 of direction d, i.e. the 64 interleaved gate rows
+// 64g .. 64g + 63 of R[d], which it loads into shared memory once (bf16
+// R - zp, K-major, 128-byte swizzle) and keeps for the whole sequence.  Per
+// step the TMA producer streams the previous step's h codes (uh - 128,
+// bf16, 64 batch rows x Hp) through an 11-stage ring and one thread issues
+// the product as M = 64 batch rows x N = 64 gate rows on tcgen05, fp32
+// chunks of 2^24 / 2^log2 K-elements drained exactly to int32 as in the
+// per-step kernels.  Products this small are bound by the latency of MMAs
+// that accumulate into the same tile, so the four 16-K sub-steps of each
+// 64-K slab go to four accumulators (TMEM columns 0, 64, 128, 192), summed
+// in int32 by the drain.  With M = 64 the accumulator rows 16w .. 16w + 15 sit in
+// TMEM lanes 32w .. 32w + 15, so the epilogue warps of all four
+// sub-partitions read them; a row's 16 columns (four units, gates i, o, f, c
+// interleaved) are split between a lane and the lane 16 above it, two units
+// each, and each thread updates its cells without further exchange.  The
+// new h is quantized per row right away: each CTA folds min/max of its units
+// per row, merges them into a global per-row pair (order-preserving integer
+// images, atomicMax), and after a barrier over the direction's CTAs every
+// CTA derives the same scale and zero point and writes the codes of its
+// units; a second barrier publishes them to the direction's next TMA reads
+// (the two directions never wait on each other).  Codes, scales/zero
+// points and the min/max pairs are double buffered by step parity.  Every
+// wait is bounded: on expiry the kernel sets ST_TIMEOUT in the status word,
+// which every other wait also polls, and all CTAs leave after their copies
+// and products in flight have landed.
+namespace prs {
+
+using namespace tc;
+using tcs::clip_gate;
+
+constexpr int BM = 64, BN = 64, BK = 64, STAGES = 11;
+constexpr int EPI_WARPS = 16, THREADS = 32 * (2 + EPI_WARPS);  // warps 2..17: TMEM sub-partition warp % 4
+constexpr int NACC = 4;                // independent accumulators: the 16-K sub-steps of a 64-K slab
+constexpr int TMEM_COLS = NACC * 64;
+constexpr int A_STAGE = BM * BK * 2;   // 8 KB
+constexpr int R_SLAB = BN * BK * 2;    // 8 KB per 64 K-elements of the resident R tile
+constexpr uint32_t ST_TIMEOUT = 1u << 9;
+constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, accf, acce, rbar, hready, mdone
+
+struct Params {
+  const int32_t* Rcs;  // [D, 4H]
+  const float* Rsc;    // [D, 4H]
+  const float* Gx;     // [D, T*B, 4H]
+  const float* Wbi;    // [D, 4H]
+  const float* Rbi;    // [D, 4H]
+  float* c;            // [D, B, H]
+  float* hbuf;         // 2 x [D, B, H] (step s reads parity s & 1, writes (s + 1) & 1)
+  float* Y;            // [T, D, B, H] or null
+  __nv_bfloat16* uhc;  // 2 x [D * B, Hp] h codes - 128 (step s reads parity (s + 1) & 1, writes s & 1)
+  float* sh;           // 2 x [D * B]
+  int32_t* zh;         // 2 x [D * B]
+  uint32_t* mm;        // 2 x [D * B][2]: max image of -h, of h
+  uint32_t* gbar;      // [D] barrier counters of each direction's CTAs (0 at launch)
+  int T, B, H, Hp, D, direction, CS, tiles;  // tiles = H / 16 per direction
+  uint32_t* status;
+  const int32_t* seq_lens;
+  const float* P;
+  float clip;
+  int input_forget;
+};
+
+size_t smem_bytes(int64_t Hp) { return 1024 + (size_t)STAGES * A_STAGE + (size_t)(Hp / BK) * R_SLAB + NUM_BARS * 8 + 16; }
+
+// Order-preserving image of a float as an unsigned integer (0 is below the
+// image of every float, so 0 is the empty value of an atomicMax).
+__device__ __forceinline__ uint32_t ord_image(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ord_value(uint32_t v) {
+  return __uint_as_float((v & 0x80000000u) ? (v & 0x7fffffffu) : ~v);
+}
+
+// Grid barrier number k (1, 2, ...), called by one thread per CTA after a
+// CTA-wide barrier: the fence makes the CTA's writes visible before the
+// arrival (cumulatively); true when every CTA has arrived, false on
+// timeout or when another CTA gave up.
+__device__ __forceinline__ bool grid_barrier(uint32_t* gbar, uint32_t target, uint32_t* status) {
+  __threadfence();
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(gbar) : "memory");
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(gbar) : "memory");
+    if (v >= target) return true;
+    if ((i & 63u) == 63u) {
+      if (*(volatile uint32_t*)status & ST_TIMEOUT) return false;
+      if (global_ns() - t0 > WAIT_LIMIT_NS) {
+        atomicOr(status, ST_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// bf16 bit pattern of an integer code in [-128, 127] (exact): the top half
+// of its fp32 image, formed without a conversion instruction.
+__device__ __forceinline__ uint32_t code_bits(int c) {
+  return __float_as_uint(__fsub_rn(__int_as_float(0x4B400000 + c), 12582912.0f)) >> 16;
+}
+
+// A wait expected to last microseconds: as wait_bar, but the thread sleeps
+// between polls, so that the producer and MMA threads sharing its
+// sub-partition keep their issue slots.
+__device__ __forceinline__ bool wait_bar_idle(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t* status) {
+  unsigned long long t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    __nanosleep(128);
+    if ((i & 15u) == 15u) {
+      if (*abort_flag) return false;
+      const unsigned long long now = global_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > WAIT_LIMIT_NS) {
+        atomicOr(status, ST_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(EPI_WARPS * 32) : "memory"); }
+
+template <bool VAR>
+__global__ void __launch_bounds__(THREADS, 1)
+lstm_persist_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmH, Params p) {
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int KT = p.Hp / BK;
+  uint8_t* rtile = smem + STAGES * A_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rtile + (size_t)KT * R_SLAB);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  __shared__ float cst[4][BN];           // Rcs (as int), Rsc, Wbi, Rbi of the tile's 64 gate rows
+  __shared__ float pw[3][16];            // peepholes i, o, f of the tile's units
+  __shared__ float red[4][2][64];        // per column group: min, max of h per batch row
+  __shared__ int gok;
+  const uint32_t smem0 = smem_u32(smem);
+  auto sA = [&](int st) { return smem0 + (uint32_t)(st * A_STAGE); };
+  const uint32_t sR = smem_u32(rtile);
+  auto full = [&](int st) { return smem_u32(bars + st); };
+  auto empty = [&](int st) { return smem_u32(bars + STAGES + st); };
+  const uint32_t accf = smem_u32(bars + 2 * STAGES), acce = smem_u32(bars + 2 * STAGES + 1);
+  const uint32_t rbar = smem_u32(bars + 2 * STAGES + 2), hready = smem_u32(bars + 2 * STAGES + 3);
+  const uint32_t mdone = smem_u32(bars + 2 * STAGES + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = blockIdx.x / p.tiles, g = blockIdx.x % p.tiles;
+  const int H4 = 4 * p.H;
+  const int nchunks = (KT + p.CS - 1) / p.CS;
+  const int64_t DB = (int64_t)p.D * p.B;
+  const uint32_t nctas = (uint32_t)p.tiles;  // CTAs of this direction
+  uint32_t* dbar = p.gbar + d;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(full(st), 1);
+      mbar_init(empty(st), 1);
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, EPI_WARPS);
+    mbar_init(rbar, 1);
+    mbar_init(hready, 1);
+    mbar_init(mdone, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  for (int i = threadIdx.x; i < BN; i += THREADS) {
+    const int64_t dn = (int64_t)d * H4 + g * BN + i;
+    cst[0][i] = __int_as_float(__ldg(p.Rcs + dn));
+    cst[1][i] = __ldg(p.Rsc + dn);
+    cst[2][i] = __ldg(p.Wbi + dn);
+    cst[3][i] = __ldg(p.Rbi + dn);
+  }
+  if (VAR && threadIdx.x < 48) {
+    const int k = threadIdx.x / 16, ul = threadIdx.x % 16;
+    pw[k][ul] = p.P ? __ldg(p.P + (int64_t)d * 3 * p.H + k * p.H + g * 16 + ul) : 0.0f;
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(rbar, (uint32_t)(KT * R_SLAB));
+      for (int kt = 0; kt < KT; ++kt) tma_load_2d(sR + (uint32_t)(kt * R_SLAB), &tmR, rbar, kt * BK, d * H4 + g * BN);
+      // stage st, round parity ph (counters, no division in the loop)
+      uint32_t st = 0, ph = 0, it = 0;
+      for (int s = 0; ok && s < p.T; ++s) {
+        if (s > 0) {
+          if (!wait_bar_idle(hready, (uint32_t)(s - 1) & 1u, abort_flag, p.status)) break;
+          // the codes were written by other CTAs' generic stores
+          asm volatile("fence.proxy.async.global;\n" ::: "memory");
+        }
+        const int y = (int)((((s + 1) & 1) * DB) + (int64_t)d * p.B);
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          if (!wait_bar(empty(st), ph ^ 1u, abort_flag, p.status, ST_TIMEOUT)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full(st), (uint32_t)A_STAGE);
+          tma_load_2d(sA(st), &tmH, full(st), kt * BK, y);
+          if (++st == (uint32_t)STAGES) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // the copies in flight land before the CTA leaves (bounded)
+      const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+      for (uint32_t i = first; i < it; ++i) {
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(full(i % STAGES), (i / STAGES) & 1u))
+          if (global_ns() - t0 > WAIT_LIMIT_NS) break;
+      }
+      {
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(rbar, 0))
+          if (global_ns() - t0 > WAIT_LIMIT_NS) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = wait_bar(rbar, 0, abort_flag, p.status, ST_TIMEOUT);
+      tc_fence_after();
+      // counters instead of division: stage st, round parity ph, chunk
+      // step kc; descriptors advanced by addition (start address >> 4)
+      const uint64_t adesc0 = desc_sw128(sA(0)), bdesc0 = desc_sw128(sR);
+      uint32_t st = 0, ph = 0, chunk = 0;
+      for (int s = 0; ok && s < p.T; ++s) {
+        int kc = 0;
+        for (int kt = 0; kt < KT; ++kt) {
+          if (kc == 0) {
+            if (!wait_bar(acce, (chunk & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          if (!wait_bar(full(st), ph, abort_flag, p.status, ST_TIMEOUT)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = adesc0 + (uint64_t)((st * (uint32_t)A_STAGE) >> 4);
+          const uint64_t bd = bdesc0 + (uint64_t)(((uint32_t)kt * (uint32_t)R_SLAB) >> 4);
+          const uint32_t acc = kc == 0 ? 0u : 1u;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma(tmem + (uint32_t)(k * BN), ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, acc);
+          tc_commit(empty(st));
+          if (++kc == p.CS || kt == KT - 1) {
+            tc_commit(accf);
+            ++chunk;
+            kc = 0;
+          }
+          if (++st == (uint32_t)STAGES) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // every product issued has completed before TMEM is freed (bounded)
+      tc_commit(mdone);
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(mdone, 0))
+        if (global_ns() - t0 > WAIT_LIMIT_NS) break;
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    // sub-partition qd holds batch rows 16 qd .. 16 qd + 15 in its lanes
+    // 0..15; lane t and lane t + 16 take row 16 qd + (t mod 16), units
+    // 2 hi, 2 hi + 1 of the column group cg (hi = t >= 16)
+    const int qd = warp & 3, cg = (warp - 2) >> 2, hi = lane >> 4;
+    const int b = qd * 16 + (lane & 15);
+    const bool bvalid = b < p.B;
+    const int u0 = g * 16 + 4 * cg + 2 * hi;  // first of this thread's 2 units
+    const int col0 = 16 * cg + 8 * hi;        // its first gate column in the tile
+    const bool rev = p.direction == I8Q_LSTM_REVERSE || (p.direction == I8Q_LSTM_BIDIRECTIONAL && d == 1);
+    const int64_t TB = (int64_t)p.T * p.B;
+    const int64_t row = (int64_t)d * p.B + b;  // state row
+    int L = p.T;
+    if (VAR && bvalid && p.seq_lens) L = min(max(__ldg(p.seq_lens + b), 0), p.T);  // lengths outside [0, T] clamp
+    uint32_t chunk = 0;
+    bool ok = true;
+    for (int s = 0; s < p.T; ++s) {
+      const bool live = bvalid && s < L;
+      const int tb = rev ? L - 1 - s : s;  // for VAR rows, within the row's own length
+      const int t = VAR ? tb : (rev ? p.T - 1 - s : s);
+      const float* hprev = p.hbuf + (int64_t)(s & 1) * DB * p.H;
+      float* hnext = p.hbuf + (int64_t)((s + 1) & 1) * DB * p.H;
+      const int prv = (s + 1) & 1, cur = s & 1;
+      // operands that do not depend on the product
+      float gx[8], cp[2], hp[2];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) gx[i] = 0.0f;
+      cp[0] = cp[1] = hp[0] = hp[1] = 0.0f;
+      float shb = 0.0f;
+      int zhb = 0;
+      if (live) {
+        const float4* gsrc = reinterpret_cast<const float4*>(p.Gx + ((int64_t)d * TB + (int64_t)t * p.B + b) * H4 +
+                                                             g * BN + col0);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float4 v = __ldg(gsrc + k);
+          gx[4 * k] = v.x; gx[4 * k + 1] = v.y; gx[4 * k + 2] = v.z; gx[4 * k + 3] = v.w;
+        }
+        const float2 c2 = *reinterpret_cast<const float2*>(p.c + row * p.H + u0);
+        cp[0] = c2.x; cp[1] = c2.y;
+        shb = __ldcg(p.sh + prv * DB + row);  // written by another CTA in the previous step
+        zhb = __ldcg(p.zh + prv * DB + row);
+      } else if (bvalid) {
+        const float2 h2 = *reinterpret_cast<const float2*>(hprev + row * p.H + u0);
+        hp[0] = h2.x; hp[1] = h2.y;
+      }
+      // the exact sums of this step
+      int32_t run[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) run[i] = 0;
+      for (int c = 0; c < nchunks; ++c, ++chunk) {
+        const bool got = ok && wait_bar_idle(accf, chunk & 1u, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int a = 0; a < NACC; ++a) {
+          uint32_t v[16];
+          tmem_ld16(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(a * BN + 16 * cg), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t up = __shfl_sync(0xffffffffu, v[8 + i], lane & 15);
+            run[i] += __float2int_rn(__uint_as_float(hi ? up : v[i]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce);
+      }
+      // cell update of the 2 units (the operation order of the per-step kernels)
+      float hn[2] = {hp[0], hp[1]};
+      if (ok && live) {
+        float pre[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          // h entered as uh - 128: sum_k (uh - zh) R = run - (zh - 128) colsum
+          const int32_t v = run[i] - (zhb - 128) * __float_as_int(cst[0][col0 + i]);
+          float gh = __fmul_rn(__int2float_rn(v), shb);
+          gh = __fmul_rn(gh, cst[1][col0 + i]);
+          pre[i] = __fadd_rn(gx[i], gh);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int c0 = col0 + 4 * k;  // gate columns of unit k: i, o, f, c
+          float si = pre[4 * k], so = pre[4 * k + 1], sf = pre[4 * k + 2], sc = pre[4 * k + 3];
+          float cn, og;
+          if (VAR) {
+            const int ul = 4 * cg + 2 * hi + k;
+            if (p.P) {
+              si = __fadd_rn(si, __fmul_rn(pw[0][ul], cp[k]));
+              sf = __fadd_rn(sf, __fmul_rn(pw[2][ul], cp[k]));
+            }
+            const float ig = sigmoid_f32(clip_gate(__fadd_rn(__fadd_rn(si, cst[2][c0]), cst[3][c0]), p.clip));
+            const float fg = p.input_forget
+                                 ? __fsub_rn(1.0f, ig)
+                                 : sigmoid_f32(clip_gate(__fadd_rn(__fadd_rn(sf, cst[2][c0 + 2]), cst[3][c0 + 2]), p.clip));
+            const float ct = tanhf(clip_gate(__fadd_rn(__fadd_rn(sc, cst[2][c0 + 3]), cst[3][c0 + 3]), p.clip));
+            cn = __fadd_rn(__fmul_rn(fg, cp[k]), __fmul_rn(ig, ct));
+            if (p.P) so = __fadd_rn(so, __fmul_rn(pw[1][ul], cn));
+            og = sigmoid_f32(clip_gate(__fadd_rn(__fadd_rn(so, cst[2][c0 + 1]), cst[3][c0 + 1]), p.clip));
+          } else {
+            const float ig = sigmoid_f32(__fadd_rn(__fadd_rn(si, cst[2][c0]), cst[3][c0]));
+            og = sigmoid_f32(__fadd_rn(__fadd_rn(so, cst[2][c0 + 1]), cst[3][c0 + 1]));
+            const float fg = sigmoid_f32(__fadd_rn(__fadd_rn(sf, cst[2][c0 + 2]), cst[3][c0 + 2]));
+            const float ct = tanhf(__fadd_rn(__fadd_rn(sc, cst[2][c0 + 3]), cst[3][c0 + 3]));
+            cn = __fadd_rn(__fmul_rn(fg, cp[k]), __fmul_rn(ig, ct));
+          }
+          hn[k] = __fmul_rn(og, tanhf(cn));
+          cp[k] = cn;
+        }
+        *reinterpret_cast<float2*>(p.c + row * p.H + u0) = make_float2(cp[0], cp[1]);
+        if (p.Y)
+          *reinterpret_cast<float2*>(p.Y + (((int64_t)t * p.D + d) * p.B + b) * p.H + u0) = make_float2(hn[0], hn[1]);
+      }
+      if (ok && bvalid) *reinterpret_cast<float2*>(hnext + row * p.H + u0) = make_float2(hn[0], hn[1]);
+      // per-row min / max of the new h over this CTA's 16 units
+      float mn = fminf(hn[0], hn[1]), mx = fmaxf(hn[0], hn[1]);
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      if (!hi) {
+        red[cg][0][b] = mn;
+        red[cg][1][b] = mx;
+      }
+      epi_sync();
+      if (cg == 0 && !hi && ok && bvalid) {
+        mn = fminf(fminf(red[0][0][b], red[1][0][b]), fminf(red[2][0][b], red[3][0][b]));
+        mx = fmaxf(fmaxf(red[0][1][b], red[1][1][b]), fmaxf(red[2][1][b], red[3][1][b]));
+        atomicMax(p.mm + (cur * DB + row) * 2, ord_image(-mn));
+        atomicMax(p.mm + (cur * DB + row) * 2 + 1, ord_image(mx));
+      }
+      epi_sync();
+      if (warp == 2 && lane == 0) gok = ok && grid_barrier(dbar, nctas * (uint32_t)(2 * s + 1), p.status);
+      epi_sync();
+      ok = ok && gok;
+      // the row's scale and zero point (the same in every CTA), this CTA's codes
+      if (ok && bvalid) {
+        const uint32_t* m2 = p.mm + (cur * DB + row) * 2;
+        const float rmn = fminf(-ord_value(__ldcg(m2)), 0.0f), rmx = fmaxf(ord_value(__ldcg(m2 + 1)), 0.0f);
+        float sc;
+        int z;
+        row_scale_zero(rmn, rmx, sc, z);
+        const float lo_z = (float)(-z), hi_z = (float)(255 - z);
+        const int c0 = (int)(row_code(hn[0], sc, lo_z, hi_z, z)) - 128;
+        const int c1 = (int)(row_code(hn[1], sc, lo_z, hi_z, z)) - 128;
+        *reinterpret_cast<uint32_t*>(p.uhc + (cur * DB + row) * p.Hp + u0) = code_bits(c0) | (code_bits(c1) << 16);
+        if (g == 0 && cg == 0 && !hi) {
+          p.sh[cur * DB + row] = sc;
+          p.zh[cur * DB + row] = z;
+        }
+      }
+      // the next step's min/max pairs of this direction start empty
+      if (ok && g == 0) {
+        const int e = threadIdx.x - 64;  // 0 .. 511 over the epilogue warps
+        for (int64_t i = e; i < 2 * p.B; i += EPI_WARPS * 32) p.mm[((int64_t)prv * DB + (int64_t)d * p.B) * 2 + i] = 0u;
+      }
+      epi_sync();
+      if (warp == 2 && lane == 0) {
+        gok = ok && grid_barrier(dbar, nctas * (uint32_t)(2 * s + 2), p.status);
+        if (gok) mbar_arrive(hready);
+        else *abort_flag = 1;
+      }
+      epi_sync();
+      ok = ok && gok;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace prs
+
 int grid_for(int64_t n, int threads = 256) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n, threads), (int64_t)sm_count() * 8));
 }
@@ -712,6 +1174,8 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
   __nv_bfloat16* uhc = (__nv_bfloat16*)(ws + L.off_uhc);
   float* sh = (float*)(ws + L.off_sh);
   int32_t* zh = (int32_t*)(ws + L.off_zh);
+  uint32_t* mmb = (uint32_t*)(ws + L.off_mm);
+  uint32_t* gbar = (uint32_t*)(ws + L.off_gbar);
   float* hbuf = (float*)(ws + L.off_h);
   float* cbuf = (float*)(ws + L.off_c);
   const int64_t H = hidden, BH = batch * hidden, DBH = L.D * BH;
@@ -809,12 +1273,109 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(lstm_step_tc_kernel)");
   }
 
+  // the persistent recurrence: every CTA resident at once (one per SM),
+  // at most 64 batch rows, whole 16-unit tiles
+  bool persist = false;
+  CUtensorMap mR64, mH2;
+  const int ptiles = (int)(H / 16);
+  const size_t psmem = prs::smem_bytes(L.Hp);
+  if (step_tc && batch <= 64 && H % 16 == 0 && (reinterpret_cast<uintptr_t>(Y) & 15) == 0 &&
+      !getenv("I8Q_LSTM_STEPS")) {
+    static std::once_flag pattr_once;
+    static cudaError_t pattr_err = cudaSuccess;
+    static int coop = 0;
+    std::call_once(pattr_once, [] {
+      int dev = 0;
+      pattr_err = cudaGetDevice(&dev);
+      if (pattr_err == cudaSuccess) pattr_err = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+      const int most = 227 * 1024 - 4096;
+      if (pattr_err == cudaSuccess)
+        pattr_err = cudaFuncSetAttribute(prs::lstm_persist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         most);
+      if (pattr_err == cudaSuccess)
+        pattr_err = cudaFuncSetAttribute(prs::lstm_persist_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         most);
+    });
+    if (pattr_err != cudaSuccess) return cuda_fail(pattr_err, "lstm persistent kernel attributes");
+    int per_sm = 0;
+    if (coop && psmem <= (size_t)(227 * 1024 - 4096)) {
+      I8Q_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, var ? prs::lstm_persist_kernel<true> : prs::lstm_persist_kernel<false>, prs::THREADS, psmem));
+    }
+    persist = per_sm >= 1 && L.D * ptiles <= (int64_t)per_sm * sm_count();
+    if (persist) {
+      rc = tc::make_map_2d(&mR64, Rtb, L.D * L.H4, L.Hp, prs::BN, "dq_lstm");
+      if (rc) return rc;
+      rc = tc::make_map_2d(&mH2, uhc, 2 * L.D * batch, L.Hp, prs::BN, "dq_lstm");
+      if (rc) return rc;
+    }
+  }
+
   // recurrence: both directions per launch, 2 launches per step
   auto recurrence = [&]() -> int {
     init_state<<<grid_for(DBH), 256, 0, s>>>(h0, c0, DBH, hbuf, cbuf);
     I8Q_LAUNCH_CHECK("init_state");
     // rows whose sequence ends early leave the rest of Y zero
     if (Y && seq_lens) I8Q_CUDA_TRY(cudaMemsetAsync(Y, 0, (size_t)T * DBH * sizeof(float), s));
+    if (persist) {
+      // h0's codes go to parity 1, which step 0 reads; the padding columns
+      // of both parities stay zero
+      I8Q_CUDA_TRY(cudaMemsetAsync(uhc, 0, (size_t)2 * L.D * batch * L.Hp * 2, s));
+      I8Q_CUDA_TRY(cudaMemsetAsync(mmb, 0, (size_t)2 * L.D * batch * 2 * 4, s));
+      I8Q_CUDA_TRY(cudaMemsetAsync(gbar, 0, 2 * 4, s));
+      int rcp = launch_quantize_rows(hbuf, I8Q_F32, L.D * batch, H, H, uh, uhc + L.D * batch * L.Hp, L.Hp,
+                                     sh + L.D * batch, zh + L.D * batch, s);
+      if (rcp) return rcp;
+      prs::Params pp;
+      pp.Rcs = Rcs;
+      pp.Rsc = Rsc;
+      pp.Gx = Gx;
+      pp.Wbi = Wbi;
+      pp.Rbi = Rbi;
+      pp.c = cbuf;
+      pp.hbuf = hbuf;
+      pp.Y = Y;
+      pp.uhc = uhc;
+      pp.sh = sh;
+      pp.zh = zh;
+      pp.mm = mmb;
+      pp.gbar = gbar;
+      pp.T = (int)T;
+      pp.B = (int)batch;
+      pp.H = (int)H;
+      pp.Hp = (int)L.Hp;
+      pp.D = (int)L.D;
+      pp.direction = direction;
+      pp.CS = (int)((((int64_t)1 << 24) >> prod_log2) / prs::BK);
+      pp.tiles = ptiles;
+      pp.status = device_status_word();
+      pp.seq_lens = seq_lens;
+      pp.P = P;
+      pp.clip = clip;
+      pp.input_forget = input_forget ? 1 : 0;
+      if (!pp.status) return fail(I8Q_ERR_CUDA, "dq_lstm: no device status word");
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(L.D * ptiles));
+      cfg.blockDim = dim3(prs::THREADS);
+      cfg.dynamicSmemBytes = psmem;
+      cfg.stream = s;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      I8Q_PROF("lstm_persist", s);
+      if (var)
+        I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, prs::lstm_persist_kernel<true>, mR64, mH2, pp));
+      else
+        I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, prs::lstm_persist_kernel<false>, mR64, mH2, pp));
+      I8Q_LAUNCH_CHECK("lstm_persist_kernel");
+      const float* h_last = hbuf + (T & 1) * DBH;
+      if (Y_h) copy_f32<<<grid_for(DBH), 256, 0, s>>>(h_last, Y_h, DBH);
+      if (Y_c) copy_f32<<<grid_for(DBH), 256, 0, s>>>(cbuf, Y_c, DBH);
+      I8Q_LAUNCH_CHECK("copy_f32");
+      return I8Q_OK;
+    }
     int rc2 = launch_quantize_rows(hbuf, I8Q_F32, L.D * batch, H, H, uh, step_tc ? uhc : nullptr, L.Hp, sh, zh, s);
     if (rc2) return rc2;
     StepParams sp;
@@ -898,7 +1459,8 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
   // is on (which brackets each launch).
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   I8Q_CUDA_TRY(cudaStreamIsCapturing(s, &cap));
-  if (s == nullptr || cap != cudaStreamCaptureStatusNone || profiling_enabled() || T < 4) return recurrence();
+  if (persist || s == nullptr || cap != cudaStreamCaptureStatusNone || profiling_enabled() || T < 4)
+    return recurrence();
   int64_t clip_bits = 0;
   std::memcpy(&clip_bits, &clip, sizeof(float));
   const LstmGraphKey key{X, W, R, W_scale, R_scale, Bias, h0, c0, Y, Y_h, Y_c, workspace, W_zero_point, R_zero_point,

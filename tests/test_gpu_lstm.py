@@ -21,11 +21,15 @@ pytestmark = pytest.mark.gpu
 DIRS = {"forward": q.LSTM_FORWARD, "reverse": q.LSTM_REVERSE, "bidirectional": q.LSTM_BIDIRECTIONAL}
 
 
-@pytest.fixture(params=["imma", "tc"], autouse=True)
+@pytest.fixture(params=["imma", "tc", "tc_steps"], autouse=True)
 def core(request, monkeypatch):
     """Every case runs with the recurrent product on the int8 mma.sync core
-    and on the exact-integer tcgen05 core."""
-    monkeypatch.setenv("I8Q_FORCE_CORE", request.param)
+    and on the exact-integer tcgen05 core, the latter both as the
+    persistent recurrence (one launch, where the layer fits) and as one
+    launch per step."""
+    monkeypatch.setenv("I8Q_FORCE_CORE", "imma" if request.param == "imma" else "tc")
+    if request.param == "tc_steps":
+        monkeypatch.setenv("I8Q_LSTM_STEPS", "1")
     return request.param
 
 

@@ -18,6 +18,15 @@ pytestmark = pytest.mark.gpu
 DIRS = {"forward": q.LSTM_FORWARD, "reverse": q.LSTM_REVERSE, "bidirectional": q.LSTM_BIDIRECTIONAL}
 
 
+@pytest.fixture(params=["persistent", "steps"], autouse=True)
+def recurrence(request, monkeypatch):
+    """Each case runs as the persistent recurrence (one launch, where the
+    layer fits) and as one launch per step."""
+    if request.param == "steps":
+        monkeypatch.setenv("I8Q_LSTM_STEPS", "1")
+    return request.param
+
+
 def _t(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
