@@ -43,8 +43,8 @@ WORKLOAD = ("dynamic quantized GEMM M=8192 K=4096 N=14336: bf16 A quantized per 
 NCU_TRAFFIC = {
     "gemm_tc_pair": {"sources": ["int8_quantized_gb300/csrc/gemm_tc.cu", "int8_quantized_gb300/csrc/tcgen05.cuh",
                                  "int8_quantized_gb300/csrc/common.cuh"],
-                     "sha256": "183baa2615f014a7dd3047b4b94eec8548de3fd9ed300be21001df25e58f06c3",
-                     "bytes": (577.92 + 224.25) * 1e6,
+                     "sha256": "e3883f3ed1efdcd1c2156f6bd444f6bab21424dbb75064fd801fa2b190c3a0a8",
+                     "bytes": (576.93 + 222.29) * 1e6,
                      "profile": "profiles/gemm_tc_pair_large_gemm.md"},
 }
 

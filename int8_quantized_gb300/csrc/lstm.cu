@@ -15,17 +15,20 @@
 //
 // Layout: the 4H gate columns of W, R, their scales and the biases are
 // interleaved per hidden unit (column q*H + u stored at 4u + q), so any
-// 64-column tile holds all four gates of 16 hidden units.  Then one kernel
-// per step does, for both directions at once, the recurrent integer product
-// and the whole cell update in its epilogue: on the tensor pipe
+// 64-column tile holds all four gates of 16 hidden units.  The projection
+// runs once over all T * batch rows on the tensor-core GEMM; X is quantized
+// once for both directions.  The recurrence runs, where the layer fits, as
+// one persistent cooperative kernel (prs:: below: R resident in shared
+// memory, the new h quantized per row inside the kernel).  Otherwise one
+// kernel per step does, for both directions at once, the recurrent integer
+// product and the whole cell update in its epilogue: on the tensor pipe
 // (tcgen05, 128 gate columns x 64 batch rows per CTA, h codes centred to
 // uh - 128 in bf16, fp32 chunks drained exactly to int32, the step's
 // x-projection and previous cell state loaded while the MMAs run) for wide
-// layers, or on the int8 mma.sync form (64 x 64 tiles) otherwise.  The
-// projection runs once over all T * batch rows on the tensor-core GEMM; X is
-// quantized once for both directions.  Each step's new h is quantized per
-// row (both directions in one launch) for the next step, and the whole
-// sequence of steps is replayed as one CUDA graph, cached per argument set.
+// layers, or on the int8 mma.sync form (64 x 64 tiles) otherwise.  Each
+// step's new h is then quantized per row (both directions in one launch) for
+// the next step, and the whole sequence of steps is replayed as one CUDA
+// graph, cached per argument set.
 #include <cstring>
 #include <functional>
 #include <mutex>

@@ -49,6 +49,26 @@ def test_ties_and_saturation(orc, dev):
     _run_q(orc, dev, x, np.float32(0.02), 0, None, "s8")
 
 
+def test_extreme_scales(orc, dev):
+    """Per-channel scales whose reciprocal is not a normal number (subnormal
+    and near the largest float) next to ordinary ones, inputs with zeros,
+    tiny and huge magnitudes, and exact ties."""
+    rng = np.random.default_rng(12)
+    C = 64
+    s = rng.uniform(0.005, 0.05, C).astype(np.float32)
+    s[:8] = [1e-39, 5e-40, 2.9e-39, 3e38, 1e38, 1e-30, 1e30, 7e-45]
+    x = rng.normal(0, 2, (40, C)).astype(np.float32)
+    x[0] = 0.0
+    x[1] = 1e-40
+    x[2] = -3e38
+    x[3] = 3e38
+    x[4:8, 8:] = (np.round(x[4:8, 8:] / s[8:]) + 0.5) * s[8:]  # ties on the ordinary channels
+    for t, lo, hi in (("u8", 0, 256), ("s8", -128, 128)):
+        _run_q(orc, dev, x, s, rng.integers(lo, hi, C), 1, t)
+        for sc in (np.float32(1e-39), np.float32(3e38), np.float32(0.02)):
+            _run_q(orc, dev, x, sc, 0, None, t)
+
+
 def test_closed_form_golden_cases(orc, dev):
     from conftest import read_golden_rows
     for x, s, zp, t, y in read_golden_rows("quantize_linear_cases.txt"):
