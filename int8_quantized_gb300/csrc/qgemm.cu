@@ -30,37 +30,50 @@
 namespace i8q {
 namespace {
 
-constexpr int PT = 64;  // rows x K elements per tile of the operand pass
+constexpr int PT = 64;   // rows x K elements per tile of the operand pass
+constexpr int CK = 512;  // K elements per CTA (8 tiles)
 
 // Xc[r][k] = bf16(X(r,k) - cx) for k < K, 0 for K <= k < Kp, and
-// sums[r] = sum_k (X(r,k) - cx).  X(r,k) = X[r*K + k] when k_fast, else
-// X[k*R + r].  One CTA owns 64 rows and walks K in 64-wide tiles through
-// shared memory, reading the source along its contiguous index.
-template <bool SIGNED>
+// sums[r] += sum_k (X(r,k) - cx) over the CTA's K range (sums zeroed by the
+// caller).  X(r,k) = X[r*K + k] when k_fast, else X[k*R + r].  CTA (x, y)
+// owns rows 64x .. 64x + 63 and K elements 512y .. 512y + 511, in 64-wide
+// tiles through shared memory, reading the source along its contiguous
+// index 16 bytes at a time where the layout allows (VEC), else bytewise.
+template <bool SIGNED, bool VEC>
 __global__ void __launch_bounds__(256)
 center_operand(const uint8_t* __restrict__ X, int64_t R, int64_t K, int64_t Kp, int k_fast,
                __nv_bfloat16* __restrict__ Xc, int32_t* __restrict__ sums) {
-  __shared__ int8_t tile[PT][PT + 4];  // [r][k], centred codes
+  __shared__ __align__(16) int8_t tile[PT][PT + 4];  // [r][k], centred codes
   const int t = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.x * PT;
-  const uint8_t flip = SIGNED ? 0 : 0x80;  // u8 code - 128 == int8 of (code ^ 0x80)
+  const int64_t kbeg = (int64_t)blockIdx.y * CK, kend = kbeg + CK < Kp ? kbeg + CK : Kp;
+  const uint32_t flip = SIGNED ? 0u : 0x80808080u;  // u8 code - 128 == int8 of (code ^ 0x80)
+  const int a = t >> 2, b = (t & 3) * 16;
   int part = 0;
-  for (int64_t k0 = 0; k0 < Kp; k0 += PT) {
-    // load 64 x 64 codes: thread -> one source line segment of 16 bytes
-    const int a = t >> 2, b = (t & 3) * 16;
+  for (int64_t k0 = kbeg; k0 < kend; k0 += PT) {
+    // load 64 x 64 codes: thread -> one 16-byte segment of a source line
     if (k_fast) {
-      const int64_t r = r0 + a;
+      const int64_t r = r0 + a, k = k0 + b;
+      if (VEC && r < R && k + 16 <= K) {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(X + r * K + k));
+        uint32_t* d = reinterpret_cast<uint32_t*>(&tile[a][b]);
+        d[0] = v.x ^ flip; d[1] = v.y ^ flip; d[2] = v.z ^ flip; d[3] = v.w ^ flip;
+      } else {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int64_t k = k0 + b + e;
-        tile[a][b + e] = (r < R && k < K) ? (int8_t)(X[r * K + k] ^ flip) : (int8_t)0;
+        for (int e = 0; e < 16; ++e)
+          tile[a][b + e] = (r < R && k + e < K) ? (int8_t)(X[r * K + k + e] ^ (uint8_t)flip) : (int8_t)0;
       }
     } else {
-      const int64_t k = k0 + a;
+      const int64_t k = k0 + a, r = r0 + b;
+      if (VEC && k < K && r + 16 <= R) {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(X + k * R + r));
+        const uint32_t w[4] = {v.x ^ flip, v.y ^ flip, v.z ^ flip, v.w ^ flip};
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int64_t r = r0 + b + e;
-        tile[b + e][a] = (r < R && k < K) ? (int8_t)(X[k * R + r] ^ flip) : (int8_t)0;
+        for (int e = 0; e < 16; ++e) tile[b + e][a] = (int8_t)(w[e >> 2] >> (8 * (e & 3)));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          tile[b + e][a] = (r + e < R && k < K) ? (int8_t)(X[k * R + r + e] ^ (uint8_t)flip) : (int8_t)0;
       }
     }
     __syncthreads();
@@ -83,8 +96,8 @@ center_operand(const uint8_t* __restrict__ X, int64_t R, int64_t K, int64_t Kp, 
   // the four threads of a row are adjacent lanes
   part += __shfl_xor_sync(0xffffffffu, part, 1);
   part += __shfl_xor_sync(0xffffffffu, part, 2);
-  const int64_t r = r0 + (t >> 2);
-  if ((t & 3) == 0 && r < R) sums[r] = part;
+  const int64_t r = r0 + a;
+  if ((t & 3) == 0 && r < R) atomicAdd(sums + r, part);
 }
 
 // g[j] = cb - bz[j]; e[j] = colsum[j] + K g[j] (wrapping int32);
@@ -230,14 +243,21 @@ QgLayout qg_layout(int64_t M, int64_t N, int64_t K) {
 
 int launch_center(const void* X, int type, int64_t R, int64_t K, int64_t Kp, int k_fast, __nv_bfloat16* Xc,
                   int32_t* sums, cudaStream_t s) {
-  const int64_t blocks = ceil_div(R, PT);
-  if (blocks > 0x7fffffff) return fail(I8Q_ERR_UNSUPPORTED, "qgemm: too many rows");
+  const int64_t bx = ceil_div(R, PT), by = ceil_div(Kp, CK);
+  if (bx > 0x7fffffff || by > 65535) return fail(I8Q_ERR_UNSUPPORTED, "qgemm: operand too large");
+  if (bx == 0) return I8Q_OK;
   I8Q_PROF("qgemm_center", s);
-  if (type == I8Q_S8)
-    center_operand<true><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t*>(X), R, K, Kp, k_fast, Xc, sums);
-  else
-    center_operand<false><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint8_t*>(X), R, K, Kp, k_fast, Xc,
-                                                            sums);
+  I8Q_CUDA_TRY(cudaMemsetAsync(sums, 0, (size_t)R * sizeof(int32_t), s));
+  const bool vec = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && (k_fast ? K % 16 == 0 : R % 16 == 0);
+  const dim3 grid((unsigned)bx, (unsigned)by);
+  const auto* x8 = static_cast<const uint8_t*>(X);
+  if (type == I8Q_S8) {
+    if (vec) center_operand<true, true><<<grid, 256, 0, s>>>(x8, R, K, Kp, k_fast, Xc, sums);
+    else center_operand<true, false><<<grid, 256, 0, s>>>(x8, R, K, Kp, k_fast, Xc, sums);
+  } else {
+    if (vec) center_operand<false, true><<<grid, 256, 0, s>>>(x8, R, K, Kp, k_fast, Xc, sums);
+    else center_operand<false, false><<<grid, 256, 0, s>>>(x8, R, K, Kp, k_fast, Xc, sums);
+  }
   I8Q_LAUNCH_CHECK("center_operand");
   return I8Q_OK;
 }
