@@ -17,6 +17,8 @@
 // operator's 256 possible outputs are computed once per block, with the same
 // arithmetic, into a table replicated per lane in shared memory (entry e of
 // lane l at word e * 32 + l, so every lookup of a warp is conflict-free).
+#include <mutex>
+
 #include "common.cuh"
 
 namespace i8q {
@@ -107,6 +109,69 @@ binary_fast(const uint8_t* __restrict__ A, int amode, int64_t aper, const uint8_
   }
 }
 
+// QLinearAdd / QLinearMul on large tensors: the output code depends only
+// on the two input codes, so each block first fills a 256 x 256 table of
+// codes (byte a * 256 + b, computed by binary_one, so bit for bit the
+// per-element result) in shared memory, then streams 16 codes per thread
+// and group, four groups in flight, each output one table lookup.  Modes as
+// in binary_fast.
+constexpr int kTabThreads = 1024, kTabBytes = 65536;
+
+template <bool AS, bool BS>
+__global__ void __launch_bounds__(kTabThreads, 1)
+binary_table(const uint8_t* __restrict__ A, int amode, int64_t aper, const uint8_t* __restrict__ B, int bmode,
+             int64_t bper, int64_t n, BinParams p, uint8_t* __restrict__ C) {
+  extern __shared__ uint32_t tab[];  // 16384 words, codes (a, 4w' .. 4w' + 3) in word a * 64 + w'
+  for (int wi = threadIdx.x; wi < kTabBytes / 4; wi += kTabThreads) {
+    const uint32_t a = (uint32_t)wi >> 6, b0 = ((uint32_t)wi & 63u) * 4u;
+    int32_t unused;
+    tab[wi] = pack_low_bytes(binary_one<AS, BS>(a, b0, p, &unused), binary_one<AS, BS>(a, b0 + 1, p, &unused),
+                             binary_one<AS, BS>(a, b0 + 2, p, &unused), binary_one<AS, BS>(a, b0 + 3, p, &unused));
+  }
+  __syncthreads();
+  const uint8_t* t8 = reinterpret_cast<const uint8_t*>(tab);
+  constexpr int U = 4;
+  const int64_t groups = n / 16;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g0 < groups; g0 += U * stride) {
+    uint32_t aw[U][4], bw[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = (g0 + u * stride) * 16;
+      const bool in = g0 + u * stride < groups;
+      if (amode == 1) {
+        const uint32_t v = A[0] * 0x01010101u;
+        aw[u][0] = aw[u][1] = aw[u][2] = aw[u][3] = v;
+      } else {
+        const uint4 v = in ? __ldcs(reinterpret_cast<const uint4*>(A + fast_offset(amode, i, aper))) : make_uint4(0, 0, 0, 0);
+        aw[u][0] = v.x, aw[u][1] = v.y, aw[u][2] = v.z, aw[u][3] = v.w;
+      }
+      if (bmode == 1) {
+        const uint32_t v = B[0] * 0x01010101u;
+        bw[u][0] = bw[u][1] = bw[u][2] = bw[u][3] = v;
+      } else {
+        const uint4 v = in ? __ldcs(reinterpret_cast<const uint4*>(B + fast_offset(bmode, i, bper))) : make_uint4(0, 0, 0, 0);
+        bw[u][0] = v.x, bw[u][1] = v.y, bw[u][2] = v.z, bw[u][3] = v.w;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t gi = g0 + u * stride;
+      if (gi >= groups) break;
+      uint32_t ow[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t c[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          c[e] = t8[(((aw[u][w] >> (8 * e)) & 0xffu) << 8) | ((bw[u][w] >> (8 * e)) & 0xffu)];
+        ow[w] = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+      }
+      __stcs(reinterpret_cast<uint4*>(C + gi * 16), make_uint4(ow[0], ow[1], ow[2], ow[3]));
+    }
+  }
+}
+
 struct Strides {
   int rank;
   int64_t out[kMaxRank];
@@ -169,17 +234,29 @@ unary_lut(const uint8_t* __restrict__ X, int64_t n, int op, float x_scale, int x
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const bool aligned = ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(Y)) & 15) == 0;
   if (aligned) {
-    for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups; gi += stride) {
-      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(X) + gi);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[4];
+    // four 16-byte groups per thread in flight before any is used
+    constexpr int U = 4;
+    for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g0 < groups; g0 += U * stride) {
+      uint4 v[U];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t c0 = lut[((w[q] >> 0) & 0xff) * 32 + lane], c1 = lut[((w[q] >> 8) & 0xff) * 32 + lane];
-        const uint32_t c2 = lut[((w[q] >> 16) & 0xff) * 32 + lane], c3 = lut[(w[q] >> 24) * 32 + lane];
-        o[q] = pack_low_bytes(c0, c1, c2, c3);
+      for (int u = 0; u < U; ++u) {
+        const int64_t gi = g0 + u * stride;
+        v[u] = gi < groups ? __ldcs(reinterpret_cast<const uint4*>(X) + gi) : make_uint4(0, 0, 0, 0);
       }
-      __stcs(reinterpret_cast<uint4*>(Y) + gi, make_uint4(o[0], o[1], o[2], o[3]));
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t gi = g0 + u * stride;
+        if (gi >= groups) break;
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t c0 = lut[((w[q] >> 0) & 0xff) * 32 + lane], c1 = lut[((w[q] >> 8) & 0xff) * 32 + lane];
+          const uint32_t c2 = lut[((w[q] >> 16) & 0xff) * 32 + lane], c3 = lut[(w[q] >> 24) * 32 + lane];
+          o[q] = pack_low_bytes(c0, c1, c2, c3);
+        }
+        __stcs(reinterpret_cast<uint4*>(Y) + gi, make_uint4(o[0], o[1], o[2], o[3]));
+      }
     }
   }
   for (int64_t i = (aligned ? groups * 16 : 0) + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
@@ -268,7 +345,19 @@ int run_binary(const uint8_t* A, const uint8_t* B, const Strides& st, int64_t n,
   const bool aligned =
       ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 15) == 0;
   int64_t done = 0;
-  if (am >= 0 && bm >= 0 && aligned && n >= 16) {
+  if (am >= 0 && bm >= 0 && aligned && p.op != 2 && n >= ((int64_t)1 << 20) && !getenv("I8Q_QEW_NO_TABLE")) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+      attr = cudaFuncSetAttribute(binary_table<AS, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTabBytes);
+    });
+    I8Q_CUDA_TRY(attr);
+    const int grid = (int)std::min<int64_t>(sm_count(), ceil_div(n / 16, (int64_t)kTabThreads));
+    binary_table<AS, BS><<<grid, kTabThreads, kTabBytes, s>>>(A, am, aper, B, bm, bper, n, p,
+                                                               static_cast<uint8_t*>(C));
+    I8Q_LAUNCH_CHECK("binary_table");
+    done = (n / 16) * 16;
+  } else if (am >= 0 && bm >= 0 && aligned && n >= 16) {
     binary_fast<AS, BS><<<grid_for(n / 16), 256, 0, s>>>(A, am, aper, B, bm, bper, n, p, C);
     I8Q_LAUNCH_CHECK("binary_fast");
     done = (n / 16) * 16;
@@ -357,7 +446,13 @@ extern "C" int i8q_qlinear_unary(int op, const void* X, int64_t n, int qtype, fl
   const int o = op == I8Q_QLINEAR_LEAKY_RELU ? 0 : 1;
   const float lo_z = (qtype == I8Q_U8 ? 0.0f : -128.0f) - (float)y_zero_point;
   const float hi_z = (qtype == I8Q_U8 ? 255.0f : 127.0f) - (float)y_zero_point;
-  const int grid = grid_for(std::max<int64_t>(n / 16, 1));
+  // no more blocks than fit at once (each holds a 32 KB table): a second
+  // wave of blocks would double the time of the SMs that run it
+  int per_sm = 0;
+  I8Q_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, (qtype == I8Q_S8) ? unary_lut<true> : unary_lut<false>, 256, 0));
+  const int grid = (int)std::max<int64_t>(
+      1, std::min<int64_t>(ceil_div(std::max<int64_t>(n / 16, 1), 256), (int64_t)sm_count() * std::max(per_sm, 1)));
   I8Q_PROF(o == 0 ? "qlinear_leaky_relu" : "qlinear_sigmoid", s);
   if (qtype == I8Q_S8)
     unary_lut<true><<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(X), n, o, x_scale, x_zero_point, y_scale,

@@ -14,6 +14,15 @@ from conftest import read_golden
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["table", "arithmetic"], autouse=True)
+def binary_path(request, monkeypatch):
+    """Large QLinearAdd / QLinearMul run through the 256 x 256 code table,
+    and with the per-element arithmetic."""
+    if request.param == "arithmetic":
+        monkeypatch.setenv("I8Q_QEW_NO_TABLE", "1")
+    return request.param
+
+
 def _t(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
@@ -93,6 +102,20 @@ def test_large_same_shape(orc, dev):
     B = rng.integers(0, 256, (4, 1024, 4096)).astype(np.uint8)
     binary(orc, dev, "add", A, 0.02, 128, B, 0.03, 120, 0.04, 125)
     binary(orc, dev, "mul", A, 0.02, 128, B, 0.03, 120, 0.05, 125)
+
+
+@pytest.mark.parametrize("qt", ["u8", "s8"])
+@pytest.mark.parametrize("bshape", [(), (4096,), (1024, 4096)])
+def test_large_broadcast(orc, dev, qt, bshape):
+    """2^24 outputs: B a single value, a repeating row, or a repeating
+    matrix; both operand types."""
+    rng = np.random.default_rng(len(bshape) + 10 * (qt == "s8"))
+    lo, hi, dt = (0, 256, np.uint8) if qt == "u8" else (-128, 128, np.int8)
+    A = rng.integers(lo, hi, (4, 1024, 4096)).astype(dt)
+    B = rng.integers(lo, hi, bshape).astype(dt)
+    for op in ("add", "mul"):
+        binary(orc, dev, op, A, 0.021, int(rng.integers(lo, hi)), B, 0.033, int(rng.integers(lo, hi)),
+               0.05 if op == "add" else 0.3, int(rng.integers(lo, hi)))
 
 
 @pytest.mark.parametrize("qt", ["u8", "s8"])
