@@ -32,10 +32,16 @@ struct QRange<int8_t> {
 };
 
 // Low byte of the result: the code of x (IEEE division, then saturating
-// round-half-even with the zero point).
+// round-half-even with the zero point).  The quotient is first bounded to
+// [-2^16, 2^16] (beyond every code once the zero point is added; NaN goes
+// to the lower bound), rounded to the nearest integer, ties to even, by
+// adding 1.5 * 2^23, shifted by the zero point and saturated in integers:
+// the same code as saturating rint(q) + zp, without a conversion.
 template <typename QT>
 __device__ __forceinline__ uint32_t quant_one(float x, float s, int zp) {
-  return rint_code_bits(__fdiv_rn(x, s), QRange<QT>::lo - (float)zp, QRange<QT>::hi - (float)zp, zp);
+  const float q = fminf(fmaxf(__fdiv_rn(x, s), -65536.0f), 65536.0f);
+  const int r = __float_as_int(__fadd_rn(q, 12582912.0f)) - 0x4B400000 + zp;
+  return (uint32_t)min(max(r, (int)QRange<QT>::lo), (int)QRange<QT>::hi);
 }
 
 template <typename QT>
@@ -102,6 +108,31 @@ __global__ void __launch_bounds__(256) quantize_warp512(const float* __restrict_
   }
   const float4* x4 = reinterpret_cast<const float4*>(x);
   uint32_t* y32 = reinterpret_cast<uint32_t*>(y);
+  // per tensor, or the last axis when the grid stride is a whole number of
+  // channel cycles: every tile of this warp sees the same parameters
+  if (MODE == AX_TENSOR || (MODE == AX_LAST && c_step == 0)) {
+    float s[4][4];
+    int z[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int off = 128 * q + 4 * lane;
+      params4<MODE, QT>(scale, zp, channel_of<MODE>(w * 512 + off, c_tile, off, axis_len, inner), s[q], z[q]);
+    }
+    for (; w < ntiles; w += wstride) {
+      const int64_t base4 = w * 128;
+      float4 a[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) a[q] = __ldcs(x4 + base4 + 32 * q + lane);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t code =
+            pack_low_bytes(quant_one<QT>(a[q].x, s[q][0], z[q][0]), quant_one<QT>(a[q].y, s[q][1], z[q][1]),
+                           quant_one<QT>(a[q].z, s[q][2], z[q][2]), quant_one<QT>(a[q].w, s[q][3], z[q][3]));
+        __stcs(y32 + base4 + 32 * q + lane, code);
+      }
+    }
+    return;
+  }
   for (; w < ntiles; w += wstride) {
     const int64_t base4 = w * 128;  // tile start in units of 4 elements
     float4 a[4];
