@@ -44,10 +44,12 @@ __device__ __forceinline__ uint32_t quant_one(float x, float s, int zp) {
   return (uint32_t)min(max(r, (int)QRange<QT>::lo), (int)QRange<QT>::hi);
 }
 
+// (x - zp) * s; the difference (|x - zp| <= 255) goes to float exactly
+// through the 1.5 * 2^23 bit pattern instead of a conversion instruction.
 template <typename QT>
 __device__ __forceinline__ float dequant_one(uint32_t byte, float s, int zp) {
-  int v = (int)(QT)(byte & 0xff);
-  return __fmul_rn(__int2float_rn(v - zp), s);
+  const int v = (int)(QT)(byte & 0xff) - zp;
+  return __fmul_rn(__fsub_rn(__int_as_float(0x4B400000 + v), 12582912.0f), s);
 }
 
 template <typename QT>
@@ -173,6 +175,42 @@ __global__ void __launch_bounds__(256) dequantize_warp512(const QT* __restrict__
   // The 8-bit side moves only 4 bytes per lane per access, so four warp
   // tiles (16 loads per lane) are put in flight before any is used.
   constexpr int U = 4;
+  // per tensor, or the last axis when the grid stride is a whole number of
+  // channel cycles: every tile of this warp sees the same parameters
+  if (MODE == AX_TENSOR || (MODE == AX_LAST && c_step == 0)) {
+    float s[4][4];
+    int z[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int off = 128 * q + 4 * lane;
+      params4<MODE, QT>(scale, zp, channel_of<MODE>(w * 512 + off, c_tile, off, axis_len, inner), s[q], z[q]);
+    }
+    for (; w < ntiles; w += U * wstride) {
+      uint32_t in[U][4];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t wu = w + u * wstride;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) in[u][q] = wu < ntiles ? __ldcs(x32 + wu * 128 + 32 * q + lane) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t wu = w + u * wstride;
+        if (wu < ntiles) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float4 o;
+            o.x = dequant_one<QT>(in[u][q], s[q][0], z[q][0]);
+            o.y = dequant_one<QT>(in[u][q] >> 8, s[q][1], z[q][1]);
+            o.z = dequant_one<QT>(in[u][q] >> 16, s[q][2], z[q][2]);
+            o.w = dequant_one<QT>(in[u][q] >> 24, s[q][3], z[q][3]);
+            __stcs(y4 + wu * 128 + 32 * q + lane, o);
+          }
+        }
+      }
+    }
+    return;
+  }
   for (; w < ntiles; w += U * wstride) {
     uint32_t in[U][4];
 #pragma unroll
