@@ -81,6 +81,39 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
   nt = r / gsize;
 }
 
+// Eight dequantized and activated values of a row, columns j .. j + 7 of
+// the slice.
+template <int ACT, bool BF16>
+__device__ __forceinline__ void epi8(const int32_t (&run)[SLICE], int j, int32_t zA, float sA, const int32_t* pc,
+                                     const float* ps, const float* pb, float2 (&o)[4]) {
+  const int4 c0 = *reinterpret_cast<const int4*>(pc + j), c1 = *reinterpret_cast<const int4*>(pc + j + 4);
+  const float4 s0 = *reinterpret_cast<const float4*>(ps + j), s1 = *reinterpret_cast<const float4*>(ps + j + 4);
+  const float4 b0 = *reinterpret_cast<const float4*>(pb + j), b1 = *reinterpret_cast<const float4*>(pb + j + 4);
+  const int32_t cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float2 sb[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
+                        make_float2(s1.z, s1.w)};
+  const float2 bb[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                        make_float2(b1.z, b1.w)};
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    // zA arrives shifted by 128.  Scalar operations: the compiler may
+    // fuse a paired multiply and a following paired add.
+    float2 v = make_float2(__int2float_rn(run[j + 2 * u] - zA * cc[2 * u]),
+                           __int2float_rn(run[j + 2 * u + 1] - zA * cc[2 * u + 1]));
+    v.x = __fadd_rn(__fmul_rn(__fmul_rn(v.x, sA), sb[u].x), bb[u].x);
+    v.y = __fadd_rn(__fmul_rn(__fmul_rn(v.y, sA), sb[u].y), bb[u].y);
+    if constexpr (ACT == I8Q_ACT_RELU) {
+      v = make_float2(v.x > 0.0f ? v.x : 0.0f, v.y > 0.0f ? v.y : 0.0f);
+    } else if constexpr (ACT == I8Q_ACT_GELU) {
+      if constexpr (BF16)
+        v = gelu_bf16out2(v);
+      else
+        v = make_float2(gelu_erf(v.x), gelu_erf(v.y));
+    }
+    o[u] = v;
+  }
+}
+
 // Dequantized values of one row's 64-column slice, eight at a time, as
 // ((float)sum * scaleA) * scaleB + bias (the roundings of dequant_epilogue),
 // then the activation ACT (GELU on pairs for bf16 outputs), then stored as
@@ -93,33 +126,8 @@ __device__ __forceinline__ void store_slice_float(const GemmEpilogue& ep, int64_
                                                   const int32_t* pc, const float* ps, const float* pb, bool vec) {
 #pragma unroll
   for (int j = 0; j < SLICE; j += 8) {
-    const int4 c0 = *reinterpret_cast<const int4*>(pc + j), c1 = *reinterpret_cast<const int4*>(pc + j + 4);
-    const float4 s0 = *reinterpret_cast<const float4*>(ps + j), s1 = *reinterpret_cast<const float4*>(ps + j + 4);
-    const float4 b0 = *reinterpret_cast<const float4*>(pb + j), b1 = *reinterpret_cast<const float4*>(pb + j + 4);
-    const int32_t cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const float2 sb[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
-                          make_float2(s1.z, s1.w)};
-    const float2 bb[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
-                          make_float2(b1.z, b1.w)};
     float2 o[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      // zA arrives shifted by 128.  Scalar operations: the compiler may
-      // fuse a paired multiply and a following paired add.
-      float2 v = make_float2(__int2float_rn(run[j + 2 * u] - zA * cc[2 * u]),
-                             __int2float_rn(run[j + 2 * u + 1] - zA * cc[2 * u + 1]));
-      v.x = __fadd_rn(__fmul_rn(__fmul_rn(v.x, sA), sb[u].x), bb[u].x);
-      v.y = __fadd_rn(__fmul_rn(__fmul_rn(v.y, sA), sb[u].y), bb[u].y);
-      if constexpr (ACT == I8Q_ACT_RELU) {
-        v = make_float2(v.x > 0.0f ? v.x : 0.0f, v.y > 0.0f ? v.y : 0.0f);
-      } else if constexpr (ACT == I8Q_ACT_GELU) {
-        if constexpr (BF16)
-          v = gelu_bf16out2(v);
-        else
-          v = make_float2(gelu_erf(v.x), gelu_erf(v.y));
-      }
-      o[u] = v;
-    }
+    epi8<ACT, BF16>(run, j, zA, sA, pc, ps, pb, o);
     if constexpr (BF16) {
       __nv_bfloat16* C = static_cast<__nv_bfloat16*>(ep.C) + row * ep.ldc + col0 + j;
       __nv_bfloat162 h[4];
@@ -188,6 +196,47 @@ __device__ __forceinline__ void store_slice(const GemmEpilogue& ep, int64_t row,
     else I8Q_SLICE(I8Q_ACT_IDENTITY, false);
   }
 #undef I8Q_SLICE
+}
+
+// The same slice for bf16 outputs, stored by TMA: the warp's 32 rows
+// (row0 .. row0 + 31, lane = row) go out in 16-column chunks through the
+// warp's 1 KB staging buffer (32 rows x 32 bytes, dense), one bulk store
+// per chunk issued by lane 0 once the previous one has read the buffer.
+// Rows and columns past the tensor are clipped by the store itself.
+template <int ACT>
+__device__ __forceinline__ void store_slice_tma(const CUtensorMap* tmC, int64_t M, int64_t N, int64_t row0,
+                                                int64_t col0, int lane, const int32_t (&run)[SLICE], int32_t zA,
+                                                float sA, const int32_t* pc, const float* ps, const float* pb,
+                                                uint8_t* stg) {
+  const uint32_t stg_s = smem_u32(stg);
+#pragma unroll
+  for (int ch = 0; ch < SLICE / 16; ++ch) {
+    uint32_t wd[8];
+#pragma unroll
+    for (int hg = 0; hg < 2; ++hg) {
+      float2 o[4];
+      epi8<ACT, true>(run, ch * 16 + hg * 8, zA, sA, pc, ps, pb, o);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const __nv_bfloat162 hv = __float22bfloat162_rn(o[u]);
+        wd[hg * 4 + u] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+    }
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
+    uint4* d = reinterpret_cast<uint4*>(stg + lane * 32);
+    d[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    d[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      const int64_t x = col0 + ch * 16;
+      if (x < N && row0 < M) {
+        tma_store_2d(tmC, stg_s, (int)x, (int)row0);
+        bulk_commit();
+      }
+    }
+  }
 }
 
 // Epilogue of one row's 64-column slice for the 8-bit-code products (see
@@ -491,7 +540,8 @@ constexpr int P_A_STAGE = HALF_ROWS * BK * 2;  // 16 KB
 constexpr int P_B_STAGE = HALF_ROWS * BK * 2;  // 16 KB
 constexpr int P_STAGE_BYTES = P_A_STAGE + P_B_STAGE;
 constexpr int P_NUM_BARS = 2 * P_STAGES + 4 + 1;
-constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + PARAM_BYTES + P_NUM_BARS * 8 + 16;
+constexpr int P_STG_BYTES = NUM_EPI_WARPS * 1024;  // per-warp staging of bf16 C (32 rows x 32 bytes)
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + PARAM_BYTES + P_STG_BYTES + P_NUM_BARS * 8 + 16;
 constexpr int P_GROUP_M = 8;
 constexpr uint32_t IDESC_PAIR = idesc_bf16(PBM, PBN);
 static_assert(P_SMEM_BYTES <= 227 * 1024, "shared memory of the pair kernel");
@@ -517,13 +567,16 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
   return r;
 }
 
-template <int EPI>
+// TMA_C: bf16 C of EPI_DYN stored by TMA through per-warp staging.
+template <int EPI, bool TMA_C = false>
 __global__ void __launch_bounds__(THREADS, 1)
-gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcParams p) {
+gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* params = smem + P_STAGES * P_STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(params + PARAM_BYTES);
+  uint8_t* stg_all = params + PARAM_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + P_STG_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + P_NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t smem0 = smem_u32(smem);
@@ -714,10 +767,29 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       }
       if (!ok) break;
       __syncwarp();
-      const int64_t row = (int64_t)mt * PBM + (int64_t)rank * HALF_ROWS + q * 32 + lane;
+      const int64_t row0 = (int64_t)mt * PBM + (int64_t)rank * HALF_ROWS + q * 32, row = row0 + lane;
+      if constexpr (EPI == EPI_DYN && TMA_C) {
+        {
+          const bool in = row < p.M;
+          const float sA = in ? __ldg(p.ep.scaleA + row) : 0.0f;
+          const int32_t zA = in ? __ldg(p.ep.zeroA + row) - 128 : 0;  // A entered as uA - 128
+          uint8_t* stg = stg_all + (warp - 2) * 1024;
+          if (p.ep.act == I8Q_ACT_GELU)
+            store_slice_tma<I8Q_ACT_GELU>(&tmC, p.M, p.N, row0, col0, lane, run, zA, sA, pc, ps, pb, stg);
+          else if (p.ep.act == I8Q_ACT_RELU)
+            store_slice_tma<I8Q_ACT_RELU>(&tmC, p.M, p.N, row0, col0, lane, run, zA, sA, pc, ps, pb, stg);
+          else
+            store_slice_tma<I8Q_ACT_IDENTITY>(&tmC, p.M, p.N, row0, col0, lane, run, zA, sA, pc, ps, pb, stg);
+          __syncwarp();
+          continue;
+        }
+      }
       if (row < p.M) finish_row<EPI>(p, row, col0, run, pc, ps, pb, pd);
       __syncwarp();
     }
+    // the bulk stores are complete before the CTA leaves
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -739,6 +811,10 @@ int pair_max_clusters() {
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
     err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+    if constexpr (EPI == EPI_DYN)
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   P_SMEM_BYTES);
     if (err != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -827,7 +903,25 @@ int launch_tc_impl(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     I8Q_PROF(prof2, s);
-    I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI>, pA, pB, p));
+    // bf16 C of the dynamic inner product goes out by TMA when its rows
+    // are 16-byte aligned
+    CUtensorMap pC = pA;
+    bool tma_c = false;
+    if constexpr (EPI == EPI_DYN) {
+      if (p.ep.out_mode == OUT_BF16 && p.ep.ldc % 8 == 0 && (reinterpret_cast<uintptr_t>(p.ep.C) & 15) == 0 &&
+          M < ((int64_t)1 << 31) && N < ((int64_t)1 << 31) && !getenv("I8Q_GEMM_DIRECT_STORE")) {
+        rc = make_map_plain_2d(&pC, p.ep.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, p.ep.ldc * 2, 16, 32, "gemm_tc");
+        if (rc) return rc;
+        tma_c = true;
+      }
+    }
+    if constexpr (EPI == EPI_DYN)
+      if (tma_c) {
+        I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI, true>, pA, pB, pC, p));
+        I8Q_LAUNCH_CHECK("gemm_tc_pair_kernel");
+        return I8Q_OK;
+      }
+    I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI, false>, pA, pB, pC, p));
     I8Q_LAUNCH_CHECK("gemm_tc_pair_kernel");
     return I8Q_OK;
   }
