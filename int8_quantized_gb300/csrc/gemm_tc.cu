@@ -297,6 +297,66 @@ __device__ __forceinline__ void store_slice_qg(const QgEpilogue& qg, int64_t row
   }
 }
 
+// The 8-bit-code products' slice stored by TMA (fp32 Y in 8-column chunks,
+// 8-bit Y in 32-column chunks, 32 bytes per row either way) through the
+// warp's staging buffer, as store_slice_tma.  Rows past M hold zeros in
+// their parameters (never stored: the store clips them).
+__device__ __forceinline__ void store_slice_qg_tma(const QgEpilogue& qg, const CUtensorMap* tmY, int64_t M,
+                                                   int64_t N, int64_t row0, int64_t col0, int lane,
+                                                   const int32_t (&run)[SLICE], int32_t rs, int32_t dr, float ar,
+                                                   const int32_t* pg, const int32_t* pe, const float* pb,
+                                                   const float* pz, uint8_t* stg) {
+  const int64_t row = row0 + lane;
+  const int32_t* crow = (qg.C && row < M) ? qg.C + row * qg.c_si : nullptr;
+  const bool has_bias = qg.bias != nullptr;
+  auto value_at = [&](int j) -> float {
+    uint32_t a = (uint32_t)run[j] + (uint32_t)rs * (uint32_t)pg[j] + (uint32_t)dr * (uint32_t)pe[j];
+    if (crow && col0 + j < N) a += (uint32_t)__ldg(crow + (col0 + j) * qg.c_sj);
+    float v = __fmul_rn(__int2float_rn((int32_t)a), __fmul_rn(ar, pb[j]));
+    if (has_bias) v = __fadd_rn(v, pz[j]);
+    return v;
+  };
+  const uint32_t stg_s = smem_u32(stg);
+  auto put = [&](const uint32_t (&wd)[8], int64_t x) {
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
+    uint4* d = reinterpret_cast<uint4*>(stg + lane * 32);
+    d[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    d[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    __syncwarp();
+    if (lane == 0 && x < N && row0 < M) {
+      tma_store_2d(tmY, stg_s, (int)x, (int)row0);
+      bulk_commit();
+    }
+  };
+  if (qg.ytype == I8Q_F32) {
+#pragma unroll
+    for (int j = 0; j < SLICE; j += 8) {
+      uint32_t wd[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) wd[u] = __float_as_uint(value_at(j + u));
+      put(wd, col0 + j);
+    }
+    return;
+  }
+  const int zp = qg.y_zero_point;
+  const float lo = (qg.ytype == I8Q_U8 ? 0.0f : -128.0f) - (float)zp;
+  const float hi = (qg.ytype == I8Q_U8 ? 255.0f : 127.0f) - (float)zp;
+#pragma unroll
+  for (int j = 0; j < SLICE; j += 32) {
+    uint32_t wd[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      uint32_t b[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) b[u] = rint_code_bits(__fdiv_rn(value_at(j + 4 * w + u), qg.y_scale), lo, hi, zp);
+      wd[w] = pack_low_bytes(b[0], b[1], b[2], b[3]);
+    }
+    put(wd, col0 + j);
+  }
+}
+
 // Stage one epilogue warp's column parameters for the tile (read back after
 // the K loop).
 template <int EPI>
@@ -768,6 +828,16 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       if (!ok) break;
       __syncwarp();
       const int64_t row0 = (int64_t)mt * PBM + (int64_t)rank * HALF_ROWS + q * 32, row = row0 + lane;
+      if constexpr (EPI == EPI_QG && TMA_C) {
+        const bool in = row < p.M;
+        const int32_t rs = in ? __ldg(p.qg.rowsum + row) : 0;
+        const int32_t dr = in ? __ldg(p.qg.d + row * p.qg.d_stride) : 0;
+        const float ar = in ? __ldg(p.qg.asc + row * p.qg.asc_stride) : 0.0f;
+        store_slice_qg_tma(p.qg, &tmC, p.M, p.N, row0, col0, lane, run, rs, dr, ar, pc,
+                           reinterpret_cast<const int32_t*>(ps), pb, pd, stg_all + (warp - 2) * 1024);
+        __syncwarp();
+        continue;
+      }
       if constexpr (EPI == EPI_DYN && TMA_C) {
         {
           const bool in = row < p.M;
@@ -811,10 +881,9 @@ int pair_max_clusters() {
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
     err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
-    if constexpr (EPI == EPI_DYN)
-      if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   P_SMEM_BYTES);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 P_SMEM_BYTES);
     if (err != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -915,12 +984,23 @@ int launch_tc_impl(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M,
         tma_c = true;
       }
     }
-    if constexpr (EPI == EPI_DYN)
-      if (tma_c) {
-        I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI, true>, pA, pB, pC, p));
-        I8Q_LAUNCH_CHECK("gemm_tc_pair_kernel");
-        return I8Q_OK;
+    if constexpr (EPI == EPI_QG) {
+      // fp32 or 8-bit Y of the 8-bit-code products, likewise
+      const int esz = p.qg.ytype == I8Q_F32 ? 4 : 1;
+      if ((p.qg.ldy * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.qg.Y) & 15) == 0 && M < ((int64_t)1 << 31) &&
+          N < ((int64_t)1 << 31) && !getenv("I8Q_GEMM_DIRECT_STORE")) {
+        rc = make_map_plain_2d(&pC, p.qg.Y,
+                               esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT8, N, M,
+                               p.qg.ldy * esz, 32 / esz, 32, "gemm_tc");
+        if (rc) return rc;
+        tma_c = true;
       }
+    }
+    if (tma_c) {
+      I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI, true>, pA, pB, pC, p));
+      I8Q_LAUNCH_CHECK("gemm_tc_pair_kernel");
+      return I8Q_OK;
+    }
     I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI, false>, pA, pB, pC, p));
     I8Q_LAUNCH_CHECK("gemm_tc_pair_kernel");
     return I8Q_OK;
