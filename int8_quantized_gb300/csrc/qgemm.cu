@@ -139,10 +139,19 @@ __global__ void __launch_bounds__(256) tensor_range(const float* __restrict__ x,
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
     const int64_t n4 = n / 4;
-    for (int64_t i = t; i < n4; i += stride) {
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(x) + i);
-      mx = fmaxf(fmaxf(mx, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
-      nmn = fmaxf(fmaxf(nmn, fmaxf(-v.x, -v.y)), fmaxf(-v.z, -v.w));
+    // four 16-byte loads per thread in flight
+    for (int64_t i0 = t; i0 < n4; i0 += 4 * stride) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t i = i0 + u * stride;
+        v[u] = i < n4 ? __ldcs(reinterpret_cast<const float4*>(x) + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        mx = fmaxf(fmaxf(mx, fmaxf(v[u].x, v[u].y)), fmaxf(v[u].z, v[u].w));
+        nmn = fmaxf(fmaxf(nmn, fmaxf(-v[u].x, -v[u].y)), fmaxf(-v[u].z, -v[u].w));
+      }
     }
     for (int64_t i = n4 * 4 + t; i < n; i += stride) {
       mx = fmaxf(mx, x[i]);
@@ -159,7 +168,19 @@ __global__ void __launch_bounds__(256) tensor_range(const float* __restrict__ x,
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     nmn = fmaxf(nmn, __shfl_xor_sync(0xffffffffu, nmn, o));
   }
+  // one merge per block: atomics on a single word serialize
+  __shared__ float red[2][8];
+  const int warp = threadIdx.x >> 5;
   if ((threadIdx.x & 31) == 0) {
+    red[0][warp] = nmn;
+    red[1][warp] = mx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+      nmn = fmaxf(nmn, red[0][w]);
+      mx = fmaxf(mx, red[1][w]);
+    }
     atomicMax(mm, __float_as_uint(nmn));
     atomicMax(mm + 1, __float_as_uint(mx));
   }
@@ -192,20 +213,49 @@ quantize_tensor_center(const float* __restrict__ A, int64_t M, int64_t K, int64_
   const float* a = A + row * K;
   __nv_bfloat16* out = Ac + row * Kp;
   int part = 0;
-  for (int64_t k0 = (int64_t)lane * 8; k0 < Kp; k0 += 256) {
+  // bf16 bits of a code - 128 (exact small integer) from its fp32 image
+  auto bits = [](int c) { return __float_as_uint(__fsub_rn(__int_as_float(0x4B400000 + c), 12582912.0f)); };
+  auto emit = [&](int64_t k0, const float (&v)[8]) {
     uint32_t w[4];
 #pragma unroll
     for (int e2 = 0; e2 < 4; ++e2) {
       int c[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int64_t k = k0 + 2 * e2 + h;
-        c[h] = k < K ? (int)(row_code(a[k], sc, lo_z, hi_z, z)) - 128 : 0;
+        c[h] = k0 + 2 * e2 + h < K ? (int)(row_code(v[2 * e2 + h], sc, lo_z, hi_z, z)) - 128 : 0;
         part += c[h];
       }
-      w[e2] = (__float_as_uint((float)c[0]) >> 16) | (__float_as_uint((float)c[1]) & 0xffff0000u);
+      w[e2] = (bits(c[0]) >> 16) | (bits(c[1]) & 0xffff0000u);
     }
     *reinterpret_cast<uint4*>(out + k0) = make_uint4(w[0], w[1], w[2], w[3]);
+  };
+  const bool vec = K % 8 == 0 && (reinterpret_cast<uintptr_t>(A) & 15) == 0;
+  if (vec) {
+    // two 8-element groups per lane in flight (four 16-byte loads)
+    for (int64_t k0 = (int64_t)lane * 8; k0 < Kp; k0 += 512) {
+      float v[2][8];
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int64_t k = k0 + 256 * g;
+        float4 x0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), x1 = x0;
+        if (k < K) {
+          x0 = __ldcs(reinterpret_cast<const float4*>(a + k));
+          x1 = __ldcs(reinterpret_cast<const float4*>(a + k + 4));
+        }
+        v[g][0] = x0.x; v[g][1] = x0.y; v[g][2] = x0.z; v[g][3] = x0.w;
+        v[g][4] = x1.x; v[g][5] = x1.y; v[g][6] = x1.z; v[g][7] = x1.w;
+      }
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+        if (k0 + 256 * g < Kp) emit(k0 + 256 * g, v[g]);
+    }
+  } else {
+    for (int64_t k0 = (int64_t)lane * 8; k0 < Kp; k0 += 256) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = k0 + e < K ? a[k0 + e] : 0.0f;
+      emit(k0, v);
+    }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
