@@ -117,22 +117,34 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
+      // counters instead of division: stage st / round parity ph, and the
+      // K step's 64-channel slab cch, filter column kw and row kh
       int it = 0;
+      uint32_t st = 0, ph = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         int mt, rg, n;
         conv_tile_coords(tile, p, mt, rg, n);
+        int cch = 0, kw = 0, kh = 0;
         for (int kt = 0; kt < KT; ++kt, ++it) {
-          const int s = it % STAGES;
-          if (!wait_bar(empty(s), ((uint32_t)(it / STAGES) & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT_PRODUCER)) {
+          if (!wait_bar(empty(st), ph ^ 1u, abort_flag, p.status, ST_TIMEOUT_PRODUCER)) {
             ok = false;
             break;
           }
-          const int tap = kt / p.CC, cch = kt - tap * p.CC;
-          const int kh = tap / p.kW, kw = tap - kh * p.kW;
-          mbar_arrive_expect_tx(full(s), T::STAGE_BYTES);
-          tma_load_2d(sA(s), &tmW, full(s), kt * BK, mt * BM);
-          tma_load_4d(sB(s), &tmX, full(s), cch * BK, kw - p.pl, rg * p.R + kh - p.pt, n);
+          mbar_arrive_expect_tx(full(st), T::STAGE_BYTES);
+          tma_load_2d(sA(st), &tmW, full(st), kt * BK, mt * BM);
+          tma_load_4d(sB(st), &tmX, full(st), cch * BK, kw - p.pl, rg * p.R + kh - p.pt, n);
+          if (++cch == p.CC) {
+            cch = 0;
+            if (++kw == p.kW) {
+              kw = 0;
+              ++kh;
+            }
+          }
+          if (++st == (uint32_t)STAGES) {
+            st = 0;
+            ph ^= 1u;
+          }
         }
       }
       if (!ok) {
@@ -149,12 +161,16 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      int it = 0, chunk = 0;
+      // counters instead of division; descriptors advanced by addition
+      // (start address >> 4)
+      const uint64_t adesc0 = desc_sw128(sA(0)), bdesc0 = desc_sw128(sB(0));
+      uint32_t st = 0, ph = 0;
+      int chunk = 0;
       bool ok = true;
       uint32_t d = tmem_base;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        for (int kt = 0; kt < KT; ++kt, ++it) {
-          const int kc = kt % CS;
+        int kc = 0;
+        for (int kt = 0; kt < KT; ++kt) {
           if (kc == 0) {
             const int b = chunk & 1;
             if (!wait_bar(acce(b), ((uint32_t)(chunk >> 1) & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT_MMA)) {
@@ -164,22 +180,26 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             tc_fence_after();
             d = tmem_base + (uint32_t)(b * TN);
           }
-          const int s = it % STAGES;
-          if (!wait_bar(full(s), (uint32_t)(it / STAGES) & 1u, abort_flag, p.status, ST_TIMEOUT_MMA)) {
+          if (!wait_bar(full(st), ph, abort_flag, p.status, ST_TIMEOUT_MMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const uint64_t soff = (uint64_t)((st * (uint32_t)T::STAGE_BYTES) >> 4);
+          const uint32_t acc = kc == 0 ? 0u : 1u;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = desc_sw128(sA(s) + (uint32_t)(k * 32));
-            const uint64_t bd = desc_sw128(sB(s) + (uint32_t)(k * 32));
-            tc_mma(d, ad, bd, IDESC, (kc == 0 && k == 0) ? 0u : 1u);
-          }
-          tc_commit(empty(s));
-          if (kc == CS - 1 || kt == KT - 1) {
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma(d, adesc0 + soff + (uint64_t)(2 * k), bdesc0 + soff + (uint64_t)(2 * k), IDESC,
+                   (k == 0) ? acc : 1u);
+          tc_commit(empty(st));
+          if (++kc == CS || kt == KT - 1) {
             tc_commit(accf(chunk & 1));
             ++chunk;
+            kc = 0;
+          }
+          if (++st == (uint32_t)STAGES) {
+            st = 0;
+            ph ^= 1u;
           }
         }
       }
