@@ -19,6 +19,8 @@
 //   y = saturate(rint(((float)(acc + B[m]) * (x_scale * w_scale[m])) / y_scale) + y_zero_point),
 // and stores NCHW bytes: thread = output channel, its slice = consecutive
 // pixels of one output row.
+#include <type_traits>
+
 #include "tcgen05.cuh"
 
 namespace i8q {
@@ -351,27 +353,39 @@ center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv
   const int ld = Cp + 2;
   const XT* xr = x + ((int64_t)n * C * H + h) * W;  // + c * H * W + w
   if ((W & 7) == 0 && ((int64_t)H * W) % 8 == 0 && (reinterpret_cast<uintptr_t>(xr) & 7) == 0) {
-    // 8-byte pieces of the channel rows, eight loads in flight per thread
-    const int cw = W / 8, total = Cp * cw;
-    for (int base = 0; base < total; base += 8 * blockDim.x) {
-      uint2 v[8];
-      int cc[8], ww[8];
+    // 8-byte pieces of two adjacent channel rows per work item (their codes
+    // meet in 32-bit shared stores), four items in flight per thread
+    const int cw = W / 8, pairs = Cp / 2, total = pairs * cw;
+    const uint32_t flip = std::is_signed<XT>::value ? 0x80808080u : 0u;  // signed codes as unsigned + 128
+    const int xzu = std::is_signed<XT>::value ? xz + 128 : xz;
+    uint32_t* rw = reinterpret_cast<uint32_t*>(rowt);
+    for (int base = 0; base < total; base += 4 * blockDim.x) {
+      uint2 v[4][2];
+      int cp[4], ww[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 4; ++u) {
         const int idx = base + threadIdx.x + u * blockDim.x;
-        cc[u] = idx < total ? idx / cw : Cp;
-        ww[u] = (idx - cc[u] * cw) * 8;
-        v[u] = (idx < total && cc[u] < C) ? __ldg(reinterpret_cast<const uint2*>(xr + (int64_t)cc[u] * H * W + ww[u]))
-                                          : make_uint2(0, 0);
+        cp[u] = idx < total ? idx / cw : pairs;
+        ww[u] = (idx - cp[u] * cw) * 8;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int c = 2 * cp[u] + h2;
+          v[u][h2] = (idx < total && c < C) ? __ldg(reinterpret_cast<const uint2*>(xr + (int64_t)c * H * W + ww[u]))
+                                            : make_uint2(0, 0);
+        }
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (cc[u] >= Cp) continue;
-        const uint32_t wd[2] = {v[u].x, v[u].y};
+      for (int u = 0; u < 4; ++u) {
+        if (cp[u] >= pairs) continue;
+        const bool in0 = 2 * cp[u] < C, in1 = 2 * cp[u] + 1 < C;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float f = cc[u] < C ? (float)((int)(XT)((wd[e >> 2] >> (8 * (e & 3))) & 0xff) - xz) : 0.0f;
-          rowt[(ww[u] + e) * ld + cc[u]] = (uint16_t)(__float_as_uint(f) >> 16);  // exact: |f| <= 255
+          const uint32_t b0 = ((e < 4 ? v[u][0].x : v[u][0].y) ^ flip) >> (8 * (e & 3)) & 0xffu;
+          const uint32_t b1 = ((e < 4 ? v[u][1].x : v[u][1].y) ^ flip) >> (8 * (e & 3)) & 0xffu;
+          // x - xz as fp32 through the 1.5 * 2^23 bit pattern (exact: |x - xz| <= 255); bf16 = top half
+          const uint32_t f0 = in0 ? __float_as_uint(__fsub_rn(__int_as_float(0x4B400000 + (int)b0 - xzu), 12582912.0f)) : 0u;
+          const uint32_t f1 = in1 ? __float_as_uint(__fsub_rn(__int_as_float(0x4B400000 + (int)b1 - xzu), 12582912.0f)) : 0u;
+          rw[((ww[u] + e) * ld + 2 * cp[u]) >> 1] = (f0 >> 16) | (f1 & 0xffff0000u);
         }
       }
     }
