@@ -195,9 +195,12 @@ struct i8q_qgemm_ctx {
   float* biasv = nullptr;
   void* fallback = nullptr;
   size_t internal_bytes = 0;
-  // host staging of forward_host
+  // host staging of forward_host, and its upload / compute / download
+  // streams with per-chunk events (created on first use)
   void* stage = nullptr;
   size_t stage_bytes = 0;
+  cudaStream_t pipe[3] = {nullptr, nullptr, nullptr};
+  cudaEvent_t ev_in[16] = {}, ev_out[16] = {}, ev_start = nullptr;
   std::string info;
 };
 
@@ -240,6 +243,13 @@ void free_ctx_buffers(i8q_qgemm_ctx* c) {
   cudaFree(c->biasv);
   cudaFree(c->fallback);
   cudaFree(c->stage);
+  for (auto& st : c->pipe)
+    if (st) cudaStreamDestroy(st), st = nullptr;
+  for (auto& e : c->ev_in)
+    if (e) cudaEventDestroy(e), e = nullptr;
+  for (auto& e : c->ev_out)
+    if (e) cudaEventDestroy(e), e = nullptr;
+  if (c->ev_start) cudaEventDestroy(c->ev_start), c->ev_start = nullptr;
   c->iBt = nullptr;
   c->iBt_bf16 = nullptr;
   c->scaleB = nullptr;
@@ -416,7 +426,11 @@ extern "C" int i8q_qgemm_dyn_set_params(i8q_qgemm_ctx* ctx, const void* weight, 
 
 namespace {
 
-int forward_impl(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf, void* C, int out_mode, cudaStream_t s) {
+// Forward of rows row0 .. row0 + rows - 1 (all rows by default): A and C
+// point at the first of them; their row quantization goes to the same rows
+// of buf.
+int forward_impl(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf, void* C, int out_mode, cudaStream_t s,
+                 int64_t row0 = 0, int64_t rows = -1) {
   if (!ctx) return fail(I8Q_ERR_NOT_INITIALIZED, "qgemm_dyn_forward: no context");
   if (!ctx->params_set) return fail(I8Q_ERR_NOT_INITIALIZED, "qgemm_dyn_forward: SetParams was not called");
   if (!A || !C) return fail(I8Q_ERR_INVALID_ARG, "qgemm_dyn_forward: A and C are required");
@@ -424,11 +438,11 @@ int forward_impl(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf, vo
   uint8_t* base = static_cast<uint8_t*>(buf ? buf : ctx->fallback);
   if (reinterpret_cast<uintptr_t>(base) & 255) return fail(I8Q_ERR_INVALID_ARG, "qgemm_dyn_forward: buf must be 256-byte aligned");
   const BufLayout L = buf_layout(ctx);
-  uint8_t* uA = base + L.uA;
-  __nv_bfloat16* uA_bf16 = ctx->use_tc ? reinterpret_cast<__nv_bfloat16*>(base + L.uA_bf16) : nullptr;
-  float* scaleA = reinterpret_cast<float*>(base + L.scaleA);
-  int32_t* zeroA = reinterpret_cast<int32_t*>(base + L.zeroA);
-  const int64_t M = (int64_t)ctx->M, N = (int64_t)ctx->N, K = (int64_t)ctx->K;
+  uint8_t* uA = base + L.uA + row0 * ctx->Kp;
+  __nv_bfloat16* uA_bf16 = ctx->use_tc ? reinterpret_cast<__nv_bfloat16*>(base + L.uA_bf16) + row0 * ctx->Kp : nullptr;
+  float* scaleA = reinterpret_cast<float*>(base + L.scaleA) + row0;
+  int32_t* zeroA = reinterpret_cast<int32_t*>(base + L.zeroA) + row0;
+  const int64_t M = rows < 0 ? (int64_t)ctx->M : rows, N = (int64_t)ctx->N, K = (int64_t)ctx->K;
   const bool small = ctx->core == CORE_SMALL;
   int rc = I8Q_OK;
   if (!small) {
@@ -504,11 +518,55 @@ extern "C" int i8q_qgemm_dyn_forward_host(i8q_qgemm_ctx* ctx, const void* A_host
   cudaStream_t s = as_stream(stream);
   uint8_t* dA = static_cast<uint8_t*>(ctx->stage);
   uint8_t* dC = dA + a256(a_bytes);
-  I8Q_CUDA_TRY(cudaMemcpyAsync(dA, A_host, a_bytes, cudaMemcpyHostToDevice, s));
-  int rc = i8q_qgemm_dyn_forward(ctx, dA, nullptr, nullptr, dC, stream);
-  if (rc) return rc;
-  I8Q_CUDA_TRY(cudaMemcpyAsync(C_host, dC, c_bytes, cudaMemcpyDeviceToHost, s));
-  I8Q_CUDA_TRY(cudaStreamSynchronize(s));
+  // Rows are independent (A is quantized per row, B is constant), so the
+  // call runs as a pipeline over row chunks: chunk i computes while chunk
+  // i + 1 is uploaded and chunk i - 1 downloaded, on three streams of the
+  // context ordered by events; it still returns only when C_host is filled.
+  const int64_t M = (int64_t)ctx->M;
+  const int nch = (int)std::max<int64_t>(1, std::min<int64_t>(8, M / 1024));
+  if (nch == 1) {
+    I8Q_CUDA_TRY(cudaMemcpyAsync(dA, A_host, a_bytes, cudaMemcpyHostToDevice, s));
+    int rc = i8q_qgemm_dyn_forward(ctx, dA, nullptr, nullptr, dC, stream);
+    if (rc) return rc;
+    I8Q_CUDA_TRY(cudaMemcpyAsync(C_host, dC, c_bytes, cudaMemcpyDeviceToHost, s));
+    I8Q_CUDA_TRY(cudaStreamSynchronize(s));
+    return I8Q_OK;
+  }
+  for (auto& st : ctx->pipe)
+    if (!st) I8Q_CUDA_TRY(cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking));
+  for (int i = 0; i < nch; ++i) {
+    if (!ctx->ev_in[i]) I8Q_CUDA_TRY(cudaEventCreateWithFlags(&ctx->ev_in[i], cudaEventDisableTiming));
+    if (!ctx->ev_out[i]) I8Q_CUDA_TRY(cudaEventCreateWithFlags(&ctx->ev_out[i], cudaEventDisableTiming));
+  }
+  if (!ctx->ev_start) I8Q_CUDA_TRY(cudaEventCreateWithFlags(&ctx->ev_start, cudaEventDisableTiming));
+  // work already queued on the caller's stream comes first
+  I8Q_CUDA_TRY(cudaEventRecord(ctx->ev_start, s));
+  for (auto st : ctx->pipe) I8Q_CUDA_TRY(cudaStreamWaitEvent(st, ctx->ev_start, 0));
+  const size_t a_row = a_bytes / M, c_row = c_bytes / M;
+  const int out_mode = ctx->typeC == I8Q_BF16 ? OUT_BF16 : OUT_F32;
+  const int64_t per = (M + nch - 1) / nch;
+  for (int i = 0; i < nch; ++i) {
+    const int64_t r0 = i * per, rows = std::min<int64_t>(per, M - r0);
+    if (rows <= 0) break;
+    I8Q_CUDA_TRY(cudaMemcpyAsync(dA + r0 * a_row, static_cast<const uint8_t*>(A_host) + r0 * a_row, rows * a_row,
+                                 cudaMemcpyHostToDevice, ctx->pipe[0]));
+    I8Q_CUDA_TRY(cudaEventRecord(ctx->ev_in[i], ctx->pipe[0]));
+    I8Q_CUDA_TRY(cudaStreamWaitEvent(ctx->pipe[1], ctx->ev_in[i], 0));
+    int rc = forward_impl(ctx, dA + r0 * a_row, nullptr, nullptr, dC + r0 * c_row, out_mode, ctx->pipe[1], r0, rows);
+    if (rc) {
+      cudaStreamSynchronize(ctx->pipe[0]);
+      cudaStreamSynchronize(ctx->pipe[1]);
+      cudaStreamSynchronize(ctx->pipe[2]);
+      return rc;
+    }
+    I8Q_CUDA_TRY(cudaEventRecord(ctx->ev_out[i], ctx->pipe[1]));
+    I8Q_CUDA_TRY(cudaStreamWaitEvent(ctx->pipe[2], ctx->ev_out[i], 0));
+    I8Q_CUDA_TRY(cudaMemcpyAsync(static_cast<uint8_t*>(C_host) + r0 * c_row, dC + r0 * c_row, rows * c_row,
+                                 cudaMemcpyDeviceToHost, ctx->pipe[2]));
+  }
+  I8Q_CUDA_TRY(cudaStreamSynchronize(ctx->pipe[0]));
+  I8Q_CUDA_TRY(cudaStreamSynchronize(ctx->pipe[1]));
+  I8Q_CUDA_TRY(cudaStreamSynchronize(ctx->pipe[2]));
   return I8Q_OK;
 }
 

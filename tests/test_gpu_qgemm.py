@@ -286,6 +286,33 @@ def test_forward_host_buffers(orc, dev):
     ctx.clear()
 
 
+@pytest.mark.parametrize("M", [2048, 5000])
+def test_forward_host_pipelined_rows(orc, dev, M):
+    """Large host-buffer calls run as a pipeline over row chunks (the last
+    one ragged at M=5000): the result equals the device-buffer Forward bit
+    for bit, and the oracle on sampled rows."""
+    rng = np.random.default_rng(M)
+    K, N = 384, 520
+    A = workloads.bf16_bits(rng.normal(0, 1, (M, K)).astype(np.float32))
+    iB = rng.integers(-128, 128, (K, N)).astype(np.int8)
+    sB = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+    bias = rng.normal(0, 0.02, N).astype(np.float32)
+    ctx = q.QGemmDyn(M, N, K, q.BF16, q.S8, q.BF16, constB=True, bias=True, activation=q.ACT_GELU)
+    ctx.set_params(_t(iB, dev), _t(sB, dev), _t(bias, dev))
+    Ah = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Ch = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    ctx.forward_host(Ah, Ch)
+    Cd = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    ctx.forward(Ah.to(dev), Cd)
+    q.sync_status()
+    assert torch.equal(Ch.view(torch.int16), Cd.cpu().view(torch.int16))
+    rows = np.array([0, 1, 1023, 1024, M // 2, M - 2, M - 1])
+    ref = orc.dynamic_quantized_inner_product(A[rows], iB=iB, scaleB=sB, bias=bias, act=orc.ACT_GELU, typeC="bf16")
+    d = bf16_ulp_distance(Ch.view(torch.int16).numpy().view(np.uint16)[rows], ref["C"])
+    assert d.max() <= 1
+    ctx.clear()
+
+
 SAMPLE_ROWS = np.array([0, 1, 2, 777, 1024, 3000, 4095, 4096, 5001, 6666, 8190, 8191])
 
 
