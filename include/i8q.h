@@ -167,11 +167,17 @@ int i8q_qgemm_dyn_set_params(i8q_qgemm_ctx* ctx, const void* weight, const float
 int i8q_qgemm_dyn_forward(i8q_qgemm_ctx* ctx, const void* A, const void* B, void* buf, void* C,
                           void* stream);
 
-/* Same as Forward, but A and C are HOST pointers (pinned or pageable): A is
- * copied to context-owned device staging memory, the product runs, and C is
- * copied back, all on `stream`; returns after C is in host memory.  Not on
- * the pages: it is the whole host-to-host path of Forward for callers that
- * keep their tensors in host memory.  B must be NULL (constB contexts). */
+/* Same as Forward, but A and C are HOST pointers (pinned for asynchronous
+ * copies, or pageable): A is copied to context-owned device staging memory,
+ * the product runs, and C is copied back; returns after C is in host
+ * memory.  Work already queued on `stream` runs first.  With M >= 2048 the
+ * call is pipelined over up to 8 row chunks (rows are independent: A is
+ * quantized per row and B is constant) on streams owned by the context, so
+ * one chunk's upload, another's product and a third's download overlap;
+ * results are those of Forward, bit for bit.  Not on the pages: it is the
+ * whole host-to-host path of Forward for callers that keep their tensors in
+ * host memory.  B must be NULL (constB contexts).  Calls on one context must
+ * not overlap. */
 int i8q_qgemm_dyn_forward_host(i8q_qgemm_ctx* ctx, const void* A_host, void* C_host, void* stream);
 
 /* Test hook, not on the pages: run Forward's quantization and integer
