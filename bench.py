@@ -533,10 +533,25 @@ def run_i8q(args):
     barrier(world)
     q_secs = reduce_max(time_loop(qstep, args.steps, stream), world)
     dq_secs = reduce_max(time_loop(dstep, args.steps, stream), world)
+    # the per-tensor variant: int8 codes, scale 0.02, zero point 0
+    s1 = torch.tensor([float(d["s8_scale"])], dtype=torch.float32, device=dev)
+    z1 = torch.tensor([int(d["s8_zero_point"])], dtype=torch.int8, device=dev)
+    y8 = torch.empty(QDQ_SHAPE, dtype=torch.int8, device=dev)
+    q8step = lambda: q.quantize_linear(x, s1, z1, y8)  # noqa: E731
+    d8step = lambda: q.dequantize_linear(y8, s1, z1, xr)  # noqa: E731
+    for _ in range(args.warmup):
+        q8step()
+        d8step()
+    torch.cuda.synchronize()
+    barrier(world)
+    q8_secs = reduce_max(time_loop(q8step, args.steps, stream), world)
+    dq8_secs = reduce_max(time_loop(d8step, args.steps, stream), world)
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     q_gbs = weak_scaling_value(5.0 * nel, args.steps, world, q_secs) / 1e9
     dq_gbs = weak_scaling_value(5.0 * nel, args.steps, world, dq_secs) / 1e9
-    del x, y, xr
+    q8_gbs = weak_scaling_value(5.0 * nel, args.steps, world, q8_secs) / 1e9
+    dq8_gbs = weak_scaling_value(5.0 * nel, args.steps, world, dq8_secs) / 1e9
+    del x, y, xr, y8
 
     rows = {} if args.no_rows else measure_rows(args, dev, stream, world)
 
@@ -568,6 +583,14 @@ def run_i8q(args):
             "dequantize_linear": {"value": dq_gbs, "unit": "GB/s", "ms": dq_secs / args.steps * 1e3,
                                   "frac_hbm": dq_gbs / world / hbm, "frac_8tbs": dq_gbs / world / 8000.0,
                                   "bytes": 5 * nel, "workload": "uint8 [32,1024,4096] per-axis(2) -> fp32"},
+            "quantize_linear_s8_per_tensor": {
+                "value": q8_gbs, "unit": "GB/s", "ms": q8_secs / args.steps * 1e3,
+                "frac_hbm": q8_gbs / world / hbm, "frac_8tbs": q8_gbs / world / 8000.0, "bytes": 5 * nel,
+                "workload": "x fp32 [32,1024,4096] per-tensor scale 0.02, zero point 0 -> int8"},
+            "dequantize_linear_s8_per_tensor": {
+                "value": dq8_gbs, "unit": "GB/s", "ms": dq8_secs / args.steps * 1e3,
+                "frac_hbm": dq8_gbs / world / hbm, "frac_8tbs": dq8_gbs / world / 8000.0, "bytes": 5 * nel,
+                "workload": "int8 [32,1024,4096] per-tensor scale 0.02, zero point 0 -> fp32"},
             "kernels": {k: {"launches": v[0], "ms": v[1] / max(v[0], 1)} for k, v in prof.items()},
             "rows": rows,
             "gpu_launches": launches,

@@ -15,6 +15,8 @@
 // tile instead of dividing.
 #include "common.cuh"
 
+#include <numeric>
+
 namespace i8q {
 namespace {
 
@@ -96,6 +98,58 @@ __device__ __forceinline__ int64_t channel_of(int64_t e, int64_t c_tile, int off
   return c % axis_len;
 }
 
+// Per tensor, or the last axis with a grid stride of whole channel cycles:
+// every tile of a warp sees the same parameters, so they are loaded once and
+// held in registers.  On the last axis those are 16 channels' worth, which
+// leaves room for 3 blocks per SM; two warp tiles are then loaded before
+// either is used, to keep enough reads in flight.  Per tensor, one scalar
+// pair leaves room for 6 blocks per SM, enough with one tile.
+template <int MODE, typename QT>
+__global__ void __launch_bounds__(256) quantize_fixed(const float* __restrict__ x, QT* __restrict__ y, int64_t ntiles,
+                                                     const float* __restrict__ scale, const QT* __restrict__ zp,
+                                                     int64_t axis_len) {
+  static_assert(MODE == AX_TENSOR || MODE == AX_LAST, "fixed parameters: per tensor or the last axis");
+  constexpr int U = MODE == AX_TENSOR ? 1 : 2;
+  const int lane = threadIdx.x & 31;
+  const int64_t wstride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t c_tile = MODE == AX_LAST ? (w * 512) % axis_len : 0;
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  uint32_t* y32 = reinterpret_cast<uint32_t*>(y);
+  float s[4][4];
+  int z[4][4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int off = 128 * q + 4 * lane;
+    params4<MODE, QT>(scale, zp, channel_of<MODE>(w * 512 + off, c_tile, off, axis_len, 1), s[q], z[q]);
+  }
+  for (; w < ntiles; w += U * wstride) {
+    float4 a[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t wu = w + u * wstride;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        a[u][q] = wu < ntiles ? __ldcs(x4 + wu * 128 + 32 * q + lane) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t wu = w + u * wstride;
+      if (wu < ntiles) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t code =
+              pack_low_bytes(quant_one<QT>(a[u][q].x, s[q][0], z[q][0]), quant_one<QT>(a[u][q].y, s[q][1], z[q][1]),
+                             quant_one<QT>(a[u][q].z, s[q][2], z[q][2]), quant_one<QT>(a[u][q].w, s[q][3], z[q][3]));
+          __stcs(y32 + wu * 128 + 32 * q + lane, code);
+        }
+      }
+    }
+  }
+}
+
+// Per-axis parameters that change from tile to tile (the last axis with a
+// grid stride that is not whole channel cycles, or an inner axis).
 template <int MODE, typename QT>
 __global__ void __launch_bounds__(256) quantize_warp512(const float* __restrict__ x, QT* __restrict__ y,
                                                         int64_t ntiles, const float* __restrict__ scale,
@@ -110,31 +164,6 @@ __global__ void __launch_bounds__(256) quantize_warp512(const float* __restrict_
   }
   const float4* x4 = reinterpret_cast<const float4*>(x);
   uint32_t* y32 = reinterpret_cast<uint32_t*>(y);
-  // per tensor, or the last axis when the grid stride is a whole number of
-  // channel cycles: every tile of this warp sees the same parameters
-  if (MODE == AX_TENSOR || (MODE == AX_LAST && c_step == 0)) {
-    float s[4][4];
-    int z[4][4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int off = 128 * q + 4 * lane;
-      params4<MODE, QT>(scale, zp, channel_of<MODE>(w * 512 + off, c_tile, off, axis_len, inner), s[q], z[q]);
-    }
-    for (; w < ntiles; w += wstride) {
-      const int64_t base4 = w * 128;
-      float4 a[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) a[q] = __ldcs(x4 + base4 + 32 * q + lane);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t code =
-            pack_low_bytes(quant_one<QT>(a[q].x, s[q][0], z[q][0]), quant_one<QT>(a[q].y, s[q][1], z[q][1]),
-                           quant_one<QT>(a[q].z, s[q][2], z[q][2]), quant_one<QT>(a[q].w, s[q][3], z[q][3]));
-        __stcs(y32 + base4 + 32 * q + lane, code);
-      }
-    }
-    return;
-  }
   for (; w < ntiles; w += wstride) {
     const int64_t base4 = w * 128;  // tile start in units of 4 elements
     float4 a[4];
@@ -300,6 +329,13 @@ int make_view(const int64_t* shape, int rank, int axis, size_t n_scale, AxisView
   return I8Q_OK;
 }
 
+// Blocks of `threads` threads that are resident at once on the whole GPU.
+int64_t wave_blocks(const void* kern, int threads) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess) per_sm = 1;
+  return (int64_t)sm_count() * std::max(per_sm, 1);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -315,13 +351,30 @@ int run_quantize(const float* x, const AxisView& v, const float* scale, const QT
   const int64_t ntiles = (mode >= 0 && ok_ptr) ? v.n / 512 : 0;
   const int threads = 256;
   if (ntiles > 0) {
-    int64_t blocks = std::min<int64_t>(ceil_div(ntiles, threads / 32), (int64_t)sm_count() * 8);
-    if (mode == AX_TENSOR)
-      quantize_warp512<AX_TENSOR, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, v.axis_len, v.inner);
-    else if (mode == AX_LAST)
-      quantize_warp512<AX_LAST, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, v.axis_len, v.inner);
-    else
+    // One wave of resident blocks (two for the per-tensor form): a partial
+    // last wave leaves SMs with too few reads in flight.  On the last axis
+    // the block count is rounded down, where that keeps at least half of
+    // it, to a multiple that makes the grid stride whole channel cycles
+    // (the form with parameters held in registers).
+    const int64_t want = ceil_div(ntiles, threads / 32);
+    if (mode == AX_TENSOR) {
+      static const int64_t full = wave_blocks((const void*)quantize_fixed<AX_TENSOR, QT>, threads);
+      const int64_t blocks = std::min<int64_t>(want, 2 * full);
+      quantize_fixed<AX_TENSOR, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, 1);
+    } else if (mode == AX_LAST) {
+      static const int64_t full = wave_blocks((const void*)quantize_fixed<AX_LAST, QT>, threads);
+      const int64_t cyc = v.axis_len / std::gcd<int64_t>(v.axis_len, (int64_t)threads / 32 * 512);
+      int64_t blocks = std::min<int64_t>(want, full);
+      if (blocks % cyc != 0 && 2 * (blocks / cyc) * cyc >= blocks) blocks = (blocks / cyc) * cyc;
+      if ((blocks * (threads / 32) * 512) % v.axis_len == 0)
+        quantize_fixed<AX_LAST, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, v.axis_len);
+      else
+        quantize_warp512<AX_LAST, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, v.axis_len, v.inner);
+    } else {
+      static const int64_t full = wave_blocks((const void*)quantize_warp512<AX_BLOCK, QT>, threads);
+      const int64_t blocks = std::min<int64_t>(want, full);
       quantize_warp512<AX_BLOCK, QT><<<blocks, threads, 0, s>>>(x, y, ntiles, scale, zp, v.axis_len, v.inner);
+    }
     I8Q_LAUNCH_CHECK("quantize_warp512");
   }
   int64_t begin = ntiles * 512;

@@ -113,3 +113,20 @@ def test_full_size_round_trip(orc, dev):
         dref = orc.dequantize_linear(ref, s, np.atleast_1d(z).astype(np.int32), axis)
         assert np.array_equal(yd.cpu().numpy(), dref)
         del y, yd
+
+
+@pytest.mark.parametrize("shape,axis", [((3, 700, 4096), 2), ((5000, 768), 1), ((20000, 48), 1), ((300, 1000), 1),
+                                        ((64, 12, 1000), 1), ((3, 700, 4096), None)])
+def test_mid_size_vector_paths(orc, dev, shape, axis):
+    """Sizes between the small cases and the full one: several waves of
+    blocks with a ragged last round, last axes whose length does or does not
+    divide the grid stride, an inner axis, and the per-tensor form."""
+    rng = np.random.default_rng(sum(shape))
+    x = rng.normal(0, 2, size=shape).astype(np.float32)
+    if axis is None:
+        _run_q(orc, dev, x, np.float32(0.02), 0, None, "s8")
+        _run_q(orc, dev, x, np.float32(0.013), 77, None, "u8")
+    else:
+        n = shape[axis]
+        _run_q(orc, dev, x, rng.uniform(0.005, 0.05, n).astype(np.float32), rng.integers(0, 256, n), axis, "u8")
+        _run_q(orc, dev, x, rng.uniform(0.005, 0.05, n).astype(np.float32), rng.integers(-128, 128, n), axis, "s8")
