@@ -13,7 +13,7 @@
 // (c0, kw - pad_left, oh0 + kh - pad_top, n); coordinates outside the input
 // read 0, which is exactly the padding of QLinearConv (a padded position is
 // real 0, i.e. x_zero_point, so xc = 0 there).  Products are within
-// max|xc| * 255, so fp32 chunks of CS K-steps stay exact (partial sums at
+// max|xc| * max|wc|, so fp32 chunks of CS K-steps stay exact (partial sums at
 // most 2^24) and are drained into int32 as in the GEMM core.  The epilogue
 // requantizes each output,
 //   y = saturate(rint(((float)(acc + B[m]) * (x_scale * w_scale[m])) / y_scale) + y_zero_point),
@@ -53,7 +53,10 @@ struct ConvTile {
 struct ConvParams {
   int M, CC, taps, kW, pt, pl, OH, OW, R, NB;
   int tiles_m, row_groups, num_tiles;
-  int KT, CS;
+  int KT;
+  int xmax;            // max |x - x_zero_point| over the input type
+  const void* wzp;     // w zero points (w's type), n_wzp of them; null = 0
+  int n_wzp, wsigned;
   float x_scale, y_scale, qlo_z, qhi_z;  // qlo_z = qlo - y_zp, qhi_z = qhi - y_zp
   int y_zp;
   const int32_t* bias;
@@ -88,6 +91,7 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   auto accf = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
   auto acce = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
   const uint32_t fin = smem_u32(bars + 2 * STAGES + 4);
+  __shared__ int wmax_w[THREADS / 32];  // per warp: max |w - w_zero_point| bound
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -108,12 +112,30 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
   }
+  {
+    const int lo = p.wsigned ? -128 : 0, hi = p.wsigned ? 127 : 255;
+    int wm = p.wzp ? 0 : max(-lo, hi);
+    for (int i = threadIdx.x; p.wzp && i < p.n_wzp; i += THREADS) {
+      const int z = p.wsigned ? (int)static_cast<const int8_t*>(p.wzp)[i] : (int)static_cast<const uint8_t*>(p.wzp)[i];
+      wm = max(wm, max(z - lo, hi - z));
+    }
+    wm = __reduce_max_sync(0xffffffffu, wm);
+    if (lane == 0) wmax_w[warp] = wm;
+  }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int KT = p.KT, CS = p.CS;
+  const int KT = p.KT;
+  // K steps per exact fp32 chunk: every partial sum of CS * 64 products
+  // stays within 2^24 when CS * 64 * max|xc| * max|wc| <= 2^24, with
+  // max|wc| = max over the zero points of their distance to the ends of
+  // w's type (the warps' maxima were merged across the barrier above)
+  int wmax = 0;
+#pragma unroll 1
+  for (int i = 0; i < THREADS / 32; ++i) wmax = max(wmax, wmax_w[i]);
+  const int CS = max(1, (int)((int64_t(1) << 24) / ((int64_t)BK * p.xmax * max(wmax, 1))));
   const int nchunks = (KT + CS - 1) / CS;
 
   if (warp == 0) {
@@ -408,19 +430,85 @@ center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv
   }
 }
 
-// wc[m][kh][kw][c] = w[m][c][kh][kw] - wz[m] (bf16), zero for c >= C.
+// Same result, no shared memory: one CTA per (n, h), one warp per 64-channel
+// block.  Lane t reads the rows of channels 2t, 2t + 1 of its block (8 bytes
+// at a time) and writes, for every column w, the 32-bit word of those two
+// channels; the warp's words of one column are 128 contiguous bytes of the
+// output row.  A code b becomes the fp32 number 1.5 * 2^23 + b by one byte
+// permute (b under the exponent bits), so one subtraction gives b - xz
+// exactly, and a second permute packs the two channels' bf16 halves.
+// Needs W % 8 == 0 and an 8-byte aligned x.
+template <typename XT>
+__global__ void __launch_bounds__(256)
+center_x_lanes(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv_bfloat16* __restrict__ xc) {
+  constexpr bool SG = std::is_signed<XT>::value;
+  const uint32_t flip = SG ? 0x80808080u : 0u;  // signed codes as unsigned + 128
+  const float magic = 12582912.0f;              // 1.5 * 2^23
+  const float off = magic + (float)(SG ? xz + 128 : xz);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int n = blockIdx.x / H, h = blockIdx.x - n * H;
+  const int64_t HW = (int64_t)H * W;
+  const uint8_t* xrow = reinterpret_cast<const uint8_t*>(x) + ((int64_t)n * C * H + h) * W;
+  uint32_t* orow = reinterpret_cast<uint32_t*>(xc + ((int64_t)n * H + h) * W * Cp);
+  const int64_t ostride = Cp / 2;  // words per column
+  for (int cb = warp; cb < Cp / 64; cb += nw) {
+    const int c0 = cb * 64 + 2 * lane;
+    const bool in0 = c0 < C, in1 = c0 + 1 < C;
+    // a channel beyond C loads the code that flips to 0 and subtracts only
+    // the magic number, so its half of the word is +0
+    const float off0 = in0 ? off : magic, off1 = in1 ? off : magic;
+    const uint8_t* r0 = xrow + (int64_t)c0 * HW;
+    const uint8_t* r1 = r0 + HW;
+    uint32_t* o = orow + (c0 >> 1);
+    for (int w0 = 0; w0 < W; w0 += 32) {
+      uint2 a[4], b[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int w = w0 + 8 * k;
+        a[k] = (in0 && w < W) ? __ldg(reinterpret_cast<const uint2*>(r0 + w)) : make_uint2(flip, flip);
+        b[k] = (in1 && w < W) ? __ldg(reinterpret_cast<const uint2*>(r1 + w)) : make_uint2(flip, flip);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int w = w0 + 8 * k;
+        if (w < W) {
+          const uint32_t av[2] = {a[k].x ^ flip, a[k].y ^ flip}, bv[2] = {b[k].x ^ flip, b[k].y ^ flip};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t sel = 0x7650u | (uint32_t)(e & 3);
+            const float f0 = __fsub_rn(__uint_as_float(__byte_perm(av[e >> 2], 0x4B400000u, sel)), off0);
+            const float f1 = __fsub_rn(__uint_as_float(__byte_perm(bv[e >> 2], 0x4B400000u, sel)), off1);
+            o[(int64_t)(w + e) * ostride] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
+          }
+        }
+      }
+    }
+  }
+}
+
+// wc[m][kh][kw][c] = w[m][c][kh][kw] - wz[m] (bf16), zero for c >= C.  One
+// thread per (m, tap, 8 channels): 8 strided byte reads, one 16-byte store.
 template <typename WT>
 __global__ void center_w(const WT* __restrict__ w, const WT* __restrict__ wz, int per_channel, int M, int C, int taps,
                          int Cp, __nv_bfloat16* __restrict__ wc) {
-  const int64_t total = (int64_t)M * taps * Cp;
+  const int groups = Cp / 8;
+  const int64_t total = (int64_t)M * taps * groups;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(i % Cp);
-    const int64_t r = i / Cp;
-    const int tap = (int)(r % taps);
-    const int m = (int)(r / taps);
-    float v = 0.0f;
-    if (c < C) v = (float)((int)w[((int64_t)m * C + c) * taps + tap] - (int)wz[per_channel ? m : 0]);
-    wc[i] = __float2bfloat16_rn(v);  // exact: |v| <= 255
+    const int g = (int)(i % groups);
+    const int r = (int)(i / groups);  // m * taps + tap
+    const int m = r / taps, tap = r - m * taps;
+    const int z = wz ? (int)wz[per_channel ? m : 0] : 0;
+    const WT* src = w + (int64_t)m * C * taps + tap;
+    uint32_t pk[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = g * 8 + 2 * u;
+      // exact: |w - z| <= 255; bf16 = top half of the fp32 value
+      const float v0 = c < C ? (float)((int)src[(int64_t)c * taps] - z) : 0.0f;
+      const float v1 = c + 1 < C ? (float)((int)src[(int64_t)(c + 1) * taps] - z) : 0.0f;
+      pk[u] = __byte_perm(__float_as_uint(v0), __float_as_uint(v1), 0x7632u);
+    }
+    *reinterpret_cast<uint4*>(wc + (int64_t)r * Cp + g * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
 }
 
@@ -465,7 +553,15 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
   {
     I8Q_PROF("conv_center_operands", s);
     const size_t row_smem = (size_t)W * (Cp + 2) * 2;
-    if (row_smem <= 200 * 1024) {
+    if (W % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 7) == 0 && N * H <= INT32_MAX) {
+      const int threads = 32 * (int)std::min<int64_t>(Cp / 64, 8);
+      if (xtype == I8Q_U8)
+        center_x_lanes<uint8_t><<<(unsigned)(N * H), threads, 0, s>>>((const uint8_t*)x, (int)C, (int)H, (int)W,
+                                                                       (int)Cp, x_zp, xc);
+      else
+        center_x_lanes<int8_t><<<(unsigned)(N * H), threads, 0, s>>>((const int8_t*)x, (int)C, (int)H, (int)W,
+                                                                      (int)Cp, x_zp, xc);
+    } else if (row_smem <= 200 * 1024) {
       static std::once_flag once_u8, once_s8;
       if (xtype == I8Q_U8) {
         std::call_once(once_u8, [] {
@@ -487,7 +583,7 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
       else
         center_x_nhwc<int8_t><<<gx, 256, 0, s>>>((const int8_t*)x, (int)C, (int)H, (int)W, (int)Cp, x_zp, xc);
     }
-    const int64_t tw = M * taps * Cp;
+    const int64_t tw = M * taps * (Cp / 8);
     const int gw = (int)std::min<int64_t>(ceil_div(tw, 256), (int64_t)sm_count() * 8);
     if (wtype == I8Q_U8)
       center_w<uint8_t><<<gw, 256, 0, s>>>((const uint8_t*)w, (const uint8_t*)w_zp, per_channel, (int)M, (int)C, taps,
@@ -509,9 +605,6 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
   }
   // |xc| <= max distance of x_zp to its type's ends; |wc| <= 255
   const int xmax = xtype == I8Q_U8 ? std::max(x_zp, 255 - x_zp) : std::max(x_zp + 128, 127 - x_zp);
-  int log2b = 0;
-  while ((int64_t(1) << log2b) < (int64_t)xmax * 255) ++log2b;
-  const int CS = (int)std::max<int64_t>(1, ((int64_t(1) << 24) >> log2b) / BK);
   constexpr int TN = 224;
   using T = ConvTile<TN>;
   static std::once_flag attr_once;
@@ -535,7 +628,10 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
   p.row_groups = (int)ceil_div(OH, R);
   p.num_tiles = p.tiles_m * p.row_groups * (int)N;
   p.KT = taps * p.CC;
-  p.CS = CS;
+  p.xmax = std::max(xmax, 1);
+  p.wzp = w_zp;
+  p.n_wzp = per_channel ? (int)M : 1;
+  p.wsigned = wtype == I8Q_S8 ? 1 : 0;
   p.x_scale = x_scale;
   p.y_scale = y_scale;
   const float qlo = ytype == I8Q_U8 ? 0.0f : -128.0f, qhi = ytype == I8Q_U8 ? 255.0f : 127.0f;

@@ -130,15 +130,20 @@ binary_table(const uint8_t* __restrict__ A, int amode, int64_t aper, const uint8
   }
   __syncthreads();
   const uint8_t* t8 = reinterpret_cast<const uint8_t*>(tab);
-  constexpr int U = 4;
+  // a warp moves U * 512 consecutive codes per step (lane t: the 16-code
+  // groups t, t + 32, ...), so each operand stream is read in 1 KB runs
+  constexpr int U = 2;
+  const int lane = threadIdx.x & 31;
   const int64_t groups = n / 16;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g0 < groups; g0 += U * stride) {
+  const int64_t chunks = (groups + 32 * U - 1) / (32 * U);
+  const int64_t wstride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t ch = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; ch < chunks; ch += wstride) {
     uint32_t aw[U][4], bw[U][4];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t i = (g0 + u * stride) * 16;
-      const bool in = g0 + u * stride < groups;
+      const int64_t gi = ch * 32 * U + 32 * u + lane;
+      const int64_t i = gi * 16;
+      const bool in = gi < groups;
       if (amode == 1) {
         const uint32_t v = A[0] * 0x01010101u;
         aw[u][0] = aw[u][1] = aw[u][2] = aw[u][3] = v;
@@ -156,7 +161,7 @@ binary_table(const uint8_t* __restrict__ A, int amode, int64_t aper, const uint8
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t gi = g0 + u * stride;
+      const int64_t gi = ch * 32 * U + 32 * u + lane;
       if (gi >= groups) break;
       uint32_t ow[4];
 #pragma unroll
@@ -234,18 +239,22 @@ unary_lut(const uint8_t* __restrict__ X, int64_t n, int op, float x_scale, int x
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const bool aligned = ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(Y)) & 15) == 0;
   if (aligned) {
-    // four 16-byte groups per thread in flight before any is used
-    constexpr int U = 4;
-    for (int64_t g0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g0 < groups; g0 += U * stride) {
+    // a warp moves U * 512 consecutive codes per step (lane t: the 16-code
+    // groups t, t + 32, ...): 4 KB runs of the input, all loaded before any
+    // is used
+    constexpr int U = 8;
+    const int64_t chunks = (groups + 32 * U - 1) / (32 * U);
+    const int64_t wstride = stride >> 5;
+    for (int64_t ch = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; ch < chunks; ch += wstride) {
       uint4 v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t gi = g0 + u * stride;
+        const int64_t gi = ch * 32 * U + 32 * u + lane;
         v[u] = gi < groups ? __ldcs(reinterpret_cast<const uint4*>(X) + gi) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t gi = g0 + u * stride;
+        const int64_t gi = ch * 32 * U + 32 * u + lane;
         if (gi >= groups) break;
         const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
         uint32_t o[4];
@@ -352,7 +361,7 @@ int run_binary(const uint8_t* A, const uint8_t* B, const Strides& st, int64_t n,
       attr = cudaFuncSetAttribute(binary_table<AS, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTabBytes);
     });
     I8Q_CUDA_TRY(attr);
-    const int grid = (int)std::min<int64_t>(sm_count(), ceil_div(n / 16, (int64_t)kTabThreads));
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), ceil_div(n / 16, (int64_t)kTabThreads)));
     binary_table<AS, BS><<<grid, kTabThreads, kTabBytes, s>>>(A, am, aper, B, bm, bper, n, p,
                                                                static_cast<uint8_t*>(C));
     I8Q_LAUNCH_CHECK("binary_table");
@@ -452,7 +461,7 @@ extern "C" int i8q_qlinear_unary(int op, const void* X, int64_t n, int qtype, fl
   I8Q_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       &per_sm, (qtype == I8Q_S8) ? unary_lut<true> : unary_lut<false>, 256, 0));
   const int grid = (int)std::max<int64_t>(
-      1, std::min<int64_t>(ceil_div(std::max<int64_t>(n / 16, 1), 256), (int64_t)sm_count() * std::max(per_sm, 1)));
+      1, std::min<int64_t>(ceil_div(n / 16, 256 * 8), (int64_t)sm_count() * std::max(per_sm, 1)));
   I8Q_PROF(o == 0 ? "qlinear_leaky_relu" : "qlinear_sigmoid", s);
   if (qtype == I8Q_S8)
     unary_lut<true><<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(X), n, o, x_scale, x_zero_point, y_scale,

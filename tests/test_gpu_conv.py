@@ -85,6 +85,8 @@ TC_CASES = [
     (1, 16, 9, 56, 64, 5, (2, 2, 2, 2)),     # 5x5
     (1, 8, 6, 58, 24, 3, (0, 0, 0, 0)),      # unpadded, OW 56 from W 58
     (3, 128, 8, 56, 256, 3, (1, 1, 1, 1)),   # two output-channel tiles, partial row group
+    (1, 72, 7, 56, 40, 3, (1, 1, 1, 1)),     # W % 8 == 0 with C not a multiple of 64
+    (1, 40, 6, 112, 48, 3, (1, 1, 1, 1)),    # OW 112: two rows per tile, several column rounds
 ]
 
 
