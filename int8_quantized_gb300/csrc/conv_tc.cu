@@ -430,62 +430,6 @@ center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv
   }
 }
 
-// Same result, no shared memory: one CTA per (n, h), one warp per 64-channel
-// block.  Lane t reads the rows of channels 2t, 2t + 1 of its block (8 bytes
-// at a time) and writes, for every column w, the 32-bit word of those two
-// channels; the warp's words of one column are 128 contiguous bytes of the
-// output row.  A code b becomes the fp32 number 1.5 * 2^23 + b by one byte
-// permute (b under the exponent bits), so one subtraction gives b - xz
-// exactly, and a second permute packs the two channels' bf16 halves.
-// Needs W % 8 == 0 and an 8-byte aligned x.
-template <typename XT>
-__global__ void __launch_bounds__(256)
-center_x_lanes(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv_bfloat16* __restrict__ xc) {
-  constexpr bool SG = std::is_signed<XT>::value;
-  const uint32_t flip = SG ? 0x80808080u : 0u;  // signed codes as unsigned + 128
-  const float magic = 12582912.0f;              // 1.5 * 2^23
-  const float off = magic + (float)(SG ? xz + 128 : xz);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int n = blockIdx.x / H, h = blockIdx.x - n * H;
-  const int64_t HW = (int64_t)H * W;
-  const uint8_t* xrow = reinterpret_cast<const uint8_t*>(x) + ((int64_t)n * C * H + h) * W;
-  uint32_t* orow = reinterpret_cast<uint32_t*>(xc + ((int64_t)n * H + h) * W * Cp);
-  const int64_t ostride = Cp / 2;  // words per column
-  for (int cb = warp; cb < Cp / 64; cb += nw) {
-    const int c0 = cb * 64 + 2 * lane;
-    const bool in0 = c0 < C, in1 = c0 + 1 < C;
-    // a channel beyond C loads the code that flips to 0 and subtracts only
-    // the magic number, so its half of the word is +0
-    const float off0 = in0 ? off : magic, off1 = in1 ? off : magic;
-    const uint8_t* r0 = xrow + (int64_t)c0 * HW;
-    const uint8_t* r1 = r0 + HW;
-    uint32_t* o = orow + (c0 >> 1);
-    for (int w0 = 0; w0 < W; w0 += 32) {
-      uint2 a[4], b[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int w = w0 + 8 * k;
-        a[k] = (in0 && w < W) ? __ldg(reinterpret_cast<const uint2*>(r0 + w)) : make_uint2(flip, flip);
-        b[k] = (in1 && w < W) ? __ldg(reinterpret_cast<const uint2*>(r1 + w)) : make_uint2(flip, flip);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int w = w0 + 8 * k;
-        if (w < W) {
-          const uint32_t av[2] = {a[k].x ^ flip, a[k].y ^ flip}, bv[2] = {b[k].x ^ flip, b[k].y ^ flip};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint32_t sel = 0x7650u | (uint32_t)(e & 3);
-            const float f0 = __fsub_rn(__uint_as_float(__byte_perm(av[e >> 2], 0x4B400000u, sel)), off0);
-            const float f1 = __fsub_rn(__uint_as_float(__byte_perm(bv[e >> 2], 0x4B400000u, sel)), off1);
-            o[(int64_t)(w + e) * ostride] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
-          }
-        }
-      }
-    }
-  }
-}
-
 // wc[m][kh][kw][c] = w[m][c][kh][kw] - wz[m] (bf16), zero for c >= C.  One
 // thread per (m, tap, 8 channels): 8 strided byte reads, one 16-byte store.
 template <typename WT>
@@ -553,15 +497,7 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
   {
     I8Q_PROF("conv_center_operands", s);
     const size_t row_smem = (size_t)W * (Cp + 2) * 2;
-    if (W % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 7) == 0 && N * H <= INT32_MAX) {
-      const int threads = 32 * (int)std::min<int64_t>(Cp / 64, 8);
-      if (xtype == I8Q_U8)
-        center_x_lanes<uint8_t><<<(unsigned)(N * H), threads, 0, s>>>((const uint8_t*)x, (int)C, (int)H, (int)W,
-                                                                       (int)Cp, x_zp, xc);
-      else
-        center_x_lanes<int8_t><<<(unsigned)(N * H), threads, 0, s>>>((const int8_t*)x, (int)C, (int)H, (int)W,
-                                                                      (int)Cp, x_zp, xc);
-    } else if (row_smem <= 200 * 1024) {
+    if (row_smem <= 200 * 1024) {
       static std::once_flag once_u8, once_s8;
       if (xtype == I8Q_U8) {
         std::call_once(once_u8, [] {

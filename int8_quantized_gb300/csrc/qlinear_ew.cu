@@ -117,7 +117,9 @@ binary_fast(const uint8_t* __restrict__ A, int amode, int64_t aper, const uint8_
 // in binary_fast.
 constexpr int kTabThreads = 1024, kTabBytes = 65536;
 
-template <bool AS, bool BS>
+// SAME: both operands have the output's shape (modes 0), the common case,
+// compiled without the broadcast branches.
+template <bool AS, bool BS, bool SAME>
 __global__ void __launch_bounds__(kTabThreads, 1)
 binary_table(const uint8_t* __restrict__ A, int amode, int64_t aper, const uint8_t* __restrict__ B, int bmode,
              int64_t bper, int64_t n, BinParams p, uint8_t* __restrict__ C) {
@@ -144,18 +146,20 @@ binary_table(const uint8_t* __restrict__ A, int amode, int64_t aper, const uint8
       const int64_t gi = ch * 32 * U + 32 * u + lane;
       const int64_t i = gi * 16;
       const bool in = gi < groups;
-      if (amode == 1) {
+      if (!SAME && amode == 1) {
         const uint32_t v = A[0] * 0x01010101u;
         aw[u][0] = aw[u][1] = aw[u][2] = aw[u][3] = v;
       } else {
-        const uint4 v = in ? __ldcs(reinterpret_cast<const uint4*>(A + fast_offset(amode, i, aper))) : make_uint4(0, 0, 0, 0);
+        const int64_t off = SAME ? i : fast_offset(amode, i, aper);
+        const uint4 v = in ? __ldcs(reinterpret_cast<const uint4*>(A + off)) : make_uint4(0, 0, 0, 0);
         aw[u][0] = v.x, aw[u][1] = v.y, aw[u][2] = v.z, aw[u][3] = v.w;
       }
-      if (bmode == 1) {
+      if (!SAME && bmode == 1) {
         const uint32_t v = B[0] * 0x01010101u;
         bw[u][0] = bw[u][1] = bw[u][2] = bw[u][3] = v;
       } else {
-        const uint4 v = in ? __ldcs(reinterpret_cast<const uint4*>(B + fast_offset(bmode, i, bper))) : make_uint4(0, 0, 0, 0);
+        const int64_t off = SAME ? i : fast_offset(bmode, i, bper);
+        const uint4 v = in ? __ldcs(reinterpret_cast<const uint4*>(B + off)) : make_uint4(0, 0, 0, 0);
         bw[u][0] = v.x, bw[u][1] = v.y, bw[u][2] = v.z, bw[u][3] = v.w;
       }
     }
@@ -358,12 +362,18 @@ int run_binary(const uint8_t* A, const uint8_t* B, const Strides& st, int64_t n,
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-      attr = cudaFuncSetAttribute(binary_table<AS, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTabBytes);
+      attr = cudaFuncSetAttribute(binary_table<AS, BS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTabBytes);
+      if (attr == cudaSuccess)
+        attr = cudaFuncSetAttribute(binary_table<AS, BS, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTabBytes);
     });
     I8Q_CUDA_TRY(attr);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), ceil_div(n / 16, (int64_t)kTabThreads)));
-    binary_table<AS, BS><<<grid, kTabThreads, kTabBytes, s>>>(A, am, aper, B, bm, bper, n, p,
-                                                               static_cast<uint8_t*>(C));
+    if (am == 0 && bm == 0)
+      binary_table<AS, BS, true><<<grid, kTabThreads, kTabBytes, s>>>(A, am, aper, B, bm, bper, n, p,
+                                                                       static_cast<uint8_t*>(C));
+    else
+      binary_table<AS, BS, false><<<grid, kTabThreads, kTabBytes, s>>>(A, am, aper, B, bm, bper, n, p,
+                                                                        static_cast<uint8_t*>(C));
     I8Q_LAUNCH_CHECK("binary_table");
     done = (n / 16) * 16;
   } else if (am >= 0 && bm >= 0 && aligned && n >= 16) {
