@@ -81,6 +81,32 @@ __device__ __forceinline__ uint32_t rint_code_bits(float q, float lo_z, float hi
   return (uint32_t)(__float_as_int(r) + zp);
 }
 
+// fl(1 / s) when s and its reciprocal are normal numbers (quot_code_bits
+// may then use it), else NaN (quot_code_bits then always divides).
+__host__ __device__ inline float quot_rcp(float s) {
+  const float a = s < 0.0f ? -s : s;
+  return (a >= 0x1p-125f && a <= 0x1p125f) ? 1.0f / s : __builtin_nanf("");
+}
+
+// rint_code_bits of the IEEE quotient fl(v / s), usually without forming
+// it: with r = quot_rcp(s), q = fl(v * r) is within (2^-23 + 2^-48) |v / s|
+// of v / s (r carries one rounding, the product another) and fl(v / s)
+// within 2^-24 |v / s|, so the two differ by less than 2^-22 |q|.  Where q
+// is farther than 2^-21 |q| from every half-integer, both round to the same
+// integer, and the saturation bounds are integers, so the codes agree;
+// beyond 1024 in magnitude both saturate alike (the bounds are within
+// +-255).  Any other q (close to a half-integer, NaN, or r NaN) is replaced
+// by the quotient itself.
+__device__ __forceinline__ uint32_t quot_code_bits(float v, float s, float r, float lo_z, float hi_z, int zp) {
+  float q = __fmul_rn(v, r);
+  const float a = fabsf(q);
+  if (!(a > 1024.0f)) {
+    const float dist = fabsf(__fsub_rn(__fsub_rn(q, floorf(q)), 0.5f));
+    if (!(dist > a * 0x1p-21f)) q = __fdiv_rn(v, s);
+  }
+  return rint_code_bits(q, lo_z, hi_z, zp);
+}
+
 // Row quantization of A (uint8, per row, range widened to contain 0) from
 // the row's mn = min(0, min A) and mx = max(0, max A):
 //   scale = (mx - mn) / 255, zero = sat_u8(rint(-mn / scale)),
@@ -299,8 +325,10 @@ struct QgEpilogue {
   const float* bias;      // [N] or null
   const int32_t* C;       // element (i, j) at C[i * c_si + j * c_sj], or null
   int64_t c_si, c_sj;
+  int c_col;              // C is the same for every row (c_si == 0) and bias is null: C is staged per column
   int ytype;              // I8Q_F32, I8Q_U8 or I8Q_S8
   float y_scale;
+  float y_rcp;            // quot_rcp(y_scale)
   int y_zero_point;
   void* Y;
   int64_t ldy;

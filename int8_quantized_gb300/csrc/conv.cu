@@ -225,6 +225,7 @@ qlinearconv_depthwise_strip(const XT* __restrict__ x, const WT* __restrict__ w, 
   const int32_t bc = B ? B[c] : 0;
   const float mul = __fmul_rn(x_scale, w_scale[per_channel ? c : 0]);
   const float lo_z = qlo - (float)y_zp, hi_z = qhi - (float)y_zp;
+  const float yr = quot_rcp(y_scale);
   __syncthreads();
   YT* yp = y + ((int64_t)n * C + c) * OH * OW;
   const bool vec_rows = (OW % kStrip) == 0 && (reinterpret_cast<uintptr_t>(y) & 7) == 0;
@@ -256,9 +257,7 @@ qlinearconv_depthwise_strip(const XT* __restrict__ x, const WT* __restrict__ w, 
 #pragma unroll
     for (int e = 0; e < kStrip; ++e) {
       const int32_t a = __float2int_rn(acc[e]) + bc;
-      float vq = __fmul_rn(__int2float_rn(a), mul);
-      vq = __fdiv_rn(vq, y_scale);
-      code[e] = rint_code_bits(vq, lo_z, hi_z, y_zp);
+      code[e] = quot_code_bits(__fmul_rn(__int2float_rn(a), mul), y_scale, yr, lo_z, hi_z, y_zp);
     }
     YT* out = yp + oh * OW + ow0;
     if (vec_rows && ((reinterpret_cast<uintptr_t>(out) & 7) == 0)) {

@@ -247,11 +247,12 @@ __device__ __forceinline__ void store_slice_qg(const QgEpilogue& qg, int64_t row
                                                const int32_t* pg, const int32_t* pe, const float* pb,
                                                const float* pz) {
   const bool full = col0 + SLICE <= N;
-  const int32_t* crow = qg.C ? qg.C + row * qg.c_si : nullptr;
+  const int32_t* crow = (qg.C && !qg.c_col) ? qg.C + row * qg.c_si : nullptr;
   const bool has_bias = qg.bias != nullptr;
   auto value_at = [&](int j) -> float {
     // wrapping int32 arithmetic: the exact sum fits int32
     uint32_t a = (uint32_t)run[j] + (uint32_t)rs * (uint32_t)pg[j] + (uint32_t)dr * (uint32_t)pe[j];
+    if (qg.c_col) a += (uint32_t)__float_as_int(pz[j]);
     if (crow && col0 + j < N) a += (uint32_t)__ldg(crow + (col0 + j) * qg.c_sj);
     float v = __fmul_rn(__int2float_rn((int32_t)a), __fmul_rn(ar, pb[j]));
     if (has_bias) v = __fadd_rn(v, pz[j]);
@@ -284,7 +285,7 @@ __device__ __forceinline__ void store_slice_qg(const QgEpilogue& qg, int64_t row
   for (int j = 0; j < SLICE; j += 16) {
     uint32_t b[16];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) b[u] = rint_code_bits(__fdiv_rn(value_at(j + u), qg.y_scale), lo, hi, zp);
+    for (int u = 0; u < 16; ++u) b[u] = quot_code_bits(value_at(j + u), qg.y_scale, qg.y_rcp, lo, hi, zp);
     if (vec) {
       *reinterpret_cast<uint4*>(Y + j) =
           make_uint4(pack_low_bytes(b[0], b[1], b[2], b[3]), pack_low_bytes(b[4], b[5], b[6], b[7]),
@@ -307,10 +308,11 @@ __device__ __forceinline__ void store_slice_qg_tma(const QgEpilogue& qg, const C
                                                    const int32_t* pg, const int32_t* pe, const float* pb,
                                                    const float* pz, uint8_t* stg) {
   const int64_t row = row0 + lane;
-  const int32_t* crow = (qg.C && row < M) ? qg.C + row * qg.c_si : nullptr;
+  const int32_t* crow = (qg.C && !qg.c_col && row < M) ? qg.C + row * qg.c_si : nullptr;
   const bool has_bias = qg.bias != nullptr;
   auto value_at = [&](int j) -> float {
     uint32_t a = (uint32_t)run[j] + (uint32_t)rs * (uint32_t)pg[j] + (uint32_t)dr * (uint32_t)pe[j];
+    if (qg.c_col) a += (uint32_t)__float_as_int(pz[j]);
     if (crow && col0 + j < N) a += (uint32_t)__ldg(crow + (col0 + j) * qg.c_sj);
     float v = __fmul_rn(__int2float_rn((int32_t)a), __fmul_rn(ar, pb[j]));
     if (has_bias) v = __fadd_rn(v, pz[j]);
@@ -350,7 +352,7 @@ __device__ __forceinline__ void store_slice_qg_tma(const QgEpilogue& qg, const C
     for (int w = 0; w < 8; ++w) {
       uint32_t b[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) b[u] = rint_code_bits(__fdiv_rn(value_at(j + 4 * w + u), qg.y_scale), lo, hi, zp);
+      for (int u = 0; u < 4; ++u) b[u] = quot_code_bits(value_at(j + 4 * w + u), qg.y_scale, qg.y_rcp, lo, hi, zp);
       wd[w] = pack_low_bytes(b[0], b[1], b[2], b[3]);
     }
     put(wd, col0 + j);
@@ -373,7 +375,10 @@ __device__ __forceinline__ void stage_params(const TcParams& p, int64_t col0, in
       pc[j] = in ? __ldg(p.qg.g + c) : 0;
       reinterpret_cast<int32_t*>(ps)[j] = in ? __ldg(p.qg.e + c) : 0;
       pb[j] = in ? __ldg(p.qg.bsc + c) : 0.0f;
-      pd[j] = (in && p.qg.bias) ? __ldg(p.qg.bias + c) : 0.0f;
+      if (p.qg.c_col)  // the row-independent C, as int32 bits in the bias slot
+        reinterpret_cast<int32_t*>(pd)[j] = in ? __ldg(p.qg.C + c * p.qg.c_sj) : 0;
+      else
+        pd[j] = (in && p.qg.bias) ? __ldg(p.qg.bias + c) : 0.0f;
     }
   }
 }

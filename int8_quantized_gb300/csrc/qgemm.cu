@@ -441,8 +441,10 @@ extern "C" int i8q_qgemm(const void* A, int atype, int transA, int64_t M, int64_
   qg.C = C;
   qg.c_si = C ? (c_rows == 1 ? 0 : c_cols) : 0;
   qg.c_sj = C ? (c_cols == 1 ? 0 : 1) : 0;
+  qg.c_col = (C && qg.c_si == 0) ? 1 : 0;  // QGemm has no bias
   qg.ytype = quantize_y ? ytype : I8Q_F32;
   qg.y_scale = y_scale;
+  qg.y_rcp = quot_rcp(y_scale);
   qg.y_zero_point = y_zero_point;
   qg.Y = Y;
   return finish_product(L, base, M, N, K, Kp, B, btype, transB, b_scale, b_zero_point, (int64_t)n_b, ca, rp, qg, s);

@@ -183,3 +183,21 @@ def test_depthwise_kernels(orc, dev, monkeypatch, kernel, case, types):
     B = rng.integers(-5000, 5001, C).astype(np.int32)
     run_conv(orc, dev, x, np.float32(0.0037), int(rng.integers(xt[0], xt[1])), w, ws, wz, np.float32(0.05),
              int(rng.integers(yt[0], yt[1])), B, pads, group=C, ytype=types[2])
+
+
+@pytest.mark.parametrize("kernel", ["strip", "halo"])
+@pytest.mark.parametrize("ys", [2.0, 0.5, 3.0, 0.1, 1e-30, 1e30, 3e38])
+def test_depthwise_requantization_ties(orc, dev, monkeypatch, kernel, ys):
+    """Unit input and filter scales make every rescaled sum an integer, so
+    y_scale 2 puts half the quotients exactly on a tie (round half to even
+    decides them); the other scales give exact, inexact, saturating,
+    vanishing quotients and one whose reciprocal is not a normal number."""
+    if kernel == "halo":
+        monkeypatch.setenv("I8Q_FORCE_CONV_HALO", "1")
+    rng = np.random.default_rng(int(ys * 7) % 1000 if ys < 1e3 else 5)
+    N, C, H, W, k = 2, 6, 20, 24, 3
+    x = rng.integers(0, 16, (N, C, H, W)).astype(np.uint8)
+    w = rng.integers(-8, 8, (C, 1, k, k)).astype(np.int8)
+    B = rng.integers(-50, 51, C).astype(np.int32)
+    run_conv(orc, dev, x, np.float32(1.0), 3, w, np.ones(C, np.float32), np.zeros(C, np.int64), np.float32(ys), 0, B,
+             (1, 1, 1, 1), group=C, ytype="s8")

@@ -301,15 +301,30 @@ def test_forward_host_pipelined_rows(orc, dev, M):
     ctx.set_params(_t(iB, dev), _t(sB, dev), _t(bias, dev))
     Ah = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).pin_memory()
     Ch = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
-    ctx.forward_host(Ah, Ch)
     Cd = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-    ctx.forward(Ah.to(dev), Cd)
-    q.sync_status()
-    assert torch.equal(Ch.view(torch.int16), Cd.cpu().view(torch.int16))
+    # calls 1 (direct), 2 (captured as a graph) and 3, 4 (graph replays)
+    # with the same host buffers; A changes before each of the later calls,
+    # so every replay must read the buffer's current contents
+    for call in range(4):
+        if call:
+            Ah.copy_(torch.from_numpy(np.roll(A, 37 * call, axis=0).view(np.int16)).view(torch.bfloat16))
+        Ch.fill_(0)
+        ctx.forward_host(Ah, Ch)
+        ctx.forward(Ah.to(dev), Cd)
+        q.sync_status()
+        assert torch.equal(Ch.view(torch.int16), Cd.cpu().view(torch.int16)), f"call {call}"
     rows = np.array([0, 1, 1023, 1024, M // 2, M - 2, M - 1])
-    ref = orc.dynamic_quantized_inner_product(A[rows], iB=iB, scaleB=sB, bias=bias, act=orc.ACT_GELU, typeC="bf16")
+    A_last = np.roll(A, 37 * 3, axis=0)
+    ref = orc.dynamic_quantized_inner_product(A_last[rows], iB=iB, scaleB=sB, bias=bias, act=orc.ACT_GELU,
+                                              typeC="bf16")
     d = bf16_ulp_distance(Ch.view(torch.int16).numpy().view(np.uint16)[rows], ref["C"])
     assert d.max() <= 1
+    # new parameters invalidate the captured pipeline
+    ctx.set_params(_t(-iB, dev), _t(sB, dev), _t(bias, dev))
+    ctx.forward_host(Ah, Ch)
+    ctx.forward(Ah.to(dev), Cd)
+    q.sync_status()
+    assert torch.equal(Ch.view(torch.int16), Cd.cpu().view(torch.int16)), "after SetParams"
     ctx.clear()
 
 

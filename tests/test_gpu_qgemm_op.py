@@ -124,6 +124,19 @@ def test_worst_case_magnitudes(orc, dev):
     run(orc, dev, A, 1.0, 255, B, np.full(N, 2.0 ** -20, np.float32), zb, y_scale=1.0, yzp=0)
 
 
+@pytest.mark.parametrize("y_scale", [2.0, 0.5, 3.0, 0.1, 1e-30, 1e30, 3e38])
+def test_requantization_ties(orc, dev, y_scale):
+    """Unit scales make every rescaled sum an integer, so y_scale 2 puts half
+    the quotients exactly on a tie (round half to even decides them); the
+    other scales give exact, inexact, saturating, vanishing quotients and one
+    whose reciprocal is not a normal number."""
+    rng = np.random.default_rng(31)
+    M, K, N = 300, 4, 520
+    A = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    B = rng.integers(-8, 8, (K, N)).astype(np.int8)
+    run(orc, dev, A, 1.0, 0, B, np.ones(N, np.float32), y_scale=y_scale, yzp=0, ytype="s8")
+
+
 def test_mid_size_full(orc, dev):
     w = workloads.qgemm(seed=14, M=512, K=2048, N=1024)
     run(orc, dev, w["A"], w["a_scale"], w["a_zero_point"], w["B"], w["b_scale"], w["b_zero_point"], C=w["C"],
