@@ -100,7 +100,87 @@ center_operand(const uint8_t* __restrict__ X, int64_t R, int64_t K, int64_t Kp, 
   if ((t & 3) == 0 && r < R) atomicAdd(sums + r, part);
 }
 
-// g[j] = cb - bz[j]; e[j] = colsum[j] + K g[j] (wrapping int32);
+// The same result when K is the contiguous index (no transpose): a stream
+// of 16-code groups, Xc keeping X's row order.  Thread g takes group g of
+// the padded rows (Kp / 16 groups each) and three more a grid apart, all
+// loaded before any is used; groups at or beyond K are written as zeros.
+// A row's groups are consecutive threads, so its sum is reduced across the
+// warp when all lanes share the row, else added lane by lane.  Needs
+// K % 16 == 0 and a 16-byte aligned X.
+template <bool SIGNED>
+__global__ void __launch_bounds__(256)
+center_rows(const uint8_t* __restrict__ X, int64_t R, int64_t K, int64_t Kp, __nv_bfloat16* __restrict__ Xc,
+            int32_t* __restrict__ sums) {
+  constexpr int U = 4;
+  const uint32_t flip = SIGNED ? 0u : 0x80808080u;  // u8 code - 128 == int8 of (code ^ 0x80)
+  const int64_t gpr = Kp / 16, total = R * gpr;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  // (row, group in row) of g, advanced by addition: one division per thread
+  const int64_t sr = stride / gpr, sg = stride - sr * gpr;
+  int64_t g0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int64_t r_at = g0 / gpr, c_at = g0 - r_at * gpr;
+  auto advance = [&](int64_t& r, int64_t& c) {
+    r += sr;
+    c += sg;
+    if (c >= gpr) {
+      c -= gpr;
+      ++r;
+    }
+  };
+  for (; g0 - lane < total; g0 += U * stride) {
+    uint4 v[U];
+    int64_t rr[U], kk[U];
+    {
+      int64_t r = r_at, c = c_at;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (u) advance(r, c);
+        rr[u] = r;
+        kk[u] = c * 16;
+      }
+      advance(r, c);
+      r_at = r;
+      c_at = c;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = g0 + u * stride;
+      v[u] = (g < total && kk[u] < K) ? __ldcs(reinterpret_cast<const uint4*>(X + rr[u] * K + kk[u]))
+                                      : make_uint4(flip, flip, flip, flip);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = g0 + u * stride;
+      const uint32_t wd[4] = {v[u].x ^ flip, v[u].y ^ flip, v[u].z ^ flip, v[u].w ^ flip};
+      uint32_t o[8];
+      int part = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        // two centred codes (int8 bytes) as bf16: exact through fp32
+        const int c0 = (int)(int8_t)(wd[e >> 1] >> (16 * (e & 1))), c1 = (int)(int8_t)(wd[e >> 1] >> (16 * (e & 1) + 8));
+        part += c0 + c1;
+        o[e] = (__float_as_uint((float)c0) >> 16) | (__float_as_uint((float)c1) & 0xffff0000u);
+      }
+      if (g < total) {
+        uint4* dst = reinterpret_cast<uint4*>(Xc + rr[u] * Kp + kk[u]);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      // row sum: one atomic per warp when the warp's groups share a row
+      const int64_t r = g < total ? rr[u] : -1;
+      const int64_t r_first = __shfl_sync(0xffffffffu, r, 0);
+      if (__all_sync(0xffffffffu, r == r_first)) {
+        part = __reduce_add_sync(0xffffffffu, part);
+        if (lane == 0 && r >= 0) atomicAdd(sums + r, part);
+      } else if (r >= 0 && part != 0) {
+        atomicAdd(sums + r, part);
+      }
+    }
+  }
+}
+
+// g[j] = cb - bz[j]; e[j] = colsum[j] + K g[j] (wrapping int32);// g[j] = cb - bz[j]; e[j] = colsum[j] + K g[j] (wrapping int32);
 // bsc[j] = b_scale[j] (expanded when per tensor).  Thread 0 also writes the
 // per-tensor row values d0 = ca - za and asc0 when asked (write_row0).
 __global__ void col_params(const int32_t* __restrict__ colsum, const float* __restrict__ b_scale,
@@ -299,8 +379,24 @@ int launch_center(const void* X, int type, int64_t R, int64_t K, int64_t Kp, int
   I8Q_PROF("qgemm_center", s);
   I8Q_CUDA_TRY(cudaMemsetAsync(sums, 0, (size_t)R * sizeof(int32_t), s));
   const bool vec = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && (k_fast ? K % 16 == 0 : R % 16 == 0);
-  const dim3 grid((unsigned)bx, (unsigned)by);
   const auto* x8 = static_cast<const uint8_t*>(X);
+  if (k_fast && vec) {
+    // no transpose: a stream; one wave of resident blocks
+    static int per_sm = 0;
+    if (per_sm == 0) {
+      int a = 0, b = 0;
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, center_rows<true>, 256, 0);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, center_rows<false>, 256, 0);
+      per_sm = std::max(1, std::min(a, b));
+    }
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(ceil_div(R * (Kp / 16), 256 * 4),
+                                                                  (int64_t)sm_count() * per_sm));
+    if (type == I8Q_S8) center_rows<true><<<(unsigned)blocks, 256, 0, s>>>(x8, R, K, Kp, Xc, sums);
+    else center_rows<false><<<(unsigned)blocks, 256, 0, s>>>(x8, R, K, Kp, Xc, sums);
+    I8Q_LAUNCH_CHECK("center_rows");
+    return I8Q_OK;
+  }
+  const dim3 grid((unsigned)bx, (unsigned)by);
   if (type == I8Q_S8) {
     if (vec) center_operand<true, true><<<grid, 256, 0, s>>>(x8, R, K, Kp, k_fast, Xc, sums);
     else center_operand<true, false><<<grid, 256, 0, s>>>(x8, R, K, Kp, k_fast, Xc, sums);
