@@ -43,8 +43,8 @@ WORKLOAD = ("dynamic quantized GEMM M=8192 K=4096 N=14336: bf16 A quantized per 
 NCU_TRAFFIC = {
     "gemm_tc_pair": {"sources": ["int8_quantized_gb300/csrc/gemm_tc.cu", "int8_quantized_gb300/csrc/tcgen05.cuh",
                                  "int8_quantized_gb300/csrc/common.cuh"],
-                     "sha256": "3fe75b796939631406e8d7f64058ffb8462418b01dd832c3699687cb75ebe7e4",
-                     "bytes": (556.23 + 222.80) * 1e6,
+                     "sha256": "c9b42f324f6fff05b77dd113f5000fac5ef9569cc77f280efe7cc2d80bbd5f83",
+                     "bytes": (567.96 + 222.04) * 1e6,
                      "profile": "profiles/gemm_tc_pair_large_gemm.md"},
 }
 
