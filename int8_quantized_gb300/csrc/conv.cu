@@ -171,93 +171,124 @@ qlinearconv_depthwise_halo(const XT* __restrict__ x, const WT* __restrict__ w, c
 }
 
 // Depthwise KS x KS, stride 1, dilation 1: one CTA of 128 threads per
-// (image, channel) plane.  The plane sits in shared memory as centred
-// values (x - x_zero_point, held as fp32) with a zero halo, rows padded to a
-// multiple of 4 words; each thread computes strips of 8 consecutive outputs
-// of a row from a window loaded with 16-byte shared-memory reads, and
-// writes them as one 8-byte store.  The taps accumulate in fp32 with FMAs:
-// every product (|v w| <= 255^2) and every partial sum (<= 25 * 255^2 <
-// 2^24) is an integer exactly representable, so the sum is the exact int32
-// one; the bias is then added in int32.
-constexpr int kStrip = 8;
+// (image, channel) plane, integer tap sums on the byte dot product (dp4a)
+// over the raw codes.  The plane sits in shared memory as its codes, each
+// row at byte kX0 of a row of RW words, the halo filled with the x zero
+// point's code (so that a padded tap contributes x - x_zp = 0).  For the KS
+// taps of a filter row, with w packed four codes a word (zeros beyond KS),
+//   sum (x - x_zp)(w - w_zp) = sum x w - w_zp sum x - x_zp sum w + KS x_zp w_zp
+// per row, all exact in int32: sum x w and sum x come from dp4a of a 4-byte
+// window of the row with the packed weights and with ones.  Each thread
+// computes strips of 8 consecutive outputs of a row: it loads the strip's
+// words of each input row, shifts them once to the strip's first byte and
+// takes the eight windows with byte permutes whose selectors are constants.
+// The codes are requantized (quot_code_bits) and written as one 8-byte store.
+constexpr int kStrip = 8, kX0 = 8;  // outputs per strip; byte of x column 0 in a shared row
+
+template <bool AS, bool BS>
+__device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
+  int d;
+  if (AS && BS) asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else if (AS) asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else if (BS) asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__host__ __device__ constexpr int dw_row_words(int nstrips, int ks) {
+  return (kX0 + nstrips * kStrip + 4 * ((ks + 3) / 4) + 8 + 3) / 4;
+}
+
 template <typename XT, typename WT, typename YT, int KS>
 __global__ void __launch_bounds__(128)
 qlinearconv_depthwise_strip(const XT* __restrict__ x, const WT* __restrict__ w, const float* __restrict__ w_scale,
                             const WT* __restrict__ w_zp, int per_channel, const int32_t* __restrict__ B, int C, int H,
                             int W, int OH, int OW, int pt, int pl, float x_scale, int x_zp, float y_scale, int y_zp,
                             float qlo, float qhi, YT* __restrict__ y) {
-  extern __shared__ __align__(16) float plf[];
+  constexpr bool XS = std::is_signed<XT>::value, WS = std::is_signed<WT>::value;
+  constexpr int TW = (KS + 3) / 4;  // words of a filter row
+  constexpr int NWD = 3 + TW;       // words loaded per input row of a strip
+  extern __shared__ __align__(16) uint32_t plw[];
   const int c = blockIdx.x % C, n = blockIdx.x / C;
   const int nstrips = (OW + kStrip - 1) / kStrip;
-  const int HP = OH + KS - 1, WPs = (nstrips * kStrip + KS - 1 + 3) & ~3;  // shared plane: HP x WPs
-  const XT* xp = x + ((int64_t)n * C + c) * H * W;
-  // shared (r, col) holds x(r - pt, col - pl) - x_zp, 0 outside the input:
-  // zero the padded plane, then scatter the plane's codes into it, read in
-  // one burst of 16-byte loads when aligned (one or two per thread)
-  for (int i = threadIdx.x; i < HP * WPs / 4; i += blockDim.x)
-    reinterpret_cast<float4*>(plf)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  const int HP = OH + KS - 1, RW = dw_row_words(nstrips, KS);
+  const uint32_t fill = (uint32_t)(uint8_t)x_zp * 0x01010101u;
+  for (int i = threadIdx.x; i < HP * RW; i += blockDim.x) plw[i] = fill;
   __syncthreads();
-  const int HW = H * W;
-  if ((reinterpret_cast<uintptr_t>(xp) & 15) == 0 && (HW & 15) == 0) {
-    for (int v16 = threadIdx.x; v16 < HW / 16; v16 += blockDim.x) {
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(xp) + v16);
-      const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
-      int r = (16 * v16) / W, col = 16 * v16 - r * W;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        plf[(r + pt) * WPs + col + pl] = (float)((int)(XT)((wd[e >> 2] >> (8 * (e & 3))) & 0xffu) - x_zp);
-        if (++col == W) {
-          col = 0;
-          ++r;
-        }
-      }
+  const XT* xp = x + ((int64_t)n * C + c) * H * W;
+  uint8_t* plb = reinterpret_cast<uint8_t*>(plw);
+  const int rows = min(H, HP - pt);  // input rows that reach an output
+  if ((W & 3) == 0 && (reinterpret_cast<uintptr_t>(xp) & 3) == 0) {
+    // the plane is contiguous: 32-bit words, consecutive threads on
+    // consecutive words, each landing at a word of its shared row
+    const int wpr = W / 4;
+    for (int i = threadIdx.x; i < rows * wpr; i += blockDim.x) {
+      const int r = i / wpr, j = i - r * wpr;
+      plw[(r + pt) * RW + kX0 / 4 + j] = __ldg(reinterpret_cast<const uint32_t*>(xp) + i);
     }
   } else {
-    for (int i = threadIdx.x; i < HW; i += blockDim.x) {
+    for (int i = threadIdx.x; i < rows * W; i += blockDim.x) {
       const int r = i / W, col = i - r * W;
-      plf[(r + pt) * WPs + col + pl] = (float)((int)xp[i] - x_zp);
+      plb[(r + pt) * RW * 4 + kX0 + col] = (uint8_t)xp[i];
     }
   }
-  const int wz = (int)w_zp[per_channel ? c : 0];
-  float wc[KS * KS];
+  // the filter rows packed four codes a word, their code sum, the constant terms
+  uint32_t wr[KS][TW];
+  int wsum = 0;
 #pragma unroll
-  for (int t = 0; t < KS * KS; ++t) wc[t] = (float)((int)w[(int64_t)c * KS * KS + t] - wz);
-  const int32_t bc = B ? B[c] : 0;
+  for (int kh = 0; kh < KS; ++kh)
+#pragma unroll
+    for (int t = 0; t < TW; ++t) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (4 * t + e < KS) {
+          const WT q = w[(int64_t)c * KS * KS + kh * KS + 4 * t + e];
+          wsum += (int)q;
+          v |= (uint32_t)(uint8_t)q << (8 * e);
+        }
+      wr[kh][t] = v;
+    }
+  // ones over the taps a filter-row word holds (all four but in the last word)
+  constexpr uint32_t ones0 = 0x01010101u >> (8 * (4 - (KS - 4 * (TW - 1))));
+  const int wz = (int)w_zp[per_channel ? c : 0];
+  const int32_t k0 = (B ? B[c] : 0) - x_zp * wsum + KS * KS * x_zp * wz;
   const float mul = __fmul_rn(x_scale, w_scale[per_channel ? c : 0]);
-  const float lo_z = qlo - (float)y_zp, hi_z = qhi - (float)y_zp;
   const float yr = quot_rcp(y_scale);
+  const float lo_z = qlo - (float)y_zp, hi_z = qhi - (float)y_zp;
   __syncthreads();
   YT* yp = y + ((int64_t)n * C + c) * OH * OW;
   const bool vec_rows = (OW % kStrip) == 0 && (reinterpret_cast<uintptr_t>(y) & 7) == 0;
-  constexpr int NV = (kStrip + KS - 1 + 3) & ~3;  // window words, whole 16-byte reads
   for (int sidx = threadIdx.x; sidx < OH * nstrips; sidx += blockDim.x) {
     const int oh = sidx / nstrips, ow0 = (sidx - oh * nstrips) * kStrip;
-    float acc[kStrip];
+    const int s0 = kX0 - pl + ow0;  // first byte of the strip's windows in a shared row
+    const uint32_t shift = 0x3210u + (uint32_t)(s0 & 3) * 0x1111u;
+    int sxw[kStrip], sx[kStrip];
 #pragma unroll
-    for (int e = 0; e < kStrip; ++e) acc[e] = 0.0f;
+    for (int e = 0; e < kStrip; ++e) sxw[e] = sx[e] = 0;
 #pragma unroll
     for (int kh = 0; kh < KS; ++kh) {
-      // 16-byte aligned: WPs and ow0 are multiples of 4 words
-      const float4* row = reinterpret_cast<const float4*>(plf + (oh + kh) * WPs + ow0);
-      float v[NV];
+      const uint32_t* row = plw + (oh + kh) * RW + (s0 >> 2);
+      uint32_t wd[NWD], a[NWD - 1];
 #pragma unroll
-      for (int q4 = 0; q4 < NV / 4; ++q4) {
-        const float4 t4 = row[q4];
-        v[4 * q4] = t4.x;
-        v[4 * q4 + 1] = t4.y;
-        v[4 * q4 + 2] = t4.z;
-        v[4 * q4 + 3] = t4.w;
-      }
+      for (int i = 0; i < NWD; ++i) wd[i] = row[i];
 #pragma unroll
-      for (int kw = 0; kw < KS; ++kw)
+      for (int i = 0; i < NWD - 1; ++i) a[i] = __byte_perm(wd[i], wd[i + 1], shift);  // bytes from s0 on
 #pragma unroll
-        for (int e = 0; e < kStrip; ++e) acc[e] = fmaf(v[e + kw], wc[kh * KS + kw], acc[e]);
+      for (int e = 0; e < kStrip; ++e)
+#pragma unroll
+        for (int t = 0; t < TW; ++t) {
+          const int k = (e >> 2) + t;
+          const uint32_t win = (e & 3) ? __byte_perm(a[k], a[k + 1], 0x3210u + (uint32_t)(e & 3) * 0x1111u) : a[k];
+          sxw[e] = dp4a<XS, WS>(win, wr[kh][t], sxw[e]);
+          sx[e] = dp4a<XS, false>(win, t == TW - 1 ? ones0 : 0x01010101u, sx[e]);
+        }
     }
     uint32_t code[kStrip];
 #pragma unroll
     for (int e = 0; e < kStrip; ++e) {
-      const int32_t a = __float2int_rn(acc[e]) + bc;
-      code[e] = quot_code_bits(__fmul_rn(__int2float_rn(a), mul), y_scale, yr, lo_z, hi_z, y_zp);
+      const int32_t acc = sxw[e] - wz * sx[e] + k0;
+      code[e] = quot_code_bits(__fmul_rn(__int2float_rn(acc), mul), y_scale, yr, lo_z, hi_z, y_zp);
     }
     YT* out = yp + oh * OW + ow0;
     if (vec_rows && ((reinterpret_cast<uintptr_t>(out) & 7) == 0)) {
@@ -312,9 +343,10 @@ int run_direct(const ConvShape& s, const void* x, float x_scale, int x_zp, const
   {
     // strip kernel: depthwise 3x3 / 5x5, stride 1, dilation 1
     const int64_t nstrips = (s.OW + kStrip - 1) / kStrip;
-    const size_t ssmem = (size_t)(s.OH + s.kH - 1) * ((nstrips * kStrip + s.kW - 1 + 3) & ~3) * 4;
+    const size_t ssmem = (size_t)(s.OH + s.kH - 1) * dw_row_words((int)std::min<int64_t>(nstrips, 1 << 20), (int)s.kW) * 4;
     if (s.group == s.C && s.M == s.C && s.Cg == 1 && s.sh == 1 && s.sw == 1 && s.dh == 1 && s.dw == 1 &&
-        s.kH == s.kW && (s.kH == 3 || s.kH == 5) && ssmem <= 160 * 1024 && !getenv("I8Q_FORCE_CONV_HALO")) {
+        s.kH == s.kW && (s.kH == 3 || s.kH == 5) && s.pl <= kX0 && ssmem <= 160 * 1024 &&
+        !getenv("I8Q_FORCE_CONV_HALO")) {
       auto kern = s.kH == 3 ? qlinearconv_depthwise_strip<XT, WT, YT, 3> : qlinearconv_depthwise_strip<XT, WT, YT, 5>;
       if (ssmem > 48 * 1024)
         I8Q_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem));
