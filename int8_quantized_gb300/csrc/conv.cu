@@ -222,9 +222,16 @@ qlinearconv_depthwise_strip(const XT* __restrict__ x, const WT* __restrict__ w, 
     // the plane is contiguous: 32-bit words, consecutive threads on
     // consecutive words, each landing at a word of its shared row
     const int wpr = W / 4;
+    const int dr = (int)blockDim.x / wpr, dj = (int)blockDim.x - dr * wpr;  // the stride as (rows, words)
+    int r = (int)threadIdx.x / wpr, j = (int)threadIdx.x - r * wpr;
     for (int i = threadIdx.x; i < rows * wpr; i += blockDim.x) {
-      const int r = i / wpr, j = i - r * wpr;
       plw[(r + pt) * RW + kX0 / 4 + j] = __ldg(reinterpret_cast<const uint32_t*>(xp) + i);
+      r += dr;
+      j += dj;
+      if (j >= wpr) {
+        j -= wpr;
+        ++r;
+      }
     }
   } else {
     for (int i = threadIdx.x; i < rows * W; i += blockDim.x) {
@@ -259,8 +266,10 @@ qlinearconv_depthwise_strip(const XT* __restrict__ x, const WT* __restrict__ w, 
   __syncthreads();
   YT* yp = y + ((int64_t)n * C + c) * OH * OW;
   const bool vec_rows = (OW % kStrip) == 0 && (reinterpret_cast<uintptr_t>(y) & 7) == 0;
+  const int doh = (int)blockDim.x / nstrips, dst = (int)blockDim.x - doh * nstrips;  // the stride as (rows, strips)
+  int oh = (int)threadIdx.x / nstrips, st = (int)threadIdx.x - oh * nstrips;
   for (int sidx = threadIdx.x; sidx < OH * nstrips; sidx += blockDim.x) {
-    const int oh = sidx / nstrips, ow0 = (sidx - oh * nstrips) * kStrip;
+    const int ow0 = st * kStrip;
     const int s0 = kX0 - pl + ow0;  // first byte of the strip's windows in a shared row
     const uint32_t shift = 0x3210u + (uint32_t)(s0 & 3) * 0x1111u;
     int sxw[kStrip], sx[kStrip];
@@ -298,6 +307,12 @@ qlinearconv_depthwise_strip(const XT* __restrict__ x, const WT* __restrict__ w, 
 #pragma unroll
       for (int e = 0; e < kStrip; ++e)
         if (ow0 + e < OW) out[e] = (YT)code[e];
+    }
+    oh += doh;
+    st += dst;
+    if (st >= nstrips) {
+      st -= nstrips;
+      ++oh;
     }
   }
 }
