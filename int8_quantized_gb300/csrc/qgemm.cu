@@ -382,13 +382,13 @@ int launch_center(const void* X, int type, int64_t R, int64_t K, int64_t Kp, int
   const auto* x8 = static_cast<const uint8_t*>(X);
   if (k_fast && vec) {
     // no transpose: a stream; one wave of resident blocks
-    static int per_sm = 0;
-    if (per_sm == 0) {
+    static const int per_sm = [] {
       int a = 0, b = 0;
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, center_rows<true>, 256, 0);
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, center_rows<false>, 256, 0);
-      per_sm = std::max(1, std::min(a, b));
-    }
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, center_rows<true>, 256, 0) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, center_rows<false>, 256, 0) != cudaSuccess)
+        cudaGetLastError();
+      return std::max(1, std::min(a, b));
+    }();
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(ceil_div(R * (Kp / 16), 256 * 4),
                                                                   (int64_t)sm_count() * per_sm));
     if (type == I8Q_S8) center_rows<true><<<(unsigned)blocks, 256, 0, s>>>(x8, R, K, Kp, Xc, sums);
