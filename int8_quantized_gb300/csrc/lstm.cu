@@ -747,7 +747,7 @@ __device__ __forceinline__ bool wait_bar_idle(uint32_t bar, uint32_t parity, vol
   unsigned long long t0 = 0;
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    __nanosleep(128);
+    __nanosleep(32);
     if ((i & 15u) == 15u) {
       if (*abort_flag) return false;
       const unsigned long long now = global_ns();
