@@ -376,7 +376,10 @@ size_t i8q_matmul_integer_workspace_size(int64_t M, int64_t N, int64_t K);
  *   add: C = (A_scale * (A - A_zp) + B_scale * (B - B_zp)) / C_scale + C_zp
  *   mul: C = ((A - A_zp) * (B - B_zp)) * (A_scale * B_scale) / C_scale + C_zp
  * evaluated in the order written (fp32, each operation rounded once), then
- * round half to even and saturation. */
+ * round half to even and saturation.  Large outputs go through the table of
+ * all 256 x 256 codes; the library keeps up to 16 such tables (64 KB each,
+ * in static device memory of each GPU that loads it) for parameter sets
+ * seen before, and computes the table inside the call otherwise. */
 int i8q_qlinear_binary(int op, const void* A, const int64_t* a_shape, int a_rank, float a_scale, int a_zero_point,
                        const void* B, const int64_t* b_shape, int b_rank, float b_scale, int b_zero_point,
                        float c_scale, int c_zero_point, int qtype, void* C, void* stream);

@@ -17,6 +17,7 @@
 // operator's 256 possible outputs are computed once per block, with the same
 // arithmetic, into a table replicated per lane in shared memory (entry e of
 // lane l at word e * 32 + l, so every lookup of a warp is conflict-free).
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -117,18 +118,36 @@ binary_fast(const uint8_t* __restrict__ A, int amode, int64_t aper, const uint8_
 // in binary_fast.
 constexpr int kTabThreads = 1024, kTabBytes = 65536;
 
+// Word wi of the table: the codes of (a, 4w' .. 4w' + 3), wi = a * 64 + w'.
+template <bool AS, bool BS>
+__device__ __forceinline__ uint32_t table_word(int wi, const BinParams& p) {
+  const uint32_t a = (uint32_t)wi >> 6, b0 = ((uint32_t)wi & 63u) * 4u;
+  int32_t unused;
+  return pack_low_bytes(binary_one<AS, BS>(a, b0, p, &unused), binary_one<AS, BS>(a, b0 + 1, p, &unused),
+                        binary_one<AS, BS>(a, b0 + 2, p, &unused), binary_one<AS, BS>(a, b0 + 3, p, &unused));
+}
+
+// The table in global memory, one word per thread (kept for later calls
+// with the same parameters, see table_slot).
+template <bool AS, bool BS>
+__global__ void __launch_bounds__(256) build_binary_table(BinParams p, uint32_t* __restrict__ table) {
+  const int wi = blockIdx.x * blockDim.x + threadIdx.x;
+  if (wi < kTabBytes / 4) table[wi] = table_word<AS, BS>(wi, p);
+}
+
 // SAME: both operands have the output's shape (modes 0), the common case,
-// compiled without the broadcast branches.
+// compiled without the broadcast branches.  The shared table is copied from
+// a prebuilt global one when given (64 KB from L2), else computed here.
 template <bool AS, bool BS, bool SAME>
 __global__ void __launch_bounds__(kTabThreads, 1)
 binary_table(const uint8_t* __restrict__ A, int amode, int64_t aper, const uint8_t* __restrict__ B, int bmode,
-             int64_t bper, int64_t n, BinParams p, uint8_t* __restrict__ C) {
+             int64_t bper, int64_t n, BinParams p, const uint32_t* __restrict__ gtab, uint8_t* __restrict__ C) {
   extern __shared__ uint32_t tab[];  // 16384 words, codes (a, 4w' .. 4w' + 3) in word a * 64 + w'
-  for (int wi = threadIdx.x; wi < kTabBytes / 4; wi += kTabThreads) {
-    const uint32_t a = (uint32_t)wi >> 6, b0 = ((uint32_t)wi & 63u) * 4u;
-    int32_t unused;
-    tab[wi] = pack_low_bytes(binary_one<AS, BS>(a, b0, p, &unused), binary_one<AS, BS>(a, b0 + 1, p, &unused),
-                             binary_one<AS, BS>(a, b0 + 2, p, &unused), binary_one<AS, BS>(a, b0 + 3, p, &unused));
+  if (gtab) {
+    for (int q = threadIdx.x; q < kTabBytes / 16; q += kTabThreads)
+      reinterpret_cast<uint4*>(tab)[q] = __ldg(reinterpret_cast<const uint4*>(gtab) + q);
+  } else {
+    for (int wi = threadIdx.x; wi < kTabBytes / 4; wi += kTabThreads) tab[wi] = table_word<AS, BS>(wi, p);
   }
   __syncthreads();
   const uint8_t* t8 = reinterpret_cast<const uint8_t*>(tab);
@@ -350,6 +369,66 @@ int fast_mode(const Strides& st, bool is_a, int64_t numel, int64_t* period) {
   return numel % 16 == 0 ? 2 : -1;
 }
 
+// Tables kept in file-scope device memory (no allocation), up to kTabSlots
+// per device, each written once for one (signedness, parameters) key and
+// never again, so any stream may read it after waiting on the event that
+// follows its build.  When the slots are taken, the table is computed inside
+// the product kernel.
+constexpr int kTabSlots = 16, kTabMaxDev = 64;
+static __device__ __align__(16) uint32_t g_tables[kTabSlots][kTabBytes / 4];
+
+struct TabSlot {
+  bool used = false;
+  int as = 0, bs = 0;
+  BinParams p{};
+  cudaEvent_t ready = nullptr;
+};
+std::mutex g_tab_mu;
+TabSlot g_tab[kTabMaxDev][kTabSlots];
+uint32_t* g_tab_base[kTabMaxDev] = {nullptr};
+
+bool same_params(const BinParams& a, const BinParams& b) { return std::memcmp(&a, &b, sizeof(BinParams)) == 0; }
+
+// The prebuilt table for p on this device, built on s the first time (s
+// waits for it after), or null when no slot is free.
+template <bool AS, bool BS>
+int table_slot(const BinParams& p, cudaStream_t s, const uint32_t** out) {
+  *out = nullptr;
+  int dev = 0;
+  I8Q_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kTabMaxDev) return I8Q_OK;
+  std::lock_guard<std::mutex> lk(g_tab_mu);
+  if (!g_tab_base[dev]) {
+    void* base = nullptr;
+    I8Q_CUDA_TRY(cudaGetSymbolAddress(&base, g_tables));
+    g_tab_base[dev] = static_cast<uint32_t*>(base);
+  }
+  for (int i = 0; i < kTabSlots; ++i) {
+    TabSlot& t = g_tab[dev][i];
+    if (t.used && t.as == AS && t.bs == BS && same_params(t.p, p)) {
+      I8Q_CUDA_TRY(cudaStreamWaitEvent(s, t.ready, 0));
+      *out = g_tab_base[dev] + (size_t)i * (kTabBytes / 4);
+      return I8Q_OK;
+    }
+  }
+  for (int i = 0; i < kTabSlots; ++i) {
+    TabSlot& t = g_tab[dev][i];
+    if (t.used) continue;
+    if (!t.ready) I8Q_CUDA_TRY(cudaEventCreateWithFlags(&t.ready, cudaEventDisableTiming));
+    uint32_t* tab = g_tab_base[dev] + (size_t)i * (kTabBytes / 4);
+    build_binary_table<AS, BS><<<kTabBytes / 4 / 256, 256, 0, s>>>(p, tab);
+    I8Q_LAUNCH_CHECK("build_binary_table");
+    I8Q_CUDA_TRY(cudaEventRecord(t.ready, s));
+    t.used = true;
+    t.as = AS;
+    t.bs = BS;
+    t.p = p;
+    *out = tab;
+    return I8Q_OK;
+  }
+  return I8Q_OK;
+}
+
 template <bool AS, bool BS>
 int run_binary(const uint8_t* A, const uint8_t* B, const Strides& st, int64_t n, int64_t an, int64_t bn,
                const BinParams& p, void* C, cudaStream_t s) {
@@ -368,11 +447,16 @@ int run_binary(const uint8_t* A, const uint8_t* B, const Strides& st, int64_t n,
     });
     I8Q_CUDA_TRY(attr);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), ceil_div(n / 16, (int64_t)kTabThreads)));
+    const uint32_t* gtab = nullptr;
+    if (!getenv("I8Q_QEW_NO_TABLE_CACHE")) {
+      const int rc = table_slot<AS, BS>(p, s, &gtab);
+      if (rc) return rc;
+    }
     if (am == 0 && bm == 0)
-      binary_table<AS, BS, true><<<grid, kTabThreads, kTabBytes, s>>>(A, am, aper, B, bm, bper, n, p,
+      binary_table<AS, BS, true><<<grid, kTabThreads, kTabBytes, s>>>(A, am, aper, B, bm, bper, n, p, gtab,
                                                                        static_cast<uint8_t*>(C));
     else
-      binary_table<AS, BS, false><<<grid, kTabThreads, kTabBytes, s>>>(A, am, aper, B, bm, bper, n, p,
+      binary_table<AS, BS, false><<<grid, kTabThreads, kTabBytes, s>>>(A, am, aper, B, bm, bper, n, p, gtab,
                                                                         static_cast<uint8_t*>(C));
     I8Q_LAUNCH_CHECK("binary_table");
     done = (n / 16) * 16;

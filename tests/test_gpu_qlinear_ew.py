@@ -104,6 +104,27 @@ def test_large_same_shape(orc, dev):
     binary(orc, dev, "mul", A, 0.02, 128, B, 0.03, 120, 0.05, 125)
 
 
+def test_table_cache_hits_and_overflow(orc, dev, monkeypatch):
+    """The code tables kept across calls: the same parameters twice (the
+    second call reuses the first call's table), from a second stream, and
+    more distinct parameter sets than the kept slots (the rest compute their
+    table inside the kernel); every result against the oracle."""
+    rng = np.random.default_rng(21)
+    A = rng.integers(0, 256, (1 << 20,)).astype(np.uint8)
+    B = rng.integers(0, 256, (1 << 20,)).astype(np.uint8)
+    for k in range(20):
+        cs = 0.04 + 0.001 * k
+        binary(orc, dev, "add", A, 0.02, 128, B, 0.03, 120, cs, 125)
+        if k % 7 == 0:
+            binary(orc, dev, "add", A, 0.02, 128, B, 0.03, 120, cs, 125)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        binary(orc, dev, "mul", A, 0.02, 128, B, 0.03, 120, 0.041, 125)
+    binary(orc, dev, "mul", A, 0.02, 128, B, 0.03, 120, 0.041, 125)
+    monkeypatch.setenv("I8Q_QEW_NO_TABLE_CACHE", "1")
+    binary(orc, dev, "add", A, 0.02, 128, B, 0.03, 120, 0.04, 125)
+
+
 @pytest.mark.parametrize("qt", ["u8", "s8"])
 @pytest.mark.parametrize("bshape", [(), (4096,), (1024, 4096)])
 def test_large_broadcast(orc, dev, qt, bshape):
