@@ -101,15 +101,15 @@ __device__ __forceinline__ int64_t channel_of(int64_t e, int64_t c_tile, int off
 // Per tensor, or the last axis with a grid stride of whole channel cycles:
 // every tile of a warp sees the same parameters, so they are loaded once and
 // held in registers.  On the last axis those are 16 channels' worth, which
-// leaves room for 3 blocks per SM; two warp tiles are then loaded before
-// either is used, to keep enough reads in flight.  Per tensor, one scalar
-// pair leaves room for 6 blocks per SM, enough with one tile.
+// leaves room for 4 blocks per SM with one warp tile in flight (measured
+// slightly ahead of 3 blocks with two tiles each); per tensor, one scalar
+// pair leaves room for 6 blocks per SM.
 template <int MODE, typename QT>
-__global__ void __launch_bounds__(256) quantize_fixed(const float* __restrict__ x, QT* __restrict__ y, int64_t ntiles,
+__global__ void __launch_bounds__(256, MODE == AX_TENSOR ? 6 : 4) quantize_fixed(const float* __restrict__ x, QT* __restrict__ y, int64_t ntiles,
                                                      const float* __restrict__ scale, const QT* __restrict__ zp,
                                                      int64_t axis_len) {
   static_assert(MODE == AX_TENSOR || MODE == AX_LAST, "fixed parameters: per tensor or the last axis");
-  constexpr int U = MODE == AX_TENSOR ? 1 : 2;
+  constexpr int U = 1;
   const int lane = threadIdx.x & 31;
   const int64_t wstride = ((int64_t)gridDim.x * blockDim.x) >> 5;
   int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
