@@ -239,6 +239,37 @@ __device__ __forceinline__ void store_slice_tma(const CUtensorMap* tmC, int64_t 
   }
 }
 
+// The same slice for fp32 outputs: 8-column chunks (32 rows x 32 bytes)
+// through the warp's staging buffer, one bulk store each.
+template <int ACT>
+__device__ __forceinline__ void store_slice_tma_f32(const CUtensorMap* tmC, int64_t M, int64_t N, int64_t row0,
+                                                    int64_t col0, int lane, const int32_t (&run)[SLICE], int32_t zA,
+                                                    float sA, const int32_t* pc, const float* ps, const float* pb,
+                                                    uint8_t* stg) {
+  const uint32_t stg_s = smem_u32(stg);
+#pragma unroll
+  for (int ch = 0; ch < SLICE / 8; ++ch) {
+    float2 o[4];
+    epi8<ACT, false>(run, ch * 8, zA, sA, pc, ps, pb, o);
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
+    uint4* d = reinterpret_cast<uint4*>(stg + lane * 32);
+    d[0] = make_uint4(__float_as_uint(o[0].x), __float_as_uint(o[0].y), __float_as_uint(o[1].x),
+                      __float_as_uint(o[1].y));
+    d[1] = make_uint4(__float_as_uint(o[2].x), __float_as_uint(o[2].y), __float_as_uint(o[3].x),
+                      __float_as_uint(o[3].y));
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      const int64_t x = col0 + ch * 8;
+      if (x < N && row0 < M) {
+        tma_store_2d(tmC, stg_s, (int)x, (int)row0);
+        bulk_commit();
+      }
+    }
+  }
+}
+
 // Epilogue of one row's 64-column slice for the 8-bit-code products (see
 // QgEpilogue): column parameters pg (g), pe (e), pb (bsc), pz (bias) from
 // shared memory; rs, dr, ar: the row's rowsum, d and asc.
@@ -632,8 +663,10 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
   return r;
 }
 
-// TMA_C: bf16 C of EPI_DYN stored by TMA through per-warp staging.
-template <int EPI, bool TMA_C = false>
+// TMA_C: outputs stored by TMA through per-warp staging (1: the 8-bit-code
+// products' Y, or bf16 C of EPI_DYN; 2: fp32 C of EPI_DYN); 0: stored
+// directly.
+template <int EPI, int TMA_C = 0>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, TcParams p) {
@@ -843,7 +876,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         __syncwarp();
         continue;
       }
-      if constexpr (EPI == EPI_DYN && TMA_C) {
+      if constexpr (EPI == EPI_DYN && TMA_C == 1) {
         {
           const bool in = row < p.M;
           const float sA = in ? __ldg(p.ep.scaleA + row) : 0.0f;
@@ -858,6 +891,20 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           __syncwarp();
           continue;
         }
+      }
+      if constexpr (EPI == EPI_DYN && TMA_C == 2) {
+        const bool in = row < p.M;
+        const float sA = in ? __ldg(p.ep.scaleA + row) : 0.0f;
+        const int32_t zA = in ? __ldg(p.ep.zeroA + row) - 128 : 0;  // A entered as uA - 128
+        uint8_t* stg = stg_all + (warp - 2) * 1024;
+        if (p.ep.act == I8Q_ACT_GELU)
+          store_slice_tma_f32<I8Q_ACT_GELU>(&tmC, p.M, p.N, row0, col0, lane, run, zA, sA, pc, ps, pb, stg);
+        else if (p.ep.act == I8Q_ACT_RELU)
+          store_slice_tma_f32<I8Q_ACT_RELU>(&tmC, p.M, p.N, row0, col0, lane, run, zA, sA, pc, ps, pb, stg);
+        else
+          store_slice_tma_f32<I8Q_ACT_IDENTITY>(&tmC, p.M, p.N, row0, col0, lane, run, zA, sA, pc, ps, pb, stg);
+        __syncwarp();
+        continue;
       }
       if (row < p.M) finish_row<EPI>(p, row, col0, run, pc, ps, pb, pd);
       __syncwarp();
@@ -887,8 +934,12 @@ int pair_max_clusters() {
   std::call_once(once, [] {
     err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  P_SMEM_BYTES);
+    if constexpr (EPI == EPI_DYN)
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   P_SMEM_BYTES);
     if (err != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -977,16 +1028,19 @@ int launch_tc_impl(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     I8Q_PROF(prof2, s);
-    // bf16 C of the dynamic inner product goes out by TMA when its rows
-    // are 16-byte aligned
+    // bf16 or fp32 C of the dynamic inner product goes out by TMA when its
+    // rows are 16-byte aligned
     CUtensorMap pC = pA;
-    bool tma_c = false;
+    int tma_c = 0;
     if constexpr (EPI == EPI_DYN) {
-      if (p.ep.out_mode == OUT_BF16 && p.ep.ldc % 8 == 0 && (reinterpret_cast<uintptr_t>(p.ep.C) & 15) == 0 &&
-          M < ((int64_t)1 << 31) && N < ((int64_t)1 << 31) && !getenv("I8Q_GEMM_DIRECT_STORE")) {
-        rc = make_map_plain_2d(&pC, p.ep.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, p.ep.ldc * 2, 16, 32, "gemm_tc");
+      const bool bf = p.ep.out_mode == OUT_BF16;
+      if ((bf || p.ep.out_mode == OUT_F32) && (p.ep.ldc * (bf ? 2 : 4)) % 16 == 0 &&
+          (reinterpret_cast<uintptr_t>(p.ep.C) & 15) == 0 && M < ((int64_t)1 << 31) && N < ((int64_t)1 << 31) &&
+          !getenv("I8Q_GEMM_DIRECT_STORE")) {
+        rc = make_map_plain_2d(&pC, p.ep.C, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N,
+                               M, p.ep.ldc * (bf ? 2 : 4), bf ? 16 : 8, 32, "gemm_tc");
         if (rc) return rc;
-        tma_c = true;
+        tma_c = bf ? 1 : 2;
       }
     }
     if constexpr (EPI == EPI_QG) {
@@ -998,15 +1052,22 @@ int launch_tc_impl(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M,
                                esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT8, N, M,
                                p.qg.ldy * esz, 32 / esz, 32, "gemm_tc");
         if (rc) return rc;
-        tma_c = true;
+        tma_c = 1;
+      }
+    }
+    if constexpr (EPI == EPI_DYN) {
+      if (tma_c == 2) {
+        I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI, 2>, pA, pB, pC, p));
+        I8Q_LAUNCH_CHECK("gemm_tc_pair_kernel");
+        return I8Q_OK;
       }
     }
     if (tma_c) {
-      I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI, true>, pA, pB, pC, p));
+      I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI, 1>, pA, pB, pC, p));
       I8Q_LAUNCH_CHECK("gemm_tc_pair_kernel");
       return I8Q_OK;
     }
-    I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI, false>, pA, pB, pC, p));
+    I8Q_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI, 0>, pA, pB, pC, p));
     I8Q_LAUNCH_CHECK("gemm_tc_pair_kernel");
     return I8Q_OK;
   }
