@@ -246,6 +246,29 @@ def test_chunk_boundaries(orc, dev, K):
     run_case(orc, dev, A, iB=iB, scaleB=rng.uniform(1e-3, 1e-2, N).astype(np.float32), bias=None)
 
 
+@pytest.mark.parametrize("register", [False, True])
+@pytest.mark.parametrize("typeA,K,M", [("f32", 2056, 1237), ("f32", 3200, 1300), ("bf16", 4104, 1237),
+                                       ("bf16", 2048, 1300), ("f32", 1024, 1237)])
+def test_row_quantization_forms(orc, dev, core, monkeypatch, register, typeA, K, M):
+    """Rows of A long enough for the shared-memory staged form (more than
+    2048 elements, at least 152 groups of 8 rows, a ragged last group) and
+    shorter ones that take the register form, each also forced to the
+    register form or its fallback: all codes, scales and zero points."""
+    if core != "tc2":
+        pytest.skip("row quantization does not depend on the integer core")
+    if register:
+        monkeypatch.setenv("I8Q_ROWS_REGISTER", "1")
+    rng = np.random.default_rng(K + M)
+    A = rng.normal(0, 1, (M, K)).astype(np.float32)
+    A[::5, ::7] *= 40.0
+    A[3] = 0.0
+    if typeA == "bf16":
+        A = (A.view(np.uint32) >> 16).astype(np.uint16)
+    iB = rng.integers(-128, 128, (K, 32)).astype(np.int8)
+    run_case(orc, dev, A, iB=iB, scaleB=rng.uniform(1e-3, 1e-2, 32).astype(np.float32), bias=None, typeA=typeA,
+             rows=np.array([0, 3, 5, 600, M - 2, M - 1]))
+
+
 @pytest.mark.parametrize("M,N,K,expect", [(64, 128, 256, "dp4a"), (1, 7, 3, "dp4a"), (8192, 14336, 4096, "tcgen05"),
                                           (64, 1024, 4096, "tcgen05"), (64, 128, 10000, "tcgen05")])
 def test_default_core_choice(monkeypatch, core, M, N, K, expect):
