@@ -248,12 +248,14 @@ def test_chunk_boundaries(orc, dev, K):
 
 @pytest.mark.parametrize("register", [False, True])
 @pytest.mark.parametrize("typeA,K,M", [("f32", 2056, 1237), ("f32", 3200, 1300), ("bf16", 4104, 1237),
-                                       ("bf16", 2048, 1300), ("f32", 1024, 1237)])
+                                       ("f32", 4104, 701), ("bf16", 2048, 1300), ("f32", 1024, 1237),
+                                       ("f32", 6408, 640)])
 def test_row_quantization_forms(orc, dev, core, monkeypatch, register, typeA, K, M):
     """Rows of A long enough for the shared-memory staged form (more than
-    2048 elements, at least 152 groups of 8 rows, a ragged last group) and
-    shorter ones that take the register form, each also forced to the
-    register form or its fallback: all codes, scales and zero points."""
+    2048 elements, at least 152 groups of 4 rows, a ragged last group),
+    shorter ones that take the register form, fp32 rows of 6408 too long for
+    either (CTA per row), each also forced to the register form or its
+    fallback: codes, scales and zero points of sampled rows."""
     if core != "tc2":
         pytest.skip("row quantization does not depend on the integer core")
     if register:
