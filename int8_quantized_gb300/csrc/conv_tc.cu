@@ -365,22 +365,29 @@ center_x_nhwc(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __n
 
 // Same result, one CTA per (n, h): the whole NHWC row xc[n][h][:][:] is
 // W * Cp * 2 contiguous bytes.  Inputs land in shared memory as [w][c] with
-// a row stride of Cp + 2 halfwords (consecutive w fall in consecutive banks),
-// then leave in 16-byte pieces of the contiguous output row.
+// a row stride of Cp + 8 halfwords (16-byte aligned rows, read back as 16-byte
+// vectors) and, within a row, 4-pair groups of channels XOR-swizzled by the
+// 8-pixel piece (w / 8) so the stores of one warp spread over the banks;
+// then they leave in 16-byte pieces of the contiguous output row.
+__device__ __forceinline__ int center_swz(int w) { return ((w >> 3) & 7) << 2; }  // in channel pairs
+
 template <typename XT>
 __global__ void __launch_bounds__(256)
 center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv_bfloat16* __restrict__ xc) {
-  extern __shared__ uint16_t rowt[];  // W x (Cp + 2)
+  extern __shared__ __align__(16) uint16_t rowt[];  // W x (Cp + 8)
   const int n = blockIdx.y, h = blockIdx.x;
-  const int ld = Cp + 2;
+  const int ld = Cp + 8, ldw = ld / 2;
   const XT* xr = x + ((int64_t)n * C * H + h) * W;  // + c * H * W + w
+  uint32_t* rw = reinterpret_cast<uint32_t*>(rowt);
   if ((W & 7) == 0 && ((int64_t)H * W) % 8 == 0 && (reinterpret_cast<uintptr_t>(xr) & 7) == 0) {
     // 8-byte pieces of two adjacent channel rows per work item (their codes
     // meet in 32-bit shared stores), four items in flight per thread
     const int cw = W / 8, pairs = Cp / 2, total = pairs * cw;
     const uint32_t flip = std::is_signed<XT>::value ? 0x80808080u : 0u;  // signed codes as unsigned + 128
     const int xzu = std::is_signed<XT>::value ? xz + 128 : xz;
-    uint32_t* rw = reinterpret_cast<uint32_t*>(rowt);
+    // code b as the fp32 1.5 * 2^23 + b (one byte permute), minus 1.5 * 2^23 + xz:
+    // exactly b - xz (|b - xz| <= 255), whose bf16 is the top half
+    const float zf = __int_as_float(0x4B400000 + xzu);
     for (int base = 0; base < total; base += 4 * blockDim.x) {
       uint2 v[4][2];
       int cp[4], ww[4];
@@ -400,14 +407,14 @@ center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv
       for (int u = 0; u < 4; ++u) {
         if (cp[u] >= pairs) continue;
         const bool in0 = 2 * cp[u] < C, in1 = 2 * cp[u] + 1 < C;
+        uint32_t* dst = rw + ww[u] * ldw + (cp[u] ^ center_swz(ww[u]));
+        const uint32_t a[2] = {v[u][0].x ^ flip, v[u][0].y ^ flip}, b[2] = {v[u][1].x ^ flip, v[u][1].y ^ flip};
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const uint32_t b0 = ((e < 4 ? v[u][0].x : v[u][0].y) ^ flip) >> (8 * (e & 3)) & 0xffu;
-          const uint32_t b1 = ((e < 4 ? v[u][1].x : v[u][1].y) ^ flip) >> (8 * (e & 3)) & 0xffu;
-          // x - xz as fp32 through the 1.5 * 2^23 bit pattern (exact: |x - xz| <= 255); bf16 = top half
-          const uint32_t f0 = in0 ? __float_as_uint(__fsub_rn(__int_as_float(0x4B400000 + (int)b0 - xzu), 12582912.0f)) : 0u;
-          const uint32_t f1 = in1 ? __float_as_uint(__fsub_rn(__int_as_float(0x4B400000 + (int)b1 - xzu), 12582912.0f)) : 0u;
-          rw[((ww[u] + e) * ld + 2 * cp[u]) >> 1] = (f0 >> 16) | (f1 & 0xffff0000u);
+          const uint32_t sel = 0x7640u + (e & 3);
+          const float f0 = in0 ? __fsub_rn(__uint_as_float(__byte_perm(a[e >> 2], 0x4B400000u, sel)), zf) : 0.0f;
+          const float f1 = in1 ? __fsub_rn(__uint_as_float(__byte_perm(b[e >> 2], 0x4B400000u, sel)), zf) : 0.0f;
+          dst[e * ldw] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
         }
       }
     }
@@ -417,7 +424,7 @@ center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv
       for (int w = lane; w < W; w += 32) {
         float v = 0.0f;
         if (c < C) v = (float)((int)xr[(int64_t)c * H * W + w] - xz);
-        rowt[w * ld + c] = (uint16_t)(__float_as_uint(v) >> 16);  // exact: |v| <= 255
+        rowt[w * ld + (c ^ (center_swz(w) << 1))] = (uint16_t)(__float_as_uint(v) >> 16);  // exact: |v| <= 255
       }
   }
   __syncthreads();
@@ -425,8 +432,7 @@ center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv
   const int per_w = Cp / 8;
   for (int qi = threadIdx.x; qi < W * per_w; qi += blockDim.x) {
     const int w = qi / per_w, c8 = (qi - w * per_w) * 8;
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(rowt + w * ld + c8);
-    dst[qi] = make_uint4(src[0], src[1], src[2], src[3]);
+    dst[qi] = *reinterpret_cast<const uint4*>(rw + w * ldw + ((c8 >> 1) ^ center_swz(w)));
   }
 }
 
@@ -496,7 +502,7 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
   if (!status) return fail(I8Q_ERR_CUDA, "qlinearconv: no device status word");
   {
     I8Q_PROF("conv_center_operands", s);
-    const size_t row_smem = (size_t)W * (Cp + 2) * 2;
+    const size_t row_smem = (size_t)W * (Cp + 8) * 2;
     if (row_smem <= 200 * 1024) {
       static std::once_flag once_u8, once_s8;
       if (xtype == I8Q_U8) {
