@@ -372,7 +372,7 @@ center_x_nhwc(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __n
 __device__ __forceinline__ int center_swz(int w) { return ((w >> 3) & 7) << 2; }  // in channel pairs
 
 template <typename XT>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 6)
 center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv_bfloat16* __restrict__ xc) {
   extern __shared__ __align__(16) uint16_t rowt[];  // W x (Cp + 8)
   const int n = blockIdx.y, h = blockIdx.x;
@@ -388,33 +388,52 @@ center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv
     // code b as the fp32 1.5 * 2^23 + b (one byte permute), minus 1.5 * 2^23 + xz:
     // exactly b - xz (|b - xz| <= 255), whose bf16 is the top half
     const float zf = __int_as_float(0x4B400000 + xzu);
+    // (pair, piece) of item idx = base + tid + u * blockDim.x, advanced
+    // without division
+    const int dq = blockDim.x / cw, dr = blockDim.x - dq * cw;
+    int cpn = threadIdx.x / cw, pcn = threadIdx.x - cpn * cw;
     for (int base = 0; base < total; base += 4 * blockDim.x) {
       uint2 v[4][2];
       int cp[4], ww[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int idx = base + threadIdx.x + u * blockDim.x;
-        cp[u] = idx < total ? idx / cw : pairs;
-        ww[u] = (idx - cp[u] * cw) * 8;
+        const bool live = base + (int)threadIdx.x + u * (int)blockDim.x < total;
+        cp[u] = live ? cpn : pairs;
+        ww[u] = pcn * 8;
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-          const int c = 2 * cp[u] + h2;
-          v[u][h2] = (idx < total && c < C) ? __ldg(reinterpret_cast<const uint2*>(xr + (int64_t)c * H * W + ww[u]))
-                                            : make_uint2(0, 0);
+          const int c = 2 * cpn + h2;
+          v[u][h2] = (live && c < C) ? __ldg(reinterpret_cast<const uint2*>(xr + (int64_t)c * H * W + ww[u]))
+                                     : make_uint2(0, 0);
+        }
+        cpn += dq;
+        pcn += dr;
+        if (pcn >= cw) {
+          pcn -= cw;
+          ++cpn;
         }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (cp[u] >= pairs) continue;
-        const bool in0 = 2 * cp[u] < C, in1 = 2 * cp[u] + 1 < C;
         uint32_t* dst = rw + ww[u] * ldw + (cp[u] ^ center_swz(ww[u]));
         const uint32_t a[2] = {v[u][0].x ^ flip, v[u][0].y ^ flip}, b[2] = {v[u][1].x ^ flip, v[u][1].y ^ flip};
+        if (2 * cp[u] + 1 < C) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t sel = 0x7640u + (e & 3);
-          const float f0 = in0 ? __fsub_rn(__uint_as_float(__byte_perm(a[e >> 2], 0x4B400000u, sel)), zf) : 0.0f;
-          const float f1 = in1 ? __fsub_rn(__uint_as_float(__byte_perm(b[e >> 2], 0x4B400000u, sel)), zf) : 0.0f;
-          dst[e * ldw] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t sel = 0x7640u + (e & 3);
+            const float f0 = __fsub_rn(__uint_as_float(__byte_perm(a[e >> 2], 0x4B400000u, sel)), zf);
+            const float f1 = __fsub_rn(__uint_as_float(__byte_perm(b[e >> 2], 0x4B400000u, sel)), zf);
+            dst[e * ldw] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+          }
+        } else {  // channel padding: zeros beyond C
+          const bool in0 = 2 * cp[u] < C;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t sel = 0x7640u + (e & 3);
+            const float f0 = in0 ? __fsub_rn(__uint_as_float(__byte_perm(a[e >> 2], 0x4B400000u, sel)), zf) : 0.0f;
+            dst[e * ldw] = __float_as_uint(f0) >> 16;
+          }
         }
       }
     }
@@ -430,9 +449,16 @@ center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv
   __syncthreads();
   uint4* dst = reinterpret_cast<uint4*>(xc + ((int64_t)n * H + h) * W * Cp);
   const int per_w = Cp / 8;
+  const int sq = blockDim.x / per_w, sr = blockDim.x - sq * per_w;
+  int w = threadIdx.x / per_w, g8 = threadIdx.x - w * per_w;  // pixel, 8-channel group of qi
   for (int qi = threadIdx.x; qi < W * per_w; qi += blockDim.x) {
-    const int w = qi / per_w, c8 = (qi - w * per_w) * 8;
-    dst[qi] = *reinterpret_cast<const uint4*>(rw + w * ldw + ((c8 >> 1) ^ center_swz(w)));
+    dst[qi] = *reinterpret_cast<const uint4*>(rw + w * ldw + ((g8 * 4) ^ center_swz(w)));
+    w += sq;
+    g8 += sr;
+    if (g8 >= per_w) {
+      g8 -= per_w;
+      ++w;
+    }
   }
 }
 

@@ -87,6 +87,7 @@ TC_CASES = [
     (3, 128, 8, 56, 256, 3, (1, 1, 1, 1)),   # two output-channel tiles, partial row group
     (1, 72, 7, 56, 40, 3, (1, 1, 1, 1)),     # W % 8 == 0 with C not a multiple of 64
     (1, 40, 6, 112, 48, 3, (1, 1, 1, 1)),    # OW 112: two rows per tile, several column rounds
+    (2, 37, 5, 56, 40, 3, (1, 1, 1, 1)),     # odd C: a channel pair half in the padding
 ]
 
 
