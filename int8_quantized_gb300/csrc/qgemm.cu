@@ -80,12 +80,21 @@ center_operand(const uint8_t* __restrict__ X, int64_t R, int64_t K, int64_t Kp, 
     // write: thread -> row a, 16 consecutive k as bf16 (two 16-byte stores)
     const int64_t r = r0 + a;
     if (r < R) {
+      // centred code c as the fp32 1.5 * 2^23 + (c + 128) by one byte
+      // permute, minus 1.5 * 2^23 + 128: exactly c; its bf16 is the top half
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(&tile[a][b]);
       uint32_t w[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int c0 = tile[a][b + 2 * e], c1 = tile[a][b + 2 * e + 1];
-        part += c0 + c1;
-        w[e] = (__float_as_uint((float)c0) >> 16) | (__float_as_uint((float)c1) & 0xffff0000u);
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t cw = src[q];
+        part = __dp4a((int)cw, 0x01010101, part);
+        const uint32_t uw = cw ^ 0x80808080u;
+        float f[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          f[e] = __fsub_rn(__uint_as_float(__byte_perm(uw, 0x4B400000u, 0x7640u + e)), 12583040.0f);
+        w[2 * q] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632);
+        w[2 * q + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632);
       }
       uint4* dst = reinterpret_cast<uint4*>(Xc + r * Kp + k0 + b);
       dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
