@@ -189,7 +189,7 @@ center_rows(const uint8_t* __restrict__ X, int64_t R, int64_t K, int64_t Kp, __n
   }
 }
 
-// g[j] = cb - bz[j]; e[j] = colsum[j] + K g[j] (wrapping int32);// g[j] = cb - bz[j]; e[j] = colsum[j] + K g[j] (wrapping int32);
+// g[j] = cb - bz[j]; e[j] = colsum[j] + K g[j] (wrapping int32);
 // bsc[j] = b_scale[j] (expanded when per tensor).  Thread 0 also writes the
 // per-tensor row values d0 = ca - za and asc0 when asked (write_row0).
 __global__ void col_params(const int32_t* __restrict__ colsum, const float* __restrict__ b_scale,
