@@ -38,7 +38,8 @@ def load(path):
     l.or_qlinearconv.argtypes = [p, c_int, i64, i64, i64, i64, f32, i32, p, c_int, i64, i64,
                                  i64, p, p, c_int, f32, i32, p, p, p, p, i64, p, c_int]
     l.or_lstm_cell.argtypes = [p, p, p, p, p, p, p, i64, i64]
-    l.or_lstm_cell_ex.argtypes = [p, p, p, p, p, f32, c_int, p, p, p, i64, i64]
+    l.or_lstm_cell_ex.argtypes = [p, p, p, p, p, f32, c_int, p, p, p, p, p, p, i64, i64]
+    l.or_elementary.argtypes = [c_int, p, i64, p]
     l.or_dyn_product_zp.argtypes = [p, p, p, p, c_int, p, i64, p, i64, i64, i64, p]
     l.or_qgemm.argtypes = [p, c_int, c_int, i64, i64, f32, i32, p, c_int, c_int, i64, p, p, i64, p, i64, i64,
                            f32, c_int, f32, i32, c_int, p]
@@ -49,7 +50,7 @@ def load(path):
     for fn in ("or_quantize_linear", "or_dequantize_linear", "or_quantize_rows_u8",
                "or_quantize_cols_s8", "or_qgemm_dyn_rows", "or_qlinearconv", "or_lstm_cell", "or_qgemm",
                "or_matmul_integer_to_float", "or_mul_integer", "or_qlinear_binary", "or_qlinear_unary",
-               "or_lstm_cell_ex", "or_dyn_product_zp"):
+               "or_lstm_cell_ex", "or_dyn_product_zp", "or_elementary"):
         getattr(l, fn).restype = ctypes.c_int
     return l
 
@@ -371,9 +372,62 @@ def qlinear_unary(op, X, x_scale, x_zero_point, y_scale, y_zero_point, alpha=0.0
     return Y
 
 
-def lstm_cell(Gx, Gh, Wb, Rb, c_prev, P=None, clip=0.0, input_forget=False):
-    """One DynamicQuantizeLSTM cell update (default activations, iofc);
-    P: peepholes (3H, iof) or None; clip <= 0: no clip."""
+ELEMENTARY = {"exp": 0, "expm1": 1, "log1p": 2, "sigmoid": 3, "tanh": 4, "softplus": 5}
+
+
+def elementary(name, x):
+    """The oracle's fp32 exp / expm1 / log1p (argument in [0, 1]) / sigmoid /
+    tanh / softplus, elementwise."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty_like(x)
+    _check(lib().or_elementary(ELEMENTARY[name], _ptr(x), x.size, _ptr(y)), "elementary")
+    return y
+
+
+# The ONNX LSTM activation functions, in the order of the operator's list;
+# the value is the index the oracle's C code takes.
+LSTM_ACTIVATIONS = ["Relu", "Tanh", "Sigmoid", "Affine", "LeakyRelu", "ThresholdedRelu", "ScaledTanh", "HardSigmoid",
+                    "Elu", "Softsign", "Softplus"]
+# (alpha, beta) each function takes, with the default of the corresponding
+# ONNX operator (None: the function takes no such attribute).  LeakyRelu's
+# 0.01 is the one the DynamicQuantizeLSTM pages state; the others are the
+# ONNX operators' own defaults, and ScaledTanh (whose operator names none)
+# takes 1 and 1, which makes it Tanh.
+LSTM_ACTIVATION_PARAMS = {"Relu": (None, None), "Tanh": (None, None), "Sigmoid": (None, None),
+                          "Affine": (1.0, 0.0), "LeakyRelu": (0.01, None), "ThresholdedRelu": (1.0, None),
+                          "ScaledTanh": (1.0, 1.0), "HardSigmoid": (0.2, 0.5), "Elu": (1.0, None),
+                          "Softsign": (None, None), "Softplus": (None, None)}
+
+
+def resolve_lstm_activations(activations, activation_alpha, activation_beta, D):
+    """Per direction, the three (f, g, h) activations as (index, alpha, beta).
+
+    activations: None (Sigmoid, Tanh, Tanh in each direction) or 3*D names.
+    activation_alpha / activation_beta are "consumed in the order of
+    activation functions": walking the list, each function that takes an
+    alpha (beta) takes the next unused value, or its default once the list
+    is exhausted."""
+    if activations is None:
+        activations = ["Sigmoid", "Tanh", "Tanh"] * D
+    assert len(activations) == 3 * D, "activations needs 3 entries per direction"
+    alphas = list(activation_alpha or [])
+    betas = list(activation_beta or [])
+    out = []
+    for name in activations:
+        da, db = LSTM_ACTIVATION_PARAMS[name]
+        a = b = 0.0
+        if da is not None:
+            a = alphas.pop(0) if alphas else da
+        if db is not None:
+            b = betas.pop(0) if betas else db
+        out.append((LSTM_ACTIVATIONS.index(name), float(a), float(b)))
+    return [out[3 * d:3 * d + 3] for d in range(D)]
+
+
+def lstm_cell(Gx, Gh, Wb, Rb, c_prev, P=None, clip=0.0, input_forget=False, acts=None):
+    """One DynamicQuantizeLSTM cell update (iofc); P: peepholes (3H, iof) or
+    None; clip <= 0: no clip; acts: the (f, g, h) activations as three
+    (index, alpha, beta) or None for the defaults."""
     Gx = np.ascontiguousarray(Gx, dtype=np.float32)
     Gh = np.ascontiguousarray(Gh, dtype=np.float32)
     c_prev = np.ascontiguousarray(c_prev, dtype=np.float32)
@@ -382,10 +436,15 @@ def lstm_cell(Gx, Gh, Wb, Rb, c_prev, P=None, clip=0.0, input_forget=False):
     Wb = None if Wb is None else np.ascontiguousarray(Wb, dtype=np.float32)
     Rb = None if Rb is None else np.ascontiguousarray(Rb, dtype=np.float32)
     P = None if P is None else np.ascontiguousarray(P, dtype=np.float32)
+    ak = al = be = None
+    if acts is not None:
+        ak = np.array([a[0] for a in acts], np.int32)
+        al = np.array([a[1] for a in acts], np.float32)
+        be = np.array([a[2] for a in acts], np.float32)
     h = np.empty((batch, H), dtype=np.float32)
     c = np.empty((batch, H), dtype=np.float32)
     _check(lib().or_lstm_cell_ex(_ptr(Gx), _ptr(Gh), _ptr(Wb), _ptr(Rb), _ptr(P), float(clip), int(bool(input_forget)),
-                                 _ptr(c_prev), _ptr(h), _ptr(c), batch, H), "lstm_cell")
+                                 _ptr(ak), _ptr(al), _ptr(be), _ptr(c_prev), _ptr(h), _ptr(c), batch, H), "lstm_cell")
     return h, c
 
 
@@ -421,18 +480,20 @@ def lstm_projection(X, W, W_scale, W_zero_point=None):
     return _lstm_product(X.reshape(T * batch, I), W, W_scale, W_zero_point).reshape(T, batch, -1)
 
 
-def lstm_step(Gx_t, h_prev, c_prev, R, R_scale, Wb, Rb, R_zero_point=None, P=None, clip=0.0, input_forget=False):
+def lstm_step(Gx_t, h_prev, c_prev, R, R_scale, Wb, Rb, R_zero_point=None, P=None, clip=0.0, input_forget=False,
+              acts=None):
     """One recurrence step of one direction: quantize h_prev per row, take
     the dequantized product with 8-bit R, then the cell update."""
     Gh = _lstm_product(h_prev, R, R_scale, R_zero_point)
-    return lstm_cell(Gx_t, Gh, Wb, Rb, c_prev, P, clip, input_forget)
+    return lstm_cell(Gx_t, Gh, Wb, Rb, c_prev, P, clip, input_forget, acts)
 
 
 def dynamic_quantize_lstm(X, W, R, B, W_scale, R_scale, h0=None, c0=None, direction="forward", steps=None,
                           W_zero_point=None, R_zero_point=None, P=None, clip=0.0, input_forget=False,
-                          sequence_lens=None):
-    """DynamicQuantizeLSTM (ONNX Runtime contrib schema), default
-    activations.  X (T, batch, I); W (D, I, 4H) and R (D, H, 4H) uint8 or
+                          sequence_lens=None, activations=None, activation_alpha=None, activation_beta=None):
+    """DynamicQuantizeLSTM (ONNX Runtime contrib schema).  activations: None
+    (the defaults) or 3 names per direction, with the alpha/beta attribute
+    lists (see resolve_lstm_activations).  X (T, batch, I); W (D, I, 4H) and R (D, H, 4H) uint8 or
     int8 with zero points (D, 4H) / (D,) or None; scales (D, 4H); B (D, 8H)
     or None; P (D, 3H) or None; sequence_lens (batch,) or None.  A batch row
     with length L runs steps t = 0..L-1 (forward) or L-1..0 (reverse); Y is 0
@@ -451,6 +512,7 @@ def dynamic_quantize_lstm(X, W, R, B, W_scale, R_scale, h0=None, c0=None, direct
     Yc = np.zeros((D, batch, H), dtype=np.float32)
     zp = lambda z, d: None if z is None else np.asarray(z)[d]  # noqa: E731
     rows = np.arange(batch)
+    acts = resolve_lstm_activations(activations, activation_alpha, activation_beta, D)
     for d, kind in enumerate(dirs):
         Gx = lstm_projection(X, W[d], W_scale[d], zp(W_zero_point, d))
         h = np.zeros((batch, H), np.float32) if h0 is None else np.array(h0[d], np.float32)
@@ -462,7 +524,8 @@ def dynamic_quantize_lstm(X, W, R, B, W_scale, R_scale, h0=None, c0=None, direct
             t_b = np.where(kind == 0, n, L - 1 - n)
             active = n < L
             Gx_t = Gx[np.clip(t_b, 0, T - 1), rows]
-            hn, cn = lstm_step(Gx_t, h, c, R[d], R_scale[d], Wb, Rb, zp(R_zero_point, d), Pd, clip, input_forget)
+            hn, cn = lstm_step(Gx_t, h, c, R[d], R_scale[d], Wb, Rb, zp(R_zero_point, d), Pd, clip, input_forget,
+                               acts[d])
             h = np.where(active[:, None], hn, h)
             c = np.where(active[:, None], cn, c)
             for b in np.nonzero(active)[0]:

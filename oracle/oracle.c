@@ -491,10 +491,144 @@ int or_qlinear_binary(int op, const void* A, const int64_t* a_shape, float a_sca
   return OR_OK;
 }
 
+/* ---------------------------------------------------------------------------
+ * [EF] fp32 elementary functions: exp, expm1, log1p, sigmoid, tanh and
+ * softplus, as used by the LSTM activations and QLinearSigmoid.
+ *
+ * The pages fix no evaluation of these functions.  Library versions differ
+ * in the last bit between platforms, and one such bit in h can move a uint8
+ * code of the next step's dynamically quantized hidden state.  So each is
+ * defined here as a fixed sequence of IEEE fp32 operations (each rounds
+ * once to nearest even; fmaf rounds the exact a*b+c once, and scaling by a
+ * power of two is exact unless the result leaves the normal range); any
+ * implementation that performs the same sequence gets the same bits.  The
+ * methods are textbook ones:
+ *
+ *  exp   Cody and Waite's argument reduction (W. J. Cody and W. Waite,
+ *        "Software Manual for the Elementary Functions", 1980):
+ *        x = n ln2 + r, n = rint(x / ln2), r = (x - n LN2_HI) - n LN2_LO,
+ *        where LN2_HI is ln 2 rounded to fp32 and LN2_LO the fp32 rounding
+ *        of the remainder; e^r by its Taylor series to r^7/7! in Horner
+ *        form (|r| <= ln2/2: the truncation is below 2^-27 relative); the
+ *        result scaled by 2^n as two multiplications by powers of two, so
+ *        that a subnormal result rounds once.
+ *  expm1 the same reduction; e^r - 1 = r (1 + r/2! + ... + r^7/8!), and
+ *        e^x - 1 = 2^n (e^r - 1) + (2^n - 1).
+ *  log1p (argument in [0, 1]) 1 + u = 2^k (1 + v) with k = 0 or 1 and v in
+ *        [sqrt(1/2) - 1, sqrt(2) - 1]; log(1 + v) = 2 atanh(s) with
+ *        s = v / (2 + v), by the series 2 s (1 + s^2/3 + ... + s^8/9).
+ *  sigmoid(x) = 1 / (1 + exp(-x));  tanh(x) = sign(x) t(|x|) with
+ *        t(a) = e / (e + 2), e = expm1(2a), for a < 0.625, where the
+ *        cancellation of 1 - 2 / (e^2a + 1) would cost accuracy;
+ *        1 - 2 / (exp(2a) + 1) up to 9.5; and 1 above (tanh rounds to 1);
+ *        softplus(x) = log(1 + e^x), as x + log1p(e^-x) for x > 0.
+ * Each constant is written in hexadecimal; the comment names the number it
+ * is the fp32 rounding of.
+ */
+static float pow2i(int k) { return ldexpf(1.0f, k); } /* exact for -149 <= k <= 127 */
+
+static const float EF_L2E = 0x1.715476p+0f;     /* 1 / ln 2 */
+static const float EF_LN2_HI = 0x1.62e430p-1f;  /* ln 2 */
+static const float EF_LN2_LO = -0x1.05c610p-29f; /* ln 2 - EF_LN2_HI */
+
+static float ef_exp(float x) {
+  if (x > 89.0f) x = 89.0f;    /* e^89 is above the fp32 range: the result is +inf */
+  if (x < -104.0f) x = -104.0f; /* e^-104 is below half the least subnormal: 0 */
+  const float nf = rintf(x * EF_L2E);
+  const int n = (int)nf;
+  float r = fmaf(-nf, EF_LN2_HI, x);
+  r = fmaf(-nf, EF_LN2_LO, r);
+  float p = 0x1.a01a02p-13f;       /* 1/7! */
+  p = fmaf(p, r, 0x1.6c16c2p-10f); /* 1/6! */
+  p = fmaf(p, r, 0x1.111112p-7f);  /* 1/5! */
+  p = fmaf(p, r, 0x1.555556p-5f);  /* 1/4! */
+  p = fmaf(p, r, 0x1.555556p-3f);  /* 1/3! */
+  p = fmaf(p, r, 0.5f);            /* 1/2! */
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  const int n1 = n / 2, n2 = n - n1;
+  return (p * pow2i(n1)) * pow2i(n2);
+}
+
+/* e^x - 1 for x <= 20 (e^x itself above, -1 below -20, where e^x is under
+ * a quarter of an fp32 ulp of 1). */
+static float ef_expm1(float x) {
+  if (x > 20.0f) return ef_exp(x);
+  if (x < -20.0f) return -1.0f;
+  const float nf = rintf(x * EF_L2E);
+  const int n = (int)nf;
+  float r = fmaf(-nf, EF_LN2_HI, x);
+  r = fmaf(-nf, EF_LN2_LO, r);
+  float q = 0x1.a01a02p-16f;       /* 1/8! */
+  q = fmaf(q, r, 0x1.a01a02p-13f); /* 1/7! */
+  q = fmaf(q, r, 0x1.6c16c2p-10f); /* 1/6! */
+  q = fmaf(q, r, 0x1.111112p-7f);  /* 1/5! */
+  q = fmaf(q, r, 0x1.555556p-5f);  /* 1/4! */
+  q = fmaf(q, r, 0x1.555556p-3f);  /* 1/3! */
+  q = fmaf(q, r, 0.5f);            /* 1/2! */
+  q = fmaf(q, r, 1.0f);
+  q = q * r; /* e^r - 1 */
+  if (n == 0) return q;
+  const float t = pow2i(n);
+  return fmaf(t, q, t - 1.0f);
+}
+
+/* log(1 + u) for 0 <= u <= 1. */
+static float ef_log1p01(float u) {
+  float v = u, k = 0.0f;
+  if (u > 0x1.a8279ap-2f) { /* sqrt(2) - 1 */
+    v = (u - 1.0f) * 0.5f;  /* exact: 1 + u = 2 (1 + v) */
+    k = 1.0f;
+  }
+  const float s = v / (2.0f + v);
+  const float z = s * s;
+  float w = 0x1.c71c72p-4f;       /* 1/9 */
+  w = fmaf(w, z, 0x1.24924ap-3f); /* 1/7 */
+  w = fmaf(w, z, 0x1.99999ap-3f); /* 1/5 */
+  w = fmaf(w, z, 0x1.555556p-2f); /* 1/3 */
+  w = fmaf(w, z, 1.0f);
+  const float l = (s + s) * w; /* log(1 + v) */
+  return fmaf(k, EF_LN2_HI, l);
+}
+
+static float ef_sigmoid(float x) { return 1.0f / (1.0f + ef_exp(-x)); }
+
+static float ef_tanh(float x) {
+  const float a = fabsf(x);
+  float t = 1.0f;
+  if (a < 0.625f) {
+    const float e = ef_expm1(a + a);
+    t = e / (e + 2.0f);
+  } else if (a <= 9.5f) {
+    t = 1.0f - 2.0f / (ef_exp(a + a) + 1.0f);
+  }
+  return copysignf(t, x);
+}
+
+static float ef_softplus(float x) {
+  return x > 0.0f ? x + ef_log1p01(ef_exp(-x)) : ef_log1p01(ef_exp(x));
+}
+
+/* Single-argument entry points for the pins (n values each). */
+int or_elementary(int fn, const float* x, int64_t n, float* y) {
+  for (int64_t i = 0; i < n; ++i) {
+    switch (fn) {
+      case 0: y[i] = ef_exp(x[i]); break;
+      case 1: y[i] = ef_expm1(x[i]); break;
+      case 2: y[i] = ef_log1p01(x[i]); break;
+      case 3: y[i] = ef_sigmoid(x[i]); break;
+      case 4: y[i] = ef_tanh(x[i]); break;
+      case 5: y[i] = ef_softplus(x[i]); break;
+      default: return OR_ERR_ARG;
+    }
+  }
+  return OR_OK;
+}
+
 /* [QEW] QLinearLeakyRelu (op 0) and QLinearSigmoid (op 1) on n codes:
  *   d = DequantizeLinear(x) = (x - X_zp) * X_scale
  *   leaky relu: f = alpha * d when d < 0, else d
- *   sigmoid:    f = 1 / (1 + exp(-d))
+ *   sigmoid:    f = 1 / (1 + exp(-d))   ([EF] sigmoid)
  *   y = QuantizeLinear(f) = saturate(rint(f / Y_scale) + Y_zp) */
 int or_qlinear_unary(int op, const void* X, int64_t n, int qtype, float x_scale, int32_t x_zp, float y_scale,
                      int32_t y_zp, float alpha, void* Y) {
@@ -507,32 +641,81 @@ int or_qlinear_unary(int op, const void* X, int64_t n, int qtype, float x_scale,
     if (op == 0)
       f = d < 0.0f ? alpha * d : d;
     else
-      f = 1.0f / (1.0f + expf(-d));
+      f = ef_sigmoid(d);
     store_q(Y, qtype, i, sat_rint_plus(f / y_scale, y_zp, lo, hi));
   }
   return OR_OK;
 }
 
-static float sigmoid_f32(float x) { return 1.0f / (1.0f + expf(-x)); }
+/* [LSTM] The activation functions the "activations" attribute may name: the
+ * ONNX LSTM operator's list (the schema refers to it; it is not printed on
+ * the pages), in that list's order.  alpha and beta are the function's
+ * attributes, resolved by the caller (defaults of the corresponding ONNX
+ * operators where the attribute lists run out).  Each is its operator's
+ * formula in fp32, one rounding per operation:
+ *   Relu            max(0, x)
+ *   Tanh, Sigmoid   [EF] tanh, sigmoid
+ *   Affine          alpha x + beta
+ *   LeakyRelu       x for x >= 0, alpha x otherwise
+ *   ThresholdedRelu x for x > alpha, 0 otherwise
+ *   ScaledTanh      alpha tanh(beta x)
+ *   HardSigmoid     min(max(alpha x + beta, 0), 1)
+ *   Elu             x for x >= 0, alpha (e^x - 1) otherwise ([EF] expm1)
+ *   Softsign        x / (1 + |x|)
+ *   Softplus        log(e^x + 1) ([EF] softplus) */
+enum {
+  OR_LA_RELU, OR_LA_TANH, OR_LA_SIGMOID, OR_LA_AFFINE, OR_LA_LEAKY_RELU, OR_LA_THRESHOLDED_RELU,
+  OR_LA_SCALED_TANH, OR_LA_HARD_SIGMOID, OR_LA_ELU, OR_LA_SOFTSIGN, OR_LA_SOFTPLUS
+};
 
-/* [LSTM] one cell update for one direction and one time step, default
- * activations (sigmoid for i, o, f; tanh for the candidate and the output),
- * gate columns in iofc order.  The ONNX LSTM equations the schema points to
- * (not printed on the pages) give each gate's terms in this order, summed
- * left to right:
+static float lstm_activation(int kind, float alpha, float beta, float x) {
+  switch (kind) {
+    case OR_LA_RELU: return x > 0.0f ? x : 0.0f;
+    case OR_LA_TANH: return ef_tanh(x);
+    case OR_LA_SIGMOID: return ef_sigmoid(x);
+    case OR_LA_AFFINE: return alpha * x + beta;
+    case OR_LA_LEAKY_RELU: return x >= 0.0f ? x : alpha * x;
+    case OR_LA_THRESHOLDED_RELU: return x > alpha ? x : 0.0f;
+    case OR_LA_SCALED_TANH: return alpha * ef_tanh(beta * x);
+    case OR_LA_HARD_SIGMOID: {
+      const float v = alpha * x + beta;
+      return v < 0.0f ? 0.0f : (v > 1.0f ? 1.0f : v);
+    }
+    case OR_LA_ELU: return x >= 0.0f ? x : alpha * ef_expm1(x);
+    case OR_LA_SOFTSIGN: return x / (1.0f + fabsf(x));
+    case OR_LA_SOFTPLUS: return ef_softplus(x);
+  }
+  return x;
+}
+
+/* [LSTM] one cell update for one direction and one time step, gate columns
+ * in iofc order.  The ONNX LSTM equations the schema points to (not printed
+ * on the pages) give each gate's terms in this order, summed left to right:
  *   i = f(X Wi + H Ri + Pi (.) C_prev + Wbi + Rbi)
  *   f = f(X Wf + H Rf + Pf (.) C_prev + Wbf + Rbf)     (1 - i when input_forget)
  *   c~ = g(X Wc + H Rc + Wbc + Rbc)
  *   C = f (.) C_prev + i (.) c~
  *   o = f(X Wo + H Ro + Po (.) C + Wbo + Rbo)
  *   H = o (.) h(C)
- * Gx and Gh are the two dequantized products.  P holds Pi, Po, Pf (3H,
- * "P[iof]") or is NULL (no peephole terms).  clip > 0 bounds each gate's
- * input to [-clip, clip] before its activation; clip <= 0 is no clip (the
- * schema: "No clip if not specified"; the third-party page lists a default
- * of 0, read as the same).  A missing bias adds nothing. */
+ * f, g, h are act[0..2] with their alpha/beta (NULL act: the defaults
+ * Sigmoid, Tanh, Tanh).  Gx and Gh are the two dequantized products.  P
+ * holds Pi, Po, Pf (3H, "P[iof]") or is NULL (no peephole terms).  clip > 0
+ * bounds each gate's input to [-clip, clip] before its activation; clip <= 0
+ * is no clip (the schema: "No clip if not specified"; the third-party page
+ * lists a default of 0, read as the same).  A missing bias adds nothing. */
 int or_lstm_cell_ex(const float* Gx, const float* Gh, const float* Wb, const float* Rb, const float* P, float clip,
-                    int input_forget, const float* c_prev, float* h_out, float* c_out, int64_t batch, int64_t H) {
+                    int input_forget, const int* act, const float* act_alpha, const float* act_beta,
+                    const float* c_prev, float* h_out, float* c_out, int64_t batch, int64_t H) {
+  static const int default_act[3] = {OR_LA_SIGMOID, OR_LA_TANH, OR_LA_TANH};
+  static const float zero3[3] = {0.0f, 0.0f, 0.0f};
+  if (!act) act = default_act;
+  if (!act_alpha) act_alpha = zero3;
+  if (!act_beta) act_beta = zero3;
+  for (int q = 0; q < 3; ++q)
+    if (act[q] < OR_LA_RELU || act[q] > OR_LA_SOFTPLUS) return OR_ERR_ARG;
+#define F_(v) lstm_activation(act[0], act_alpha[0], act_beta[0], (v))
+#define G_(v) lstm_activation(act[1], act_alpha[1], act_beta[1], (v))
+#define H_(v) lstm_activation(act[2], act_alpha[2], act_beta[2], (v))
   for (int64_t b = 0; b < batch; ++b) {
     for (int64_t u = 0; u < H; ++u) {
       const float cp = c_prev[b * H + u];
@@ -549,27 +732,30 @@ int or_lstm_cell_ex(const float* Gx, const float* Gh, const float* Wb, const flo
         }
         g[q] = v;
       }
-      float ig = sigmoid_f32(g[0]);
-      float fg = input_forget ? 1.0f - ig : sigmoid_f32(g[2]);
-      float ct = tanhf(g[3]);
+      float ig = F_(g[0]);
+      float fg = input_forget ? 1.0f - ig : F_(g[2]);
+      float ct = G_(g[3]);
       float c = fg * cp + ig * ct;
       float vo = g[1];
       if (P) vo = vo + P[H + u] * c;
       if (Wb) vo = vo + Wb[H + u];
       if (Rb) vo = vo + Rb[H + u];
       if (clip > 0.0f) vo = vo < -clip ? -clip : (vo > clip ? clip : vo);
-      float og = sigmoid_f32(vo);
+      float og = F_(vo);
       c_out[b * H + u] = c;
-      h_out[b * H + u] = og * tanhf(c);
+      h_out[b * H + u] = og * H_(c);
     }
   }
+#undef F_
+#undef G_
+#undef H_
   return OR_OK;
 }
 
 /* The default cell: no peepholes, no clip, input_forget 0. */
 int or_lstm_cell(const float* Gx, const float* Gh, const float* Wb, const float* Rb, const float* c_prev,
                  float* h_out, float* c_out, int64_t batch, int64_t H) {
-  return or_lstm_cell_ex(Gx, Gh, Wb, Rb, NULL, 0.0f, 0, c_prev, h_out, c_out, batch, H);
+  return or_lstm_cell_ex(Gx, Gh, Wb, Rb, NULL, 0.0f, 0, NULL, NULL, NULL, c_prev, h_out, c_out, batch, H);
 }
 
 /* [DQIP] / [LSTM] the dequantized product of per-row uint8 codes uA (M x K,

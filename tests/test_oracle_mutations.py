@@ -41,11 +41,35 @@ MUTATIONS = {
     "conv_bias_dropped": ("if (B) acc += B[m];", "(void)B;"),
     "conv_weight_zero_point_per_tensor": ("const int64_t wz = w_zero_point[per_channel ? m : 0];",
                                           "const int64_t wz = w_zero_point[0];"),
-    "lstm_gates_o_f_swapped": ("float fg = input_forget ? 1.0f - ig : sigmoid_f32(g[2]);",
-                               "float fg = input_forget ? 1.0f - ig : sigmoid_f32(g[1]);"),
+    "lstm_gates_o_f_swapped": ("float fg = input_forget ? 1.0f - ig : F_(g[2]);",
+                               "float fg = input_forget ? 1.0f - ig : F_(g[1]);"),
     "lstm_peephole_o_uses_old_cell": ("if (P) vo = vo + P[H + u] * c;", "if (P) vo = vo + P[H + u] * cp;"),
-    "lstm_coupled_gate_is_i": ("float fg = input_forget ? 1.0f - ig : sigmoid_f32(g[2]);",
-                               "float fg = input_forget ? ig : sigmoid_f32(g[2]);"),
+    "lstm_coupled_gate_is_i": ("float fg = input_forget ? 1.0f - ig : F_(g[2]);",
+                               "float fg = input_forget ? ig : F_(g[2]);"),
+    "exp_low_part_of_ln2_dropped": ("  r = fmaf(-nf, EF_LN2_LO, r);\n  float p", "  float p"),
+    "exp_taylor_coefficient": ("p = fmaf(p, r, 0x1.111112p-7f);  /* 1/5! */", "p = fmaf(p, r, 0x1.555556p-5f);  /* 1/5! */"),
+    "exp_scale_halves_wrong": ("const int n1 = n / 2, n2 = n - n1;\n  return", "const int n1 = n / 2, n2 = n1;\n  return"),
+    "expm1_missing_2n_minus_1": ("return fmaf(t, q, t - 1.0f);", "return t * q;"),
+    "log1p_range_step_dropped": ("return fmaf(k, EF_LN2_HI, l);", "return l;"),
+    "tanh_large_argument_threshold": ("} else if (a <= 9.5f) {", "} else if (a <= 4.0f) {"),
+    "tanh_small_branch_formula": ("t = e / (e + 2.0f);", "t = e / (e + 1.0f);"),
+    "sigmoid_sign": ("static float ef_sigmoid(float x) { return 1.0f / (1.0f + ef_exp(-x)); }",
+                     "static float ef_sigmoid(float x) { return 1.0f / (1.0f + ef_exp(x)); }"),
+    "softplus_positive_branch": ("return x > 0.0f ? x + ef_log1p01(ef_exp(-x))", "return x > 0.0f ? ef_log1p01(ef_exp(-x))"),
+    "lstm_candidate_uses_f": ("float ct = G_(g[3]);", "float ct = F_(g[3]);"),
+    "lstm_output_uses_g": ("h_out[b * H + u] = og * H_(c);", "h_out[b * H + u] = og * G_(c);"),
+    "activation_hard_sigmoid_unclamped": ("return v < 0.0f ? 0.0f : (v > 1.0f ? 1.0f : v);", "return v;"),
+    "activation_thresholded_relu_at_zero": ("case OR_LA_THRESHOLDED_RELU: return x > alpha ? x : 0.0f;",
+                                            "case OR_LA_THRESHOLDED_RELU: return x > 0.0f ? x : 0.0f;"),
+    "activation_elu_without_alpha": ("case OR_LA_ELU: return x >= 0.0f ? x : alpha * ef_expm1(x);",
+                                     "case OR_LA_ELU: return x >= 0.0f ? x : ef_expm1(x);"),
+    "activation_scaled_tanh_beta_dropped": ("case OR_LA_SCALED_TANH: return alpha * ef_tanh(beta * x);",
+                                            "case OR_LA_SCALED_TANH: return alpha * ef_tanh(x);"),
+    "activation_affine_beta_dropped": ("case OR_LA_AFFINE: return alpha * x + beta;", "case OR_LA_AFFINE: return alpha * x;"),
+    "activation_softsign_sign": ("case OR_LA_SOFTSIGN: return x / (1.0f + fabsf(x));",
+                                 "case OR_LA_SOFTSIGN: return x / (1.0f + x);"),
+    "activation_leaky_relu_on_positive": ("case OR_LA_LEAKY_RELU: return x >= 0.0f ? x : alpha * x;",
+                                          "case OR_LA_LEAKY_RELU: return x >= 0.0f ? alpha * x : x;"),
     "lstm_clip_skips_candidate": ("        if (q != 1) {\n          if (Wb) v = v + Wb[n];\n          if (Rb) v = v + Rb[n];\n          if (clip > 0.0f)",
                                   "        if (q != 1) {\n          if (Wb) v = v + Wb[n];\n          if (Rb) v = v + Rb[n];\n          if (clip > 0.0f && q != 3)"),
     "zp_product_zero_point_per_tensor": ("const int64_t zb = zeroB ? zeroB[n_zb == N ? j : 0] : 0;",
@@ -72,18 +96,39 @@ MUTATIONS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTATIONS))
-def test_pins_catch_planted_mistake(name, tmp_path):
+def _run_mutant(name, workdir):
+    """Build the oracle with mutation `name` planted and run the pin suite
+    against it in a child process; returns (returncode, stdout)."""
     old, new = MUTATIONS[name]
     src = open(ORACLE_SRC).read()
-    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
-    mutant = tmp_path / "oracle_mutant.c"
-    mutant.write_text(src.replace(old, new, 1))
-    so = tmp_path / "liboracle_mutant.so"
-    subprocess.run(["gcc", *oracle_build.CFLAGS, str(mutant), "-o", str(so), "-lm"], check=True)
-    env = dict(os.environ, ORACLE_LIB_UNDER_TEST=str(so))
+    if src.count(old) < 1:
+        return None, f"mutation anchor for {name} not found"
+    mutant = os.path.join(workdir, f"oracle_{name}.c")
+    with open(mutant, "w") as f:
+        f.write(src.replace(old, new, 1))
+    so = os.path.join(workdir, f"liboracle_{name}.so")
+    subprocess.run(["gcc", *oracle_build.CFLAGS, mutant, "-o", so, "-lm"], check=True)
+    env = dict(os.environ, ORACLE_LIB_UNDER_TEST=so, OMP_NUM_THREADS="1")
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode != 0, f"no pin failed for planted mistake {name}:\n{r.stdout[-2000:]}"
-    assert "failed" in r.stdout
+    return r.returncode, r.stdout
+
+
+@pytest.fixture(scope="module")
+def mutant_results(tmp_path_factory):
+    """Every planted mistake, built and run concurrently (one child process
+    per mutation, as many at once as this host has cores)."""
+    from concurrent.futures import ThreadPoolExecutor
+    workdir = str(tmp_path_factory.mktemp("mutants"))
+    with ThreadPoolExecutor(max_workers=max(1, len(os.sched_getaffinity(0)))) as ex:
+        futs = {n: ex.submit(_run_mutant, n, workdir) for n in MUTATIONS}
+        return {n: f.result() for n, f in futs.items()}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, mutant_results):
+    rc, out = mutant_results[name]
+    assert rc is not None, out
+    assert rc != 0, f"no pin failed for planted mistake {name}:\n{out[-2000:]}"
+    assert "failed" in out

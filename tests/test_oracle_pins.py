@@ -846,3 +846,137 @@ def test_lstm_sequence_lens_equal_truncated_runs(orc, direction):
                                                  w["W_scale"][sel], w["R_scale"][sel], direction=direction)
         assert np.array_equal(Y[:L, :, b], Yb[:, :, 0])
         assert np.array_equal(Yh[:, b], Yhb[:, 0]) and np.array_equal(Yc[:, b], Ycb[:, 0])
+
+
+# ---- fp32 elementary functions (exp, expm1, log1p, sigmoid, tanh, softplus) --
+
+def _ulps(y, ref):
+    """|y - ref| in fp32 ulps of ref (the spacing of fp32 at |ref|; the least
+    subnormal below the normal range)."""
+    sp = np.maximum(np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64), 2.0 ** -149)
+    return np.abs(y.astype(np.float64) - ref) / sp
+
+
+def _sweep(lo, hi, n=200_000, seed=0):
+    rng = np.random.default_rng(seed)
+    return np.concatenate([np.linspace(lo, hi, n), rng.uniform(lo, hi, n)]).astype(np.float32)
+
+
+@pytest.mark.parametrize("name,lo,hi,ref,bound", [
+    ("exp", -103.0, 88.7, np.exp, 1.0),
+    ("expm1", -20.0, 20.0, np.expm1, 2.0),
+    ("expm1", -1e-3, 1e-3, np.expm1, 2.0),
+    ("log1p", 0.0, 1.0, np.log1p, 3.0),
+    ("sigmoid", -87.0, 100.0, lambda v: 1.0 / (1.0 + np.exp(-v)), 3.0),
+    ("tanh", -12.0, 12.0, np.tanh, 3.5),
+    ("tanh", -1e-3, 1e-3, np.tanh, 3.5),
+    ("softplus", -100.0, 100.0, lambda v: np.logaddexp(0.0, v), 3.5),
+])
+def test_elementary_functions_within_ulps_of_fp64(orc, name, lo, hi, ref, bound):
+    """Each fp32 function is within a few ulps of the fp64 library value
+    (numpy's exp, expm1, log1p, tanh, logaddexp) over its range."""
+    x = _sweep(lo, hi)
+    err = _ulps(orc.elementary(name, x), ref(x.astype(np.float64)))
+    assert err.max() <= bound, (name, float(err.max()), float(x[np.argmax(err)]))
+
+
+def test_elementary_special_values(orc):
+    e = orc.elementary
+    assert e("exp", [0.0])[0] == 1.0
+    assert e("exp", [89.0])[0] == np.inf and e("exp", [-104.0])[0] == 0.0
+    assert np.isfinite(e("exp", [88.72])[0])
+    # exact powers of two: e^(k ln 2) rounds to 2^k within an ulp
+    k = np.arange(-120, 127)
+    assert np.all(_ulps(e("exp", (k * math.log(2)).astype(np.float32)), np.exp((k * math.log(2)).astype(np.float32)
+                                                                                 .astype(np.float64))) <= 1.0)
+    assert e("sigmoid", [0.0])[0] == 0.5
+    assert e("sigmoid", [200.0])[0] == 1.0 and e("sigmoid", [-200.0])[0] == 0.0
+    t = e("tanh", [0.0, -0.0, 9.6, -9.6, 1e-30])
+    assert t[0] == 0.0 and np.signbit(t[1]) and t[2] == 1.0 and t[3] == -1.0 and t[4] == np.float32(1e-30)
+    assert e("expm1", [0.0])[0] == 0.0 and e("expm1", [-30.0])[0] == -1.0
+    assert e("log1p", [0.0])[0] == 0.0 and abs(float(e("log1p", [1.0])[0]) - math.log(2)) <= 6e-8
+    assert e("softplus", [0.0])[0] == np.float32(math.log(2))
+    assert e("softplus", [100.0])[0] == 100.0 and e("softplus", [-100.0])[0] > 0.0
+
+
+def test_elementary_symmetries(orc):
+    """tanh is odd bit for bit (it is evaluated on |x|); sigmoid(x) +
+    sigmoid(-x) = 1 and softplus(x) - softplus(-x) = x to rounding; exp
+    and sigmoid are non-decreasing on a fine grid (tanh and softplus, each
+    a quotient or sum of separately rounded terms, may step back by an
+    ulp)."""
+    x = _sweep(-15.0, 15.0, n=20_000)
+    assert np.array_equal(orc.elementary("tanh", -x), -orc.elementary("tanh", x))
+    s = orc.elementary("sigmoid", x).astype(np.float64) + orc.elementary("sigmoid", -x)
+    assert np.abs(s - 1.0).max() <= 2.5e-7
+    d = orc.elementary("softplus", x).astype(np.float64) - orc.elementary("softplus", -x)
+    assert np.abs(d - x).max() <= 1e-5 * np.abs(x).max()
+    g = np.sort(x)
+    for name in ("sigmoid", "exp"):
+        assert np.all(np.diff(orc.elementary(name, g).astype(np.float64)) >= 0), name
+
+
+# ---- DynamicQuantizeLSTM activations ("activations", "activation_alpha/beta") --
+
+_F64_ACT = {
+    "Relu": lambda x, a, b: np.maximum(x, 0.0),
+    "Tanh": lambda x, a, b: np.tanh(x),
+    "Sigmoid": lambda x, a, b: 1.0 / (1.0 + np.exp(-x)),
+    "Affine": lambda x, a, b: a * x + b,
+    "LeakyRelu": lambda x, a, b: np.where(x >= 0, x, a * x),
+    "ThresholdedRelu": lambda x, a, b: np.where(x > a, x, 0.0),
+    "ScaledTanh": lambda x, a, b: a * np.tanh(b * x),
+    "HardSigmoid": lambda x, a, b: np.clip(a * x + b, 0.0, 1.0),
+    "Elu": lambda x, a, b: np.where(x >= 0, x, a * np.expm1(np.minimum(x, 0.0))),
+    "Softsign": lambda x, a, b: x / (1.0 + np.abs(x)),
+    "Softplus": lambda x, a, b: np.logaddexp(0.0, x),
+}
+
+
+def test_lstm_activation_attribute_lists_are_consumed_in_order(orc):
+    """alpha / beta values go, in order, to the functions that take them;
+    functions past the end of a list take the ONNX operators' defaults
+    (LeakyRelu 0.01 as the pages state)."""
+    r = orc.resolve_lstm_activations(["LeakyRelu", "Tanh", "HardSigmoid", "Elu", "Softplus", "ScaledTanh"],
+                                     [0.3, 0.4], [0.6], 2)
+    A = orc.LSTM_ACTIVATIONS.index
+    assert r == [[(A("LeakyRelu"), 0.3, 0.0), (A("Tanh"), 0.0, 0.0),
+                  (A("HardSigmoid"), pytest.approx(0.4), pytest.approx(0.6))],
+                 [(A("Elu"), 1.0, 0.0), (A("Softplus"), 0.0, 0.0), (A("ScaledTanh"), 1.0, 1.0)]]
+    assert orc.resolve_lstm_activations(["LeakyRelu"] * 3, None, None, 1)[0][0] == (A("LeakyRelu"), 0.01, 0.0)
+    d = orc.resolve_lstm_activations(None, None, None, 1)[0]
+    assert [k for k, _, _ in d] == [A("Sigmoid"), A("Tanh"), A("Tanh")]
+
+
+@pytest.mark.parametrize("slot", [0, 1, 2])
+@pytest.mark.parametrize("name", sorted(_F64_ACT))
+def test_lstm_activation_first_step_equals_textbook(orc, slot, name):
+    """Step 0 with h0 = 0 (Gh exactly 0) and X on the lossless grid with
+    power-of-two W scales (Gx exact): with `name` as f (slot 0: the i, o, f
+    gates), g (slot 1: the cell candidate) or h (slot 2: the output), the
+    cell is the fp64 ONNX LSTM cell with that function, to fp32 rounding."""
+    rng = np.random.default_rng(70 + slot)
+    T, b, I, H = 1, 4, 24, 8
+    X = lossless_A(rng, T * b, I).reshape(T, b, I)
+    W = rng.integers(-128, 128, size=(1, I, 4 * H)).astype(np.int8)
+    R = rng.integers(-128, 128, size=(1, H, 4 * H)).astype(np.int8)
+    Ws = (2.0 ** rng.integers(-9, -6, size=(1, 4 * H))).astype(np.float32)
+    Rs = (2.0 ** rng.integers(-9, -6, size=(1, 4 * H))).astype(np.float32)
+    Bb = rng.normal(0, 0.1, size=(1, 8 * H)).astype(np.float32)
+    c0 = rng.normal(0, 1, size=(1, b, H)).astype(np.float32)
+    names = ["Sigmoid", "Tanh", "Tanh"]
+    names[slot] = name
+    alpha, beta = [0.7, 1.3, 0.9], [0.25, 0.5, 0.75]   # each slot's values, whether used or not
+    al = [alpha[k] for k in range(3) if orc.LSTM_ACTIVATION_PARAMS[names[k]][0] is not None]
+    be = [beta[k] for k in range(3) if orc.LSTM_ACTIVATION_PARAMS[names[k]][1] is not None]
+    Y, Yh, Yc = orc.dynamic_quantize_lstm(X, W, R, Bb, Ws, Rs, c0=c0, activations=names, activation_alpha=al,
+                                          activation_beta=be)
+    gx = X[0].astype(np.float64) @ (W[0] * Ws[0].astype(np.float64))
+    Bd = Bb[0].astype(np.float64)
+    g = gx + Bd[:4 * H] + Bd[4 * H:]
+    fa = [lambda v, k=k: _F64_ACT[names[k]](v, alpha[k], beta[k]) for k in range(3)]
+    i, o, f = fa[0](g[:, :H]), fa[0](g[:, H:2 * H]), fa[0](g[:, 2 * H:3 * H])
+    c = f * c0[0] + i * fa[1](g[:, 3 * H:])
+    h = o * fa[2](c)
+    assert np.allclose(Yc[0], c, rtol=1e-5, atol=1e-6)
+    assert np.allclose(Yh[0], h, rtol=1e-5, atol=1e-6)
