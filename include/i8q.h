@@ -81,6 +81,27 @@ extern "C" {
 #define I8Q_LSTM_REVERSE 1
 #define I8Q_LSTM_BIDIRECTIONAL 2
 
+/* ---- LSTM activation functions ("activations" attribute) ----------------
+ * The ONNX LSTM operator's list, in its order.  Each is its operator's
+ * formula in fp32 with one rounding per operation; exp, expm1, log1p, tanh
+ * and sigmoid are fixed operation sequences (the library's own, not the
+ * platform's math library), so results are reproducible bit for bit:
+ *   RELU max(0,x); TANH; SIGMOID 1/(1+e^-x); AFFINE a*x+b;
+ *   LEAKY_RELU x>=0 ? x : a*x; THRESHOLDED_RELU x>a ? x : 0;
+ *   SCALED_TANH a*tanh(b*x); HARD_SIGMOID min(max(a*x+b,0),1);
+ *   ELU x>=0 ? x : a*(e^x-1); SOFTSIGN x/(1+|x|); SOFTPLUS log(1+e^x). */
+#define I8Q_LSTM_ACT_RELU 0
+#define I8Q_LSTM_ACT_TANH 1
+#define I8Q_LSTM_ACT_SIGMOID 2
+#define I8Q_LSTM_ACT_AFFINE 3
+#define I8Q_LSTM_ACT_LEAKY_RELU 4
+#define I8Q_LSTM_ACT_THRESHOLDED_RELU 5
+#define I8Q_LSTM_ACT_SCALED_TANH 6
+#define I8Q_LSTM_ACT_HARD_SIGMOID 7
+#define I8Q_LSTM_ACT_ELU 8
+#define I8Q_LSTM_ACT_SOFTSIGN 9
+#define I8Q_LSTM_ACT_SOFTPLUS 10
+
 /* Text of the last error raised on this host thread ("" if none).  The
  * pointer stays valid until the next call on this thread. */
 const char* i8q_last_error(void);
@@ -193,11 +214,15 @@ int i8q_qgemm_dyn_forward_s32(i8q_qgemm_ctx* ctx, const void* A, const void* B, 
 int i8q_qgemm_dyn_buf_views(i8q_qgemm_ctx* ctx, void* buf, uint8_t** uA, size_t* lda, float** scaleA,
                             int32_t** zeroA);
 
-/* Test hook, not on the pages: device addresses of the stored quantized
- * constant B, transposed to N x K int8 (row stride *ldb bytes), its N fp32
- * scales and N int32 column sums. */
-int i8q_qgemm_dyn_weight_views(i8q_qgemm_ctx* ctx, int8_t** iBt, size_t* ldb, float** scaleB,
-                               int32_t** colsum);
+/* Test hook, not on the pages: device addresses of the quantized B --
+ * the stored constant B, or the B the last Forward quantized into `buf`
+ * (or the fallback scratch when buf is NULL) -- transposed to N rows of K
+ * codes (row stride *ldb elements): *iBt as int8 and *iBt_bf16 as bf16
+ * holding the same integers, either set to NULL when that copy is not kept
+ * (a non-constant B keeps only the copy its product reads); its N fp32
+ * scales and N int32 column sums.  Any output pointer may be NULL. */
+int i8q_qgemm_dyn_weight_views(i8q_qgemm_ctx* ctx, void* buf, int8_t** iBt, void** iBt_bf16, size_t* ldb,
+                               float** scaleB, int32_t** colsum);
 
 /* Clear [DQIP]: release the context and everything it owns; *ctx = NULL.
  * Synchronizes the device first.  NULL or *ctx == NULL is a no-op. */
@@ -391,8 +416,8 @@ int i8q_mul_integer(const void* A, int atype, const int64_t* a_shape, int a_rank
 /* QLinearLeakyRelu (alpha used) / QLinearSigmoid on n codes of qtype:
  *   d = (x - x_zp) * x_scale;  f = alpha * d if d < 0 else d  |  1 / (1 + exp(-d))
  *   y = saturate(rint(f / y_scale) + y_zp).
- * The sigmoid uses the device expf, which may differ from another
- * library's by an ulp and so move a code that lies at a rounding boundary. */
+ * The sigmoid is the library's fixed-sequence fp32 function (see
+ * I8Q_LSTM_ACT_SIGMOID), so the codes do not depend on a math library. */
 int i8q_qlinear_unary(int op, const void* X, int64_t n, int qtype, float x_scale, int x_zero_point, float y_scale,
                       int y_zero_point, float alpha, void* Y, void* stream);
 
@@ -426,7 +451,8 @@ int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int64_t input,
 size_t i8q_dq_lstm_workspace_size(int64_t T, int64_t batch, int64_t input, int64_t hidden, int direction);
 
 /* DynamicQuantizeLSTM [LSTM] with the schema's optional inputs and
- * attributes (default activations only: the pages do not list the others).
+ * attributes ("activations", "activation_alpha", "activation_beta", "clip",
+ * "input_forget"; graiphic.io "DynamicQuantizeLSTM", attributes).
  *   W, R: device codes of wtype (I8Q_S8 | I8Q_U8), shapes as above.
  *   W_zero_point, R_zero_point: device codes of wtype, n_wscale / n_rscale
  *   entries (per direction or per channel, in iofc column order), or NULL.
@@ -436,20 +462,44 @@ size_t i8q_dq_lstm_workspace_size(int64_t T, int64_t batch, int64_t input, int64
  *   P: device fp32 [D, 3H] peepholes (Pi, Po, Pf) or NULL.
  *   clip > 0 bounds every gate input to [-clip, clip]; clip <= 0: no clip.
  *   input_forget != 0: f = 1 - i.
- *   Gate terms are summed in the order of the default ONNX LSTM equations:
- *   i = sigmoid(clip(X Wi + H Ri + Pi*C_prev + Wbi + Rbi)),
- *   f = sigmoid(clip(X Wf + H Rf + Pf*C_prev + Wbf + Rbf)),
- *   c~ = tanh(clip(X Wc + H Rc + Wbc + Rbc)), C = f*C_prev + i*c~,
- *   o = sigmoid(clip(X Wo + H Ro + Po*C + Wbo + Rbo)), H = o*tanh(C),
+ *   activations: host array of n_activations I8Q_LSTM_ACT_* values, 3 per
+ *   direction (f, g, h; forward first), or NULL / 0 for Sigmoid, Tanh, Tanh.
+ *   activation_alpha / activation_beta: host arrays (n_alpha, n_beta values,
+ *   may be 0), consumed in the order of the activation functions: each
+ *   function that takes an alpha (beta) takes the next unused value, or its
+ *   ONNX operator's default when the list runs out (LeakyRelu 0.01,
+ *   ThresholdedRelu 1, HardSigmoid 0.2 / 0.5, Elu 1, Affine 1 / 0,
+ *   ScaledTanh 1 / 1).
+ *   Gate terms are summed in the order of the ONNX LSTM equations:
+ *   i = f(clip(X Wi + H Ri + Pi*C_prev + Wbi + Rbi)),
+ *   f = f(clip(X Wf + H Rf + Pf*C_prev + Wbf + Rbf)),
+ *   c~ = g(clip(X Wc + H Rc + Wbc + Rbc)), C = f*C_prev + i*c~,
+ *   o = f(clip(X Wo + H Ro + Po*C + Wbo + Rbo)), H = o*h(C),
  *   where X W and H R are the dequantized products of the per-row uint8
  *   codes with (W - W_zero_point), (R - R_zero_point).
- * Same workspace as i8q_dq_lstm_forward.  Errors: INVALID_ARG, CUDA. */
+ * Same workspace as i8q_dq_lstm_forward.  Errors: INVALID_ARG (also for an
+ * activation outside the list or a wrong count), CUDA. */
 int i8q_dq_lstm_forward_ex(const float* X, int64_t T, int64_t batch, int64_t input, int64_t hidden, int direction,
                            const void* W, const void* R, int wtype, const float* W_scale, const void* W_zero_point,
                            size_t n_wscale, const float* R_scale, const void* R_zero_point, size_t n_rscale,
                            const float* Bias, const int32_t* sequence_lens, const float* h0, const float* c0,
-                           const float* P, float clip, int input_forget, float* Y, float* Y_h, float* Y_c,
+                           const float* P, float clip, int input_forget, const int* activations,
+                           size_t n_activations, const float* activation_alpha, size_t n_alpha,
+                           const float* activation_beta, size_t n_beta, float* Y, float* Y_h, float* Y_c,
                            void* workspace, size_t ws_bytes, void* stream);
+
+/* Test hook (not on the pages): where, inside the workspace of a completed
+ * i8q_dq_lstm_forward / _ex call with these shape arguments, the per-row
+ * uint8 quantization of a hidden state lies.  which = 0: the state the
+ * last step read (h after T-1 steps; h0 when T == 1); which = 1: the final
+ * state (Y_h).  *codes: device bf16 values uh - 128 (exact integers),
+ * [D * batch rows][*row_stride elements], the first `hidden` of each row
+ * meaningful, rows ordered direction-major; *scale, *zero: device fp32 and
+ * int32 [D * batch].  Valid until the workspace is reused.  Synchronize
+ * the call's stream before reading.  Errors: INVALID_ARG. */
+int i8q_dq_lstm_state_codes(const void* workspace, int64_t T, int64_t batch, int64_t input, int64_t hidden,
+                            int direction, int which, const void** codes, const float** scale, const int32_t** zero,
+                            int64_t* row_stride);
 
 /* ========================================================================
  * Measurement (not on the pages)
@@ -478,6 +528,17 @@ int i8q_measure_int8_mma_peak(int64_t iters, void* stream, double* tops);
  * bounded wait since the last call (I8Q_ERR_DEVICE_TIMEOUT), or a pending
  * CUDA error (I8Q_ERR_CUDA).  Clears the recorded state. */
 int i8q_sync_status(void* stream);
+
+/* Failure-detection probe (not on the pages): launch one small kernel on
+ * `stream` that runs one of the library's bounded device waits, with a
+ * limit of limit_ns nanoseconds (1 us .. 1 s), on an event that never
+ * comes: kind 0, an mbarrier phase nobody arrives on (the waits of the
+ * tcgen05 pipelines); kind 1, a grid barrier whose other CTAs never arrive
+ * (the persistent LSTM's).  The wait gives up, records the timeout in the
+ * device status word and the kernel returns, so the next i8q_sync_status
+ * reports I8Q_ERR_DEVICE_TIMEOUT and the context stays usable.  Nothing
+ * else is in flight in the probe.  Errors: INVALID_ARG, CUDA. */
+int i8q_debug_wait_timeout(int kind, int64_t limit_ns, void* stream);
 
 #ifdef __cplusplus
 }

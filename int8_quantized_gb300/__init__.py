@@ -16,7 +16,8 @@ from ._lib import (ACT_GELU, ACT_IDENTITY, ACT_RELU, BF16, F32, LSTM_BIDIRECTION
                    NO_AXIS, S8, S32, U8, I8QError, check, last_error)
 
 __all__ = ["QGemmDyn", "quantize_linear", "dequantize_linear", "qlinearconv", "qlinearconv_workspace_size",
-           "dq_lstm_forward", "dq_lstm_workspace_size", "sync_status", "version", "I8QError", "last_error",
+           "dq_lstm_forward", "dq_lstm_forward_ex", "dq_lstm_state_codes", "dq_lstm_workspace_size", "sync_status",
+           "version", "I8QError", "last_error",
            "F32", "BF16", "S8", "U8", "S32", "ACT_IDENTITY", "ACT_RELU", "ACT_GELU", "NO_AXIS",
            "LSTM_FORWARD", "LSTM_REVERSE", "LSTM_BIDIRECTIONAL"]
 
@@ -152,13 +153,22 @@ class QGemmDyn:
         return (_wrap(uA.value, (self.M, lda.value), torch.uint8), _wrap(sA.value, (self.M,), torch.float32),
                 _wrap(zA.value, (self.M,), torch.int32), lda.value)
 
-    def weight_views(self):
-        """(iBt N x ldb int8, scaleB N fp32, colsum N int32) of the stored B."""
-        q, ldb, s, cs = ctypes.c_void_p(), ctypes.c_size_t(), ctypes.c_void_p(), ctypes.c_void_p()
-        check(_L().i8q_qgemm_dyn_weight_views(self._ctx, ctypes.byref(q), ctypes.byref(ldb), ctypes.byref(s),
-                                              ctypes.byref(cs)), "qgemm_dyn_weight_views")
-        return (_wrap(q.value, (self.N, ldb.value), torch.int8), _wrap(s.value, (self.N,), torch.float32),
-                _wrap(cs.value, (self.N,), torch.int32), ldb.value)
+    def weight_views(self, buf=None):
+        """(iBt N x ldb int32 codes, scaleB N fp32, colsum N int32, ldb) of
+        the stored constant B, or of the B the last forward quantized into
+        buf; the codes are read from whichever copy (int8 or bf16) is kept."""
+        q8, qb, ldb = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_size_t()
+        s, cs = ctypes.c_void_p(), ctypes.c_void_p()
+        check(_L().i8q_qgemm_dyn_weight_views(self._ctx, _dev(buf, "buf"), ctypes.byref(q8), ctypes.byref(qb),
+                                              ctypes.byref(ldb), ctypes.byref(s), ctypes.byref(cs)),
+              "qgemm_dyn_weight_views")
+        if q8.value:
+            codes = _wrap(q8.value, (self.N, ldb.value), torch.int8).to(torch.int32)
+        else:
+            raw = _wrap(qb.value, (self.N, ldb.value), torch.int16)
+            codes = raw.view(torch.bfloat16).float().to(torch.int32)
+        return (codes, _wrap(s.value, (self.N,), torch.float32), _wrap(cs.value, (self.N,), torch.int32),
+                ldb.value)
 
     def clear(self):
         if getattr(self, "_ctx", None) is not None and self._ctx.value:
@@ -171,7 +181,7 @@ class QGemmDyn:
             pass
 
 
-_TYPESTR = {torch.uint8: "|u1", torch.int8: "|i1", torch.float32: "<f4", torch.int32: "<i4"}
+_TYPESTR = {torch.uint8: "|u1", torch.int8: "|i1", torch.float32: "<f4", torch.int32: "<i4", torch.int16: "<i2"}
 
 
 class _DeviceArray:
@@ -401,11 +411,15 @@ def dq_lstm_forward(X, W, R, W_scale, R_scale, workspace, direction=LSTM_FORWARD
 
 def dq_lstm_forward_ex(X, W, R, W_scale, R_scale, workspace, direction=LSTM_FORWARD, B=None, sequence_lens=None,
                        h0=None, c0=None, P=None, clip=0.0, input_forget=False, Y=None, Y_h=None, Y_c=None,
-                       W_zero_point=None, R_zero_point=None, stream=None):
+                       W_zero_point=None, R_zero_point=None, activations=None, activation_alpha=None,
+                       activation_beta=None, stream=None):
     """DynamicQuantizeLSTM with the optional inputs and attributes: W, R
     uint8 or int8 (one dtype) with zero points of that dtype ([D] or
     [D, 4H]); sequence_lens int32 [batch]; P [D, 3H]; clip (<= 0: none);
-    input_forget.  Shapes otherwise as dq_lstm_forward."""
+    input_forget; activations: 3 names per direction from
+    _lib.LSTM_ACTIVATIONS (None: Sigmoid, Tanh, Tanh) with the
+    activation_alpha / activation_beta lists.  Shapes otherwise as
+    dq_lstm_forward."""
     T, batch, I = X.shape
     H = R.shape[1]
     if W.dtype != R.dtype or W.dtype not in (torch.uint8, torch.int8):
@@ -413,13 +427,46 @@ def dq_lstm_forward_ex(X, W, R, W_scale, R_scale, workspace, direction=LSTM_FORW
     for z, n in ((W_zero_point, "W_zero_point"), (R_zero_point, "R_zero_point")):
         if z is not None and z.dtype != W.dtype:
             raise TypeError(f"{n} must have W's dtype")
+    kinds = [_lib.LSTM_ACTIVATIONS.index(a) for a in (activations or [])]
+    alpha = [float(a) for a in (activation_alpha or [])]
+    beta = [float(b) for b in (activation_beta or [])]
+    c_kinds = (ctypes.c_int * max(1, len(kinds)))(*kinds)
+    c_alpha = (ctypes.c_float * max(1, len(alpha)))(*alpha)
+    c_beta = (ctypes.c_float * max(1, len(beta)))(*beta)
     check(_L().i8q_dq_lstm_forward_ex(
         _dev(X, "X", torch.float32), T, batch, I, H, direction, _dev(W, "W"), _dev(R, "R"), _TORCH_TYPE[W.dtype],
         _dev(W_scale, "W_scale", torch.float32), _dev(W_zero_point, "W_zero_point"), W_scale.numel(),
         _dev(R_scale, "R_scale", torch.float32), _dev(R_zero_point, "R_zero_point"), R_scale.numel(),
         _dev(B, "B", torch.float32), _dev(sequence_lens, "sequence_lens", torch.int32),
         _dev(h0, "h0", torch.float32), _dev(c0, "c0", torch.float32), _dev(P, "P", torch.float32), float(clip),
-        int(bool(input_forget)), _dev(Y, "Y", torch.float32), _dev(Y_h, "Y_h", torch.float32),
+        int(bool(input_forget)), c_kinds, len(kinds), c_alpha, len(alpha), c_beta, len(beta),
+        _dev(Y, "Y", torch.float32), _dev(Y_h, "Y_h", torch.float32),
         _dev(Y_c, "Y_c", torch.float32), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)), "dq_lstm_forward_ex")
     return Y, Y_h, Y_c
+
+
+def dq_lstm_state_codes(workspace, T, batch, input_size, hidden, direction, which):
+    """Test hook: the per-row uint8 codes (as int32 [D * batch, hidden]),
+    scales and zero points of a hidden state, read back from the workspace
+    of a completed LSTM call (which 0: the state the last step read; 1: the
+    final state).  Synchronizes the current stream."""
+    codes, scale, zero = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+    stride = ctypes.c_int64()
+    check(_L().i8q_dq_lstm_state_codes(_dev(workspace, "workspace"), T, batch, input_size, hidden, direction, which,
+                                       ctypes.byref(codes), ctypes.byref(scale), ctypes.byref(zero),
+                                       ctypes.byref(stride)), "dq_lstm_state_codes")
+    D = 2 if direction == LSTM_BIDIRECTIONAL else 1
+    base = workspace.data_ptr()
+    torch.cuda.current_stream().synchronize()
+
+    def view(ptr, n, dtype, esize):
+        off = ptr - base
+        if off < 0 or off % esize or off + n * esize > workspace.numel() * workspace.element_size():
+            raise ValueError("state codes outside the workspace")
+        return workspace.view(torch.uint8)[off:off + n * esize].view(dtype)
+
+    rows = D * batch
+    c = view(codes.value, rows * stride.value, torch.bfloat16, 2).view(rows, stride.value)[:, :hidden]
+    return (c.float().to(torch.int32) + 128, view(scale.value, rows, torch.float32, 4).clone(),
+            view(zero.value, rows, torch.int32, 4).clone())

@@ -9,6 +9,9 @@ F32, BF16, S8, U8, S32 = 0, 1, 2, 3, 4
 ACT_IDENTITY, ACT_RELU, ACT_GELU = 0, 1, 2
 NO_AXIS = -(2 ** 31)
 LSTM_FORWARD, LSTM_REVERSE, LSTM_BIDIRECTIONAL = 0, 1, 2
+# I8Q_LSTM_ACT_*: the ONNX LSTM activation functions, in the operator's order
+LSTM_ACTIVATIONS = ["Relu", "Tanh", "Sigmoid", "Affine", "LeakyRelu", "ThresholdedRelu", "ScaledTanh", "HardSigmoid",
+                    "Elu", "Softsign", "Softplus"]
 
 OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NOT_INITIALIZED, ERR_ALLOC, ERR_CUDA, ERR_DEVICE_TIMEOUT = -1, -2, -3, -4, -5, -6
@@ -34,8 +37,8 @@ SIGNATURES = {
     "i8q_qgemm_dyn_forward_s32": (_i, [_p, _p, _p, _p, _p, _p]),
     "i8q_qgemm_dyn_buf_views": (_i, [_p, _p, ctypes.POINTER(_p), ctypes.POINTER(_sz), ctypes.POINTER(_p),
                                      ctypes.POINTER(_p)]),
-    "i8q_qgemm_dyn_weight_views": (_i, [_p, ctypes.POINTER(_p), ctypes.POINTER(_sz), ctypes.POINTER(_p),
-                                        ctypes.POINTER(_p)]),
+    "i8q_qgemm_dyn_weight_views": (_i, [_p, _p, ctypes.POINTER(_p), ctypes.POINTER(_p), ctypes.POINTER(_sz),
+                                        ctypes.POINTER(_p), ctypes.POINTER(_p)]),
     "i8q_qgemm_dyn_clear": (None, [ctypes.POINTER(_p)]),
     "i8q_quantize_linear": (_i, [_p, _p, _i, _i, _p, _p, _sz, _i, _p, _p]),
     "i8q_dequantize_linear": (_i, [_p, _i, _p, _i, _i, _p, _p, _sz, _p, _p]),
@@ -50,7 +53,9 @@ SIGNATURES = {
     "i8q_dynamic_quantize_matmul": (_i, [_p, _i64, _i64, _p, _i, _i64, _p, _p, _sz, _p, _p, _p, _p, _p, _sz, _p]),
     "i8q_matmul_integer_workspace_size": (_sz, [_i64, _i64, _i64]),
     "i8q_dq_lstm_forward_ex": (_i, [_p, _i64, _i64, _i64, _i64, _i, _p, _p, _i, _p, _p, _sz, _p, _p, _sz, _p, _p, _p,
-                                    _p, _p, _f, _i, _p, _p, _p, _p, _sz, _p]),
+                                    _p, _p, _f, _i, _p, _sz, _p, _sz, _p, _sz, _p, _p, _p, _p, _sz, _p]),
+    "i8q_dq_lstm_state_codes": (_i, [_p, _i64, _i64, _i64, _i64, _i, _i, ctypes.POINTER(_p), ctypes.POINTER(_p),
+                                     ctypes.POINTER(_p), ctypes.POINTER(_i64)]),
     "i8q_qlinear_binary": (_i, [_i, _p, _p, _i, _f, _i, _p, _p, _i, _f, _i, _f, _i, _i, _p, _p]),
     "i8q_mul_integer": (_i, [_p, _i, _p, _i, _i, _p, _i, _p, _i, _i, _p, _p]),
     "i8q_qlinear_unary": (_i, [_i, _p, _i64, _i, _f, _i, _f, _i, _f, _p, _p]),
@@ -58,6 +63,7 @@ SIGNATURES = {
                                  _p, _p, _p, _sz, _p]),
     "i8q_dq_lstm_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i]),
     "i8q_sync_status": (_i, [_p]),
+    "i8q_debug_wait_timeout": (_i, [_i, _i64, _p]),
     "i8q_profile_enable": (_i, [_i]),
     "i8q_profile_collect": (_i, []),
     "i8q_profile_entry": (_i, [_i, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_longlong),

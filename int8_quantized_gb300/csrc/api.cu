@@ -2,6 +2,7 @@
 // dynamic quantized inner-product context (Simd
 // "SynetDynamicQuantizedInnerProduct16b": Init, Enable, InternalBufferSize,
 // ExternalBufferSize, Info, SetParams, Forward, Clear).
+#include <map>
 #include <mutex>
 #include <new>
 #include <string>
@@ -42,6 +43,32 @@ int sm_count() {
     g_sm_count[dev] = n;
   }
   return g_sm_count[dev];
+}
+
+int once_per_device(const void* key, int (*init)(void*), void* arg) {
+  int dev = 0;
+  I8Q_CUDA_TRY(cudaGetDevice(&dev));
+  static std::recursive_mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;
+  std::lock_guard<std::recursive_mutex> lk(mu);
+  const auto k = std::make_pair(key, dev);
+  auto it = done.find(k);
+  if (it != done.end()) return it->second;
+  const int rc = init(arg);
+  done[k] = rc;
+  return rc;
+}
+
+int smem_attr(const void* func, int bytes) {
+  struct A {
+    const void* f;
+    int b;
+  } a{func, bytes};
+  return once_per_device(func, [](void* p) -> int {
+    const A* x = static_cast<const A*>(p);
+    I8Q_CUDA_TRY(cudaFuncSetAttribute(x->f, cudaFuncAttributeMaxDynamicSharedMemorySize, x->b));
+    return I8Q_OK;
+  }, &a);
 }
 
 uint32_t* device_status_word() {
@@ -582,14 +609,26 @@ extern "C" int i8q_qgemm_dyn_buf_views(i8q_qgemm_ctx* ctx, void* buf, uint8_t** 
   return I8Q_OK;
 }
 
-extern "C" int i8q_qgemm_dyn_weight_views(i8q_qgemm_ctx* ctx, int8_t** iBt, size_t* ldb, float** scaleB,
-                                          int32_t** colsum) {
+extern "C" int i8q_qgemm_dyn_weight_views(i8q_qgemm_ctx* ctx, void* buf, int8_t** iBt, void** iBt_bf16, size_t* ldb,
+                                          float** scaleB, int32_t** colsum) {
   if (!ctx) return fail(I8Q_ERR_NOT_INITIALIZED, "qgemm_dyn_weight_views: no context");
-  if (!ctx->constB) return fail(I8Q_ERR_INVALID_ARG, "qgemm_dyn_weight_views: B is not constant");
-  if (iBt) *iBt = ctx->iBt;
   if (ldb) *ldb = (size_t)ctx->Kp;
-  if (scaleB) *scaleB = ctx->scaleB;
-  if (colsum) *colsum = ctx->colsum;
+  if (ctx->constB) {
+    if (iBt) *iBt = ctx->iBt;
+    if (iBt_bf16) *iBt_bf16 = ctx->iBt_bf16;
+    if (scaleB) *scaleB = ctx->scaleB;
+    if (colsum) *colsum = ctx->colsum;
+    return I8Q_OK;
+  }
+  // B quantized by the last Forward into buf: the tensor-core product
+  // writes only the bf16 codes, the other cores only the int8 ones
+  uint8_t* base = static_cast<uint8_t*>(buf ? buf : ctx->fallback);
+  if (!base) return fail(I8Q_ERR_INVALID_ARG, "qgemm_dyn_weight_views: no buffer");
+  const BufLayout L = buf_layout(ctx);
+  if (iBt) *iBt = ctx->use_tc ? nullptr : reinterpret_cast<int8_t*>(base + L.iBt);
+  if (iBt_bf16) *iBt_bf16 = ctx->use_tc ? base + L.iBt_bf16 : nullptr;
+  if (scaleB) *scaleB = reinterpret_cast<float*>(base + L.scaleB);
+  if (colsum) *colsum = reinterpret_cast<int32_t*>(base + L.colsum);
   return I8Q_OK;
 }
 

@@ -38,6 +38,16 @@ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
 
+// Run init once per (key, current device), thread-safely, and return its
+// status; later calls on that device return the first status.  Kernel
+// attributes and occupancy figures belong to a device, so each device sets
+// them up the first time a launch meets it.
+int once_per_device(const void* key, int (*init)(void*), void* arg);
+
+// cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes) once per
+// device.
+int smem_attr(const void* func, int bytes);
+
 // Device-side status word for bounded waits (see i8q_sync_status).
 uint32_t* device_status_word();
 
@@ -228,6 +238,136 @@ __device__ __forceinline__ float2 gelu_bf16out2(float2 x) {
   const float2 te = mul2_rn(mul2_rn(t, make_float2(kT, kT)), e);
   return fma2_rn(ax, te, make_float2(fmaxf(x.x, 0.0f), fmaxf(x.y, 0.0f)));
 }
+
+// ---- fp32 elementary functions with a fixed operation sequence ----------
+// exp, expm1, log1p, sigmoid, tanh and softplus as used by the LSTM gates
+// and QLinearSigmoid.  Library versions of these differ in the last bit
+// between platforms, and one bit of an LSTM hidden state can move a uint8
+// code of the next step's dynamic quantization.  Each is therefore one fixed
+// sequence of IEEE fp32 operations (every add, multiply, divide and fused
+// multiply-add rounds once to nearest even; scaling by a power of two is
+// exact in the normal range), so any IEEE implementation of the same
+// sequence gives the same bits.
+//  exp   Cody and Waite's argument reduction (Software Manual for the
+//        Elementary Functions, 1980): n = rint(x / ln2), r = (x - n LN2_HI)
+//        - n LN2_LO with LN2_HI = fl(ln 2), LN2_LO = fl(ln 2 - LN2_HI);
+//        e^r = sum_{k<=7} r^k / k! in Horner form (truncation below 2^-27
+//        for |r| <= ln2 / 2); times 2^n as two exact power-of-two factors,
+//        so that a subnormal result rounds once.  Within 1 ulp.
+//  expm1 the same reduction, e^r - 1 = r (1 + r/2! + ... + r^7/8!), and
+//        e^x - 1 = 2^n (e^r - 1) + (2^n - 1); e^x above 20, -1 below -20.
+//  log1p on [0, 1]: 1 + u = 2^k (1 + v), k in {0, 1}, v in [sqrt(1/2) - 1,
+//        sqrt(2) - 1]; log(1 + v) = 2 atanh(s), s = v / (2 + v), by the
+//        series 2 s (1 + s^2/3 + s^4/5 + s^6/7 + s^8/9).
+//  sigmoid(x) = 1 / (1 + e^-x).  tanh(a) for a = |x|: e / (e + 2) with
+//        e = expm1(2a) below 0.625, 1 - 2 / (e^2a + 1) up to 9.5, 1 above
+//        (where tanh rounds to 1); the sign of x copied on.
+//  softplus(x) = x + log1p(e^-x) for x > 0, log1p(e^x) otherwise.
+// The constants are the fp32 roundings of the numbers named beside them.
+namespace ef {
+constexpr float kL2E = 0x1.715476p+0f;      // 1 / ln 2
+constexpr float kLn2Hi = 0x1.62e430p-1f;    // ln 2
+constexpr float kLn2Lo = -0x1.05c610p-29f;  // ln 2 - kLn2Hi
+
+// 2^k for -126 <= k <= 127, exactly.
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
+
+__device__ __forceinline__ float exp32(float x) {
+  x = fminf(fmaxf(x, -104.0f), 89.0f);  // e^89 overflows to inf; e^-104 rounds to 0
+  const float nf = rintf(__fmul_rn(x, kL2E));
+  const int n = (int)nf;
+  float r = __fmaf_rn(-nf, kLn2Hi, x);
+  r = __fmaf_rn(-nf, kLn2Lo, r);
+  float p = 0x1.a01a02p-13f;            // 1/7!
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/6!
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);   // 1/5!
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);   // 1/4!
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);   // 1/3!
+  p = __fmaf_rn(p, r, 0.5f);             // 1/2!
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const int n1 = n / 2, n2 = n - n1;     // both within [-75, 65]
+  return __fmul_rn(__fmul_rn(p, pow2i(n1)), pow2i(n2));
+}
+
+__device__ __forceinline__ float expm1_32(float x) {
+  if (x > 20.0f) return exp32(x);
+  if (x < -20.0f) return -1.0f;
+  const float nf = rintf(__fmul_rn(x, kL2E));
+  const int n = (int)nf;                 // |n| <= 29
+  float r = __fmaf_rn(-nf, kLn2Hi, x);
+  r = __fmaf_rn(-nf, kLn2Lo, r);
+  float q = 0x1.a01a02p-16f;             // 1/8!
+  q = __fmaf_rn(q, r, 0x1.a01a02p-13f);  // 1/7!
+  q = __fmaf_rn(q, r, 0x1.6c16c2p-10f);  // 1/6!
+  q = __fmaf_rn(q, r, 0x1.111112p-7f);   // 1/5!
+  q = __fmaf_rn(q, r, 0x1.555556p-5f);   // 1/4!
+  q = __fmaf_rn(q, r, 0x1.555556p-3f);   // 1/3!
+  q = __fmaf_rn(q, r, 0.5f);             // 1/2!
+  q = __fmaf_rn(q, r, 1.0f);
+  q = __fmul_rn(q, r);                   // e^r - 1
+  if (n == 0) return q;
+  const float t = pow2i(n);
+  return __fmaf_rn(t, q, __fsub_rn(t, 1.0f));
+}
+
+// log(1 + u), 0 <= u <= 1.
+__device__ __forceinline__ float log1p01(float u) {
+  float v = u, k = 0.0f;
+  if (u > 0x1.a8279ap-2f) {  // sqrt(2) - 1
+    v = __fmul_rn(__fsub_rn(u, 1.0f), 0.5f);  // exact: 1 + u = 2 (1 + v)
+    k = 1.0f;
+  }
+  const float s = __fdiv_rn(v, __fadd_rn(2.0f, v));
+  const float z = __fmul_rn(s, s);
+  float w = 0x1.c71c72p-4f;              // 1/9
+  w = __fmaf_rn(w, z, 0x1.24924ap-3f);   // 1/7
+  w = __fmaf_rn(w, z, 0x1.99999ap-3f);   // 1/5
+  w = __fmaf_rn(w, z, 0x1.555556p-2f);   // 1/3
+  w = __fmaf_rn(w, z, 1.0f);
+  return __fmaf_rn(k, kLn2Hi, __fmul_rn(__fadd_rn(s, s), w));
+}
+
+__device__ __forceinline__ float sigmoid32(float x) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp32(-x))); }
+
+__device__ __forceinline__ float tanh32(float x) {
+  const float a = fabsf(x);
+  float t = 1.0f;
+  if (a < 0.625f) {
+    const float e = expm1_32(__fadd_rn(a, a));
+    t = __fdiv_rn(e, __fadd_rn(e, 2.0f));
+  } else if (a <= 9.5f) {
+    t = __fsub_rn(1.0f, __fdiv_rn(2.0f, __fadd_rn(exp32(__fadd_rn(a, a)), 1.0f)));
+  }
+  return copysignf(t, x);
+}
+
+__device__ __forceinline__ float softplus32(float x) {
+  return x > 0.0f ? __fadd_rn(x, log1p01(exp32(-x))) : log1p01(exp32(x));
+}
+
+// The LSTM activation functions (I8Q_LSTM_ACT_*, the ONNX LSTM list) with
+// their alpha / beta, each its operator's formula, one rounding per step.
+__device__ __forceinline__ float lstm_act(int kind, float alpha, float beta, float x) {
+  switch (kind) {
+    case I8Q_LSTM_ACT_RELU: return x > 0.0f ? x : 0.0f;
+    case I8Q_LSTM_ACT_TANH: return tanh32(x);
+    case I8Q_LSTM_ACT_SIGMOID: return sigmoid32(x);
+    case I8Q_LSTM_ACT_AFFINE: return __fadd_rn(__fmul_rn(alpha, x), beta);
+    case I8Q_LSTM_ACT_LEAKY_RELU: return x >= 0.0f ? x : __fmul_rn(alpha, x);
+    case I8Q_LSTM_ACT_THRESHOLDED_RELU: return x > alpha ? x : 0.0f;
+    case I8Q_LSTM_ACT_SCALED_TANH: return __fmul_rn(alpha, tanh32(__fmul_rn(beta, x)));
+    case I8Q_LSTM_ACT_HARD_SIGMOID: {
+      const float v = __fadd_rn(__fmul_rn(alpha, x), beta);
+      return v < 0.0f ? 0.0f : (v > 1.0f ? 1.0f : v);
+    }
+    case I8Q_LSTM_ACT_ELU: return x >= 0.0f ? x : __fmul_rn(alpha, expm1_32(x));
+    case I8Q_LSTM_ACT_SOFTSIGN: return __fdiv_rn(x, __fadd_rn(1.0f, fabsf(x)));
+    case I8Q_LSTM_ACT_SOFTPLUS: return softplus32(x);
+  }
+  return x;
+}
+}  // namespace ef
 
 __device__ __forceinline__ float activate(float v, int act) {
   if (act == I8Q_ACT_RELU) return v > 0.0f ? v : 0.0f;

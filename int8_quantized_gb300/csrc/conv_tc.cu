@@ -530,17 +530,14 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
     I8Q_PROF("conv_center_operands", s);
     const size_t row_smem = (size_t)W * (Cp + 8) * 2;
     if (row_smem <= 200 * 1024) {
-      static std::once_flag once_u8, once_s8;
       if (xtype == I8Q_U8) {
-        std::call_once(once_u8, [] {
-          cudaFuncSetAttribute(center_x_row<uint8_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        });
+        const int ar = smem_attr((const void*)center_x_row<uint8_t>, 200 * 1024);
+        if (ar) return ar;
         center_x_row<uint8_t><<<dim3((unsigned)H, (unsigned)N), 256, row_smem, s>>>((const uint8_t*)x, (int)C, (int)H,
                                                                                    (int)W, (int)Cp, x_zp, xc);
       } else {
-        std::call_once(once_s8, [] {
-          cudaFuncSetAttribute(center_x_row<int8_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        });
+        const int ar = smem_attr((const void*)center_x_row<int8_t>, 200 * 1024);
+        if (ar) return ar;
         center_x_row<int8_t><<<dim3((unsigned)H, (unsigned)N), 256, row_smem, s>>>((const int8_t*)x, (int)C, (int)H,
                                                                                  (int)W, (int)Cp, x_zp, xc);
       }
@@ -575,12 +572,8 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
   const int xmax = xtype == I8Q_U8 ? std::max(x_zp, 255 - x_zp) : std::max(x_zp + 128, 127 - x_zp);
   constexpr int TN = 224;
   using T = ConvTile<TN>;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(conv_tc_kernel<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(conv_tc_kernel)");
+  const int ar = smem_attr((const void*)conv_tc_kernel<TN>, T::SMEM_BYTES);
+  if (ar) return ar;
   ConvParams p;
   p.M = (int)M;
   p.CC = (int)(Cp / 64);

@@ -188,11 +188,8 @@ int launch_gemm_imma(const uint8_t* uA, const int8_t* iBt, int64_t M, int64_t N,
                      cudaStream_t s) {
   if (M <= 0 || N <= 0) return I8Q_OK;
   if (Kp % BK != 0) return fail(I8Q_ERR_INVALID_ARG, "gemm_imma: Kp must be a multiple of 64");
-  static bool attr_set = false;
-  if (!attr_set) {
-    I8Q_CUDA_TRY(cudaFuncSetAttribute(gemm_imma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-    attr_set = true;
-  }
+  const int ar = smem_attr((const void*)gemm_imma_kernel, SMEM_BYTES);
+  if (ar) return ar;
   if (ceil_div(M, BM) > 65535) return fail(I8Q_ERR_UNSUPPORTED, "gemm_imma: M too large");
   dim3 grid((unsigned)ceil_div(N, BN), (unsigned)ceil_div(M, BM));
   I8Q_PROF("gemm_imma", s);

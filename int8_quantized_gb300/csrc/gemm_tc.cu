@@ -924,15 +924,18 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   }
 }
 
-// Clusters of two CTAs of the pair kernel that fit on the device at once
-// (0 when none do; -1 on a CUDA error), computed once per instantiation.
+// Clusters of two CTAs of the pair kernel that fit on the current device
+// at once (0 when none do; -1 on a CUDA error), computed once per
+// instantiation and device.
 template <int EPI>
 int pair_max_clusters() {
-  static std::once_flag once;
-  static int n = -1;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+  static int n[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(I8Q_ERR_CUDA, "gemm_tc: no device"), -1;
+  const int rc = once_per_device((const void*)&n, [](void* p) -> int {
+    int* out = static_cast<int*>(p);
+    cudaError_t err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           P_SMEM_BYTES);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  P_SMEM_BYTES);
@@ -940,7 +943,7 @@ int pair_max_clusters() {
       if (err == cudaSuccess)
         err = cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    P_SMEM_BYTES);
-    if (err != cudaSuccess) return;
+    if (err != cudaSuccess) return cuda_fail(err, "gemm_tc: pair kernel setup");
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -954,13 +957,11 @@ int pair_max_clusters() {
     cfg.numAttrs = 1;
     int c = 0;
     err = cudaOccupancyMaxActiveClusters(&c, gemm_tc_pair_kernel<EPI>, &cfg);
-    if (err == cudaSuccess) n = c;
-  });
-  if (err != cudaSuccess) {
-    cuda_fail(err, "gemm_tc: pair kernel setup");
-    return -1;
-  }
-  return n;
+    if (err != cudaSuccess) return cuda_fail(err, "gemm_tc: pair kernel occupancy");
+    *out = c;
+    return I8Q_OK;
+  }, n + dev);
+  return rc ? -1 : n[dev];
 }
 
 // Shared launch of both kernels for either epilogue kind.  prof1 / prof2
@@ -982,12 +983,8 @@ int launch_tc_impl(const __nv_bfloat16* uA, const __nv_bfloat16* iBt, int64_t M,
   const int CS = (int)std::max<int64_t>(1, chunk_k / BK);
   uint32_t* status = device_status_word();
   if (!status) return fail(I8Q_ERR_CUDA, "gemm_tc: no device status word");
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(gemm_tc_kernel)");
+  const int ar = smem_attr((const void*)gemm_tc_kernel<EPI>, SMEM_BYTES);
+  if (ar) return ar;
   TcParams p = base;
   p.M = M;
   p.N = N;

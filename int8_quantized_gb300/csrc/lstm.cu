@@ -4,8 +4,11 @@
 //
 // int8 W [D, input, 4H] and R [D, H, 4H] with per-channel (or per-direction)
 // scales and zero point 0; fp32 X; default activations (sigmoid for the
-// i, o, f gates, tanh for the cell candidate and the output); gate column
-// order i, o, f, c.  X and each step's hidden state are quantized per row to
+// i, o, f gates, tanh for the cell candidate and the output; the general
+// form takes any of the ONNX LSTM activation functions); gate column
+// order i, o, f, c.  sigmoid and tanh are the fixed-sequence fp32
+// functions of common.cuh (ef::), so a step's result does not depend on
+// the platform's math library.  X and each step's hidden state are quantized per row to
 // uint8 exactly like A of the dynamic quantized inner product.
 //   input projection (all steps at once): Gx = X W[d]
 //   per step t: Gh = h_{t-1} R[d]; g = ((Gx_t + Gh) + Wb) + Rb
@@ -74,10 +77,12 @@ LstmLayout lstm_layout(int64_t T, int64_t batch, int64_t input, int64_t hidden, 
   L.off_sX = take((size_t)L.TB * 4);
   L.off_zX = take((size_t)L.TB * 4);
   L.off_Gx = take((size_t)L.D * L.TB * L.H4 * 4);
-  L.off_uh = take((size_t)L.D * batch * L.Hp);
-  // h codes, scales and zero points: two step parities (the per-step
-  // kernels use the first), per-row min/max pairs and a barrier counter
-  // for the persistent recurrence
+  // h codes (uint8 for the mma.sync step, bf16 uh - 128 for the tensor
+  // pipe), scales and zero points, in two step parities: step s reads
+  // parity (s + 1) & 1 and the codes of its new h go to parity s & 1 (h0's
+  // to parity 1); then per-row min/max pairs and a barrier counter for the
+  // persistent recurrence
+  L.off_uh = take((size_t)2 * L.D * batch * L.Hp);
   L.off_uhc = take((size_t)2 * L.D * batch * L.Hp * 2);
   L.off_sh = take((size_t)2 * L.D * batch * 4);
   L.off_zh = take((size_t)2 * L.D * batch * 4);
@@ -183,7 +188,15 @@ repack_gates_zp(const uint8_t* __restrict__ W, int64_t K, int64_t H, const uint8
   }
 }
 
-__device__ __forceinline__ float sigmoid_f32(float x) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x))); }
+using ef::sigmoid32;
+using ef::tanh32;
+
+// The three activation functions (f, g, h) of each direction with their
+// alpha / beta (the general form only).
+struct LstmActs {
+  int kind[2][3];
+  float alpha[2][3], beta[2][3];
+};
 
 // ---- the fused step ------------------------------------------------------------
 constexpr int SB = 64, SN = 64, SK = 64, SSTAGES = 3, STHREADS = 128;
@@ -339,13 +352,13 @@ __global__ void __launch_bounds__(STHREADS) lstm_step_kernel(StepParams p) {
     const int r = pi >> 4, uu = pi & 15;
     const int b = m0 + r, u = n0 / 4 + uu;
     if (b >= p.B || u >= p.H) continue;
-    const float ig = sigmoid_f32(gs[r][4 * uu + 0]);
-    const float og = sigmoid_f32(gs[r][4 * uu + 1]);
-    const float fg = sigmoid_f32(gs[r][4 * uu + 2]);
-    const float ct = tanhf(gs[r][4 * uu + 3]);
+    const float ig = sigmoid32(gs[r][4 * uu + 0]);
+    const float og = sigmoid32(gs[r][4 * uu + 1]);
+    const float fg = sigmoid32(gs[r][4 * uu + 2]);
+    const float ct = tanh32(gs[r][4 * uu + 3]);
     const int64_t e = ((int64_t)d * p.B + b) * p.H + u;
     const float cn = __fadd_rn(__fmul_rn(fg, p.c[e]), __fmul_rn(ig, ct));
-    const float hn = __fmul_rn(og, tanhf(cn));
+    const float hn = __fmul_rn(og, tanh32(cn));
     p.c[e] = cn;
     p.h_next[e] = hn;
     if (p.Y) p.Y[(((int64_t)t * p.D + d) * p.B + b) * p.H + u] = hn;
@@ -371,8 +384,9 @@ constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
 constexpr uint32_t ST_TIMEOUT = 1u << 8;
 
 struct TcStepParams {
-  const float* sh;     // [D*B]
+  const float* sh;     // [D*B] of the parity this step reads
   const int32_t* zh;   // [D*B]
+  int hrow0;           // first row of that parity in the h-code tensor map
   const int32_t* Rcs;  // [D, 4H]
   const float* Rsc;    // [D, 4H]
   const float* Gx;     // [D, T*B, 4H]
@@ -389,6 +403,7 @@ struct TcStepParams {
   const float* P;            // [D, 3H] peepholes (i, o, f) or null
   float clip;                // > 0: gate inputs bounded to [-clip, clip]
   int input_forget;          // f = 1 - i
+  LstmActs acts;
 };
 
 __device__ __forceinline__ float clip_gate(float v, float clip) {
@@ -442,7 +457,7 @@ lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
         if (!wait_bar(empty(s), ((uint32_t)(kt / STAGES) & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT)) break;
         mbar_arrive_expect_tx(full(s), STAGE_BYTES);
         tma_load_2d(sA(s), &tmR, full(s), kt * BK, d * H4 + mt * BM);
-        tma_load_2d(sB(s), &tmH, full(s), kt * BK, d * p.B + nb * BN);
+        tma_load_2d(sB(s), &tmH, full(s), kt * BK, p.hrow0 + d * p.B + nb * BN);
       }
       if (kt < KT)
         for (int j = max(0, kt - STAGES); j < kt; ++j) {
@@ -556,7 +571,8 @@ lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
           if (q != 1) {
             float gg = __fadd_rn(__fadd_rn(sum, wb), rb);
             gg = clip_gate(gg, p.clip);
-            act = q == 3 ? tanhf(gg) : sigmoid_f32(gg);
+            act = q == 3 ? ef::lstm_act(p.acts.kind[d][1], p.acts.alpha[d][1], p.acts.beta[d][1], gg)
+                         : ef::lstm_act(p.acts.kind[d][0], p.acts.alpha[d][0], p.acts.beta[d][0], gg);
           }
         }
         const float ig = __shfl_sync(0xffffffffu, act, base_lane + 0);
@@ -570,13 +586,13 @@ lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
           float so = sum;
           if (p.P) so = __fadd_rn(so, __fmul_rn(pw, cn));
           so = __fadd_rn(__fadd_rn(so, wb), rb);
-          og = sigmoid_f32(clip_gate(so, p.clip));
+          og = ef::lstm_act(p.acts.kind[d][0], p.acts.alpha[d][0], p.acts.beta[d][0], clip_gate(so, p.clip));
         }
         og = __shfl_sync(0xffffffffu, og, base_lane + 1);
         if (q == 0 && b < p.B && nvalid && u < p.H) {
           const int64_t e = ((int64_t)d * p.B + b) * p.H + u;
           if (live) {
-            const float hn = __fmul_rn(og, tanhf(cn));
+            const float hn = __fmul_rn(og, ef::lstm_act(p.acts.kind[d][2], p.acts.alpha[d][2], p.acts.beta[d][2], cn));
             p.c[e] = cn;
             p.h_next[e] = hn;
             if (p.Y) {
@@ -610,7 +626,7 @@ lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
           float gg = __fadd_rn(gx[j], gh);
           gg = __fadd_rn(gg, wb);
           gg = __fadd_rn(gg, rb);
-          act = q < 3 ? sigmoid_f32(gg) : tanhf(gg);
+          act = q < 3 ? sigmoid32(gg) : tanh32(gg);
         }
         const float ig = __shfl_sync(0xffffffffu, act, base_lane + 0);
         const float og = __shfl_sync(0xffffffffu, act, base_lane + 1);
@@ -619,7 +635,7 @@ lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
         if (q == 0 && bvalid && nvalid && u < p.H) {
           const int64_t e = ((int64_t)d * p.B + b) * p.H + u;
           const float cn = __fadd_rn(__fmul_rn(fg, cprev[j]), __fmul_rn(ig, ct));
-          const float hn = __fmul_rn(og, tanhf(cn));
+          const float hn = __fmul_rn(og, tanh32(cn));
           p.c[e] = cn;
           p.h_next[e] = hn;
           if (p.Y) p.Y[(((int64_t)t * p.D + d) * p.B + b) * p.H + u] = hn;
@@ -697,6 +713,7 @@ struct Params {
   const float* P;
   float clip;
   int input_forget;
+  LstmActs acts;
 };
 
 size_t smem_bytes(int64_t Hp) { return 1024 + (size_t)STAGES * A_STAGE + (size_t)(Hp / BK) * R_SLAB + NUM_BARS * 8 + 16; }
@@ -715,7 +732,8 @@ __device__ __forceinline__ float ord_value(uint32_t v) {
 // CTA-wide barrier: the fence makes the CTA's writes visible before the
 // arrival (cumulatively); true when every CTA has arrived, false on
 // timeout or when another CTA gave up.
-__device__ __forceinline__ bool grid_barrier(uint32_t* gbar, uint32_t target, uint32_t* status) {
+__device__ __forceinline__ bool grid_barrier(uint32_t* gbar, uint32_t target, uint32_t* status,
+                                             unsigned long long limit_ns = WAIT_LIMIT_NS) {
   __threadfence();
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(gbar) : "memory");
   const unsigned long long t0 = global_ns();
@@ -725,11 +743,36 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* gbar, uint32_t target, ui
     if (v >= target) return true;
     if ((i & 63u) == 63u) {
       if (*(volatile uint32_t*)status & ST_TIMEOUT) return false;
-      if (global_ns() - t0 > WAIT_LIMIT_NS) {
+      if (global_ns() - t0 > limit_ns) {
         atomicOr(status, ST_TIMEOUT);
         return false;
       }
     }
+  }
+}
+
+// Failure-detection probe: one CTA runs one of the bounded waits above with
+// a short limit on an event that never comes -- an mbarrier phase nobody
+// arrives on (kind 0, the waits of the tcgen05 pipelines) or a grid
+// barrier whose other CTAs never arrive (kind 1, the persistent
+// recurrence's) -- so that the wait gives up, records its code in the
+// status word and the kernel returns.  Nothing is in flight while it waits.
+__device__ uint32_t g_probe_counter;
+
+__global__ void wait_probe_kernel(int kind, unsigned long long limit_ns, uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  if (kind == 0) {
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    wait_bar(b, 0, &abort_flag, status, ST_TIMEOUT, limit_ns);
+  } else {
+    g_probe_counter = 0;
+    __threadfence();
+    grid_barrier(&g_probe_counter, 2, status, limit_ns);   // a second CTA that does not exist
   }
 }
 
@@ -1010,22 +1053,27 @@ lstm_persist_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
               si = __fadd_rn(si, __fmul_rn(pw[0][ul], cp[k]));
               sf = __fadd_rn(sf, __fmul_rn(pw[2][ul], cp[k]));
             }
-            const float ig = sigmoid_f32(clip_gate(__fadd_rn(__fadd_rn(si, cst[2][c0]), cst[3][c0]), p.clip));
-            const float fg = p.input_forget
-                                 ? __fsub_rn(1.0f, ig)
-                                 : sigmoid_f32(clip_gate(__fadd_rn(__fadd_rn(sf, cst[2][c0 + 2]), cst[3][c0 + 2]), p.clip));
-            const float ct = tanhf(clip_gate(__fadd_rn(__fadd_rn(sc, cst[2][c0 + 3]), cst[3][c0 + 3]), p.clip));
+            const int fk = p.acts.kind[d][0], gk = p.acts.kind[d][1];
+            const float fa = p.acts.alpha[d][0], fb = p.acts.beta[d][0];
+            const float ig = ef::lstm_act(fk, fa, fb, clip_gate(__fadd_rn(__fadd_rn(si, cst[2][c0]), cst[3][c0]), p.clip));
+            const float fg =
+                p.input_forget
+                    ? __fsub_rn(1.0f, ig)
+                    : ef::lstm_act(fk, fa, fb, clip_gate(__fadd_rn(__fadd_rn(sf, cst[2][c0 + 2]), cst[3][c0 + 2]), p.clip));
+            const float ct = ef::lstm_act(gk, p.acts.alpha[d][1], p.acts.beta[d][1],
+                                          clip_gate(__fadd_rn(__fadd_rn(sc, cst[2][c0 + 3]), cst[3][c0 + 3]), p.clip));
             cn = __fadd_rn(__fmul_rn(fg, cp[k]), __fmul_rn(ig, ct));
             if (p.P) so = __fadd_rn(so, __fmul_rn(pw[1][ul], cn));
-            og = sigmoid_f32(clip_gate(__fadd_rn(__fadd_rn(so, cst[2][c0 + 1]), cst[3][c0 + 1]), p.clip));
+            og = ef::lstm_act(fk, fa, fb, clip_gate(__fadd_rn(__fadd_rn(so, cst[2][c0 + 1]), cst[3][c0 + 1]), p.clip));
+            hn[k] = __fmul_rn(og, ef::lstm_act(p.acts.kind[d][2], p.acts.alpha[d][2], p.acts.beta[d][2], cn));
           } else {
-            const float ig = sigmoid_f32(__fadd_rn(__fadd_rn(si, cst[2][c0]), cst[3][c0]));
-            og = sigmoid_f32(__fadd_rn(__fadd_rn(so, cst[2][c0 + 1]), cst[3][c0 + 1]));
-            const float fg = sigmoid_f32(__fadd_rn(__fadd_rn(sf, cst[2][c0 + 2]), cst[3][c0 + 2]));
-            const float ct = tanhf(__fadd_rn(__fadd_rn(sc, cst[2][c0 + 3]), cst[3][c0 + 3]));
+            const float ig = sigmoid32(__fadd_rn(__fadd_rn(si, cst[2][c0]), cst[3][c0]));
+            og = sigmoid32(__fadd_rn(__fadd_rn(so, cst[2][c0 + 1]), cst[3][c0 + 1]));
+            const float fg = sigmoid32(__fadd_rn(__fadd_rn(sf, cst[2][c0 + 2]), cst[3][c0 + 2]));
+            const float ct = tanh32(__fadd_rn(__fadd_rn(sc, cst[2][c0 + 3]), cst[3][c0 + 3]));
             cn = __fadd_rn(__fmul_rn(fg, cp[k]), __fmul_rn(ig, ct));
+            hn[k] = __fmul_rn(og, tanh32(cn));
           }
-          hn[k] = __fmul_rn(og, tanhf(cn));
           cp[k] = cn;
         }
         *reinterpret_cast<float2*>(p.c + row * p.H + u0) = make_float2(cp[0], cp[1]);
@@ -1112,6 +1160,8 @@ struct LstmGraphKey {
   const void *X, *W, *R, *W_scale, *R_scale, *Bias, *h0, *c0, *Y, *Y_h, *Y_c, *workspace;
   const void *W_zero_point, *R_zero_point, *seq_lens, *P;
   int64_t T, batch, input, hidden, direction, n_wscale, n_rscale, wtype, input_forget, clip_bits;
+  int64_t act_kinds;      // the six activation kinds, 4 bits each
+  int64_t act_params[6];  // alpha, beta bit patterns of each
 };
 
 // Launch the recurrence as a CUDA graph on s: the cached one when key
@@ -1130,12 +1180,61 @@ extern "C" size_t i8q_dq_lstm_workspace_size(int64_t T, int64_t batch, int64_t i
 
 namespace {
 
+// The activations attribute (3 per direction: f, g, h; or none, for
+// Sigmoid, Tanh, Tanh) with the activation_alpha / activation_beta lists,
+// which are consumed in the order of the functions: each function that
+// takes an alpha (beta) takes the next unused value, or its operator's
+// default once the list runs out.  Sets nondefault when any function
+// differs from the defaults.
+int resolve_activations(const int* kinds, size_t n_kinds, const float* alpha, size_t n_alpha, const float* beta,
+                        size_t n_beta, int64_t D, LstmActs& out, bool& nondefault) {
+  struct Def {
+    bool has_a;
+    float a;
+    bool has_b;
+    float b;
+  };
+  // indexed by I8Q_LSTM_ACT_*: the ONNX operators' defaults (LeakyRelu
+  // 0.01 as the DynamicQuantizeLSTM pages state); ScaledTanh's operator
+  // names none, and 1, 1 make it Tanh
+  static const Def defs[11] = {{false, 0, false, 0}, {false, 0, false, 0}, {false, 0, false, 0},
+                               {true, 1.0f, true, 0.0f},  {true, 0.01f, false, 0}, {true, 1.0f, false, 0},
+                               {true, 1.0f, true, 1.0f},  {true, 0.2f, true, 0.5f}, {true, 1.0f, false, 0},
+                               {false, 0, false, 0},      {false, 0, false, 0}};
+  static const int dflt[3] = {I8Q_LSTM_ACT_SIGMOID, I8Q_LSTM_ACT_TANH, I8Q_LSTM_ACT_TANH};
+  nondefault = false;
+  if (n_kinds != 0 && (int64_t)n_kinds != 3 * D)
+    return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: activations needs 3 entries per direction (or none)");
+  if (n_kinds && !kinds) return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: activations is NULL");
+  if ((n_alpha && !alpha) || (n_beta && !beta)) return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: alpha / beta list is NULL");
+  size_t ia = 0, ib = 0;
+  for (int d = 0; d < 2; ++d)
+    for (int k = 0; k < 3; ++k) {
+      out.kind[d][k] = dflt[k];
+      out.alpha[d][k] = out.beta[d][k] = 0.0f;
+    }
+  for (int64_t d = 0; d < D; ++d)
+    for (int k = 0; k < 3; ++k) {
+      const int kind = n_kinds ? kinds[3 * d + k] : dflt[k];
+      if (kind < I8Q_LSTM_ACT_RELU || kind > I8Q_LSTM_ACT_SOFTPLUS)
+        return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: unknown activation " + std::to_string(kind));
+      const Def& df = defs[kind];
+      out.kind[d][k] = kind;
+      if (df.has_a) out.alpha[d][k] = ia < n_alpha ? alpha[ia++] : df.a;
+      if (df.has_b) out.beta[d][k] = ib < n_beta ? beta[ib++] : df.b;
+      if (!(out.alpha[d][k] == out.alpha[d][k]) || !(out.beta[d][k] == out.beta[d][k]))
+        return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: activation alpha / beta is NaN");
+      if (kind != dflt[k]) nondefault = true;
+    }
+  return I8Q_OK;
+}
+
 int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, int64_t hidden, int direction,
                       const void* W_, const void* R_, int wtype, const float* W_scale, const void* W_zero_point_,
                       size_t n_wscale, const float* R_scale, const void* R_zero_point_, size_t n_rscale,
                       const float* Bias, const int32_t* seq_lens, const float* h0, const float* c0, const float* P,
-                      float clip, int input_forget, float* Y, float* Y_h, float* Y_c, void* workspace,
-                      size_t ws_bytes, void* stream) {
+                      float clip, int input_forget, const LstmActs& acts, bool acts_nondefault, float* Y, float* Y_h,
+                      float* Y_c, void* workspace, size_t ws_bytes, void* stream) {
   const int8_t* W = static_cast<const int8_t*>(W_);
   const int8_t* R = static_cast<const int8_t*>(R_);
   const int8_t* W_zero_point = static_cast<const int8_t*>(W_zero_point_);
@@ -1181,7 +1280,7 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
   uint32_t* gbar = (uint32_t*)(ws + L.off_gbar);
   float* hbuf = (float*)(ws + L.off_h);
   float* cbuf = (float*)(ws + L.off_c);
-  const int64_t H = hidden, BH = batch * hidden, DBH = L.D * BH;
+  const int64_t H = hidden, BH = batch * hidden, DBH = L.D * BH, DB = L.D * batch;
 
   // The general form (uint8 weights, zero points, sequence lengths,
   // peepholes, clip, coupled gates) runs on the tensor-core kernels: the
@@ -1189,7 +1288,7 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
   // 2^15 and the exact fp32 chunks hold 512 K-elements.  int8 weights whose
   // given zero points are all 0 (checked on the device, reported
   // synchronously) keep the plain form.
-  bool var = wtype != I8Q_S8 || seq_lens || P || clip > 0.0f || input_forget;
+  bool var = wtype != I8Q_S8 || seq_lens || P || clip > 0.0f || input_forget || acts_nondefault;
   if (!var && (W_zero_point || R_zero_point)) {
     int* flag = reinterpret_cast<int*>(sh);  // scratch word, overwritten later
     I8Q_CUDA_TRY(cudaMemsetAsync(flag, 0, sizeof(int), s));
@@ -1262,18 +1361,11 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
   if (step_tc) {
     rc = tc::make_map_2d(&mR, Rtb, L.D * L.H4, L.Hp, tcs::BM, "dq_lstm");
     if (rc) return rc;
-    rc = tc::make_map_2d(&mH, uhc, L.D * batch, L.Hp, tcs::BN, "dq_lstm");
+    rc = tc::make_map_2d(&mH, uhc, 2 * L.D * batch, L.Hp, tcs::BN, "dq_lstm");
     if (rc) return rc;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-      attr_err = cudaFuncSetAttribute(tcs::lstm_step_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      tcs::SMEM_BYTES);
-      if (attr_err == cudaSuccess)
-        attr_err = cudaFuncSetAttribute(tcs::lstm_step_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        tcs::SMEM_BYTES);
-    });
-    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(lstm_step_tc_kernel)");
+    rc = smem_attr((const void*)tcs::lstm_step_tc_kernel<false>, tcs::SMEM_BYTES);
+    if (!rc) rc = smem_attr((const void*)tcs::lstm_step_tc_kernel<true>, tcs::SMEM_BYTES);
+    if (rc) return rc;
   }
 
   // the persistent recurrence: every CTA resident at once (one per SM),
@@ -1284,22 +1376,13 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
   const size_t psmem = prs::smem_bytes(L.Hp);
   if (step_tc && batch <= 64 && H % 16 == 0 && (reinterpret_cast<uintptr_t>(Y) & 15) == 0 &&
       !getenv("I8Q_LSTM_STEPS")) {
-    static std::once_flag pattr_once;
-    static cudaError_t pattr_err = cudaSuccess;
-    static int coop = 0;
-    std::call_once(pattr_once, [] {
-      int dev = 0;
-      pattr_err = cudaGetDevice(&dev);
-      if (pattr_err == cudaSuccess) pattr_err = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-      const int most = 227 * 1024 - 4096;
-      if (pattr_err == cudaSuccess)
-        pattr_err = cudaFuncSetAttribute(prs::lstm_persist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         most);
-      if (pattr_err == cudaSuccess)
-        pattr_err = cudaFuncSetAttribute(prs::lstm_persist_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         most);
-    });
-    if (pattr_err != cudaSuccess) return cuda_fail(pattr_err, "lstm persistent kernel attributes");
+    int dev = 0, coop = 0;
+    I8Q_CUDA_TRY(cudaGetDevice(&dev));
+    I8Q_CUDA_TRY(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev));
+    const int most = 227 * 1024 - 4096;
+    rc = smem_attr((const void*)prs::lstm_persist_kernel<false>, most);
+    if (!rc) rc = smem_attr((const void*)prs::lstm_persist_kernel<true>, most);
+    if (rc) return rc;
     int per_sm = 0;
     if (coop && psmem <= (size_t)(227 * 1024 - 4096)) {
       I8Q_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
@@ -1326,8 +1409,8 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
       I8Q_CUDA_TRY(cudaMemsetAsync(uhc, 0, (size_t)2 * L.D * batch * L.Hp * 2, s));
       I8Q_CUDA_TRY(cudaMemsetAsync(mmb, 0, (size_t)2 * L.D * batch * 2 * 4, s));
       I8Q_CUDA_TRY(cudaMemsetAsync(gbar, 0, 2 * 4, s));
-      int rcp = launch_quantize_rows(hbuf, I8Q_F32, L.D * batch, H, H, uh, uhc + L.D * batch * L.Hp, L.Hp,
-                                     sh + L.D * batch, zh + L.D * batch, s);
+      int rcp = launch_quantize_rows(hbuf, I8Q_F32, DB, H, H, uh + DB * L.Hp, uhc + DB * L.Hp, L.Hp, sh + DB,
+                                     zh + DB, s);
       if (rcp) return rcp;
       prs::Params pp;
       pp.Rcs = Rcs;
@@ -1356,6 +1439,7 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
       pp.P = P;
       pp.clip = clip;
       pp.input_forget = input_forget ? 1 : 0;
+      pp.acts = acts;
       if (!pp.status) return fail(I8Q_ERR_CUDA, "dq_lstm: no device status word");
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)(L.D * ptiles));
@@ -1379,7 +1463,10 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
       I8Q_LAUNCH_CHECK("copy_f32");
       return I8Q_OK;
     }
-    int rc2 = launch_quantize_rows(hbuf, I8Q_F32, L.D * batch, H, H, uh, step_tc ? uhc : nullptr, L.Hp, sh, zh, s);
+    // step s reads the codes of parity (s + 1) & 1 and writes those of its
+    // new h to parity s & 1 (every step, the last included, so that the
+    // workspace ends with the codes of the final state); h0's go to parity 1
+    int rc2 = launch_quantize_rows(hbuf, I8Q_F32, DB, H, H, uh + DB * L.Hp, uhc + DB * L.Hp, L.Hp, sh + DB, zh + DB, s);
     if (rc2) return rc2;
     StepParams sp;
     sp.uh = uh;
@@ -1422,15 +1509,23 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
     tp.P = P;
     tp.clip = clip;
     tp.input_forget = input_forget ? 1 : 0;
+    tp.acts = acts;
     tp.status = device_status_word();
     if (step_tc && !tp.status) return fail(I8Q_ERR_CUDA, "dq_lstm: no device status word");
     for (int64_t step = 0; step < T; ++step) {
       float* h_next = hbuf + ((step + 1) & 1) * DBH;
+      const int64_t pin = (step + 1) & 1, pout = step & 1;
       sp.step = (int)step;
       sp.h_next = h_next;
+      sp.uh = uh + pin * DB * L.Hp;
+      sp.sh = sh + pin * DB;
+      sp.zh = zh + pin * DB;
       if (step_tc) {
         I8Q_PROF("lstm_step_tc", s);
         tp.step = (int)step;
+        tp.sh = sh + pin * DB;
+        tp.zh = zh + pin * DB;
+        tp.hrow0 = (int)(pin * DB);
         tp.h_next = h_next;
         tp.h_prev = hbuf + (step & 1) * DBH;
         if (var)
@@ -1443,10 +1538,9 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
         lstm_step_kernel<<<sgrid, STHREADS, 0, s>>>(sp);
         I8Q_LAUNCH_CHECK("lstm_step_kernel");
       }
-      if (step + 1 < T) {
-        rc2 = launch_quantize_rows(h_next, I8Q_F32, L.D * batch, H, H, uh, step_tc ? uhc : nullptr, L.Hp, sh, zh, s);
-        if (rc2) return rc2;
-      }
+      rc2 = launch_quantize_rows(h_next, I8Q_F32, DB, H, H, uh + pout * DB * L.Hp, uhc + pout * DB * L.Hp, L.Hp,
+                                 sh + pout * DB, zh + pout * DB, s);
+      if (rc2) return rc2;
     }
     const float* h_last = hbuf + (T & 1) * DBH;
     if (Y_h) copy_f32<<<grid_for(DBH), 256, 0, s>>>(h_last, Y_h, DBH);
@@ -1466,9 +1560,17 @@ int lstm_forward_impl(const float* X, int64_t T, int64_t batch, int64_t input, i
     return recurrence();
   int64_t clip_bits = 0;
   std::memcpy(&clip_bits, &clip, sizeof(float));
-  const LstmGraphKey key{X, W, R, W_scale, R_scale, Bias, h0, c0, Y, Y_h, Y_c, workspace, W_zero_point, R_zero_point,
-                         seq_lens, P, T, batch, input, hidden, direction, (int64_t)n_wscale, (int64_t)n_rscale,
-                         (int64_t)wtype, (int64_t)(input_forget ? 1 : 0), clip_bits};
+  LstmGraphKey key{X, W, R, W_scale, R_scale, Bias, h0, c0, Y, Y_h, Y_c, workspace, W_zero_point, R_zero_point,
+                   seq_lens, P, T, batch, input, hidden, direction, (int64_t)n_wscale, (int64_t)n_rscale,
+                   (int64_t)wtype, (int64_t)(input_forget ? 1 : 0), clip_bits, 0, {0, 0, 0, 0, 0, 0}};
+  for (int d = 0; d < 2; ++d)
+    for (int k = 0; k < 3; ++k) {
+      uint32_t a = 0, b = 0;
+      std::memcpy(&a, &acts.alpha[d][k], 4);
+      std::memcpy(&b, &acts.beta[d][k], 4);
+      key.act_kinds |= (int64_t)acts.kind[d][k] << (4 * (3 * d + k));
+      key.act_params[3 * d + k] = (int64_t)(((uint64_t)a << 32) | b);
+    }
   return run_cached_graph(key, s, recurrence);
 }
 
@@ -1480,9 +1582,14 @@ extern "C" int i8q_dq_lstm_forward(const float* X, int64_t T, int64_t batch, int
                                    const int8_t* R_zero_point, size_t n_rscale, const float* Bias, const float* h0,
                                    const float* c0, float* Y, float* Y_h, float* Y_c, void* workspace,
                                    size_t ws_bytes, void* stream) {
+  LstmActs acts;
+  bool nondefault = false;
+  const int64_t D = direction == I8Q_LSTM_BIDIRECTIONAL ? 2 : 1;
+  int rc = resolve_activations(nullptr, 0, nullptr, 0, nullptr, 0, D, acts, nondefault);
+  if (rc) return rc;
   return lstm_forward_impl(X, T, batch, input, hidden, direction, W, R, I8Q_S8, W_scale, W_zero_point, n_wscale,
-                           R_scale, R_zero_point, n_rscale, Bias, nullptr, h0, c0, nullptr, 0.0f, 0, Y, Y_h, Y_c,
-                           workspace, ws_bytes, stream);
+                           R_scale, R_zero_point, n_rscale, Bias, nullptr, h0, c0, nullptr, 0.0f, 0, acts, false, Y,
+                           Y_h, Y_c, workspace, ws_bytes, stream);
 }
 
 extern "C" int i8q_dq_lstm_forward_ex(const float* X, int64_t T, int64_t batch, int64_t input, int64_t hidden,
@@ -1490,11 +1597,52 @@ extern "C" int i8q_dq_lstm_forward_ex(const float* X, int64_t T, int64_t batch, 
                                       const void* W_zero_point, size_t n_wscale, const float* R_scale,
                                       const void* R_zero_point, size_t n_rscale, const float* Bias,
                                       const int32_t* sequence_lens, const float* h0, const float* c0, const float* P,
-                                      float clip, int input_forget, float* Y, float* Y_h, float* Y_c,
-                                      void* workspace, size_t ws_bytes, void* stream) {
+                                      float clip, int input_forget, const int* activations, size_t n_activations,
+                                      const float* activation_alpha, size_t n_alpha, const float* activation_beta,
+                                      size_t n_beta, float* Y, float* Y_h, float* Y_c, void* workspace,
+                                      size_t ws_bytes, void* stream) {
+  if (direction < I8Q_LSTM_FORWARD || direction > I8Q_LSTM_BIDIRECTIONAL)
+    return fail(I8Q_ERR_INVALID_ARG, "dq_lstm: bad direction");
+  LstmActs acts;
+  bool nondefault = false;
+  const int64_t D = direction == I8Q_LSTM_BIDIRECTIONAL ? 2 : 1;
+  int rc = resolve_activations(activations, n_activations, activation_alpha, n_alpha, activation_beta, n_beta, D,
+                               acts, nondefault);
+  if (rc) return rc;
   return lstm_forward_impl(X, T, batch, input, hidden, direction, W, R, wtype, W_scale, W_zero_point, n_wscale,
-                           R_scale, R_zero_point, n_rscale, Bias, sequence_lens, h0, c0, P, clip, input_forget, Y,
-                           Y_h, Y_c, workspace, ws_bytes, stream);
+                           R_scale, R_zero_point, n_rscale, Bias, sequence_lens, h0, c0, P, clip, input_forget, acts,
+                           nondefault, Y, Y_h, Y_c, workspace, ws_bytes, stream);
+}
+
+extern "C" int i8q_debug_wait_timeout(int kind, int64_t limit_ns, void* stream) {
+  if (kind != 0 && kind != 1) return fail(I8Q_ERR_INVALID_ARG, "debug_wait_timeout: kind must be 0 or 1");
+  if (limit_ns < 1000 || limit_ns > 1000000000)
+    return fail(I8Q_ERR_INVALID_ARG, "debug_wait_timeout: limit must be within [1 us, 1 s]");
+  uint32_t* status = device_status_word();
+  if (!status) return fail(I8Q_ERR_CUDA, "debug_wait_timeout: no device status word");
+  prs::wait_probe_kernel<<<1, 32, 0, as_stream(stream)>>>(kind, (unsigned long long)limit_ns, status);
+  I8Q_LAUNCH_CHECK("wait_probe_kernel");
+  return I8Q_OK;
+}
+
+extern "C" int i8q_dq_lstm_state_codes(const void* workspace, int64_t T, int64_t batch, int64_t input,
+                                       int64_t hidden, int direction, int which, const void** codes,
+                                       const float** scale, const int32_t** zero, int64_t* row_stride) {
+  if (!workspace || !codes || !scale || !zero || !row_stride)
+    return fail(I8Q_ERR_INVALID_ARG, "dq_lstm_state_codes: NULL argument");
+  if (T <= 0 || batch <= 0 || input <= 0 || hidden <= 0 || direction < I8Q_LSTM_FORWARD ||
+      direction > I8Q_LSTM_BIDIRECTIONAL)
+    return fail(I8Q_ERR_INVALID_ARG, "dq_lstm_state_codes: bad shape or direction");
+  if (which != 0 && which != 1) return fail(I8Q_ERR_INVALID_ARG, "dq_lstm_state_codes: which must be 0 or 1");
+  const LstmLayout L = lstm_layout(T, batch, input, hidden, direction);
+  const int64_t DB = L.D * batch;
+  const int64_t par = which == 0 ? (T & 1) : ((T - 1) & 1);
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  *codes = ws + L.off_uhc + (size_t)par * DB * L.Hp * 2;
+  *scale = reinterpret_cast<const float*>(ws + L.off_sh) + par * DB;
+  *zero = reinterpret_cast<const int32_t*>(ws + L.off_zh) + par * DB;
+  *row_stride = L.Hp;
+  return I8Q_OK;
 }
 
 namespace i8q {

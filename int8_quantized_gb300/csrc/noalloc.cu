@@ -97,7 +97,12 @@ extern "C" int i8q_qgemm_dyn_static(size_t M, size_t N, size_t K, int typeA, con
   if (rc) return rc;
   GemmEpilogue ep{zeroA, scaleA, colsum, scaleB, bias, activation, typeC == I8Q_BF16 ? OUT_BF16 : OUT_F32, C,
                   (int64_t)N};
-  if (Kp <= small_max_kp())
+  // the same rule as a context's choice: small products (Kp <= 8192 and
+  // at most 2^27 multiply-adds) on the fused dp4a kernel, larger ones on the
+  // row kernel and the int8 mma.sync core (the tensor-pipe path would need
+  // bf16 copies of both operands, twice the scratch)
+  const double macs = (double)M * (double)N * (double)Kp;
+  if (Kp <= small_max_kp() && macs <= (double)(1 << 27))
     return launch_gemm_small(A, typeA, (int64_t)M, (int64_t)K, Kp, iBt, (int64_t)N, uA, scaleA, zeroA, ep, s);
   rc = launch_quantize_rows(A, typeA, (int64_t)M, (int64_t)K, (int64_t)K, uA, nullptr, Kp, scaleA, zeroA, s);
   if (rc) return rc;

@@ -241,7 +241,7 @@ __device__ __forceinline__ uint32_t unary_code(int code_index, int op, float x_s
   if (op == 0)
     f = d < 0.0f ? __fmul_rn(alpha, d) : d;
   else
-    f = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-d)));
+    f = ef::sigmoid32(d);
   return rint_code_bits(__fdiv_rn(f, y_scale), lo_z, hi_z, y_zp) & 0xffu;
 }
 
@@ -438,14 +438,9 @@ int run_binary(const uint8_t* A, const uint8_t* B, const Strides& st, int64_t n,
       ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 15) == 0;
   int64_t done = 0;
   if (am >= 0 && bm >= 0 && aligned && p.op != 2 && n >= ((int64_t)1 << 20) && !getenv("I8Q_QEW_NO_TABLE")) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-      attr = cudaFuncSetAttribute(binary_table<AS, BS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTabBytes);
-      if (attr == cudaSuccess)
-        attr = cudaFuncSetAttribute(binary_table<AS, BS, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTabBytes);
-    });
-    I8Q_CUDA_TRY(attr);
+    int ar = smem_attr((const void*)binary_table<AS, BS, true>, kTabBytes);
+    if (!ar) ar = smem_attr((const void*)binary_table<AS, BS, false>, kTabBytes);
+    if (ar) return ar;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), ceil_div(n / 16, (int64_t)kTabThreads)));
     const uint32_t* gtab = nullptr;
     if (!getenv("I8Q_QEW_NO_TABLE_CACHE")) {

@@ -813,12 +813,8 @@ col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int
 template <typename T>
 int launch_col_quant_tma(const T* B, int64_t K, int64_t N, int64_t Kp, int qmin, int qmax, int8_t* iBt,
                          __nv_bfloat16* iBt_bf16, float* scaleB, int32_t* colsum, uint32_t* status, cudaStream_t s) {
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(col_quant_tma<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCqSmem);
-  });
-  I8Q_CUDA_TRY(attr);
+  const int ar = smem_attr((const void*)col_quant_tma<T>, (int)kCqSmem);
+  if (ar) return ar;
   constexpr int W = 128 / (int)sizeof(T);
   CUtensorMap map;
   const int rc = tc::make_map_plain_2d(&map, B,
@@ -854,15 +850,9 @@ int launch_quantize_rows(const void* A, int typeA, int64_t M, int64_t K, int64_t
     // worth it once the row groups fill the GPU; fewer rows keep the
     // register form (lower latency per launch)
     if (aligned && status && K > 2048 && smem <= 200 * 1024 && groups >= sm_count() && !getenv("I8Q_ROWS_REGISTER")) {
-      static std::once_flag once;
-      static cudaError_t attr = cudaSuccess;
-      std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(quantize_rows_staged<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024 + 64);
-        if (attr == cudaSuccess)
-          attr = cudaFuncSetAttribute(quantize_rows_staged<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      200 * 1024 + 64);
-      });
-      I8Q_CUDA_TRY(attr);
+      int ar = smem_attr((const void*)quantize_rows_staged<float>, 200 * 1024 + 64);
+      if (!ar) ar = smem_attr((const void*)quantize_rows_staged<__nv_bfloat16>, 200 * 1024 + 64);
+      if (ar) return ar;
       const void* kern = bf ? (const void*)quantize_rows_staged<__nv_bfloat16> : (const void*)quantize_rows_staged<float>;
       // one wave of the blocks that fit at once (shared memory and threads)
       int per_sm = 0;

@@ -55,10 +55,11 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Bounded wait: true when the phase completed; false on timeout (recorded)
-// or when another role already gave up.
+// or when another role already gave up.  limit_ns is WAIT_LIMIT_NS except
+// in the failure-detection probe, which shortens it.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* status,
-                                         uint32_t code) {
+                                         uint32_t code, unsigned long long limit_ns = WAIT_LIMIT_NS) {
   unsigned long long t0 = 0;
   for (uint32_t i = 0;; ++i) {
     if (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
@@ -67,7 +68,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
       unsigned long long now = global_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > WAIT_LIMIT_NS) {
+      } else if (now - t0 > limit_ns) {
         atomicOr(status, code);
         *abort_flag = 1;
         return false;

@@ -123,6 +123,56 @@ def test_lstm_validation(lib):
     assert rc == _lib.ERR_INVALID_ARG and b"workspace" in lib.i8q_last_error()
 
 
+def test_lstm_activation_validation(lib):
+    """The activations attribute is checked on the host before anything
+    runs: 3 entries per direction (or none), each one of the ONNX list."""
+    from int8_quantized_gb300 import _lib
+    p = ctypes.c_void_p(256)
+
+    def ex(kinds, n):
+        arr = (ctypes.c_int * max(1, len(kinds)))(*kinds)
+        return lib.i8q_dq_lstm_forward_ex(p, 2, 3, 8, 4, 0, p, p, _lib.S8, p, None, 1, p, None, 1, None, None, None,
+                                          None, None, 0.0, 0, arr, n, None, 0, None, 0, None, None, None, p,
+                                          1 << 20, None)
+    assert ex([2, 1], 2) == _lib.ERR_INVALID_ARG and b"3 entries" in lib.i8q_last_error()
+    assert ex([2, 1, 11], 3) == _lib.ERR_INVALID_ARG and b"unknown activation" in lib.i8q_last_error()
+    assert ex([2, 1, -1], 3) == _lib.ERR_INVALID_ARG
+
+
+def test_lstm_state_codes_layout(lib):
+    """The hook only computes addresses inside the workspace: the two
+    parities are one block of D * batch code rows apart, and which = 0 / 1
+    swap with the parity of T (step s reads parity (s + 1) % 2 and writes
+    parity s % 2)."""
+    from int8_quantized_gb300 import _lib
+    ws = 1 << 20
+    out = [ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_int64()]
+
+    def codes(T, which):
+        rc = lib.i8q_dq_lstm_state_codes(ctypes.c_void_p(ws), T, 3, 8, 40, _lib.LSTM_BIDIRECTIONAL, which,
+                                         *[ctypes.byref(o) for o in out])
+        assert rc == 0
+        return out[0].value, out[1].value, out[3].value
+    c0, s0, stride = codes(4, 0)
+    c1, s1, _ = codes(4, 1)
+    assert stride == 64 and abs(c1 - c0) == 2 * 3 * 64 * 2 and abs(s1 - s0) == 2 * 3 * 4
+    assert c1 - c0 == 2 * 3 * 64 * 2                   # T even: the last step read parity 0, wrote parity 1
+    d0, _, _ = codes(5, 0)
+    d1, _, _ = codes(5, 1)
+    assert d0 - d1 == 2 * 3 * 64 * 2                   # T odd: the other way round
+    assert ws < min(c0, c1) < ws + lib.i8q_dq_lstm_workspace_size(4, 3, 8, 40, _lib.LSTM_BIDIRECTIONAL)
+    assert lib.i8q_dq_lstm_state_codes(None, 4, 3, 8, 40, 2, 0, *[ctypes.byref(o) for o in out]) == \
+        _lib.ERR_INVALID_ARG
+    assert lib.i8q_dq_lstm_state_codes(ctypes.c_void_p(ws), 4, 3, 8, 40, 2, 2, *[ctypes.byref(o) for o in out]) == \
+        _lib.ERR_INVALID_ARG
+
+
+def test_wait_probe_validation(lib):
+    from int8_quantized_gb300 import _lib
+    assert lib.i8q_debug_wait_timeout(2, 3_000_000, None) == _lib.ERR_INVALID_ARG
+    assert lib.i8q_debug_wait_timeout(0, 10, None) == _lib.ERR_INVALID_ARG
+
+
 def test_qgemm_validation(lib):
     from int8_quantized_gb300 import _lib
     p = ctypes.c_void_p(256)

@@ -1,13 +1,13 @@
-"""DynamicQuantizeLSTM on the GPU vs the CPU oracle.
+"""DynamicQuantizeLSTM on the GPU vs the CPU oracle, bit for bit.
 
-The gates use the platform's expf/tanhf on each side, which may differ by an
-fp32 ulp; over many steps such differences can move a uint8 code of the
-next hidden state.  So parity is checked (1) step-locally: one step from a
-given (h, c) state, where the quantized codes, and so the int32 products,
-are the same on both sides and the outputs agree to within a few fp32 ulps,
-and (2) over short whole sequences within a small tolerance.  At the full
-size, sampled steps are checked step-locally: a GPU run over the first t
-inputs gives the state (h, c) that step t starts from.
+Both sides evaluate sigmoid and tanh as the same fixed sequence of fp32
+operations, so every step computes the same bits: the hidden and cell
+states, and the uint8 codes, scales and zero points of the hidden state that
+the next step's product reads (read back from the workspace through the
+i8q_dq_lstm_state_codes hook).  Checked step-locally from a given (h, c),
+over whole sequences, and at the full size: sampled steps of the 512-step
+run from their GPU states, the codes of the state each sampled step read,
+and a whole 32-step sequence at the full width.
 """
 import numpy as np
 import pytest
@@ -37,7 +37,7 @@ def _t(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
 
-def gpu_lstm(dev, w, direction, X=None, h0=None, c0=None, per_channel=True):
+def gpu_lstm(dev, w, direction, X=None, h0=None, c0=None, per_channel=True, codes=False):
     X = w["X"] if X is None else X
     T, batch, I = X.shape
     D = 2 if direction == "bidirectional" else 1
@@ -56,7 +56,23 @@ def gpu_lstm(dev, w, direction, X=None, h0=None, c0=None, per_channel=True):
                       Y=Y, Y_h=Yh, Y_c=Yc, W_zero_point=_t(np.zeros(Ws.size, np.int8), dev),
                       R_zero_point=_t(np.zeros(Rs.size, np.int8), dev))
     q.sync_status()
-    return Y.cpu().numpy(), Yh.cpu().numpy(), Yc.cpu().numpy()
+    out = (Y.cpu().numpy(), Yh.cpu().numpy(), Yc.cpu().numpy())
+    if codes:
+        # codes of the state the last step read, and of the final state
+        out += tuple(tuple(a.cpu().numpy() for a in q.dq_lstm_state_codes(ws, T, batch, I, H, DIRS[direction], k))
+                     for k in (0, 1))
+    return out
+
+
+def assert_codes(orc, got, h, d, batch):
+    """The GPU's codes, scale and zero point of direction d's rows equal the
+    oracle's per-row quantization of h."""
+    uh, sh, zh = got
+    rows = slice(d * batch, (d + 1) * batch)
+    u, s, z = orc.quantize_rows_u8(h)
+    assert np.array_equal(uh[rows], u.astype(np.int32))
+    assert np.array_equal(sh[rows], s)
+    assert np.array_equal(zh[rows], z)
 
 
 def oracle_step(orc, w, d, X_t, h, c):
@@ -73,13 +89,15 @@ def test_single_step_from_given_state(orc, dev, direction):
     D = 2 if direction == "bidirectional" else 1
     h0 = rng.uniform(-0.9, 0.9, (D, 5, 40)).astype(np.float32)
     c0 = rng.normal(0, 1, (D, 5, 40)).astype(np.float32)
-    Y, Yh, Yc = gpu_lstm(dev, w, direction, h0=h0, c0=c0)
+    Y, Yh, Yc, c_in, c_out = gpu_lstm(dev, w, direction, h0=h0, c0=c0, codes=True)
     for d in range(D):
         widx = 1 if direction == "reverse" else d
+        assert_codes(orc, c_in, h0[d], d, 5)
         h, c = oracle_step(orc, w, widx, w["X"][0], h0[d], c0[d])
-        np.testing.assert_allclose(Y[0, d], h, rtol=1e-5, atol=1e-6)
-        np.testing.assert_allclose(Yc[d], c, rtol=1e-5, atol=1e-6)
+        assert np.array_equal(Y[0, d], h)
+        assert np.array_equal(Yc[d], c)
         assert np.array_equal(Yh[d], Y[0, d])
+        assert_codes(orc, c_out, h, d, 5)
 
 
 @pytest.mark.parametrize("direction", ["forward", "reverse", "bidirectional"])
@@ -90,13 +108,17 @@ def test_short_sequence(orc, dev, direction, per_channel):
         w["W_scale"][:] = w["W_scale"][:, :1]
         w["R_scale"][:] = w["R_scale"][:, :1]
     D = 2 if direction == "bidirectional" else 1
-    Y, Yh, Yc = gpu_lstm(dev, w, direction, per_channel=per_channel)
+    Y, Yh, Yc, c_in, c_out = gpu_lstm(dev, w, direction, per_channel=per_channel, codes=True)
     sl = slice(0, D) if direction != "reverse" else slice(1, 2)
     ref = orc.dynamic_quantize_lstm(w["X"], w["W"][sl], w["R"][sl], w["B"][sl], w["W_scale"][sl], w["R_scale"][sl],
                                     direction=direction)
-    np.testing.assert_allclose(Y, ref[0], rtol=1e-4, atol=1e-5)
-    np.testing.assert_allclose(Yh, ref[1], rtol=1e-4, atol=1e-5)
-    np.testing.assert_allclose(Yc, ref[2], rtol=1e-4, atol=1e-5)
+    assert np.array_equal(Y, ref[0])
+    assert np.array_equal(Yh, ref[1])
+    assert np.array_equal(Yc, ref[2])
+    for d in range(D):
+        rev = direction == "reverse" or d == 1
+        assert_codes(orc, c_in, Y[1 if rev else 5, d], d, 3)   # the state the last step read
+        assert_codes(orc, c_out, Yh[d], d, 3)
 
 
 def test_nonzero_zero_point(orc, dev):
@@ -114,12 +136,27 @@ def test_nonzero_zero_point(orc, dev):
     q.sync_status()
     ref = orc.dynamic_quantize_lstm(w["X"], w["W"], w["R"], w["B"], w["W_scale"], w["R_scale"],
                                     W_zero_point=zp.astype(np.int32), R_zero_point=zp.astype(np.int32))
-    np.testing.assert_allclose(Y.cpu().numpy(), ref[0], rtol=1e-4, atol=1e-5)
+    assert np.array_equal(Y.cpu().numpy(), ref[0])
+
+
+def test_full_width_whole_sequence(orc, dev):
+    """T=32 of the full-size layer (batch 64, I = H = 1024, bidirectional):
+    every output of the whole sequence, bit for bit."""
+    w = workloads.lstm(seed=4, T=32)
+    Y, Yh, Yc, _, c_out = gpu_lstm(dev, w, "bidirectional", codes=True)
+    ref = orc.dynamic_quantize_lstm(w["X"], w["W"], w["R"], w["B"], w["W_scale"], w["R_scale"],
+                                    direction="bidirectional")
+    assert np.array_equal(Y, ref[0])
+    assert np.array_equal(Yh, ref[1]) and np.array_equal(Yc, ref[2])
+    for d in range(2):
+        assert_codes(orc, c_out, Yh[d], d, 64)
 
 
 def test_full_size_sampled_steps(orc, dev):
     """T=512 batch=64 I=H=1024 bidirectional.  For sampled steps, the state
-    the step starts from comes from a GPU run over the preceding inputs."""
+    the step starts from comes from the GPU: h from the whole run's Y, c
+    (and the codes of h that the step read) from a GPU run over the
+    preceding inputs."""
     w = workloads.lstm(seed=4)
     Y, Yh, Yc = gpu_lstm(dev, w, "bidirectional")
     assert np.all(np.isfinite(Y)) and np.abs(Y).max() < 1.0
@@ -130,17 +167,21 @@ def test_full_size_sampled_steps(orc, dev):
             h = np.zeros((64, 1024), np.float32)
             c = np.zeros((64, 1024), np.float32)
         else:
-            _, h, c = gpu_lstm(dev, w, "forward", X=w["X"][:t])
-            h, c = h[0], c[0]
+            _, hp, cp, _, c_out = gpu_lstm(dev, w, "forward", X=w["X"][:t], codes=True)
+            h, c = hp[0], cp[0]
+            assert np.array_equal(h, Y[t - 1, 0])
+            assert_codes(orc, c_out, h, 0, 64)
         hf, _ = oracle_step(orc, w, 0, w["X"][t], h, c)
-        np.testing.assert_allclose(Y[t, 0], hf, rtol=1e-5, atol=2e-6)
+        assert np.array_equal(Y[t, 0], hf)
     for t in (511, 300):
         # reverse direction: state after steps T-1..t+1
         if t == T - 1:
             h = np.zeros((64, 1024), np.float32)
             c = np.zeros((64, 1024), np.float32)
         else:
-            _, h, c = gpu_lstm(dev, w, "reverse", X=w["X"][t + 1:])
-            h, c = h[0], c[0]
+            _, hp, cp, _, c_out = gpu_lstm(dev, w, "reverse", X=w["X"][t + 1:], codes=True)
+            h, c = hp[0], cp[0]
+            assert np.array_equal(h, Y[t + 1, 1])
+            assert_codes(orc, c_out, h, 0, 64)
         hr, _ = oracle_step(orc, w, 1, w["X"][t], h, c)
-        np.testing.assert_allclose(Y[t, 1], hr, rtol=1e-5, atol=2e-6)
+        assert np.array_equal(Y[t, 1], hr)

@@ -1,10 +1,10 @@
 """DynamicQuantizeLSTM with its optional inputs and attributes on the GPU vs
-the CPU oracle: sequence_lens, peepholes, clip, input_forget, uint8 weights
-and nonzero W/R zero points (per direction and per channel).
+the CPU oracle: sequence_lens, peepholes, clip, input_forget, uint8 weights,
+nonzero W/R zero points (per direction and per channel), and the ONNX
+activation functions with their alpha / beta lists.
 
-As for the plain LSTM, the gates use each platform's expf/tanhf, which may
-differ by an fp32 ulp, so sequences are compared within a small tolerance
-and a single step from a given state within a few ulps.
+Both sides evaluate the activations as the same fixed sequences of fp32
+operations, so every output is compared bit for bit.
 """
 import numpy as np
 import pytest
@@ -55,7 +55,8 @@ def weights(seed, T, batch, I, H, direction, wtype="s8", zp="none"):
     return dict(X=w["X"], W=W, R=R, B=w["B"][sel], Ws=Ws, Rs=Rs, Wz=Wz, Rz=Rz, D=D, H=H)
 
 
-def run_gpu(dev, p, direction, seq=None, P=None, clip=0.0, coupled=False, h0=None, c0=None):
+def run_gpu(dev, p, direction, seq=None, P=None, clip=0.0, coupled=False, h0=None, c0=None, acts=None, alpha=None,
+            beta=None):
     T, batch, I = p["X"].shape
     D, H = p["D"], p["H"]
     ws = torch.empty(q.dq_lstm_workspace_size(T, batch, I, H, DIRS[direction]), dtype=torch.uint8, device=dev)
@@ -66,12 +67,14 @@ def run_gpu(dev, p, direction, seq=None, P=None, clip=0.0, coupled=False, h0=Non
     q.dq_lstm_forward_ex(_t(p["X"], dev), _t(p["W"], dev), _t(p["R"], dev), _t(p["Ws"], dev), _t(p["Rs"], dev), ws,
                          direction=DIRS[direction], B=_t(p["B"], dev), sequence_lens=opt(seq, np.int32),
                          h0=opt(h0), c0=opt(c0), P=opt(P), clip=clip, input_forget=coupled, Y=Y, Y_h=Yh, Y_c=Yc,
-                         W_zero_point=opt(p["Wz"]), R_zero_point=opt(p["Rz"]))
+                         W_zero_point=opt(p["Wz"]), R_zero_point=opt(p["Rz"]), activations=acts,
+                         activation_alpha=alpha, activation_beta=beta)
     q.sync_status()
     return Y.cpu().numpy(), Yh.cpu().numpy(), Yc.cpu().numpy()
 
 
-def run_oracle(orc, p, direction, seq=None, P=None, clip=0.0, coupled=False, h0=None, c0=None):
+def run_oracle(orc, p, direction, seq=None, P=None, clip=0.0, coupled=False, h0=None, c0=None, acts=None, alpha=None,
+               beta=None):
     D, H = p["D"], p["H"]
     Ws = np.broadcast_to(p["Ws"], (D, 4 * H)).astype(np.float32)
     Rs = np.broadcast_to(p["Rs"], (D, 4 * H)).astype(np.float32)
@@ -79,12 +82,13 @@ def run_oracle(orc, p, direction, seq=None, P=None, clip=0.0, coupled=False, h0=
     Rz = None if p["Rz"] is None else np.broadcast_to(np.asarray(p["Rz"]).reshape(D, -1), (D, 4 * H)).astype(np.int32)
     return orc.dynamic_quantize_lstm(p["X"], p["W"], p["R"], p["B"], Ws, Rs, h0=h0, c0=c0, direction=direction,
                                      W_zero_point=Wz, R_zero_point=Rz, P=P, clip=clip, input_forget=coupled,
-                                     sequence_lens=seq)
+                                     sequence_lens=seq, activations=acts, activation_alpha=alpha,
+                                     activation_beta=beta)
 
 
-def compare(got, ref, rtol=1e-4, atol=1e-5):
+def compare(got, ref):
     for g, r in zip(got, ref):
-        np.testing.assert_allclose(g, r, rtol=rtol, atol=atol)
+        assert np.array_equal(g, r), float(np.abs(g.astype(np.float64) - r).max())
 
 
 FEATURES = {
@@ -121,14 +125,14 @@ def test_weight_types_and_zero_points(orc, dev, wtype, zp, direction):
 
 
 def test_single_step_from_given_state(orc, dev):
-    """One step with every feature from a given (h, c): a few fp32 ulps."""
+    """One step with every feature from a given (h, c)."""
     p = weights(43, 1, 6, 128, 48, "bidirectional", "u8", "chan")
     rng = np.random.default_rng(44)
     h0 = rng.uniform(-0.9, 0.9, (2, 6, 48)).astype(np.float32)
     c0 = rng.normal(0, 1, (2, 6, 48)).astype(np.float32)
     P = rng.normal(0, 0.5, (2, 144)).astype(np.float32)
     kw = dict(P=P, clip=1.5, coupled=True, h0=h0, c0=c0, seq=np.array([1, 1, 0, 1, 1, 0]))
-    compare(run_gpu(dev, p, "bidirectional", **kw), run_oracle(orc, p, "bidirectional", **kw), rtol=1e-5, atol=1e-6)
+    compare(run_gpu(dev, p, "bidirectional", **kw), run_oracle(orc, p, "bidirectional", **kw))
 
 
 def test_all_features_wider_layer(orc, dev):
@@ -140,7 +144,7 @@ def test_all_features_wider_layer(orc, dev):
     seq = rng.integers(0, 13, 64)
     seq[:3] = [12, 0, 1]
     kw = dict(P=P, clip=2.0, coupled=False, seq=seq)
-    compare(run_gpu(dev, p, "bidirectional", **kw), run_oracle(orc, p, "bidirectional", **kw), rtol=2e-4, atol=2e-5)
+    compare(run_gpu(dev, p, "bidirectional", **kw), run_oracle(orc, p, "bidirectional", **kw))
 
 
 def test_lengths_outside_range_are_clamped(orc, dev):
@@ -148,3 +152,46 @@ def test_lengths_outside_range_are_clamped(orc, dev):
     got = run_gpu(dev, p, "reverse", seq=np.array([9, -2, 5]))
     ref = run_oracle(orc, p, "reverse", seq=np.array([5, 0, 5]))
     compare(got, ref)
+
+
+ACTIVATIONS = ["Relu", "Tanh", "Sigmoid", "Affine", "LeakyRelu", "ThresholdedRelu", "ScaledTanh", "HardSigmoid",
+               "Elu", "Softsign", "Softplus"]
+
+
+@pytest.mark.parametrize("slot", [0, 1, 2])
+@pytest.mark.parametrize("name", ACTIVATIONS)
+def test_activation_functions(orc, dev, name, slot):
+    """Each ONNX activation as f (the i, o, f gates), g (the candidate) or h
+    (the output), with the operator's default alpha / beta, over a short
+    forward sequence from a nonzero state."""
+    p = weights(48, 5, 3, 32, 16, "forward")
+    acts = ["Sigmoid", "Tanh", "Tanh"]
+    acts[slot] = name
+    rng = np.random.default_rng(49)
+    h0 = rng.uniform(-0.9, 0.9, (1, 3, 16)).astype(np.float32)
+    c0 = rng.normal(0, 1, (1, 3, 16)).astype(np.float32)
+    kw = dict(acts=acts, h0=h0, c0=c0)
+    compare(run_gpu(dev, p, "forward", **kw), run_oracle(orc, p, "forward", **kw))
+
+
+def test_activation_lists_per_direction(orc, dev):
+    """Six functions (three per direction) whose alpha / beta come from the
+    attribute lists, consumed in the order of the functions; the last
+    functions fall back to their defaults; combined with peepholes, clip
+    and sequence lengths."""
+    p = weights(50, 6, 5, 64, 32, "bidirectional", "u8", "chan")
+    rng = np.random.default_rng(51)
+    kw = dict(acts=["HardSigmoid", "Elu", "ScaledTanh", "LeakyRelu", "Affine", "Softsign"],
+              alpha=[0.3, 0.8, 1.2, 0.05], beta=[0.45, 0.7],
+              P=rng.normal(0, 0.5, (2, 96)).astype(np.float32), clip=3.0, seq=np.array([6, 2, 0, 5, 1]))
+    compare(run_gpu(dev, p, "bidirectional", **kw), run_oracle(orc, p, "bidirectional", **kw))
+    # the default functions given explicitly are the default path
+    d = dict(acts=["Sigmoid", "Tanh", "Tanh"] * 2)
+    compare(run_gpu(dev, p, "bidirectional", **d), run_gpu(dev, p, "bidirectional"))
+
+
+def test_activation_arguments_rejected(dev):
+    p = weights(52, 2, 2, 16, 8, "forward")
+    for bad in (["Sigmoid", "Tanh"], ["Sigmoid", "Tanh", "Tanh"] * 2):
+        with pytest.raises(q.I8QError):
+            run_gpu(dev, p, "forward", acts=bad)

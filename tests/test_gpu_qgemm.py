@@ -86,11 +86,13 @@ def run_case(orc, dev, A, B=None, iB=None, scaleB=None, bias=None, act="identity
         assert np.all(uA.cpu().numpy()[sel, K:] == 0)
         assert np.array_equal(sA.cpu().numpy()[sel], ref["scaleA"])
         assert np.array_equal(zA.cpu().numpy()[sel], ref["zeroA"])
-        if constB:
-            iBt, sB, cs, ldb = ctx.weight_views()
-            assert np.array_equal(iBt.cpu().numpy()[:, :K], ref["iB"].T)
-            assert np.array_equal(sB.cpu().numpy(), ref["scaleB"])
-            assert np.array_equal(cs.cpu().numpy(), ref["iB"].astype(np.int64).sum(0))
+        # B's codes, scales and column sums: stored by SetParams (constant B)
+        # or written by this Forward into buf (B quantized per call)
+        iBt, sB, cs, ldb = ctx.weight_views(None if constB else buf)
+        assert np.array_equal(iBt.cpu().numpy()[:, :K], ref["iB"].T)
+        assert np.all(iBt.cpu().numpy()[:, K:] == 0)
+        assert np.array_equal(sB.cpu().numpy(), ref["scaleB"])
+        assert np.array_equal(cs.cpu().numpy(), ref["iB"].astype(np.int64).sum(0))
     assert np.array_equal(acc.cpu().numpy()[sel], ref["acc"])
     if typeC == "bf16":
         d = bf16_ulp_distance(_bits(C)[sel], ref["C"])
