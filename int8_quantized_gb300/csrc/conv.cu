@@ -170,150 +170,294 @@ qlinearconv_depthwise_halo(const XT* __restrict__ x, const WT* __restrict__ w, c
     }
 }
 
-// Depthwise KS x KS, stride 1, dilation 1: one CTA of 128 threads per
-// (image, channel) plane, integer tap sums on the byte dot product (dp4a)
-// over the raw codes.  The plane sits in shared memory as its codes, each
-// row at byte kX0 of a row of RW words, the halo filled with the x zero
-// point's code (so that a padded tap contributes x - x_zp = 0).  For the KS
-// taps of a filter row, with w packed four codes a word (zeros beyond KS),
-//   sum (x - x_zp)(w - w_zp) = sum x w - w_zp sum x - x_zp sum w + KS x_zp w_zp
-// per row, all exact in int32: sum x w and sum x come from dp4a of a 4-byte
-// window of the row with the packed weights and with ones.  Each thread
-// computes strips of 8 consecutive outputs of a row: it loads the strip's
-// words of each input row, shifts them once to the strip's first byte and
-// takes the eight windows with byte permutes whose selectors are constants.
-// The codes are requantized (quot_code_bits) and written as one 8-byte store.
-constexpr int kStrip = 8, kX0 = 8;  // outputs per strip; byte of x column 0 in a shared row
+// Depthwise KS x KS, stride 1, dilation 1, on the two-way dot product of
+// 16-bit and 8-bit integers (dp2a) over the raw input codes.  A CTA takes
+// `ppc` consecutive (image, channel) planes; each sits in shared memory as
+// its codes, row r of the plane at byte kX0 of shared row r + pt (rows of
+// RW words), the halo filled with the x zero point's code.  With the
+// centred filter w' = w - w_zp (|w'| <= 255, exact in 16 bits),
+//   sum (x - x_zp)(w - w_zp) = sum x w' - x_zp sum w'
+// over all KS^2 taps: a padded tap holds x = x_zp and so adds nothing, and
+// x_zp sum w' is a constant of the channel.  dp2a multiplies the two 16-bit
+// halves of one operand with two bytes of the other (bytes 0, 1 or 2, 3),
+// so a 4-byte window of an input row starting at output e serves outputs e
+// and e + 1: e takes (w'0, w'1) on bytes 0, 1 and (w'2, 0) on bytes 2, 3;
+// e + 1 takes (0, w'0) and (w'1, w'2) (for KS = 5 a second window adds the
+// taps past the fourth byte).  Every sum is exact in int32.
+//
+// A thread owns an item: R output rows x 8 consecutive outputs.  It reads
+// each of the R + KS - 1 input rows the item needs once (NWD words, shifted
+// once to the item's first byte), forms the windows of the even outputs by
+// byte permutes with constant selectors, and feeds every output row that
+// row reaches (up to KS of them); an output row is requantized and stored
+// (one 8-byte store) as soon as its last input row is in.  The
+// requantization code of fl(fl(acc * mul) / y_scale) comes from
+// q = fl(fl(acc * mul) * r), r = fl(1 / y_scale): q clamped to the code
+// range and rounded by adding 1.5 * 2^23 (round half to even).  Within the
+// range (|q| < 2^9) q and the quotient differ by less than 2^-22 |q|, so
+// they round alike unless q lies within 2^-21 |q| of a half-integer, where
+// the quotient is formed exactly (checked once per row of 8 outputs);
+// beyond the range both saturate alike.  A scale whose reciprocal is not a
+// normal number takes the quotient always.  (Tap sums on the fp32 pipe,
+// exact for these magnitudes, were measured slower: the byte-to-float
+// conversions outweigh the faster multiply-adds.)
+constexpr int kStrip = 8, kX0 = 8;  // outputs per item row; byte of x column 0 in a shared row
 
-template <bool AS, bool BS>
-__device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
+// Words of a shared row: the slack before column 0, the items' outputs, the
+// filter's reach past them; a multiple of 4 so rows are 16-byte aligned.
+__host__ __device__ constexpr int dw_row_words(int nstrips, int ks) {
+  return ((kX0 + nstrips * kStrip + 4 * ((ks + 3) / 4) + 8 + 15) / 16) * 4;
+}
+
+// Output rows per item: KS = 3 keeps three rows of sums in flight, KS = 5 five.
+template <int KS>
+constexpr int dw_rows() { return KS == 3 ? 7 : 4; }
+
+// Per-plane constants staged in shared memory after the planes.
+template <int KS>
+struct DwPlane {
+  // per filter row, the 16-bit pairs of w' = w - w_zp the dp2a steps take:
+  // KS = 3: (w'0, w'1), (w'2, 0) for an even output, (0, w'0), (w'1, w'2)
+  // for the odd one; KS = 5 adds (w'4, 0) and (w'3, w'4) on the window four
+  // bytes on
+  uint32_t wp[KS][KS == 3 ? 4 : 6];
+  int k0;     // B - x_zp sum w'
+  float mul;  // x_scale * w_scale
+};
+
+// d = c + a.lo16 * b.byte(0|2) + a.hi16 * b.byte(1|3): a holds two signed
+// 16-bit values, b four codes (signed when BS).
+template <bool HI, bool BS>
+__device__ __forceinline__ int dp2a(uint32_t a, uint32_t b, int c) {
   int d;
-  if (AS && BS) asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  else if (AS) asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  else if (BS) asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  else asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  if (HI && BS) asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else if (HI) asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else if (BS) asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 
-__host__ __device__ constexpr int dw_row_words(int nstrips, int ks) {
-  return (kX0 + nstrips * kStrip + 4 * ((ks + 3) / 4) + 8 + 3) / 4;
+__device__ __forceinline__ uint32_t pair16(int lo, int hi) {
+  return (uint32_t)(lo & 0xffff) | ((uint32_t)hi << 16);
 }
 
+__device__ __forceinline__ void dw_cp_async(uint32_t dst, const void* src, int bytes) {
+  if (bytes == 8) asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src) : "memory");
+  else asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void dw_cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void dw_cp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Persistent: CTA b takes the groups of `ppc` consecutive planes b, b +
+// gridDim.x, ...; two shared buffers, the next group's planes copied in
+// (cp.async, 8- or 4-byte pieces) while the current one is computed.  The
+// halo of both buffers is written once: copies touch only the interior.
 template <typename XT, typename WT, typename YT, int KS>
-__global__ void __launch_bounds__(128)
-qlinearconv_depthwise_strip(const XT* __restrict__ x, const WT* __restrict__ w, const float* __restrict__ w_scale,
-                            const WT* __restrict__ w_zp, int per_channel, const int32_t* __restrict__ B, int C, int H,
-                            int W, int OH, int OW, int pt, int pl, float x_scale, int x_zp, float y_scale, int y_zp,
-                            float qlo, float qhi, YT* __restrict__ y) {
-  constexpr bool XS = std::is_signed<XT>::value, WS = std::is_signed<WT>::value;
-  constexpr int TW = (KS + 3) / 4;  // words of a filter row
-  constexpr int NWD = 3 + TW;       // words loaded per input row of a strip
-  extern __shared__ __align__(16) uint32_t plw[];
-  const int c = blockIdx.x % C, n = blockIdx.x / C;
-  const int nstrips = (OW + kStrip - 1) / kStrip;
-  const int HP = OH + KS - 1, RW = dw_row_words(nstrips, KS);
+__global__ void __launch_bounds__(256)
+qlinearconv_depthwise_rows(const XT* __restrict__ x, const WT* __restrict__ w, const float* __restrict__ w_scale,
+                           const WT* __restrict__ w_zp, int per_channel, const int32_t* __restrict__ B, int C, int H,
+                           int W, int OH, int OW, int pt, int pl, int planes, int ppc, float x_scale, int x_zp,
+                           float y_scale, int y_zp, float qlo, float qhi, YT* __restrict__ y) {
+  constexpr bool XS = std::is_signed<XT>::value;  // the weights enter centred, as 16-bit values
+  constexpr int NWD = KS == 3 ? 4 : 5;  // words read per input row of an item (8 outputs + KS - 1)
+  constexpr int R = dw_rows<KS>();
+  extern __shared__ __align__(16) uint32_t smw[];
+  const int nstrips = (OW + kStrip - 1) / kStrip, nblocks = (OH + R - 1) / R;
+  const int HP = OH + KS - 1, RW = dw_row_words(nstrips, KS), PW = HP * RW;
+  const int buf_words = ppc * PW;
+  DwPlane<KS>* prm_base = reinterpret_cast<DwPlane<KS>*>(smw + 2 * buf_words);
+  const int nthr = (int)blockDim.x, tid = (int)threadIdx.x;
   const uint32_t fill = (uint32_t)(uint8_t)x_zp * 0x01010101u;
-  for (int i = threadIdx.x; i < HP * RW; i += blockDim.x) plw[i] = fill;
+  const int rows_in = min(H, HP - pt);  // input rows that reach an output
+  const int ngroups = (planes + ppc - 1) / ppc;
+
+  // both buffers: every word the zero point's code, once
+  for (int i = tid; i < 2 * buf_words / 4; i += nthr)
+    reinterpret_cast<uint4*>(smw)[i] = make_uint4(fill, fill, fill, fill);
   __syncthreads();
-  const XT* xp = x + ((int64_t)n * C + c) * H * W;
-  uint8_t* plb = reinterpret_cast<uint8_t*>(plw);
-  const int rows = min(H, HP - pt);  // input rows that reach an output
-  if ((W & 3) == 0 && (reinterpret_cast<uintptr_t>(xp) & 3) == 0) {
-    // the plane is contiguous: 32-bit words, consecutive threads on
-    // consecutive words, each landing at a word of its shared row
-    const int wpr = W / 4;
-    const int dr = (int)blockDim.x / wpr, dj = (int)blockDim.x - dr * wpr;  // the stride as (rows, words)
-    int r = (int)threadIdx.x / wpr, j = (int)threadIdx.x - r * wpr;
-    for (int i = threadIdx.x; i < rows * wpr; i += blockDim.x) {
-      plw[(r + pt) * RW + kX0 / 4 + j] = __ldg(reinterpret_cast<const uint32_t*>(xp) + i);
-      r += dr;
-      j += dj;
-      if (j >= wpr) {
-        j -= wpr;
-        ++r;
+
+  // copies: a thread takes whole input rows, in pieces of 8 or 4 bytes
+  // (single bytes when the rows are not word aligned)
+  const int pb = ((W & 7) == 0 && (reinterpret_cast<uintptr_t>(x) & 7) == 0) ? 8
+                 : ((W & 3) == 0 && (reinterpret_cast<uintptr_t>(x) & 3) == 0) ? 4 : 1;
+
+  // issue the copies of group grp into buffer bi and its plane constants
+  auto stage = [&](int grp, int bi) {
+    const int p0 = grp * ppc, np = min(ppc, planes - p0);
+    const uint8_t* xs = reinterpret_cast<const uint8_t*>(x + (int64_t)p0 * H * W);
+    const uint32_t dsts = (uint32_t)__cvta_generic_to_shared(smw + bi * buf_words) + kX0;
+    for (int g = tid; g < np * H; g += nthr) {
+      const int p = g / H, r = g - p * H;
+      if (r >= rows_in) continue;
+      const uint8_t* src = xs + (int64_t)g * W;
+      const uint32_t dst = dsts + (uint32_t)((p * HP + pt + r) * RW) * 4u;
+      if (pb > 1) {
+        for (int j = 0; j < W; j += pb) dw_cp_async(dst + j, src + j, pb);
+      } else {
+        uint8_t* db = reinterpret_cast<uint8_t*>(smw + bi * buf_words) + (size_t)((p * HP + pt + r) * RW) * 4 + kX0;
+        for (int j = 0; j < W; ++j) db[j] = src[j];
       }
     }
-  } else {
-    for (int i = threadIdx.x; i < rows * W; i += blockDim.x) {
-      const int r = i / W, col = i - r * W;
-      plb[(r + pt) * RW * 4 + kX0 + col] = (uint8_t)xp[i];
-    }
-  }
-  // the filter rows packed four codes a word, their code sum, the constant terms
-  uint32_t wr[KS][TW];
-  int wsum = 0;
+    for (int i = tid; i < np * (KS + 1); i += nthr) {
+      if (i < np * KS) {
+        // (plane, filter row): the row's 16-bit weight pairs
+        const int pi = i / KS, kh = i - pi * KS;
+        const int c = (p0 + pi) % C;
+        DwPlane<KS>& P = prm_base[bi * ppc + pi];
+        const int wz = (int)w_zp[per_channel ? c : 0];
+        int v[KS];
 #pragma unroll
-  for (int kh = 0; kh < KS; ++kh)
-#pragma unroll
-    for (int t = 0; t < TW; ++t) {
-      uint32_t v = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (4 * t + e < KS) {
-          const WT q = w[(int64_t)c * KS * KS + kh * KS + 4 * t + e];
-          wsum += (int)q;
-          v |= (uint32_t)(uint8_t)q << (8 * e);
+        for (int kw = 0; kw < KS; ++kw) v[kw] = (int)w[(int64_t)c * KS * KS + kh * KS + kw] - wz;
+        P.wp[kh][0] = pair16(v[0], v[1]);
+        P.wp[kh][2] = pair16(0, v[0]);
+        P.wp[kh][3] = pair16(v[1], v[2]);
+        if constexpr (KS == 3) {
+          P.wp[kh][1] = pair16(v[2], 0);
+        } else {
+          P.wp[kh][1] = pair16(v[2], v[3]);
+          P.wp[kh][4] = pair16(v[4], 0);
+          P.wp[kh][5] = pair16(v[3], v[4]);
         }
-      wr[kh][t] = v;
+      } else {
+        // (plane): the constant term and the scale
+        const int pi = i - np * KS;
+        const int c = (p0 + pi) % C;
+        DwPlane<KS>& P = prm_base[bi * ppc + pi];
+        const int wz = (int)w_zp[per_channel ? c : 0];
+        int wsum = 0;
+        for (int t = 0; t < KS * KS; ++t) wsum += (int)w[(int64_t)c * KS * KS + t] - wz;
+        P.k0 = (B ? B[c] : 0) - x_zp * wsum;
+        P.mul = __fmul_rn(x_scale, w_scale[per_channel ? c : 0]);
+      }
     }
-  // ones over the taps a filter-row word holds (all four but in the last word)
-  constexpr uint32_t ones0 = 0x01010101u >> (8 * (4 - (KS - 4 * (TW - 1))));
-  const int wz = (int)w_zp[per_channel ? c : 0];
-  const int32_t k0 = (B ? B[c] : 0) - x_zp * wsum + KS * KS * x_zp * wz;
-  const float mul = __fmul_rn(x_scale, w_scale[per_channel ? c : 0]);
-  const float yr = quot_rcp(y_scale);
+    dw_cp_commit();
+  };
+
   const float lo_z = qlo - (float)y_zp, hi_z = qhi - (float)y_zp;
-  __syncthreads();
-  YT* yp = y + ((int64_t)n * C + c) * OH * OW;
-  const bool vec_rows = (OW % kStrip) == 0 && (reinterpret_cast<uintptr_t>(y) & 7) == 0;
-  const int doh = (int)blockDim.x / nstrips, dst = (int)blockDim.x - doh * nstrips;  // the stride as (rows, strips)
-  int oh = (int)threadIdx.x / nstrips, st = (int)threadIdx.x - oh * nstrips;
-  for (int sidx = threadIdx.x; sidx < OH * nstrips; sidx += blockDim.x) {
-    const int ow0 = st * kStrip;
-    const int s0 = kX0 - pl + ow0;  // first byte of the strip's windows in a shared row
-    const uint32_t shift = 0x3210u + (uint32_t)(s0 & 3) * 0x1111u;
-    int sxw[kStrip], sx[kStrip];
-#pragma unroll
-    for (int e = 0; e < kStrip; ++e) sxw[e] = sx[e] = 0;
-#pragma unroll
-    for (int kh = 0; kh < KS; ++kh) {
-      const uint32_t* row = plw + (oh + kh) * RW + (s0 >> 2);
-      uint32_t wd[NWD], a[NWD - 1];
-#pragma unroll
-      for (int i = 0; i < NWD; ++i) wd[i] = row[i];
-#pragma unroll
-      for (int i = 0; i < NWD - 1; ++i) a[i] = __byte_perm(wd[i], wd[i + 1], shift);  // bytes from s0 on
-#pragma unroll
-      for (int e = 0; e < kStrip; ++e)
-#pragma unroll
-        for (int t = 0; t < TW; ++t) {
-          const int k = (e >> 2) + t;
-          const uint32_t win = (e & 3) ? __byte_perm(a[k], a[k + 1], 0x3210u + (uint32_t)(e & 3) * 0x1111u) : a[k];
-          sxw[e] = dp4a<XS, WS>(win, wr[kh][t], sxw[e]);
-          sx[e] = dp4a<XS, false>(win, t == TW - 1 ? ones0 : 0x01010101u, sx[e]);
-        }
-    }
-    uint32_t code[kStrip];
-#pragma unroll
-    for (int e = 0; e < kStrip; ++e) {
-      const int32_t acc = sxw[e] - wz * sx[e] + k0;
-      code[e] = quot_code_bits(__fmul_rn(__int2float_rn(acc), mul), y_scale, yr, lo_z, hi_z, y_zp);
-    }
-    YT* out = yp + oh * OW + ow0;
-    if (vec_rows && ((reinterpret_cast<uintptr_t>(out) & 7) == 0)) {
-      *reinterpret_cast<uint2*>(out) =
-          make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]), pack_low_bytes(code[4], code[5], code[6], code[7]));
+  const float yr = quot_rcp(y_scale);
+  const bool rcp_ok = yr == yr;
+  const int ipp = nstrips * nblocks;
+
+  int grp = blockIdx.x;
+  if (grp < ngroups) stage(grp, 0);
+  for (int k = 0; grp < ngroups; ++k, grp += gridDim.x) {
+    const int bi = k & 1;
+    const int nxt = grp + (int)gridDim.x;
+    if (nxt < ngroups) {
+      stage(nxt, bi ^ 1);
+      dw_cp_wait<1>();
     } else {
+      dw_cp_wait<0>();
+    }
+    __syncthreads();  // this group's planes and constants are in
+    const int p0 = grp * ppc, np = min(ppc, planes - p0);
+    const uint32_t* buf = smw + bi * buf_words;
+    const DwPlane<KS>* prm = prm_base + bi * ppc;
+    for (int it = tid; it < np * ipp; it += nthr) {
+      const int p = it / ipp, rem = it - p * ipp;
+      const int blk = rem / nstrips, st = rem - blk * nstrips;
+      const DwPlane<KS>& P = prm[p];
+      constexpr int NP = KS == 3 ? 4 : 6;
+      uint32_t wp[KS][NP];
 #pragma unroll
-      for (int e = 0; e < kStrip; ++e)
-        if (ow0 + e < OW) out[e] = (YT)code[e];
+      for (int kh = 0; kh < KS; ++kh)
+#pragma unroll
+        for (int t = 0; t < NP; ++t) wp[kh][t] = P.wp[kh][t];
+      const int k0 = P.k0;
+      const float mul = P.mul;
+      const int oh0 = blk * R, ow0 = st * kStrip;
+      const int s0 = kX0 - pl + ow0;  // first byte of the item's windows in a shared row
+      const uint32_t shift = 0x3210u + (uint32_t)(s0 & 3) * 0x1111u;
+      const uint32_t* rows = buf + (size_t)p * PW + oh0 * RW + (s0 >> 2);
+      YT* yp = y + (int64_t)(p0 + p) * OH * OW + ow0;
+      // whole 8-byte stores when the item's rows are complete and aligned
+      const bool vec = ow0 + kStrip <= OW && (OW & 7) == 0 && (reinterpret_cast<uintptr_t>(yp) & 7) == 0;
+      int acc[R][kStrip];
+#pragma unroll
+      for (int ir = 0; ir < R + KS - 1; ++ir) {
+        // input row oh0 + ir of the shared plane (rows past the plane feed
+        // only rows past OH, which are not stored)
+        uint32_t wd[NWD];
+        const bool rin = oh0 + ir < HP;
+#pragma unroll
+        for (int i = 0; i < NWD; ++i) wd[i] = rin ? rows[ir * RW + i] : fill;
+        uint32_t a[NWD - 1];
+#pragma unroll
+        for (int i = 0; i < NWD - 1; ++i) a[i] = __byte_perm(wd[i], wd[i + 1], shift);  // bytes from s0 on
+        // win[m]: the 4 bytes from output 2m's first tap; KS = 5 also reads win[m + 2]
+        constexpr int NWIN = kStrip / 2 + (KS == 5 ? 2 : 0);
+        uint32_t win[NWIN];
+#pragma unroll
+        for (int m = 0; m < NWIN; ++m) win[m] = (m & 1) ? __byte_perm(a[m >> 1], a[(m >> 1) + 1], 0x5432u) : a[m >> 1];
+#pragma unroll
+        for (int kh = 0; kh < KS; ++kh) {
+          const int o = ir - kh;  // the item's output row this input row feeds through filter row kh
+          if (o < 0 || o >= R) continue;
+#pragma unroll
+          for (int m = 0; m < kStrip / 2; ++m) {
+            int ve = kh == 0 ? k0 : acc[o][2 * m];
+            int vo = kh == 0 ? k0 : acc[o][2 * m + 1];
+            ve = dp2a<false, XS>(wp[kh][0], win[m], ve);
+            ve = dp2a<true, XS>(wp[kh][1], win[m], ve);
+            vo = dp2a<false, XS>(wp[kh][2], win[m], vo);
+            vo = dp2a<true, XS>(wp[kh][3], win[m], vo);
+            if constexpr (KS == 5) {
+              ve = dp2a<false, XS>(wp[kh][4], win[m + 2], ve);
+              vo = dp2a<false, XS>(wp[kh][5], win[m + 2], vo);
+            }
+            acc[o][2 * m] = ve;
+            acc[o][2 * m + 1] = vo;
+          }
+          if (kh == KS - 1 && oh0 + o < OH) {
+            // output row oh0 + o is complete: requantize and store its 8 codes
+            uint32_t code[kStrip];
+            float vv[kStrip];
+            bool slow = !rcp_ok;
+#pragma unroll
+            for (int e = 0; e < kStrip; e += 2) {
+              const float2 v = mul2_rn(make_float2(__int2float_rn(acc[o][e]), __int2float_rn(acc[o][e + 1])),
+                                       make_float2(mul, mul));
+              const float2 q = mul2_rn(v, make_float2(yr, yr));
+              vv[e] = v.x;
+              vv[e + 1] = v.y;
+              const float qq[2] = {q.x, q.y};
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const float cq = fminf(fmaxf(qq[h], lo_z), hi_z);
+                const float r1 = __fadd_rn(cq, 12582912.0f);
+                const float d = __fsub_rn(cq, __fsub_rn(r1, 12582912.0f));
+                code[e + h] = (uint32_t)(__float_as_int(r1) + y_zp);
+                slow |= fabsf(d) > __fmaf_rn(fabsf(cq), -0x1p-21f, 0.5f);
+              }
+            }
+            if (slow) {
+              // near a half-integer (or no usable reciprocal): the quotient itself
+#pragma unroll
+              for (int e = 0; e < kStrip; ++e) {
+                const float q = __fmul_rn(vv[e], yr);
+                const float cq = fminf(fmaxf(q, lo_z), hi_z);
+                const float d = __fsub_rn(cq, __fsub_rn(__fadd_rn(cq, 12582912.0f), 12582912.0f));
+                if (!rcp_ok || fabsf(d) > __fmaf_rn(fabsf(cq), -0x1p-21f, 0.5f))
+                  code[e] = rint_code_bits(__fdiv_rn(vv[e], y_scale), lo_z, hi_z, y_zp);
+              }
+            }
+            YT* out = yp + (int64_t)(oh0 + o) * OW;
+            if (vec) {
+              *reinterpret_cast<uint2*>(out) = make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]),
+                                                          pack_low_bytes(code[4], code[5], code[6], code[7]));
+            } else {
+#pragma unroll
+              for (int e = 0; e < kStrip; ++e)
+                if (ow0 + e < OW) out[e] = (YT)code[e];
+            }
+          }
+        }
+      }
     }
-    oh += doh;
-    st += dst;
-    if (st >= nstrips) {
-      st -= nstrips;
-      ++oh;
-    }
+    __syncthreads();  // the buffer is read before the copies into it two groups on
   }
 }
 
@@ -356,20 +500,35 @@ int run_direct(const ConvShape& s, const void* x, float x_scale, int x_zp, const
   const float dq_hi = std::is_same<YT, uint8_t>::value ? 255.0f : 127.0f;
   const int64_t P = std::max(std::max(s.pt, s.pb), std::max(s.pl, s.pr));
   {
-    // strip kernel: depthwise 3x3 / 5x5, stride 1, dilation 1
+    // dp4a row kernel: depthwise 3x3 / 5x5, stride 1, dilation 1; planes
+    // per CTA so that the items (rows x 8 outputs) of a CTA fill 256 threads
     const int64_t nstrips = (s.OW + kStrip - 1) / kStrip;
-    const size_t ssmem = (size_t)(s.OH + s.kH - 1) * dw_row_words((int)std::min<int64_t>(nstrips, 1 << 20), (int)s.kW) * 4;
+    const int64_t R = s.kH == 3 ? dw_rows<3>() : dw_rows<5>();
+    const int64_t ipp = nstrips * ((s.OH + R - 1) / R);
+    const size_t pbytes = nstrips <= (1 << 20)
+                              ? (size_t)(s.OH + s.kH - 1) * dw_row_words((int)nstrips, (int)s.kW) * 4
+                              : (size_t)-1 / 2;
+    const size_t prm = s.kH == 3 ? sizeof(DwPlane<3>) : sizeof(DwPlane<5>);
+    int64_t ppc = std::max<int64_t>(1, std::min<int64_t>(256 / std::max<int64_t>(ipp, 1), 8));
+    while (ppc > 1 && 2 * ppc * (pbytes + prm) > 160 * 1024) --ppc;
+    const size_t ssmem = 2 * (size_t)ppc * (pbytes + prm);
     if (s.group == s.C && s.M == s.C && s.Cg == 1 && s.sh == 1 && s.sw == 1 && s.dh == 1 && s.dw == 1 &&
         s.kH == s.kW && (s.kH == 3 || s.kH == 5) && s.pl <= kX0 && ssmem <= 160 * 1024 &&
-        !getenv("I8Q_FORCE_CONV_HALO")) {
-      auto kern = s.kH == 3 ? qlinearconv_depthwise_strip<XT, WT, YT, 3> : qlinearconv_depthwise_strip<XT, WT, YT, 5>;
-      if (ssmem > 48 * 1024)
-        I8Q_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem));
+        s.N * s.C < ((int64_t)1 << 31) && !getenv("I8Q_FORCE_CONV_HALO")) {
+      auto kern = s.kH == 3 ? qlinearconv_depthwise_rows<XT, WT, YT, 3> : qlinearconv_depthwise_rows<XT, WT, YT, 5>;
+      const int ar = smem_attr((const void*)kern, 160 * 1024);
+      if (ar) return ar;
+      const int threads = (int)std::min<int64_t>(256, round_up(ppc * ipp, 32));
+      const int64_t planes = s.N * s.C, groups = ceil_div(planes, ppc);
+      // persistent: as many CTAs as fit at once, at most one per group
+      int per_sm = 0;
+      I8Q_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, ssmem));
+      const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(groups, (int64_t)std::max(per_sm, 1) * sm_count()));
       I8Q_PROF("qlinearconv_depthwise", st);
-      kern<<<(unsigned)(s.N * s.C), 128, ssmem, st>>>((const XT*)x, (const WT*)w, w_scale, (const WT*)w_zp, per_ch, B,
-                                                      (int)s.C, (int)s.H, (int)s.W, (int)s.OH, (int)s.OW, (int)s.pt,
-                                                      (int)s.pl, x_scale, x_zp, y_scale, y_zp, dq_lo, dq_hi, (YT*)y);
-      I8Q_LAUNCH_CHECK("qlinearconv_depthwise_strip");
+      kern<<<(unsigned)grid, threads, ssmem, st>>>(
+          (const XT*)x, (const WT*)w, w_scale, (const WT*)w_zp, per_ch, B, (int)s.C, (int)s.H, (int)s.W, (int)s.OH,
+          (int)s.OW, (int)s.pt, (int)s.pl, (int)planes, (int)ppc, x_scale, x_zp, y_scale, y_zp, dq_lo, dq_hi, (YT*)y);
+      I8Q_LAUNCH_CHECK("qlinearconv_depthwise_rows");
       return I8Q_OK;
     }
   }

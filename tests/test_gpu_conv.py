@@ -164,10 +164,14 @@ DW_CASES = [
     (3, 4, 9, 16, 5, (2, 2, 2, 2)),
     (1, 6, 30, 7, 5, (0, 0, 0, 0)),
     (2, 3, 8, 8, 3, (2, 1, 0, 2)),
+    (1, 7, 56, 56, 3, (1, 1, 1, 1)),     # planes not a multiple of the planes per CTA
+    (1, 3, 130, 130, 3, (1, 1, 1, 1)),   # more items per plane than threads
+    (2, 5, 33, 21, 5, (2, 2, 2, 2)),     # rows of W % 4 != 0 bytes
+    (1, 4, 12, 12, 3, (1, 1, 1, 1)),     # rows of whole words, not 8-byte pieces
 ]
 
 
-@pytest.mark.parametrize("kernel", ["strip", "halo"])
+@pytest.mark.parametrize("kernel", ["rows", "halo"])
 @pytest.mark.parametrize("case", DW_CASES)
 @pytest.mark.parametrize("types", [("u8", "u8", "u8"), ("s8", "s8", "s8"), ("u8", "s8", "s8")])
 def test_depthwise_kernels(orc, dev, monkeypatch, kernel, case, types):
@@ -186,7 +190,7 @@ def test_depthwise_kernels(orc, dev, monkeypatch, kernel, case, types):
              int(rng.integers(yt[0], yt[1])), B, pads, group=C, ytype=types[2])
 
 
-@pytest.mark.parametrize("kernel", ["strip", "halo"])
+@pytest.mark.parametrize("kernel", ["rows", "halo"])
 @pytest.mark.parametrize("ys", [2.0, 0.5, 3.0, 0.1, 1e-30, 1e30, 3e38])
 def test_depthwise_requantization_ties(orc, dev, monkeypatch, kernel, ys):
     """Unit input and filter scales make every rescaled sum an integer, so
