@@ -418,7 +418,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmH, TcStepParams p) {
   constexpr uint32_t IDESC = idesc_bf16(BM, BN);
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned, indexed from the shared array itself so that accesses stay shared-space
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -812,7 +813,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 lstm_persist_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmH, Params p) {
   constexpr uint32_t IDESC = idesc_bf16(BM, BN);
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned, indexed from the shared array itself so that accesses stay shared-space
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int KT = p.Hp / BK;
   uint8_t* rtile = smem + STAGES * A_STAGE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(rtile + (size_t)KT * R_SLAB);

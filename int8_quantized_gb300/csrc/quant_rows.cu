@@ -668,7 +668,8 @@ col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int
   constexpr int RG = kCqConsumers / W;      // row groups of a box
   constexpr int R = kCqBoxRows / RG;        // rows per consumer thread per box
   extern __shared__ uint8_t cq_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(cq_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned, indexed from the shared array itself so that accesses stay shared-space
+  uint8_t* ring = cq_raw + ((1024u - (tc::smem_u32(cq_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)kCqStages * kCqStageBytes);
   uint64_t* empty = full + kCqStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kCqStages);
