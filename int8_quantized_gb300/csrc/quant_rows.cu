@@ -629,12 +629,12 @@ col_quant_wide(const T* __restrict__ B, int64_t K, int64_t N, int64_t Kp, const 
 }
 
 // ---- columns, one strip per CTA -------------------------------------------
-// A persistent CTA owns a strip of 128 bytes of every row of B (32 fp32 or
-// 64 bf16 columns).  One thread streams the strip through a 4-stage ring of
+// A persistent CTA owns a strip of 64 bytes of every row of B (16 fp32 or
+// 32 bf16 columns).  One thread streams the strip through an 8-stage ring of
 // 256-row TMA boxes twice: first for max|B| per column, then -- from L2: a
-// strip per SM is 0.5 MB at K = 4096 -- for the codes.  Each consumer
-// thread owns one column and a run of R adjacent rows of every box (16 for
-// fp32, 32 for bf16), reads it down the column in shared memory and writes
+// strip per SM is 0.25 MB at K = 4096 -- for the codes.  Each consumer
+// thread owns one column and a run of R adjacent rows of every box (8 for
+// fp32, 16 for bf16), reads it down the column in shared memory and writes
 // its R codes, contiguous along K, straight to the transposed outputs.  Rows
 // past K read as zero from the tensor map, which gives the zero padding up
 // to Kp.  The rounding avoids the conversion units: q is clamped to
@@ -643,7 +643,8 @@ col_quant_wide(const T* __restrict__ B, int64_t K, int64_t N, int64_t Kp, const 
 // gives the code as an exact float, whose bf16 bits are its top 16 bits and
 // whose column sum is exact in fp32 (|sum| <= 2^23).
 constexpr int kCqConsumers = 512, kCqThreads = kCqConsumers + 32;
-constexpr int kCqBoxRows = 256, kCqStages = 4, kCqStageBytes = kCqBoxRows * 128;
+constexpr int kCqRowBytes = 64;  // strip width in bytes (128: 4 % slower; 32: 6 % slower)
+constexpr int kCqBoxRows = 256, kCqStages = 8, kCqStageBytes = kCqBoxRows * kCqRowBytes;
 constexpr size_t kCqSmem = 1024 + (size_t)kCqStages * kCqStageBytes + 2 * kCqStages * 8 + 16;
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 constexpr uint32_t ST_TIMEOUT_COLS = 1u << 13;
@@ -664,7 +665,7 @@ __global__ void __launch_bounds__(kCqThreads, 1)
 col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int64_t Kp, int qmin, int qmax,
               int8_t* __restrict__ iBt, __nv_bfloat16* __restrict__ iBt_bf16, float* __restrict__ scaleB,
               int32_t* __restrict__ colsum, uint32_t* status) {
-  constexpr int W = 128 / (int)sizeof(T);   // strip width in columns
+  constexpr int W = kCqRowBytes / (int)sizeof(T);  // strip width in columns
   constexpr int RG = kCqConsumers / W;      // row groups of a box
   constexpr int R = kCqBoxRows / RG;        // rows per consumer thread per box
   extern __shared__ uint8_t cq_raw[];
@@ -733,9 +734,9 @@ col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int
       const uint32_t st = it % kCqStages;
       if (ok) ok = tc::wait_bar(tc::smem_u32(full + st), (it / kCqStages) & 1u, abort_flag, status, ST_TIMEOUT_COLS);
       if (ok) {
-        const uint8_t* src = ring + (size_t)st * kCqStageBytes + (size_t)(rg * R) * 128 + (size_t)c * sizeof(T);
+        const uint8_t* src = ring + (size_t)st * kCqStageBytes + (size_t)(rg * R) * kCqRowBytes + (size_t)c * sizeof(T);
 #pragma unroll
-        for (int r = 0; r < R; ++r) m = fmaxf(m, fabsf(elem_f32(src + r * 128, T())));
+        for (int r = 0; r < R; ++r) m = fmaxf(m, fabsf(elem_f32(src + r * kCqRowBytes, T())));
       }
       __syncwarp();
       if (ok && lane == 0) tc::mbar_arrive(tc::smem_u32(empty + st));
@@ -760,13 +761,13 @@ col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int
       if (ok) ok = tc::wait_bar(tc::smem_u32(full + st), (it / kCqStages) & 1u, abort_flag, status, ST_TIMEOUT_COLS);
       uint32_t w[R / 2];
       if (ok) {
-        const uint8_t* src = ring + (size_t)st * kCqStageBytes + (size_t)(rg * R) * 128 + (size_t)c * sizeof(T);
+        const uint8_t* src = ring + (size_t)st * kCqStageBytes + (size_t)(rg * R) * kCqRowBytes + (size_t)c * sizeof(T);
 #pragma unroll
         for (int r = 0; r < R; r += 2) {
           float f[2];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const float q = fminf(fmaxf(__fdiv_rn(elem_f32(src + (r + h) * 128, T()), s), lo), hi);
+            const float q = fminf(fmaxf(__fdiv_rn(elem_f32(src + (r + h) * kCqRowBytes, T()), s), lo), hi);
             f[h] = __fsub_rn(__fadd_rn(q, kRoundMagic), kRoundMagic);
             fsum = __fadd_rn(fsum, f[h]);
           }
@@ -783,17 +784,21 @@ col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int
           for (int q = 0; q < R / 8; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         }
         if (iBt) {
-          uint4* d = reinterpret_cast<uint4*>(iBt + j * Kp + k);
+          uint32_t o[R / 4];
 #pragma unroll
-          for (int q = 0; q < R / 16; ++q) {
-            uint32_t o[4];
+          for (int e = 0; e < R / 4; ++e) {
+            const uint32_t w0 = w[2 * e], w1 = w[2 * e + 1];
+            o[e] = code_byte(w0 << 16) | (code_byte(w0 & 0xffff0000u) << 8) | (code_byte(w1 << 16) << 16) |
+                   (code_byte(w1 & 0xffff0000u) << 24);
+          }
+          if constexpr (R % 16 == 0) {
+            uint4* d = reinterpret_cast<uint4*>(iBt + j * Kp + k);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t w0 = w[8 * q + 2 * e], w1 = w[8 * q + 2 * e + 1];
-              o[e] = code_byte(w0 << 16) | (code_byte(w0 & 0xffff0000u) << 8) | (code_byte(w1 << 16) << 16) |
-                     (code_byte(w1 & 0xffff0000u) << 24);
-            }
-            d[q] = make_uint4(o[0], o[1], o[2], o[3]);
+            for (int q = 0; q < R / 16; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          } else {
+            uint2* d = reinterpret_cast<uint2*>(iBt + j * Kp + k);
+#pragma unroll
+            for (int q = 0; q < R / 8; ++q) d[q] = make_uint2(o[2 * q], o[2 * q + 1]);
           }
         }
       }
@@ -816,7 +821,7 @@ int launch_col_quant_tma(const T* B, int64_t K, int64_t N, int64_t Kp, int qmin,
                          __nv_bfloat16* iBt_bf16, float* scaleB, int32_t* colsum, uint32_t* status, cudaStream_t s) {
   const int ar = smem_attr((const void*)col_quant_tma<T>, (int)kCqSmem);
   if (ar) return ar;
-  constexpr int W = 128 / (int)sizeof(T);
+  constexpr int W = kCqRowBytes / (int)sizeof(T);
   CUtensorMap map;
   const int rc = tc::make_map_plain_2d(&map, B,
                                        sizeof(T) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
