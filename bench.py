@@ -43,8 +43,8 @@ WORKLOAD = ("dynamic quantized GEMM M=8192 K=4096 N=14336: bf16 A quantized per 
 NCU_TRAFFIC = {
     "gemm_tc_pair": {"sources": ["int8_quantized_gb300/csrc/gemm_tc.cu", "int8_quantized_gb300/csrc/tcgen05.cuh",
                                  "int8_quantized_gb300/csrc/common.cuh"],
-                     "sha256": "ac8dd190dd93fe384d017b1d1a9223fc4f77e5e4087d9be16fe695c579f7d15b",
-                     "bytes": (568.43 + 221.29) * 1e6,
+                     "sha256": "82b0d94f172358ad233dbaaf2881547df9fde12b706617a0c8ebe655bfd0e565",
+                     "bytes": (566.65 + 220.04) * 1e6,
                      "profile": "profiles/gemm_tc_pair_large_gemm.md"},
 }
 
