@@ -754,6 +754,13 @@ col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int
     }
     consumers_sync();
     const float s = sscale[c];
+    // the codes of fl(B / s) from q = fl(B * rs), rs = fl(1 / s): q and the
+    // quotient differ by less than 2^-22 |q|, so they round alike unless q
+    // lies within 2^-21 |q| of a half-integer (checked for the R values at
+    // once), where the quotient itself is formed; a scale whose reciprocal
+    // is not a normal number always takes the quotient
+    const float rs = quot_rcp(s);
+    const bool rs_ok = rs == rs;
     float fsum = 0.0f;
     // pass 2: codes of the thread's R rows of each box
     for (int b = 0; b < nb2; ++b, ++it) {
@@ -762,16 +769,25 @@ col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int
       uint32_t w[R / 2];
       if (ok) {
         const uint8_t* src = ring + (size_t)st * kCqStageBytes + (size_t)(rg * R) * kCqRowBytes + (size_t)c * sizeof(T);
+        float f[R];
+        bool slow = !rs_ok;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float q = fminf(fmaxf(__fmul_rn(elem_f32(src + r * kCqRowBytes, T()), rs), lo), hi);
+          f[r] = __fsub_rn(__fadd_rn(q, kRoundMagic), kRoundMagic);
+          slow |= fabsf(__fsub_rn(q, f[r])) > __fmaf_rn(fabsf(q), -0x1p-21f, 0.5f);
+        }
+        if (slow) {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float q = fminf(fmaxf(__fdiv_rn(elem_f32(src + r * kCqRowBytes, T()), s), lo), hi);
+            f[r] = __fsub_rn(__fadd_rn(q, kRoundMagic), kRoundMagic);
+          }
+        }
 #pragma unroll
         for (int r = 0; r < R; r += 2) {
-          float f[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float q = fminf(fmaxf(__fdiv_rn(elem_f32(src + (r + h) * kCqRowBytes, T()), s), lo), hi);
-            f[h] = __fsub_rn(__fadd_rn(q, kRoundMagic), kRoundMagic);
-            fsum = __fadd_rn(fsum, f[h]);
-          }
-          w[r / 2] = (__float_as_uint(f[0]) >> 16) | (__float_as_uint(f[1]) & 0xffff0000u);
+          fsum = __fadd_rn(__fadd_rn(fsum, f[r]), f[r + 1]);
+          w[r / 2] = (__float_as_uint(f[r]) >> 16) | (__float_as_uint(f[r + 1]) & 0xffff0000u);
         }
       }
       __syncwarp();
