@@ -88,6 +88,10 @@ TC_CASES = [
     (1, 72, 7, 56, 40, 3, (1, 1, 1, 1)),     # W % 8 == 0 with C not a multiple of 64
     (1, 40, 6, 112, 48, 3, (1, 1, 1, 1)),    # OW 112: two rows per tile, several column rounds
     (2, 37, 5, 56, 40, 3, (1, 1, 1, 1)),     # odd C: a channel pair half in the padding
+    # H % 8 == 0: the input centred in blocks of 8 rows x 64 channels
+    (2, 72, 16, 28, 40, 3, (1, 1, 1, 1)),    # C not a multiple of 64
+    (1, 37, 8, 56, 40, 3, (1, 1, 1, 1)),     # odd C
+    (1, 64, 16, 14, 64, 3, (1, 1, 1, 1)),    # rows of 14 pixels, 8 rows a block
 ]
 
 
