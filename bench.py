@@ -43,8 +43,8 @@ WORKLOAD = ("dynamic quantized GEMM M=8192 K=4096 N=14336: bf16 A quantized per 
 NCU_TRAFFIC = {
     "gemm_tc_pair": {"sources": ["int8_quantized_gb300/csrc/gemm_tc.cu", "int8_quantized_gb300/csrc/tcgen05.cuh",
                                  "int8_quantized_gb300/csrc/common.cuh"],
-                     "sha256": "82b0d94f172358ad233dbaaf2881547df9fde12b706617a0c8ebe655bfd0e565",
-                     "bytes": (566.65 + 220.04) * 1e6,
+                     "sha256": "24a3c853b3c15c1c4b822a55fcaa697092d7a78d56e066ce1e9776e44a9ea737",
+                     "bytes": (380.54 + 222.00) * 1e6,
                      "profile": "profiles/gemm_tc_pair_large_gemm.md"},
 }
 

@@ -639,7 +639,7 @@ constexpr int P_STAGE_BYTES = P_A_STAGE + P_B_STAGE;
 constexpr int P_NUM_BARS = 2 * P_STAGES + 4 + 1;
 constexpr int P_STG_BYTES = NUM_EPI_WARPS * 1024;  // per-warp staging of bf16 C (32 rows x 32 bytes)
 constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + PARAM_BYTES + P_STG_BYTES + P_NUM_BARS * 8 + 16;
-constexpr int P_GROUP_M = 8;
+constexpr int P_GROUP_M = 16;
 constexpr uint32_t IDESC_PAIR = idesc_bf16(PBM, PBN);
 static_assert(P_SMEM_BYTES <= 227 * 1024, "shared memory of the pair kernel");
 
