@@ -139,6 +139,21 @@ def test_nonzero_zero_point(orc, dev):
     assert np.array_equal(Y.cpu().numpy(), ref[0])
 
 
+@pytest.mark.parametrize("H,batch", [(144, 64), (336, 17), (1088, 64)])
+def test_slab_counts(orc, dev, H, batch):
+    """Hidden sizes padded to 3, 6 and 17 slabs of 64 (the last too wide
+    for the persistent kernel's shared memory: one launch per step), whole
+    sequences bit for bit."""
+    w = workloads.lstm(seed=5, T=5, batch=batch, I=64, H=H)
+    Y, Yh, Yc, _, c_out = gpu_lstm(dev, w, "bidirectional", codes=True)
+    ref = orc.dynamic_quantize_lstm(w["X"], w["W"], w["R"], w["B"], w["W_scale"], w["R_scale"],
+                                    direction="bidirectional")
+    assert np.array_equal(Y, ref[0])
+    assert np.array_equal(Yh, ref[1]) and np.array_equal(Yc, ref[2])
+    for d in range(2):
+        assert_codes(orc, c_out, Yh[d], d, batch)
+
+
 def test_full_width_whole_sequence(orc, dev):
     """T=32 of the full-size layer (batch 64, I = H = 1024, bidirectional):
     every output of the whole sequence, bit for bit."""
