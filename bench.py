@@ -43,8 +43,8 @@ WORKLOAD = ("dynamic quantized GEMM M=8192 K=4096 N=14336: bf16 A quantized per 
 NCU_TRAFFIC = {
     "gemm_tc_pair": {"sources": ["int8_quantized_gb300/csrc/gemm_tc.cu", "int8_quantized_gb300/csrc/tcgen05.cuh",
                                  "int8_quantized_gb300/csrc/common.cuh"],
-                     "sha256": "24a3c853b3c15c1c4b822a55fcaa697092d7a78d56e066ce1e9776e44a9ea737",
-                     "bytes": (380.54 + 222.00) * 1e6,
+                     "sha256": "e103875cb5047e60a774d67784cdd1d28d137b8fbf0db579bbfafe36a2bdfb64",
+                     "bytes": (380.33 + 217.93) * 1e6,
                      "profile": "profiles/gemm_tc_pair_large_gemm.md"},
 }
 

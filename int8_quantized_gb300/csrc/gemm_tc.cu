@@ -202,26 +202,30 @@ __device__ __forceinline__ void store_slice(const GemmEpilogue& ep, int64_t row,
 // (row0 .. row0 + 31, lane = row) go out in 16-column chunks through the
 // warp's 1 KB staging buffer (32 rows x 32 bytes, dense), one bulk store
 // per chunk issued by lane 0 once the previous one has read the buffer.
-// Rows and columns past the tensor are clipped by the store itself.
+// Rows and columns past the tensor are clipped by the store itself.  The
+// chunk loop is rolled (the sums shift down by 16 after each chunk, which
+// consumes run[]): the unrolled form's larger code ran 1 % slower.
 template <int ACT>
 __device__ __forceinline__ void store_slice_tma(const CUtensorMap* tmC, int64_t M, int64_t N, int64_t row0,
-                                                int64_t col0, int lane, const int32_t (&run)[SLICE], int32_t zA,
+                                                int64_t col0, int lane, int32_t (&run)[SLICE], int32_t zA,
                                                 float sA, const int32_t* pc, const float* ps, const float* pb,
                                                 uint8_t* stg) {
   const uint32_t stg_s = smem_u32(stg);
-#pragma unroll
+#pragma unroll 1
   for (int ch = 0; ch < SLICE / 16; ++ch) {
     uint32_t wd[8];
 #pragma unroll
     for (int hg = 0; hg < 2; ++hg) {
       float2 o[4];
-      epi8<ACT, true>(run, ch * 16 + hg * 8, zA, sA, pc, ps, pb, o);
+      epi8<ACT, true>(run, hg * 8, zA, sA, pc + ch * 16, ps + ch * 16, pb + ch * 16, o);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const __nv_bfloat162 hv = __float22bfloat162_rn(o[u]);
         wd[hg * 4 + u] = *reinterpret_cast<const uint32_t*>(&hv);
       }
     }
+#pragma unroll
+    for (int i = 0; i < SLICE - 16; ++i) run[i] = run[i + 16];
     if (lane == 0) bulk_wait_read();
     __syncwarp();
     uint4* d = reinterpret_cast<uint4*>(stg + lane * 32);
