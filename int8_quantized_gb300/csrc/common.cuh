@@ -259,8 +259,8 @@ __device__ __forceinline__ float2 gelu_bf16out2(float2 x) {
 //  log1p on [0, 1]: 1 + u = 2^k (1 + v), k in {0, 1}, v in [sqrt(1/2) - 1,
 //        sqrt(2) - 1]; log(1 + v) = 2 atanh(s), s = v / (2 + v), by the
 //        series 2 s (1 + s^2/3 + s^4/5 + s^6/7 + s^8/9).
-//  sigmoid(x) = 1 / (1 + e^-x).  tanh(a) for a = |x|: e / (e + 2) with
-//        e = expm1(2a) below 0.625, 1 - 2 / (e^2a + 1) up to 9.5, 1 above
+//  sigmoid(x) = 1 / (1 + e^-x).  tanh(a) for a = |x|: with e = expm1(2a),
+//        e / (e + 2) below 0.625 and 1 - 2 / (e + 2) up to 9.5, 1 above
 //        (where tanh rounds to 1); the sign of x copied on.
 //  softplus(x) = x + log1p(e^-x) for x > 0, log1p(e^x) otherwise.
 // The constants are the fp32 roundings of the numbers named beside them.
@@ -330,15 +330,16 @@ __device__ __forceinline__ float log1p01(float u) {
 
 __device__ __forceinline__ float sigmoid32(float x) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp32(-x))); }
 
+// tanh(a) = e / (e + 2) = 1 - 2 / (e + 2), e = e^(2a) - 1: the first form
+// below |a| = 0.625, the second up to 9.5, 1 beyond (and for NaN).  One
+// expm1 and one division for every lane, so a warp does not run two forms.
 __device__ __forceinline__ float tanh32(float x) {
   const float a = fabsf(x);
-  float t = 1.0f;
-  if (a < 0.625f) {
-    const float e = expm1_32(__fadd_rn(a, a));
-    t = __fdiv_rn(e, __fadd_rn(e, 2.0f));
-  } else if (a <= 9.5f) {
-    t = __fsub_rn(1.0f, __fdiv_rn(2.0f, __fadd_rn(exp32(__fadd_rn(a, a)), 1.0f)));
-  }
+  const float ac = fminf(a, 9.5f);
+  const float e = expm1_32(__fadd_rn(ac, ac));
+  const bool small = a < 0.625f;
+  const float q = __fdiv_rn(small ? e : 2.0f, __fadd_rn(e, 2.0f));
+  const float t = a <= 9.5f ? (small ? q : __fsub_rn(1.0f, q)) : 1.0f;
   return copysignf(t, x);
 }
 

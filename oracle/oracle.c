@@ -593,14 +593,16 @@ static float ef_log1p01(float u) {
 
 static float ef_sigmoid(float x) { return 1.0f / (1.0f + ef_exp(-x)); }
 
+/* tanh(a) = e / (e + 2) = 1 - 2 / (e + 2) with e = e^(2a) - 1: the first
+   form below |a| = 0.625, the second above (no cancellation in either);
+   1 beyond 9.5, where tanh rounds to 1 in fp32. */
 static float ef_tanh(float x) {
   const float a = fabsf(x);
   float t = 1.0f;
-  if (a < 0.625f) {
+  if (a <= 9.5f) {
     const float e = ef_expm1(a + a);
-    t = e / (e + 2.0f);
-  } else if (a <= 9.5f) {
-    t = 1.0f - 2.0f / (ef_exp(a + a) + 1.0f);
+    const float q = (a < 0.625f ? e : 2.0f) / (e + 2.0f);
+    t = a < 0.625f ? q : 1.0f - q;
   }
   return copysignf(t, x);
 }

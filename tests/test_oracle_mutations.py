@@ -51,8 +51,9 @@ MUTATIONS = {
     "exp_scale_halves_wrong": ("const int n1 = n / 2, n2 = n - n1;\n  return", "const int n1 = n / 2, n2 = n1;\n  return"),
     "expm1_missing_2n_minus_1": ("return fmaf(t, q, t - 1.0f);", "return t * q;"),
     "log1p_range_step_dropped": ("return fmaf(k, EF_LN2_HI, l);", "return l;"),
-    "tanh_large_argument_threshold": ("} else if (a <= 9.5f) {", "} else if (a <= 4.0f) {"),
-    "tanh_small_branch_formula": ("t = e / (e + 2.0f);", "t = e / (e + 1.0f);"),
+    "tanh_large_argument_threshold": ("  if (a <= 9.5f) {", "  if (a <= 4.0f) {"),
+    "tanh_quotient_denominator": ("? e : 2.0f) / (e + 2.0f);", "? e : 2.0f) / (e + 1.0f);"),
+    "tanh_forms_swapped": ("t = a < 0.625f ? q : 1.0f - q;", "t = a < 0.625f ? 1.0f - q : q;"),
     "sigmoid_sign": ("static float ef_sigmoid(float x) { return 1.0f / (1.0f + ef_exp(-x)); }",
                      "static float ef_sigmoid(float x) { return 1.0f / (1.0f + ef_exp(x)); }"),
     "softplus_positive_branch": ("return x > 0.0f ? x + ef_log1p01(ef_exp(-x))", "return x > 0.0f ? ef_log1p01(ef_exp(-x))"),
