@@ -343,6 +343,67 @@ __device__ __forceinline__ float tanh32(float x) {
   return copysignf(t, x);
 }
 
+// Two lanes at once: the same operations as exp32, expm1_32 (for |x| <=
+// 20), sigmoid32 and tanh32 on x.x and x.y, with the multiplies and fused
+// multiply-adds paired (each rounds per lane as its scalar form); sums
+// of two terms are written as fused multiply-adds by 1, which round once as
+// the scalar additions do, and the divisions stay scalar.
+__device__ __forceinline__ float2 exp32x2(float2 x) {
+  x = make_float2(fminf(fmaxf(x.x, -104.0f), 89.0f), fminf(fmaxf(x.y, -104.0f), 89.0f));
+  const float2 t = mul2_rn(x, make_float2(kL2E, kL2E));
+  const float2 nf = make_float2(rintf(t.x), rintf(t.y));
+  const int nx = (int)nf.x, ny = (int)nf.y;
+  const float2 mn = make_float2(-nf.x, -nf.y);
+  float2 r = fma2_rn(mn, make_float2(kLn2Hi, kLn2Hi), x);
+  r = fma2_rn(mn, make_float2(kLn2Lo, kLn2Lo), r);
+  float2 p = fma2_rn(make_float2(0x1.a01a02p-13f, 0x1.a01a02p-13f), r, make_float2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
+  p = fma2_rn(p, r, make_float2(0x1.111112p-7f, 0x1.111112p-7f));
+  p = fma2_rn(p, r, make_float2(0x1.555556p-5f, 0x1.555556p-5f));
+  p = fma2_rn(p, r, make_float2(0x1.555556p-3f, 0x1.555556p-3f));
+  p = fma2_rn(p, r, make_float2(0.5f, 0.5f));
+  p = fma2_rn(p, r, make_float2(1.0f, 1.0f));
+  p = fma2_rn(p, r, make_float2(1.0f, 1.0f));
+  const int n1x = nx / 2, n2x = nx - n1x, n1y = ny / 2, n2y = ny - n1y;
+  return mul2_rn(mul2_rn(p, make_float2(pow2i(n1x), pow2i(n1y))), make_float2(pow2i(n2x), pow2i(n2y)));
+}
+
+__device__ __forceinline__ float2 expm1_32x2(float2 x) {  // |x.x|, |x.y| <= 20
+  const float2 t = mul2_rn(x, make_float2(kL2E, kL2E));
+  const float2 nf = make_float2(rintf(t.x), rintf(t.y));
+  const int nx = (int)nf.x, ny = (int)nf.y;
+  const float2 mn = make_float2(-nf.x, -nf.y);
+  float2 r = fma2_rn(mn, make_float2(kLn2Hi, kLn2Hi), x);
+  r = fma2_rn(mn, make_float2(kLn2Lo, kLn2Lo), r);
+  float2 q = fma2_rn(make_float2(0x1.a01a02p-16f, 0x1.a01a02p-16f), r, make_float2(0x1.a01a02p-13f, 0x1.a01a02p-13f));
+  q = fma2_rn(q, r, make_float2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
+  q = fma2_rn(q, r, make_float2(0x1.111112p-7f, 0x1.111112p-7f));
+  q = fma2_rn(q, r, make_float2(0x1.555556p-5f, 0x1.555556p-5f));
+  q = fma2_rn(q, r, make_float2(0x1.555556p-3f, 0x1.555556p-3f));
+  q = fma2_rn(q, r, make_float2(0.5f, 0.5f));
+  q = fma2_rn(q, r, make_float2(1.0f, 1.0f));
+  q = mul2_rn(q, r);
+  const float2 s = make_float2(pow2i(nx), pow2i(ny));
+  const float2 v = fma2_rn(s, q, make_float2(__fsub_rn(s.x, 1.0f), __fsub_rn(s.y, 1.0f)));
+  return make_float2(nx == 0 ? q.x : v.x, ny == 0 ? q.y : v.y);
+}
+
+__device__ __forceinline__ float2 sigmoid32x2(float2 x) {
+  const float2 d = fma2_rn(exp32x2(make_float2(-x.x, -x.y)), make_float2(1.0f, 1.0f), make_float2(1.0f, 1.0f));
+  return make_float2(__fdiv_rn(1.0f, d.x), __fdiv_rn(1.0f, d.y));
+}
+
+__device__ __forceinline__ float2 tanh32x2(float2 x) {
+  const float2 a = make_float2(fabsf(x.x), fabsf(x.y));
+  const float2 ac = make_float2(fminf(a.x, 9.5f), fminf(a.y, 9.5f));
+  const float2 e = expm1_32x2(mul2_rn(ac, make_float2(2.0f, 2.0f)));  // ac + ac, exactly
+  const float2 d = fma2_rn(e, make_float2(1.0f, 1.0f), make_float2(2.0f, 2.0f));
+  const bool sx = a.x < 0.625f, sy = a.y < 0.625f;
+  const float qx = __fdiv_rn(sx ? e.x : 2.0f, d.x), qy = __fdiv_rn(sy ? e.y : 2.0f, d.y);
+  const float tx = a.x <= 9.5f ? (sx ? qx : __fsub_rn(1.0f, qx)) : 1.0f;
+  const float ty = a.y <= 9.5f ? (sy ? qy : __fsub_rn(1.0f, qy)) : 1.0f;
+  return make_float2(copysignf(tx, x.x), copysignf(ty, x.y));
+}
+
 __device__ __forceinline__ float softplus32(float x) {
   return x > 0.0f ? __fadd_rn(x, log1p01(exp32(-x))) : log1p01(exp32(x));
 }

@@ -251,6 +251,60 @@ __device__ __forceinline__ void dw_cp_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// The code of fl(v / y_scale) when the reciprocal product q = fl(v * yr)
+// may round differently (near a half-integer, or no usable reciprocal);
+// otherwise the code already formed.  Kept out of line: it runs rarely.
+__device__ __noinline__ uint32_t dw_code_checked(float v, float yr, bool rcp_ok, float y_scale, float lo_z, float hi_z,
+                                                 int y_zp, uint32_t code) {
+  const float q = __fmul_rn(v, yr);
+  const float cq = fminf(fmaxf(q, lo_z), hi_z);
+  const float d = __fsub_rn(cq, __fsub_rn(__fadd_rn(cq, 12582912.0f), 12582912.0f));
+  if (!rcp_ok || fabsf(d) > __fmaf_rn(fabsf(cq), -0x1p-21f, 0.5f))
+    return rint_code_bits(__fdiv_rn(v, y_scale), lo_z, hi_z, y_zp);
+  return code;
+}
+
+// Requantize the 8 sums of an output row (av: the exact int32 sums as
+// floats, rounded as __int2float_rn) and store the codes at out (one
+// 8-byte store when vec, else the first min(n, 8) bytes).
+template <typename YT>
+__device__ __forceinline__ void dw_requant_store(const float (&av)[kStrip], float mul, float yr, bool rcp_ok,
+                                                 float y_scale, float lo_z, float hi_z, int y_zp, YT* out, bool vec,
+                                                 int n) {
+  uint32_t code[kStrip];
+  float vv[kStrip];
+  bool slow = !rcp_ok;
+#pragma unroll
+  for (int e = 0; e < kStrip; e += 2) {
+    const float2 v = mul2_rn(make_float2(av[e], av[e + 1]), make_float2(mul, mul));
+    const float2 q = mul2_rn(v, make_float2(yr, yr));
+    vv[e] = v.x;
+    vv[e + 1] = v.y;
+    const float qq[2] = {q.x, q.y};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float cq = fminf(fmaxf(qq[h], lo_z), hi_z);
+      const float r1 = __fadd_rn(cq, 12582912.0f);
+      const float d = __fsub_rn(cq, __fsub_rn(r1, 12582912.0f));
+      code[e + h] = (uint32_t)(__float_as_int(r1) + y_zp);
+      slow |= fabsf(d) > __fmaf_rn(fabsf(cq), -0x1p-21f, 0.5f);
+    }
+  }
+  if (slow) {
+    // near a half-integer (or no usable reciprocal): the quotient itself
+#pragma unroll
+    for (int e = 0; e < kStrip; ++e) code[e] = dw_code_checked(vv[e], yr, rcp_ok, y_scale, lo_z, hi_z, y_zp, code[e]);
+  }
+  if (vec) {
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]),
+                                                pack_low_bytes(code[4], code[5], code[6], code[7]));
+  } else {
+#pragma unroll
+    for (int e = 0; e < kStrip; ++e)
+      if (e < n) out[e] = (YT)code[e];
+  }
+}
+
 // Persistent: CTA b takes the groups of `ppc` consecutive planes b, b +
 // gridDim.x, ...; two shared buffers, the next group's planes copied in
 // (cp.async, 8- or 4-byte pieces) while the current one is computed.  The
@@ -346,13 +400,11 @@ qlinearconv_depthwise_rows(const XT* __restrict__ x, const WT* __restrict__ w, c
   for (int k = 0; grp < ngroups; ++k, grp += gridDim.x) {
     const int bi = k & 1;
     const int nxt = grp + (int)gridDim.x;
-    if (nxt < ngroups) {
-      stage(nxt, bi ^ 1);
-      dw_cp_wait<1>();
-    } else {
-      dw_cp_wait<0>();
-    }
-    __syncthreads();  // this group's planes and constants are in
+    dw_cp_wait<0>();  // this group's copies, the only ones in flight
+    // this group's planes and constants are in, and every thread is done
+    // with the previous group, whose buffer the next group's copies take
+    __syncthreads();
+    if (nxt < ngroups) stage(nxt, bi ^ 1);
     const int p0 = grp * ppc, np = min(ppc, planes - p0);
     const uint32_t* buf = smw + bi * buf_words;
     const DwPlane<KS>* prm = prm_base + bi * ppc;
@@ -413,51 +465,15 @@ qlinearconv_depthwise_rows(const XT* __restrict__ x, const WT* __restrict__ w, c
           }
           if (kh == KS - 1 && oh0 + o < OH) {
             // output row oh0 + o is complete: requantize and store its 8 codes
-            uint32_t code[kStrip];
-            float vv[kStrip];
-            bool slow = !rcp_ok;
+            float av[kStrip];
 #pragma unroll
-            for (int e = 0; e < kStrip; e += 2) {
-              const float2 v = mul2_rn(make_float2(__int2float_rn(acc[o][e]), __int2float_rn(acc[o][e + 1])),
-                                       make_float2(mul, mul));
-              const float2 q = mul2_rn(v, make_float2(yr, yr));
-              vv[e] = v.x;
-              vv[e + 1] = v.y;
-              const float qq[2] = {q.x, q.y};
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const float cq = fminf(fmaxf(qq[h], lo_z), hi_z);
-                const float r1 = __fadd_rn(cq, 12582912.0f);
-                const float d = __fsub_rn(cq, __fsub_rn(r1, 12582912.0f));
-                code[e + h] = (uint32_t)(__float_as_int(r1) + y_zp);
-                slow |= fabsf(d) > __fmaf_rn(fabsf(cq), -0x1p-21f, 0.5f);
-              }
-            }
-            if (slow) {
-              // near a half-integer (or no usable reciprocal): the quotient itself
-#pragma unroll
-              for (int e = 0; e < kStrip; ++e) {
-                const float q = __fmul_rn(vv[e], yr);
-                const float cq = fminf(fmaxf(q, lo_z), hi_z);
-                const float d = __fsub_rn(cq, __fsub_rn(__fadd_rn(cq, 12582912.0f), 12582912.0f));
-                if (!rcp_ok || fabsf(d) > __fmaf_rn(fabsf(cq), -0x1p-21f, 0.5f))
-                  code[e] = rint_code_bits(__fdiv_rn(vv[e], y_scale), lo_z, hi_z, y_zp);
-              }
-            }
-            YT* out = yp + (int64_t)(oh0 + o) * OW;
-            if (vec) {
-              *reinterpret_cast<uint2*>(out) = make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]),
-                                                          pack_low_bytes(code[4], code[5], code[6], code[7]));
-            } else {
-#pragma unroll
-              for (int e = 0; e < kStrip; ++e)
-                if (ow0 + e < OW) out[e] = (YT)code[e];
-            }
+            for (int e = 0; e < kStrip; ++e) av[e] = __int2float_rn(acc[o][e]);
+            dw_requant_store(av, mul, yr, rcp_ok, y_scale, lo_z, hi_z, y_zp, yp + (int64_t)(oh0 + o) * OW, vec,
+                             OW - ow0);
           }
         }
       }
     }
-    __syncthreads();  // the buffer is read before the copies into it two groups on
   }
 }
 

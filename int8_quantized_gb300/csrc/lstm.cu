@@ -1045,11 +1045,36 @@ lstm_persist_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
           pre[i] = __fadd_rn(gx[i], gh);
         }
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
+        if (!VAR) {
+          // the two units' gates in pairs (the per-lane operations of sigmoid32 and tanh32)
+          float gi[2], go[2], gf[2], gc[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int c0 = col0 + 4 * k;  // gate columns of unit k: i, o, f, c
+            gi[k] = __fadd_rn(__fadd_rn(pre[4 * k], cst[2][c0]), cst[3][c0]);
+            go[k] = __fadd_rn(__fadd_rn(pre[4 * k + 1], cst[2][c0 + 1]), cst[3][c0 + 1]);
+            gf[k] = __fadd_rn(__fadd_rn(pre[4 * k + 2], cst[2][c0 + 2]), cst[3][c0 + 2]);
+            gc[k] = __fadd_rn(__fadd_rn(pre[4 * k + 3], cst[2][c0 + 3]), cst[3][c0 + 3]);
+          }
+          const float2 ig = ef::sigmoid32x2(make_float2(gi[0], gi[1]));
+          const float2 og = ef::sigmoid32x2(make_float2(go[0], go[1]));
+          const float2 fg = ef::sigmoid32x2(make_float2(gf[0], gf[1]));
+          const float2 ct = ef::tanh32x2(make_float2(gc[0], gc[1]));
+          const float cn0 = __fadd_rn(__fmul_rn(fg.x, cp[0]), __fmul_rn(ig.x, ct.x));
+          const float cn1 = __fadd_rn(__fmul_rn(fg.y, cp[1]), __fmul_rn(ig.y, ct.y));
+          const float2 th = ef::tanh32x2(make_float2(cn0, cn1));
+          hn[0] = __fmul_rn(og.x, th.x);
+          hn[1] = __fmul_rn(og.y, th.y);
+          cp[0] = cn0;
+          cp[1] = cn1;
+        }
+#pragma unroll
+        for (int k = 0; k < 2 && VAR; ++k) {
+          // the general form: peepholes, clip, coupled gates, the activation list
           const int c0 = col0 + 4 * k;  // gate columns of unit k: i, o, f, c
           float si = pre[4 * k], so = pre[4 * k + 1], sf = pre[4 * k + 2], sc = pre[4 * k + 3];
           float cn, og;
-          if (VAR) {
+          {
             const int ul = 4 * cg + 2 * hi + k;
             if (p.P) {
               si = __fadd_rn(si, __fmul_rn(pw[0][ul], cp[k]));
@@ -1068,13 +1093,6 @@ lstm_persist_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
             if (p.P) so = __fadd_rn(so, __fmul_rn(pw[1][ul], cn));
             og = ef::lstm_act(fk, fa, fb, clip_gate(__fadd_rn(__fadd_rn(so, cst[2][c0 + 1]), cst[3][c0 + 1]), p.clip));
             hn[k] = __fmul_rn(og, ef::lstm_act(p.acts.kind[d][2], p.acts.alpha[d][2], p.acts.beta[d][2], cn));
-          } else {
-            const float ig = sigmoid32(__fadd_rn(__fadd_rn(si, cst[2][c0]), cst[3][c0]));
-            og = sigmoid32(__fadd_rn(__fadd_rn(so, cst[2][c0 + 1]), cst[3][c0 + 1]));
-            const float fg = sigmoid32(__fadd_rn(__fadd_rn(sf, cst[2][c0 + 2]), cst[3][c0 + 2]));
-            const float ct = tanh32(__fadd_rn(__fadd_rn(sc, cst[2][c0 + 3]), cst[3][c0 + 3]));
-            cn = __fadd_rn(__fmul_rn(fg, cp[k]), __fmul_rn(ig, ct));
-            hn[k] = __fmul_rn(og, tanh32(cn));
           }
           cp[k] = cn;
         }

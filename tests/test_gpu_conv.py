@@ -175,12 +175,20 @@ DW_CASES = [
 ]
 
 
-@pytest.mark.parametrize("kernel", ["rows", "halo"])
+def force_dw_kernel(monkeypatch, kernel):
+    """rows: the persistent row kernel; halo: the halo-tile kernel."""
+    if kernel == "halo":
+        monkeypatch.setenv("I8Q_FORCE_CONV_HALO", "1")
+
+
+DW_KERNELS = ["rows", "halo"]
+
+
+@pytest.mark.parametrize("kernel", DW_KERNELS)
 @pytest.mark.parametrize("case", DW_CASES)
 @pytest.mark.parametrize("types", [("u8", "u8", "u8"), ("s8", "s8", "s8"), ("u8", "s8", "s8")])
 def test_depthwise_kernels(orc, dev, monkeypatch, kernel, case, types):
-    if kernel == "halo":
-        monkeypatch.setenv("I8Q_FORCE_CONV_HALO", "1")
+    force_dw_kernel(monkeypatch, kernel)
     N, C, H, W, k, pads = case
     rng = np.random.default_rng(N * 100 + C * 10 + k)
     rg = {"u8": (0, 256, np.uint8), "s8": (-128, 128, np.int8)}
@@ -194,15 +202,14 @@ def test_depthwise_kernels(orc, dev, monkeypatch, kernel, case, types):
              int(rng.integers(yt[0], yt[1])), B, pads, group=C, ytype=types[2])
 
 
-@pytest.mark.parametrize("kernel", ["rows", "halo"])
+@pytest.mark.parametrize("kernel", DW_KERNELS)
 @pytest.mark.parametrize("ys", [2.0, 0.5, 3.0, 0.1, 1e-30, 1e30, 3e38])
 def test_depthwise_requantization_ties(orc, dev, monkeypatch, kernel, ys):
     """Unit input and filter scales make every rescaled sum an integer, so
     y_scale 2 puts half the quotients exactly on a tie (round half to even
     decides them); the other scales give exact, inexact, saturating,
     vanishing quotients and one whose reciprocal is not a normal number."""
-    if kernel == "halo":
-        monkeypatch.setenv("I8Q_FORCE_CONV_HALO", "1")
+    force_dw_kernel(monkeypatch, kernel)
     rng = np.random.default_rng(int(ys * 7) % 1000 if ys < 1e3 else 5)
     N, C, H, W, k = 2, 6, 20, 24, 3
     x = rng.integers(0, 16, (N, C, H, W)).astype(np.uint8)
@@ -210,3 +217,24 @@ def test_depthwise_requantization_ties(orc, dev, monkeypatch, kernel, ys):
     B = rng.integers(-50, 51, C).astype(np.int32)
     run_conv(orc, dev, x, np.float32(1.0), 3, w, np.ones(C, np.float32), np.zeros(C, np.int64), np.float32(ys), 0, B,
              (1, 1, 1, 1), group=C, ytype="s8")
+
+
+@pytest.mark.parametrize("kernel", DW_KERNELS)
+@pytest.mark.parametrize("types", [("u8", "u8", "u8"), ("s8", "s8", "s8")])
+def test_depthwise_large_bias(orc, dev, monkeypatch, kernel, types):
+    """Biases around 2^24 and 2^30: int32 sums whose conversion to fp32
+    rounds, with unit scales and y_scale 2^17 so that the codes still move
+    with the tap sums."""
+    force_dw_kernel(monkeypatch, kernel)
+    rng = np.random.default_rng(11)
+    rg = {"u8": (0, 256, np.uint8), "s8": (-128, 128, np.int8)}
+    xt, wt, yt = (rg[t] for t in types)
+    N, C, H, W, k = 2, 8, 19, 24, 3
+    x = rng.integers(xt[0], xt[1], (N, C, H, W)).astype(xt[2])
+    w = rng.integers(wt[0], wt[1], (C, 1, k, k)).astype(wt[2])
+    wz = rng.integers(wt[0], wt[1], C)
+    B = np.array([2 ** 24, -2 ** 24, 2 ** 24 - 2 ** 21, -(2 ** 24 - 2 ** 21), 2 ** 24 - 2 ** 21 + 1, 2 ** 30,
+                  -2 ** 30, 12345], np.int32)
+    # unit scales and y_scale 2^17: codes near +-128 that move with the tap sums
+    run_conv(orc, dev, x, np.float32(1.0), int(rng.integers(xt[0], xt[1])), w, np.ones(C, np.float32), wz,
+             np.float32(2.0 ** 17), 128 if types[2] == "u8" else 0, B, (1, 1, 1, 1), group=C, ytype=types[2])
