@@ -193,7 +193,47 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
       int chunk = 0;
       bool ok = true;
       uint32_t d = tmem_base;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      if (KT % STAGES == 0) {
+        // every tile starts at stage 0: the K loop unrolled by the ring's
+        // length, so that each stage's descriptors are the base plus a
+        // constant and the stage index is static (a leaner issue loop)
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+          int kc = 0;
+          for (int kt0 = 0; ok && kt0 < KT; kt0 += STAGES) {
+#pragma unroll
+            for (int j = 0; j < STAGES; ++j) {
+              if (kc == 0) {
+                const int b = chunk & 1;
+                if (!wait_bar(acce(b), ((uint32_t)(chunk >> 1) & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT_MMA)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                d = tmem_base + (uint32_t)(b * TN);
+              }
+              if (!wait_bar(full(j), ph, abort_flag, p.status, ST_TIMEOUT_MMA)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t soff = (uint64_t)(((uint32_t)j * (uint32_t)T::STAGE_BYTES) >> 4);
+              const uint32_t acc = kc == 0 ? 0u : 1u;
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k)
+                tc_mma(d, adesc0 + soff + (uint64_t)(2 * k), bdesc0 + soff + (uint64_t)(2 * k), IDESC,
+                       (k == 0) ? acc : 1u);
+              tc_commit(empty(j));
+              if (++kc == CS || kt0 + j == KT - 1) {
+                tc_commit(accf(chunk & 1));
+                ++chunk;
+                kc = 0;
+              }
+            }
+            ph ^= 1u;
+          }
+        }
+      }
+      for (int tile = blockIdx.x; ok && KT % STAGES != 0 && tile < p.num_tiles; tile += gridDim.x) {
         int kc = 0;
         for (int kt = 0; kt < KT; ++kt) {
           if (kc == 0) {
