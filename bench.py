@@ -43,8 +43,8 @@ WORKLOAD = ("dynamic quantized GEMM M=8192 K=4096 N=14336: bf16 A quantized per 
 NCU_TRAFFIC = {
     "gemm_tc_pair": {"sources": ["int8_quantized_gb300/csrc/gemm_tc.cu", "int8_quantized_gb300/csrc/tcgen05.cuh",
                                  "int8_quantized_gb300/csrc/common.cuh"],
-                     "sha256": "47713938b9cb57f9363f6321815b3c9b60d062a87b18775b9b43d7576d14eb3e",
-                     "bytes": (379.96 + 218.39) * 1e6,
+                     "sha256": "a29e7612bd5d9427493364716c1b1603eecd0975a1406497b61ed49f9ba4d496",
+                     "bytes": (354.62 + 221.32) * 1e6,
                      "profile": "profiles/gemm_tc_pair_large_gemm.md"},
 }
 
