@@ -632,7 +632,8 @@ col_quant_wide(const T* __restrict__ B, int64_t K, int64_t N, int64_t Kp, const 
 // A persistent CTA owns a strip of 64 bytes of every row of B (16 fp32 or
 // 32 bf16 columns).  One thread streams the strip through an 8-stage ring of
 // 256-row TMA boxes twice: first for max|B| per column, then -- from L2: a
-// strip per SM is 0.25 MB at K = 4096 -- for the codes.  Each consumer
+// strip per SM is 0.25 MB at K = 4096 -- for the codes; the second pass of
+// a strip runs box by box alongside the first pass of the CTA's next strip.  Each consumer
 // thread owns one column and a run of R adjacent rows of every box (8 for
 // fp32, 16 for bf16), reads it down the column in shared memory and writes
 // its R codes, contiguous along K, straight to the transposed outputs.  Rows
@@ -648,12 +649,6 @@ constexpr int kCqBoxRows = 256, kCqStages = 8, kCqStageBytes = kCqBoxRows * kCqR
 constexpr size_t kCqSmem = 1024 + (size_t)kCqStages * kCqStageBytes + 2 * kCqStages * 8 + 16;
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 constexpr uint32_t ST_TIMEOUT_COLS = 1u << 13;
-
-// int8 code of a bf16 code held in the high half of a word (an exact small
-// integer): the low byte of code + 1.5 * 2^23.
-__device__ __forceinline__ uint32_t code_byte(uint32_t bf16_bits_high) {
-  return (uint32_t)__float_as_int(__fadd_rn(__uint_as_float(bf16_bits_high), kRoundMagic)) & 0xffu;
-}
 
 __device__ __forceinline__ float elem_f32(const uint8_t* p, float) { return *reinterpret_cast<const float*>(p); }
 __device__ __forceinline__ float elem_f32(const uint8_t* p, __nv_bfloat16) {
@@ -694,19 +689,36 @@ col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int64_t strip = blockIdx.x; ok && strip < nstrips; strip += gridDim.x)
-        for (int b = 0; ok && b < nb1 + nb2; ++b, ++it) {
-          const uint32_t st = it % kCqStages;
-          if (it >= (uint32_t)kCqStages &&
-              !tc::wait_bar(tc::smem_u32(empty + st), ((it / kCqStages) - 1) & 1u, abort_flag, status, ST_TIMEOUT_COLS)) {
-            ok = false;
-            break;
-          }
-          const int y = (b < nb1 ? b : b - nb1) * kCqBoxRows;
-          tc::mbar_arrive_expect_tx(tc::smem_u32(full + st), (uint32_t)kCqStageBytes);
-          tc::tma_load_2d(tc::smem_u32(ring + (size_t)st * kCqStageBytes), &tmB, tc::smem_u32(full + st),
-                          (int)(strip * W), y);
+      // a strip's second pass reads its lines for the last time
+      const uint64_t drop = tc::policy_evict_first();
+      auto load = [&](int64_t strip, int b, bool first_pass) {
+        const uint32_t st = it % kCqStages;
+        if (it >= (uint32_t)kCqStages &&
+            !tc::wait_bar(tc::smem_u32(empty + st), ((it / kCqStages) - 1) & 1u, abort_flag, status, ST_TIMEOUT_COLS)) {
+          ok = false;
+          return;
         }
+        tc::mbar_arrive_expect_tx(tc::smem_u32(full + st), (uint32_t)kCqStageBytes);
+        if (first_pass)
+          tc::tma_load_2d(tc::smem_u32(ring + (size_t)st * kCqStageBytes), &tmB, tc::smem_u32(full + st),
+                          (int)(strip * W), b * kCqBoxRows);
+        else
+          tc::tma_load_2d_hint(tc::smem_u32(ring + (size_t)st * kCqStageBytes), &tmB, tc::smem_u32(full + st),
+                               (int)(strip * W), b * kCqBoxRows, drop);
+        ++it;
+      };
+      // the boxes in the consumers' order: the first strip's max pass, then
+      // each strip's code pass interleaved box by box with the next strip's
+      // max pass
+      for (int b = 0; ok && b < nb1 && (int64_t)blockIdx.x < nstrips; ++b) load(blockIdx.x, b, true);
+      for (int64_t strip = blockIdx.x; ok && strip < nstrips; strip += gridDim.x) {
+        const int64_t nxt = strip + gridDim.x;
+        const int nbm = nxt < nstrips ? nb1 : 0;
+        for (int b = 0; ok && b < (nb2 > nbm ? nb2 : nbm); ++b) {
+          if (b < nb2) load(strip, b, false);
+          if (ok && b < nbm) load(nxt, b, true);
+        }
+      }
       // the copies in flight land before the CTA leaves (bounded)
       const uint32_t first = it > (uint32_t)kCqStages ? it - kCqStages : 0u;
       for (uint32_t i = first; i < it; ++i) {
@@ -726,21 +738,104 @@ col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int
   uint32_t it = 0;
   bool ok = true;
   auto consumers_sync = [] { asm volatile("bar.sync 1, %0;\n" ::"n"(kCqConsumers) : "memory"); };
+  // max |B| of this thread's column over its rows of the next box
+  auto max_box = [&](float& m) {
+    const uint32_t st = it % kCqStages;
+    if (ok) ok = tc::wait_bar(tc::smem_u32(full + st), (it / kCqStages) & 1u, abort_flag, status, ST_TIMEOUT_COLS);
+    if (ok) {
+      const uint8_t* src = ring + (size_t)st * kCqStageBytes + (size_t)(rg * R) * kCqRowBytes + (size_t)c * sizeof(T);
+#pragma unroll
+      for (int r = 0; r < R; ++r) m = fmaxf(m, fabsf(elem_f32(src + r * kCqRowBytes, T())));
+    }
+    __syncwarp();
+    if (ok && lane == 0) tc::mbar_arrive(tc::smem_u32(empty + st));
+    ++it;
+  };
+  // the codes of this thread's R rows of the next box (box b of column j)
+  // from q = fl(B * rs), rs = fl(1 / s): q and the quotient fl(B / s) differ
+  // by less than 2^-22 |q|, so they round alike unless q lies within
+  // 2^-21 |q| of a half-integer (checked for the R values at once), where
+  // the quotient itself is formed; a scale whose reciprocal is not a normal
+  // number always takes the quotient
+  auto code_box = [&](int64_t j, int b, float s, float rs, bool rs_ok, float& fsum) {
+    const uint32_t st = it % kCqStages;
+    if (ok) ok = tc::wait_bar(tc::smem_u32(full + st), (it / kCqStages) & 1u, abort_flag, status, ST_TIMEOUT_COLS);
+    uint32_t w[R / 2], o[R / 4];
+    if (ok) {
+      const uint8_t* src = ring + (size_t)st * kCqStageBytes + (size_t)(rg * R) * kCqRowBytes + (size_t)c * sizeof(T);
+      // rr = code + 1.5 * 2^23 (the code in its low byte, two's complement),
+      // ff = the code as an exact float; pairs on the paired fp32 pipe (an
+      // fma by 1 rounds once, as the addition does)
+      float2 rr[R / 2], ff[R / 2];
+      bool slow = !rs_ok;
+#pragma unroll
+      for (int r = 0; r < R; r += 2) {
+        float2 q = mul2_rn(make_float2(elem_f32(src + r * kCqRowBytes, T()), elem_f32(src + (r + 1) * kCqRowBytes, T())),
+                           make_float2(rs, rs));
+        q = make_float2(fminf(fmaxf(q.x, lo), hi), fminf(fmaxf(q.y, lo), hi));
+        rr[r / 2] = fma2_rn(q, make_float2(1.0f, 1.0f), make_float2(kRoundMagic, kRoundMagic));
+        ff[r / 2] = fma2_rn(rr[r / 2], make_float2(1.0f, 1.0f), make_float2(-kRoundMagic, -kRoundMagic));
+        const float2 d = fma2_rn(ff[r / 2], make_float2(-1.0f, -1.0f), q);  // q - code, exact
+        // |q| <= 128, so 0.5 - 2^-21 |q| >= 0.5 - 2^-14: a constant bound
+        // that flags every near tie (and a few more)
+        slow |= fabsf(d.x) > 0.5f - 0x1p-14f || fabsf(d.y) > 0.5f - 0x1p-14f;
+      }
+      if (slow) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float q = fminf(fmaxf(__fdiv_rn(elem_f32(src + r * kCqRowBytes, T()), s), lo), hi);
+          const float r1 = __fadd_rn(q, kRoundMagic);
+          if (r & 1) {
+            rr[r / 2].y = r1;
+            ff[r / 2].y = __fsub_rn(r1, kRoundMagic);
+          } else {
+            rr[r / 2].x = r1;
+            ff[r / 2].x = __fsub_rn(r1, kRoundMagic);
+          }
+        }
+      }
+      float2 fs2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int r = 0; r < R; r += 2) {
+        fs2 = fma2_rn(ff[r / 2], make_float2(1.0f, 1.0f), fs2);  // exact integer sums
+        w[r / 2] = __byte_perm(__float_as_uint(ff[r / 2].x), __float_as_uint(ff[r / 2].y), 0x7632);
+      }
+      fsum = __fadd_rn(fsum, __fadd_rn(fs2.x, fs2.y));
+#pragma unroll
+      for (int e = 0; e < R / 4; ++e)
+        o[e] = pack_low_bytes(__float_as_uint(rr[2 * e].x), __float_as_uint(rr[2 * e].y),
+                              __float_as_uint(rr[2 * e + 1].x), __float_as_uint(rr[2 * e + 1].y));
+    }
+    __syncwarp();
+    if (ok && lane == 0) tc::mbar_arrive(tc::smem_u32(empty + st));
+    ++it;
+    const int64_t k = (int64_t)b * kCqBoxRows + rg * R;
+    if (ok && j < N && k < Kp) {
+      if (iBt_bf16) {
+        uint4* d = reinterpret_cast<uint4*>(iBt_bf16 + j * Kp + k);
+#pragma unroll
+        for (int q = 0; q < R / 8; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      }
+      if (iBt) {  // streaming stores: the product reads the bf16 copy, not these
+        if constexpr (R % 16 == 0) {
+          uint4* d = reinterpret_cast<uint4*>(iBt + j * Kp + k);
+#pragma unroll
+          for (int q = 0; q < R / 16; ++q) __stcs(d + q, make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
+        } else {
+          uint2* d = reinterpret_cast<uint2*>(iBt + j * Kp + k);
+#pragma unroll
+          for (int q = 0; q < R / 8; ++q) __stcs(d + q, make_uint2(o[2 * q], o[2 * q + 1]));
+        }
+      }
+    }
+  };
+  // pass 1 of the first strip, then each strip's pass 2 interleaved box by
+  // box with the next strip's pass 1, so that every CTA keeps reading new
+  // rows from DRAM while it codes the strip it has in L2
+  float m = 0.0f;
+  for (int b = 0; b < nb1 && (int64_t)blockIdx.x < nstrips; ++b) max_box(m);
   for (int64_t strip = blockIdx.x; strip < nstrips; strip += gridDim.x) {
     const int64_t j = strip * W + c;
-    // pass 1: max |B| of this column over the thread's rows
-    float m = 0.0f;
-    for (int b = 0; b < nb1; ++b, ++it) {
-      const uint32_t st = it % kCqStages;
-      if (ok) ok = tc::wait_bar(tc::smem_u32(full + st), (it / kCqStages) & 1u, abort_flag, status, ST_TIMEOUT_COLS);
-      if (ok) {
-        const uint8_t* src = ring + (size_t)st * kCqStageBytes + (size_t)(rg * R) * kCqRowBytes + (size_t)c * sizeof(T);
-#pragma unroll
-        for (int r = 0; r < R; ++r) m = fmaxf(m, fabsf(elem_f32(src + r * kCqRowBytes, T())));
-      }
-      __syncwarp();
-      if (ok && lane == 0) tc::mbar_arrive(tc::smem_u32(empty + st));
-    }
     red[rg][c] = m;
     consumers_sync();
     if (tid < W) {
@@ -753,71 +848,16 @@ col_quant_tma(const __grid_constant__ CUtensorMap tmB, int64_t K, int64_t N, int
       if (ok && strip * W + tid < N) scaleB[strip * W + tid] = sv;
     }
     consumers_sync();
-    const float s = sscale[c];
-    // the codes of fl(B / s) from q = fl(B * rs), rs = fl(1 / s): q and the
-    // quotient differ by less than 2^-22 |q|, so they round alike unless q
-    // lies within 2^-21 |q| of a half-integer (checked for the R values at
-    // once), where the quotient itself is formed; a scale whose reciprocal
-    // is not a normal number always takes the quotient
-    const float rs = quot_rcp(s);
+    const float sc = sscale[c];
+    const float rs = quot_rcp(sc);
     const bool rs_ok = rs == rs;
     float fsum = 0.0f;
-    // pass 2: codes of the thread's R rows of each box
-    for (int b = 0; b < nb2; ++b, ++it) {
-      const uint32_t st = it % kCqStages;
-      if (ok) ok = tc::wait_bar(tc::smem_u32(full + st), (it / kCqStages) & 1u, abort_flag, status, ST_TIMEOUT_COLS);
-      uint32_t w[R / 2];
-      if (ok) {
-        const uint8_t* src = ring + (size_t)st * kCqStageBytes + (size_t)(rg * R) * kCqRowBytes + (size_t)c * sizeof(T);
-        float f[R];
-        bool slow = !rs_ok;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float q = fminf(fmaxf(__fmul_rn(elem_f32(src + r * kCqRowBytes, T()), rs), lo), hi);
-          f[r] = __fsub_rn(__fadd_rn(q, kRoundMagic), kRoundMagic);
-          slow |= fabsf(__fsub_rn(q, f[r])) > __fmaf_rn(fabsf(q), -0x1p-21f, 0.5f);
-        }
-        if (slow) {
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const float q = fminf(fmaxf(__fdiv_rn(elem_f32(src + r * kCqRowBytes, T()), s), lo), hi);
-            f[r] = __fsub_rn(__fadd_rn(q, kRoundMagic), kRoundMagic);
-          }
-        }
-#pragma unroll
-        for (int r = 0; r < R; r += 2) {
-          fsum = __fadd_rn(__fadd_rn(fsum, f[r]), f[r + 1]);
-          w[r / 2] = (__float_as_uint(f[r]) >> 16) | (__float_as_uint(f[r + 1]) & 0xffff0000u);
-        }
-      }
-      __syncwarp();
-      if (ok && lane == 0) tc::mbar_arrive(tc::smem_u32(empty + st));
-      const int64_t k = (int64_t)b * kCqBoxRows + rg * R;
-      if (ok && j < N && k < Kp) {
-        if (iBt_bf16) {
-          uint4* d = reinterpret_cast<uint4*>(iBt_bf16 + j * Kp + k);
-#pragma unroll
-          for (int q = 0; q < R / 8; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-        }
-        if (iBt) {
-          uint32_t o[R / 4];
-#pragma unroll
-          for (int e = 0; e < R / 4; ++e) {
-            const uint32_t w0 = w[2 * e], w1 = w[2 * e + 1];
-            o[e] = code_byte(w0 << 16) | (code_byte(w0 & 0xffff0000u) << 8) | (code_byte(w1 << 16) << 16) |
-                   (code_byte(w1 & 0xffff0000u) << 24);
-          }
-          if constexpr (R % 16 == 0) {
-            uint4* d = reinterpret_cast<uint4*>(iBt + j * Kp + k);
-#pragma unroll
-            for (int q = 0; q < R / 16; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-          } else {
-            uint2* d = reinterpret_cast<uint2*>(iBt + j * Kp + k);
-#pragma unroll
-            for (int q = 0; q < R / 8; ++q) d[q] = make_uint2(o[2 * q], o[2 * q + 1]);
-          }
-        }
-      }
+    const int64_t nxt = strip + gridDim.x;
+    const int nbm = nxt < nstrips ? nb1 : 0;
+    m = 0.0f;
+    for (int b = 0; b < (nb2 > nbm ? nb2 : nbm); ++b) {
+      if (b < nb2) code_box(j, b, sc, rs, rs_ok, fsum);
+      if (b < nbm) max_box(m);
     }
     // column sums (exact integers in fp32)
     red[rg][c] = fsum;
