@@ -274,8 +274,8 @@ def cpu_baseline(rows, seed=2):
 def oracle_row_baselines(d=None):
     """The oracle, as it stands, on bounded samples of the other workloads
     (QuantizeLinear / DequantizeLinear, dense and depthwise QLinearConv, the
-    LSTM): {row: {value, unit, sample, seconds}}, each a few seconds of host
-    work at most."""
+    LSTM, the small inner product whole): {row: {value, unit, sample,
+    seconds}}, each a few seconds of host work at most."""
     import numpy as np
 
     import oracle
@@ -313,6 +313,10 @@ def oracle_row_baselines(d=None):
     ops = 2 * (2.0 * 2 * 64 * 1024 * 4096) * 2
     out["dq_lstm_bidirectional"] = {"value": ops / dt / 1e12, "unit": "TOPS", "seconds": round(dt, 3),
                                     "sample": "2 of 512 steps (projection and recurrence), both directions"}
+    w = workloads.inner_product(seed=0)
+    _, dt = timed(lambda: oracle.dynamic_quantized_inner_product(w["A"], w["B"], bias=w["bias"]))
+    out["inner_product_64x128x256"] = {"value": dt * 1e6, "unit": "us", "seconds": round(dt, 4),
+                                       "sample": "the whole 64x128x256 product (one Forward)"}
     return out
 
 
