@@ -517,7 +517,48 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int it = 0, chunk = 0;
       bool ok = true;
       uint32_t d = tmem_base;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      if (KT % STAGES == 0) {
+        // every tile starts at stage 0: the K loop unrolled by the ring's
+        // length, stage indices and descriptor offsets constant (as in the
+        // pair kernel)
+        const uint64_t a0 = desc_sw128(sA(0)), b0 = desc_sw128(sB(0));
+        constexpr uint64_t STAGE_STEP = STAGE_BYTES >> 4, K_STEP = 32 >> 4;
+        uint32_t ph = 0;
+        int kc = 0;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+          for (int kt0 = 0; ok && kt0 < KT; kt0 += STAGES) {
+#pragma unroll
+            for (int j = 0; j < STAGES; ++j) {
+              if (kc == 0) {
+                const int b = chunk & 1;
+                if (!wait_bar(acce(b), ((uint32_t)(chunk >> 1) & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT_MMA)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                d = tmem_base + (uint32_t)(b * BN);
+              }
+              if (!wait_bar(full(j), ph, abort_flag, p.status, ST_TIMEOUT_MMA)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t ad = a0 + (uint64_t)j * STAGE_STEP, bd = b0 + (uint64_t)j * STAGE_STEP;
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k)
+                tc_mma(d, ad + k * K_STEP, bd + k * K_STEP, IDESC, (kc == 0 && k == 0) ? 0u : 1u);
+              tc_commit(empty(j));
+              if (++kc == CS || kt0 + j == KT - 1) {
+                tc_commit(accf(chunk & 1));
+                ++chunk;
+                kc = 0;
+              }
+            }
+            ph ^= 1u;
+          }
+        }
+      }
+      for (int tile = blockIdx.x; ok && KT % STAGES != 0 && tile < p.num_tiles; tile += gridDim.x) {
         for (int kt = 0; kt < KT; ++kt, ++it) {
           const int kc = kt % CS;
           if (kc == 0) {
