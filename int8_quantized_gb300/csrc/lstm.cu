@@ -920,35 +920,41 @@ lstm_persist_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
       // step kc; descriptors advanced by addition (start address >> 4)
       const uint64_t adesc0 = desc_sw128(sA(0)), bdesc0 = desc_sw128(sR);
       uint32_t st = 0, ph = 0, chunk = 0;
-      if (KT == 2 * STAGES && p.CS >= KT) {
-        // the common shape (K = 1024, one exact chunk per step): the step's
-        // 16 slabs pass the 8 stages twice, so slab kt always sits in stage
-        // kt mod 8 with phase kt / 8, and every descriptor is the base plus a
-        // constant (a lean, fully unrolled issue loop)
+      if (KT % STAGES == 0 && p.CS >= KT) {
+        // K a multiple of 512 with one exact chunk per step (K = 1024 at the
+        // full size): every step starts at stage 0 and slab r * 8 + j sits in
+        // stage j, so the issue loop is unrolled over the ring with constant
+        // stage offsets and a phase that turns once per round
+        uint32_t ph = 0;
         for (int s = 0; ok && s < p.T; ++s) {
           if (!wait_bar(acce, ((uint32_t)s & 1u) ^ 1u, abort_flag, p.status, ST_TIMEOUT)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          for (int r = 0; ok && r < KT / STAGES; ++r) {
+            const uint64_t bround = bdesc0 + (uint64_t)(((uint32_t)r * STAGES * R_SLAB) >> 4);
 #pragma unroll
-          for (int kt = 0; kt < 2 * STAGES; ++kt) {
-            if (!wait_bar(full(kt % STAGES), (uint32_t)(kt / STAGES), abort_flag, p.status, ST_TIMEOUT)) {
-              ok = false;
-              break;
+            for (int j = 0; j < STAGES; ++j) {
+              if (!wait_bar(full(j), ph, abort_flag, p.status, ST_TIMEOUT)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t ad = adesc0 + (uint64_t)((j * A_STAGE) >> 4);
+              const uint64_t bd = bround + (uint64_t)((j * R_SLAB) >> 4);
+              const uint32_t acc = (r > 0 || j > 0) ? 1u : 0u;
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k)
+                tc_mma(tmem + (uint32_t)(k * BN), ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, acc);
+              tc_commit(empty(j));
             }
-            tc_fence_after();
-            const uint64_t ad = adesc0 + (uint64_t)(((kt % STAGES) * A_STAGE) >> 4);
-            const uint64_t bd = bdesc0 + (uint64_t)((kt * R_SLAB) >> 4);
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-              tc_mma(tmem + (uint32_t)(k * BN), ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, kt > 0 ? 1u : 0u);
-            tc_commit(empty(kt % STAGES));
+            ph ^= 1u;
           }
           if (ok) tc_commit(accf);
         }
       }
-      for (int s = 0; ok && s < p.T && !(KT == 2 * STAGES && p.CS >= KT); ++s) {
+      for (int s = 0; ok && s < p.T && !(KT % STAGES == 0 && p.CS >= KT); ++s) {
         int kc = 0;
         for (int kt = 0; kt < KT; ++kt) {
           if (kc == 0) {

@@ -139,11 +139,11 @@ def test_nonzero_zero_point(orc, dev):
     assert np.array_equal(Y.cpu().numpy(), ref[0])
 
 
-@pytest.mark.parametrize("H,batch", [(144, 64), (336, 17), (1088, 64)])
+@pytest.mark.parametrize("H,batch", [(144, 64), (336, 17), (512, 64), (1088, 64)])
 def test_slab_counts(orc, dev, H, batch):
-    """Hidden sizes padded to 3, 6 and 17 slabs of 64 (the last too wide
-    for the persistent kernel's shared memory: one launch per step), whole
-    sequences bit for bit."""
+    """Hidden sizes padded to 3, 6, 8 and 17 slabs of 64 (8: one round of
+    the persistent kernel's ring per step; 17: too wide for its shared
+    memory, one launch per step), whole sequences bit for bit."""
     w = workloads.lstm(seed=5, T=5, batch=batch, I=64, H=H)
     Y, Yh, Yc, _, c_out = gpu_lstm(dev, w, "bidirectional", codes=True)
     ref = orc.dynamic_quantize_lstm(w["X"], w["W"], w["R"], w["B"], w["W_scale"], w["R_scale"],
