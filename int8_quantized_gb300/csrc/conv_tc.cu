@@ -45,7 +45,10 @@ struct ConvTile {
   static constexpr int B_STAGE = TN * BK * 2;
   static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
   static constexpr int SL = TN / 4;  // pixels per epilogue warp
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+  // staging of the codes of 32 channels x TN pixels per TMEM lane quadrant,
+  // for the bulk store of y (1024-byte aligned groups)
+  static constexpr int STG_GROUP = ((32 * TN + 1023) / 1024) * 1024;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 4 * STG_GROUP + NUM_BARS * 8 + 16;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(TN % 32 == 0 && TN <= 256, "tile width");
 };
@@ -64,7 +67,17 @@ struct ConvParams {
   int per_channel;
   uint8_t* y;  // NCHW bytes (uint8 or int8 codes)
   uint32_t* status;
+  int tma_y;   // y stored by bulk tensor copies through shared memory (R * OW == TN)
 };
+
+// Tiled TMA store of a 3-D box from this CTA's shared memory (dense rows)
+// to the tensor at (x, y, z), in the calling thread's bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 
 __device__ __forceinline__ void conv_tile_coords(int tile, const ConvParams& p, int& mt, int& rg, int& n) {
   mt = tile % p.tiles_m;
@@ -75,13 +88,15 @@ __device__ __forceinline__ void conv_tile_coords(int tile, const ConvParams& p, 
 
 template <int TN>
 __global__ void __launch_bounds__(THREADS, 1)
-conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, ConvParams p) {
+conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+               const __grid_constant__ CUtensorMap tmY, ConvParams p) {
   using T = ConvTile<TN>;
   constexpr uint32_t IDESC = idesc_bf16(BM, TN);
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned, indexed from the shared array itself so that accesses stay shared-space
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * T::STAGE_BYTES);
+  uint8_t* stg_all = smem + STAGES * T::STAGE_BYTES;  // 4 groups of T::STG_GROUP bytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + 4 * T::STG_GROUP);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t smem0 = smem_u32(smem);
@@ -112,6 +127,7 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+    if (p.tma_y) asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmY)) : "memory");
   }
   {
     const int lo = p.wsigned ? -128 : 0, hi = p.wsigned ? 127 : 255;
@@ -314,8 +330,52 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         __syncwarp();
         if (lane == 0) mbar_arrive(acce(b));
       }
-      if (!ok) break;
       const int m = mt * BM + q * 32 + lane;
+      if (p.tma_y) {
+        // the four slices of quadrant q (warps q + 2 .. q + 14 step 4) stage
+        // their 32 channels x SL codes as one dense 32 x TN box, stored by
+        // one bulk tensor copy (coalesced rows of the NCHW planes)
+        uint8_t* stg = stg_all + q * T::STG_GROUP;
+        const uint32_t group_bar = 1u + (uint32_t)q;
+        if (ok && slice == 0 && lane == 0) bulk_wait_read();  // the previous tile's store has read the buffer
+        // barrier over the quadrant's 128 threads, which also agree on ok
+        // (so that they leave the tile loop together)
+        uint32_t all_ok;
+        asm volatile(
+            "{\n .reg .pred p, r;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred r, %2, 128, p;\n selp.u32 %0, 1, 0, r;\n}\n"
+            : "=r"(all_ok)
+            : "r"((uint32_t)ok), "r"(group_bar)
+            : "memory");
+        if (!all_ok) {
+          ok = false;
+          break;
+        }
+        const int32_t bm = (m < p.M && p.bias) ? __ldg(p.bias + m) : 0;
+        const float mul = __fmul_rn(p.x_scale, __ldg(p.w_scale + (p.per_channel ? min(m, p.M - 1) : 0)));
+        uint8_t* dst = stg + lane * TN + slice * SL;
+#pragma unroll
+        for (int j = 0; j < SL; j += 8) {
+          uint32_t code[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            float v = __fmul_rn(__int2float_rn(run[j + u] + bm), mul);
+            v = __fdiv_rn(v, p.y_scale);
+            code[u] = rint_code_bits(v, p.qlo_z, p.qhi_z, p.y_zp);
+          }
+          *reinterpret_cast<uint2*>(dst + j) = make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]),
+                                                          pack_low_bytes(code[4], code[5], code[6], code[7]));
+        }
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        asm volatile("bar.sync %0, 128;\n" ::"r"(group_bar) : "memory");
+        if (slice == 0 && lane == 0) {
+          // rows past OH and channels past M fall outside the tensor: not written
+          tma_store_3d(&tmY, smem_u32(stg), rg * p.R * p.OW, mt * BM + q * 32, n);
+          bulk_commit();
+        }
+        __syncwarp();
+        continue;
+      }
+      if (!ok) break;
       if (m < p.M) {
         const int32_t bm = p.bias ? __ldg(p.bias + m) : 0;
         const float mul = __fmul_rn(p.x_scale, __ldg(p.w_scale + (p.per_channel ? m : 0)));
@@ -357,6 +417,9 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
       }
       __syncwarp();
     }
+    // the bulk stores are complete before the CTA leaves
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -645,9 +708,29 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
   p.per_channel = per_channel;
   p.y = static_cast<uint8_t*>(y);
   p.status = status;
+  // y as [N][M][OH * OW] bytes for bulk stores of 32 channels x TN pixels:
+  // when a tile is whole rows filling TN and the planes and y are 16-byte
+  // aligned
+  CUtensorMap mY = mX;
+  p.tma_y = 0;
+  if ((int64_t)R * OW == TN && (OH * OW) % 16 == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0 &&
+      OH * OW < ((int64_t)1 << 31) && !getenv("I8Q_CONV_DIRECT_STORE")) {
+    auto fn = tc::encode_fn();
+    if (!fn) return fail(I8Q_ERR_CUDA, "qlinearconv: cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[3] = {(cuuint64_t)(OH * OW), (cuuint64_t)M, (cuuint64_t)N};
+    cuuint64_t strides[2] = {(cuuint64_t)(OH * OW), (cuuint64_t)(M * OH * OW)};
+    cuuint32_t box[3] = {(cuuint32_t)TN, 32u, 1u};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(&mY, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3u, y, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(I8Q_ERR_CUDA, "qlinearconv: cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    p.tma_y = 1;
+  }
   const int grid = std::min(p.num_tiles, sm_count());
   I8Q_PROF("qlinearconv_tc", s);
-  conv_tc_kernel<TN><<<grid, THREADS, T::SMEM_BYTES, s>>>(mW, mX, p);
+  conv_tc_kernel<TN><<<grid, THREADS, T::SMEM_BYTES, s>>>(mW, mX, mY, p);
   I8Q_LAUNCH_CHECK("conv_tc_kernel");
   return I8Q_OK;
 }

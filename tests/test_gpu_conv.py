@@ -92,12 +92,19 @@ TC_CASES = [
     (2, 72, 16, 28, 40, 3, (1, 1, 1, 1)),    # C not a multiple of 64
     (1, 37, 8, 56, 40, 3, (1, 1, 1, 1)),     # odd C
     (1, 64, 16, 14, 64, 3, (1, 1, 1, 1)),    # rows of 14 pixels, 8 rows a block
+    (1, 24, 6, 56, 40, 3, (1, 1, 1, 1)),     # planes of 336 pixels: bulk stores, last row group half empty
 ]
 
 
 @pytest.mark.parametrize("case", TC_CASES)
 @pytest.mark.parametrize("types", [("u8", "u8", "u8"), ("s8", "s8", "s8"), ("u8", "s8", "s8")])
-def test_tensor_core_path(orc, dev, case, types):
+@pytest.mark.parametrize("store", ["bulk", "direct"])
+def test_tensor_core_path(orc, dev, monkeypatch, case, types, store):
+    """y by bulk tensor stores of 32 channels x 224 pixels where the planes
+    allow (16-byte multiples, whole rows per tile), else (and forced) by
+    the epilogue threads' own stores."""
+    if store == "direct":
+        monkeypatch.setenv("I8Q_CONV_DIRECT_STORE", "1")
     N, C, H, W, M, k, pads = case
     rng = np.random.default_rng(N * 1000 + C + M + k)
     dt = {"u8": (np.uint8, 0, 256), "s8": (np.int8, -128, 128)}
