@@ -659,13 +659,16 @@ lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
 // 64g .. 64g + 63 of R[d], which it loads into shared memory once (bf16
 // R - zp, K-major, 128-byte swizzle) and keeps for the whole sequence.  Per
 // step the TMA producer streams the previous step's h codes (uh - 128,
-// bf16, 64 batch rows x Hp) through an 11-stage ring and one thread issues
+// bf16, 64 batch rows x Hp) through an 8-stage ring and one thread issues
 // the product as M = 64 batch rows x N = 64 gate rows on tcgen05, fp32
 // chunks of 2^24 / 2^log2 K-elements drained exactly to int32 as in the
-// per-step kernels.  Products this small are bound by the latency of MMAs
-// that accumulate into the same tile, so the four 16-K sub-steps of each
-// 64-K slab go to four accumulators (TMEM columns 0, 64, 128, 192), summed
-// in int32 by the drain.  With M = 64 the accumulator rows 16w .. 16w + 15 sit in
+// per-step kernels.  Products this small are bound by the issuing thread
+// (an MMA of this size takes about 79 SM clocks to issue back to back, and
+// more with any other instruction between) and by the latency of MMAs that
+// accumulate into the same tile: the issue loop is unrolled over the ring
+// (K a multiple of 512), and the four 16-K sub-steps of each 64-K slab go
+// to four accumulators (TMEM columns 0, 64, 128, 192), summed in int32 by
+// the drain.  With M = 64 the accumulator rows 16w .. 16w + 15 sit in
 // TMEM lanes 32w .. 32w + 15, so the epilogue warps of all four
 // sub-partitions read them; a row's 16 columns (four units, gates i, o, f, c
 // interleaved) are split between a lane and the lane 16 above it, two units
