@@ -666,9 +666,9 @@ lstm_step_tc_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
 // (an MMA of this size takes about 79 SM clocks to issue back to back, and
 // more with any other instruction between) and by the latency of MMAs that
 // accumulate into the same tile: the issue loop is unrolled over the ring
-// (K a multiple of 512), and the four 16-K sub-steps of each 64-K slab go
-// to four accumulators (TMEM columns 0, 64, 128, 192), summed in int32 by
-// the drain.  With M = 64 the accumulator rows 16w .. 16w + 15 sit in
+// (K a multiple of 512).  At this issue rate one accumulator (TMEM columns
+// 0..63) is fastest: two or four independent ones, which hide the MMAs'
+// accumulation latency, cost more in the drain than they save.  With M = 64 the accumulator rows 16w .. 16w + 15 sit in
 // TMEM lanes 32w .. 32w + 15, so the epilogue warps of all four
 // sub-partitions read them; a row's 16 columns (four units, gates i, o, f, c
 // interleaved) are split between a lane and the lane 16 above it, two units
@@ -690,7 +690,7 @@ using tcs::clip_gate;
 
 constexpr int BM = 64, BN = 64, BK = 64, STAGES = 8;
 constexpr int EPI_WARPS = 16, THREADS = 32 * (2 + EPI_WARPS);  // warps 2..17: TMEM sub-partition warp % 4
-constexpr int NACC = 4;                // independent accumulators: the 16-K sub-steps of a 64-K slab
+constexpr int NACC = 1;                // accumulators the 16-K sub-steps of a slab rotate over
 constexpr int TMEM_COLS = NACC * 64;
 constexpr int A_STAGE = BM * BK * 2;   // 8 KB
 constexpr int R_SLAB = BN * BK * 2;    // 8 KB per 64 K-elements of the resident R tile
@@ -949,7 +949,8 @@ lstm_persist_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
               const uint32_t acc = (r > 0 || j > 0) ? 1u : 0u;
 #pragma unroll
               for (int k = 0; k < BK / 16; ++k)
-                tc_mma(tmem + (uint32_t)(k * BN), ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, acc);
+                tc_mma(tmem + (uint32_t)((k % NACC) * BN), ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC,
+                       (acc || k >= NACC) ? 1u : 0u);
               tc_commit(empty(j));
             }
             ph ^= 1u;
@@ -977,7 +978,8 @@ lstm_persist_kernel(const __grid_constant__ CUtensorMap tmR, const __grid_consta
           const uint32_t acc = kc == 0 ? 0u : 1u;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma(tmem + (uint32_t)(k * BN), ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC, acc);
+            tc_mma(tmem + (uint32_t)((k % NACC) * BN), ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC,
+                   (acc || k >= NACC) ? 1u : 0u);
           tc_commit(empty(st));
           if (++kc == p.CS || kt == KT - 1) {
             tc_commit(accf);
