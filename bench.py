@@ -75,6 +75,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-rows", type=int, default=2048, help="rows of the CPU-baseline sample")
     p.add_argument("--no-rows", action="store_true", help="skip the other hot-path workloads")
+    p.add_argument("--rows", default=None,
+                   help="comma-separated names of the hot-path workloads to time (default: all of them)")
     p.add_argument("--m", type=int, default=M,
                    help="rows of A in the GEMM step (default: the full workload; smaller for profiler captures)")
     p.add_argument("--detail", default=None,
@@ -350,7 +352,30 @@ def measure_rows(args, dev, stream, world):
     steps, warm = max(3, args.steps // 2), max(2, args.warmup)
     out = {}
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    sel = set(args.rows.split(",")) if getattr(args, "rows", None) else None
+    want = lambda *keys: sel is None or any(k in sel for k in keys)  # noqa: E731
+    if want("large_gemm_avoid_overflow"):
+        _row_avoid_overflow(out, dev, stream, steps, warm, t)
+    if want("inner_product_64x128x256"):
+        _row_inner_product(out, dev, stream, steps, warm, t)
+    for dw in (False, True):
+        if want("qlinearconv_depthwise" if dw else "qlinearconv_dense"):
+            _row_qlinearconv(out, dev, stream, steps, warm, t, dw)
+    if want("qgemm_u8s8_to_u8", "matmul_integer_to_float", "dynamic_quantize_matmul"):
+        _row_qgemm_family(out, dev, stream, steps, warm, t)
+    if want("qlinear_add", "qlinear_leaky_relu"):
+        _row_qlinear_ew(out, dev, stream, steps, warm)
+    if want("dq_lstm_bidirectional"):
+        _row_lstm(out, dev, stream, t)
+    return out
 
+
+def _row_avoid_overflow(out, dev, stream, steps, warm, t):
+    import numpy as np
+    import torch
+
+    import int8_quantized_gb300 as q
+    from int8_quantized_gb300 import workloads
     # large GEMM with avoidOverflow: non-constant fp32 B quantized in every Forward
     w = workloads.large_gemm(seed=2, avoid_overflow=True)
     ctx = q.QGemmDyn(M, N, K, q.BF16, q.F32, q.BF16, constB=False, bias=True, activation=q.ACT_GELU,
@@ -367,6 +392,12 @@ def measure_rows(args, dev, stream, world):
     ctx.clear()
     del A, B, C, buf
 
+
+def _row_inner_product(out, dev, stream, steps, warm, t):
+    import torch
+
+    import int8_quantized_gb300 as q
+    from int8_quantized_gb300 import workloads
     # small inner product (latency)
     w = workloads.inner_product(seed=0)
     ctx = q.QGemmDyn(64, 128, 256, q.F32, q.F32, q.F32, constB=True, bias=True)
@@ -377,25 +408,37 @@ def measure_rows(args, dev, stream, world):
     out["inner_product_64x128x256"] = {"us": sec * 1e6, "kernels": prof}
     ctx.clear()
 
-    # QLinearConv dense and depthwise
-    for dw in (False, True):
-        c = workloads.qlinearconv(seed=3, depthwise=dw)
-        x, wt = t(c["x"]), t(c["w"])
-        ws, wz, bias = t(c["w_scale"]), t(c["w_zero_point"]), t(c["B"])
-        y = torch.empty(32, 256, 56, 56, dtype=torch.uint8, device=dev)
-        wsb = q.qlinearconv_workspace_size(c["x"].shape, c["w"].shape, c["pads"], (1, 1), (1, 1), c["group"])
-        wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
-        fn = lambda: q.qlinearconv(x, float(c["x_scale"]), c["x_zero_point"], wt, ws, wz,  # noqa: E731
-                                   float(c["y_scale"]), c["y_zero_point"], y, B=bias, pads=c["pads"],
-                                   group=c["group"], workspace=wsp if wsb else None)
-        sec, prof = _timed(fn, steps, warm, stream)
-        ops = 2.0 * 32 * 256 * 56 * 56 * (c["w"].shape[1] * 9)
-        moved = c["x"].nbytes + c["w"].nbytes + y.numel()
-        key = "qlinearconv_depthwise" if dw else "qlinearconv_dense"
-        out[key] = {"ms": sec * 1e3, "TOPS": ops / sec / 1e12, "GB/s": moved / sec / 1e9, "kernels": prof,
-                    "workload": "x u8 [32,256,56,56], w [256,%d,3,3], pad 1, per-channel w" % c["w"].shape[1]}
-        del x, wt, y, wsp
 
+def _row_qlinearconv(out, dev, stream, steps, warm, t, dw):
+    import torch
+
+    import int8_quantized_gb300 as q
+    from int8_quantized_gb300 import workloads
+    # QLinearConv dense or depthwise
+    c = workloads.qlinearconv(seed=3, depthwise=dw)
+    x, wt = t(c["x"]), t(c["w"])
+    ws, wz, bias = t(c["w_scale"]), t(c["w_zero_point"]), t(c["B"])
+    y = torch.empty(32, 256, 56, 56, dtype=torch.uint8, device=dev)
+    wsb = q.qlinearconv_workspace_size(c["x"].shape, c["w"].shape, c["pads"], (1, 1), (1, 1), c["group"])
+    wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    fn = lambda: q.qlinearconv(x, float(c["x_scale"]), c["x_zero_point"], wt, ws, wz,  # noqa: E731
+                               float(c["y_scale"]), c["y_zero_point"], y, B=bias, pads=c["pads"],
+                               group=c["group"], workspace=wsp if wsb else None)
+    sec, prof = _timed(fn, steps, warm, stream)
+    ops = 2.0 * 32 * 256 * 56 * 56 * (c["w"].shape[1] * 9)
+    moved = c["x"].nbytes + c["w"].nbytes + y.numel()
+    key = "qlinearconv_depthwise" if dw else "qlinearconv_dense"
+    out[key] = {"ms": sec * 1e3, "TOPS": ops / sec / 1e12, "GB/s": moved / sec / 1e9, "kernels": prof,
+                "workload": "x u8 [32,256,56,56], w [256,%d,3,3], pad 1, per-channel w" % c["w"].shape[1]}
+    del x, wt, y, wsp
+
+
+def _row_qgemm_family(out, dev, stream, steps, warm, t):
+    import numpy as np
+    import torch
+
+    import int8_quantized_gb300 as q
+    from int8_quantized_gb300 import workloads
     # QGemm at the large GEMM's shape: u8 A x s8 B with per-column
     # parameters, int32 C of shape (1, N), alpha, u8 output
     w = workloads.qgemm(seed=5)
@@ -433,6 +476,11 @@ def measure_rows(args, dev, stream, world):
                                                   "column, bias, fp32 Y"}
     del Af, B, Yf, wsp
 
+
+def _row_qlinear_ew(out, dev, stream, steps, warm):
+    import torch
+
+    import int8_quantized_gb300 as q
     # QLinear elementwise on the [32,1024,4096] uint8 tensors: QLinearAdd of
     # two same-shape tensors (3 B per element), QLinearLeakyRelu (2 B)
     g = torch.Generator(device="cpu").manual_seed(6)
@@ -452,6 +500,11 @@ def measure_rows(args, dev, stream, world):
                                  "workload": "QLinearLeakyRelu u8 [32,1024,4096], 2 B per element"}
     del Xa, Xb, Yq
 
+
+def _row_lstm(out, dev, stream, t):
+    import int8_quantized_gb300 as q
+    from int8_quantized_gb300 import workloads
+    import torch
     # DynamicQuantizeLSTM, bidirectional T=512 batch=64 I=H=1024
     w = workloads.lstm(seed=4)
     T_, b_, I_, H_ = 512, 64, 1024, 1024
@@ -468,7 +521,6 @@ def measure_rows(args, dev, stream, world):
     out["dq_lstm_bidirectional"] = {"ms": sec * 1e3, "TOPS": ops / sec / 1e12, "kernels": prof,
                                     "workload": "T=512 batch=64 I=H=1024, projection + 512 steps per direction"}
     del X, Wd, Rd, wsp, Y
-    return out
 
 
 def run_reference(args):

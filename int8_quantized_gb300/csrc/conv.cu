@@ -190,17 +190,17 @@ qlinearconv_depthwise_halo(const XT* __restrict__ x, const WT* __restrict__ w, c
 // once to the item's first byte), forms the windows of the even outputs by
 // byte permutes with constant selectors, and feeds every output row that
 // row reaches (up to KS of them); an output row is requantized and stored
-// (one 8-byte store) as soon as its last input row is in.  The
-// requantization code of fl(fl(acc * mul) / y_scale) comes from
-// q = fl(fl(acc * mul) * r), r = fl(1 / y_scale): q clamped to the code
-// range and rounded by adding 1.5 * 2^23 (round half to even).  Within the
-// range (|q| < 2^9) q and the quotient differ by less than 2^-22 |q|, so
-// they round alike unless q lies within 2^-21 |q| of a half-integer, where
-// the quotient is formed exactly (checked once per row of 8 outputs);
-// beyond the range both saturate alike.  A scale whose reciprocal is not a
-// normal number takes the quotient always.  (Tap sums on the fp32 pipe,
-// exact for these magnitudes, were measured slower: the byte-to-float
-// conversions outweigh the faster multiply-adds.)
+// (one 8-byte store) as soon as its last input row is in.  A plane whose
+// sums all stay below 2^22 in magnitude and whose quotients stay below 2^20
+// (bounded from its filter, bias and scales when its constants are staged)
+// takes the bracketed form of dw_requant_fast: its sums carry 1.5 * 2^23
+// from the start, so each int32 pattern is already an exact float, and two
+// rounded ends of an interval around the quotient give the code when they
+// agree.  Other planes take each code from the reciprocal product
+// (quot_code_bits), with the quotient itself near a half-integer or when
+// 1 / y_scale is not a normal number.  (Tap sums on the fp32 pipe, exact
+// for these magnitudes, were measured slower: the byte-to-float conversions
+// outweigh the faster multiply-adds.)
 constexpr int kStrip = 8, kX0 = 8;  // outputs per item row; byte of x column 0 in a shared row
 
 // Words of a shared row: the slack before column 0, the items' outputs, the
@@ -221,8 +221,9 @@ struct DwPlane {
   // for the odd one; KS = 5 adds (w'4, 0) and (w'3, w'4) on the window four
   // bytes on
   uint32_t wp[KS][KS == 3 ? 4 : 6];
-  int k0;     // B - x_zp sum w'
+  int k0;     // B - x_zp sum w', plus 0x4B400000 when fast
   float mul;  // x_scale * w_scale
+  int fast;   // the plane's sums and quotients fit the bracketed requantization
 };
 
 // d = c + a.lo16 * b.byte(0|2) + a.hi16 * b.byte(1|3): a holds two signed
@@ -251,57 +252,70 @@ __device__ __forceinline__ void dw_cp_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// The code of fl(v / y_scale) when the reciprocal product q = fl(v * yr)
-// may round differently (near a half-integer, or no usable reciprocal);
-// otherwise the code already formed.  Kept out of line: it runs rarely.
-__device__ __noinline__ uint32_t dw_code_checked(float v, float yr, bool rcp_ok, float y_scale, float lo_z, float hi_z,
-                                                 int y_zp, uint32_t code) {
-  const float q = __fmul_rn(v, yr);
-  const float cq = fminf(fmaxf(q, lo_z), hi_z);
-  const float d = __fsub_rn(cq, __fsub_rn(__fadd_rn(cq, 12582912.0f), 12582912.0f));
-  if (!rcp_ok || fabsf(d) > __fmaf_rn(fabsf(cq), -0x1p-21f, 0.5f))
-    return rint_code_bits(__fdiv_rn(v, y_scale), lo_z, hi_z, y_zp);
-  return code;
+// The code of one sum from the quotient itself: the fallback of
+// dw_requant_fast (accb carries 1.5 * 2^23 + acc).  Out of line: rare.
+__device__ __noinline__ int dw_code_exact(int accb, float mul, float y_scale, float lo_z, float hi_z, int y_zp) {
+  const float v = __fmul_rn(__fsub_rn(__int_as_float(accb), 12582912.0f), mul);
+  return (int)(rint_code_bits(__fdiv_rn(v, y_scale), lo_z, hi_z, y_zp) - 0x4B400000u);
 }
 
-// Requantize the 8 sums of an output row (av: the exact int32 sums as
-// floats, rounded as __int2float_rn) and store the codes at out (one
-// 8-byte store when vec, else the first min(n, 8) bytes).
+// Four codes saturated to the range of YT, packed with byte 0 from a.
 template <typename YT>
-__device__ __forceinline__ void dw_requant_store(const float (&av)[kStrip], float mul, float yr, bool rcp_ok,
-                                                 float y_scale, float lo_z, float hi_z, int y_zp, YT* out, bool vec,
-                                                 int n) {
-  uint32_t code[kStrip];
-  float vv[kStrip];
-  bool slow = !rcp_ok;
+__device__ __forceinline__ uint32_t pack_sat4(int a, int b, int c, int d) {
+  uint32_t hi, r;
+  if (std::is_same<YT, uint8_t>::value) {
+    asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(d), "r"(c), "r"(0u));
+    asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(b), "r"(a), "r"(hi));
+  } else {
+    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(d), "r"(c), "r"(0u));
+    asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(b), "r"(a), "r"(hi));
+  }
+  return r;
+}
+
+// Requantize the 8 sums of an output row of a fast plane and store the
+// codes.  Each sum arrives as the bit pattern of 1.5 * 2^23 + acc (the
+// plane's constant carries the offset; |acc| < 2^22, so the pattern is the
+// exact float and subtracting the offset gives fl(acc) exactly).  With
+// v = fl(acc * mul) and yrl < 1 / y_scale < yrh (yr scaled by 1 -+ 2^-20,
+// each rounded once), the exact products v * yrl and v * yrh enclose v /
+// y_scale with a margin of more than 2^-21 |v / y_scale|, so they strictly
+// enclose the quotient fl(v / y_scale) too.  Each fma adds mz = 1.5 * 2^23 +
+// y_zp to one product and rounds once to an integer (|q| < 2^21 keeps the
+// sum in the binade of unit spacing), a non-decreasing function of the
+// product: when both ends give the same integer, so does the quotient,
+// which is then no half-integer (both neighbours would lie inside), so the
+// integer is y_zp + rint(quotient), saturated by the pack.  Ends that differ
+// send the row to the quotient itself.
+template <typename YT>
+__device__ __forceinline__ void dw_requant_fast(const int (&accb)[kStrip], float mul, float yrh, float yrl, float mz,
+                                                float y_scale, float lo_z, float hi_z, int y_zp, YT* out, bool vec,
+                                                int n) {
+  int code[kStrip];
+  uint32_t diff = 0;
 #pragma unroll
   for (int e = 0; e < kStrip; e += 2) {
-    const float2 v = mul2_rn(make_float2(av[e], av[e + 1]), make_float2(mul, mul));
-    const float2 q = mul2_rn(v, make_float2(yr, yr));
-    vv[e] = v.x;
-    vv[e + 1] = v.y;
-    const float qq[2] = {q.x, q.y};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float cq = fminf(fmaxf(qq[h], lo_z), hi_z);
-      const float r1 = __fadd_rn(cq, 12582912.0f);
-      const float d = __fsub_rn(cq, __fsub_rn(r1, 12582912.0f));
-      code[e + h] = (uint32_t)(__float_as_int(r1) + y_zp);
-      slow |= fabsf(d) > __fmaf_rn(fabsf(cq), -0x1p-21f, 0.5f);
-    }
+    const float2 a = fma2_rn(make_float2(__int_as_float(accb[e]), __int_as_float(accb[e + 1])),
+                             make_float2(1.0f, 1.0f), make_float2(-12582912.0f, -12582912.0f));
+    const float2 v = mul2_rn(a, make_float2(mul, mul));
+    const float2 rh = fma2_rn(v, make_float2(yrh, yrh), make_float2(mz, mz));
+    const float2 rl = fma2_rn(v, make_float2(yrl, yrl), make_float2(mz, mz));
+    diff |= (__float_as_uint(rh.x) ^ __float_as_uint(rl.x)) | (__float_as_uint(rh.y) ^ __float_as_uint(rl.y));
+    code[e] = __float_as_int(rh.x) - 0x4B400000;
+    code[e + 1] = __float_as_int(rh.y) - 0x4B400000;
   }
-  if (slow) {
-    // near a half-integer (or no usable reciprocal): the quotient itself
+  if (diff) {
 #pragma unroll
-    for (int e = 0; e < kStrip; ++e) code[e] = dw_code_checked(vv[e], yr, rcp_ok, y_scale, lo_z, hi_z, y_zp, code[e]);
+    for (int e = 0; e < kStrip; ++e) code[e] = dw_code_exact(accb[e], mul, y_scale, lo_z, hi_z, y_zp);
   }
   if (vec) {
-    *reinterpret_cast<uint2*>(out) = make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]),
-                                                pack_low_bytes(code[4], code[5], code[6], code[7]));
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_sat4<YT>(code[0], code[1], code[2], code[3]),
+                                                pack_sat4<YT>(code[4], code[5], code[6], code[7]));
   } else {
+    constexpr int lo = std::is_same<YT, uint8_t>::value ? 0 : -128, hi = lo + 255;
 #pragma unroll
     for (int e = 0; e < kStrip; ++e)
-      if (e < n) out[e] = (YT)code[e];
+      if (e < n) out[e] = (YT)min(max(code[e], lo), hi);
   }
 }
 
@@ -310,7 +324,7 @@ __device__ __forceinline__ void dw_requant_store(const float (&av)[kStrip], floa
 // (cp.async, 8- or 4-byte pieces) while the current one is computed.  The
 // halo of both buffers is written once: copies touch only the interior.
 template <typename XT, typename WT, typename YT, int KS>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(224, 3)  // 3 CTAs of 7 warps per SM: at most 80 registers
 qlinearconv_depthwise_rows(const XT* __restrict__ x, const WT* __restrict__ w, const float* __restrict__ w_scale,
                            const WT* __restrict__ w_zp, int per_channel, const int32_t* __restrict__ B, int C, int H,
                            int W, int OH, int OW, int pt, int pl, int planes, int ppc, float x_scale, int x_zp,
@@ -327,6 +341,10 @@ qlinearconv_depthwise_rows(const XT* __restrict__ x, const WT* __restrict__ w, c
   const uint32_t fill = (uint32_t)(uint8_t)x_zp * 0x01010101u;
   const int rows_in = min(H, HP - pt);  // input rows that reach an output
   const int ngroups = (planes + ppc - 1) / ppc;
+  const float yr = quot_rcp(y_scale);
+  const bool rcp_ok = yr == yr;
+  const float yrh = __fmul_rn(yr, 1.0f + 0x1p-20f), yrl = __fmul_rn(yr, 1.0f - 0x1p-20f);
+  const float mz = 12582912.0f + (float)y_zp;
 
   // both buffers: every word the zero point's code, once
   for (int i = tid; i < 2 * buf_words / 4; i += nthr)
@@ -381,18 +399,29 @@ qlinearconv_depthwise_rows(const XT* __restrict__ x, const WT* __restrict__ w, c
         const int c = (p0 + pi) % C;
         DwPlane<KS>& P = prm_base[bi * ppc + pi];
         const int wz = (int)w_zp[per_channel ? c : 0];
-        int wsum = 0;
-        for (int t = 0; t < KS * KS; ++t) wsum += (int)w[(int64_t)c * KS * KS + t] - wz;
-        P.k0 = (B ? B[c] : 0) - x_zp * wsum;
-        P.mul = __fmul_rn(x_scale, w_scale[per_channel ? c : 0]);
+        int wsum = 0, wabs = 0;
+        for (int t = 0; t < KS * KS; ++t) {
+          const int d = (int)w[(int64_t)c * KS * KS + t] - wz;
+          wsum += d;
+          wabs += abs(d);
+        }
+        const long long k0 = (long long)(B ? B[c] : 0) - (long long)x_zp * wsum;
+        const float mul = __fmul_rn(x_scale, w_scale[per_channel ? c : 0]);
+        // every sum of the plane is within amax of 0: below 2^22 it rides on
+        // 1.5 * 2^23 as an exact float; and |q| <= 2^20 keeps the rounded
+        // codes in the binade of unit spacing
+        const long long amax = (k0 < 0 ? -k0 : k0) + (long long)(XS ? 128 : 255) * wabs;
+        const bool fast =
+            rcp_ok && amax < (1ll << 22) && fabsf(__fmul_rn(__fmul_rn((float)amax, mul), yrh)) <= 0x1p20f;
+        P.k0 = (int)k0 + (fast ? 0x4B400000 : 0);
+        P.mul = mul;
+        P.fast = fast;
       }
     }
     dw_cp_commit();
   };
 
   const float lo_z = qlo - (float)y_zp, hi_z = qhi - (float)y_zp;
-  const float yr = quot_rcp(y_scale);
-  const bool rcp_ok = yr == yr;
   const int ipp = nstrips * nblocks;
 
   int grp = blockIdx.x;
@@ -420,6 +449,7 @@ qlinearconv_depthwise_rows(const XT* __restrict__ x, const WT* __restrict__ w, c
         for (int t = 0; t < NP; ++t) wp[kh][t] = P.wp[kh][t];
       const int k0 = P.k0;
       const float mul = P.mul;
+      const bool fast = P.fast != 0;
       const int oh0 = blk * R, ow0 = st * kStrip;
       const int s0 = kX0 - pl + ow0;  // first byte of the item's windows in a shared row
       const uint32_t shift = 0x3210u + (uint32_t)(s0 & 3) * 0x1111u;
@@ -465,11 +495,26 @@ qlinearconv_depthwise_rows(const XT* __restrict__ x, const WT* __restrict__ w, c
           }
           if (kh == KS - 1 && oh0 + o < OH) {
             // output row oh0 + o is complete: requantize and store its 8 codes
-            float av[kStrip];
+            if (fast) {
+              dw_requant_fast<YT>(acc[o], mul, yrh, yrl, mz, y_scale, lo_z, hi_z, y_zp,
+                                  yp + (int64_t)(oh0 + o) * OW, vec, OW - ow0);
+            } else {
+              // the other planes: each code from the reciprocal product,
+              // or from the quotient near a half-integer
+              uint32_t code[kStrip];
 #pragma unroll
-            for (int e = 0; e < kStrip; ++e) av[e] = __int2float_rn(acc[o][e]);
-            dw_requant_store(av, mul, yr, rcp_ok, y_scale, lo_z, hi_z, y_zp, yp + (int64_t)(oh0 + o) * OW, vec,
-                             OW - ow0);
+              for (int e = 0; e < kStrip; ++e)
+                code[e] = quot_code_bits(__fmul_rn(__int2float_rn(acc[o][e]), mul), y_scale, yr, lo_z, hi_z, y_zp);
+              YT* out = yp + (int64_t)(oh0 + o) * OW;
+              if (vec) {
+                *reinterpret_cast<uint2*>(out) = make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]),
+                                                            pack_low_bytes(code[4], code[5], code[6], code[7]));
+              } else {
+#pragma unroll
+                for (int e = 0; e < kStrip; ++e)
+                  if (e < OW - ow0) out[e] = (YT)code[e];
+              }
+            }
           }
         }
       }
@@ -517,7 +562,7 @@ int run_direct(const ConvShape& s, const void* x, float x_scale, int x_zp, const
   const int64_t P = std::max(std::max(s.pt, s.pb), std::max(s.pl, s.pr));
   {
     // dp4a row kernel: depthwise 3x3 / 5x5, stride 1, dilation 1; planes
-    // per CTA so that the items (rows x 8 outputs) of a CTA fill 256 threads
+    // per CTA so that the items (rows x 8 outputs) of a CTA fill 224 threads
     const int64_t nstrips = (s.OW + kStrip - 1) / kStrip;
     const int64_t R = s.kH == 3 ? dw_rows<3>() : dw_rows<5>();
     const int64_t ipp = nstrips * ((s.OH + R - 1) / R);
@@ -525,7 +570,7 @@ int run_direct(const ConvShape& s, const void* x, float x_scale, int x_zp, const
                               ? (size_t)(s.OH + s.kH - 1) * dw_row_words((int)nstrips, (int)s.kW) * 4
                               : (size_t)-1 / 2;
     const size_t prm = s.kH == 3 ? sizeof(DwPlane<3>) : sizeof(DwPlane<5>);
-    int64_t ppc = std::max<int64_t>(1, std::min<int64_t>(256 / std::max<int64_t>(ipp, 1), 8));
+    int64_t ppc = std::max<int64_t>(1, std::min<int64_t>(224 / std::max<int64_t>(ipp, 1), 8));
     while (ppc > 1 && 2 * ppc * (pbytes + prm) > 160 * 1024) --ppc;
     const size_t ssmem = 2 * (size_t)ppc * (pbytes + prm);
     if (s.group == s.C && s.M == s.C && s.Cg == 1 && s.sh == 1 && s.sw == 1 && s.dh == 1 && s.dw == 1 &&
@@ -534,7 +579,7 @@ int run_direct(const ConvShape& s, const void* x, float x_scale, int x_zp, const
       auto kern = s.kH == 3 ? qlinearconv_depthwise_rows<XT, WT, YT, 3> : qlinearconv_depthwise_rows<XT, WT, YT, 5>;
       const int ar = smem_attr((const void*)kern, 160 * 1024);
       if (ar) return ar;
-      const int threads = (int)std::min<int64_t>(256, round_up(ppc * ipp, 32));
+      const int threads = (int)std::min<int64_t>(224, round_up(ppc * ipp, 32));
       const int64_t planes = s.N * s.C, groups = ceil_div(planes, ppc);
       // persistent: as many CTAs as fit at once, at most one per group
       int per_sm = 0;

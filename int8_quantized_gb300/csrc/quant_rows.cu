@@ -497,6 +497,87 @@ cols_kernel(const T* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int qmin
   }
 }
 
+// ---- int8 repack in 128 x 128 tiles ------------------------------------------
+// The repack of a given int8 B (no quantization) over a grid of K x N tiles:
+// a thread loads a 4-row x 16-column block (four 16-byte loads, two lanes
+// per 32-byte sector of a row), turns it into 16 words of 4 rows each of one
+// column by byte permutes, and stores them to a column-major shared tile
+// (column stride 33 words: the lanes of a warp store to 32 distinct banks).
+// Eight consecutive lanes then write one column's 128 bytes (and its 256
+// bf16 bytes) contiguously, and merge their column-sum partials by shuffles
+// into one atomicAdd per column and tile.  Rows k >= K load as zeros, so the
+// tiles up to Kp write the padding.
+constexpr int kRtCols = 128, kRtK = 128, kRtStride = kRtK / 4 + 1;
+
+__global__ void __launch_bounds__(256)
+repack_tiles_s8(const int8_t* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int8_t* __restrict__ iBt,
+                __nv_bfloat16* __restrict__ iBt_bf16, int64_t Kp, int32_t* __restrict__ colsum, int64_t gates_H) {
+  __shared__ uint32_t tile[kRtCols * kRtStride];
+  const int t = (int)threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int64_t j0 = (int64_t)blockIdx.x * kRtCols, k0 = (int64_t)blockIdx.y * kRtK;
+  {
+    const int cq = 2 * (warp & 3) + (lane & 1), rq = 16 * (warp >> 2) + (lane >> 1);
+    const int64_t j = j0 + 16 * cq;
+    uint4 v[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int64_t k = k0 + 4 * rq + r;
+      v[r] = (k < K && j < N) ? __ldg(reinterpret_cast<const uint4*>(B + k * ldb + j)) : make_uint4(0, 0, 0, 0);
+    }
+    const uint32_t a[4][4] = {{v[0].x, v[0].y, v[0].z, v[0].w}, {v[1].x, v[1].y, v[1].z, v[1].w},
+                              {v[2].x, v[2].y, v[2].z, v[2].w}, {v[3].x, v[3].y, v[3].z, v[3].w}};
+    uint32_t* dst = tile + (16 * cq) * kRtStride + rq;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      // 4 x 4 byte transpose: word b = byte b of rows 0..3
+      const uint32_t t0 = __byte_perm(a[0][g], a[1][g], 0x5140), t1 = __byte_perm(a[0][g], a[1][g], 0x7362);
+      const uint32_t t2 = __byte_perm(a[2][g], a[3][g], 0x5140), t3 = __byte_perm(a[2][g], a[3][g], 0x7362);
+      dst[(4 * g + 0) * kRtStride] = __byte_perm(t0, t2, 0x5410);
+      dst[(4 * g + 1) * kRtStride] = __byte_perm(t0, t2, 0x7632);
+      dst[(4 * g + 2) * kRtStride] = __byte_perm(t1, t3, 0x5410);
+      dst[(4 * g + 3) * kRtStride] = __byte_perm(t1, t3, 0x7632);
+    }
+  }
+  __syncthreads();
+  // code c as fp32: byte c ^ 0x80 in 1.5 * 2^23 + (c + 128), minus 1.5 * 2^23 + 128
+  const float off = 12583040.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int task = t + 256 * i, c = task >> 3, q = task & 7;
+    const int64_t j = j0 + c, k = k0 + 16 * q;
+    const uint32_t* src = tile + c * kRtStride + 4 * q;
+    const uint32_t w[4] = {src[0], src[1], src[2], src[3]};
+    int sum = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sum = __dp4a((int)w[e], 0x01010101, sum);
+    const bool live = j < N && k < Kp;
+    if (live) {
+      const int64_t jd = dest_row(j, gates_H);
+      *reinterpret_cast<uint4*>(iBt + jd * Kp + k) = make_uint4(w[0], w[1], w[2], w[3]);
+      if (iBt_bf16) {
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t u = w[e] ^ 0x80808080u;
+          float f[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) f[b] = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B400000u, 0x7640 + b)), off);
+          o[2 * e] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632);
+          o[2 * e + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632);
+        }
+        uint4* ob = reinterpret_cast<uint4*>(iBt_bf16 + jd * Kp + k);
+        ob[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        ob[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    }
+    // the column's 8 lanes (consecutive, aligned) hold its 128 rows
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    if (q == 0 && j < N) atomicAdd(colsum + dest_row(j, gates_H), sum);
+  }
+}
+
 // ---- columns, two wide passes ---------------------------------------------
 // Each lane owns 4 consecutive columns, so a warp reads 128 columns of one
 // row per access (512 B of fp32, 256 B of bf16).  Pass 1 folds max|B| per
@@ -1035,8 +1116,17 @@ int launch_repack_cols_s8_gates(const int8_t* B, int64_t K, int64_t N, int64_t l
                                 __nv_bfloat16* iBt_bf16, int64_t Kp, int32_t* colsum, int64_t gates_H, cudaStream_t s) {
   if (N <= 0) return I8Q_OK;
   if (gates_H > 0 && N != 4 * gates_H) return fail(I8Q_ERR_INVALID_ARG, "repack: gate interleave needs N == 4H");
-  dim3 grid((unsigned)ceil_div(N, kColW));
   I8Q_PROF("repack_cols", s);
+  const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (N % 16 == 0 && ldb % 16 == 0 && Kp % 16 == 0 && Kp >= K && al16(B) && al16(iBt) &&
+      (!iBt_bf16 || al16(iBt_bf16)) && ceil_div(Kp, kRtK) <= 65535) {
+    I8Q_CUDA_TRY(cudaMemsetAsync(colsum, 0, (size_t)N * sizeof(int32_t), s));
+    dim3 grid((unsigned)ceil_div(N, kRtCols), (unsigned)ceil_div(Kp, kRtK));
+    repack_tiles_s8<<<grid, 256, 0, s>>>(B, K, N, ldb, iBt, iBt_bf16, Kp, colsum, gates_H);
+    I8Q_LAUNCH_CHECK("repack_tiles_s8");
+    return I8Q_OK;
+  }
+  dim3 grid((unsigned)ceil_div(N, kColW));
   cols_kernel<int8_t, 1><<<grid, 256, 0, s>>>(B, K, N, ldb, -128, 127, iBt, iBt_bf16, Kp, nullptr, colsum, gates_H);
   I8Q_LAUNCH_CHECK("cols_kernel(repack)");
   return I8Q_OK;

@@ -245,3 +245,38 @@ def test_depthwise_large_bias(orc, dev, monkeypatch, kernel, types):
     # unit scales and y_scale 2^17: codes near +-128 that move with the tap sums
     run_conv(orc, dev, x, np.float32(1.0), int(rng.integers(xt[0], xt[1])), w, np.ones(C, np.float32), wz,
              np.float32(2.0 ** 17), 128 if types[2] == "u8" else 0, B, (1, 1, 1, 1), group=C, ytype=types[2])
+
+
+@pytest.mark.parametrize("kernel", DW_KERNELS)
+@pytest.mark.parametrize("types", [("u8", "u8", "u8"), ("s8", "s8", "s8")])
+@pytest.mark.parametrize("ys", [2.0 ** 15, 2.0 ** 17, 4.00001, 3.99999, 4.0])
+def test_depthwise_sum_range_edges(orc, dev, monkeypatch, kernel, types, ys):
+    """Sums that reach +-(2^22 - 1) and +-2^22 (the row kernel carries sums
+    below 2^22 as exact floats and takes larger ones another way), and
+    quotients around 2^20 in magnitude, where the same switch happens for
+    the rounded codes: every channel's filter is one centred value +-200,
+    its bias puts the largest possible sum at the edge, and most inputs sit
+    at the end of their range that reaches it."""
+    force_dw_kernel(monkeypatch, kernel)
+    rng = np.random.default_rng(17)
+    s8 = types[0] == "s8"
+    xmax = 128 if s8 else 255
+    xz = -3 if s8 else 10
+    N, C, H, W, k = 2, 8, 13, 24, 3
+    wz = np.array([-128, 127] * 4 if s8 else [0, 200] * 4, np.int64)
+    wc = wz + np.array([200, -200] * 4)           # centred filter +200 or -200 at every tap
+    w = np.repeat(wc, k * k).reshape(C, 1, k, k).astype(np.int8 if s8 else np.uint8)
+    wsum = 9 * (wc - wz)
+    edge = np.array([2 ** 22 - 1, 2 ** 22 - 1, 2 ** 22, 2 ** 22, 2 ** 22 - 2, 2 ** 22 + 1, 2 ** 21, 2 ** 22 - 1])
+    # |k0| + xmax * sum |w'| = edge, with k0 of the sign that the extreme inputs push further
+    sign = np.sign(wc - wz) * (-1 if s8 else 1)
+    k0 = sign * (edge - xmax * np.abs(wsum))
+    B = (k0 + xz * wsum).astype(np.int32)
+    # inputs at the extreme code (x_max for u8, -128 for s8) with a sprinkling of others
+    lo, hi = (-128, 128) if s8 else (0, 256)
+    x = np.full((N, C, H, W), -128 if s8 else 255, np.int64)
+    m = rng.random(x.shape) < 0.3
+    x[m] = rng.integers(lo, hi, int(m.sum()))
+    x = x.astype(np.int8 if s8 else np.uint8)
+    run_conv(orc, dev, x, np.float32(1.0), xz, w, np.ones(C, np.float32), wz, np.float32(ys), 0 if s8 else 128, B,
+             (1, 1, 1, 1), group=C, ytype=types[2])
