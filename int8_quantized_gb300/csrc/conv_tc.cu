@@ -567,13 +567,15 @@ center_x_row(const XT* __restrict__ x, int C, int H, int W, int Cp, int xz, __nv
 }
 
 // wc[m][kh][kw][c] = w[m][c][kh][kw] - wz[m] (bf16), zero for c >= C.  One
-// thread per (m, tap, 8 channels): 8 strided byte reads, one 16-byte store.
+// thread per (m, tap, 8 channels): 8 strided byte reads, one 16-byte store;
+// threads first, first + stride, ... of the M * taps * Cp / 8 items.
 template <typename WT>
-__global__ void center_w(const WT* __restrict__ w, const WT* __restrict__ wz, int per_channel, int M, int C, int taps,
-                         int Cp, __nv_bfloat16* __restrict__ wc) {
+__device__ __forceinline__ void center_w_items(const WT* __restrict__ w, const WT* __restrict__ wz, int per_channel,
+                                               int M, int C, int taps, int Cp, __nv_bfloat16* __restrict__ wc,
+                                               int64_t first, int64_t stride) {
   const int groups = Cp / 8;
   const int64_t total = (int64_t)M * taps * groups;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+  for (int64_t i = first; i < total; i += stride) {
     const int g = (int)(i % groups);
     const int r = (int)(i / groups);  // m * taps + tap
     const int m = r / taps, tap = r - m * taps;
@@ -590,6 +592,93 @@ __global__ void center_w(const WT* __restrict__ w, const WT* __restrict__ wz, in
     }
     *reinterpret_cast<uint4*>(wc + (int64_t)r * Cp + g * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
+}
+
+template <typename WT>
+__global__ void center_w(const WT* __restrict__ w, const WT* __restrict__ wz, int per_channel, int M, int C, int taps,
+                         int Cp, __nv_bfloat16* __restrict__ wc) {
+  center_w_items(w, wz, per_channel, M, C, taps, Cp, wc, (int64_t)blockIdx.x * blockDim.x + threadIdx.x,
+                 (int64_t)gridDim.x * blockDim.x);
+}
+
+// Both operands in one launch, for rows of whole 8-byte pieces (W % 8 == 0,
+// H * W % 8 == 0, 8-byte aligned x): blocks [0, wblocks) centre the filter
+// as center_w; each later block of two warps centres two input rows, warp
+// r taking row n * H + h = 2 * (block - wblocks) + r whole.  Lane l takes
+// the channels 8l .. 8l + 7 of each 256-channel slab and walks the row two
+// 8-pixel pieces at a time: sixteen 8-byte reads in flight (one per channel
+// row and piece; the lane reads each channel row's sectors whole, one piece
+// after the other), then per pixel the eight codes turned into bf16 pairs
+// and one 16-byte store, the warp writing each pixel's 512 contiguous bytes
+// of xc.  A code b becomes the fp32 1.5 * 2^23 + b by one byte permute;
+// subtracting 1.5 * 2^23 + xz (paired) leaves b - xz exactly, whose bf16 is
+// the top half.  Channels C .. Cp - 1 read as the code xz and so come out 0.
+template <typename XT, typename WT>
+__global__ void __launch_bounds__(64, 8)
+center_ops_pix(const XT* __restrict__ x, int N, int C, int H, int W, int Cp, int xz, __nv_bfloat16* __restrict__ xc,
+               const WT* __restrict__ w, const WT* __restrict__ wzp, int per_channel, int M, int taps,
+               __nv_bfloat16* __restrict__ wc, int wblocks) {
+  if ((int)blockIdx.x < wblocks) {
+    center_w_items(w, wzp, per_channel, M, C, taps, Cp, wc, (int64_t)blockIdx.x * blockDim.x + threadIdx.x,
+                   (int64_t)wblocks * blockDim.x);
+    return;
+  }
+  const int64_t row = 2 * ((int64_t)blockIdx.x - wblocks) + (threadIdx.x >> 5);  // n * H + h
+  if (row >= (int64_t)N * H) return;
+  const int64_t n = row / H, h = row - n * H;
+  const int lane = (int)threadIdx.x & 31;
+  const int64_t plane = (int64_t)H * W;
+  constexpr bool XS = std::is_signed<XT>::value;
+  const uint32_t flip = XS ? 0x80808080u : 0u;  // signed codes as unsigned + 128
+  const int xzu = XS ? xz + 128 : xz;
+  const uint32_t zrow = (uint32_t)xzu * 0x01010101u;
+  const float zf = __int_as_float(0x4B400000 + xzu);
+  const XT* xrow = x + (n * C * H + h) * W;  // + c * plane + w
+  __nv_bfloat16* orow = xc + row * W * Cp;
+  for (int c0 = 8 * lane; c0 < Cp; c0 += 256) {
+    for (int w0 = 0; w0 < W; w0 += 16) {
+      const bool two = w0 + 8 < W;
+      uint32_t r[2][8][2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (c0 + i < C && (k == 0 || two)) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(xrow + (int64_t)(c0 + i) * plane + w0 + 8 * k));
+            r[k][i][0] = v.x ^ flip;
+            r[k][i][1] = v.y ^ flip;
+          } else {
+            r[k][i][0] = r[k][i][1] = zrow;
+          }
+        }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (k == 1 && !two) break;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const uint32_t sel = 0x7640u + (p & 3);
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float b0 = __uint_as_float(__byte_perm(r[k][2 * q][p >> 2], 0x4B400000u, sel));
+            const float b1 = __uint_as_float(__byte_perm(r[k][2 * q + 1][p >> 2], 0x4B400000u, sel));
+            const float2 f = fma2_rn(make_float2(b0, b1), make_float2(1.0f, 1.0f), make_float2(-zf, -zf));
+            o[q] = __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
+          }
+          *reinterpret_cast<uint4*>(orow + (int64_t)(w0 + 8 * k + p) * Cp + c0) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+  }
+}
+
+template <typename XT, typename WT>
+void launch_center_pix(cudaStream_t s, const void* x, int64_t N, int64_t C, int64_t H, int64_t W, int64_t Cp,
+                       int x_zp, __nv_bfloat16* xc, const void* w, const void* w_zp, int per_channel, int64_t M,
+                       int taps, __nv_bfloat16* wc, int wblocks) {
+  const unsigned grid = (unsigned)(wblocks + ceil_div(N * H, 2));
+  center_ops_pix<XT, WT><<<grid, 64, 0, s>>>((const XT*)x, (int)N, (int)C, (int)H, (int)W, (int)Cp, x_zp, xc,
+                                             (const WT*)w, (const WT*)w_zp, per_channel, (int)M, taps, wc, wblocks);
 }
 
 size_t a256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -633,7 +722,27 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
   {
     I8Q_PROF("conv_center_operands", s);
     const size_t row_smem = (size_t)W * (Cp + 8) * 2;
-    if (row_smem <= 200 * 1024) {
+    const int64_t tw = M * taps * (Cp / 8);
+    const bool pix = W % 8 == 0 && (H * W) % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 7) == 0 &&
+                     ceil_div(N * H, 2) + (int64_t)sm_count() * 8 < ((int64_t)1 << 31) &&
+                     !getenv("I8Q_CONV_CENTER_ROW");
+    if (pix) {
+      // the filter takes two of the eight 2-warp blocks an SM holds at first, the rows the rest
+      const int wblocks = (int)std::min<int64_t>(ceil_div(tw, 64), (int64_t)sm_count() * 2);
+      if (xtype == I8Q_U8 && wtype == I8Q_U8)
+        launch_center_pix<uint8_t, uint8_t>(s, x, N, C, H, W, Cp, x_zp, xc, w, w_zp, per_channel, M, taps, wc,
+                                             wblocks);
+      else if (xtype == I8Q_U8)
+        launch_center_pix<uint8_t, int8_t>(s, x, N, C, H, W, Cp, x_zp, xc, w, w_zp, per_channel, M, taps, wc,
+                                            wblocks);
+      else if (wtype == I8Q_U8)
+        launch_center_pix<int8_t, uint8_t>(s, x, N, C, H, W, Cp, x_zp, xc, w, w_zp, per_channel, M, taps, wc,
+                                            wblocks);
+      else
+        launch_center_pix<int8_t, int8_t>(s, x, N, C, H, W, Cp, x_zp, xc, w, w_zp, per_channel, M, taps, wc,
+                                           wblocks);
+      I8Q_LAUNCH_CHECK("conv operand centering");
+    } else if (row_smem <= 200 * 1024) {
       if (xtype == I8Q_U8) {
         const int ar = smem_attr((const void*)center_x_row<uint8_t>, 200 * 1024);
         if (ar) return ar;
@@ -652,15 +761,16 @@ int launch_conv_tc(const void* x, int xtype, int64_t N, int64_t C, int64_t H, in
       else
         center_x_nhwc<int8_t><<<gx, 256, 0, s>>>((const int8_t*)x, (int)C, (int)H, (int)W, (int)Cp, x_zp, xc);
     }
-    const int64_t tw = M * taps * (Cp / 8);
-    const int gw = (int)std::min<int64_t>(ceil_div(tw, 256), (int64_t)sm_count() * 8);
-    if (wtype == I8Q_U8)
-      center_w<uint8_t><<<gw, 256, 0, s>>>((const uint8_t*)w, (const uint8_t*)w_zp, per_channel, (int)M, (int)C, taps,
-                                           (int)Cp, wc);
-    else
-      center_w<int8_t><<<gw, 256, 0, s>>>((const int8_t*)w, (const int8_t*)w_zp, per_channel, (int)M, (int)C, taps,
-                                          (int)Cp, wc);
-    I8Q_LAUNCH_CHECK("conv operand centering");
+    if (!pix) {
+      const int gw = (int)std::min<int64_t>(ceil_div(tw, 256), (int64_t)sm_count() * 8);
+      if (wtype == I8Q_U8)
+        center_w<uint8_t><<<gw, 256, 0, s>>>((const uint8_t*)w, (const uint8_t*)w_zp, per_channel, (int)M, (int)C,
+                                             taps, (int)Cp, wc);
+      else
+        center_w<int8_t><<<gw, 256, 0, s>>>((const int8_t*)w, (const int8_t*)w_zp, per_channel, (int)M, (int)C, taps,
+                                            (int)Cp, wc);
+      I8Q_LAUNCH_CHECK("conv operand centering");
+    }
   }
   CUtensorMap mW, mX;
   int rc = make_map_2d(&mW, wc, M, (int64_t)taps * Cp, BM, "qlinearconv");
