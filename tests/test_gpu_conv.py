@@ -126,6 +126,24 @@ def test_tensor_core_path(orc, dev, monkeypatch, case, types, store):
     assert prof.get("qlinearconv_tc", (0,))[0] == 2
 
 
+@pytest.mark.parametrize("types", [("u8", "u8", "u8"), ("s8", "s8", "s8")])
+def test_row_centring_forced(orc, dev, monkeypatch, types):
+    """The operands centred by the row kernel (shared-memory transpose) and
+    a separate filter launch on a shape the one-launch form also takes."""
+    monkeypatch.setenv("I8Q_CONV_CENTER_ROW", "1")
+    N, C, H, W, M, k, pads = 2, 72, 7, 56, 40, 3, (1, 1, 1, 1)
+    rng = np.random.default_rng(29)
+    dt = {"u8": (np.uint8, 0, 256), "s8": (np.int8, -128, 128)}
+    xt, wt, yt = (dt[t] for t in types)
+    x = rng.integers(xt[1], xt[2], (N, C, H, W)).astype(xt[0])
+    w = rng.integers(wt[1], wt[2], (M, C, k, k)).astype(wt[0])
+    ws = rng.uniform(0.001, 0.01, M).astype(np.float32)
+    wz = rng.integers(wt[1], wt[2], M)
+    B = rng.integers(-5000, 5001, M).astype(np.int32)
+    run_conv(orc, dev, x, np.float32(0.0037), int(rng.integers(xt[1], xt[2])), w, ws, wz, np.float32(0.05),
+             int(rng.integers(yt[1], yt[2])), B, pads, ytype=types[2])
+
+
 def test_direct_path_forced(orc, dev, monkeypatch):
     monkeypatch.setenv("I8Q_FORCE_CONV", "direct")
     N, C, H, W, M, k, pads = TC_CASES[0]
