@@ -479,6 +479,15 @@ int launch_quantize_cols(const void* B, int typeB, int64_t K, int64_t N, int avo
 int launch_repack_cols_s8(const int8_t* B, int64_t K, int64_t N, int64_t ldb, int8_t* iBt,
                           __nv_bfloat16* iBt_bf16, int64_t Kp, int32_t* colsum, cudaStream_t s);
 
+// The tiled form of those repacks: whether it takes the operands (16-byte
+// aligned rows and pieces, N % 16 == 0, Kp % 16 == 0), and its launch, the
+// codes centred on the way when flip (uint8: code - 128); iBt or iBt_bf16
+// may be null; colsum (N entries) must be zeroed before.
+bool repack_tiles_ok(const void* B, int64_t K, int64_t N, int64_t ldb, const void* iBt, const void* iBt_bf16,
+                     int64_t Kp);
+void launch_repack_tiles(const void* B, bool flip, int64_t K, int64_t N, int64_t ldb, int8_t* iBt,
+                         __nv_bfloat16* iBt_bf16, int64_t Kp, int32_t* colsum, int64_t gates_H, cudaStream_t s);
+
 // Same, with the columns of an iofc-ordered 4H-wide matrix (N == 4 * gates_H)
 // interleaved per hidden unit: column q*H + u becomes row 4u + q of iBt.
 int launch_repack_cols_s8_gates(const int8_t* B, int64_t K, int64_t N, int64_t ldb, int8_t* iBt,

@@ -387,6 +387,12 @@ int launch_center(const void* X, int type, int64_t R, int64_t K, int64_t Kp, int
   if (bx == 0) return I8Q_OK;
   I8Q_PROF("qgemm_center", s);
   I8Q_CUDA_TRY(cudaMemsetAsync(sums, 0, (size_t)R * sizeof(int32_t), s));
+  if (!k_fast && repack_tiles_ok(X, K, R, R, nullptr, Xc, Kp)) {
+    // transposed: 128 x 128 tiles turned by byte permutes
+    launch_repack_tiles(X, type != I8Q_S8, K, R, R, nullptr, Xc, Kp, sums, 0, s);
+    I8Q_LAUNCH_CHECK("repack_tiles (centre)");
+    return I8Q_OK;
+  }
   const bool vec = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && (k_fast ? K % 16 == 0 : R % 16 == 0);
   const auto* x8 = static_cast<const uint8_t*>(X);
   if (k_fast && vec) {

@@ -497,8 +497,10 @@ cols_kernel(const T* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int qmin
   }
 }
 
-// ---- int8 repack in 128 x 128 tiles ------------------------------------------
-// The repack of a given int8 B (no quantization) over a grid of K x N tiles:
+// ---- 8-bit repack in 128 x 128 tiles -------------------------------------------
+// The repack of a given 8-bit B (no quantization) over a grid of K x N tiles,
+// codes centred on the way for uint8 (FLIP: code - 128, the int8 of code ^
+// 0x80); the int8 and bf16 copies are each optional:
 // a thread loads a 4-row x 16-column block (four 16-byte loads, two lanes
 // per 32-byte sector of a row), turns it into 16 words of 4 rows each of one
 // column by byte permutes, and stores them to a column-major shared tile
@@ -509,9 +511,11 @@ cols_kernel(const T* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int qmin
 // tiles up to Kp write the padding.
 constexpr int kRtCols = 128, kRtK = 128, kRtStride = kRtK / 4 + 1;
 
+template <bool FLIP>
 __global__ void __launch_bounds__(256)
 repack_tiles_s8(const int8_t* __restrict__ B, int64_t K, int64_t N, int64_t ldb, int8_t* __restrict__ iBt,
                 __nv_bfloat16* __restrict__ iBt_bf16, int64_t Kp, int32_t* __restrict__ colsum, int64_t gates_H) {
+  constexpr uint32_t flip = FLIP ? 0x80808080u : 0u;
   __shared__ uint32_t tile[kRtCols * kRtStride];
   const int t = (int)threadIdx.x, lane = t & 31, warp = t >> 5;
   const int64_t j0 = (int64_t)blockIdx.x * kRtCols, k0 = (int64_t)blockIdx.y * kRtK;
@@ -522,10 +526,14 @@ repack_tiles_s8(const int8_t* __restrict__ B, int64_t K, int64_t N, int64_t ldb,
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int64_t k = k0 + 4 * rq + r;
-      v[r] = (k < K && j < N) ? __ldg(reinterpret_cast<const uint4*>(B + k * ldb + j)) : make_uint4(0, 0, 0, 0);
+      v[r] = (k < K && j < N) ? __ldg(reinterpret_cast<const uint4*>(B + k * ldb + j))
+                              : make_uint4(flip, flip, flip, flip);
     }
-    const uint32_t a[4][4] = {{v[0].x, v[0].y, v[0].z, v[0].w}, {v[1].x, v[1].y, v[1].z, v[1].w},
-                              {v[2].x, v[2].y, v[2].z, v[2].w}, {v[3].x, v[3].y, v[3].z, v[3].w}};
+    // padding rows stay 0 after the flip too
+    const uint32_t a[4][4] = {{v[0].x ^ flip, v[0].y ^ flip, v[0].z ^ flip, v[0].w ^ flip},
+                              {v[1].x ^ flip, v[1].y ^ flip, v[1].z ^ flip, v[1].w ^ flip},
+                              {v[2].x ^ flip, v[2].y ^ flip, v[2].z ^ flip, v[2].w ^ flip},
+                              {v[3].x ^ flip, v[3].y ^ flip, v[3].z ^ flip, v[3].w ^ flip}};
     uint32_t* dst = tile + (16 * cq) * kRtStride + rq;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -553,7 +561,7 @@ repack_tiles_s8(const int8_t* __restrict__ B, int64_t K, int64_t N, int64_t ldb,
     const bool live = j < N && k < Kp;
     if (live) {
       const int64_t jd = dest_row(j, gates_H);
-      *reinterpret_cast<uint4*>(iBt + jd * Kp + k) = make_uint4(w[0], w[1], w[2], w[3]);
+      if (iBt) *reinterpret_cast<uint4*>(iBt + jd * Kp + k) = make_uint4(w[0], w[1], w[2], w[3]);
       if (iBt_bf16) {
         uint32_t o[8];
 #pragma unroll
@@ -1107,6 +1115,22 @@ int launch_quantize_cols(const void* B, int typeB, int64_t K, int64_t N, int avo
   return I8Q_OK;
 }
 
+bool repack_tiles_ok(const void* B, int64_t K, int64_t N, int64_t ldb, const void* iBt, const void* iBt_bf16,
+                     int64_t Kp) {
+  const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  return N > 0 && N % 16 == 0 && ldb % 16 == 0 && Kp % 16 == 0 && Kp >= K && al16(B) && (!iBt || al16(iBt)) &&
+         (!iBt_bf16 || al16(iBt_bf16)) && (iBt || iBt_bf16) && ceil_div(Kp, kRtK) <= 65535 &&
+         ceil_div(N, kRtCols) <= 0x7fffffff;
+}
+
+void launch_repack_tiles(const void* B, bool flip, int64_t K, int64_t N, int64_t ldb, int8_t* iBt,
+                         __nv_bfloat16* iBt_bf16, int64_t Kp, int32_t* colsum, int64_t gates_H, cudaStream_t s) {
+  const dim3 grid((unsigned)ceil_div(N, kRtCols), (unsigned)ceil_div(Kp, kRtK));
+  const auto* b8 = static_cast<const int8_t*>(B);
+  if (flip) repack_tiles_s8<true><<<grid, 256, 0, s>>>(b8, K, N, ldb, iBt, iBt_bf16, Kp, colsum, gates_H);
+  else repack_tiles_s8<false><<<grid, 256, 0, s>>>(b8, K, N, ldb, iBt, iBt_bf16, Kp, colsum, gates_H);
+}
+
 int launch_repack_cols_s8(const int8_t* B, int64_t K, int64_t N, int64_t ldb, int8_t* iBt, __nv_bfloat16* iBt_bf16,
                           int64_t Kp, int32_t* colsum, cudaStream_t s) {
   return launch_repack_cols_s8_gates(B, K, N, ldb, iBt, iBt_bf16, Kp, colsum, 0, s);
@@ -1117,12 +1141,9 @@ int launch_repack_cols_s8_gates(const int8_t* B, int64_t K, int64_t N, int64_t l
   if (N <= 0) return I8Q_OK;
   if (gates_H > 0 && N != 4 * gates_H) return fail(I8Q_ERR_INVALID_ARG, "repack: gate interleave needs N == 4H");
   I8Q_PROF("repack_cols", s);
-  const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-  if (N % 16 == 0 && ldb % 16 == 0 && Kp % 16 == 0 && Kp >= K && al16(B) && al16(iBt) &&
-      (!iBt_bf16 || al16(iBt_bf16)) && ceil_div(Kp, kRtK) <= 65535) {
+  if (repack_tiles_ok(B, K, N, ldb, iBt, iBt_bf16, Kp)) {
     I8Q_CUDA_TRY(cudaMemsetAsync(colsum, 0, (size_t)N * sizeof(int32_t), s));
-    dim3 grid((unsigned)ceil_div(N, kRtCols), (unsigned)ceil_div(Kp, kRtK));
-    repack_tiles_s8<<<grid, 256, 0, s>>>(B, K, N, ldb, iBt, iBt_bf16, Kp, colsum, gates_H);
+    launch_repack_tiles(B, false, K, N, ldb, iBt, iBt_bf16, Kp, colsum, gates_H, s);
     I8Q_LAUNCH_CHECK("repack_tiles_s8");
     return I8Q_OK;
   }

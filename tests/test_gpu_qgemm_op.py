@@ -105,6 +105,24 @@ def test_transposed_operands(orc, dev, transA, transB):
         transB=transB)
 
 
+@pytest.mark.parametrize("transA,transB", [(False, False), (True, False), (True, True)])
+@pytest.mark.parametrize("atype,btype", [("u8", "s8"), ("s8", "u8")])
+def test_tiled_transposing_centring(orc, dev, transA, transB, atype, btype):
+    """Operands whose K is the slow index and whose other extent is a
+    multiple of 16 are centred in 128 x 128 tiles turned by byte permutes:
+    M = 80 and N = 272 leave partial tiles, K = 200 a partial K tile and
+    the padding up to 256."""
+    w = workloads.qgemm(seed=14, M=80, K=200, N=272, atype=atype, btype=btype)
+    A = w["A"].T.copy() if transA else w["A"]
+    B = w["B"].T.copy() if transB else w["B"]
+    yt = "u8" if atype == "u8" else "s8"
+    run(orc, dev, A, w["a_scale"], w["a_zero_point"], B, w["b_scale"], w["b_zero_point"], C=w["C"],
+        alpha=float(w["alpha"]), y_scale=float(w["y_scale"]), yzp=w["y_zero_point"], ytype=yt, transA=transA,
+        transB=transB)
+    run(orc, dev, A, w["a_scale"], w["a_zero_point"], B, w["b_scale"], w["b_zero_point"], C=w["C"],
+        alpha=float(w["alpha"]), transA=transA, transB=transB)
+
+
 def test_no_zero_point_and_unit_parameters(orc, dev):
     w = workloads.qgemm(seed=13, M=96, K=64, N=128)
     run(orc, dev, w["A"], 1.0, 0, w["B"], np.float32(1.0))
