@@ -121,6 +121,27 @@ def test_dynamic_quantize_matmul_degenerate_and_one_sided(orc, dev):
         assert np.array_equal(Y.cpu().numpy(), ref["Y"])
 
 
+@pytest.mark.parametrize("scale", [1.0, 0.5, 2.0])
+def test_dynamic_quantize_matmul_quantization_ties(orc, dev, scale):
+    """A spanning exactly [0, 255 * scale] gives the scale `scale` and zero
+    point 0, and inputs at (j + 1/2) * scale put every quotient on a tie
+    (round half to even decides), others just beside one."""
+    rng = np.random.default_rng(int(scale * 10))
+    M, K, N = 40, 96, 48
+    j = rng.integers(0, 255, (M, K)).astype(np.float32)
+    A = ((j + 0.5) * np.float32(scale)).astype(np.float32)
+    A[1::3] = np.nextafter(A[1::3], np.float32(0))
+    A[0, 0], A[0, 1] = 0.0, np.float32(255 * scale)
+    B = rng.integers(-128, 128, (K, N)).astype(np.int8)
+    bs = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+    Y = torch.empty(M, N, dtype=torch.float32, device=dev)
+    q.dynamic_quantize_matmul(_t(A, dev), _t(B, dev), _t(bs, dev), Y)
+    q.sync_status()
+    ref = orc.dynamic_quantize_matmul(A, B, bs)
+    assert ref["a_scale"] == np.float32(scale) and ref["a_zero_point"] == 0
+    assert np.array_equal(Y.cpu().numpy(), ref["Y"])
+
+
 def test_dynamic_quantize_matmul_full_size_sampled(orc, dev):
     """M=8192 K=4096 N=14336: the per-tensor parameters, and sampled output
     rows recomputed by the oracle from those rows of A with the same
