@@ -319,6 +319,28 @@ __device__ __forceinline__ void dw_requant_fast(const int (&accb)[kStrip], float
   }
 }
 
+// The planes outside the bracketed form: each code from the reciprocal
+// product, or from the quotient near a half-integer.  Out of line, so the
+// row loop's code stays small.
+template <typename YT>
+__device__ __noinline__ void dw_requant_general(int a0, int a1, int a2, int a3, int a4, int a5, int a6, int a7,
+                                                float mul, float y_scale, float yr, float lo_z, float hi_z, int y_zp,
+                                                YT* out, bool vec, int n) {
+  const int a[kStrip] = {a0, a1, a2, a3, a4, a5, a6, a7};
+  uint32_t code[kStrip];
+#pragma unroll
+  for (int e = 0; e < kStrip; ++e)
+    code[e] = quot_code_bits(__fmul_rn(__int2float_rn(a[e]), mul), y_scale, yr, lo_z, hi_z, y_zp);
+  if (vec) {
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]),
+                                                pack_low_bytes(code[4], code[5], code[6], code[7]));
+  } else {
+#pragma unroll
+    for (int e = 0; e < kStrip; ++e)
+      if (e < n) out[e] = (YT)code[e];
+  }
+}
+
 // Persistent: CTA b takes the groups of `ppc` consecutive planes b, b +
 // gridDim.x, ...; two shared buffers, the next group's planes copied in
 // (cp.async, 8- or 4-byte pieces) while the current one is computed.  The
@@ -499,21 +521,9 @@ qlinearconv_depthwise_rows(const XT* __restrict__ x, const WT* __restrict__ w, c
               dw_requant_fast<YT>(acc[o], mul, yrh, yrl, mz, y_scale, lo_z, hi_z, y_zp,
                                   yp + (int64_t)(oh0 + o) * OW, vec, OW - ow0);
             } else {
-              // the other planes: each code from the reciprocal product,
-              // or from the quotient near a half-integer
-              uint32_t code[kStrip];
-#pragma unroll
-              for (int e = 0; e < kStrip; ++e)
-                code[e] = quot_code_bits(__fmul_rn(__int2float_rn(acc[o][e]), mul), y_scale, yr, lo_z, hi_z, y_zp);
-              YT* out = yp + (int64_t)(oh0 + o) * OW;
-              if (vec) {
-                *reinterpret_cast<uint2*>(out) = make_uint2(pack_low_bytes(code[0], code[1], code[2], code[3]),
-                                                            pack_low_bytes(code[4], code[5], code[6], code[7]));
-              } else {
-#pragma unroll
-                for (int e = 0; e < kStrip; ++e)
-                  if (e < OW - ow0) out[e] = (YT)code[e];
-              }
+              dw_requant_general<YT>(acc[o][0], acc[o][1], acc[o][2], acc[o][3], acc[o][4], acc[o][5], acc[o][6],
+                                     acc[o][7], mul, y_scale, yr, lo_z, hi_z, y_zp, yp + (int64_t)(oh0 + o) * OW, vec,
+                                     OW - ow0);
             }
           }
         }
