@@ -257,6 +257,20 @@ quantize_rows_warp(const T* __restrict__ A, int64_t M, int64_t K, int64_t lda, u
 // 2.4x on 1024 rows, and fp32 rows of 4096 fit.
 constexpr int kStageRows = 4;
 constexpr int kWarpsPerRow = 4;
+
+// Four codes saturated to [0, 255] and packed, byte 0 from a.
+__device__ __forceinline__ uint32_t pack_sat_u8x4(int a, int b, int c, int d) {
+  uint32_t hi, r;
+  asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(d), "r"(c), "r"(0u));
+  asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(b), "r"(a), "r"(hi));
+  return r;
+}
+
+// z + rint(fl(v / s)), saturated to [0, 255], from the quotient itself: the
+// fallback of the bracketed codes below.  Out of line: rare.
+__device__ __noinline__ int row_code_exact(float v, float s, float lo_z, float hi_z, int z) {
+  return (int)(rint_code_bits(__fdiv_rn(v, s), lo_z, hi_z, z) - 0x4B400000u);
+}
 constexpr int kStageThreads = 32 * kStageRows * kWarpsPerRow;
 constexpr uint32_t ST_TIMEOUT_ROWS = 1u << 12;
 
@@ -366,10 +380,56 @@ quantize_rows_staged(const T* __restrict__ A, int64_t M, int64_t K, int64_t lda,
       const float shift = (float)(z - 128) - 12582912.0f;  // takes rint + 1.5*2^23 to uA - 128
       uint8_t* u = uA + (live ? row : 0) * Kp;
       __nv_bfloat16* ub = uA_bf16 ? uA_bf16 + (live ? row : 0) * Kp : nullptr;
+      // Bracketed codes: with r = fl(1 / sc) scaled by 1 -+ 2^-20 (rl < 1 / sc
+      // < rh), the exact products v * rl and v * rh enclose v / sc with a margin
+      // above 2^-21 |v / sc|, so they strictly enclose the IEEE quotient too;
+      // an fma adds mz = 1.5 * 2^23 + z and rounds once to an integer (|v / sc|
+      // <= 256 here), a non-decreasing function of the product, so equal ends
+      // give z + rint(quotient) (a half-integer quotient would have both
+      // neighbours inside).  Unequal ends (near a tie) take the quotient.
+      const float rcp = quot_rcp(sc);
+      const bool brk = rcp == rcp;
+      const float rh = __fmul_rn(rcp, 1.0f + 0x1p-20f), rl = __fmul_rn(rcp, 1.0f - 0x1p-20f);
+      const float mz = 12582912.0f + (float)z;
 #pragma unroll 2
       for (int c = part * 32 + lane; live && c < nunits; c += 32 * kWarpsPerRow) {
         float v[8];
         unit(c, v);
+        uint32_t w0, w1;
+        if (brk) {
+          int n[8];
+          uint32_t diff = 0;
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const float2 h = fma2_rn(make_float2(v[e], v[e + 1]), make_float2(rh, rh), make_float2(mz, mz));
+            const float2 l = fma2_rn(make_float2(v[e], v[e + 1]), make_float2(rl, rl), make_float2(mz, mz));
+            diff |= (__float_as_uint(h.x) ^ __float_as_uint(l.x)) | (__float_as_uint(h.y) ^ __float_as_uint(l.y));
+            n[e] = __float_as_int(h.x) - 0x4B400000;
+            n[e + 1] = __float_as_int(h.y) - 0x4B400000;
+          }
+          if (diff) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) n[e] = row_code_exact(v[e], sc, lo_z, hi_z, z);
+          }
+          w0 = pack_sat_u8x4(n[0], n[1], n[2], n[3]);
+          w1 = pack_sat_u8x4(n[4], n[5], n[6], n[7]);
+          *reinterpret_cast<uint2*>(u + (size_t)c * 8) = make_uint2(w0, w1);
+          if (ub) {
+            // code c as the fp32 1.5 * 2^23 + c by one byte permute, minus
+            // 1.5 * 2^23 + 128: exactly c - 128, whose bf16 is the top half
+            uint32_t cb[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t w = q < 2 ? w0 : w1, sel = 0x7640u + 2 * (q & 1);
+              const float2 f = fma2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B400000u, sel)),
+                                                   __uint_as_float(__byte_perm(w, 0x4B400000u, sel + 1))),
+                                       make_float2(1.0f, 1.0f), make_float2(-12583040.0f, -12583040.0f));
+              cb[q] = __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
+            }
+            *reinterpret_cast<uint4*>(ub + (size_t)c * 8) = make_uint4(cb[0], cb[1], cb[2], cb[3]);
+          }
+          continue;
+        }
         uint32_t code[8], cb[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {

@@ -273,6 +273,34 @@ def test_row_quantization_forms(orc, dev, core, monkeypatch, register, typeA, K,
              rows=np.array([0, 3, 5, 600, M - 2, M - 1]))
 
 
+@pytest.mark.parametrize("register", [False, True])
+@pytest.mark.parametrize("typeA", ["f32", "bf16"])
+def test_row_quantization_ties(orc, dev, core, monkeypatch, register, typeA):
+    """Rows spanning exactly [0, 255 * s] (scale s, zero point 0) with inputs
+    at (j + 1/2) * s: every quotient a tie (round half to even decides), a
+    third of the rows just beside one; rows long enough for the staged form
+    and enough of them for a full wave, or forced to the register form."""
+    if core != "tc2":
+        pytest.skip("row quantization does not depend on the integer core")
+    if register:
+        monkeypatch.setenv("I8Q_ROWS_REGISTER", "1")
+    rng = np.random.default_rng(31)
+    M, K = 700, 2056
+    s = np.where(np.arange(M) % 2 == 0, 1.0, 0.5).astype(np.float32)[:, None]
+    j = rng.integers(0, 255, (M, K)).astype(np.float32)
+    A = ((j + 0.5) * s).astype(np.float32)
+    A[1::3] = np.nextafter(A[1::3], np.float32(0))
+    A[:, 0], A[:, 1] = 0.0, (255.0 * s[:, 0]).astype(np.float32)
+    if typeA == "bf16":
+        # bf16 holds j + 1/2 exactly only below 128: keep those rows' codes small
+        A = np.where(j < 127, A, (0.5 * s).astype(np.float32))
+        A[:, 0], A[:, 1] = 0.0, (255.0 * s[:, 0]).astype(np.float32)
+        A = (A.view(np.uint32) >> 16).astype(np.uint16)
+    iB = rng.integers(-128, 128, (K, 32)).astype(np.int8)
+    run_case(orc, dev, A, iB=iB, scaleB=rng.uniform(1e-3, 1e-2, 32).astype(np.float32), bias=None, typeA=typeA,
+             rows=np.array([0, 1, 2, 3, 350, M - 2, M - 1]))
+
+
 @pytest.mark.parametrize("M,N,K,expect", [(64, 128, 256, "dp4a"), (1, 7, 3, "dp4a"), (8192, 14336, 4096, "tcgen05"),
                                           (64, 1024, 4096, "tcgen05"), (64, 128, 10000, "tcgen05")])
 def test_default_core_choice(monkeypatch, core, M, N, K, expect):
