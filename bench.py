@@ -43,8 +43,8 @@ WORKLOAD = ("dynamic quantized GEMM M=8192 K=4096 N=14336: bf16 A quantized per 
 NCU_TRAFFIC = {
     "gemm_tc_pair": {"sources": ["int8_quantized_gb300/csrc/gemm_tc.cu", "int8_quantized_gb300/csrc/tcgen05.cuh",
                                  "int8_quantized_gb300/csrc/common.cuh"],
-                     "sha256": "bea27fefb0720e41e99799c73c7d25ef063e2fdb0e83cc4ade21d1a01f56a9ef",
-                     "bytes": (358.97 + 221.28) * 1e6,
+                     "sha256": "dfd3d191094acca86cbfde8c8c0d64895d9ba5f8879ad2f5720a3f09355167cf",
+                     "bytes": (365.95 + 220.94) * 1e6,
                      "profile": "profiles/gemm_tc_pair_large_gemm.md"},
 }
 
