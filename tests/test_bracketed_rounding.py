@@ -1,7 +1,7 @@
-"""The bracketed rounding that three kernels use for their 8-bit codes (the
-depthwise QLinearConv's requantization, the row quantization of A, and the
-argument behind the reciprocal-product codes), checked with exact rational
-arithmetic on the host.
+"""The bracketed rounding that the depthwise QLinearConv's requantization and
+the staged row quantization of A use for their 8-bit codes, checked with
+exact rational arithmetic on the host (no GPU, no oracle: the kernels' own
+parity tests compare their codes with the oracle's).
 
 Claim: with q the IEEE fp32 quotient fl(v / s), r = fl(1 / s),
 rh = fl(r * (1 + 2^-20)), rl = fl(r * (1 - 2^-20)) and mz = 1.5 * 2^23 + z,
