@@ -56,3 +56,25 @@ def test_reference_arm_only_rank0_works(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_rows_selection(monkeypatch):
+    """--rows times only the named hot-path workloads (the row functions are
+    stubbed: no GPU work)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    called = []
+    for name in ("_row_avoid_overflow", "_row_inner_product", "_row_qgemm_family", "_row_qlinear_ew", "_row_lstm"):
+        monkeypatch.setattr(bench, name, lambda *a, _n=name, **k: called.append(_n))
+    monkeypatch.setattr(bench, "_row_qlinearconv", lambda *a, **k: called.append("conv_dw" if a[-1] else "conv_dense"))
+    args = bench.parse_args(["--rows", "qlinearconv_depthwise,dq_lstm_bidirectional"])
+    bench.measure_rows(args, None, None, 1)
+    assert called == ["conv_dw", "_row_lstm"]
+    called.clear()
+    bench.measure_rows(bench.parse_args([]), None, None, 1)
+    assert called == ["_row_avoid_overflow", "_row_inner_product", "conv_dense", "conv_dw", "_row_qgemm_family",
+                      "_row_qlinear_ew", "_row_lstm"]
+    called.clear()
+    bench.measure_rows(bench.parse_args(["--rows", "matmul_integer_to_float"]), None, None, 1)
+    assert called == ["_row_qgemm_family"]
