@@ -253,8 +253,8 @@ __device__ __forceinline__ void dw_cp_wait() {
 }
 
 // The code of one sum from the quotient itself: the fallback of
-// dw_requant_fast (accb carries 1.5 * 2^23 + acc).  Out of line: rare.
-__device__ __noinline__ int dw_code_exact(int accb, float mul, float y_scale, float lo_z, float hi_z, int y_zp) {
+// dw_requant_fast (accb carries 1.5 * 2^23 + acc).
+__device__ __forceinline__ int dw_code_exact(int accb, float mul, float y_scale, float lo_z, float hi_z, int y_zp) {
   const float v = __fmul_rn(__fsub_rn(__int_as_float(accb), 12582912.0f), mul);
   return (int)(rint_code_bits(__fdiv_rn(v, y_scale), lo_z, hi_z, y_zp) - 0x4B400000u);
 }
@@ -271,6 +271,31 @@ __device__ __forceinline__ uint32_t pack_sat4(int a, int b, int c, int d) {
     asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(b), "r"(a), "r"(hi));
   }
   return r;
+}
+
+// The rare ends of a bracketed row, out of line so that the row loop's code
+// stays small: the codes from the quotient itself when the bracket's ends
+// differed, and the bytewise stores of a row that is not one whole aligned
+// 8-byte piece.
+template <typename YT>
+__device__ __noinline__ void dw_row_rare(int b0, int b1, int b2, int b3, int b4, int b5, int b6, int b7, int c0, int c1,
+                                         int c2, int c3, int c4, int c5, int c6, int c7, bool exact, float mul,
+                                         float y_scale, float lo_z, float hi_z, int y_zp, YT* out, bool vec, int n) {
+  const int accb[kStrip] = {b0, b1, b2, b3, b4, b5, b6, b7};
+  int code[kStrip] = {c0, c1, c2, c3, c4, c5, c6, c7};
+  if (exact) {
+#pragma unroll
+    for (int e = 0; e < kStrip; ++e) code[e] = dw_code_exact(accb[e], mul, y_scale, lo_z, hi_z, y_zp);
+  }
+  if (vec) {
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_sat4<YT>(code[0], code[1], code[2], code[3]),
+                                                pack_sat4<YT>(code[4], code[5], code[6], code[7]));
+  } else {
+    constexpr int lo = std::is_same<YT, uint8_t>::value ? 0 : -128, hi = lo + 255;
+#pragma unroll
+    for (int e = 0; e < kStrip; ++e)
+      if (e < n) out[e] = (YT)min(max(code[e], lo), hi);
+  }
 }
 
 // Requantize the 8 sums of an output row of a fast plane and store the
@@ -304,18 +329,13 @@ __device__ __forceinline__ void dw_requant_fast(const int (&accb)[kStrip], float
     code[e] = __float_as_int(rh.x) - 0x4B400000;
     code[e + 1] = __float_as_int(rh.y) - 0x4B400000;
   }
-  if (diff) {
-#pragma unroll
-    for (int e = 0; e < kStrip; ++e) code[e] = dw_code_exact(accb[e], mul, y_scale, lo_z, hi_z, y_zp);
-  }
-  if (vec) {
+  if (vec && !diff) {
     *reinterpret_cast<uint2*>(out) = make_uint2(pack_sat4<YT>(code[0], code[1], code[2], code[3]),
                                                 pack_sat4<YT>(code[4], code[5], code[6], code[7]));
   } else {
-    constexpr int lo = std::is_same<YT, uint8_t>::value ? 0 : -128, hi = lo + 255;
-#pragma unroll
-    for (int e = 0; e < kStrip; ++e)
-      if (e < n) out[e] = (YT)min(max(code[e], lo), hi);
+    dw_row_rare<YT>(accb[0], accb[1], accb[2], accb[3], accb[4], accb[5], accb[6], accb[7], code[0], code[1],
+                    code[2], code[3], code[4], code[5], code[6], code[7], diff != 0, mul, y_scale, lo_z, hi_z, y_zp,
+                    out, vec, n);
   }
 }
 
